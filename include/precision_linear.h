@@ -1,0 +1,148 @@
+/*
+ * precision_linear.h -- C ABI of the NVFP4 + LoRA + AQN-RMSNorm linear for GB300.
+ *
+ * The frozen-backbone linear layer of quantised RL rollout:
+ *
+ *     y = W_hat . h + lambda . B (A . h),    h = RMSNorm_AQN(x) = u (.) (w_norm + z),
+ *     u = x / sqrt(mean(x^2) + eps),        W_hat = s_g . s_b . q  (NVFP4)
+ *
+ * Sources: "QeRL: When Quantized Weights Help Reinforcement Learning, and Where
+ * the Evidence Stops" (zhongzhuzhou.org) -- section 2.1 (forward map of LoRA on
+ * a quantised backbone), section 3.1 (NVFP4: E2M1 codes, one E4M3 scale per 16
+ * weights, one FP32 tensor scale, reconstruction and argmin equations, 9P/16
+ * storage), section 5.1 (noise folded into the RMSNorm scale).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - All tensors are dense and row-major.  "BF16" buffers hold IEEE bfloat16,
+ *    "FP32" buffers IEEE float.
+ *  - Every pointer argument is a DEVICE pointer unless stated otherwise, on the
+ *    current CUDA device.  The caller owns all memory; the library never
+ *    allocates device memory on these paths.  Scratch lives in the caller's
+ *    workspace (see pl_workspace_bytes).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and never synchronise the host.
+ *  - Errors are return codes.  Argument checks (NULL, sizes, alignment, rank,
+ *    workspace size) are done on the host before anything is launched; a call
+ *    that fails them launches nothing.  Launch failures map to PL_ERR_CUDA.
+ *    Device-side waits are bounded: one that gives up records a device status
+ *    word, read (with a stream synchronise) by pl_last_device_status.
+ *  - Device requirement: compute capability 10.3 (GB300, sm_103a), else
+ *    PL_ERR_DEVICE.
+ *
+ * NVFP4 layout (canonical, what pl_nvfp4_quantize writes and the linear reads)
+ * ---------------------------------------------------------------------------
+ *  codes  uint8 [d_o][d_i/2]  : byte (o, k/2) = code(o,k) | code(o,k+1) << 4, k even.
+ *                               A code is 4-bit E2M1: sign | 2 exponent bits | 1
+ *                               mantissa bit, magnitudes {0,.5,1,1.5,2,3,4,6}.
+ *  scales uint8 [d_o][d_i/16] : OCP FP8 E4M3 ("FN") block scale of weights
+ *                               (o, 16j .. 16j+15).
+ *  s_g    float [1]           : FP32 tensor scale (device memory).
+ *  Blocks of 16 run along d_i, so d_i % 16 == 0.  Total 9*d_o*d_i/16 bytes + 4.
+ */
+#ifndef PRECISION_LINEAR_H
+#define PRECISION_LINEAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* pl_stream_t;
+
+typedef enum pl_status {
+  PL_OK = 0,
+  PL_ERR_NULL = 1,      /* a required pointer is NULL                         */
+  PL_ERR_SHAPE = 2,     /* a size is out of range or breaks a divisibility rule */
+  PL_ERR_ALIGN = 3,     /* a pointer is not 16-byte aligned                   */
+  PL_ERR_RANK = 4,      /* LoRA rank out of range (0..64)                     */
+  PL_ERR_DEVICE = 5,    /* no current CUDA device of compute capability 10.3  */
+  PL_ERR_CUDA = 6,      /* a CUDA runtime call or kernel launch failed        */
+  PL_ERR_WORKSPACE = 7, /* workspace NULL, misaligned or smaller than needed  */
+  PL_ERR_TIMEOUT = 8    /* a bounded device-side wait gave up                 */
+} pl_status;
+
+/* Static, human-readable name of a status code.  Never NULL. */
+const char* pl_status_string(pl_status status);
+
+/* ABI version of this header (major * 100 + minor). */
+int pl_version(void);
+
+/* Bytes of the packed NVFP4 payload plus block scales for a [d_o, d_i] weight:
+ * d_o*d_i/2 + d_o*d_i/16 (= 9P/16, QeRL review section 3.1 memory equation),
+ * not counting the 4-byte tensor scale.  0 if the shape is invalid. */
+size_t pl_nvfp4_bytes(int64_t d_o, int64_t d_i);
+
+/* Workspace bytes pl_nvfp4_lora_linear needs for this shape (any path the
+ * library may choose for it).  The workspace is caller-owned device memory,
+ * 256-byte aligned, reusable across calls on one stream; its contents on entry
+ * do not matter.  Calls that run concurrently need separate workspaces. */
+size_t pl_workspace_bytes(int64_t M, int64_t d_i, int64_t d_o, int r);
+
+/* NVFP4 quantiser (section 3.1, "Quantize values to E2M1 codes; retain block
+ * E4M3 scales and tensor-global scales" in the backbone-preparation algorithm).
+ *
+ *  W_bf16  in : BF16 [d_o][d_i], finite values.
+ *  codes   out: uint8 [d_o][d_i/2]  (layout above)
+ *  scales  out: uint8 [d_o][d_i/16]
+ *  s_g     out: float[1], device
+ * Arithmetic (bit-exact contract, FP32 IEEE round-to-nearest):
+ *  s_g = max|W| / 2688 (2688 = 6*448; 1 if W is all zero);
+ *  s_b = E4M3_rne_satfinite( amax_block / (6*s_g) );
+ *  code = nearest E2M1 value to |w| / (s_g*s_b), ties to the even code,
+ *         saturating at 6, sign from w, +0 for zero; 0 when s_g*s_b == 0.
+ * Requirements: d_o >= 1, 1 <= d_i, d_i % 16 == 0; W, codes 16-byte aligned.
+ * Launches three kernels (tensor amax, block quantise, scale finalise) after a
+ * 4-byte memset of s_g, which serves as the amax accumulator until the end. */
+pl_status pl_nvfp4_quantize(const void* W_bf16, int64_t d_o, int64_t d_i,
+                            uint8_t* codes, uint8_t* scales, float* s_g,
+                            pl_stream_t stream);
+
+/* RMSNorm with AQN noise folded into the scale (section 5.1):
+ *   h[m, :] = x[m, :] / sqrt(mean_j x[m, j]^2 + eps) (.) (w_norm + z)
+ *  x_bf16 in : BF16 [M][d];  w_norm in: FP32 [d];  z in: FP32 [d] or NULL (no
+ *  noise);  h_bf16 out: BF16 [M][d] (round to nearest).  w_norm + z is formed
+ *  in FP32.  Requirements: M >= 1, d >= 1, d % 8 == 0, x and h 16-byte aligned. */
+pl_status pl_rmsnorm_aqn(const void* x_bf16, int64_t M, int64_t d,
+                         const float* w_norm, const float* z, float eps,
+                         void* h_bf16, pl_stream_t stream);
+
+/* The quantised-backbone LoRA linear (section 2.1 forward map, with the
+ * section 5.1 prologue when w_norm is given):
+ *   h = RMSNorm_AQN(x; w_norm, z, eps)   if w_norm != NULL,  else h = x;
+ *   y[m, o] = sum_k W_hat[o, k] h[m, k] + lambda * sum_j B[o, j] (sum_k A[j, k] h[m, k])
+ *  x_bf16  in : BF16 [M][d_i]
+ *  codes, scales, s_g in: NVFP4 weight [d_o][d_i] (layout above)
+ *  A_bf16  in : BF16 [r][d_i], B_bf16 in: BF16 [d_o][r]; both NULL or r == 0
+ *               means no adapter.
+ *  w_norm, z in: FP32 [d_i] or NULL (z NULL = no noise; w_norm NULL = no norm)
+ *  y_bf16  out: BF16 [M][d_o]
+ *  workspace  : device scratch of at least pl_workspace_bytes(M, d_i, d_o, r).
+ * Accumulation is FP32.  M <= 64 runs the decode path, larger M the prefill
+ * path; both use tcgen05 tensor cores when d_i % 256 == 0 and a generic CUDA-core
+ * kernel otherwise.  Requirements: M >= 1, d_o >= 1, d_i >= 16, d_i % 16 == 0,
+ * 0 <= r <= 64; x, codes, scales, A, B, y 16-byte aligned. */
+pl_status pl_nvfp4_lora_linear(const void* x_bf16, int64_t M, int64_t d_i, int64_t d_o,
+                               const uint8_t* codes, const uint8_t* scales, const float* s_g,
+                               const void* A_bf16, const void* B_bf16, int r, float lambda,
+                               const float* w_norm, const float* z, float eps,
+                               void* y_bf16, void* workspace, size_t workspace_bytes,
+                               pl_stream_t stream);
+
+/* Synchronises `stream`, then returns and clears the device status word that
+ * bounded device-side waits set when they give up (PL_ERR_TIMEOUT), or PL_OK. */
+pl_status pl_last_device_status(pl_stream_t stream);
+
+/* Test hook: when `armed` is non-zero the next launch-checking step of any call
+ * reports a launch failure (PL_ERR_CUDA) as if the CUDA runtime had returned
+ * one, without faulting anything.  One-shot; 0 disarms. */
+void pl_debug_fail_next_launch(int armed);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PRECISION_LINEAR_H */

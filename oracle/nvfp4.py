@@ -85,23 +85,16 @@ E4M3_POS = E4M3_TABLE[:0x7F].copy()  # codes 0x00..0x7E: increasing, finite, >= 
 
 def _nearest_even(values: np.ndarray, grid: np.ndarray) -> np.ndarray:
     """Index of the nearest grid point to each value (grid increasing, starting at
-    0).  Exact ties go to the even index; values past the end saturate to the
-    last index.  All comparisons are exact in FP64 for FP32 inputs."""
+    0): the number of midpoints between neighbours that lie strictly below the
+    value, moved up by one when the value sits exactly on a midpoint whose upper
+    neighbour has the even index (ties to even).  Values beyond the last grid point
+    saturate to it.  Midpoints of FP32 grids are exact in FP64."""
     v = np.asarray(values, dtype=np.float64)
-    n = grid.shape[0]
-    hi = np.searchsorted(grid, v, side="left")  # first grid point >= v
-    hi_c = np.clip(hi, 0, n - 1)
-    lo_c = np.clip(hi - 1, 0, n - 1)
-    with np.errstate(invalid="ignore"):
-        d_lo = v - grid[lo_c]
-        d_hi = grid[hi_c] - v
-    pick_hi = d_hi < d_lo
-    tie = d_hi == d_lo
-    pick_hi = np.where(tie, (hi_c % 2) == 0, pick_hi)
-    idx = np.where(pick_hi, hi_c, lo_c)
-    idx = np.where(hi >= n, n - 1, idx)  # above the largest grid point
-    idx = np.where(v <= 0.0, 0, idx)
-    return idx.astype(np.int64)
+    mids = (grid[:-1] + grid[1:]) / 2.0
+    k = np.searchsorted(mids, v, side="left")  # midpoints < v
+    on_mid = mids[np.minimum(k, mids.shape[0] - 1)] == v
+    k = k + (on_mid & (k % 2 == 1))
+    return k.astype(np.int64)
 
 
 def e4m3_encode(t) -> np.ndarray:
@@ -139,8 +132,13 @@ def block_scale_codes(W: np.ndarray, s_g: np.float32) -> np.ndarray:
 
 
 def element_codes(W: np.ndarray, s_g: np.float32, sb_codes: np.ndarray) -> np.ndarray:
-    """4-bit codes (0..15) of every weight, shape [d_o, d_i]."""
+    """4-bit codes (0..15) of every weight, shape [d_o, d_i] (elementwise, so it is
+    evaluated in row chunks that stay cache-resident)."""
     d_o, d_i = W.shape
+    rows = max(1, (1 << 20) // d_i)
+    if d_o > rows:
+        return np.concatenate([element_codes(W[o:o + rows], s_g, sb_codes[o:o + rows])
+                               for o in range(0, d_o, rows)])
     W32 = W.astype(np.float32).reshape(d_o, d_i // BLOCK, BLOCK)
     s_b = E4M3_TABLE[sb_codes].astype(np.float32)
     S = (np.float32(s_g) * s_b).astype(np.float32)[..., None]

@@ -1,0 +1,197 @@
+"""ctypes binding of libprecision_linear.so: argument marshalling only.
+
+Every step of the path runs in the library's CUDA kernels; this module checks
+tensor dtypes/devices, allocates outputs with torch when the caller does not pass
+them, hands raw device pointers and the current torch stream to the C ABI, and
+turns non-zero status codes into ``PLError``.  There is no fallback: if the
+library is missing or the device is not sm_103, calls raise.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libprecision_linear.so")
+
+_c_void_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_lock = threading.Lock()
+_lib = None
+
+PL_OK = 0
+
+
+class PLError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+_SIGNATURES = {
+    "pl_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "pl_version": (ctypes.c_int, []),
+    "pl_nvfp4_bytes": (ctypes.c_size_t, [_i64, _i64]),
+    "pl_workspace_bytes": (ctypes.c_size_t, [_i64, _i64, _i64, ctypes.c_int]),
+    "pl_nvfp4_quantize": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
+    "pl_rmsnorm_aqn": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, ctypes.c_float,
+                                      _c_void_p, _c_void_p]),
+    "pl_nvfp4_lora_linear": (ctypes.c_int, [_c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p, _c_void_p,
+                                            _c_void_p, _c_void_p, ctypes.c_int, ctypes.c_float,
+                                            _c_void_p, _c_void_p, ctypes.c_float, _c_void_p,
+                                            _c_void_p, ctypes.c_size_t, _c_void_p]),
+    "pl_last_device_status": (ctypes.c_int, [_c_void_p]),
+    "pl_debug_fail_next_launch": (None, [ctypes.c_int]),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded shared library (loaded once)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is not built: run `python -m precision_linear_gb300.build`")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in _SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().pl_status_string(int(status)).decode()
+    except Exception:  # library not loadable
+        return f"status {status}"
+
+
+def _check(status: int, where: str):
+    if status != PL_OK:
+        raise PLError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else _c_void_p(t.data_ptr())
+
+
+def _stream(device) -> _c_void_p:
+    return _c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t, name, dtype, device=None, dim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if dim is not None and t.dim() != dim:
+        raise ValueError(f"{name} must be {dim}-D")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def nvfp4_bytes(d_o: int, d_i: int) -> int:
+    return int(lib().pl_nvfp4_bytes(d_o, d_i))
+
+
+def workspace_bytes(M: int, d_i: int, d_o: int, r: int) -> int:
+    return int(lib().pl_workspace_bytes(M, d_i, d_o, r))
+
+
+def nvfp4_quantize(W: torch.Tensor, codes=None, scales=None, s_g=None):
+    """BF16 W [d_o, d_i] -> (codes uint8 [d_o, d_i/2], scales uint8 [d_o, d_i/16], s_g float32 [1])."""
+    _need(W, "W", torch.bfloat16, dim=2)
+    d_o, d_i = W.shape
+    dev = W.device
+    if codes is None:
+        codes = torch.empty(d_o, d_i // 2, dtype=torch.uint8, device=dev)
+    if scales is None:
+        scales = torch.empty(d_o, max(d_i // 16, 1), dtype=torch.uint8, device=dev)
+    if s_g is None:
+        s_g = torch.empty(1, dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        st = lib().pl_nvfp4_quantize(_ptr(W), d_o, d_i, _ptr(codes), _ptr(scales), _ptr(s_g), _stream(dev))
+    _check(st, "pl_nvfp4_quantize")
+    return codes, scales, s_g
+
+
+def rmsnorm_aqn(x: torch.Tensor, w_norm: torch.Tensor, z: torch.Tensor | None = None,
+                eps: float = 1e-6, out: torch.Tensor | None = None) -> torch.Tensor:
+    """BF16 h = x / sqrt(mean(x^2) + eps) * (w_norm + z) per row."""
+    _need(x, "x", torch.bfloat16, dim=2)
+    dev = x.device
+    _need(w_norm, "w_norm", torch.float32, dev, 1)
+    if z is not None:
+        _need(z, "z", torch.float32, dev, 1)
+    if out is None:
+        out = torch.empty_like(x)
+    M, d = x.shape
+    with torch.cuda.device(dev):
+        st = lib().pl_rmsnorm_aqn(_ptr(x), M, d, _ptr(w_norm), _ptr(z), float(eps), _ptr(out), _stream(dev))
+    _check(st, "pl_rmsnorm_aqn")
+    return out
+
+
+class Workspace:
+    """A growable device scratch buffer for pl_nvfp4_lora_linear (one per stream)."""
+
+    def __init__(self, device=None):
+        self.device = torch.device(device) if device is not None else torch.device("cuda")
+        self.buf = None
+
+    def get(self, nbytes: int) -> torch.Tensor:
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+        return self.buf
+
+
+_default_ws = {}
+
+
+def nvfp4_lora_linear(x, codes, scales, s_g, A=None, B=None, lam: float = 0.0, w_norm=None, z=None,
+                      eps: float = 1e-6, out=None, workspace: Workspace | None = None) -> torch.Tensor:
+    """y = W_hat h + lam * B (A h) with h = RMSNorm_AQN(x) when w_norm is given (else x)."""
+    _need(x, "x", torch.bfloat16, dim=2)
+    dev = x.device
+    _need(codes, "codes", torch.uint8, dev, 2)
+    _need(scales, "scales", torch.uint8, dev, 2)
+    _need(s_g, "s_g", torch.float32, dev)
+    M, d_i = x.shape
+    d_o = codes.shape[0]
+    r = 0
+    if A is not None or B is not None:
+        _need(A, "A", torch.bfloat16, dev, 2)
+        _need(B, "B", torch.bfloat16, dev, 2)
+        r = A.shape[0]
+    if w_norm is not None:
+        _need(w_norm, "w_norm", torch.float32, dev, 1)
+    if z is not None:
+        _need(z, "z", torch.float32, dev, 1)
+    if out is None:
+        out = torch.empty(M, d_o, dtype=torch.bfloat16, device=dev)
+    need = workspace_bytes(M, d_i, d_o, r)
+    if workspace is None:
+        workspace = _default_ws.setdefault(dev, Workspace(dev))
+    ws = workspace.get(need)
+    with torch.cuda.device(dev):
+        st = lib().pl_nvfp4_lora_linear(_ptr(x), M, d_i, d_o, _ptr(codes), _ptr(scales), _ptr(s_g),
+                                        _ptr(A), _ptr(B), r, float(lam), _ptr(w_norm), _ptr(z), float(eps),
+                                        _ptr(out), _ptr(ws), ws.numel(), _stream(dev))
+    _check(st, "pl_nvfp4_lora_linear")
+    return out
+
+
+def last_device_status(device=None) -> int:
+    dev = torch.device(device) if device is not None else torch.device("cuda")
+    with torch.cuda.device(dev):
+        return int(lib().pl_last_device_status(_stream(dev)))

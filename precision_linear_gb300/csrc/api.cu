@@ -1,0 +1,151 @@
+// C ABI of libprecision_linear: argument checks, device check, dispatch.
+// Declarations and the contract of every entry point are in include/precision_linear.h.
+#include <atomic>
+#include <mutex>
+
+#include "../../include/precision_linear.h"
+#include "internal.h"
+
+namespace {
+
+std::atomic<int> g_fail_next_launch{0};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+pl_status check_launch(cudaError_t e) {
+  if (g_fail_next_launch.exchange(0) != 0) return PL_ERR_CUDA;
+  return e == cudaSuccess ? PL_OK : PL_ERR_CUDA;
+}
+
+struct DevInfo {
+  int ok = -1;  // -1 unknown, 0 unsupported, 1 supported
+  int sms = 0;
+};
+constexpr int kMaxDev = 64;
+DevInfo g_dev[kMaxDev];
+std::mutex g_dev_mu;
+
+pl_status device_check() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+    cudaGetLastError();
+    return PL_ERR_DEVICE;
+  }
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  if (d.ok < 0) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return PL_ERR_DEVICE;
+    }
+    d.ok = (major == 10 && minor == 3) ? 1 : 0;
+    d.sms = sms;
+  }
+  return d.ok == 1 ? PL_OK : PL_ERR_DEVICE;
+}
+
+}  // namespace
+
+namespace pl {
+int sm_count() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= kMaxDev) return 148;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  return g_dev[dev].sms > 0 ? g_dev[dev].sms : 148;
+}
+}  // namespace pl
+
+extern "C" {
+
+const char* pl_status_string(pl_status s) {
+  switch (s) {
+    case PL_OK: return "PL_OK";
+    case PL_ERR_NULL: return "PL_ERR_NULL: a required pointer is NULL";
+    case PL_ERR_SHAPE: return "PL_ERR_SHAPE: size out of range or not a multiple of the block";
+    case PL_ERR_ALIGN: return "PL_ERR_ALIGN: pointer not 16-byte aligned";
+    case PL_ERR_RANK: return "PL_ERR_RANK: LoRA rank out of range";
+    case PL_ERR_DEVICE: return "PL_ERR_DEVICE: no current CUDA device of compute capability 10.3";
+    case PL_ERR_CUDA: return "PL_ERR_CUDA: CUDA launch or runtime call failed";
+    case PL_ERR_WORKSPACE: return "PL_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case PL_ERR_TIMEOUT: return "PL_ERR_TIMEOUT: a bounded device-side wait gave up";
+  }
+  return "unknown pl_status";
+}
+
+int pl_version(void) { return 100; }
+
+size_t pl_nvfp4_bytes(int64_t d_o, int64_t d_i) {
+  if (d_o < 1 || d_i < 16 || d_i % 16 != 0) return 0;
+  const size_t P = static_cast<size_t>(d_o) * static_cast<size_t>(d_i);
+  return P / 2 + P / 16;
+}
+
+size_t pl_workspace_bytes(int64_t M, int64_t d_i, int64_t d_o, int r) {
+  if (M < 1 || d_o < 1 || d_i < 16 || d_i % 16 != 0 || r < 0 || r > 64) return 0;
+  size_t g = pl::generic_workspace_bytes(M, d_i, d_o, r);
+  size_t t = pl::tc_supported(M, d_i, d_o, r) ? pl::tc_workspace_bytes(M, d_i, d_o, r) : 0;
+  return g > t ? g : t;
+}
+
+pl_status pl_nvfp4_quantize(const void* W, int64_t d_o, int64_t d_i, uint8_t* codes,
+                            uint8_t* scales, float* s_g, pl_stream_t stream) {
+  if (!W || !codes || !scales || !s_g) return PL_ERR_NULL;
+  if (d_o < 1 || d_i < 16 || d_i % 16 != 0) return PL_ERR_SHAPE;
+  if (!aligned16(W) || !aligned16(codes) || (reinterpret_cast<uintptr_t>(s_g) & 3u)) return PL_ERR_ALIGN;
+  pl_status st = device_check();
+  if (st != PL_OK) return st;
+  return check_launch(pl::launch_quantize(W, d_o, d_i, codes, scales, s_g,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pl_status pl_rmsnorm_aqn(const void* x, int64_t M, int64_t d, const float* w_norm,
+                         const float* z, float eps, void* h, pl_stream_t stream) {
+  if (!x || !w_norm || !h) return PL_ERR_NULL;
+  if (M < 1 || d < 8 || d % 8 != 0 || M > 0x7FFFFFFF) return PL_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(h)) return PL_ERR_ALIGN;
+  pl_status st = device_check();
+  if (st != PL_OK) return st;
+  return check_launch(pl::launch_rmsnorm_aqn(x, M, d, w_norm, z, eps, h,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pl_status pl_nvfp4_lora_linear(const void* x, int64_t M, int64_t d_i, int64_t d_o,
+                               const uint8_t* codes, const uint8_t* scales, const float* s_g,
+                               const void* A, const void* B, int r, float lambda,
+                               const float* w_norm, const float* z, float eps, void* y,
+                               void* workspace, size_t ws_bytes, pl_stream_t stream) {
+  if (!x || !codes || !scales || !s_g || !y) return PL_ERR_NULL;
+  if (M < 1 || d_o < 1 || d_i < 16 || d_i % 16 != 0 || M > (1ll << 24) || d_o > (1ll << 31) ||
+      d_i > (1ll << 31))
+    return PL_ERR_SHAPE;
+  if (r < 0 || r > 64) return PL_ERR_RANK;
+  const bool lora = r > 0 && A != nullptr && B != nullptr;
+  if (r > 0 && (A == nullptr) != (B == nullptr)) return PL_ERR_NULL;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || !aligned16(y) ||
+      (lora && (!aligned16(A) || !aligned16(B))))
+    return PL_ERR_ALIGN;
+  const size_t need = pl_workspace_bytes(M, d_i, d_o, r);
+  if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return PL_ERR_WORKSPACE;
+  pl_status st = device_check();
+  if (st != PL_OK) return st;
+  pl::LinearArgs a{x, M, d_i, d_o, codes, scales, s_g, lora ? A : nullptr, lora ? B : nullptr,
+                   lora ? r : 0, lambda, w_norm, w_norm ? z : nullptr, eps, y, workspace, ws_bytes};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (pl::tc_supported(M, d_i, d_o, a.r)) return check_launch(pl::launch_linear_tc(a, s));
+  return check_launch(pl::launch_linear_generic(a, s));
+}
+
+pl_status pl_last_device_status(pl_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return PL_ERR_CUDA;
+  uint32_t bits = pl::tc_read_and_clear_status();
+  return (bits & pl::kStatusTimeout) ? PL_ERR_TIMEOUT : PL_OK;
+}
+
+void pl_debug_fail_next_launch(int armed) { g_fail_next_launch.store(armed ? 1 : 0); }
+
+}  // extern "C"

@@ -1,0 +1,55 @@
+// Internal host-side interface between the C ABI (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pl {
+
+// Device-side status bits set by bounded waits that gave up.
+enum : uint32_t { kStatusTimeout = 1u };
+
+// ---- quantize.cu
+cudaError_t launch_quantize(const void* W, int64_t d_o, int64_t d_i, uint8_t* codes,
+                            uint8_t* scales, float* s_g, cudaStream_t stream);
+
+// ---- norm.cu
+cudaError_t launch_rmsnorm_aqn(const void* x, int64_t M, int64_t d, const float* w_norm,
+                               const float* z, float eps, void* h, cudaStream_t stream);
+
+// Arguments of one linear call, shared by every path.
+struct LinearArgs {
+  const void* x;        // bf16 [M][d_i]
+  int64_t M, d_i, d_o;
+  const uint8_t* codes;   // [d_o][d_i/2]
+  const uint8_t* scales;  // [d_o][d_i/16]
+  const float* s_g;       // [1]
+  const void* A;          // bf16 [r][d_i] or null
+  const void* B;          // bf16 [d_o][r] or null
+  int r;
+  float lambda;
+  const float* w_norm;    // [d_i] or null
+  const float* z;         // [d_i] or null
+  float eps;
+  void* y;                // bf16 [M][d_o]
+  void* ws;               // workspace
+  size_t ws_bytes;
+};
+
+// ---- linear_generic.cu (CUDA cores, any d_i % 16 == 0)
+size_t generic_workspace_bytes(int64_t M, int64_t d_i, int64_t d_o, int r);
+cudaError_t launch_linear_generic(const LinearArgs& a, cudaStream_t stream);
+
+// ---- linear_tc.cu (tcgen05; d_i % 256 == 0)
+bool tc_supported(int64_t M, int64_t d_i, int64_t d_o, int r);
+size_t tc_workspace_bytes(int64_t M, int64_t d_i, int64_t d_o, int r);
+cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream);
+uint32_t tc_read_and_clear_status();
+
+// ---- api.cu
+int sm_count();  // SMs of the current device (cached)
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace pl

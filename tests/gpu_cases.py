@@ -1,0 +1,71 @@
+"""Helpers shared by the GPU parity tests: seeded cases on the device, the oracle's
+expected values on the host, and the tolerance checks the tests assert."""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import linear as olin
+from oracle import nvfp4 as onv
+from precision_linear_gb300 import synthetic
+
+DEV = "cuda"
+
+# Linear: max |y - y_ref| <= LINEAR_TOL * rms(y_ref), y_ref the FP64 oracle on the
+# oracle's own dequantised weights.  RMSNorm: elementwise relative error <= 2e-3
+# (BF16 output rounding alone contributes up to 2^-9 = 1.95e-3).
+LINEAR_TOL = 1e-2
+NORM_REL_TOL = 2e-3
+
+
+def np32(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy()
+
+
+def oracle_quantize(W_bf16: torch.Tensor):
+    packed, sb, s_g = onv.quantize(np32(W_bf16))
+    return packed, sb, s_g
+
+
+_QCACHE = {}
+
+
+def oracle_quantize_cached(key, W_bf16: torch.Tensor):
+    """Oracle NVFP4 encoding of a seeded weight, memoised on its generation key."""
+    if key not in _QCACHE:
+        if len(_QCACHE) > 8:
+            _QCACHE.clear()
+        _QCACHE[key] = oracle_quantize(W_bf16)
+    return _QCACHE[key]
+
+
+def to_dev_nvfp4(packed, sb, s_g, device=DEV):
+    return (torch.from_numpy(packed).to(device), torch.from_numpy(sb).to(device),
+            torch.tensor([float(s_g)], dtype=torch.float32, device=device))
+
+
+def assert_linear_close(y_gpu: torch.Tensor, y_ref: np.ndarray, what: str = ""):
+    y = np32(y_gpu).astype(np.float64)
+    assert y.shape == y_ref.shape, (y.shape, y_ref.shape)
+    assert np.all(np.isfinite(y)), f"{what}: non-finite output"
+    rms = float(np.sqrt(np.mean(y_ref * y_ref)))
+    err = float(np.max(np.abs(y - y_ref)))
+    assert err <= LINEAR_TOL * rms, f"{what}: max err {err:.3e} > {LINEAR_TOL} * rms {rms:.3e}"
+    return err / rms
+
+
+def make_case(d_o, d_i, M, r, sigma=1e-2, seed=0, outliers=0.0, device=DEV):
+    c = synthetic.projection_case(d_o, d_i, M, r, sigma, seed, outliers, device="cpu")
+    return {k: v.to(device) for k, v in c.items()}
+
+
+def oracle_linear(case, packed, sb, s_g, lam, norm=True, noise=True, lora=True, rows=None):
+    x = np32(case["x"]).astype(np.float64)
+    if rows is not None:
+        x = x[rows]
+    A = np32(case["A"]).astype(np.float64) if lora else None
+    B = np32(case["B"]).astype(np.float64) if lora else None
+    w = np32(case["w_norm"]).astype(np.float64) if norm else None
+    z = np32(case["z"]).astype(np.float64) if (norm and noise) else None
+    return olin.nvfp4_lora_linear(x, packed, sb, s_g, A, B, lam, w, z, synthetic.EPS)

@@ -1,0 +1,124 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the header
+declares, reports sizes, and rejects bad arguments on the host before launching."""
+
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "precision_linear.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from precision_linear_gb300 import binding, build
+    build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    src = open(HEADER, encoding="utf-8").read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pl_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings_and_version(L):
+    for s in range(9):
+        txt = L.pl_status_string(s).decode()
+        assert txt.startswith("PL_")
+    assert L.pl_status_string(99).decode() == "unknown pl_status"
+    assert L.pl_version() == 100
+
+
+def test_nvfp4_bytes_is_9P_over_16(L):
+    for d_o, d_i in [(256, 256), (3584, 3584), (512, 3584), (3584, 18944), (5120, 27648)]:
+        assert L.pl_nvfp4_bytes(d_o, d_i) == 9 * d_o * d_i // 16
+    assert L.pl_nvfp4_bytes(16, 24) == 0 and L.pl_nvfp4_bytes(0, 16) == 0
+
+
+def test_workspace_bytes(L):
+    assert L.pl_workspace_bytes(4, 256, 256, 8) > 0
+    assert L.pl_workspace_bytes(64, 3584, 3584, 32) >= 64 * 3584 * 2
+    assert L.pl_workspace_bytes(0, 256, 256, 8) == 0
+    assert L.pl_workspace_bytes(4, 250, 256, 8) == 0
+    assert L.pl_workspace_bytes(4, 256, 256, 65) == 0
+
+
+FAKE = 1 << 20  # an aligned, never-dereferenced address
+
+
+def _p(v):
+    return ctypes.c_void_p(v)
+
+
+def test_quantize_argument_checks(L):
+    ok = (_p(FAKE), 16, 32, _p(FAKE), _p(FAKE), _p(FAKE), None)
+    assert L.pl_nvfp4_quantize(None, *ok[1:]) == 1  # NULL
+    assert L.pl_nvfp4_quantize(_p(FAKE), 16, 24, *ok[3:]) == 2  # d_i % 16
+    assert L.pl_nvfp4_quantize(_p(FAKE), 0, 32, *ok[3:]) == 2
+    assert L.pl_nvfp4_quantize(_p(FAKE + 8), *ok[1:]) == 3  # misaligned W
+
+
+def test_rmsnorm_argument_checks(L):
+    args = [_p(FAKE), 4, 256, _p(FAKE), None, ctypes.c_float(1e-6), _p(FAKE), None]
+    a = list(args); a[0] = None
+    assert L.pl_rmsnorm_aqn(*a) == 1
+    a = list(args); a[2] = 250
+    assert L.pl_rmsnorm_aqn(*a) == 2
+    a = list(args); a[6] = _p(FAKE + 2)
+    assert L.pl_rmsnorm_aqn(*a) == 3
+
+
+def _lin_args(**kw):
+    d = dict(x=FAKE, M=4, d_i=256, d_o=256, codes=FAKE, scales=FAKE, s_g=FAKE, A=FAKE, B=FAKE, r=8,
+             lam=2.0, w_norm=FAKE, z=FAKE, eps=1e-6, y=FAKE, ws=FAKE, ws_bytes=1 << 30, stream=None)
+    d.update(kw)
+    return [_p(d["x"]) if d["x"] else None, d["M"], d["d_i"], d["d_o"], _p(d["codes"]) if d["codes"] else None,
+            _p(d["scales"]), _p(d["s_g"]), _p(d["A"]) if d["A"] else None, _p(d["B"]) if d["B"] else None,
+            d["r"], ctypes.c_float(d["lam"]), _p(d["w_norm"]) if d["w_norm"] else None,
+            _p(d["z"]) if d["z"] else None, ctypes.c_float(d["eps"]), _p(d["y"]),
+            _p(d["ws"]) if d["ws"] else None, d["ws_bytes"], d["stream"]]
+
+
+def test_linear_argument_checks(L):
+    f = L.pl_nvfp4_lora_linear
+    assert f(*_lin_args(x=0)) == 1
+    assert f(*_lin_args(codes=0)) == 1
+    assert f(*_lin_args(M=0)) == 2
+    assert f(*_lin_args(d_i=250)) == 2
+    assert f(*_lin_args(d_o=0)) == 2
+    assert f(*_lin_args(r=65)) == 4
+    assert f(*_lin_args(r=-1)) == 4
+    assert f(*_lin_args(B=0)) == 1  # A without B
+    assert f(*_lin_args(x=FAKE + 4)) == 3
+    assert f(*_lin_args(ws=0)) == 7
+    assert f(*_lin_args(ws_bytes=16)) == 7
+    assert f(*_lin_args(ws=FAKE + 16)) == 7  # workspace must be 256-byte aligned
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_valid_arguments_without_a_device_report_device_error(L):
+    assert L.pl_nvfp4_lora_linear(*_lin_args()) == 5
+    assert L.pl_nvfp4_quantize(_p(FAKE), 16, 32, _p(FAKE), _p(FAKE), _p(FAKE), None) == 5
+
+
+def test_product_path_does_not_import_the_oracle():
+    """The package and bench's product arm never reach oracle/: only tests, smoke()
+    and the CPU-baseline legs may."""
+    pkg = os.path.join(ROOT, "precision_linear_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                txt = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert not re.search(r"^\s*(from|import)\s+oracle\b", txt, re.M), f

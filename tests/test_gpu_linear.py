@@ -1,0 +1,106 @@
+"""GPU NVFP4 + LoRA linear vs the FP64 oracle (max |y - y_ref| <= 1e-2 rms(y_ref)).
+
+The GPU linear is fed the oracle's own NVFP4 encoding of each weight, so these
+tests do not depend on the GPU quantiser; one end-to-end test chains the GPU
+quantiser into the GPU linear."""
+
+import numpy as np
+import pytest
+import torch
+
+from precision_linear_gb300 import binding as pl
+from precision_linear_gb300 import synthetic
+from tests.gpu_cases import (DEV, assert_linear_close, make_case, np32, oracle_linear, oracle_quantize,
+                             oracle_quantize_cached, to_dev_nvfp4)
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(case, dev_w, lam, norm=True, noise=True, lora=True):
+    return pl.nvfp4_lora_linear(case["x"], *dev_w, case["A"] if lora else None, case["B"] if lora else None,
+                                lam, case["w_norm"] if norm else None, case["z"] if (norm and noise) else None,
+                                synthetic.EPS)
+
+
+def _check(d_o, d_i, M, r, lam=2.0, seed=0, outliers=0.0, sigma=1e-2, **kw):
+    case = make_case(d_o, d_i, M, r, sigma, seed, outliers)
+    packed, sb, s_g = oracle_quantize_cached((d_o, d_i, seed, outliers), case["W"])
+    y = _run(case, to_dev_nvfp4(packed, sb, s_g), lam, **kw)
+    ref = oracle_linear(case, packed, sb, s_g, lam, **kw)
+    return assert_linear_close(y, ref, f"d_o={d_o} d_i={d_i} M={M} r={r} {kw}")
+
+
+def test_tiny(cuda_ok):
+    wl = synthetic.WORKLOADS["tiny"]
+    _check(256, 256, 4, wl.r, wl.lam, seed=wl.seed)
+
+
+@pytest.mark.parametrize("M", [1, 8, 16, 32, 64])
+def test_decode_projection_sweep(cuda_ok, M):
+    wl = synthetic.WORKLOADS["decode_proj_7b"]
+    _check(3584, 3584, M, wl.r, wl.lam, seed=wl.seed, outliers=wl.outlier_frac)
+
+
+@pytest.mark.parametrize("kw", [dict(lora=False), dict(norm=False), dict(noise=False), dict(lam=0.0)])
+def test_path_variants(cuda_ok, kw):
+    lam = kw.pop("lam", 2.0)
+    _check(3584, 3584, 16, 32, lam, seed=5, **kw)
+
+
+@pytest.mark.parametrize("r", [1, 8, 64])
+def test_ranks(cuda_ok, r):
+    _check(1024, 512, 9, r, seed=r)
+
+
+@pytest.mark.parametrize("d_o,d_i,M", [(1, 256, 1), (100, 256, 3), (129, 512, 17), (300, 768, 63),
+                                       (257, 512, 64), (130, 512, 65), (77, 272, 5), (40, 48, 2),
+                                       (384, 256, 200)])
+def test_ragged_shapes(cuda_ok, d_o, d_i, M):
+    _check(d_o, d_i, M, 8, seed=d_o * 7 + M)
+
+
+@pytest.mark.parametrize("M", [8, 32, 64])
+def test_7b_layer_set(cuda_ok, M):
+    wl = synthetic.WORKLOADS["layer_7b"]
+    for i, p in enumerate(wl.projs):
+        norm = p.norm is not None
+        _check(p.d_o, p.d_i, M, wl.r, wl.lam, seed=synthetic.proj_seed(wl, 0, i), norm=norm)
+
+
+def test_7b_layer_prefill_m4096_sampled_rows(cuda_ok):
+    wl = synthetic.WORKLOADS["prefill_7b"]
+    M = wl.Ms[0]
+    rows = np.random.default_rng(0).choice(M, 48, replace=False)
+    rows.sort()
+    for i, p in enumerate(wl.projs):
+        norm = p.norm is not None
+        case = make_case(p.d_o, p.d_i, M, wl.r, wl.sigma, synthetic.proj_seed(wl, 0, i))
+        packed, sb, s_g = oracle_quantize(case["W"])
+        y = _run(case, to_dev_nvfp4(packed, sb, s_g), wl.lam, norm=norm)
+        ref = oracle_linear(case, packed, sb, s_g, wl.lam, norm=norm, rows=rows)
+        assert_linear_close(y[torch.from_numpy(rows).to(DEV)], ref, f"prefill {p.name}")
+
+
+def test_32b_stack_sampled_layer(cuda_ok):
+    wl = synthetic.WORKLOADS["stack_32b"]
+    for i, p in enumerate(wl.projs):
+        for M in wl.Ms:
+            norm = p.norm is not None
+            _check(p.d_o, p.d_i, M, wl.r, wl.lam, seed=synthetic.proj_seed(wl, 31, i), sigma=wl.sigma,
+                   norm=norm)
+
+
+def test_end_to_end_gpu_quantiser_into_linear(cuda_ok):
+    case = make_case(3584, 3584, 32, 32, 1e-2, 2, 1e-3)
+    dev_w = pl.nvfp4_quantize(case["W"])
+    y = _run(case, dev_w, 2.0)
+    packed, sb, s_g = oracle_quantize(case["W"])
+    assert_linear_close(y, oracle_linear(case, packed, sb, s_g, 2.0), "gpu quantiser -> gpu linear")
+
+
+def test_repeatable_bitwise(cuda_ok):
+    for M in (1, 64, 300):
+        case = make_case(1024, 3584, M, 32, seed=M)
+        dev_w = pl.nvfp4_quantize(case["W"])
+        ys = [_run(case, dev_w, 2.0) for _ in range(3)]
+        assert torch.equal(ys[0], ys[1]) and torch.equal(ys[0], ys[2])
