@@ -53,6 +53,14 @@ extern "C" {
 /* Same type as cudaStream_t. */
 typedef struct CUstream_st* pl_stream_t;
 
+/* Element type of an output buffer.  Arithmetic is FP32 either way; a BF16
+ * output is the round-to-nearest-even BF16 of exactly the FP32 value the FP32
+ * output would hold. */
+typedef enum pl_dtype {
+  PL_DTYPE_BF16 = 0,
+  PL_DTYPE_F32 = 1
+} pl_dtype;
+
 typedef enum pl_status {
   PL_OK = 0,
   PL_ERR_NULL = 1,      /* a required pointer is NULL                         */
@@ -104,11 +112,12 @@ pl_status pl_nvfp4_quantize(const void* W_bf16, int64_t d_o, int64_t d_i,
 /* RMSNorm with AQN noise folded into the scale (section 5.1):
  *   h[m, :] = x[m, :] / sqrt(mean_j x[m, j]^2 + eps) (.) (w_norm + z)
  *  x_bf16 in : BF16 [M][d];  w_norm in: FP32 [d];  z in: FP32 [d] or NULL (no
- *  noise);  h_bf16 out: BF16 [M][d] (round to nearest).  w_norm + z is formed
- *  in FP32.  Requirements: M >= 1, d >= 1, d % 8 == 0, x and h 16-byte aligned. */
+ *  noise);  h out: [M][d] of h_dtype (BF16 rounds to nearest even).  w_norm + z
+ *  is formed in FP32.  Requirements: M >= 1, d >= 8, d % 8 == 0, x and h 16-byte
+ *  aligned, h_dtype a pl_dtype. */
 pl_status pl_rmsnorm_aqn(const void* x_bf16, int64_t M, int64_t d,
                          const float* w_norm, const float* z, float eps,
-                         void* h_bf16, pl_stream_t stream);
+                         void* h, int h_dtype, pl_stream_t stream);
 
 /* The quantised-backbone LoRA linear (section 2.1 forward map, with the
  * section 5.1 prologue when w_norm is given):
@@ -119,7 +128,7 @@ pl_status pl_rmsnorm_aqn(const void* x_bf16, int64_t M, int64_t d,
  *  A_bf16  in : BF16 [r][d_i], B_bf16 in: BF16 [d_o][r]; both NULL or r == 0
  *               means no adapter.
  *  w_norm, z in: FP32 [d_i] or NULL (z NULL = no noise; w_norm NULL = no norm)
- *  y_bf16  out: BF16 [M][d_o]
+ *  y       out: [M][d_o] of y_dtype (a pl_dtype)
  *  workspace  : device scratch of at least pl_workspace_bytes(M, d_i, d_o, r).
  * Accumulation is FP32.  M <= 64 runs the decode path, larger M the prefill
  * path; both use tcgen05 tensor cores when d_i % 256 == 0 and a generic CUDA-core
@@ -129,7 +138,7 @@ pl_status pl_nvfp4_lora_linear(const void* x_bf16, int64_t M, int64_t d_i, int64
                                const uint8_t* codes, const uint8_t* scales, const float* s_g,
                                const void* A_bf16, const void* B_bf16, int r, float lambda,
                                const float* w_norm, const float* z, float eps,
-                               void* y_bf16, void* workspace, size_t workspace_bytes,
+                               void* y, int y_dtype, void* workspace, size_t workspace_bytes,
                                pl_stream_t stream);
 
 /* Synchronises `stream`, then returns and clears the device status word that
@@ -140,6 +149,12 @@ pl_status pl_last_device_status(pl_stream_t stream);
  * reports a launch failure (PL_ERR_CUDA) as if the CUDA runtime had returned
  * one, without faulting anything.  One-shot; 0 disarms. */
 void pl_debug_fail_next_launch(int armed);
+
+/* Test hook: launches one tiny kernel whose bounded wait on a barrier that nothing
+ * completes gives up after 2 ms, exactly as a stalled pipeline wait would; the
+ * device status word then reads PL_ERR_TIMEOUT through pl_last_device_status.
+ * Faults nothing and leaves the context usable. */
+pl_status pl_debug_wait_timeout_probe(pl_stream_t stream);
 
 #ifdef __cplusplus
 }

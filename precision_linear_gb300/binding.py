@@ -24,6 +24,9 @@ _lock = threading.Lock()
 _lib = None
 
 PL_OK = 0
+PL_DTYPE_BF16 = 0
+PL_DTYPE_F32 = 1
+_OUT_DTYPES = {torch.bfloat16: PL_DTYPE_BF16, torch.float32: PL_DTYPE_F32}
 
 
 class PLError(RuntimeError):
@@ -39,13 +42,14 @@ _SIGNATURES = {
     "pl_workspace_bytes": (ctypes.c_size_t, [_i64, _i64, _i64, ctypes.c_int]),
     "pl_nvfp4_quantize": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
     "pl_rmsnorm_aqn": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, ctypes.c_float,
-                                      _c_void_p, _c_void_p]),
+                                      _c_void_p, ctypes.c_int, _c_void_p]),
     "pl_nvfp4_lora_linear": (ctypes.c_int, [_c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p, _c_void_p,
                                             _c_void_p, _c_void_p, ctypes.c_int, ctypes.c_float,
-                                            _c_void_p, _c_void_p, ctypes.c_float, _c_void_p,
+                                            _c_void_p, _c_void_p, ctypes.c_float, _c_void_p, ctypes.c_int,
                                             _c_void_p, ctypes.c_size_t, _c_void_p]),
     "pl_last_device_status": (ctypes.c_int, [_c_void_p]),
     "pl_debug_fail_next_launch": (None, [ctypes.c_int]),
+    "pl_debug_wait_timeout_probe": (ctypes.c_int, [_c_void_p]),
 }
 
 
@@ -126,18 +130,23 @@ def nvfp4_quantize(W: torch.Tensor, codes=None, scales=None, s_g=None):
 
 
 def rmsnorm_aqn(x: torch.Tensor, w_norm: torch.Tensor, z: torch.Tensor | None = None,
-                eps: float = 1e-6, out: torch.Tensor | None = None) -> torch.Tensor:
-    """BF16 h = x / sqrt(mean(x^2) + eps) * (w_norm + z) per row."""
+                eps: float = 1e-6, out: torch.Tensor | None = None,
+                out_dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
+    """h = x / sqrt(mean(x^2) + eps) * (w_norm + z) per row, BF16 or FP32 output."""
     _need(x, "x", torch.bfloat16, dim=2)
     dev = x.device
     _need(w_norm, "w_norm", torch.float32, dev, 1)
     if z is not None:
         _need(z, "z", torch.float32, dev, 1)
     if out is None:
-        out = torch.empty_like(x)
+        out = torch.empty(x.shape, dtype=out_dtype, device=dev)
+    _need(out, "out", out.dtype, dev, 2)
+    if out.dtype not in _OUT_DTYPES:
+        raise TypeError("out must be bfloat16 or float32")
     M, d = x.shape
     with torch.cuda.device(dev):
-        st = lib().pl_rmsnorm_aqn(_ptr(x), M, d, _ptr(w_norm), _ptr(z), float(eps), _ptr(out), _stream(dev))
+        st = lib().pl_rmsnorm_aqn(_ptr(x), M, d, _ptr(w_norm), _ptr(z), float(eps), _ptr(out),
+                                  _OUT_DTYPES[out.dtype], _stream(dev))
     _check(st, "pl_rmsnorm_aqn")
     return out
 
@@ -159,7 +168,8 @@ _default_ws = {}
 
 
 def nvfp4_lora_linear(x, codes, scales, s_g, A=None, B=None, lam: float = 0.0, w_norm=None, z=None,
-                      eps: float = 1e-6, out=None, workspace: Workspace | None = None) -> torch.Tensor:
+                      eps: float = 1e-6, out=None, workspace: Workspace | None = None,
+                      out_dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
     """y = W_hat h + lam * B (A h) with h = RMSNorm_AQN(x) when w_norm is given (else x)."""
     _need(x, "x", torch.bfloat16, dim=2)
     dev = x.device
@@ -178,7 +188,10 @@ def nvfp4_lora_linear(x, codes, scales, s_g, A=None, B=None, lam: float = 0.0, w
     if z is not None:
         _need(z, "z", torch.float32, dev, 1)
     if out is None:
-        out = torch.empty(M, d_o, dtype=torch.bfloat16, device=dev)
+        out = torch.empty(M, d_o, dtype=out_dtype, device=dev)
+    if out.dtype not in _OUT_DTYPES:
+        raise TypeError("out must be bfloat16 or float32")
+    _need(out, "out", out.dtype, dev, 2)
     need = workspace_bytes(M, d_i, d_o, r)
     if workspace is None:
         workspace = _default_ws.setdefault(dev, Workspace(dev))
@@ -186,7 +199,7 @@ def nvfp4_lora_linear(x, codes, scales, s_g, A=None, B=None, lam: float = 0.0, w
     with torch.cuda.device(dev):
         st = lib().pl_nvfp4_lora_linear(_ptr(x), M, d_i, d_o, _ptr(codes), _ptr(scales), _ptr(s_g),
                                         _ptr(A), _ptr(B), r, float(lam), _ptr(w_norm), _ptr(z), float(eps),
-                                        _ptr(out), _ptr(ws), ws.numel(), _stream(dev))
+                                        _ptr(out), _OUT_DTYPES[out.dtype], _ptr(ws), ws.numel(), _stream(dev))
     _check(st, "pl_nvfp4_lora_linear")
     return out
 

@@ -103,13 +103,14 @@ pl_status pl_nvfp4_quantize(const void* W, int64_t d_o, int64_t d_i, uint8_t* co
 }
 
 pl_status pl_rmsnorm_aqn(const void* x, int64_t M, int64_t d, const float* w_norm,
-                         const float* z, float eps, void* h, pl_stream_t stream) {
+                         const float* z, float eps, void* h, int h_dtype, pl_stream_t stream) {
   if (!x || !w_norm || !h) return PL_ERR_NULL;
   if (M < 1 || d < 8 || d % 8 != 0 || M > 0x7FFFFFFF) return PL_ERR_SHAPE;
+  if (h_dtype != PL_DTYPE_BF16 && h_dtype != PL_DTYPE_F32) return PL_ERR_SHAPE;
   if (!aligned16(x) || !aligned16(h)) return PL_ERR_ALIGN;
   pl_status st = device_check();
   if (st != PL_OK) return st;
-  return check_launch(pl::launch_rmsnorm_aqn(x, M, d, w_norm, z, eps, h,
+  return check_launch(pl::launch_rmsnorm_aqn(x, M, d, w_norm, z, eps, h, h_dtype == PL_DTYPE_F32,
                                              reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -117,11 +118,12 @@ pl_status pl_nvfp4_lora_linear(const void* x, int64_t M, int64_t d_i, int64_t d_
                                const uint8_t* codes, const uint8_t* scales, const float* s_g,
                                const void* A, const void* B, int r, float lambda,
                                const float* w_norm, const float* z, float eps, void* y,
-                               void* workspace, size_t ws_bytes, pl_stream_t stream) {
+                               int y_dtype, void* workspace, size_t ws_bytes, pl_stream_t stream) {
   if (!x || !codes || !scales || !s_g || !y) return PL_ERR_NULL;
   if (M < 1 || d_o < 1 || d_i < 16 || d_i % 16 != 0 || M > (1ll << 24) || d_o > (1ll << 31) ||
       d_i > (1ll << 31))
     return PL_ERR_SHAPE;
+  if (y_dtype != PL_DTYPE_BF16 && y_dtype != PL_DTYPE_F32) return PL_ERR_SHAPE;
   if (r < 0 || r > 64) return PL_ERR_RANK;
   const bool lora = r > 0 && A != nullptr && B != nullptr;
   if (r > 0 && (A == nullptr) != (B == nullptr)) return PL_ERR_NULL;
@@ -134,7 +136,8 @@ pl_status pl_nvfp4_lora_linear(const void* x, int64_t M, int64_t d_i, int64_t d_
   pl_status st = device_check();
   if (st != PL_OK) return st;
   pl::LinearArgs a{x, M, d_i, d_o, codes, scales, s_g, lora ? A : nullptr, lora ? B : nullptr,
-                   lora ? r : 0, lambda, w_norm, w_norm ? z : nullptr, eps, y, workspace, ws_bytes};
+                   lora ? r : 0, lambda, w_norm, w_norm ? z : nullptr, eps, y, y_dtype == PL_DTYPE_F32,
+                   workspace, ws_bytes};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (pl::tc_supported(M, d_i, d_o, a.r)) return check_launch(pl::launch_linear_tc(a, s));
   return check_launch(pl::launch_linear_generic(a, s));
@@ -147,5 +150,11 @@ pl_status pl_last_device_status(pl_stream_t stream) {
 }
 
 void pl_debug_fail_next_launch(int armed) { g_fail_next_launch.store(armed ? 1 : 0); }
+
+pl_status pl_debug_wait_timeout_probe(pl_stream_t stream) {
+  pl_status st = device_check();
+  if (st != PL_OK) return st;
+  return check_launch(pl::launch_wait_timeout_probe(reinterpret_cast<cudaStream_t>(stream)));
+}
 
 }  // extern "C"

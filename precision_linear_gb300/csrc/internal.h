@@ -16,7 +16,7 @@ cudaError_t launch_quantize(const void* W, int64_t d_o, int64_t d_i, uint8_t* co
 
 // ---- norm.cu
 cudaError_t launch_rmsnorm_aqn(const void* x, int64_t M, int64_t d, const float* w_norm,
-                               const float* z, float eps, void* h, cudaStream_t stream);
+                               const float* z, float eps, void* h, bool h_f32, cudaStream_t stream);
 
 // Arguments of one linear call, shared by every path.
 struct LinearArgs {
@@ -32,7 +32,8 @@ struct LinearArgs {
   const float* w_norm;    // [d_i] or null
   const float* z;         // [d_i] or null
   float eps;
-  void* y;                // bf16 [M][d_o]
+  void* y;                // [M][d_o], bf16 or fp32
+  bool y_f32;
   void* ws;               // workspace
   size_t ws_bytes;
 };
@@ -46,6 +47,7 @@ bool tc_supported(int64_t M, int64_t d_i, int64_t d_o, int r);
 size_t tc_workspace_bytes(int64_t M, int64_t d_i, int64_t d_o, int r);
 cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream);
 uint32_t tc_read_and_clear_status();
+cudaError_t launch_wait_timeout_probe(cudaStream_t stream);
 
 // ---- api.cu
 int sm_count();  // SMs of the current device (cached)

@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(kMainWarps * 32) k_main(const uint8_t* __restr
                                                           const float* __restrict__ t,
                                                           const __nv_bfloat16* __restrict__ B, int r,
                                                           float lambda, int64_t M, int64_t d_i,
-                                                          int64_t d_o, __nv_bfloat16* __restrict__ y) {
+                                                          int64_t d_o, void* __restrict__ y, bool y_f32) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t o = static_cast<int64_t>(blockIdx.x) * kMainWarps + warp;
   if (o >= d_o) return;
@@ -148,7 +148,13 @@ __global__ void __launch_bounds__(kMainWarps * 32) k_main(const uint8_t* __restr
 #pragma unroll
       for (int s = 16; s > 0; s >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, s);
     }
-    if (lane == 0) y[(m0 + i) * d_o + o] = __float2bfloat16_rn(fmaf(lambda, l, s_g * a));
+    if (lane == 0) {
+      const float v = fmaf(lambda, l, s_g * a);
+      if (y_f32)
+        static_cast<float*>(y)[(m0 + i) * d_o + o] = v;
+      else
+        static_cast<__nv_bfloat16*>(y)[(m0 + i) * d_o + o] = __float2bfloat16_rn(v);
+    }
   }
 }
 
@@ -171,7 +177,7 @@ cudaError_t launch_linear_generic(const LinearArgs& a, cudaStream_t stream) {
             static_cast<unsigned>((a.M + kTok - 1) / kTok));
   k_main<<<grid, kMainWarps * 32, 0, stream>>>(
       a.codes, a.scales, a.s_g, w.h, w.t, lora ? static_cast<const __nv_bfloat16*>(a.B) : nullptr,
-      lora ? a.r : 0, a.lambda, a.M, a.d_i, a.d_o, static_cast<__nv_bfloat16*>(a.y));
+      lora ? a.r : 0, a.lambda, a.M, a.d_i, a.d_o, a.y, a.y_f32);
   return cudaGetLastError();
 }
 

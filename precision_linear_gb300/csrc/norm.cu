@@ -27,14 +27,14 @@ PL_DEVINL float block_sum(float v, float* red) {
   return s;
 }
 
+template <bool kF32>
 __global__ void __launch_bounds__(kThreads) k_rmsnorm_aqn(const uint4* __restrict__ x, int64_t d,
                                                           const float* __restrict__ w_norm,
                                                           const float* __restrict__ z, float eps,
-                                                          uint4* __restrict__ h) {
+                                                          void* __restrict__ h) {
   __shared__ float red[kThreads / 32];
   const int64_t nv = d / 8;
   const uint4* xr = x + blockIdx.x * nv;
-  uint4* hr = h + blockIdx.x * nv;
   float ss = 0.f;
   for (int64_t i = threadIdx.x; i < nv; i += kThreads) {
     const uint4 v = xr[i];
@@ -51,7 +51,7 @@ __global__ void __launch_bounds__(kThreads) k_rmsnorm_aqn(const uint4* __restric
   for (int64_t i = threadIdx.x; i < nv; i += kThreads) {
     const uint4 v = xr[i];
     const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[4];
+    float hv[8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int64_t k = 8 * i + 2 * j;
@@ -60,21 +60,35 @@ __global__ void __launch_bounds__(kThreads) k_rmsnorm_aqn(const uint4* __restric
         s0 += z[k];
         s1 += z[k + 1];
       }
-      const float h0 = (bf16lo_to_f32(u[j]) * inv) * s0;
-      const float h1 = (bf16hi_to_f32(u[j]) * inv) * s1;
-      const __nv_bfloat162 p = __floats2bfloat162_rn(h0, h1);
-      o[j] = *reinterpret_cast<const uint32_t*>(&p);
+      hv[2 * j] = (bf16lo_to_f32(u[j]) * inv) * s0;
+      hv[2 * j + 1] = (bf16hi_to_f32(u[j]) * inv) * s1;
     }
-    hr[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    if (kF32) {
+      float4* hr = static_cast<float4*>(h) + (blockIdx.x * nv + i) * 2;
+      hr[0] = make_float4(hv[0], hv[1], hv[2], hv[3]);
+      hr[1] = make_float4(hv[4], hv[5], hv[6], hv[7]);
+    } else {
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const __nv_bfloat162 p = __floats2bfloat162_rn(hv[2 * j], hv[2 * j + 1]);
+        o[j] = *reinterpret_cast<const uint32_t*>(&p);
+      }
+      static_cast<uint4*>(h)[blockIdx.x * nv + i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
   }
 }
 
 }  // namespace
 
 cudaError_t launch_rmsnorm_aqn(const void* x, int64_t M, int64_t d, const float* w_norm,
-                               const float* z, float eps, void* h, cudaStream_t stream) {
-  k_rmsnorm_aqn<<<static_cast<unsigned>(M), kThreads, 0, stream>>>(
-      static_cast<const uint4*>(x), d, w_norm, z, eps, static_cast<uint4*>(h));
+                               const float* z, float eps, void* h, bool h_f32, cudaStream_t stream) {
+  if (h_f32)
+    k_rmsnorm_aqn<true><<<static_cast<unsigned>(M), kThreads, 0, stream>>>(
+        static_cast<const uint4*>(x), d, w_norm, z, eps, h);
+  else
+    k_rmsnorm_aqn<false><<<static_cast<unsigned>(M), kThreads, 0, stream>>>(
+        static_cast<const uint4*>(x), d, w_norm, z, eps, h);
   return cudaGetLastError();
 }
 

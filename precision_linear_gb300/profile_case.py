@@ -1,0 +1,61 @@
+"""A small, self-contained run of one library call for profilers (ncu).
+
+    python -m precision_linear_gb300.profile_case --op linear --workload decode_proj_7b --M 64 --calls 6
+    python -m precision_linear_gb300.profile_case --op quantize --workload decode_proj_7b --calls 3
+
+It draws the seeded workload, quantises its weight once, makes enough distinct
+weight copies that the set is larger than L2 (so each profiled launch reads its
+weights from DRAM), then issues `--calls` back-to-back calls over the copies
+and synchronises.  Nothing is timed here; use bench.py for numbers.
+"""
+
+from __future__ import annotations
+
+import argparse
+
+import torch
+
+from . import binding as pl
+from . import synthetic
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--op", choices=["linear", "quantize", "rmsnorm"], default="linear")
+    ap.add_argument("--workload", default="decode_proj_7b")
+    ap.add_argument("--proj", type=int, default=0, help="index of the projection in the workload")
+    ap.add_argument("--M", type=int, default=64)
+    ap.add_argument("--calls", type=int, default=6)
+    ap.add_argument("--copies", type=int, default=0, help="distinct weight copies (0: enough for > 2x L2)")
+    a = ap.parse_args(argv)
+    dev = torch.device("cuda", 0)
+    wl = synthetic.WORKLOADS[a.workload]
+    p = wl.projs[a.proj]
+    c = synthetic.projection_case(p.d_o, p.d_i, a.M, wl.r, wl.sigma, wl.seed, wl.outlier_frac, device="cpu")
+    g = {k: v.to(dev) for k, v in c.items()}
+    if a.op == "quantize":
+        for _ in range(a.calls):
+            pl.nvfp4_quantize(g["W"])
+        torch.cuda.synchronize()
+        return
+    if a.op == "rmsnorm":
+        for _ in range(a.calls):
+            pl.rmsnorm_aqn(g["x"], g["w_norm"], g["z"], synthetic.EPS)
+        torch.cuda.synchronize()
+        return
+    codes, scales, s_g = pl.nvfp4_quantize(g["W"])
+    per = codes.numel() + scales.numel()
+    n = a.copies or max(2, (2 * 129 * 2 ** 20) // per + 1)
+    copies = [(codes.clone(), scales.clone(), s_g.clone()) for _ in range(n)]
+    norm = p.norm is not None
+    ws = pl.Workspace(dev)
+    y = torch.empty(a.M, p.d_o, dtype=torch.bfloat16, device=dev)
+    for i in range(a.calls):
+        cc, ss, sg = copies[i % n]
+        pl.nvfp4_lora_linear(g["x"], cc, ss, sg, g["A"], g["B"], wl.lam, g["w_norm"] if norm else None,
+                             g["z"] if norm else None, synthetic.EPS, out=y, workspace=ws)
+    torch.cuda.synchronize()
+
+
+if __name__ == "__main__":
+    main()

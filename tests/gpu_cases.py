@@ -13,8 +13,10 @@ from precision_linear_gb300 import synthetic
 DEV = "cuda"
 
 # Linear: max |y - y_ref| <= LINEAR_TOL * rms(y_ref), y_ref the FP64 oracle on the
-# oracle's own dequantised weights.  RMSNorm: elementwise relative error <= 2e-3
-# (BF16 output rounding alone contributes up to 2^-9 = 1.95e-3).
+# oracle's own dequantised weights.  RMSNorm: elementwise relative error <= 2e-3.
+# Both bounds are checked on the FP32 output mode: one round-to-nearest to BF16
+# alone has relative error up to 2^-8 = 3.9e-3, more than either bound allows.
+# The BF16 output mode is then required to be exactly RN-even(FP32 output).
 LINEAR_TOL = 1e-2
 NORM_REL_TOL = 2e-3
 
@@ -53,6 +55,13 @@ def assert_linear_close(y_gpu: torch.Tensor, y_ref: np.ndarray, what: str = ""):
     err = float(np.max(np.abs(y - y_ref)))
     assert err <= LINEAR_TOL * rms, f"{what}: max err {err:.3e} > {LINEAR_TOL} * rms {rms:.3e}"
     return err / rms
+
+
+def assert_bf16_is_rounded_f32(y_bf16: torch.Tensor, y_f32: torch.Tensor, what: str = ""):
+    assert y_bf16.dtype == torch.bfloat16 and y_f32.dtype == torch.float32
+    want = y_f32.to(torch.bfloat16)
+    same = torch.eq(y_bf16.view(torch.int16), want.view(torch.int16))
+    assert bool(same.all()), f"{what}: {int((~same).sum())} BF16 outputs are not RN(FP32 output)"
 
 
 def make_case(d_o, d_i, M, r, sigma=1e-2, seed=0, outliers=0.0, device=DEV):

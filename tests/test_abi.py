@@ -71,23 +71,25 @@ def test_quantize_argument_checks(L):
 
 
 def test_rmsnorm_argument_checks(L):
-    args = [_p(FAKE), 4, 256, _p(FAKE), None, ctypes.c_float(1e-6), _p(FAKE), None]
+    args = [_p(FAKE), 4, 256, _p(FAKE), None, ctypes.c_float(1e-6), _p(FAKE), 0, None]
     a = list(args); a[0] = None
     assert L.pl_rmsnorm_aqn(*a) == 1
     a = list(args); a[2] = 250
     assert L.pl_rmsnorm_aqn(*a) == 2
     a = list(args); a[6] = _p(FAKE + 2)
     assert L.pl_rmsnorm_aqn(*a) == 3
+    a = list(args); a[7] = 2  # not a pl_dtype
+    assert L.pl_rmsnorm_aqn(*a) == 2
 
 
 def _lin_args(**kw):
     d = dict(x=FAKE, M=4, d_i=256, d_o=256, codes=FAKE, scales=FAKE, s_g=FAKE, A=FAKE, B=FAKE, r=8,
-             lam=2.0, w_norm=FAKE, z=FAKE, eps=1e-6, y=FAKE, ws=FAKE, ws_bytes=1 << 30, stream=None)
+             lam=2.0, w_norm=FAKE, z=FAKE, eps=1e-6, y=FAKE, y_dtype=0, ws=FAKE, ws_bytes=1 << 30, stream=None)
     d.update(kw)
     return [_p(d["x"]) if d["x"] else None, d["M"], d["d_i"], d["d_o"], _p(d["codes"]) if d["codes"] else None,
             _p(d["scales"]), _p(d["s_g"]), _p(d["A"]) if d["A"] else None, _p(d["B"]) if d["B"] else None,
             d["r"], ctypes.c_float(d["lam"]), _p(d["w_norm"]) if d["w_norm"] else None,
-            _p(d["z"]) if d["z"] else None, ctypes.c_float(d["eps"]), _p(d["y"]),
+            _p(d["z"]) if d["z"] else None, ctypes.c_float(d["eps"]), _p(d["y"]), d["y_dtype"],
             _p(d["ws"]) if d["ws"] else None, d["ws_bytes"], d["stream"]]
 
 
@@ -105,6 +107,7 @@ def test_linear_argument_checks(L):
     assert f(*_lin_args(ws=0)) == 7
     assert f(*_lin_args(ws_bytes=16)) == 7
     assert f(*_lin_args(ws=FAKE + 16)) == 7  # workspace must be 256-byte aligned
+    assert f(*_lin_args(y_dtype=5)) == 2
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")

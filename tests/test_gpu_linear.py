@@ -10,24 +10,29 @@ import torch
 
 from precision_linear_gb300 import binding as pl
 from precision_linear_gb300 import synthetic
-from tests.gpu_cases import (DEV, assert_linear_close, make_case, np32, oracle_linear, oracle_quantize,
-                             oracle_quantize_cached, to_dev_nvfp4)
+from tests.gpu_cases import (DEV, assert_bf16_is_rounded_f32, assert_linear_close, make_case, np32,
+                             oracle_linear, oracle_quantize, oracle_quantize_cached, to_dev_nvfp4)
 
 pytestmark = pytest.mark.gpu
 
 
-def _run(case, dev_w, lam, norm=True, noise=True, lora=True):
+def _run(case, dev_w, lam, norm=True, noise=True, lora=True, out_dtype=torch.float32):
     return pl.nvfp4_lora_linear(case["x"], *dev_w, case["A"] if lora else None, case["B"] if lora else None,
                                 lam, case["w_norm"] if norm else None, case["z"] if (norm and noise) else None,
-                                synthetic.EPS)
+                                synthetic.EPS, out_dtype=out_dtype)
 
 
 def _check(d_o, d_i, M, r, lam=2.0, seed=0, outliers=0.0, sigma=1e-2, **kw):
+    """FP32 output within the tolerance of the oracle; BF16 output == RN(FP32 output)."""
     case = make_case(d_o, d_i, M, r, sigma, seed, outliers)
     packed, sb, s_g = oracle_quantize_cached((d_o, d_i, seed, outliers), case["W"])
-    y = _run(case, to_dev_nvfp4(packed, sb, s_g), lam, **kw)
+    dev_w = to_dev_nvfp4(packed, sb, s_g)
+    y = _run(case, dev_w, lam, **kw)
+    yb = _run(case, dev_w, lam, out_dtype=torch.bfloat16, **kw)
+    what = f"d_o={d_o} d_i={d_i} M={M} r={r} {kw}"
+    assert_bf16_is_rounded_f32(yb, y, what)
     ref = oracle_linear(case, packed, sb, s_g, lam, **kw)
-    return assert_linear_close(y, ref, f"d_o={d_o} d_i={d_i} M={M} r={r} {kw}")
+    return assert_linear_close(y, ref, what)
 
 
 def test_tiny(cuda_ok):

@@ -7,7 +7,7 @@ import torch
 from oracle import linear as olin
 from precision_linear_gb300 import binding as pl
 from precision_linear_gb300 import synthetic
-from tests.gpu_cases import DEV, NORM_REL_TOL, np32
+from tests.gpu_cases import DEV, NORM_REL_TOL, assert_bf16_is_rounded_f32, np32
 
 pytestmark = pytest.mark.gpu
 
@@ -19,7 +19,10 @@ def test_rmsnorm_aqn_matches_oracle(cuda_ok, M, d, noise):
     x = synthetic.activations(M, d, seed=M + d)
     w = synthetic.norm_scale(d, seed=d)
     z = synthetic.noise(d, 1e-2, seed=d) if noise else None
-    h = pl.rmsnorm_aqn(x.to(DEV), w.to(DEV), z.to(DEV) if noise else None, synthetic.EPS)
+    args = (x.to(DEV), w.to(DEV), z.to(DEV) if noise else None, synthetic.EPS)
+    h = pl.rmsnorm_aqn(*args, out_dtype=torch.float32)
+    hb = pl.rmsnorm_aqn(*args)
+    assert_bf16_is_rounded_f32(hb, h, f"M={M} d={d}")
     ref = olin.rmsnorm_aqn(np32(x), np32(w), np32(z) if noise else None, synthetic.EPS)
     got = np32(h).astype(np.float64)
     rel = np.abs(got - ref) / np.maximum(np.abs(ref), 1e-30)
