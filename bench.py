@@ -192,6 +192,7 @@ def run_ours(args, world, rank, local):
     # CUDA graphs: one per copy set (= one step), and one "round" graph holding a
     # step on every copy set, so that the GPU runs far ahead of the host
     stream = torch.cuda.Stream(dev)
+    torch.cuda.set_stream(stream)  # every launch, replay and event below is on this stream
     graphs = []
     with torch.cuda.stream(stream):
         for calls in sets:  # warm (tensor-map encode, attribute set-up) outside capture

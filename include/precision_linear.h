@@ -133,7 +133,7 @@ pl_status pl_rmsnorm_aqn(const void* x_bf16, int64_t M, int64_t d,
  * Accumulation is FP32.  M <= 64 runs the decode path, larger M the prefill
  * path; both use tcgen05 tensor cores when d_i % 256 == 0 and a generic CUDA-core
  * kernel otherwise.  Requirements: M >= 1, d_o >= 1, d_i >= 16, d_i % 16 == 0,
- * 0 <= r <= 64; x, codes, scales, A, B, y 16-byte aligned. */
+ * 0 <= r <= 64; x, codes, scales, A, B, w_norm, z, y 16-byte aligned. */
 pl_status pl_nvfp4_lora_linear(const void* x_bf16, int64_t M, int64_t d_i, int64_t d_o,
                                const uint8_t* codes, const uint8_t* scales, const float* s_g,
                                const void* A_bf16, const void* B_bf16, int r, float lambda,

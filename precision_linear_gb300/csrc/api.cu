@@ -128,7 +128,7 @@ pl_status pl_nvfp4_lora_linear(const void* x, int64_t M, int64_t d_i, int64_t d_
   const bool lora = r > 0 && A != nullptr && B != nullptr;
   if (r > 0 && (A == nullptr) != (B == nullptr)) return PL_ERR_NULL;
   if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || !aligned16(y) ||
-      (lora && (!aligned16(A) || !aligned16(B))))
+      (lora && (!aligned16(A) || !aligned16(B))) || (w_norm && !aligned16(w_norm)) || (z && !aligned16(z)))
     return PL_ERR_ALIGN;
   const size_t need = pl_workspace_bytes(M, d_i, d_o, r);
   if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))

@@ -45,6 +45,18 @@ namespace pl {
 
 __device__ uint32_t g_tc_status = 0;
 
+// Phase timestamps for development builds (-DPL_TIMELINE); compiled out otherwise.
+#ifdef PL_TIMELINE
+__device__ unsigned long long g_tl_main[1024][16];
+__device__ unsigned long long g_tl_pro[256][8];
+#define PL_TL(slot) do { if (blockIdx.x < 1024) g_tl_main[blockIdx.x][slot] = globaltimer_ns(); } while (0)
+#define PL_TLP(slot) do { const unsigned b_ = blockIdx.x + gridDim.x * blockIdx.y; \
+                          if (b_ < 256) g_tl_pro[b_][slot] = globaltimer_ns(); } while (0)
+#else
+#define PL_TL(slot) do { } while (0)
+#define PL_TLP(slot) do { } while (0)
+#endif
+
 namespace {
 
 constexpr int kTileO = 128;
@@ -74,8 +86,6 @@ struct TcParams {
   const __nv_bfloat16* Blora;
   void* y;
   int y_f32;
-  float* partial;
-  uint32_t* counters;
 };
 
 struct TcMaps {
@@ -116,6 +126,19 @@ PL_DEVINL void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
 PL_DEVINL void named_bar(uint32_t id, uint32_t n) {
   asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(n) : "memory");
 }
+PL_DEVINL void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+PL_DEVINL uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+PL_DEVINL float ld_dsmem_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
 // Named barrier that also ANDs a predicate over the participating threads.
 PL_DEVINL bool named_bar_and(uint32_t id, uint32_t n, bool pred) {
   uint32_t r;
@@ -131,7 +154,7 @@ struct Smem {
   uint64_t d_full, tq_full, a2_full, drain;
   uint32_t tmem_base;
   int abort_flag;
-  int is_last;
+  float rowscale[kMaxN];
 };
 
 // Wait that also gives up when another role of the CTA has already given up.
@@ -168,96 +191,180 @@ __global__ void k_wait_timeout_probe(uint64_t limit_ns) {
 // ------------------------------------------------------------------ prologue
 constexpr int kProThreads = 256;
 
+// One CTA per (group of TM token rows, group of 8 adapter rows).  Pass 1 reads x,
+// w_norm and z with 16-byte loads, keeps hz = x (.) (w + z) in shared memory and
+// reduces sum(x^2) and max|hz| per row; then h = hz / rms, the power-of-two row
+// scale c_m, the f16 activations h / c_m (written by the CTAs of adapter group 0)
+// and the LoRA down-projection of this CTA's 8 adapter rows, A is read once per
+// TM tokens.
+template <int TM>
 __global__ void __launch_bounds__(kProThreads) k_tc_prologue(
-    const __nv_bfloat16* __restrict__ x, int64_t d_i, const float* __restrict__ w_norm,
+    const __nv_bfloat16* __restrict__ x, int64_t M, int64_t d_i, const float* __restrict__ w_norm,
     const float* __restrict__ z, float eps, const __nv_bfloat16* __restrict__ A, int r, float lambda,
-    __half* __restrict__ hq, float* __restrict__ rowscale, __nv_bfloat16* __restrict__ tq,
-    uint32_t* __restrict__ counters, int n_counters) {
-  if (threadIdx.x == 0) pdl_launch_dependents();
+    __half* __restrict__ hq, float* __restrict__ rowscale, __nv_bfloat16* __restrict__ tq) {
+  extern __shared__ float4 hz4[];  // [TM][d_i / 4]
+  __shared__ float red[kProThreads / 32][8 * TM];
+  __shared__ float s_inv[TM], s_c[TM];
+  if (threadIdx.x == 0) {
+    PL_TLP(0);
+    pdl_launch_dependents();
+  }
   pdl_wait();  // the previous call may still read this workspace
-  __shared__ float red_s[kProThreads / 32], red_m[kProThreads / 32];
-  __shared__ float red_t[8][kProThreads / 32];
-  const int64_t m = blockIdx.x;
-  const int jb = blockIdx.y;
-  const __nv_bfloat16* xr = x + m * d_i;
-  const bool norm = w_norm != nullptr;
-  auto scale_at = [&](int64_t k) -> float {
-    return norm ? (w_norm[k] + (z != nullptr ? z[k] : 0.f)) : 1.0f;
-  };
-  // pass 1: sum of squares of x, max |x (w+z)|
-  float ss = 0.f, mx = 0.f;
-  for (int64_t k = threadIdx.x; k < d_i; k += kProThreads) {
-    const float v = __bfloat162float(xr[k]);
-    ss = fmaf(v, v, ss);
-    mx = fmaxf(mx, fabsf(v * scale_at(k)));
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
-    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-  }
+  if (threadIdx.x == 0) PL_TLP(1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) {
-    red_s[warp] = ss;
-    red_m[warp] = mx;
+  const int64_t m0 = static_cast<int64_t>(blockIdx.x) * TM;
+  const int tm = static_cast<int>(M - m0 < TM ? M - m0 : TM);
+  const int jb = blockIdx.y;
+  const int64_t nslot = d_i / 8;  // 8 elements per slot
+  const bool norm = w_norm != nullptr;
+  float ss[TM], mx[TM];
+#pragma unroll
+  for (int t = 0; t < TM; ++t) ss[t] = mx[t] = 0.f;
+  for (int64_t sl = threadIdx.x; sl < nslot; sl += kProThreads) {
+    float sc[8];
+    if (norm) {
+      const float4 w0 = reinterpret_cast<const float4*>(w_norm)[2 * sl];
+      const float4 w1 = reinterpret_cast<const float4*>(w_norm)[2 * sl + 1];
+      sc[0] = w0.x; sc[1] = w0.y; sc[2] = w0.z; sc[3] = w0.w;
+      sc[4] = w1.x; sc[5] = w1.y; sc[6] = w1.z; sc[7] = w1.w;
+      if (z != nullptr) {
+        const float4 z0 = reinterpret_cast<const float4*>(z)[2 * sl];
+        const float4 z1 = reinterpret_cast<const float4*>(z)[2 * sl + 1];
+        sc[0] += z0.x; sc[1] += z0.y; sc[2] += z0.z; sc[3] += z0.w;
+        sc[4] += z1.x; sc[5] += z1.y; sc[6] += z1.z; sc[7] += z1.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sc[i] = 1.0f;
+    }
+#pragma unroll
+    for (int t = 0; t < TM; ++t) {
+      if (t < tm) {
+        const uint4 v = reinterpret_cast<const uint4*>(x + (m0 + t) * d_i)[sl];
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+        float h[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float a0 = bf16lo_to_f32(u[j]), a1 = bf16hi_to_f32(u[j]);
+          ss[t] = fmaf(a0, a0, ss[t]);
+          ss[t] = fmaf(a1, a1, ss[t]);
+          h[2 * j] = a0 * sc[2 * j];
+          h[2 * j + 1] = a1 * sc[2 * j + 1];
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[t] = fmaxf(mx[t], fabsf(h[i]));
+        hz4[t * (d_i / 4) + 2 * sl] = make_float4(h[0], h[1], h[2], h[3]);
+        hz4[t * (d_i / 4) + 2 * sl + 1] = make_float4(h[4], h[5], h[6], h[7]);
+      }
+    }
+  }
+  if (threadIdx.x == 0) PL_TLP(2);
+#pragma unroll
+  for (int t = 0; t < TM; ++t) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      ss[t] += __shfl_xor_sync(0xFFFFFFFFu, ss[t], o);
+      mx[t] = fmaxf(mx[t], __shfl_xor_sync(0xFFFFFFFFu, mx[t], o));
+    }
+    if (lane == 0) {
+      red[warp][t] = ss[t];
+      red[warp][TM + t] = mx[t];
+    }
   }
   __syncthreads();
-  float tot = 0.f, hmx = 0.f;
+  if (threadIdx.x < TM) {
+    const int t = threadIdx.x;
+    float tot = 0.f, hm = 0.f;
 #pragma unroll
-  for (int w = 0; w < kProThreads / 32; ++w) {
-    tot += red_s[w];
-    hmx = fmaxf(hmx, red_m[w]);
-  }
-  const float inv = norm ? 1.0f / sqrtf(tot / static_cast<float>(d_i) + eps) : 1.0f;
-  const float hmax = inv * hmx;
-  // c_m = 2^e with max|h| / c_m in [2^13, 2^14)
-  int e = hmax > 0.f ? ilogbf(hmax) - 13 : 0;
-  e = e < -100 ? -100 : (e > 100 ? 100 : e);
-  const float c = ldexpf(1.0f, e), cinv = ldexpf(1.0f, -e);
-  if (jb == 0) {
-    __half* hr = hq + m * d_i;
-    for (int64_t k = threadIdx.x; k < d_i; k += kProThreads) {
-      const float h = (__bfloat162float(xr[k]) * inv) * scale_at(k);
-      hr[k] = __float2half_rn(h * cinv);
+    for (int w = 0; w < kProThreads / 32; ++w) {
+      tot += red[w][t];
+      hm = fmaxf(hm, red[w][TM + t]);
     }
-    if (threadIdx.x == 0) rowscale[m] = c;
-    if (m == 0)
-      for (int i = threadIdx.x; i < n_counters; i += kProThreads) counters[i] = 0u;
+    const float inv = norm ? 1.0f / sqrtf(tot / static_cast<float>(d_i) + eps) : 1.0f;
+    const float hmax = inv * hm;
+    int e = hmax > 0.f ? ilogbf(hmax) - 13 : 0;  // max |h| / c_m in [2^13, 2^14)
+    e = e < -100 ? -100 : (e > 100 ? 100 : e);
+    s_inv[t] = inv;
+    s_c[t] = ldexpf(1.0f, e);
+    if (jb == 0 && t < tm) rowscale[m0 + t] = ldexpf(1.0f, e);
   }
-  // LoRA down-projection for adapter rows 8 jb .. 8 jb + 7
-  __nv_bfloat16* tr = tq + m * kRpad;
-  if (A == nullptr || r == 0) {
-    if (jb == 0)
-      for (int j = threadIdx.x; j < kRpad; j += kProThreads) tr[j] = __float2bfloat16_rn(0.f);
-    return;
-  }
-  float acc[8];
+  __syncthreads();
+  if (jb == 0) {
+    for (int64_t sl = threadIdx.x; sl < nslot; sl += kProThreads) {
 #pragma unroll
-  for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+      for (int t = 0; t < TM; ++t) {
+        if (t < tm) {
+          const float f = s_inv[t] / s_c[t];
+          const float4 h0 = hz4[t * (d_i / 4) + 2 * sl], h1 = hz4[t * (d_i / 4) + 2 * sl + 1];
+          const __half2 p0 = __floats2half2_rn(h0.x * f, h0.y * f), p1 = __floats2half2_rn(h0.z * f, h0.w * f);
+          const __half2 p2 = __floats2half2_rn(h1.x * f, h1.y * f), p3 = __floats2half2_rn(h1.z * f, h1.w * f);
+          uint4 o;
+          o.x = *reinterpret_cast<const uint32_t*>(&p0);
+          o.y = *reinterpret_cast<const uint32_t*>(&p1);
+          o.z = *reinterpret_cast<const uint32_t*>(&p2);
+          o.w = *reinterpret_cast<const uint32_t*>(&p3);
+          reinterpret_cast<uint4*>(hq + (m0 + t) * d_i)[sl] = o;
+        }
+      }
+    }
+    for (int i = threadIdx.x; i < TM * kRpad; i += kProThreads) {
+      const int t = i / kRpad, j = i % kRpad;
+      if (t < tm && j >= r) tq[(m0 + t) * kRpad + j] = __float2bfloat16_rn(0.f);
+    }
+  }
+  if (threadIdx.x == 0) PL_TLP(3);
+  if (A == nullptr || r == 0) return;
+  // LoRA down-projection t = A h for adapter rows j0 .. j0 + 7, FP32
   const int j0 = 8 * jb;
-  for (int64_t k = threadIdx.x; k < d_i; k += kProThreads) {
-    const float h = (__bfloat162float(xr[k]) * inv) * scale_at(k);
+  float acc[8][TM];
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+#pragma unroll
+    for (int t = 0; t < TM; ++t) acc[q][t] = 0.f;
+#pragma unroll 2
+  for (int64_t sl = threadIdx.x; sl < nslot; sl += kProThreads) {
+    uint4 av[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q)
-      if (j0 + q < r) acc[q] = fmaf(__bfloat162float(A[static_cast<int64_t>(j0 + q) * d_i + k]), h, acc[q]);
-  }
+      av[q] = (j0 + q < r) ? reinterpret_cast<const uint4*>(A + static_cast<int64_t>(j0 + q) * d_i)[sl]
+                           : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    float v = acc[q];
+    for (int t = 0; t < TM; ++t) {
+      const float4 h0 = hz4[t * (d_i / 4) + 2 * sl], h1 = hz4[t * (d_i / 4) + 2 * sl + 1];
+      const float hh[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    if (lane == 0) red_t[q][warp] = v;
+      for (int q = 0; q < 8; ++q) {
+        const uint32_t u[4] = {av[q].x, av[q].y, av[q].z, av[q].w};
+        float a = acc[q][t];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          a = fmaf(bf16lo_to_f32(u[j]), hh[2 * j], a);
+          a = fmaf(bf16hi_to_f32(u[j]), hh[2 * j + 1], a);
+        }
+        acc[q][t] = a;
+      }
+    }
   }
+  if (threadIdx.x == 0) PL_TLP(4);
+  __syncthreads();  // red[] is reused below
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+#pragma unroll
+    for (int t = 0; t < TM; ++t) {
+      float v = acc[q][t];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+      if (lane == 0) red[warp][q * TM + t] = v;
+    }
   __syncthreads();
-  if (threadIdx.x < 8) {
-    const int q = threadIdx.x;
+  if (threadIdx.x < 8 * TM) {
+    const int q = threadIdx.x / TM, t = threadIdx.x % TM;
     float v = 0.f;
 #pragma unroll
-    for (int w = 0; w < kProThreads / 32; ++w) v += red_t[q][w];
-    if (j0 + q < r) tr[j0 + q] = __float2bfloat16_rn(lambda * v);
+    for (int w = 0; w < kProThreads / 32; ++w) v += red[w][q * TM + t];
+    if (t < tm && j0 + q < r) tq[(m0 + t) * kRpad + j0 + q] = __float2bfloat16_rn(lambda * s_inv[t] * v);
   }
-  if (jb == 0)
-    for (int j = r + threadIdx.x; j < kRpad; j += kProThreads) tr[j] = __float2bfloat16_rn(0.f);
+  if (threadIdx.x == 0) PL_TLP(5);
 }
 
 // ------------------------------------------------------------------ main kernel
@@ -277,8 +384,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
   const int nch = c1 - c0;
   const bool has_lora = (split == 0) && p.r > 0;
   const uint32_t h_bytes = static_cast<uint32_t>(N) * 512u;
+  bool go = false;  // epilogue threads: this CTA's accumulators are valid
 
   if (threadIdx.x == 0) {
+    PL_TL(0);
     pdl_launch_dependents();
     for (int s = 0; s < stages; ++s) {
       mbar_init(smem_u32(&S.full[s]), 1);
@@ -307,6 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
+  if (threadIdx.x == 0) PL_TL(1);
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
@@ -323,7 +433,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
         tma_load_2d_hint(smem_u32(st), &maps.codes, kc * (kChunkK / 2), row0, fb, pol_w);
         tma_load_2d_hint(smem_u32(st + kCodesBytes + h_bytes), &maps.scales, kc * (kChunkK / 16), row0, fb, pol_w);
       }
+      PL_TL(2);
       pdl_wait();  // activations come from the prologue
+      PL_TL(3);
       for (int c = 0; c < pre; ++c) {
         uint8_t* st = smem + static_cast<size_t>(c) * p.stage_bytes;
         const uint32_t fb = smem_u32(&S.full[c]);
@@ -392,6 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
                    kk > 0 ? 1u : 0u);
         }
       }
+      PL_TL(6);
       tc_commit(smem_u32(&S.d_full));  // also reached on abort: tracks every MMA issued
     }
   } else {
@@ -428,6 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
       ok = wait_or_abort(smem_u32(&S.full[s]), (c / stages) & 1, abort_flag) &&
            (c < 2 || wait_or_abort(smem_u32(&S.a_empty[b]), ((c >> 1) - 1) & 1, abort_flag));
       if (!ok) break;
+      if (c == 0 && threadIdx.x == 64) PL_TL(4);
       const uint8_t* st = smem + static_cast<size_t>(s) * p.stage_bytes;
       const uint8_t* crow = st + row * 128;
       const uint2 sc8 = *reinterpret_cast<const uint2*>(st + kCodesBytes + h_bytes + row * 16 + g * 8);
@@ -458,17 +572,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
         mbar_arrive(smem_u32(&S.empty[s]));
       }
     }
+    if (threadIdx.x == 64) PL_TL(5);
     // ---------------------------------------------------------------- epilogue
     ok = wait_or_abort(smem_u32(&S.d_full), 0, abort_flag) && ok;
+    if (threadIdx.x == 64) PL_TL(7);
     tc_fence_after();
-    pdl_wait();  // row scales, counters and partials belong to this call's prologue
-    // one decision for all epilogue threads (they meet at named barriers below)
-    if (named_bar_and(1, kDeqWarps * 32, ok && !*abort_flag)) {
+    pdl_wait();  // the row scales belong to this call's prologue
+    const int et = threadIdx.x - 64;  // 0 .. 255
+    if (et < N) S.rowscale[et] = et < p.M ? p.rowscale[et] : 0.f;
+    // one decision for all epilogue threads (also publishes the row scales)
+    go = named_bar_and(1, kDeqWarps * 32, ok && !*abort_flag);
+    if (threadIdx.x == 64) PL_TL(8);
+    if (go) {
       const float s_g = *p.s_g;
       const int half = N / 2;
       const int n0 = g * half;
-      float* part = p.partial + (static_cast<size_t>(tile) * p.splits + split) * (static_cast<size_t>(N) * kTileO);
-      float vals[kMaxN / 2];
+      float* red = reinterpret_cast<float*>(smem);  // [N][128] partial, reuses stage 0
       for (int cb = 0; cb < half; cb += 8) {
         uint32_t d1[8], d2[8];
         tmem_ld8(tmem + lane_addr + kColD1 + n0 + cb, d1);
@@ -477,52 +596,55 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int n = n0 + cb + i;
-          const float cs = n < p.M ? p.rowscale[n] : 0.f;
-          float v = s_g * cs * __uint_as_float(d1[i]);
+          float v = s_g * S.rowscale[n] * __uint_as_float(d1[i]);
           if (has_lora) v += __uint_as_float(d2[i]);
-          vals[cb + i] = v;
-        }
-      }
-      if (p.splits == 1) {
-        if (o < p.d_o)
-          for (int i = 0; i < half; ++i) {
-            const int n = n0 + i;
-            if (n < p.M) {
-              if (p.y_f32) static_cast<float*>(p.y)[n * p.d_o + o] = vals[i];
-              else static_cast<__nv_bfloat16*>(p.y)[n * p.d_o + o] = __float2bfloat16_rn(vals[i]);
-            }
-          }
-      } else {
-        for (int i = 0; i < half; ++i) part[(n0 + i) * kTileO + row] = vals[i];
-        __threadfence();
-        named_bar(1, kDeqWarps * 32);
-        if (threadIdx.x == 64) {
-          const uint32_t prev = atomicAdd(&p.counters[tile], 1u);
-          S.is_last = (prev == static_cast<uint32_t>(p.splits - 1)) ? 1 : 0;
-        }
-        named_bar(1, kDeqWarps * 32);
-        if (S.is_last) {
-          __threadfence();
-          const float* base = p.partial + static_cast<size_t>(tile) * p.splits * (static_cast<size_t>(N) * kTileO);
-          for (int i = 0; i < half; ++i) {
-            const int n = n0 + i;
-            float acc = 0.f;
-            for (int sp = 0; sp < p.splits; ++sp)
-              acc += (sp == split) ? vals[i] : __ldcg(base + (static_cast<size_t>(sp) * N + n) * kTileO + row);
+          if (p.splits == 1) {
             if (n < p.M && o < p.d_o) {
-              if (p.y_f32) static_cast<float*>(p.y)[n * p.d_o + o] = acc;
-              else static_cast<__nv_bfloat16*>(p.y)[n * p.d_o + o] = __float2bfloat16_rn(acc);
+              if (p.y_f32) static_cast<float*>(p.y)[n * p.d_o + o] = v;
+              else static_cast<__nv_bfloat16*>(p.y)[n * p.d_o + o] = __float2bfloat16_rn(v);
             }
+          } else {
+            red[n * kTileO + row] = v;
           }
         }
       }
     }
   }
+  if (threadIdx.x == 64) PL_TL(9);
   tc_fence_before();
   __syncthreads();
+  if (p.splits > 1) {
+    // K splits of one tile form a cluster: after every CTA has its FP32 partial in
+    // shared memory, CTA `split` sums rows [r0, r1) of all partials over DSMEM in
+    // split order (deterministic) and writes them.
+    cluster_sync();
+    if (threadIdx.x == 0) PL_TL(10);
+    if (threadIdx.x >= 64 && go) {
+      const int et = threadIdx.x - 64;
+      const int r0 = (split * kTileO) / p.splits, r1 = ((split + 1) * kTileO) / p.splits;
+      const int nr = r1 - r0;
+      const int mt = static_cast<int>(p.M < N ? p.M : N);
+      const uint32_t red_addr = smem_u32(smem);
+      for (int e = et; e < nr * mt; e += kDeqWarps * 32) {
+        const int n = e / nr, rr = r0 + e % nr;
+        const int64_t oo = static_cast<int64_t>(tile) * kTileO + rr;
+        const uint32_t off = static_cast<uint32_t>((n * kTileO + rr) * 4);
+        float acc = 0.f;
+        for (int sp = 0; sp < p.splits; ++sp) acc += ld_dsmem_f32(mapa_shared(red_addr + off, sp));
+        if (oo < p.d_o) {
+          if (p.y_f32) static_cast<float*>(p.y)[n * p.d_o + oo] = acc;
+          else static_cast<__nv_bfloat16*>(p.y)[n * p.d_o + oo] = __float2bfloat16_rn(acc);
+        }
+      }
+    }
+    if (threadIdx.x == 64) PL_TL(11);
+    cluster_sync();  // peers keep their shared memory until every reader is done
+    if (threadIdx.x == 0) PL_TL(12);
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+    if (lane == 0) PL_TL(13);
   }
 }
 
@@ -554,28 +676,95 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void*
 }
 
 struct Plan {
-  int N, tiles, kc, splits, stages;
+  int N, tiles, kc, splits, stages, tm;
   uint32_t stage_bytes;
-  size_t smem;
+  size_t smem, pro_smem;
 };
 
-Plan make_plan(int64_t M, int64_t d_i, int64_t d_o, int sms) {
+uint32_t stage_bytes_for(int N) { return kCodesBytes + kScaleBytes + static_cast<uint32_t>(N) * 512u; }
+
+int stages_for(uint32_t stage_bytes) {
+  int st = static_cast<int>((200u * 1024u) / stage_bytes);
+  return st > kMaxStages ? kMaxStages : (st < 2 ? 2 : st);
+}
+
+size_t smem_for(int N) {
+  const uint32_t sb = stage_bytes_for(N);
+  return 1024 + static_cast<size_t>(stages_for(sb)) * sb + static_cast<size_t>(N) * 128 + sizeof(Smem);
+}
+
+cudaError_t set_kernel_attributes() {
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    err = cudaFuncSetAttribute(k_tc_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(k_tc_prologue<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(k_tc_prologue<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(k_tc_prologue<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  });
+  return err;
+}
+
+// Clusters of `cs` decode CTAs that can be resident at once (cached per N class).
+int max_active_clusters(int N, int cs) {
+  static int cache[kMaxN / 16 + 1][kMaxSplit + 1];
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  int& c = cache[N / 16][cs];
+  if (c == 0) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(cs * 64));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem_for(N);
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = static_cast<unsigned>(cs);
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k_tc_decode, &cfg) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = sm_count() / cs;
+    }
+    c = n < 1 ? 1 : n;
+  }
+  return c;
+}
+
+// Split count: minimise (waves) x (chunks per CTA + fixed per-CTA cost), the fixed
+// cost counted as 1.5 chunks; ties go to fewer splits.
+int choose_splits(int N, int tiles, int kc, bool query) {
+  int best = 1;
+  double best_cost = 1e30;
+  for (int s = 1; s <= kMaxSplit && s <= kc; ++s) {
+    const int clusters = query ? max_active_clusters(N, s) : 1024;
+    const int waves = (tiles + clusters - 1) / clusters;
+    const double cost = waves * (static_cast<double>((kc + s - 1) / s) + 1.5);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
+Plan make_plan(int64_t M, int64_t d_i, int64_t d_o, bool query) {
   Plan pl{};
   pl.N = static_cast<int>((M + 15) / 16 * 16);
   pl.tiles = static_cast<int>((d_o + kTileO - 1) / kTileO);
   pl.kc = static_cast<int>(d_i / kChunkK);
-  int s = sms / pl.tiles;
-  s = s < 1 ? 1 : s;
-  s = s > kMaxSplit ? kMaxSplit : s;
-  s = s > pl.kc ? pl.kc : s;
-  pl.splits = s;
-  pl.stage_bytes = kCodesBytes + kScaleBytes + static_cast<uint32_t>(pl.N) * 512u;
-  const size_t budget = 200 * 1024;
-  int st = static_cast<int>(budget / pl.stage_bytes);
-  st = st > kMaxStages ? kMaxStages : st;
-  st = st < 2 ? 2 : st;
-  pl.stages = st;
-  pl.smem = 1024 + static_cast<size_t>(st) * pl.stage_bytes + static_cast<size_t>(pl.N) * 128 + sizeof(Smem);
+  pl.splits = choose_splits(pl.N, pl.tiles, pl.kc, query);
+  pl.stage_bytes = stage_bytes_for(pl.N);
+  pl.stages = stages_for(pl.stage_bytes);
+  pl.smem = smem_for(pl.N);
+  const int64_t tm = (160 * 1024) / (d_i * 4);
+  pl.tm = tm >= 4 ? 4 : (tm >= 2 ? 2 : 1);
+  pl.pro_smem = static_cast<size_t>(pl.tm) * d_i * 4;
   return pl;
 }
 
@@ -583,27 +772,37 @@ struct TcWs {
   __half* hq;
   float* rowscale;
   __nv_bfloat16* tq;
-  uint32_t* counters;
-  float* partial;
   size_t bytes;
 };
 
-TcWs carve(void* ws, int64_t M, int64_t d_i, const Plan& pl) {
+TcWs carve(void* ws, int64_t M, int64_t d_i) {
   TcWs w{};
+  const uintptr_t b = reinterpret_cast<uintptr_t>(ws);
   size_t off = 0;
-  char* b = static_cast<char*>(ws);
   w.hq = reinterpret_cast<__half*>(b + off);
   off += align_up(static_cast<size_t>(M) * d_i * 2, 256);
   w.rowscale = reinterpret_cast<float*>(b + off);
   off += align_up(static_cast<size_t>(M) * 4, 256);
   w.tq = reinterpret_cast<__nv_bfloat16*>(b + off);
   off += align_up(static_cast<size_t>(M) * kRpad * 2, 256);
-  w.counters = reinterpret_cast<uint32_t*>(b + off);
-  off += align_up(static_cast<size_t>(pl.tiles) * 4, 256);
-  w.partial = reinterpret_cast<float*>(b + off);
-  off += align_up(static_cast<size_t>(pl.tiles) * kMaxSplit * pl.N * kTileO * 4, 256);
   w.bytes = off;
   return w;
+}
+
+template <int TM>
+cudaError_t launch_prologue(const LinearArgs& a, const Plan& pl, const TcWs& w, cudaStream_t stream,
+                            cudaLaunchAttribute* pdl) {
+  const int ny = a.r > 0 ? (a.r + 7) / 8 : 1;
+  cudaLaunchConfig_t c{};
+  c.gridDim = dim3(static_cast<unsigned>((a.M + TM - 1) / TM), static_cast<unsigned>(ny));
+  c.blockDim = dim3(kProThreads);
+  c.dynamicSmemBytes = pl.pro_smem;
+  c.stream = stream;
+  c.attrs = pdl;
+  c.numAttrs = 1;
+  return cudaLaunchKernelEx(&c, k_tc_prologue<TM>, static_cast<const __nv_bfloat16*>(a.x), a.M, a.d_i, a.w_norm,
+                            a.z, a.eps, static_cast<const __nv_bfloat16*>(a.A), a.r, a.lambda, w.hq, w.rowscale,
+                            w.tq);
 }
 
 }  // namespace
@@ -612,14 +811,13 @@ bool tc_supported(int64_t M, int64_t d_i, int64_t, int r) {
   return M >= 1 && M <= kMaxN && d_i >= kChunkK && d_i % kChunkK == 0 && r >= 0 && r <= kRpad;
 }
 
-size_t tc_workspace_bytes(int64_t M, int64_t d_i, int64_t d_o, int) {
-  Plan pl = make_plan(M, d_i, d_o, kMaxSplit * 1024);
-  return carve(nullptr, M, d_i, pl).bytes;
-}
+size_t tc_workspace_bytes(int64_t M, int64_t d_i, int64_t, int) { return carve(nullptr, M, d_i).bytes; }
 
 cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
-  const Plan pl = make_plan(a.M, a.d_i, a.d_o, sm_count());
-  TcWs w = carve(a.ws, a.M, a.d_i, pl);
+  cudaError_t e = set_kernel_attributes();
+  if (e != cudaSuccess) return e;
+  const Plan pl = make_plan(a.M, a.d_i, a.d_o, true);
+  const TcWs w = carve(a.ws, a.M, a.d_i);
   TcMaps maps;
   bool ok = encode_2d(&maps.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.codes, a.d_i / 2, a.d_o, 128, kTileO,
                       CU_TENSOR_MAP_SWIZZLE_128B) &&
@@ -631,27 +829,16 @@ cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
                       CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
 
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(k_tc_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-  });
-  if (attr_err != cudaSuccess) return attr_err;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  attrs[1].id = cudaLaunchAttributeClusterDimension;
+  attrs[1].val.clusterDim.x = static_cast<unsigned>(pl.splits);
+  attrs[1].val.clusterDim.y = 1;
+  attrs[1].val.clusterDim.z = 1;
 
-  cudaLaunchAttribute pdl[1];
-  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  pdl[0].val.programmaticStreamSerializationAllowed = 1;
-
-  const int ny = a.r > 0 ? (a.r + 7) / 8 : 1;
-  cudaLaunchConfig_t c1{};
-  c1.gridDim = dim3(static_cast<unsigned>(a.M), static_cast<unsigned>(ny));
-  c1.blockDim = dim3(kProThreads);
-  c1.stream = stream;
-  c1.attrs = pdl;
-  c1.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&c1, k_tc_prologue, static_cast<const __nv_bfloat16*>(a.x), a.d_i, a.w_norm,
-                                     a.z, a.eps, static_cast<const __nv_bfloat16*>(a.A), a.r, a.lambda, w.hq,
-                                     w.rowscale, w.tq, w.counters, pl.tiles);
+  e = pl.tm == 4 ? launch_prologue<4>(a, pl, w, stream, attrs)
+                 : (pl.tm == 2 ? launch_prologue<2>(a, pl, w, stream, attrs) : launch_prologue<1>(a, pl, w, stream, attrs));
   if (e != cudaSuccess) return e;
 
   TcParams p{};
@@ -671,16 +858,14 @@ cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   p.Blora = static_cast<const __nv_bfloat16*>(a.B);
   p.y = a.y;
   p.y_f32 = a.y_f32 ? 1 : 0;
-  p.partial = w.partial;
-  p.counters = w.counters;
 
   cudaLaunchConfig_t c2{};
   c2.gridDim = dim3(static_cast<unsigned>(pl.tiles * pl.splits));
   c2.blockDim = dim3(kThreads);
   c2.dynamicSmemBytes = pl.smem;
   c2.stream = stream;
-  c2.attrs = pdl;
-  c2.numAttrs = 1;
+  c2.attrs = attrs;
+  c2.numAttrs = pl.splits > 1 ? 2 : 1;
   return cudaLaunchKernelEx(&c2, k_tc_decode, maps, p);
 }
 
@@ -688,6 +873,15 @@ cudaError_t launch_wait_timeout_probe(cudaStream_t stream) {
   k_wait_timeout_probe<<<1, 32, 0, stream>>>(2ull * 1000 * 1000);  // 2 ms
   return cudaGetLastError();
 }
+
+#ifdef PL_TIMELINE
+extern "C" int pl_debug_read_timeline(unsigned long long* main_out, unsigned long long* pro_out) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return 1;
+  if (cudaMemcpyFromSymbol(main_out, g_tl_main, sizeof(g_tl_main)) != cudaSuccess) return 2;
+  if (cudaMemcpyFromSymbol(pro_out, g_tl_pro, sizeof(g_tl_pro)) != cudaSuccess) return 3;
+  return 0;
+}
+#endif
 
 uint32_t tc_read_and_clear_status() {
   uint32_t v = 0, zero = 0;
