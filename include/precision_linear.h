@@ -141,6 +141,36 @@ pl_status pl_nvfp4_lora_linear(const void* x_bf16, int64_t M, int64_t d_i, int64
                                void* y, int y_dtype, void* workspace, size_t workspace_bytes,
                                pl_stream_t stream);
 
+/* Bytes of the scratch array behind pl_nvfp4_lora_linear_static_ws. */
+#define PL_STATIC_WORKSPACE_BYTES ((size_t)8 << 20)
+
+/* pl_nvfp4_lora_linear without a caller-provided workspace.  (No counterpart in
+ * the pages: it is an interface convenience, not part of the method.)
+ *
+ * For callers that cannot allocate device memory themselves -- for example a
+ * plug-in that receives only raw input and output pointers from a host program
+ * owning every allocation, or a serving loop that must not call cudaMalloc because
+ * it synchronises the device and the caching allocator is out of reach.  The
+ * caller still passes all inputs and the output; the scratch the call needs lives
+ * in one library-owned device array of PL_STATIC_WORKSPACE_BYTES (8 MiB) that
+ * every device loading this library keeps until the process exits.
+ *
+ * Arguments, layouts, arithmetic and status codes are those of
+ * pl_nvfp4_lora_linear; additionally PL_ERR_WORKSPACE is returned, with nothing
+ * launched, when pl_workspace_bytes(M, d_i, d_o, r) exceeds
+ * PL_STATIC_WORKSPACE_BYTES (e.g. M = 64 decode fits for d_i up to 28672).
+ * The call allocates nothing.  Its first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  All calls share the one array and it keeps the
+ * last call's contents (nothing in it needs to start at zero): calls that may
+ * overlap on the GPU -- on different streams, or concurrently from several host
+ * threads -- race on it and must be serialised by the caller. */
+pl_status pl_nvfp4_lora_linear_static_ws(const void* x_bf16, int64_t M, int64_t d_i, int64_t d_o,
+                                         const uint8_t* codes, const uint8_t* scales, const float* s_g,
+                                         const void* A_bf16, const void* B_bf16, int r, float lambda,
+                                         const float* w_norm, const float* z, float eps,
+                                         void* y, int y_dtype, pl_stream_t stream);
+
 /* Synchronises `stream`, then returns and clears the device status word that
  * bounded device-side waits set when they give up (PL_ERR_TIMEOUT), or PL_OK. */
 pl_status pl_last_device_status(pl_stream_t stream);
