@@ -5,32 +5,32 @@
 // on the section 3.1 NVFP4 backbone (w_hat = s_g s_b q) with the section 5.1
 // RMSNorm-AQN input h = u (.) (w_norm + z).
 //
-// Orientation ("swap AB"): the 128 weight rows of a tile are the MMA's M dimension,
-// the (padded) tokens its N dimension, d_i its K dimension.  Per CTA and K chunk of
-// 256:
-//   * warp 0 (one lane) TMA-loads the chunk's packed codes (128 rows x 128 B,
-//     128-byte swizzle), its E4M3 scales (128 x 16 B) and the activations
-//     (N rows x 256 halves, 128-byte swizzle, canonical K-major layout);
-//   * warps 2..9 dequantise: each thread owns one weight row and half the chunk,
-//     turns 8 codes per 32-bit word into 4 f16x2 words with the hardware E2M1
-//     conversion, multiplies by the block scale (q * s_b is exact in f16), and
-//     stores them into tensor memory, where they are the MMA's A operand;
-//   * warp 1 (one lane) issues 16 tcgen05.mma kind::f16 (K = 16 each) with A from
-//     tensor memory and B from the swizzled shared tile, FP32 accumulator D1 in
-//     tensor memory; the CTA holding the tile's first K split also issues the LoRA
-//     up-projection D2 = B_lora (bf16, in tensor memory) x (lambda t)^T (bf16 tile).
-// Epilogue (warps 2..9): tcgen05.ld the accumulators, y = s_g c_m D1 + D2.  When a
-// tile's K range is split across CTAs, each writes its FP32 partial to the
-// workspace and the last CTA to arrive (atomic counter, no waiting) sums the
-// partials in split order -- deterministic.
+// Two kernels per call, chained by programmatic dependent launch:
 //
-// The activations are prepared by k_tc_prologue: per token row it forms the
-// RMSNorm-AQN h in FP32, picks a power-of-two c_m that brings max|h| to [2^13, 2^14),
-// stores h / c_m as f16 (11-bit significand; no overflow), and computes the LoRA
-// down-projection t = A h in FP32, stored as bf16(lambda t).  Both kernels use
-// programmatic dependent launch: the main kernel starts streaming weights while
-// the prologue runs and waits (griddepcontrol.wait) only before it reads the
-// prologue's outputs; the prologue waits before it overwrites the workspace.
+// k_act (one CTA per token row): h = x / rms (.) (w_norm + z) in FP32, a power-of-two
+//   c_m with max|h| / c_m in [2^13, 2^14), and the f16 activations h / c_m (11-bit
+//   significand, no overflow) into the workspace; a few more CTAs copy the LoRA matrix
+//   A into the workspace as f16.
+//
+// k_tc_decode (a cluster of S CTAs per 128 weight rows; CTA s takes the s-th slice of
+//   the K = d_i axis in chunks of 256):
+//   * warp 0 TMA-loads, per chunk, the packed codes (128 rows x 128 B, 128-byte
+//     swizzle) and E4M3 scales (128 x 16 B) -- issued before the wait on k_act, they
+//     do not depend on it -- the f16 activations (N rows x 256, 128-byte swizzle:
+//     the canonical K-major layout) and the chunk of the f16 copy of A (r x 256);
+//   * warps 2..9 dequantise: each thread owns one weight row and half the chunk, turns
+//     8 codes per 32-bit word into 4 f16x2 words with the hardware E2M1 conversion,
+//     multiplies by the block scale (q * s_b is exact in f16) and stores them into
+//     tensor memory, where they are the MMA's A operand;
+//   * warp 1 issues tcgen05.mma kind::f16 (K = 16 each): weights (tensor memory) x
+//     activations^T into accumulator D1, and A (shared memory, 128-row operand whose
+//     rows >= r are don't-care) x activations^T into accumulator Dt, whose lanes < r are
+//     this CTA's K slice of t = A h;
+//   * epilogue (warps 2..9): every CTA puts s_g c_m D1 and its Dt slice in shared
+//     memory; after a cluster barrier CTA s sums, over DSMEM and in split order
+//     (deterministic), the t slices of all S CTAs into t, and the D1 partials of its
+//     share of the 128 rows; it adds the LoRA up-projection lambda B t on CUDA cores
+//     and writes y.
 //
 // Every mbarrier wait is bounded (200 ms); a wait that gives up sets the device
 // status word, the CTA drains its own copies and MMAs (again bounded), frees its
@@ -61,24 +61,25 @@ namespace {
 
 constexpr int kTileO = 128;
 constexpr int kChunkK = 256;
-constexpr int kCodesBytes = kTileO * kChunkK / 2;     // 16 KB
-constexpr int kScaleBytes = kTileO * kChunkK / 16;    // 2 KB
-constexpr int kThreads = 320;
+constexpr int kCodesBytes = kTileO * kChunkK / 2;   // 16 KB
+constexpr int kScaleBytes = kTileO * kChunkK / 16;  // 2 KB
 constexpr int kDeqWarps = 8;
-constexpr int kMaxStages = 12;
+constexpr int kThreads = 10 * 32;  // producer, MMA, 8 dequant/epilogue warps
+constexpr int kEpiThreads = kDeqWarps * 32;
+constexpr int kMaxStages = 8;
 constexpr int kMaxSplit = 8;
 constexpr int kMaxN = 64;
-constexpr int kRpad = 64;  // tq row: 64 bf16 (128 B), zero beyond r
+constexpr int kMaxR = 64;
 constexpr uint32_t kTmemCols = 512;
-// tensor-memory column map
-constexpr uint32_t kColA0 = 0;  // A buffer b at kColA0 + 128 b
+// tensor-memory columns: A buffers [0,128) and [128,256), D1 [256,256+N), Dt [320,320+N)
+constexpr uint32_t kColA0 = 0;
 constexpr uint32_t kColD1 = 256;
-constexpr uint32_t kColD2 = 320;
-constexpr uint32_t kColA2 = 384;
+constexpr uint32_t kColDt = 320;
+constexpr int kTStride = kMaxR + 4;  // floats per token row of the t buffers (16-byte rows, spread banks)
 
 struct TcParams {
   int64_t M, d_i, d_o;
-  int N, r, tiles, splits, kc, stages;
+  int N, r, rb, tiles, splits, kc, stages;
   uint32_t stage_bytes;
   float lambda;
   const float* s_g;
@@ -89,7 +90,18 @@ struct TcParams {
 };
 
 struct TcMaps {
-  CUtensorMap codes, scales, hq, tq;
+  CUtensorMap codes, scales, hq, alora;
+};
+
+struct Smem {
+  uint64_t wfull[kMaxStages], hfull[kMaxStages], empty[kMaxStages];
+  uint64_t a_full[2], a_empty[2];
+  uint64_t lfull[2], lempty[2];  // shared-memory ring of A chunks
+  uint64_t d_full;
+  uint32_t tmem_base;
+  int abort_flag;
+  float s_g;
+  float rowscale[kMaxN];
 };
 
 // ------------------------------------------------------------------ small helpers
@@ -103,6 +115,12 @@ PL_DEVINL uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
   return r;
 }
+// Two FP32 -> f16x2, `lo` into the low half.
+PL_DEVINL uint32_t f32x2_to_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 // 8 E2M1 codes (one 32-bit word, code k in nibble k) -> 4 f16x2 (codes 2p, 2p+1 in word p).
 PL_DEVINL void e2m1x8_to_f16x8(uint32_t w, uint32_t& o0, uint32_t& o1, uint32_t& o2, uint32_t& o3) {
   asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
@@ -110,7 +128,7 @@ PL_DEVINL void e2m1x8_to_f16x8(uint32_t w, uint32_t& o0, uint32_t& o1, uint32_t&
       "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
       : "=r"(o0), "=r"(o1), "=r"(o2), "=r"(o3) : "r"(w));
 }
-PL_DEVINL void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+PL_DEVINL void tmem_st16(uint32_t taddr, const uint32_t* v) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
       "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
@@ -118,26 +136,13 @@ PL_DEVINL void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
          "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
          "r"(v[15]) : "memory");
 }
-PL_DEVINL void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
+PL_DEVINL void tmem_ld8(uint32_t taddr, uint32_t* v) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
                  "=r"(v[7]) : "r"(taddr) : "memory");
 }
 PL_DEVINL void named_bar(uint32_t id, uint32_t n) {
   asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(n) : "memory");
-}
-PL_DEVINL void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-PL_DEVINL uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
-PL_DEVINL float ld_dsmem_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
 }
 // Named barrier that also ANDs a predicate over the participating threads.
 PL_DEVINL bool named_bar_and(uint32_t id, uint32_t n, bool pred) {
@@ -147,15 +152,20 @@ PL_DEVINL bool named_bar_and(uint32_t id, uint32_t n, bool pred) {
                : "=r"(r) : "r"(id), "r"(n), "r"(pred ? 1u : 0u) : "memory");
   return r != 0;
 }
-
-struct Smem {
-  uint64_t full[kMaxStages], empty[kMaxStages];
-  uint64_t a_full[2], a_empty[2];
-  uint64_t d_full, tq_full, a2_full, drain;
-  uint32_t tmem_base;
-  int abort_flag;
-  float rowscale[kMaxN];
-};
+PL_DEVINL void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+PL_DEVINL uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+PL_DEVINL float4 ld_dsmem_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
+  return v;
+}
 
 // Wait that also gives up when another role of the CTA has already given up.
 PL_DEVINL bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
@@ -173,6 +183,11 @@ PL_DEVINL bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_
     }
   }
 }
+// Bounded drain of one barrier phase (after an abort).
+PL_DEVINL void drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+}
 
 // Test probe of the bounded-wait path: waits on a barrier that nothing completes,
 // gives up after `limit_ns`, records the time-out in the status word and returns.
@@ -188,181 +203,122 @@ __global__ void k_wait_timeout_probe(uint64_t limit_ns) {
   }
 }
 
-// ------------------------------------------------------------------ prologue
-constexpr int kProThreads = 256;
+// ------------------------------------------------------------------ activation prologue
+constexpr int kActThreads = 256;
+constexpr int kActUnroll = 4;  // 16-byte slots per thread in flight
 
-// One CTA per (group of TM token rows, group of 8 adapter rows).  Pass 1 reads x,
-// w_norm and z with 16-byte loads, keeps hz = x (.) (w + z) in shared memory and
-// reduces sum(x^2) and max|hz| per row; then h = hz / rms, the power-of-two row
-// scale c_m, the f16 activations h / c_m (written by the CTAs of adapter group 0)
-// and the LoRA down-projection of this CTA's 8 adapter rows, A is read once per
-// TM tokens.
-template <int TM>
-__global__ void __launch_bounds__(kProThreads) k_tc_prologue(
-    const __nv_bfloat16* __restrict__ x, int64_t M, int64_t d_i, const float* __restrict__ w_norm,
-    const float* __restrict__ z, float eps, const __nv_bfloat16* __restrict__ A, int r, float lambda,
-    __half* __restrict__ hq, float* __restrict__ rowscale, __nv_bfloat16* __restrict__ tq) {
-  extern __shared__ float4 hz4[];  // [TM][d_i / 4]
-  __shared__ float red[kProThreads / 32][8 * TM];
-  __shared__ float s_inv[TM], s_c[TM];
+// CTAs 0 .. M-1: one token row m each.  hz = x (.) (w + z) is kept in shared memory
+// (FP32) while sum(x^2) and max |hz| are reduced; then hq = f16(hz * inv / c_m).
+// CTAs M and up: the f16 copy of A (r x d_i), 8 elements per thread and slot.
+__global__ void __launch_bounds__(kActThreads) k_act(const __nv_bfloat16* __restrict__ x, int64_t M, int64_t d_i,
+                                                     const float* __restrict__ w_norm,
+                                                     const float* __restrict__ z, float eps,
+                                                     __half* __restrict__ hq, float* __restrict__ rowscale,
+                                                     const __nv_bfloat16* __restrict__ A, int r,
+                                                     __half* __restrict__ A16) {
+  extern __shared__ float4 hz4[];  // [d_i / 4]
+  __shared__ float red_s[kActThreads / 32], red_m[kActThreads / 32];
   if (threadIdx.x == 0) {
     PL_TLP(0);
     pdl_launch_dependents();
   }
-  pdl_wait();  // the previous call may still read this workspace
+  pdl_wait();  // x may come from the preceding kernel, which may also still read the workspace
   if (threadIdx.x == 0) PL_TLP(1);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t m0 = static_cast<int64_t>(blockIdx.x) * TM;
-  const int tm = static_cast<int>(M - m0 < TM ? M - m0 : TM);
-  const int jb = blockIdx.y;
-  const int64_t nslot = d_i / 8;  // 8 elements per slot
-  const bool norm = w_norm != nullptr;
-  float ss[TM], mx[TM];
+  if (static_cast<int64_t>(blockIdx.x) >= M) {
+    const int64_t nslot = static_cast<int64_t>(r) * d_i / 8;
+    const int64_t stride = static_cast<int64_t>(gridDim.x - M) * kActThreads;
+    for (int64_t sl = (blockIdx.x - M) * kActThreads + threadIdx.x; sl < nslot; sl += stride) {
+      const uint4 v = reinterpret_cast<const uint4*>(A)[sl];
+      reinterpret_cast<uint4*>(A16)[sl] =
+          make_uint4(f32x2_to_f16x2(bf16lo_to_f32(v.x), bf16hi_to_f32(v.x)),
+                     f32x2_to_f16x2(bf16lo_to_f32(v.y), bf16hi_to_f32(v.y)),
+                     f32x2_to_f16x2(bf16lo_to_f32(v.z), bf16hi_to_f32(v.z)),
+                     f32x2_to_f16x2(bf16lo_to_f32(v.w), bf16hi_to_f32(v.w)));
+    }
+    return;
+  }
+  const int64_t m = blockIdx.x;
+  const int64_t nv8 = d_i / 8;
+  const bool norm = w_norm != nullptr, noise = norm && z != nullptr;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + m * d_i);
+  float ss = 0.f, mx = 0.f;
+  for (int64_t base = threadIdx.x; base < nv8; base += kActThreads * kActUnroll) {
+    uint4 xv[kActUnroll];
+    float4 wv[kActUnroll][2], zv[kActUnroll][2];
 #pragma unroll
-  for (int t = 0; t < TM; ++t) ss[t] = mx[t] = 0.f;
-  for (int64_t sl = threadIdx.x; sl < nslot; sl += kProThreads) {
-    float sc[8];
-    if (norm) {
-      const float4 w0 = reinterpret_cast<const float4*>(w_norm)[2 * sl];
-      const float4 w1 = reinterpret_cast<const float4*>(w_norm)[2 * sl + 1];
-      sc[0] = w0.x; sc[1] = w0.y; sc[2] = w0.z; sc[3] = w0.w;
-      sc[4] = w1.x; sc[5] = w1.y; sc[6] = w1.z; sc[7] = w1.w;
-      if (z != nullptr) {
-        const float4 z0 = reinterpret_cast<const float4*>(z)[2 * sl];
-        const float4 z1 = reinterpret_cast<const float4*>(z)[2 * sl + 1];
-        sc[0] += z0.x; sc[1] += z0.y; sc[2] += z0.z; sc[3] += z0.w;
-        sc[4] += z1.x; sc[5] += z1.y; sc[6] += z1.z; sc[7] += z1.w;
+    for (int u = 0; u < kActUnroll; ++u) {
+      const int64_t sl = base + u * kActThreads;
+      if (sl < nv8) {
+        xv[u] = xr[sl];
+        if (norm) {
+          wv[u][0] = reinterpret_cast<const float4*>(w_norm)[2 * sl];
+          wv[u][1] = reinterpret_cast<const float4*>(w_norm)[2 * sl + 1];
+        }
+        if (noise) {
+          zv[u][0] = reinterpret_cast<const float4*>(z)[2 * sl];
+          zv[u][1] = reinterpret_cast<const float4*>(z)[2 * sl + 1];
+        }
       }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) sc[i] = 1.0f;
     }
 #pragma unroll
-    for (int t = 0; t < TM; ++t) {
-      if (t < tm) {
-        const uint4 v = reinterpret_cast<const uint4*>(x + (m0 + t) * d_i)[sl];
-        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    for (int u = 0; u < kActUnroll; ++u) {
+      const int64_t sl = base + u * kActThreads;
+      if (sl < nv8) {
+        float sc[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
+        if (norm) {
+          sc[0] = wv[u][0].x; sc[1] = wv[u][0].y; sc[2] = wv[u][0].z; sc[3] = wv[u][0].w;
+          sc[4] = wv[u][1].x; sc[5] = wv[u][1].y; sc[6] = wv[u][1].z; sc[7] = wv[u][1].w;
+        }
+        if (noise) {
+          sc[0] += zv[u][0].x; sc[1] += zv[u][0].y; sc[2] += zv[u][0].z; sc[3] += zv[u][0].w;
+          sc[4] += zv[u][1].x; sc[5] += zv[u][1].y; sc[6] += zv[u][1].z; sc[7] += zv[u][1].w;
+        }
+        const uint32_t w4[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
         float h[8];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const float a0 = bf16lo_to_f32(u[j]), a1 = bf16hi_to_f32(u[j]);
-          ss[t] = fmaf(a0, a0, ss[t]);
-          ss[t] = fmaf(a1, a1, ss[t]);
+          const float a0 = bf16lo_to_f32(w4[j]), a1 = bf16hi_to_f32(w4[j]);
+          ss = fmaf(a0, a0, ss);
+          ss = fmaf(a1, a1, ss);
           h[2 * j] = a0 * sc[2 * j];
           h[2 * j + 1] = a1 * sc[2 * j + 1];
         }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx[t] = fmaxf(mx[t], fabsf(h[i]));
-        hz4[t * (d_i / 4) + 2 * sl] = make_float4(h[0], h[1], h[2], h[3]);
-        hz4[t * (d_i / 4) + 2 * sl + 1] = make_float4(h[4], h[5], h[6], h[7]);
+        for (int i = 0; i < 8; ++i) mx = fmaxf(mx, fabsf(h[i]));
+        hz4[2 * sl] = make_float4(h[0], h[1], h[2], h[3]);
+        hz4[2 * sl + 1] = make_float4(h[4], h[5], h[6], h[7]);
       }
     }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    red_s[warp] = ss;
+    red_m[warp] = mx;
+  }
+  __syncthreads();
+  float tot = 0.f, hm = 0.f;
+#pragma unroll
+  for (int w = 0; w < kActThreads / 32; ++w) {
+    tot += red_s[w];
+    hm = fmaxf(hm, red_m[w]);
   }
   if (threadIdx.x == 0) PL_TLP(2);
-#pragma unroll
-  for (int t = 0; t < TM; ++t) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      ss[t] += __shfl_xor_sync(0xFFFFFFFFu, ss[t], o);
-      mx[t] = fmaxf(mx[t], __shfl_xor_sync(0xFFFFFFFFu, mx[t], o));
-    }
-    if (lane == 0) {
-      red[warp][t] = ss[t];
-      red[warp][TM + t] = mx[t];
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x < TM) {
-    const int t = threadIdx.x;
-    float tot = 0.f, hm = 0.f;
-#pragma unroll
-    for (int w = 0; w < kProThreads / 32; ++w) {
-      tot += red[w][t];
-      hm = fmaxf(hm, red[w][TM + t]);
-    }
-    const float inv = norm ? 1.0f / sqrtf(tot / static_cast<float>(d_i) + eps) : 1.0f;
-    const float hmax = inv * hm;
-    int e = hmax > 0.f ? ilogbf(hmax) - 13 : 0;  // max |h| / c_m in [2^13, 2^14)
-    e = e < -100 ? -100 : (e > 100 ? 100 : e);
-    s_inv[t] = inv;
-    s_c[t] = ldexpf(1.0f, e);
-    if (jb == 0 && t < tm) rowscale[m0 + t] = ldexpf(1.0f, e);
-  }
-  __syncthreads();
-  if (jb == 0) {
-    for (int64_t sl = threadIdx.x; sl < nslot; sl += kProThreads) {
-#pragma unroll
-      for (int t = 0; t < TM; ++t) {
-        if (t < tm) {
-          const float f = s_inv[t] / s_c[t];
-          const float4 h0 = hz4[t * (d_i / 4) + 2 * sl], h1 = hz4[t * (d_i / 4) + 2 * sl + 1];
-          const __half2 p0 = __floats2half2_rn(h0.x * f, h0.y * f), p1 = __floats2half2_rn(h0.z * f, h0.w * f);
-          const __half2 p2 = __floats2half2_rn(h1.x * f, h1.y * f), p3 = __floats2half2_rn(h1.z * f, h1.w * f);
-          uint4 o;
-          o.x = *reinterpret_cast<const uint32_t*>(&p0);
-          o.y = *reinterpret_cast<const uint32_t*>(&p1);
-          o.z = *reinterpret_cast<const uint32_t*>(&p2);
-          o.w = *reinterpret_cast<const uint32_t*>(&p3);
-          reinterpret_cast<uint4*>(hq + (m0 + t) * d_i)[sl] = o;
-        }
-      }
-    }
-    for (int i = threadIdx.x; i < TM * kRpad; i += kProThreads) {
-      const int t = i / kRpad, j = i % kRpad;
-      if (t < tm && j >= r) tq[(m0 + t) * kRpad + j] = __float2bfloat16_rn(0.f);
-    }
-  }
-  if (threadIdx.x == 0) PL_TLP(3);
-  if (A == nullptr || r == 0) return;
-  // LoRA down-projection t = A h for adapter rows j0 .. j0 + 7, FP32
-  const int j0 = 8 * jb;
-  float acc[8][TM];
-#pragma unroll
-  for (int q = 0; q < 8; ++q)
-#pragma unroll
-    for (int t = 0; t < TM; ++t) acc[q][t] = 0.f;
-#pragma unroll 2
-  for (int64_t sl = threadIdx.x; sl < nslot; sl += kProThreads) {
-    uint4 av[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-      av[q] = (j0 + q < r) ? reinterpret_cast<const uint4*>(A + static_cast<int64_t>(j0 + q) * d_i)[sl]
-                           : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-    for (int t = 0; t < TM; ++t) {
-      const float4 h0 = hz4[t * (d_i / 4) + 2 * sl], h1 = hz4[t * (d_i / 4) + 2 * sl + 1];
-      const float hh[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const uint32_t u[4] = {av[q].x, av[q].y, av[q].z, av[q].w};
-        float a = acc[q][t];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          a = fmaf(bf16lo_to_f32(u[j]), hh[2 * j], a);
-          a = fmaf(bf16hi_to_f32(u[j]), hh[2 * j + 1], a);
-        }
-        acc[q][t] = a;
-      }
-    }
-  }
-  if (threadIdx.x == 0) PL_TLP(4);
-  __syncthreads();  // red[] is reused below
-#pragma unroll
-  for (int q = 0; q < 8; ++q)
-#pragma unroll
-    for (int t = 0; t < TM; ++t) {
-      float v = acc[q][t];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-      if (lane == 0) red[warp][q * TM + t] = v;
-    }
-  __syncthreads();
-  if (threadIdx.x < 8 * TM) {
-    const int q = threadIdx.x / TM, t = threadIdx.x % TM;
-    float v = 0.f;
-#pragma unroll
-    for (int w = 0; w < kProThreads / 32; ++w) v += red[w][q * TM + t];
-    if (t < tm && j0 + q < r) tq[(m0 + t) * kRpad + j0 + q] = __float2bfloat16_rn(lambda * s_inv[t] * v);
+  const float inv = norm ? 1.0f / sqrtf(tot / static_cast<float>(d_i) + eps) : 1.0f;
+  const float hmax = inv * hm;
+  int e = hmax > 0.f ? ilogbf(hmax) - 13 : 0;  // max |h| / c_m in [2^13, 2^14)
+  e = e < -100 ? -100 : (e > 100 ? 100 : e);
+  const float f = inv * ldexpf(1.0f, -e);
+  if (threadIdx.x == 0) rowscale[m] = ldexpf(1.0f, e);
+  uint4* hr = reinterpret_cast<uint4*>(hq + m * d_i);
+  for (int64_t sl = threadIdx.x; sl < nv8; sl += kActThreads) {
+    const float4 a = hz4[2 * sl], b = hz4[2 * sl + 1];
+    hr[sl] = make_uint4(f32x2_to_f16x2(a.x * f, a.y * f), f32x2_to_f16x2(a.z * f, a.w * f),
+                        f32x2_to_f16x2(b.x * f, b.y * f), f32x2_to_f16x2(b.z * f, b.w * f));
   }
   if (threadIdx.x == 0) PL_TLP(5);
 }
@@ -373,8 +329,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int N = p.N, stages = p.stages;
-  uint8_t* tq_smem = smem + static_cast<size_t>(stages) * p.stage_bytes;
-  Smem& S = *reinterpret_cast<Smem*>(tq_smem + N * 128);
+  const uint32_t h_bytes = static_cast<uint32_t>(N) * 512u;
+  const uint32_t l_bytes = static_cast<uint32_t>(p.rb) * 512u;  // one A chunk (rb rows x 256 bf16)
+  uint8_t* lring = smem + static_cast<size_t>(stages) * p.stage_bytes;          // 2 A chunks
+  __nv_bfloat16* sBt = reinterpret_cast<__nv_bfloat16*>(lring + 2 * l_bytes);  // [kMaxR][128]: B^T of the tile
+  Smem& S = *reinterpret_cast<Smem*>(reinterpret_cast<uint8_t*>(sBt) + kTileO * kMaxR * 2);
   volatile int* abort_flag = &S.abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -382,31 +341,40 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
   const int c0 = static_cast<int>((static_cast<int64_t>(split) * p.kc) / p.splits);
   const int c1 = static_cast<int>((static_cast<int64_t>(split + 1) * p.kc) / p.splits);
   const int nch = c1 - c0;
-  const bool has_lora = (split == 0) && p.r > 0;
-  const uint32_t h_bytes = static_cast<uint32_t>(N) * 512u;
+  const bool lora = p.r > 0;
   bool go = false;  // epilogue threads: this CTA's accumulators are valid
 
+  const uint64_t pol_w = policy_evict_first();  // weights are streamed once
+  const int pre = nch < stages ? nch : stages;
+  const int32_t row0 = tile * kTileO;
   if (threadIdx.x == 0) {
     PL_TL(0);
     pdl_launch_dependents();
     for (int s = 0; s < stages; ++s) {
-      mbar_init(smem_u32(&S.full[s]), 1);
+      mbar_init(smem_u32(&S.wfull[s]), 1);
+      mbar_init(smem_u32(&S.hfull[s]), 1);
       mbar_init(smem_u32(&S.empty[s]), kDeqWarps + 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&S.a_full[b]), kDeqWarps);
       mbar_init(smem_u32(&S.a_empty[b]), 1);
+      mbar_init(smem_u32(&S.lfull[b]), 1);
+      mbar_init(smem_u32(&S.lempty[b]), 1);
     }
     mbar_init(smem_u32(&S.d_full), 1);
-    mbar_init(smem_u32(&S.tq_full), 1);
-    mbar_init(smem_u32(&S.a2_full), 4);
-    mbar_init(smem_u32(&S.drain), 1);
     S.abort_flag = 0;
     fence_mbar_init();
-    tma_prefetch_desc(&maps.codes);
-    tma_prefetch_desc(&maps.scales);
+    // the first stages of weights do not depend on the prologue: issue them at once
+    for (int c = 0; c < pre; ++c) {
+      uint8_t* st = smem + static_cast<size_t>(c) * p.stage_bytes;
+      const uint32_t wb = smem_u32(&S.wfull[c]);
+      mbar_arrive_expect_tx(wb, kCodesBytes + kScaleBytes);
+      const int kc = c0 + c;
+      tma_load_2d_hint(smem_u32(st), &maps.codes, kc * (kChunkK / 2), row0, wb, pol_w);
+      tma_load_2d_hint(smem_u32(st + kCodesBytes + h_bytes), &maps.scales, kc * (kChunkK / 16), row0, wb, pol_w);
+    }
     tma_prefetch_desc(&maps.hq);
-    tma_prefetch_desc(&maps.tq);
+    if (lora) tma_prefetch_desc(&maps.alora);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&S.tmem_base), kTmemCols);
@@ -421,124 +389,141 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();  // weights are streamed once
-      const int pre = nch < stages ? nch : stages;
-      const int32_t row0 = tile * kTileO;
-      // weights of the first stages do not depend on the prologue: issue them now
-      for (int c = 0; c < pre; ++c) {
-        uint8_t* st = smem + static_cast<size_t>(c) * p.stage_bytes;
-        const uint32_t fb = smem_u32(&S.full[c]);
-        mbar_arrive_expect_tx(fb, kCodesBytes + kScaleBytes + h_bytes);
-        const int kc = c0 + c;
-        tma_load_2d_hint(smem_u32(st), &maps.codes, kc * (kChunkK / 2), row0, fb, pol_w);
-        tma_load_2d_hint(smem_u32(st + kCodesBytes + h_bytes), &maps.scales, kc * (kChunkK / 16), row0, fb, pol_w);
-      }
+      const int lpre = lora ? (nch < 2 ? nch : 2) : 0;
       PL_TL(2);
-      pdl_wait();  // activations come from the prologue
+      pdl_wait();  // activations and the f16 copy of A come from the prologue
       PL_TL(3);
       for (int c = 0; c < pre; ++c) {
         uint8_t* st = smem + static_cast<size_t>(c) * p.stage_bytes;
-        const uint32_t fb = smem_u32(&S.full[c]);
-        const int kc = c0 + c;
+        const uint32_t hb = smem_u32(&S.hfull[c]);
+        mbar_arrive_expect_tx(hb, h_bytes);
         for (int q = 0; q < 4; ++q)
-          tma_load_2d(smem_u32(st + kCodesBytes + q * N * 128), &maps.hq, kc * kChunkK + 64 * q, 0, fb);
+          tma_load_2d(smem_u32(st + kCodesBytes + q * N * 128), &maps.hq, (c0 + c) * kChunkK + 64 * q, 0, hb);
       }
-      if (has_lora) {
-        const uint32_t tb = smem_u32(&S.tq_full);
-        mbar_arrive_expect_tx(tb, static_cast<uint32_t>(N) * 128u);
-        tma_load_2d(smem_u32(tq_smem), &maps.tq, 0, 0, tb);
-      }
-      int c = pre;
-      for (; c < nch; ++c) {
-        const int s = c % stages;
-        if (!wait_or_abort(smem_u32(&S.empty[s]), ((c / stages) - 1) & 1, abort_flag)) break;
-        uint8_t* st = smem + static_cast<size_t>(s) * p.stage_bytes;
-        const uint32_t fb = smem_u32(&S.full[s]);
-        mbar_arrive_expect_tx(fb, kCodesBytes + kScaleBytes + h_bytes);
-        const int kc = c0 + c;
-        tma_load_2d_hint(smem_u32(st), &maps.codes, kc * (kChunkK / 2), row0, fb, pol_w);
-        tma_load_2d_hint(smem_u32(st + kCodesBytes + h_bytes), &maps.scales, kc * (kChunkK / 16), row0, fb, pol_w);
+      for (int c = 0; c < lpre; ++c) {
+        const uint32_t lb = smem_u32(&S.lfull[c]);
+        mbar_arrive_expect_tx(lb, l_bytes);
         for (int q = 0; q < 4; ++q)
-          tma_load_2d(smem_u32(st + kCodesBytes + q * N * 128), &maps.hq, kc * kChunkK + 64 * q, 0, fb);
+          tma_load_2d(smem_u32(lring + c * l_bytes + q * p.rb * 128), &maps.alora, (c0 + c) * kChunkK + 64 * q, 0,
+                      lb);
       }
-      if (*abort_flag) {
-        // drain: every issued stage's copies must land before this CTA exits
-        const int first = c - stages > 0 ? c - stages : 0;
-        for (int d = first; d < c; ++d) {
-          const uint32_t fb = smem_u32(&S.full[d % stages]);
-          const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(fb, (d / stages) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+      int c = pre, lc = lpre;
+      bool ok = true;
+      while (ok && (c < nch || lc < (lora ? nch : 0))) {
+        // A chunks run at most 2 ahead of the weights; weights `stages` ahead
+        if (lora && lc < nch && lc < c + 2) {
+          const int b = lc & 1;
+          ok = wait_or_abort(smem_u32(&S.lempty[b]), ((lc >> 1) - 1) & 1, abort_flag);
+          if (!ok) break;
+          const uint32_t lb = smem_u32(&S.lfull[b]);
+          mbar_arrive_expect_tx(lb, l_bytes);
+          for (int q = 0; q < 4; ++q)
+            tma_load_2d(smem_u32(lring + b * l_bytes + q * p.rb * 128), &maps.alora, (c0 + lc) * kChunkK + 64 * q,
+                        0, lb);
+          ++lc;
+          continue;
         }
+        if (c >= nch) break;
+        const int s = c % stages;
+        ok = wait_or_abort(smem_u32(&S.empty[s]), ((c / stages) - 1) & 1, abort_flag);
+        if (!ok) break;
+        uint8_t* st = smem + static_cast<size_t>(s) * p.stage_bytes;
+        const uint32_t wb = smem_u32(&S.wfull[s]), hb = smem_u32(&S.hfull[s]);
+        const int kc = c0 + c;
+        mbar_arrive_expect_tx(wb, kCodesBytes + kScaleBytes);
+        tma_load_2d_hint(smem_u32(st), &maps.codes, kc * (kChunkK / 2), row0, wb, pol_w);
+        tma_load_2d_hint(smem_u32(st + kCodesBytes + h_bytes), &maps.scales, kc * (kChunkK / 16), row0, wb, pol_w);
+        mbar_arrive_expect_tx(hb, h_bytes);
+        for (int q = 0; q < 4; ++q)
+          tma_load_2d(smem_u32(st + kCodesBytes + q * N * 128), &maps.hq, kc * kChunkK + 64 * q, 0, hb);
+        ++c;
+      }
+      if (*abort_flag) {  // every issued copy must land before this CTA exits
+        for (int d = (c - stages > 0 ? c - stages : 0); d < c; ++d) {
+          drain(smem_u32(&S.wfull[d % stages]), (d / stages) & 1);
+          drain(smem_u32(&S.hfull[d % stages]), (d / stages) & 1);
+        }
+        for (int d = (lc - 2 > 0 ? lc - 2 : 0); d < lc; ++d) drain(smem_u32(&S.lfull[d & 1]), (d >> 1) & 1);
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(kTileO, N, 0);
-      const uint32_t idesc_l = idesc_f16(kTileO, N, 1);
       bool ok = true;
       for (int c = 0; c < nch && ok; ++c) {
         const int s = c % stages, b = c & 1;
         ok = wait_or_abort(smem_u32(&S.a_full[b]), (c >> 1) & 1, abort_flag) &&
-             wait_or_abort(smem_u32(&S.full[s]), (c / stages) & 1, abort_flag);
+             wait_or_abort(smem_u32(&S.hfull[s]), (c / stages) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
         const uint32_t hbase = smem_u32(smem + static_cast<size_t>(s) * p.stage_bytes + kCodesBytes);
 #pragma unroll
         for (int kk = 0; kk < kChunkK / 16; ++kk) {
           const uint64_t bdesc = smem_desc_sw128(hbase + (kk >> 2) * N * 128 + (kk & 3) * 32, 1024);
-          mma_ts(tmem + kColD1, tmem + (kColA0 + 128u * b) + kk * 8, bdesc, idesc, (c > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + kColD1, tmem + kColA0 + 128u * b + kk * 8, bdesc, idesc, (c > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(smem_u32(&S.a_empty[b]));
+        if (lora) {
+          // A operand from shared memory: 128 rows at 1 KB per 8 rows; rows >= rb read
+          // bytes that follow the chunk (still inside this CTA's allocation) and only
+          // feed accumulator lanes >= r, which are never read
+          ok = wait_or_abort(smem_u32(&S.lfull[c & 1]), (c >> 1) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t abase = smem_u32(lring + (c & 1) * l_bytes);
+#pragma unroll
+          for (int kk = 0; kk < kChunkK / 16; ++kk) {
+            const uint64_t adesc = smem_desc_sw128(abase + (kk >> 2) * p.rb * 128 + (kk & 3) * 32, 1024);
+            const uint64_t bdesc = smem_desc_sw128(hbase + (kk >> 2) * N * 128 + (kk & 3) * 32, 1024);
+            mma_ss(tmem + kColDt, adesc, bdesc, idesc, (c > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&S.lempty[c & 1]));
         }
         tc_commit(smem_u32(&S.empty[s]));
-        tc_commit(smem_u32(&S.a_empty[b]));
       }
-      if (ok && has_lora) {
-        ok = wait_or_abort(smem_u32(&S.a2_full), 0, abort_flag) &&
-             wait_or_abort(smem_u32(&S.tq_full), 0, abort_flag);
-        if (ok) {
-          tc_fence_after();
-          const uint32_t tbase = smem_u32(tq_smem);
-          const int ksteps = (p.r + 15) / 16;
-          for (int kk = 0; kk < ksteps; ++kk)
-            mma_ts(tmem + kColD2, tmem + kColA2 + kk * 8, smem_desc_sw128(tbase + kk * 32, 1024), idesc_l,
-                   kk > 0 ? 1u : 0u);
-        }
-      }
-      PL_TL(6);
       tc_commit(smem_u32(&S.d_full));  // also reached on abort: tracks every MMA issued
+      PL_TL(6);
     }
   } else {
     // ---------------------------------------------------------------- dequant + epilogue
-    const int dw = warp - 2;             // 0..7
-    const int quarter = warp & 3;        // tensor-memory lane quarter of this warp
-    const int g = dw >> 2;               // K half of each chunk
-    const int row = quarter * 32 + lane; // weight row within the tile
-    const int64_t o = static_cast<int64_t>(tile) * kTileO + row;
+    const int dw = warp - 2;              // 0..7
+    const int quarter = warp & 3;         // tensor-memory lane quarter of this warp
+    const int g = dw >> 2;                // K half of each chunk
+    const int row = quarter * 32 + lane;  // weight row within the tile
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     bool ok = true;
-    if (has_lora && g == 0) {
-      // A operand of the LoRA up-projection: this row of B_lora, bf16 pairs, zero past r
-      const int rp2 = (p.r + 15) / 16 * 8;  // columns in use
-      for (int cb = 0; cb < rp2; cb += 16) {
-        uint32_t vv[16];
+    if (threadIdx.x == 64) S.s_g = *p.s_g;  // weight inputs: never written by the preceding kernel
+    if (lora) {
+      // B rows of this tile, transposed into sBt[j][row] (bf16, zero past r and past d_o);
+      // the tile's rows are one contiguous block of 128 r elements of B
+      const int et0 = threadIdx.x - 64;
+      const int64_t o0 = static_cast<int64_t>(tile) * kTileO;
+      const int rows = static_cast<int>(p.d_o - o0 < kTileO ? p.d_o - o0 : kTileO);
+      for (int i = et0; i < kTileO * kMaxR; i += kEpiThreads) sBt[i] = __float2bfloat16_rn(0.f);
+      named_bar(1, kEpiThreads);
+      const int n8 = rows * p.r / 8;  // 16-byte pieces (r % 8 == 0) or element-wise otherwise
+      if ((p.r & 7) == 0) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.Blora + o0 * p.r);
+        for (int i = et0; i < n8; i += kEpiThreads) {
+          const uint4 v = src[i];
+          const uint16_t* e8 = reinterpret_cast<const uint16_t*>(&v);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int j = 2 * (cb + i);
-          uint32_t lo = 0u, hi = 0u;
-          if (o < p.d_o && j < p.r) lo = __bfloat16_as_ushort(p.Blora[o * p.r + j]);
-          if (o < p.d_o && j + 1 < p.r) hi = __bfloat16_as_ushort(p.Blora[o * p.r + j + 1]);
-          vv[i] = lo | (hi << 16);
+          for (int q = 0; q < 8; ++q) {
+            const int flat = 8 * i + q, rr = flat / p.r, j = flat % p.r;
+            sBt[j * kTileO + rr] = __ushort_as_bfloat16(e8[q]);
+          }
         }
-        tmem_st16(tmem + lane_addr + kColA2 + cb, vv);
+      } else {
+        for (int i = et0; i < rows * p.r; i += kEpiThreads) {
+          const int rr = i / p.r, j = i % p.r;
+          sBt[j * kTileO + rr] = p.Blora[(o0 + rr) * p.r + j];
+        }
       }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&S.a2_full));
     }
     for (int c = 0; c < nch; ++c) {
       const int s = c % stages, b = c & 1;
-      ok = wait_or_abort(smem_u32(&S.full[s]), (c / stages) & 1, abort_flag) &&
+      ok = wait_or_abort(smem_u32(&S.wfull[s]), (c / stages) & 1, abort_flag) &&
            (c < 2 || wait_or_abort(smem_u32(&S.a_empty[b]), ((c >> 1) - 1) & 1, abort_flag));
       if (!ok) break;
       if (c == 0 && threadIdx.x == 64) PL_TL(4);
@@ -562,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
         for (int i = 0; i < 8; ++i) v[i] = hmul2_u32(v[i], sa);
 #pragma unroll
         for (int i = 8; i < 16; ++i) v[i] = hmul2_u32(v[i], sb);
-        tmem_st16(tmem + lane_addr + (kColA0 + 128u * b) + j * 16, v);
+        tmem_st16(tmem + lane_addr + kColA0 + 128u * b + j * 16, v);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -573,39 +558,38 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
       }
     }
     if (threadIdx.x == 64) PL_TL(5);
-    // ---------------------------------------------------------------- epilogue
+    // ---------------------------------------------------------------- epilogue, part 1
     ok = wait_or_abort(smem_u32(&S.d_full), 0, abort_flag) && ok;
-    if (threadIdx.x == 64) PL_TL(7);
     tc_fence_after();
+    if (threadIdx.x == 64) PL_TL(7);
     pdl_wait();  // the row scales belong to this call's prologue
     const int et = threadIdx.x - 64;  // 0 .. 255
     if (et < N) S.rowscale[et] = et < p.M ? p.rowscale[et] : 0.f;
-    // one decision for all epilogue threads (also publishes the row scales)
-    go = named_bar_and(1, kDeqWarps * 32, ok && !*abort_flag);
+    go = named_bar_and(1, kEpiThreads, ok && !*abort_flag);  // one decision, publishes the row scales
     if (threadIdx.x == 64) PL_TL(8);
     if (go) {
-      const float s_g = *p.s_g;
-      const int half = N / 2;
+      float* red = reinterpret_cast<float*>(smem);  // [N][128]    s_g c_n D1, reuses the stages
+      float* tred = red + N * kTileO;                // [N][kTStride]  c_n Dt: this CTA's slice of t
+      const float s_g = S.s_g;
+      const int half = N / 2;  // 8, 16, 24 or 32 tokens per thread
       const int n0 = g * half;
-      float* red = reinterpret_cast<float*>(smem);  // [N][128] partial, reuses stage 0
-      for (int cb = 0; cb < half; cb += 8) {
-        uint32_t d1[8], d2[8];
-        tmem_ld8(tmem + lane_addr + kColD1 + n0 + cb, d1);
-        if (has_lora) tmem_ld8(tmem + lane_addr + kColD2 + n0 + cb, d2);
-        tmem_ld_wait();
+      uint32_t d1[32], dt[32];
+      const bool trow = lora && quarter < 2;  // lanes 0..63 hold rows of t
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int n = n0 + cb + i;
-          float v = s_g * S.rowscale[n] * __uint_as_float(d1[i]);
-          if (has_lora) v += __uint_as_float(d2[i]);
-          if (p.splits == 1) {
-            if (n < p.M && o < p.d_o) {
-              if (p.y_f32) static_cast<float*>(p.y)[n * p.d_o + o] = v;
-              else static_cast<__nv_bfloat16*>(p.y)[n * p.d_o + o] = __float2bfloat16_rn(v);
-            }
-          } else {
-            red[n * kTileO + row] = v;
-          }
+      for (int cb = 0; cb < 4; ++cb) {
+        if (cb * 8 < half) {
+          tmem_ld8(tmem + lane_addr + kColD1 + n0 + cb * 8, &d1[cb * 8]);
+          if (trow) tmem_ld8(tmem + lane_addr + kColDt + n0 + cb * 8, &dt[cb * 8]);
+        }
+      }
+      tmem_ld_wait();
+      const int jt = row;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        if (i < half) {
+          const int n = n0 + i;
+          red[n * kTileO + row] = s_g * S.rowscale[n] * __uint_as_float(d1[i]);
+          if (trow) tred[n * kTStride + jt] = S.rowscale[n] * __uint_as_float(dt[i]);
         }
       }
     }
@@ -613,34 +597,102 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
   if (threadIdx.x == 64) PL_TL(9);
   tc_fence_before();
   __syncthreads();
-  if (p.splits > 1) {
-    // K splits of one tile form a cluster: after every CTA has its FP32 partial in
-    // shared memory, CTA `split` sums rows [r0, r1) of all partials over DSMEM in
-    // split order (deterministic) and writes them.
-    cluster_sync();
-    if (threadIdx.x == 0) PL_TL(10);
-    if (threadIdx.x >= 64 && go) {
-      const int et = threadIdx.x - 64;
-      const int r0 = (split * kTileO) / p.splits, r1 = ((split + 1) * kTileO) / p.splits;
-      const int nr = r1 - r0;
-      const int mt = static_cast<int>(p.M < N ? p.M : N);
-      const uint32_t red_addr = smem_u32(smem);
-      for (int e = et; e < nr * mt; e += kDeqWarps * 32) {
-        const int n = e / nr, rr = r0 + e % nr;
-        const int64_t oo = static_cast<int64_t>(tile) * kTileO + rr;
-        const uint32_t off = static_cast<uint32_t>((n * kTileO + rr) * 4);
-        float acc = 0.f;
-        for (int sp = 0; sp < p.splits; ++sp) acc += ld_dsmem_f32(mapa_shared(red_addr + off, sp));
-        if (oo < p.d_o) {
-          if (p.y_f32) static_cast<float*>(p.y)[n * p.d_o + oo] = acc;
-          else static_cast<__nv_bfloat16*>(p.y)[n * p.d_o + oo] = __float2bfloat16_rn(acc);
+  // ------------------------------------------------------------------ epilogue, part 2
+  // After a cluster barrier every CTA sums the t slices of all S CTAs (split order) into
+  // lambda t, then the D1 partials of its row groups (4 rows each, groups
+  // [32 split / S, 32 (split+1) / S)), adds B (lambda t) and writes y.
+  cluster_sync();
+  if (threadIdx.x == 0) PL_TL(10);
+  if (threadIdx.x >= 64 && threadIdx.x < 64 + kEpiThreads && go) {
+    const int et = threadIdx.x - 64;
+    float* red = reinterpret_cast<float*>(smem);
+    float* tred = red + N * kTileO;
+    float* tful = tred + N * kTStride;  // [N][kTStride]: lambda t
+    const uint32_t red_addr = smem_u32(red), tred_addr = smem_u32(tred);
+    const int mt = static_cast<int>(p.M < N ? p.M : N);
+    if (lora) {
+      const int rq = (p.r + 3) / 4;  // groups of 4 adapter rows
+      for (int e = et; e < mt * rq; e += kEpiThreads) {
+        const int n = e / rq, jj = 4 * (e % rq);
+        const uint32_t addr = tred_addr + static_cast<uint32_t>((n * kTStride + jj) * 4);
+        float4 part[kMaxSplit];
+#pragma unroll
+        for (int sp = 0; sp < kMaxSplit; ++sp)
+          if (sp < p.splits) part[sp] = ld_dsmem_f32x4(mapa_shared(addr, sp));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int sp = 0; sp < kMaxSplit; ++sp)
+          if (sp < p.splits) {
+            acc.x += part[sp].x;
+            acc.y += part[sp].y;
+            acc.z += part[sp].z;
+            acc.w += part[sp].w;
+          }
+        reinterpret_cast<float4*>(tful + n * kTStride + jj)[0] =
+            make_float4(p.lambda * acc.x, p.lambda * acc.y, p.lambda * acc.z, p.lambda * acc.w);
+      }
+      named_bar(1, kEpiThreads);
+    }
+    const int g0 = (split * (kTileO / 4)) / p.splits, g1 = ((split + 1) * (kTileO / 4)) / p.splits;
+    const int ng = g1 - g0;
+    // work item = (token n, row group rr, quarter jp of the adapter rows): the 4 lanes
+    // of one (n, rr) are neighbours in a warp and combine their LoRA sums by shuffles;
+    // lane jp == 0 also sums the D1 partials and writes the 4 outputs
+    const int items = ng * mt * 4;
+    const int jq = (p.r + 3) / 4;
+    for (int base = et - (et & 31); base < items; base += kEpiThreads) {
+      const int e = base + (et & 31);
+      const bool valid = e < items;
+      const int gi = e >> 2, jp = e & 3;
+      const int n = valid ? gi / ng : 0, rr = valid ? 4 * (g0 + gi % ng) : 0;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      if (valid && lora) {
+        const float* tn = tful + n * kTStride;
+        const int ja = jp * jq, jb = (jp + 1) * jq < p.r ? (jp + 1) * jq : p.r;
+        for (int jj = ja; jj < jb; ++jj) {
+          const float tj = tn[jj];
+          const uint2 b4 = *reinterpret_cast<const uint2*>(sBt + jj * kTileO + rr);  // B[rr..rr+3][jj]
+          acc[0] = fmaf(bf16lo_to_f32(b4.x), tj, acc[0]);
+          acc[1] = fmaf(bf16hi_to_f32(b4.x), tj, acc[1]);
+          acc[2] = fmaf(bf16lo_to_f32(b4.y), tj, acc[2]);
+          acc[3] = fmaf(bf16hi_to_f32(b4.y), tj, acc[3]);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[q] += __shfl_xor_sync(0xFFFFFFFFu, acc[q], 1);
+        acc[q] += __shfl_xor_sync(0xFFFFFFFFu, acc[q], 2);
+      }
+      if (valid && jp == 0) {
+        const uint32_t addr = red_addr + static_cast<uint32_t>((n * kTileO + rr) * 4);
+        float4 part[kMaxSplit];
+#pragma unroll
+        for (int sp = 0; sp < kMaxSplit; ++sp)
+          if (sp < p.splits) part[sp] = ld_dsmem_f32x4(mapa_shared(addr, sp));
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int sp = 0; sp < kMaxSplit; ++sp)
+          if (sp < p.splits) {
+            d[0] += part[sp].x;
+            d[1] += part[sp].y;
+            d[2] += part[sp].z;
+            d[3] += part[sp].w;
+          }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int64_t oo = static_cast<int64_t>(tile) * kTileO + rr + q;
+          const float v = d[q] + acc[q];
+          if (oo < p.d_o) {
+            if (p.y_f32) static_cast<float*>(p.y)[n * p.d_o + oo] = v;
+            else static_cast<__nv_bfloat16*>(p.y)[n * p.d_o + oo] = __float2bfloat16_rn(v);
+          }
         }
       }
     }
-    if (threadIdx.x == 64) PL_TL(11);
-    cluster_sync();  // peers keep their shared memory until every reader is done
-    if (threadIdx.x == 0) PL_TL(12);
   }
+  if (threadIdx.x == 64) PL_TL(11);
+  cluster_sync();  // peers keep their shared memory until every reader is done
+  if (threadIdx.x == 0) PL_TL(12);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -676,21 +728,25 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void*
 }
 
 struct Plan {
-  int N, tiles, kc, splits, stages, tm;
+  int N, rb, tiles, kc, splits, stages;
   uint32_t stage_bytes;
-  size_t smem, pro_smem;
+  size_t smem, act_smem;
 };
 
 uint32_t stage_bytes_for(int N) { return kCodesBytes + kScaleBytes + static_cast<uint32_t>(N) * 512u; }
 
-int stages_for(uint32_t stage_bytes) {
-  int st = static_cast<int>((200u * 1024u) / stage_bytes);
-  return st > kMaxStages ? kMaxStages : (st < 2 ? 2 : st);
-}
-
-size_t smem_for(int N) {
-  const uint32_t sb = stage_bytes_for(N);
-  return 1024 + static_cast<size_t>(stages_for(sb)) * sb + static_cast<size_t>(N) * 128 + sizeof(Smem);
+// Shared memory: `stages` stages, the 2-chunk ring of A (rb rows x 512 B each), the B
+// rows of the tile, the control block and 1 KB of alignment slack.  The epilogue
+// reuses the stage region for its partials ([N][128] + 2 x [N][68] FP32 < 1.1 KB x N),
+// which two stages always cover.
+void stage_plan(int N, int rb, int& stages, uint32_t& sb, size_t& total) {
+  sb = stage_bytes_for(N);
+  const size_t fixed = 1024 + 2 * static_cast<size_t>(rb) * 512 + kTileO * kMaxR * 2 + sizeof(Smem);
+  const size_t limit = 227 * 1024;
+  int st = static_cast<int>((limit - fixed) / sb);
+  st = st > kMaxStages ? kMaxStages : st;
+  stages = st < 2 ? 2 : st;
+  total = fixed + static_cast<size_t>(stages) * sb;
 }
 
 cudaError_t set_kernel_attributes() {
@@ -699,26 +755,26 @@ cudaError_t set_kernel_attributes() {
   std::call_once(once, [] {
     err = cudaFuncSetAttribute(k_tc_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(k_tc_prologue<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(k_tc_prologue<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(k_tc_prologue<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+      err = cudaFuncSetAttribute(k_act, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
   });
   return err;
 }
 
-// Clusters of `cs` decode CTAs that can be resident at once (cached per N class).
-int max_active_clusters(int N, int cs) {
-  static int cache[kMaxN / 16 + 1][kMaxSplit + 1];
+// Clusters of `cs` decode CTAs that can be resident at once (cached per N and A rows).
+int max_active_clusters(int N, int rb, int cs) {
+  static int cache[kMaxN / 16 + 1][kMaxR / 8 + 1][kMaxSplit + 1];
   static std::mutex mu;
   std::lock_guard<std::mutex> lk(mu);
-  int& c = cache[N / 16][cs];
+  int& c = cache[N / 16][rb / 8][cs];
   if (c == 0) {
+    int st;
+    uint32_t sb;
+    size_t total;
+    stage_plan(N, rb, st, sb, total);
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(cs * 64));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem_for(N);
+    cfg.dynamicSmemBytes = total;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = static_cast<unsigned>(cs);
@@ -738,11 +794,11 @@ int max_active_clusters(int N, int cs) {
 
 // Split count: minimise (waves) x (chunks per CTA + fixed per-CTA cost), the fixed
 // cost counted as 1.5 chunks; ties go to fewer splits.
-int choose_splits(int N, int tiles, int kc, bool query) {
+int choose_splits(int N, int rb, int tiles, int kc) {
   int best = 1;
   double best_cost = 1e30;
   for (int s = 1; s <= kMaxSplit && s <= kc; ++s) {
-    const int clusters = query ? max_active_clusters(N, s) : 1024;
+    const int clusters = max_active_clusters(N, rb, s);
     const int waves = (tiles + clusters - 1) / clusters;
     const double cost = waves * (static_cast<double>((kc + s - 1) / s) + 1.5);
     if (cost < best_cost - 1e-9) {
@@ -753,29 +809,26 @@ int choose_splits(int N, int tiles, int kc, bool query) {
   return best;
 }
 
-Plan make_plan(int64_t M, int64_t d_i, int64_t d_o, bool query) {
+Plan make_plan(int64_t M, int64_t d_i, int64_t d_o, int r) {
   Plan pl{};
   pl.N = static_cast<int>((M + 15) / 16 * 16);
+  pl.rb = r > 0 ? (r + 7) / 8 * 8 : 8;
   pl.tiles = static_cast<int>((d_o + kTileO - 1) / kTileO);
   pl.kc = static_cast<int>(d_i / kChunkK);
-  pl.splits = choose_splits(pl.N, pl.tiles, pl.kc, query);
-  pl.stage_bytes = stage_bytes_for(pl.N);
-  pl.stages = stages_for(pl.stage_bytes);
-  pl.smem = smem_for(pl.N);
-  const int64_t tm = (160 * 1024) / (d_i * 4);
-  pl.tm = tm >= 4 ? 4 : (tm >= 2 ? 2 : 1);
-  pl.pro_smem = static_cast<size_t>(pl.tm) * d_i * 4;
+  pl.splits = choose_splits(pl.N, pl.rb, pl.tiles, pl.kc);
+  stage_plan(pl.N, pl.rb, pl.stages, pl.stage_bytes, pl.smem);
+  pl.act_smem = static_cast<size_t>(d_i) * 4;
   return pl;
 }
 
 struct TcWs {
   __half* hq;
   float* rowscale;
-  __nv_bfloat16* tq;
+  __half* A16;
   size_t bytes;
 };
 
-TcWs carve(void* ws, int64_t M, int64_t d_i) {
+TcWs carve(void* ws, int64_t M, int64_t d_i, int r) {
   TcWs w{};
   const uintptr_t b = reinterpret_cast<uintptr_t>(ws);
   size_t off = 0;
@@ -783,50 +836,38 @@ TcWs carve(void* ws, int64_t M, int64_t d_i) {
   off += align_up(static_cast<size_t>(M) * d_i * 2, 256);
   w.rowscale = reinterpret_cast<float*>(b + off);
   off += align_up(static_cast<size_t>(M) * 4, 256);
-  w.tq = reinterpret_cast<__nv_bfloat16*>(b + off);
-  off += align_up(static_cast<size_t>(M) * kRpad * 2, 256);
+  w.A16 = reinterpret_cast<__half*>(b + off);
+  off += align_up(static_cast<size_t>(r) * d_i * 2, 256);
   w.bytes = off;
   return w;
-}
-
-template <int TM>
-cudaError_t launch_prologue(const LinearArgs& a, const Plan& pl, const TcWs& w, cudaStream_t stream,
-                            cudaLaunchAttribute* pdl) {
-  const int ny = a.r > 0 ? (a.r + 7) / 8 : 1;
-  cudaLaunchConfig_t c{};
-  c.gridDim = dim3(static_cast<unsigned>((a.M + TM - 1) / TM), static_cast<unsigned>(ny));
-  c.blockDim = dim3(kProThreads);
-  c.dynamicSmemBytes = pl.pro_smem;
-  c.stream = stream;
-  c.attrs = pdl;
-  c.numAttrs = 1;
-  return cudaLaunchKernelEx(&c, k_tc_prologue<TM>, static_cast<const __nv_bfloat16*>(a.x), a.M, a.d_i, a.w_norm,
-                            a.z, a.eps, static_cast<const __nv_bfloat16*>(a.A), a.r, a.lambda, w.hq, w.rowscale,
-                            w.tq);
 }
 
 }  // namespace
 
 bool tc_supported(int64_t M, int64_t d_i, int64_t, int r) {
-  return M >= 1 && M <= kMaxN && d_i >= kChunkK && d_i % kChunkK == 0 && r >= 0 && r <= kRpad;
+  // k_act keeps one FP32 row in shared memory (<= 192 KB)
+  return M >= 1 && M <= kMaxN && d_i >= kChunkK && d_i % kChunkK == 0 && d_i <= 49152 && r >= 0 && r <= kMaxR;
 }
 
-size_t tc_workspace_bytes(int64_t M, int64_t d_i, int64_t, int) { return carve(nullptr, M, d_i).bytes; }
+size_t tc_workspace_bytes(int64_t M, int64_t d_i, int64_t, int r) { return carve(nullptr, M, d_i, r).bytes; }
 
 cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   cudaError_t e = set_kernel_attributes();
   if (e != cudaSuccess) return e;
-  const Plan pl = make_plan(a.M, a.d_i, a.d_o, true);
-  const TcWs w = carve(a.ws, a.M, a.d_i);
+  const Plan pl = make_plan(a.M, a.d_i, a.d_o, a.r);
+  const TcWs w = carve(a.ws, a.M, a.d_i, a.r);
   TcMaps maps;
   bool ok = encode_2d(&maps.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.codes, a.d_i / 2, a.d_o, 128, kTileO,
                       CU_TENSOR_MAP_SWIZZLE_128B) &&
             encode_2d(&maps.scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.scales, a.d_i / 16, a.d_o, 16, kTileO,
                       CU_TENSOR_MAP_SWIZZLE_NONE) &&
             encode_2d(&maps.hq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.hq, a.d_i, a.M, 64, pl.N,
-                      CU_TENSOR_MAP_SWIZZLE_128B) &&
-            encode_2d(&maps.tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w.tq, kRpad, a.M, 64, pl.N,
                       CU_TENSOR_MAP_SWIZZLE_128B);
+  if (ok && a.r > 0)
+    ok = encode_2d(&maps.alora, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.A16, a.d_i, a.r, 64, pl.rb,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+  else
+    maps.alora = maps.hq;  // unused
   if (!ok) return cudaErrorInvalidValue;
 
   cudaLaunchAttribute attrs[2];
@@ -837,8 +878,19 @@ cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   attrs[1].val.clusterDim.y = 1;
   attrs[1].val.clusterDim.z = 1;
 
-  e = pl.tm == 4 ? launch_prologue<4>(a, pl, w, stream, attrs)
-                 : (pl.tm == 2 ? launch_prologue<2>(a, pl, w, stream, attrs) : launch_prologue<1>(a, pl, w, stream, attrs));
+  // extra prologue CTAs copy A to f16 (about 2048 elements per thread and CTA at most 32)
+  const int64_t a_slots = static_cast<int64_t>(a.r) * a.d_i / 8;
+  int nconv = static_cast<int>((a_slots + kActThreads * 4 - 1) / (kActThreads * 4));
+  nconv = a.r > 0 ? (nconv < 1 ? 1 : (nconv > 32 ? 32 : nconv)) : 0;
+  cudaLaunchConfig_t c1{};
+  c1.gridDim = dim3(static_cast<unsigned>(a.M + nconv));
+  c1.blockDim = dim3(kActThreads);
+  c1.dynamicSmemBytes = pl.act_smem;
+  c1.stream = stream;
+  c1.attrs = attrs;
+  c1.numAttrs = 1;
+  e = cudaLaunchKernelEx(&c1, k_act, static_cast<const __nv_bfloat16*>(a.x), a.M, a.d_i, a.w_norm, a.z, a.eps,
+                         w.hq, w.rowscale, static_cast<const __nv_bfloat16*>(a.A), a.r, w.A16);
   if (e != cudaSuccess) return e;
 
   TcParams p{};
@@ -847,6 +899,7 @@ cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   p.d_o = a.d_o;
   p.N = pl.N;
   p.r = a.r;
+  p.rb = pl.rb;
   p.tiles = pl.tiles;
   p.splits = pl.splits;
   p.kc = pl.kc;
@@ -865,7 +918,7 @@ cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   c2.dynamicSmemBytes = pl.smem;
   c2.stream = stream;
   c2.attrs = attrs;
-  c2.numAttrs = pl.splits > 1 ? 2 : 1;
+  c2.numAttrs = 2;
   return cudaLaunchKernelEx(&c2, k_tc_decode, maps, p);
 }
 
