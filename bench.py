@@ -57,13 +57,21 @@ def measured_peaks():
 
 
 def profile_traffic(kernel: str, workload: str):
-    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if any."""
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, or None when
+    there is none or the kernel's source has changed since the counters were taken."""
+    import hashlib
+
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         e = d.get(f"{kernel}@{workload}")
-        return None if e is None else e.get("dram_bytes_per_launch")
+        if e is None:
+            return None
+        with open(os.path.join(ROOT, e["src"]), "rb") as f:
+            if hashlib.sha1(f.read()).hexdigest() != e["src_sha1"]:
+                return None
+        return e.get("dram_bytes_per_launch")
     except Exception:
         return None
 
@@ -333,7 +341,7 @@ def run_ours(args, world, rank, local):
                        "parallelism": f"replicas x{world}"},
             "tflops": round(step_flops * args.steps * world / (ms * 1e-3) / 1e12, 2),
             "per_M": per_m,
-            "roofline": {"bound": "hbm", "kernel": "nvfp4_lora_linear (k_tc_prologue + k_tc_decode)",
+            "roofline": {"bound": "hbm", "kernel": "nvfp4_lora_linear call (k_act + k_tc_decode, CUDA events around the call)",
                          "M": int(dom), "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": round(achieved / hbm_peak, 4), "peak_kind": peak_kind,
                          "traffic": profile_traffic("k_tc_decode", f"{args.workload}/M{dom}")},
