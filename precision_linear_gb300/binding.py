@@ -49,6 +49,7 @@ _SIGNATURES = {
                                             _c_void_p, ctypes.c_size_t, _c_void_p]),
     "pl_last_device_status": (ctypes.c_int, [_c_void_p]),
     "pl_debug_fail_next_launch": (None, [ctypes.c_int]),
+    "pl_debug_linear_path": (ctypes.c_int, [_i64, _i64, _i64, ctypes.c_int]),
     "pl_debug_wait_timeout_probe": (ctypes.c_int, [_c_void_p]),
 }
 
@@ -208,3 +209,9 @@ def last_device_status(device=None) -> int:
     dev = torch.device(device) if device is not None else torch.device("cuda")
     with torch.cuda.device(dev):
         return int(lib().pl_last_device_status(_stream(dev)))
+
+
+def linear_path(M: int, d_i: int, d_o: int, r: int) -> int:
+    """Kernel path the linear takes for this shape on the current device: 2 fused
+    tcgen05 kernel, 1 tcgen05 prologue + main kernel, 0 CUDA-core kernels, -1 invalid."""
+    return int(lib().pl_debug_linear_path(M, d_i, d_o, r))

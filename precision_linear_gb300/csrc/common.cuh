@@ -174,6 +174,93 @@ PL_DEVINL void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
                : "r"(taddr) : "memory");
 }
 
+// ---------------------------------------------------------------- f16 / E2M1 / TMEM / cluster helpers
+PL_DEVINL uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+PL_DEVINL uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+// Two FP32 -> f16x2, `lo` into the low half.
+PL_DEVINL uint32_t f32x2_to_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// 8 E2M1 codes (one 32-bit word, code k in nibble k) -> 4 f16x2 (codes 2p, 2p+1 in word p).
+PL_DEVINL void e2m1x8_to_f16x8(uint32_t w, uint32_t& o0, uint32_t& o1, uint32_t& o2, uint32_t& o3) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(o0), "=r"(o1), "=r"(o2), "=r"(o3) : "r"(w));
+}
+PL_DEVINL void tmem_st16(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+         "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+         "r"(v[15]) : "memory");
+}
+PL_DEVINL void tmem_ld8(uint32_t taddr, uint32_t* v) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+                 "=r"(v[7]) : "r"(taddr) : "memory");
+}
+PL_DEVINL void named_bar(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(n) : "memory");
+}
+// Named barrier that also ANDs a predicate over the participating threads.
+PL_DEVINL bool named_bar_and(uint32_t id, uint32_t n, bool pred) {
+  uint32_t r;
+  asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %3, 0;\n\t"
+               "bar.red.and.pred p, %1, %2, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(r) : "r"(id), "r"(n), "r"(pred ? 1u : 0u) : "memory");
+  return r != 0;
+}
+PL_DEVINL void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+PL_DEVINL uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+PL_DEVINL float4 ld_dsmem_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+
+// Wait for phase `parity` that also gives up when another role of the CTA has
+// already given up (*abort_flag != 0); on its own time-out it raises the flag and
+// sets the time-out bit of the kernel's status word.
+PL_DEVINL bool wait_or_abort_status(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicOr(status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+// Bounded drain of one barrier phase (after an abort).
+PL_DEVINL void drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+}
+
 // Instruction descriptor for tcgen05.mma kind::f16, K-major A and B, FP32 accumulator.
 // ab_bf16: 0 -> f16 operands, 1 -> bf16 operands.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int ab_bf16) {

@@ -49,6 +49,11 @@ cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream);
 uint32_t tc_read_and_clear_status();
 cudaError_t launch_wait_timeout_probe(cudaStream_t stream);
 
+// ---- linear_fused.cu (tcgen05, one kernel; M <= 64 and at most 3 K chunks of 256 per CTA)
+bool fused_supported(int64_t M, int64_t d_i, int64_t d_o, int r);
+cudaError_t launch_linear_fused(const LinearArgs& a, cudaStream_t stream);
+uint32_t fused_read_and_clear_status();
+
 // ---- api.cu
 int sm_count();  // SMs of the current device (cached)
 

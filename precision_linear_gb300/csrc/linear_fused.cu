@@ -1,0 +1,737 @@
+// Single-kernel tcgen05 NVFP4 + LoRA + RMSNorm-AQN linear for decode (M <= 64), sm_103a.
+//
+// Computes the forward map of "QeRL: When Quantized Weights Help Reinforcement
+// Learning, and Where the Evidence Stops", section 2.1 (y = W_hat h + lambda B (A h)),
+// on the section 3.1 NVFP4 backbone (w_hat = s_g s_b q), with the section 5.1 input
+// h = x / rms(x) (.) (w_norm + z).
+//
+// Used when every CTA's slice of the K = d_i axis is at most 3 chunks of 256, so that
+// the CTA holds all of its weights (dequantised, in tensor memory) and all of its
+// activations (shared memory) at once.  A cluster of S CTAs covers 128 weight rows;
+// CTA s takes chunks [s kc / S, (s+1) kc / S).  The norm is folded in by linearity:
+//   y[m, o] = rs_m * ( sum_k W_hat[o, k] u[m, k] + lambda sum_j B[o, j] sum_k A[j, k] u[m, k] ),
+//   u = x (.) (w_norm + z),   rs_m = 1 / sqrt(sum_k x[m, k]^2 / d_i + eps),
+// so no CTA needs the whole row before its MMAs: each converts its own slice of u to
+// f16 with a power-of-two scale c of its own (max |u c| in [2^13, 2^14)), and the
+// per-split sums of x^2 are added up in the epilogue.
+//
+// Roles (14 warps):
+//   warp 0       TMA: the CTA's codes and E4M3 scales and the LoRA A slice at once
+//                (weights; they do not depend on the preceding kernel), then, after
+//                the programmatic-dependent-launch wait, the x slice;
+//   warps 10-13  B rows of the CTA's output share into shared memory; after the wait
+//                w_norm + z; A bf16 -> f16 in place; x: sum of squares and max |u| per
+//                token row, then u c -> f16 in place; the row sums go to every CTA of
+//                the cluster;
+//   warps 2-9    dequantise every chunk into tensor memory (E2M1 -> f16 conversion,
+//                times the block scale: exact in f16), then the epilogue;
+//   warp 1       tcgen05.mma kind::f16: D1 += W_hat/s_g (tensor memory) x u^T and
+//                Dt^T += u x A^T (both from shared memory), accumulators in tensor memory.
+// Epilogue: each CTA sends, with st.async into its peers' shared memory, the rows of
+// s_g / c D1 that each peer owns (peer p owns rows [128 p / S, 128 (p+1) / S)) and its
+// whole t slice Dt^T / c to every peer.  Each CTA sums what it owns in split order
+// (deterministic), adds lambda B t on CUDA cores, scales by rs and writes y.
+//
+// Every mbarrier wait is bounded (200 ms).  A wait that gives up sets the status word;
+// the CTA still takes part in every cluster barrier and still sends its (then
+// meaningless) share, so that no peer waits on it for ever, drains its own copies,
+// frees its tensor memory and returns.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace pl {
+
+__device__ uint32_t g_fused_status = 0;
+
+namespace {
+
+constexpr int kTileO = 128;
+constexpr int kChunkK = 256;
+constexpr int kCodesBytes = kTileO * kChunkK / 2;   // 16 KB
+constexpr int kScaleBytes = kTileO * kChunkK / 16;  // 2 KB
+constexpr int kMaxChunks = 3;
+constexpr int kMaxSplit = 8;
+constexpr int kMaxN = 64;
+constexpr int kMaxR = 64;
+constexpr int kDeqWarps = 8;
+constexpr int kConvWarps = 4;
+constexpr int kConvThreads = kConvWarps * 32;
+constexpr int kEpiThreads = kDeqWarps * 32;
+constexpr int kThreads = (2 + kDeqWarps + kConvWarps) * 32;  // 448
+constexpr int kConvWarp0 = 2 + kDeqWarps;                    // first conversion warp
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColD1 = 384;  // A buffers: chunk c at columns [128 c, 128 c + 128)
+constexpr uint32_t kColDt = 448;
+constexpr size_t kMinSmem = 120 * 1024;  // > half an SM: one CTA per SM, so its 512 TMEM columns are free
+
+struct FParams {
+  int64_t M, d_i, d_o;
+  int N, Np, rb, r, S, kc, rows_max;
+  float lambda, eps;
+  const float* s_g;
+  const float* w_norm;
+  const float* z;
+  const __nv_bfloat16* B;
+  void* y;
+  int y_f32;
+  // shared-memory layout (byte offsets from the 1 KB-aligned base)
+  uint32_t off_scales, off_x, off_a, off_g, off_bt, off_q, off_ctrl;
+  uint32_t off_rt, off_ts;  // receive buffers, over the dead stage region (receive P at 0)
+};
+
+struct FMaps {
+  CUtensorMap codes, scales, x, a;
+};
+
+struct Ctrl {
+  uint64_t wfull[kMaxChunks];
+  uint64_t a_in, x_in, act_ready;
+  uint64_t a_full[kMaxChunks];
+  uint64_t d_full, recv;
+  uint32_t tmem_base;
+  int abort_flag;
+  float s_g;
+  float cinv[kMaxN];  // 1 / c of this split, per token row
+  float rs[kMaxN];
+};
+
+PL_DEVINL bool wait_f(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  return wait_or_abort_status(bar, parity, abort_flag, &g_fused_status);
+}
+PL_DEVINL uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+PL_DEVINL void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+PL_DEVINL void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+PL_DEVINL void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// 16 bytes into a peer's shared memory, completing `bytes` of its mbarrier's transaction.
+PL_DEVINL void st_async_f32x4(uint32_t addr, float4 v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+               :: "r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar) : "memory");
+}
+PL_DEVINL void st_async_f32(uint32_t addr, float v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+               :: "r"(addr), "r"(__float_as_uint(v)), "r"(bar) : "memory");
+}
+// First weight row of the share that CTA `s` of the cluster owns.
+PL_DEVINL int owner_row0(int s, int S) { return (s * kTileO) / S; }
+
+__global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_constant__ FMaps maps, const FParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Ctrl& C = *reinterpret_cast<Ctrl*>(smem + p.off_ctrl);
+  volatile int* abort_flag = &C.abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = p.S, N = p.N;
+  const int me = static_cast<int>(cluster_rank());
+  const int tile = blockIdx.x / S;
+  const int c0 = (me * p.kc) / S, c1 = ((me + 1) * p.kc) / S;
+  const int nch = c1 - c0;
+  const int nslab = nch * 4;  // 64-element k slabs of this CTA
+  const bool lora = p.r > 0, norm = p.w_norm != nullptr;
+  const int R0 = owner_row0(me, S), rows_own = owner_row0(me + 1, S) - R0;
+  const int32_t row0 = tile * kTileO;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t x_bytes = static_cast<uint32_t>(nslab) * N * 128u;
+  const uint32_t a_bytes = static_cast<uint32_t>(nslab) * p.rb * 128u;
+
+  if (threadIdx.x == 0) {
+    pdl_launch_dependents();
+    for (int c = 0; c < kMaxChunks; ++c) {
+      mbar_init(smem_u32(&C.wfull[c]), 1);
+      mbar_init(smem_u32(&C.a_full[c]), kDeqWarps);
+    }
+    mbar_init(smem_u32(&C.a_in), 1);
+    mbar_init(smem_u32(&C.x_in), 1);
+    mbar_init(smem_u32(&C.act_ready), kConvWarps);
+    mbar_init(smem_u32(&C.d_full), 1);
+    mbar_init(smem_u32(&C.recv), 1);
+    C.abort_flag = 0;
+    C.s_g = *p.s_g;  // a weight input: not written by the preceding kernel
+    fence_mbar_init();
+    const uint64_t pol = policy_evict_first();  // weights are streamed once
+    for (int c = 0; c < nch; ++c) {
+      const uint32_t wb = smem_u32(&C.wfull[c]);
+      mbar_arrive_expect_tx(wb, kCodesBytes + kScaleBytes);
+      tma_load_2d_hint(sbase + c * kCodesBytes, &maps.codes, (c0 + c) * (kChunkK / 2), row0, wb, pol);
+      tma_load_2d_hint(sbase + p.off_scales + c * kScaleBytes, &maps.scales, (c0 + c) * (kChunkK / 16), row0, wb,
+                       pol);
+    }
+    if (lora) {
+      const uint32_t ab = smem_u32(&C.a_in);
+      mbar_arrive_expect_tx(ab, a_bytes);
+      for (int j = 0; j < nslab; ++j)
+        tma_load_2d(sbase + p.off_a + j * p.rb * 128, &maps.a, c0 * kChunkK + 64 * j, 0, ab);
+    }
+    tma_prefetch_desc(&maps.x);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&C.tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_arrive();  // phase 1: this CTA's barriers are initialised
+  const uint32_t tmem = C.tmem_base;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      pdl_wait();  // x may come from the preceding kernel
+      const uint32_t xb = smem_u32(&C.x_in);
+      mbar_arrive_expect_tx(xb, x_bytes);
+      for (int j = 0; j < nslab; ++j) tma_load_2d(sbase + p.off_x + j * N * 128, &maps.x, c0 * kChunkK + 64 * j, 0, xb);
+      // every copy lands before the stage region is handed to the peers (phase 2)
+      for (int c = 0; c < nch; ++c) drain(smem_u32(&C.wfull[c]), 0);
+      if (lora) drain(smem_u32(&C.a_in), 0);
+      drain(xb, 0);
+    }
+    __syncwarp();
+    cluster_wait();
+    cluster_arrive();
+    cluster_wait();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t id1 = idesc_f16(kTileO, N, 0), idt = idesc_f16(kTileO, lora ? p.rb : 16, 0);
+      bool ok = wait_f(smem_u32(&C.act_ready), 0, abort_flag);
+      for (int c = 0; c < nch && ok; ++c) {
+        ok = wait_f(smem_u32(&C.a_full[c]), 0, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kChunkK / 16; ++kk) {
+          const int slab = 4 * c + (kk >> 2);
+          const uint64_t xdesc = smem_desc_sw128(sbase + p.off_x + slab * N * 128 + (kk & 3) * 32, 1024);
+          mma_ts(tmem + kColD1, tmem + 128u * c + kk * 8, xdesc, id1, (c > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (lora) {
+          // A operand: 128 rows of u (rows >= N read bytes of the following slabs and
+          // regions, inside this CTA's allocation; they only feed unread lanes)
+#pragma unroll
+          for (int kk = 0; kk < kChunkK / 16; ++kk) {
+            const int slab = 4 * c + (kk >> 2);
+            const uint64_t xdesc = smem_desc_sw128(sbase + p.off_x + slab * N * 128 + (kk & 3) * 32, 1024);
+            const uint64_t adesc = smem_desc_sw128(sbase + p.off_a + slab * p.rb * 128 + (kk & 3) * 32, 1024);
+            mma_ss(tmem + kColDt, xdesc, adesc, idt, (c > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+      }
+      tc_commit(smem_u32(&C.d_full));  // also reached on abort: tracks every MMA issued
+    }
+    __syncwarp();
+    cluster_wait();
+    cluster_arrive();
+    cluster_wait();
+  } else if (warp >= kConvWarp0) {
+    // ---------------------------------------------------------------- activations
+    const int ct = threadIdx.x - kConvWarp0 * 32;  // 0 .. 127
+    float* gsh = reinterpret_cast<float*>(smem + p.off_g);
+    float* bt = reinterpret_cast<float*>(smem + p.off_bt);  // [j][rows_max]: B of the owned rows
+    float* qrecv = reinterpret_cast<float*>(smem + p.off_q);  // [S][N]: sums of x^2 of every split
+    if (lora) {
+      for (int i = ct; i < rows_own * p.r; i += kConvThreads) {
+        const int rl = i / p.r, j = i % p.r;
+        const int64_t o = static_cast<int64_t>(row0) + R0 + rl;
+        bt[j * p.rows_max + rl] = o < p.d_o ? __bfloat162float(p.B[o * p.r + j]) : 0.f;
+      }
+    }
+    pdl_wait();  // w_norm, z and x may come from the preceding kernel
+    const int klen = nch * kChunkK;
+    const int64_t k0 = static_cast<int64_t>(c0) * kChunkK;
+    for (int k4 = ct; k4 < klen / 4; k4 += kConvThreads) {
+      float4 g = make_float4(1.f, 1.f, 1.f, 1.f);
+      if (norm) {
+        g = reinterpret_cast<const float4*>(p.w_norm + k0)[k4];
+        if (p.z) {
+          const float4 zz = reinterpret_cast<const float4*>(p.z + k0)[k4];
+          g.x += zz.x; g.y += zz.y; g.z += zz.z; g.w += zz.w;
+        }
+      }
+      reinterpret_cast<float4*>(gsh)[k4] = g;
+    }
+    named_bar(2, kConvThreads);
+    bool ok = true;
+    if (lora) {
+      ok = wait_f(smem_u32(&C.a_in), 0, abort_flag);
+      uint4* a4 = reinterpret_cast<uint4*>(smem + p.off_a);
+      for (int i = ct; ok && i < static_cast<int>(a_bytes / 16); i += kConvThreads) {
+        const uint4 v = a4[i];
+        a4[i] = make_uint4(f32x2_to_f16x2(bf16lo_to_f32(v.x), bf16hi_to_f32(v.x)),
+                           f32x2_to_f16x2(bf16lo_to_f32(v.y), bf16hi_to_f32(v.y)),
+                           f32x2_to_f16x2(bf16lo_to_f32(v.z), bf16hi_to_f32(v.z)),
+                           f32x2_to_f16x2(bf16lo_to_f32(v.w), bf16hi_to_f32(v.w)));
+      }
+    }
+    ok = ok && wait_f(smem_u32(&C.x_in), 0, abort_flag);
+    // token row n = ct / tpr; the tpr threads of a row are neighbouring lanes
+    const int np2 = N <= 16 ? 16 : (N <= 32 ? 32 : 64);
+    const int tpr = kConvThreads / np2, n = ct / tpr, part = ct % tpr;
+    const int nq = nch * 32;  // 16-byte pieces of one row
+    float ss = 0.f, mx = 0.f;
+    if (ok && n < N) {
+      for (int q = part; q < nq; q += tpr) {
+        const int slab = q >> 3, ch = q & 7;
+        const uint4 v = *reinterpret_cast<const uint4*>(smem + p.off_x + slab * N * 128 + n * 128 + ((ch ^ (n & 7)) << 4));
+        const float4 ga = reinterpret_cast<const float4*>(gsh)[(slab * 64 + ch * 8) / 4];
+        const float4 gb = reinterpret_cast<const float4*>(gsh)[(slab * 64 + ch * 8) / 4 + 1];
+        const float xv[8] = {bf16lo_to_f32(v.x), bf16hi_to_f32(v.x), bf16lo_to_f32(v.y), bf16hi_to_f32(v.y),
+                             bf16lo_to_f32(v.z), bf16hi_to_f32(v.z), bf16lo_to_f32(v.w), bf16hi_to_f32(v.w)};
+        const float gv[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          ss = fmaf(xv[i], xv[i], ss);
+          mx = fmaxf(mx, fabsf(xv[i] * gv[i]));
+        }
+      }
+    }
+    for (int o = tpr / 2; o > 0; o >>= 1) {
+      ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    }
+    int e = mx > 0.f ? 13 - ilogbf(mx) : 0;  // max |u| c in [2^13, 2^14)
+    e = e < -100 ? -100 : (e > 100 ? 100 : e);
+    const float cs = ldexpf(1.0f, e);
+    if (ok && n < N) {
+      for (int q = part; q < nq; q += tpr) {
+        const int slab = q >> 3, ch = q & 7;
+        uint4* pv = reinterpret_cast<uint4*>(smem + p.off_x + slab * N * 128 + n * 128 + ((ch ^ (n & 7)) << 4));
+        const uint4 v = *pv;
+        const float4 ga = reinterpret_cast<const float4*>(gsh)[(slab * 64 + ch * 8) / 4];
+        const float4 gb = reinterpret_cast<const float4*>(gsh)[(slab * 64 + ch * 8) / 4 + 1];
+        *pv = make_uint4(f32x2_to_f16x2(bf16lo_to_f32(v.x) * ga.x * cs, bf16hi_to_f32(v.x) * ga.y * cs),
+                         f32x2_to_f16x2(bf16lo_to_f32(v.y) * ga.z * cs, bf16hi_to_f32(v.y) * ga.w * cs),
+                         f32x2_to_f16x2(bf16lo_to_f32(v.z) * gb.x * cs, bf16hi_to_f32(v.z) * gb.y * cs),
+                         f32x2_to_f16x2(bf16lo_to_f32(v.w) * gb.z * cs, bf16hi_to_f32(v.w) * gb.w * cs));
+      }
+      if (part == 0) {
+        C.cinv[n] = ldexpf(1.0f, -e);
+        if (norm) qrecv[me * N + n] = ss;
+      }
+    }
+    fence_proxy_async_smem();  // the f16 operands are read by the tensor cores
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&C.act_ready));
+    cluster_wait();  // phase 1: every peer's barriers exist
+    if (norm && n < N && part == 0) {
+      for (int d = 1; d < S; ++d) {
+        const uint32_t dst = static_cast<uint32_t>((me + d) % S);
+        st_async_f32(mapa_shared(smem_u32(&qrecv[me * N + n]), dst), ss, mapa_shared(smem_u32(&C.recv), dst));
+      }
+    }
+    cluster_arrive();
+    cluster_wait();
+  } else {
+    // ---------------------------------------------------------------- dequant + epilogue
+    const int dw = warp - 2;              // 0..7
+    const int quarter = warp & 3;         // tensor-memory lane quarter of this warp
+    const int g = dw >> 2;                // K half of each chunk
+    const int row = quarter * 32 + lane;  // weight row within the tile
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    const int et = threadIdx.x - 64;      // 0 .. 255
+    bool ok = true;
+    for (int c = 0; c < nch; ++c) {
+      ok = wait_f(smem_u32(&C.wfull[c]), 0, abort_flag);
+      if (!ok) break;
+      const uint8_t* crow = smem + c * kCodesBytes + row * 128;
+      const uint2 sc8 = *reinterpret_cast<const uint2*>(smem + p.off_scales + c * kScaleBytes + row * 16 + g * 8);
+      const uint32_t sc_words[2] = {sc8.x, sc8.y};
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int j = 4 * g + jj;  // 16-byte piece of the row (32 codes, 2 scale blocks)
+        const uint4 cw = *reinterpret_cast<const uint4*>(crow + ((j ^ (row & 7)) << 4));
+        const uint32_t sbytes = (sc_words[jj >> 1] >> (16 * (jj & 1))) & 0xFFFFu;
+        const uint32_t s2 = cvt_e4m3x2_to_f16x2(sbytes);
+        const uint32_t sa = prmt(s2, s2, 0x1010u), sb = prmt(s2, s2, 0x3232u);
+        uint32_t v[16];
+        e2m1x8_to_f16x8(cw.x, v[0], v[1], v[2], v[3]);
+        e2m1x8_to_f16x8(cw.y, v[4], v[5], v[6], v[7]);
+        e2m1x8_to_f16x8(cw.z, v[8], v[9], v[10], v[11]);
+        e2m1x8_to_f16x8(cw.w, v[12], v[13], v[14], v[15]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = hmul2_u32(v[i], sa);
+#pragma unroll
+        for (int i = 8; i < 16; ++i) v[i] = hmul2_u32(v[i], sb);
+        tmem_st16(tmem + lane_addr + 128u * c + j * 16, v);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&C.a_full[c]));
+    }
+    // ---------------------------------------------------------------- epilogue: gather
+    ok = wait_f(smem_u32(&C.d_full), 0, abort_flag) && ok;
+    tc_fence_after();
+    const int half = N / 2, n0 = g * half;  // tokens [n0, n0 + half) of D1 for this thread
+    const int thalf = p.rb / 2, j0 = g * thalf;
+    const bool trow = lora && quarter * 32 < N && quarter < 2;  // lanes 0..63: token rows of Dt^T
+    uint32_t d1[32], dt[32];
+#pragma unroll
+    for (int cb = 0; cb < 4; ++cb) {
+      if (cb * 8 < half) tmem_ld8(tmem + lane_addr + kColD1 + n0 + cb * 8, &d1[cb * 8]);
+      if (trow && cb * 8 < thalf) tmem_ld8(tmem + lane_addr + kColDt + j0 + cb * 8, &dt[cb * 8]);
+    }
+    tmem_ld_wait();
+    const bool good = ok && !*abort_flag;
+    cluster_wait();
+    cluster_arrive();  // phase 2: this CTA no longer reads its stage region
+    cluster_wait();
+    // ---------------------------------------------------------------- epilogue: exchange
+    const uint32_t recv_bar = smem_u32(&C.recv);
+    const float s_g = C.s_g;
+    {
+      int o = S - 1;
+      while (o > 0 && owner_row0(o, S) > row) --o;
+      const int rl = row - owner_row0(o, S);
+      const uint32_t dst = smem_u32(smem) + static_cast<uint32_t>(((me * p.rows_max + rl) * p.Np + n0) * 4);
+      const uint32_t rdst = mapa_shared(dst, static_cast<uint32_t>(o)), rbar = mapa_shared(recv_bar, o);
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        if (i < half) {
+          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (good)
+            v = make_float4(s_g * C.cinv[n0 + i] * __uint_as_float(d1[i]),
+                            s_g * C.cinv[n0 + i + 1] * __uint_as_float(d1[i + 1]),
+                            s_g * C.cinv[n0 + i + 2] * __uint_as_float(d1[i + 2]),
+                            s_g * C.cinv[n0 + i + 3] * __uint_as_float(d1[i + 3]));
+          if (o == me) *reinterpret_cast<float4*>(smem + (dst - smem_u32(smem)) + 4 * i) = v;
+          else st_async_f32x4(rdst + 4 * i, v, rbar);
+        }
+      }
+    }
+    if (trow && quarter * 32 + lane < N) {
+      const int n = quarter * 32 + lane;
+      const float ci = C.cinv[n];
+      const uint32_t dst = smem_u32(smem) + p.off_rt + static_cast<uint32_t>(((me * N + n) * p.rb + j0) * 4);
+      for (int d = 0; d < S; ++d) {
+        const int o = (me + d) % S;
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          if (i < thalf) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (good)
+              v = make_float4(ci * __uint_as_float(dt[i]), ci * __uint_as_float(dt[i + 1]),
+                              ci * __uint_as_float(dt[i + 2]), ci * __uint_as_float(dt[i + 3]));
+            if (o == me) *reinterpret_cast<float4*>(smem + (dst - smem_u32(smem)) + 4 * i) = v;
+            else st_async_f32x4(mapa_shared(dst + 4 * i, o), v, mapa_shared(recv_bar, o));
+          }
+        }
+      }
+    }
+    if (et == 0) {
+      const uint32_t per_peer = static_cast<uint32_t>(rows_own * N * 4 + (lora ? N * p.rb * 4 : 0) + (norm ? N * 4 : 0));
+      mbar_arrive_expect_tx(recv_bar, per_peer * static_cast<uint32_t>(S - 1));
+    }
+    named_bar(1, kEpiThreads);  // this CTA's own shares are in place
+    ok = wait_f(recv_bar, 0, abort_flag) && good;
+    // ---------------------------------------------------------------- epilogue: combine
+    const float* qrecv = reinterpret_cast<const float*>(smem + p.off_q);
+    const float* rt = reinterpret_cast<const float*>(smem + p.off_rt);
+    float* ts = reinterpret_cast<float*>(smem + p.off_ts);  // [N][rb + 4]: lambda t
+    const int tstr = p.rb + 4;
+    if (et < N) {
+      float rs = 1.f;
+      if (norm) {
+        float tot = 0.f;
+        for (int s = 0; s < S; ++s) tot += qrecv[s * N + et];
+        rs = 1.0f / sqrtf(tot / static_cast<float>(p.d_i) + p.eps);
+      }
+      C.rs[et] = rs;
+    }
+    if (lora) {
+      for (int i = et; i < N * p.rb; i += kEpiThreads) {
+        const int n = i / p.rb, j = i % p.rb;
+        float acc = 0.f;
+        for (int s = 0; s < S; ++s) acc += rt[(s * N + n) * p.rb + j];
+        ts[n * tstr + j] = p.lambda * acc;
+      }
+    }
+    named_bar(1, kEpiThreads);
+    if (ok) {
+      const float* rp = reinterpret_cast<const float*>(smem);
+      const float* bt = reinterpret_cast<const float*>(smem + p.off_bt);
+      const int mq = static_cast<int>((p.M + 3) / 4);
+      const int items = rows_own * mq;
+      for (int e = et; e < items; e += kEpiThreads) {
+        const int rl = e % rows_own, n4 = 4 * (e / rows_own);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int s = 0; s < S; ++s) {
+          const float4 v = *reinterpret_cast<const float4*>(rp + (s * p.rows_max + rl) * p.Np + n4);
+          acc[0] += v.x; acc[1] += v.y; acc[2] += v.z; acc[3] += v.w;
+        }
+        if (lora) {
+          float l[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int j = 0; j < p.r; j += 4) {
+            const float b0 = bt[j * p.rows_max + rl];
+            const float b1 = j + 1 < p.r ? bt[(j + 1) * p.rows_max + rl] : 0.f;
+            const float b2 = j + 2 < p.r ? bt[(j + 2) * p.rows_max + rl] : 0.f;
+            const float b3 = j + 3 < p.r ? bt[(j + 3) * p.rows_max + rl] : 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float4 t = *reinterpret_cast<const float4*>(ts + (n4 + q) * tstr + j);
+              l[q] = fmaf(b0, t.x, fmaf(b1, t.y, fmaf(b2, t.z, fmaf(b3, t.w, l[q]))));
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[q] += l[q];
+        }
+        const int64_t oo = static_cast<int64_t>(row0) + R0 + rl;
+        if (oo < p.d_o) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int n = n4 + q;
+            if (n < p.M) {
+              const float v = C.rs[n] * acc[q];
+              if (p.y_f32) static_cast<float*>(p.y)[n * p.d_o + oo] = v;
+              else static_cast<__nv_bfloat16*>(p.y)[n * p.d_o + oo] = __float2bfloat16_rn(v);
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void* base, uint64_t inner,
+               uint64_t outer, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  auto fn = get_encode();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * esize};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct FPlan {
+  int N, Np, rb, S, kc, tiles, rows_max, nchmax;
+  uint32_t off_scales, off_x, off_a, off_g, off_bt, off_q, off_ctrl, off_rt, off_ts;
+  size_t smem;
+};
+
+uint32_t al1k(size_t v) { return static_cast<uint32_t>(align_up(v, 1024)); }
+
+// Shared-memory layout for S splits; false if it does not fit.
+bool layout(FPlan& f, int r) {
+  const int nslab = f.nchmax * 4;
+  f.off_scales = static_cast<uint32_t>(f.nchmax * kCodesBytes);
+  f.off_x = al1k(f.off_scales + static_cast<size_t>(f.nchmax) * kScaleBytes);
+  f.off_a = al1k(f.off_x + static_cast<size_t>(nslab) * f.N * 128);
+  f.off_g = al1k(f.off_a + static_cast<size_t>(nslab) * f.rb * 128);
+  f.off_bt = f.off_g + f.nchmax * kChunkK * 4;
+  f.off_q = f.off_bt + static_cast<uint32_t>(align_up(static_cast<size_t>(r > 0 ? r : 1) * f.rows_max * 4, 16));
+  f.off_ctrl = f.off_q + static_cast<uint32_t>(align_up(static_cast<size_t>(f.S) * f.N * 4, 16));
+  f.off_ctrl = static_cast<uint32_t>(align_up(f.off_ctrl, 128));
+  size_t end = f.off_ctrl + sizeof(Ctrl);
+  // the LoRA-down MMA reads 128 rows of every u slab (rows >= N are don't-care)
+  const size_t read_end = f.off_x + static_cast<size_t>(nslab - 1) * f.N * 128 + 128 * 128;
+  if (end < read_end) end = read_end;
+  f.smem = end + 1024;  // alignment slack
+  if (f.smem < kMinSmem) f.smem = kMinSmem;
+  // receive buffers over the dead stages: P [S][rows_max][Np], T [S][N][rb], lambda t [N][rb + 4]
+  f.off_rt = static_cast<uint32_t>(align_up(static_cast<size_t>(f.S) * f.rows_max * f.Np * 4, 16));
+  f.off_ts = f.off_rt + static_cast<uint32_t>(static_cast<size_t>(f.S) * f.N * f.rb * 4);
+  const size_t alias_end = f.off_ts + static_cast<size_t>(f.N) * (f.rb + 4) * 4;
+  return f.smem <= 227 * 1024 && alias_end <= f.off_g;
+}
+
+int max_active_clusters(size_t smem, int cs) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(cs * 64));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = static_cast<unsigned>(cs);
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k_fused_decode, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  return n;
+}
+
+cudaError_t set_attributes() {
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    err = cudaFuncSetAttribute(k_fused_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  });
+  return err;
+}
+
+// Split count S: the largest (at most 8) for which the grid is one wave on the SMs,
+// every CTA's slice is at most 3 chunks, shared memory fits and all clusters can be
+// resident at once; none -> this path does not apply.
+bool make_plan(int64_t M, int64_t d_i, int64_t d_o, int r, FPlan& out) {
+  if (M < 1 || M > kMaxN || d_i < kChunkK || d_i % kChunkK != 0 || r < 0 || r > kMaxR || d_o < 1) return false;
+  FPlan f{};
+  f.N = static_cast<int>((M + 15) / 16 * 16);
+  f.Np = f.N + 4;
+  f.rb = r > 0 ? (r + 15) / 16 * 16 : 16;
+  f.kc = static_cast<int>(d_i / kChunkK);
+  const int64_t tiles = (d_o + kTileO - 1) / kTileO;
+  if (tiles > 4096) return false;
+  f.tiles = static_cast<int>(tiles);
+  if (set_attributes() != cudaSuccess) return false;
+  const int smin = (f.kc + kMaxChunks - 1) / kMaxChunks;
+  const int smax = f.kc < kMaxSplit ? f.kc : kMaxSplit;
+  for (int S = smax; S >= smin; --S) {
+    if (static_cast<int64_t>(f.tiles) * S > sm_count()) continue;
+    FPlan g = f;
+    g.S = S;
+    g.nchmax = (f.kc + S - 1) / S;
+    g.rows_max = (kTileO + S - 1) / S;
+    if (!layout(g, r)) continue;
+    if (max_active_clusters(g.smem, S) < f.tiles) continue;
+    out = g;
+    return true;
+  }
+  return false;
+}
+
+struct PlanKey {
+  int64_t M, d_i, d_o;
+  int r;
+  int dev;
+};
+struct PlanEntry {
+  PlanKey k;
+  bool ok;
+  FPlan f;
+};
+
+bool cached_plan(int64_t M, int64_t d_i, int64_t d_o, int r, FPlan& out) {
+  static std::mutex mu;
+  static PlanEntry cache[64];
+  static int used = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lk(mu);
+  for (int i = 0; i < used; ++i) {
+    const PlanKey& k = cache[i].k;
+    if (k.M == M && k.d_i == d_i && k.d_o == d_o && k.r == r && k.dev == dev) {
+      out = cache[i].f;
+      return cache[i].ok;
+    }
+  }
+  FPlan f{};
+  const bool ok = make_plan(M, d_i, d_o, r, f);
+  PlanEntry& e = cache[used < 64 ? used++ : (used = 1, 0)];
+  e.k = PlanKey{M, d_i, d_o, r, dev};
+  e.ok = ok;
+  e.f = f;
+  out = f;
+  return ok;
+}
+
+}  // namespace
+
+bool fused_supported(int64_t M, int64_t d_i, int64_t d_o, int r) {
+  FPlan f;
+  return cached_plan(M, d_i, d_o, r, f);
+}
+
+cudaError_t launch_linear_fused(const LinearArgs& a, cudaStream_t stream) {
+  FPlan f;
+  if (!cached_plan(a.M, a.d_i, a.d_o, a.r, f)) return cudaErrorInvalidValue;
+  FMaps maps;
+  bool ok = encode_2d(&maps.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.codes, a.d_i / 2, a.d_o, 128, kTileO,
+                      CU_TENSOR_MAP_SWIZZLE_128B) &&
+            encode_2d(&maps.scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.scales, a.d_i / 16, a.d_o, 16, kTileO,
+                      CU_TENSOR_MAP_SWIZZLE_NONE) &&
+            encode_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.x, a.d_i, a.M, 64, f.N,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+  if (ok && a.r > 0)
+    ok = encode_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.A, a.d_i, a.r, 64, f.rb,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+  else
+    maps.a = maps.x;  // unused
+  if (!ok) return cudaErrorInvalidValue;
+
+  FParams p{};
+  p.M = a.M;
+  p.d_i = a.d_i;
+  p.d_o = a.d_o;
+  p.N = f.N;
+  p.Np = f.Np;
+  p.rb = f.rb;
+  p.r = a.r;
+  p.S = f.S;
+  p.kc = f.kc;
+  p.rows_max = f.rows_max;
+  p.lambda = a.lambda;
+  p.eps = a.eps;
+  p.s_g = a.s_g;
+  p.w_norm = a.w_norm;
+  p.z = a.z;
+  p.B = static_cast<const __nv_bfloat16*>(a.B);
+  p.y = a.y;
+  p.y_f32 = a.y_f32 ? 1 : 0;
+  p.off_scales = f.off_scales;
+  p.off_x = f.off_x;
+  p.off_a = f.off_a;
+  p.off_g = f.off_g;
+  p.off_bt = f.off_bt;
+  p.off_q = f.off_q;
+  p.off_ctrl = f.off_ctrl;
+  p.off_rt = f.off_rt;
+  p.off_ts = f.off_ts;
+
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  attrs[1].id = cudaLaunchAttributeClusterDimension;
+  attrs[1].val.clusterDim.x = static_cast<unsigned>(f.S);
+  attrs[1].val.clusterDim.y = 1;
+  attrs[1].val.clusterDim.z = 1;
+  cudaLaunchConfig_t c{};
+  c.gridDim = dim3(static_cast<unsigned>(f.tiles * f.S));
+  c.blockDim = dim3(kThreads);
+  c.dynamicSmemBytes = f.smem;
+  c.stream = stream;
+  c.attrs = attrs;
+  c.numAttrs = 2;
+  return cudaLaunchKernelEx(&c, k_fused_decode, maps, p);
+}
+
+uint32_t fused_read_and_clear_status() {
+  uint32_t v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_fused_status, sizeof(v)) != cudaSuccess) return 0;
+  if (v) cudaMemcpyToSymbol(g_fused_status, &zero, sizeof(zero));
+  return v;
+}
+
+}  // namespace pl
