@@ -82,6 +82,15 @@ PL_DEVINL bool mbar_try_wait(uint32_t bar, uint32_t parity) {
                "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
   return ok != 0;
 }
+// Same test, but the thread may be suspended in hardware (until the phase completes
+// or about `hint_ns` pass) instead of spinning: waiting warps then take no issue slots
+// from the warps that do the work.
+PL_DEVINL bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(ok) : "r"(bar), "r"(parity), "r"(hint_ns) : "memory");
+  return ok != 0;
+}
 // Wait for phase `parity` of a barrier, giving up after kWaitLimitNs.  Returns
 // false on time-out.  Every wait in every kernel goes through this.
 constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;  // 200 ms
@@ -243,15 +252,13 @@ PL_DEVINL float4 ld_dsmem_f32x4(uint32_t addr) {
 PL_DEVINL bool wait_or_abort_status(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
-        atomicOr(status, kStatusTimeout);
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;  // <= ~0.1 ms asleep per round
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      atomicOr(status, kStatusTimeout);
+      return false;
     }
   }
 }

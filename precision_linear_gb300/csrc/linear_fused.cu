@@ -18,15 +18,20 @@
 // Roles (14 warps):
 //   warp 0       TMA: the CTA's codes and E4M3 scales and the LoRA A slice at once
 //                (weights; they do not depend on the preceding kernel), then, after
-//                the programmatic-dependent-launch wait, the x slice;
-//   warps 10-13  B rows of the CTA's output share into shared memory; after the wait
-//                w_norm + z; A bf16 -> f16 in place; x: sum of squares and max |u| per
-//                token row, then u c -> f16 in place; the row sums go to every CTA of
-//                the cluster;
-//   warps 2-9    dequantise every chunk into tensor memory (E2M1 -> f16 conversion,
-//                times the block scale: exact in f16), then the epilogue;
-//   warp 1       tcgen05.mma kind::f16: D1 += W_hat/s_g (tensor memory) x u^T and
-//                Dt^T += u x A^T (both from shared memory), accumulators in tensor memory.
+//                the programmatic-dependent-launch wait, the x slice and the w_norm
+//                and z slices;
+//   warps 10-13  B rows of the CTA's output share into shared memory; w_norm + z;
+//                A bf16 -> f16 in place; token rows of x from a shared queue (sum of
+//                squares and max |u| of the row, then u c -> f16 in place; the row
+//                sums go to every CTA of the cluster); then lane 0 of each issues
+//                tcgen05.mma kind::f16 into its own accumulator (a single issuing
+//                thread is latency-bound on these small MMAs): D1 += W_hat/s_g (tensor
+//                memory) x u^T over even / odd K steps, and Dt^T += u x A^T (shared
+//                memory) over even / odd K steps;
+//   warps 2-9    dequantise chunks into two tensor-memory buffers (E2M1 -> f16
+//                conversion, times the block scale: exact in f16), take token rows
+//                from the queue when the second buffer is full, then the epilogue;
+//   warp 1       tensor-memory allocation.
 // Epilogue: each CTA sends, with st.async into its peers' shared memory, the rows of
 // s_g / c D1 that each peer owns (peer p owns rows [128 p / S, 128 (p+1) / S)) and its
 // whole t slice Dt^T / c to every peer.  Each CTA sums what it owns in split order
@@ -46,6 +51,14 @@ namespace pl {
 
 __device__ uint32_t g_fused_status = 0;
 
+// Phase timestamps for development builds (-DPL_TIMELINE); compiled out otherwise.
+#ifdef PL_TIMELINE
+__device__ unsigned long long g_tl_fused[1024][64];
+#define PL_TLF(slot) do { if (blockIdx.x < 1024) g_tl_fused[blockIdx.x][slot] = globaltimer_ns(); } while (0)
+#else
+#define PL_TLF(slot) do { } while (0)
+#endif
+
 namespace {
 
 constexpr int kTileO = 128;
@@ -63,14 +76,12 @@ constexpr int kEpiThreads = kDeqWarps * 32;
 constexpr int kThreads = (2 + kDeqWarps + kConvWarps) * 32;  // 448
 constexpr int kConvWarp0 = 2 + kDeqWarps;                    // first conversion warp
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColD1 = 384;  // A buffers: chunk c at columns [128 c, 128 c + 128)
-constexpr uint32_t kColDt = 448;
 constexpr size_t kMinSmem = 120 * 1024;  // > half an SM: one CTA per SM, so its 512 TMEM columns are free
 
 struct FParams {
   int64_t M, d_i, d_o;
-  int N, Np, rb, r, S, kc, rows_max;
-  float lambda, eps;
+  int N, Np, Mp, rb, r, S, kc, rows_max, nbuf;
+  float lambda, eps, inv_d;
   const float* s_g;
   const float* w_norm;
   const float* z;
@@ -78,7 +89,7 @@ struct FParams {
   void* y;
   int y_f32;
   // shared-memory layout (byte offsets from the 1 KB-aligned base)
-  uint32_t off_scales, off_x, off_a, off_g, off_bt, off_q, off_ctrl;
+  uint32_t off_scales, off_x, off_a, off_gw, off_gz, off_bt, off_q, off_ctrl;
   uint32_t off_rt, off_ts;  // receive buffers, over the dead stage region (receive P at 0)
 };
 
@@ -87,19 +98,28 @@ struct FMaps {
 };
 
 struct Ctrl {
-  uint64_t wfull[kMaxChunks];
-  uint64_t a_in, x_in, act_ready;
-  uint64_t a_full[kMaxChunks];
-  uint64_t d_full, recv;
+  uint64_t wfull[kMaxChunks];  // codes + scales of chunk c landed
+  uint64_t a_full[kMaxChunks]; // chunk c dequantised into its tensor-memory buffer
+  uint64_t a_empty[kMaxChunks]; // the MMAs reading buffer b are done
+  uint64_t a_in, x_in, g_in;   // LoRA A slice, x slice, w_norm / z slices landed
+  uint64_t g_ready;            // w_norm + z formed
+  uint64_t act_ready;          // every token row converted
+  uint64_t d_full;             // every MMA done
+  uint64_t recv;               // the peers' shares arrived
   uint32_t tmem_base;
   int abort_flag;
+  int next_row;                // token-row queue of the conversion
   float s_g;
-  float cinv[kMaxN];  // 1 / c of this split, per token row
+  alignas(16) float cinv[kMaxN];  // 1 / c of this split, per token row
   float rs[kMaxN];
 };
 
-PL_DEVINL bool wait_f(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __noinline__ bool wait_f_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   return wait_or_abort_status(bar, parity, abort_flag, &g_fused_status);
+}
+// Bounded wait: the common case (already complete) inline, the polling loop out of line.
+PL_DEVINL bool wait_f(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  return mbar_try_wait(bar, parity) || wait_f_slow(bar, parity, abort_flag);
 }
 PL_DEVINL uint32_t cluster_rank() {
   uint32_t r;
@@ -109,7 +129,7 @@ PL_DEVINL uint32_t cluster_rank() {
 PL_DEVINL void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
 PL_DEVINL void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 PL_DEVINL void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-// 16 bytes into a peer's shared memory, completing `bytes` of its mbarrier's transaction.
+// 16 bytes into a peer's shared memory, completing 16 bytes of its mbarrier's transaction.
 PL_DEVINL void st_async_f32x4(uint32_t addr, float4 v, uint32_t bar) {
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
                :: "r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar) : "memory");
@@ -118,8 +138,111 @@ PL_DEVINL void st_async_f32(uint32_t addr, float v, uint32_t bar) {
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
                :: "r"(addr), "r"(__float_as_uint(v)), "r"(bar) : "memory");
 }
+// One contiguous global -> shared copy (16-byte aligned, size a multiple of 16).
+PL_DEVINL void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
 // First weight row of the share that CTA `s` of the cluster owns.
 PL_DEVINL int owner_row0(int s, int S) { return (s * kTileO) / S; }
+
+// Token rows of x (one warp): sum of squares and max |u| over this CTA's slice, then
+// u c -> f16 in place.  Rows come from a queue shared by the conversion and dequant
+// warps, 32 / L at a time: lanes L i .. L i + L - 1 take row base + i, lane L i + l the
+// 16-byte pieces l, l + L, ... of the row (piece q: slab q / 8, column q % 8).  L is 32
+// for few rows (short chains per lane), 8 for many (more rows in flight).  Out of line:
+// it is called from two roles.
+__device__ __noinline__ void convert_rows_warp(uint8_t* smem, uint32_t off_x, const float* gsh, float* qrecv, Ctrl* C,
+                                               int N, int nslab, int M, int S, int me, bool norm,
+                                               volatile int* abort_flag) {
+  const int L = M <= 12 ? 32 : (M <= 24 ? 16 : 8);
+  const int lane = threadIdx.x & 31, gi = lane / L, sl = lane % L, step = 32 / L;
+  const int npieces = nslab * 8;
+  const uint32_t recv_bar = smem_u32(&C->recv);
+  for (;;) {
+    int base = 0;
+    if (lane == 0) base = atomicAdd(&C->next_row, step);
+    base = __shfl_sync(0xFFFFFFFFu, base, 0);
+    if (base >= M || *abort_flag) break;
+    const int n = base + gi;
+    const bool live = n < M;
+    uint8_t* rowp = smem + off_x + n * 128;
+    const float4* g4 = reinterpret_cast<const float4*>(gsh);
+    float ss = 0.f, mx = 0.f;
+    if (live) {
+#pragma unroll 2
+      for (int q = sl; q < npieces; q += L) {
+        const int slab = q >> 3, ch = q & 7;
+        const uint4 v = *reinterpret_cast<const uint4*>(rowp + slab * N * 128 + ((ch ^ (n & 7)) << 4));
+        float4 ga = make_float4(1.f, 1.f, 1.f, 1.f), gb = ga;
+        if (norm) {
+          ga = g4[slab * 16 + ch * 2];
+          gb = g4[slab * 16 + ch * 2 + 1];
+        }
+        const float x0 = bf16lo_to_f32(v.x), x1 = bf16hi_to_f32(v.x), x2 = bf16lo_to_f32(v.y), x3 = bf16hi_to_f32(v.y);
+        const float x4 = bf16lo_to_f32(v.z), x5 = bf16hi_to_f32(v.z), x6 = bf16lo_to_f32(v.w), x7 = bf16hi_to_f32(v.w);
+        ss = fmaf(x0, x0, fmaf(x1, x1, fmaf(x2, x2, fmaf(x3, x3, ss))));
+        ss = fmaf(x4, x4, fmaf(x5, x5, fmaf(x6, x6, fmaf(x7, x7, ss))));
+        mx = fmaxf(fmaxf(fmaxf(fabsf(x0 * ga.x), fabsf(x1 * ga.y)), fmaxf(fabsf(x2 * ga.z), fabsf(x3 * ga.w))),
+                   fmaxf(fmaxf(fabsf(x4 * gb.x), fabsf(x5 * gb.y)), fmaxf(fabsf(x6 * gb.z), fmaxf(fabsf(x7 * gb.w), mx))));
+      }
+    }
+    for (int o = L / 2; o > 0; o >>= 1) {
+      ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    }
+    // c = 2^e with max |u| c in [2^13, 2^14): e from the exponent field of max |u|
+    const int ex = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu) - 127;
+    int e = mx > 0.f ? 13 - ex : 0;
+    e = e < -100 ? -100 : (e > 100 ? 100 : e);
+    const float cs = __int_as_float((127 + e) << 23);
+    if (live) {
+#pragma unroll 2
+      for (int q = sl; q < npieces; q += L) {
+        const int slab = q >> 3, ch = q & 7;
+        uint4* pv = reinterpret_cast<uint4*>(rowp + slab * N * 128 + ((ch ^ (n & 7)) << 4));
+        const uint4 v = *pv;
+        float4 ga = make_float4(cs, cs, cs, cs), gb = ga;
+        if (norm) {
+          ga = g4[slab * 16 + ch * 2];
+          gb = g4[slab * 16 + ch * 2 + 1];
+          ga.x *= cs; ga.y *= cs; ga.z *= cs; ga.w *= cs;
+          gb.x *= cs; gb.y *= cs; gb.z *= cs; gb.w *= cs;
+        }
+        *pv = make_uint4(f32x2_to_f16x2(bf16lo_to_f32(v.x) * ga.x, bf16hi_to_f32(v.x) * ga.y),
+                         f32x2_to_f16x2(bf16lo_to_f32(v.y) * ga.z, bf16hi_to_f32(v.y) * ga.w),
+                         f32x2_to_f16x2(bf16lo_to_f32(v.z) * gb.x, bf16hi_to_f32(v.z) * gb.y),
+                         f32x2_to_f16x2(bf16lo_to_f32(v.w) * gb.z, bf16hi_to_f32(v.w) * gb.w));
+      }
+      if (sl == 0) {
+        C->cinv[n] = __int_as_float((127 - e) << 23);
+        if (norm) qrecv[me * N + n] = ss;
+      } else if (norm && sl < S) {  // the row's sum of squares to every peer
+        const uint32_t dst = static_cast<uint32_t>((me + sl) % S);
+        st_async_f32(mapa_shared(smem_u32(&qrecv[me * N + n]), dst), ss, mapa_shared(recv_bar, dst));
+      }
+    }
+  }
+  fence_proxy_async_smem();  // the f16 operands are read by the tensor cores
+  __syncwarp();
+  if (lane == 0) mbar_arrive(smem_u32(&C->act_ready));
+  if (lane == 0) PL_TLF(32 + (threadIdx.x >> 5));
+}
+
+// The staged LoRA A slice, bf16 -> f16 in place (16 bytes per step; `who` of `nthreads`).
+__device__ __noinline__ bool convert_a(uint8_t* a, uint32_t bytes, int who, int nthreads, uint32_t a_in,
+                                       volatile int* abort_flag) {
+  if (!wait_f(a_in, 0, abort_flag)) return false;
+  uint4* a4 = reinterpret_cast<uint4*>(a);
+  for (int i = who; i < static_cast<int>(bytes / 16); i += nthreads) {
+    const uint4 v = a4[i];
+    a4[i] = make_uint4(f32x2_to_f16x2(bf16lo_to_f32(v.x), bf16hi_to_f32(v.x)),
+                       f32x2_to_f16x2(bf16lo_to_f32(v.y), bf16hi_to_f32(v.y)),
+                       f32x2_to_f16x2(bf16lo_to_f32(v.z), bf16hi_to_f32(v.z)),
+                       f32x2_to_f16x2(bf16lo_to_f32(v.w), bf16hi_to_f32(v.w)));
+  }
+  return true;
+}
 
 __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_constant__ FMaps maps, const FParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -128,32 +251,39 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
   volatile int* abort_flag = &C.abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = p.S, N = p.N;
+  const int M = static_cast<int>(p.M);
   const int me = static_cast<int>(cluster_rank());
   const int tile = blockIdx.x / S;
   const int c0 = (me * p.kc) / S, c1 = ((me + 1) * p.kc) / S;
   const int nch = c1 - c0;
   const int nslab = nch * 4;  // 64-element k slabs of this CTA
-  const bool lora = p.r > 0, norm = p.w_norm != nullptr;
+  const bool lora = p.r > 0, norm = p.w_norm != nullptr, noise = norm && p.z != nullptr;
   const int R0 = owner_row0(me, S), rows_own = owner_row0(me + 1, S) - R0;
   const int32_t row0 = tile * kTileO;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t x_bytes = static_cast<uint32_t>(nslab) * N * 128u;
   const uint32_t a_bytes = static_cast<uint32_t>(nslab) * p.rb * 128u;
+  const uint32_t g_bytes = static_cast<uint32_t>(nch) * kChunkK * 4u;
+  const int nbuf = p.nbuf;  // tensor-memory weight buffers (2 or 3) of 128 columns
+  const uint32_t colD1a = 128u * nbuf, colD1b = colD1a + N, colDta = colD1a + 2 * N, colDtb = colDta + p.rb;
 
   if (threadIdx.x == 0) {
+    PL_TLF(0);
     pdl_launch_dependents();
     for (int c = 0; c < kMaxChunks; ++c) {
       mbar_init(smem_u32(&C.wfull[c]), 1);
       mbar_init(smem_u32(&C.a_full[c]), kDeqWarps);
     }
+    for (int b = 0; b < kMaxChunks; ++b) mbar_init(smem_u32(&C.a_empty[b]), kConvWarps);
     mbar_init(smem_u32(&C.a_in), 1);
     mbar_init(smem_u32(&C.x_in), 1);
-    mbar_init(smem_u32(&C.act_ready), kConvWarps);
-    mbar_init(smem_u32(&C.d_full), 1);
+    mbar_init(smem_u32(&C.g_in), 1);
+    mbar_init(smem_u32(&C.g_ready), kConvWarps);
+    mbar_init(smem_u32(&C.act_ready), kDeqWarps + kConvWarps + 1);  // + warp 1 (its share of A)
+    mbar_init(smem_u32(&C.d_full), kConvWarps);
     mbar_init(smem_u32(&C.recv), 1);
-    C.abort_flag = 0;
-    C.s_g = *p.s_g;  // a weight input: not written by the preceding kernel
     fence_mbar_init();
+    PL_TLF(16);
     const uint64_t pol = policy_evict_first();  // weights are streamed once
     for (int c = 0; c < nch; ++c) {
       const uint32_t wb = smem_u32(&C.wfull[c]);
@@ -162,6 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
       tma_load_2d_hint(sbase + p.off_scales + c * kScaleBytes, &maps.scales, (c0 + c) * (kChunkK / 16), row0, wb,
                        pol);
     }
+    PL_TLF(17);
     if (lora) {
       const uint32_t ab = smem_u32(&C.a_in);
       mbar_arrive_expect_tx(ab, a_bytes);
@@ -169,162 +300,157 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
         tma_load_2d(sbase + p.off_a + j * p.rb * 128, &maps.a, c0 * kChunkK + 64 * j, 0, ab);
     }
     tma_prefetch_desc(&maps.x);
+    C.abort_flag = 0;
+    C.next_row = 0;
+    PL_TLF(18);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&C.tmem_base), kTmemCols);
     tmem_relinquish();
+    if (lane == 0) PL_TLF(19);
   }
+  if (threadIdx.x >= 64 && threadIdx.x < 64 + kMaxN) C.cinv[threadIdx.x - 64] = 1.f;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  cluster_arrive();  // phase 1: this CTA's barriers are initialised
+  if (threadIdx.x == 0) PL_TLF(20);
+  // every CTA's barriers are initialised before any peer touches them (the init fence
+  // above orders the initialisation; the arrive itself need not)
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  cluster_wait();
   const uint32_t tmem = C.tmem_base;
+  if (threadIdx.x == 0) PL_TLF(1);
+
+  float* qrecv = reinterpret_cast<float*>(smem + p.off_q);  // [S][N]: sums of x^2 of every split
+  const float* gsh = reinterpret_cast<const float*>(smem + p.off_gw);
+
+  auto convert_rows = [&]() {
+    convert_rows_warp(smem, p.off_x, gsh, qrecv, &C, N, nslab, M, S, me, norm, abort_flag);
+  };
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
-      pdl_wait();  // x may come from the preceding kernel
+      pdl_wait();  // x, w_norm and z may come from the preceding kernel
+      PL_TLF(2);
       const uint32_t xb = smem_u32(&C.x_in);
       mbar_arrive_expect_tx(xb, x_bytes);
       for (int j = 0; j < nslab; ++j) tma_load_2d(sbase + p.off_x + j * N * 128, &maps.x, c0 * kChunkK + 64 * j, 0, xb);
-      // every copy lands before the stage region is handed to the peers (phase 2)
+      const int64_t k0 = static_cast<int64_t>(c0) * kChunkK;
+      if (norm) {
+        const uint32_t gb = smem_u32(&C.g_in);
+        mbar_arrive_expect_tx(gb, noise ? 2 * g_bytes : g_bytes);
+        bulk_g2s(sbase + p.off_gw, p.w_norm + k0, g_bytes, gb);
+        if (noise) bulk_g2s(sbase + p.off_gz, p.z + k0, g_bytes, gb);
+      }
+      // every copy lands before the stage region is handed to the peers
       for (int c = 0; c < nch; ++c) drain(smem_u32(&C.wfull[c]), 0);
       if (lora) drain(smem_u32(&C.a_in), 0);
+      if (norm) drain(smem_u32(&C.g_in), 0);
       drain(xb, 0);
     }
     __syncwarp();
-    cluster_wait();
     cluster_arrive();
     cluster_wait();
   } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t id1 = idesc_f16(kTileO, N, 0), idt = idesc_f16(kTileO, lora ? p.rb : 16, 0);
-      bool ok = wait_f(smem_u32(&C.act_ready), 0, abort_flag);
-      for (int c = 0; c < nch && ok; ++c) {
-        ok = wait_f(smem_u32(&C.a_full[c]), 0, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kChunkK / 16; ++kk) {
-          const int slab = 4 * c + (kk >> 2);
-          const uint64_t xdesc = smem_desc_sw128(sbase + p.off_x + slab * N * 128 + (kk & 3) * 32, 1024);
-          mma_ts(tmem + kColD1, tmem + 128u * c + kk * 8, xdesc, id1, (c > 0 || kk > 0) ? 1u : 0u);
-        }
-        if (lora) {
-          // A operand: 128 rows of u (rows >= N read bytes of the following slabs and
-          // regions, inside this CTA's allocation; they only feed unread lanes)
-#pragma unroll
-          for (int kk = 0; kk < kChunkK / 16; ++kk) {
-            const int slab = 4 * c + (kk >> 2);
-            const uint64_t xdesc = smem_desc_sw128(sbase + p.off_x + slab * N * 128 + (kk & 3) * 32, 1024);
-            const uint64_t adesc = smem_desc_sw128(sbase + p.off_a + slab * p.rb * 128 + (kk & 3) * 32, 1024);
-            mma_ss(tmem + kColDt, xdesc, adesc, idt, (c > 0 || kk > 0) ? 1u : 0u);
-          }
-        }
-      }
-      tc_commit(smem_u32(&C.d_full));  // also reached on abort: tracks every MMA issued
-    }
+    if (lora) convert_a(smem + p.off_a, a_bytes, kConvThreads + lane, kConvThreads + 32, smem_u32(&C.a_in), abort_flag);
+    fence_proxy_async_smem();
     __syncwarp();
-    cluster_wait();
+    if (lane == 0) mbar_arrive(smem_u32(&C.act_ready));
     cluster_arrive();
     cluster_wait();
   } else if (warp >= kConvWarp0) {
-    // ---------------------------------------------------------------- activations
-    const int ct = threadIdx.x - kConvWarp0 * 32;  // 0 .. 127
-    float* gsh = reinterpret_cast<float*>(smem + p.off_g);
+    // ---------------------------------------------------------------- activations, then MMA issue
+    const int cw = warp - kConvWarp0;              // 0..3
+    const int ct = threadIdx.x - kConvWarp0 * 32;  // 0..127
     float* bt = reinterpret_cast<float*>(smem + p.off_bt);  // [j][rows_max]: B of the owned rows
-    float* qrecv = reinterpret_cast<float*>(smem + p.off_q);  // [S][N]: sums of x^2 of every split
     if (lora) {
-      for (int i = ct; i < rows_own * p.r; i += kConvThreads) {
-        const int rl = i / p.r, j = i % p.r;
-        const int64_t o = static_cast<int64_t>(row0) + R0 + rl;
-        bt[j * p.rows_max + rl] = o < p.d_o ? __bfloat162float(p.B[o * p.r + j]) : 0.f;
-      }
-    }
-    pdl_wait();  // w_norm, z and x may come from the preceding kernel
-    const int klen = nch * kChunkK;
-    const int64_t k0 = static_cast<int64_t>(c0) * kChunkK;
-    for (int k4 = ct; k4 < klen / 4; k4 += kConvThreads) {
-      float4 g = make_float4(1.f, 1.f, 1.f, 1.f);
-      if (norm) {
-        g = reinterpret_cast<const float4*>(p.w_norm + k0)[k4];
-        if (p.z) {
-          const float4 zz = reinterpret_cast<const float4*>(p.z + k0)[k4];
-          g.x += zz.x; g.y += zz.y; g.z += zz.z; g.w += zz.w;
-        }
-      }
-      reinterpret_cast<float4*>(gsh)[k4] = g;
-    }
-    named_bar(2, kConvThreads);
-    bool ok = true;
-    if (lora) {
-      ok = wait_f(smem_u32(&C.a_in), 0, abort_flag);
-      uint4* a4 = reinterpret_cast<uint4*>(smem + p.off_a);
-      for (int i = ct; ok && i < static_cast<int>(a_bytes / 16); i += kConvThreads) {
-        const uint4 v = a4[i];
-        a4[i] = make_uint4(f32x2_to_f16x2(bf16lo_to_f32(v.x), bf16hi_to_f32(v.x)),
-                           f32x2_to_f16x2(bf16lo_to_f32(v.y), bf16hi_to_f32(v.y)),
-                           f32x2_to_f16x2(bf16lo_to_f32(v.z), bf16hi_to_f32(v.z)),
-                           f32x2_to_f16x2(bf16lo_to_f32(v.w), bf16hi_to_f32(v.w)));
-      }
-    }
-    ok = ok && wait_f(smem_u32(&C.x_in), 0, abort_flag);
-    // token row n = ct / tpr; the tpr threads of a row are neighbouring lanes
-    const int np2 = N <= 16 ? 16 : (N <= 32 ? 32 : 64);
-    const int tpr = kConvThreads / np2, n = ct / tpr, part = ct % tpr;
-    const int nq = nch * 32;  // 16-byte pieces of one row
-    float ss = 0.f, mx = 0.f;
-    if (ok && n < N) {
-      for (int q = part; q < nq; q += tpr) {
-        const int slab = q >> 3, ch = q & 7;
-        const uint4 v = *reinterpret_cast<const uint4*>(smem + p.off_x + slab * N * 128 + n * 128 + ((ch ^ (n & 7)) << 4));
-        const float4 ga = reinterpret_cast<const float4*>(gsh)[(slab * 64 + ch * 8) / 4];
-        const float4 gb = reinterpret_cast<const float4*>(gsh)[(slab * 64 + ch * 8) / 4 + 1];
-        const float xv[8] = {bf16lo_to_f32(v.x), bf16hi_to_f32(v.x), bf16lo_to_f32(v.y), bf16hi_to_f32(v.y),
-                             bf16lo_to_f32(v.z), bf16hi_to_f32(v.z), bf16lo_to_f32(v.w), bf16hi_to_f32(v.w)};
-        const float gv[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+      // B is a weight: read before the wait on the preceding kernel
+      const int nb = rows_own * p.r;
+      for (int i0 = 0; i0 < nb; i0 += 8 * kConvThreads) {
+        float b[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          ss = fmaf(xv[i], xv[i], ss);
-          mx = fmaxf(mx, fabsf(xv[i] * gv[i]));
+        for (int u = 0; u < 8; ++u) {
+          const int i = i0 + u * kConvThreads + ct;
+          const int rl = i / p.r, j = i % p.r;
+          const int64_t o = static_cast<int64_t>(row0) + R0 + rl;
+          b[u] = (i < nb && o < p.d_o) ? __bfloat162float(p.B[o * p.r + j]) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = i0 + u * kConvThreads + ct;
+          if (i < nb) bt[(i % p.r) * p.rows_max + i / p.r] = b[u];
         }
       }
     }
-    for (int o = tpr / 2; o > 0; o >>= 1) {
-      ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
-      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-    }
-    int e = mx > 0.f ? 13 - ilogbf(mx) : 0;  // max |u| c in [2^13, 2^14)
-    e = e < -100 ? -100 : (e > 100 ? 100 : e);
-    const float cs = ldexpf(1.0f, e);
-    if (ok && n < N) {
-      for (int q = part; q < nq; q += tpr) {
-        const int slab = q >> 3, ch = q & 7;
-        uint4* pv = reinterpret_cast<uint4*>(smem + p.off_x + slab * N * 128 + n * 128 + ((ch ^ (n & 7)) << 4));
-        const uint4 v = *pv;
-        const float4 ga = reinterpret_cast<const float4*>(gsh)[(slab * 64 + ch * 8) / 4];
-        const float4 gb = reinterpret_cast<const float4*>(gsh)[(slab * 64 + ch * 8) / 4 + 1];
-        *pv = make_uint4(f32x2_to_f16x2(bf16lo_to_f32(v.x) * ga.x * cs, bf16hi_to_f32(v.x) * ga.y * cs),
-                         f32x2_to_f16x2(bf16lo_to_f32(v.y) * ga.z * cs, bf16hi_to_f32(v.y) * ga.w * cs),
-                         f32x2_to_f16x2(bf16lo_to_f32(v.z) * gb.x * cs, bf16hi_to_f32(v.z) * gb.y * cs),
-                         f32x2_to_f16x2(bf16lo_to_f32(v.w) * gb.z * cs, bf16hi_to_f32(v.w) * gb.w * cs));
-      }
-      if (part == 0) {
-        C.cinv[n] = ldexpf(1.0f, -e);
-        if (norm) qrecv[me * N + n] = ss;
+    bool ok = true;
+    if (lora)  // A lands early (a weight): convert it while x is still on its way
+      ok = convert_a(smem + p.off_a, a_bytes, ct, kConvThreads + 32, smem_u32(&C.a_in), abort_flag);
+    if (ct == 0) PL_TLF(21);
+    if (norm) {
+      ok = wait_f(smem_u32(&C.g_in), 0, abort_flag) && ok;
+      if (noise) {
+        float4* gw = reinterpret_cast<float4*>(smem + p.off_gw);
+        const float4* gz = reinterpret_cast<const float4*>(smem + p.off_gz);
+        for (int k4 = ct; k4 < nch * kChunkK / 4; k4 += kConvThreads) {
+          float4 a = gw[k4];
+          const float4 b = gz[k4];
+          a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+          gw[k4] = a;
+        }
       }
     }
-    fence_proxy_async_smem();  // the f16 operands are read by the tensor cores
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&C.act_ready));
-    cluster_wait();  // phase 1: every peer's barriers exist
-    if (norm && n < N && part == 0) {
-      for (int d = 1; d < S; ++d) {
-        const uint32_t dst = static_cast<uint32_t>((me + d) % S);
-        st_async_f32(mapa_shared(smem_u32(&qrecv[me * N + n]), dst), ss, mapa_shared(smem_u32(&C.recv), dst));
+    if (lane == 0) mbar_arrive(smem_u32(&C.g_ready));
+    if (ct == 0) PL_TLF(3);
+    ok = wait_f(smem_u32(&C.g_ready), 0, abort_flag) && wait_f(smem_u32(&C.x_in), 0, abort_flag) && ok;
+    if (ct == 0) PL_TLF(4);
+    convert_rows();  // also fences and arrives on act_ready
+    if (ct == 0) PL_TLF(5);
+    if (lane == 0) {
+      // issuer cw: accumulator D1a / D1b (cw 0 / 1) or Dta / Dtb (cw 2 / 3), even / odd K steps
+      const bool tpart = cw >= 2, issue = !tpart || lora;
+      const int par = cw & 1;
+      const uint32_t idesc = tpart ? idesc_f16(kTileO, p.rb, 0) : idesc_f16(kTileO, N, 0);
+      const uint32_t dcol = cw == 0 ? colD1a : (cw == 1 ? colD1b : (cw == 2 ? colDta : colDtb));
+      // Descriptors advance by constants: one K step is 32 bytes (2 units of 16 B), one
+      // 64-element slab N * 128 bytes (x) or rb * 128 bytes (A).  A single issuing thread
+      // spends most of its time on the arithmetic between MMAs, so none is left there.
+      const uint64_t xd0 = smem_desc_sw128(sbase + p.off_x, 1024) + 2u * par;
+      const uint64_t ad0 = smem_desc_sw128(sbase + p.off_a, 1024) + 2u * par;
+      const uint32_t xslab = static_cast<uint32_t>(N) * 8u, aslab = static_cast<uint32_t>(p.rb) * 8u;
+      const uint32_t dtm = tmem + dcol;
+      bool go = wait_f(smem_u32(&C.act_ready), 0, abort_flag);
+      if (cw == 0) PL_TLF(15);
+      for (int c = 0; c < nch && go; ++c) {
+        go = wait_f(smem_u32(&C.a_full[c]), 0, abort_flag);
+        if (!go) break;
+        if (cw == 0) PL_TLF(23 + c);
+        tc_fence_after();
+        if (issue) {
+          const uint64_t xc = xd0 + static_cast<uint64_t>(4u * c * xslab);
+          if (!tpart) {
+            const uint32_t ac = tmem + 128u * (c % nbuf) + 8u * par;  // K step kk = 2 h + par
+#pragma unroll
+            for (int h = 0; h < kChunkK / 32; ++h)
+              mma_ts(dtm, ac + 16u * h, xc + (h >> 1) * xslab + 4u * (h & 1), idesc, (c > 0 || h > 0) ? 1u : 0u);
+          } else {
+            // A operand: 128 rows of u (rows >= N read bytes of the following slabs and
+            // regions, inside this CTA's allocation; they only feed unread lanes)
+            const uint64_t acd = ad0 + static_cast<uint64_t>(4u * c * aslab);
+#pragma unroll
+            for (int h = 0; h < kChunkK / 32; ++h)
+              mma_ss(dtm, xc + (h >> 1) * xslab + 4u * (h & 1), acd + (h >> 1) * aslab + 4u * (h & 1), idesc,
+                     (c > 0 || h > 0) ? 1u : 0u);
+          }
+        }
+        if (cw == 0) PL_TLF(26 + c);
+        if (c + nbuf < nch) tc_commit(smem_u32(&C.a_empty[c % nbuf]));  // buffer reused by chunk c + nbuf
       }
+      tc_commit(smem_u32(&C.d_full));  // also reached on abort: tracks every MMA issued
+      if (cw == 0) PL_TLF(8);
     }
+    __syncwarp();
     cluster_arrive();
     cluster_wait();
   } else {
@@ -335,10 +461,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
     const int row = quarter * 32 + lane;  // weight row within the tile
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const int et = threadIdx.x - 64;      // 0 .. 255
-    bool ok = true;
+    bool ok = true, converted = false;
     for (int c = 0; c < nch; ++c) {
-      ok = wait_f(smem_u32(&C.wfull[c]), 0, abort_flag);
+      if (c == nbuf) {  // buffer 0 is needed again: help with the activations first
+        if (et == 0) PL_TLF(7);
+        ok = wait_f(smem_u32(&C.g_ready), 0, abort_flag) && wait_f(smem_u32(&C.x_in), 0, abort_flag) && ok;
+        convert_rows();
+        converted = true;
+      }
+      const int b = c % nbuf;
+      ok = ok && wait_f(smem_u32(&C.wfull[c]), 0, abort_flag) &&
+           (c < nbuf || wait_f(smem_u32(&C.a_empty[b]), 0, abort_flag));
       if (!ok) break;
+      if (c == 0 && et == 0) PL_TLF(6);
       const uint8_t* crow = smem + c * kCodesBytes + row * 128;
       const uint2 sc8 = *reinterpret_cast<const uint2*>(smem + p.off_scales + c * kScaleBytes + row * 16 + g * 8);
       const uint32_t sc_words[2] = {sc8.x, sc8.y};
@@ -358,106 +493,140 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
         for (int i = 0; i < 8; ++i) v[i] = hmul2_u32(v[i], sa);
 #pragma unroll
         for (int i = 8; i < 16; ++i) v[i] = hmul2_u32(v[i], sb);
-        tmem_st16(tmem + lane_addr + 128u * c + j * 16, v);
+        tmem_st16(tmem + lane_addr + 128u * b + j * 16, v);
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&C.a_full[c]));
     }
+    if (!converted) {
+      if (et == 0) PL_TLF(7);
+      ok = wait_f(smem_u32(&C.g_ready), 0, abort_flag) && wait_f(smem_u32(&C.x_in), 0, abort_flag) && ok;
+      convert_rows();
+    }
+    if (et == 0) C.s_g = *p.s_g;  // a weight input: not written by the preceding kernel
     // ---------------------------------------------------------------- epilogue: gather
     ok = wait_f(smem_u32(&C.d_full), 0, abort_flag) && ok;
+    if (et == 0) PL_TLF(9);
     tc_fence_after();
     const int half = N / 2, n0 = g * half;  // tokens [n0, n0 + half) of D1 for this thread
     const int thalf = p.rb / 2, j0 = g * thalf;
-    const bool trow = lora && quarter * 32 < N && quarter < 2;  // lanes 0..63: token rows of Dt^T
-    uint32_t d1[32], dt[32];
+    const bool trow = lora && quarter * 32 < M && quarter < 2;  // lanes 0..63: token rows of Dt^T
+    // accumulators into registers first (their latency hides behind the cluster barrier)
+    float d1[32], dt[32];
 #pragma unroll
     for (int cb = 0; cb < 4; ++cb) {
-      if (cb * 8 < half) tmem_ld8(tmem + lane_addr + kColD1 + n0 + cb * 8, &d1[cb * 8]);
-      if (trow && cb * 8 < thalf) tmem_ld8(tmem + lane_addr + kColDt + j0 + cb * 8, &dt[cb * 8]);
+      if (cb * 8 < half && n0 + cb * 8 < p.Mp) {
+        uint32_t a8[8], b8[8];
+        tmem_ld8(tmem + lane_addr + colD1a + n0 + cb * 8, a8);
+        tmem_ld8(tmem + lane_addr + colD1b + n0 + cb * 8, b8);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) d1[cb * 8 + i] = __uint_as_float(a8[i]) + __uint_as_float(b8[i]);
+      }
+      if (trow && cb * 8 < thalf) {
+        uint32_t a8[8], b8[8];
+        tmem_ld8(tmem + lane_addr + colDta + j0 + cb * 8, a8);
+        tmem_ld8(tmem + lane_addr + colDtb + j0 + cb * 8, b8);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dt[cb * 8 + i] = __uint_as_float(a8[i]) + __uint_as_float(b8[i]);
+      }
     }
-    tmem_ld_wait();
     const bool good = ok && !*abort_flag;
+    cluster_arrive();  // this CTA no longer reads its stage region
     cluster_wait();
-    cluster_arrive();  // phase 2: this CTA no longer reads its stage region
-    cluster_wait();
+    if (et == 0) PL_TLF(10);
     // ---------------------------------------------------------------- epilogue: exchange
     const uint32_t recv_bar = smem_u32(&C.recv);
     const float s_g = C.s_g;
+    const int Mp = p.Mp;
     {
       int o = S - 1;
       while (o > 0 && owner_row0(o, S) > row) --o;
       const int rl = row - owner_row0(o, S);
-      const uint32_t dst = smem_u32(smem) + static_cast<uint32_t>(((me * p.rows_max + rl) * p.Np + n0) * 4);
+      const uint32_t dst = sbase + static_cast<uint32_t>(((me * p.rows_max + rl) * p.Np + n0) * 4);
       const uint32_t rdst = mapa_shared(dst, static_cast<uint32_t>(o)), rbar = mapa_shared(recv_bar, o);
 #pragma unroll
       for (int i = 0; i < 32; i += 4) {
-        if (i < half) {
+        if (i < half && n0 + i < Mp) {
           float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (good)
-            v = make_float4(s_g * C.cinv[n0 + i] * __uint_as_float(d1[i]),
-                            s_g * C.cinv[n0 + i + 1] * __uint_as_float(d1[i + 1]),
-                            s_g * C.cinv[n0 + i + 2] * __uint_as_float(d1[i + 2]),
-                            s_g * C.cinv[n0 + i + 3] * __uint_as_float(d1[i + 3]));
-          if (o == me) *reinterpret_cast<float4*>(smem + (dst - smem_u32(smem)) + 4 * i) = v;
+          if (good) {
+            const float4 ci = *reinterpret_cast<const float4*>(&C.cinv[n0 + i]);
+            v = make_float4(s_g * ci.x * d1[i], s_g * ci.y * d1[i + 1], s_g * ci.z * d1[i + 2], s_g * ci.w * d1[i + 3]);
+          }
+          if (o == me) *reinterpret_cast<float4*>(smem + (dst - sbase) + 4 * i) = v;
           else st_async_f32x4(rdst + 4 * i, v, rbar);
         }
       }
     }
-    if (trow && quarter * 32 + lane < N) {
+    if (et == 0) PL_TLF(48);
+    float* rtw = reinterpret_cast<float*>(smem + p.off_rt);
+    if (trow && quarter * 32 + lane < M) {  // this split's t slice, local copy first
       const int n = quarter * 32 + lane;
       const float ci = C.cinv[n];
-      const uint32_t dst = smem_u32(smem) + p.off_rt + static_cast<uint32_t>(((me * N + n) * p.rb + j0) * 4);
-      for (int d = 0; d < S; ++d) {
-        const int o = (me + d) % S;
+      float* dst = rtw + (me * N + n) * p.rb + j0;
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          if (i < thalf) {
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (good)
-              v = make_float4(ci * __uint_as_float(dt[i]), ci * __uint_as_float(dt[i + 1]),
-                              ci * __uint_as_float(dt[i + 2]), ci * __uint_as_float(dt[i + 3]));
-            if (o == me) *reinterpret_cast<float4*>(smem + (dst - smem_u32(smem)) + 4 * i) = v;
-            else st_async_f32x4(mapa_shared(dst + 4 * i, o), v, mapa_shared(recv_bar, o));
-          }
+      for (int i = 0; i < 32; i += 4) {
+        if (i < thalf) {
+          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (good) v = make_float4(ci * dt[i], ci * dt[i + 1], ci * dt[i + 2], ci * dt[i + 3]);
+          *reinterpret_cast<float4*>(dst + i) = v;
         }
       }
     }
+    if (et == 0) PL_TLF(49);
+    if (lora && S > 1) {  // then from there to every peer, spread over all epilogue threads
+      named_bar(1, kEpiThreads);
+      if (et == 0) PL_TLF(50);
+      const int per = M * p.rb / 4;  // 16-byte pieces of the slice
+      const uint32_t src = sbase + p.off_rt + static_cast<uint32_t>(me * N * p.rb * 4);
+      for (int i = et; i < per * (S - 1); i += kEpiThreads) {
+        const int d = 1 + i / per, k = i % per;
+        const uint32_t o = static_cast<uint32_t>((me + d) % S);
+        const float4 v = *reinterpret_cast<const float4*>(smem + (src - sbase) + 16 * k);
+        st_async_f32x4(mapa_shared(src + 16 * k, o), v, mapa_shared(recv_bar, o));
+      }
+    }
     if (et == 0) {
-      const uint32_t per_peer = static_cast<uint32_t>(rows_own * N * 4 + (lora ? N * p.rb * 4 : 0) + (norm ? N * 4 : 0));
+      const uint32_t per_peer =
+          static_cast<uint32_t>(rows_own * Mp * 4 + (lora ? M * p.rb * 4 : 0) + (norm ? M * 4 : 0));
       mbar_arrive_expect_tx(recv_bar, per_peer * static_cast<uint32_t>(S - 1));
+      PL_TLF(11);
     }
     named_bar(1, kEpiThreads);  // this CTA's own shares are in place
     ok = wait_f(recv_bar, 0, abort_flag) && good;
+    if (et == 0) PL_TLF(12);
     // ---------------------------------------------------------------- epilogue: combine
-    const float* qrecv = reinterpret_cast<const float*>(smem + p.off_q);
-    const float* rt = reinterpret_cast<const float*>(smem + p.off_rt);
+    const float* rt = rtw;
     float* ts = reinterpret_cast<float*>(smem + p.off_ts);  // [N][rb + 4]: lambda t
     const int tstr = p.rb + 4;
-    if (et < N) {
+    if (et < M) {
       float rs = 1.f;
       if (norm) {
         float tot = 0.f;
         for (int s = 0; s < S; ++s) tot += qrecv[s * N + et];
-        rs = 1.0f / sqrtf(tot / static_cast<float>(p.d_i) + p.eps);
+        rs = rsqrtf(tot * p.inv_d + p.eps);
       }
       C.rs[et] = rs;
     }
+    if (et == 0) PL_TLF(51);
     if (lora) {
-      for (int i = et; i < N * p.rb; i += kEpiThreads) {
+      for (int i = et; i < M * p.rb; i += kEpiThreads) {
         const int n = i / p.rb, j = i % p.rb;
         float acc = 0.f;
         for (int s = 0; s < S; ++s) acc += rt[(s * N + n) * p.rb + j];
         ts[n * tstr + j] = p.lambda * acc;
       }
     }
+    if (et == 0) PL_TLF(52);
     named_bar(1, kEpiThreads);
+    if (et == 0) PL_TLF(22);
     if (ok) {
       const float* rp = reinterpret_cast<const float*>(smem);
       const float* bt = reinterpret_cast<const float*>(smem + p.off_bt);
-      const int mq = static_cast<int>((p.M + 3) / 4);
-      const int items = rows_own * mq;
+      const int items = rows_own * (Mp / 4);
       for (int e = et; e < items; e += kEpiThreads) {
         const int rl = e % rows_own, n4 = 4 * (e / rows_own);
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -466,7 +635,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
           acc[0] += v.x; acc[1] += v.y; acc[2] += v.z; acc[3] += v.w;
         }
         if (lora) {
-          float l[4] = {0.f, 0.f, 0.f, 0.f};
+          const int nq = M - n4 < 4 ? M - n4 : 4;
+#pragma unroll 2
           for (int j = 0; j < p.r; j += 4) {
             const float b0 = bt[j * p.rows_max + rl];
             const float b1 = j + 1 < p.r ? bt[(j + 1) * p.rows_max + rl] : 0.f;
@@ -474,34 +644,36 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
             const float b3 = j + 3 < p.r ? bt[(j + 3) * p.rows_max + rl] : 0.f;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const float4 t = *reinterpret_cast<const float4*>(ts + (n4 + q) * tstr + j);
-              l[q] = fmaf(b0, t.x, fmaf(b1, t.y, fmaf(b2, t.z, fmaf(b3, t.w, l[q]))));
+              if (q < nq) {
+                const float4 t = *reinterpret_cast<const float4*>(ts + (n4 + q) * tstr + j);
+                acc[q] = fmaf(b0, t.x, fmaf(b1, t.y, fmaf(b2, t.z, fmaf(b3, t.w, acc[q]))));
+              }
             }
           }
-#pragma unroll
-          for (int q = 0; q < 4; ++q) acc[q] += l[q];
         }
         const int64_t oo = static_cast<int64_t>(row0) + R0 + rl;
         if (oo < p.d_o) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int n = n4 + q;
-            if (n < p.M) {
+            if (n < M) {
               const float v = C.rs[n] * acc[q];
-              if (p.y_f32) static_cast<float*>(p.y)[n * p.d_o + oo] = v;
-              else static_cast<__nv_bfloat16*>(p.y)[n * p.d_o + oo] = __float2bfloat16_rn(v);
+              if (p.y_f32) static_cast<float*>(p.y)[static_cast<int64_t>(n) * p.d_o + oo] = v;
+              else static_cast<__nv_bfloat16*>(p.y)[static_cast<int64_t>(n) * p.d_o + oo] = __float2bfloat16_rn(v);
             }
           }
         }
       }
     }
   }
+  if (threadIdx.x == 64) PL_TLF(13);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  if (threadIdx.x == 0) PL_TLF(14);
 }
 
 // ------------------------------------------------------------------ host side
@@ -533,7 +705,7 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void*
 
 struct FPlan {
   int N, Np, rb, S, kc, tiles, rows_max, nchmax;
-  uint32_t off_scales, off_x, off_a, off_g, off_bt, off_q, off_ctrl, off_rt, off_ts;
+  uint32_t off_scales, off_x, off_a, off_gw, off_gz, off_bt, off_q, off_ctrl, off_rt, off_ts;
   size_t smem;
 };
 
@@ -545,8 +717,9 @@ bool layout(FPlan& f, int r) {
   f.off_scales = static_cast<uint32_t>(f.nchmax * kCodesBytes);
   f.off_x = al1k(f.off_scales + static_cast<size_t>(f.nchmax) * kScaleBytes);
   f.off_a = al1k(f.off_x + static_cast<size_t>(nslab) * f.N * 128);
-  f.off_g = al1k(f.off_a + static_cast<size_t>(nslab) * f.rb * 128);
-  f.off_bt = f.off_g + f.nchmax * kChunkK * 4;
+  f.off_gw = al1k(f.off_a + static_cast<size_t>(nslab) * f.rb * 128);
+  f.off_gz = f.off_gw + f.nchmax * kChunkK * 4;
+  f.off_bt = f.off_gz + f.nchmax * kChunkK * 4;
   f.off_q = f.off_bt + static_cast<uint32_t>(align_up(static_cast<size_t>(r > 0 ? r : 1) * f.rows_max * 4, 16));
   f.off_ctrl = f.off_q + static_cast<uint32_t>(align_up(static_cast<size_t>(f.S) * f.N * 4, 16));
   f.off_ctrl = static_cast<uint32_t>(align_up(f.off_ctrl, 128));
@@ -560,7 +733,9 @@ bool layout(FPlan& f, int r) {
   f.off_rt = static_cast<uint32_t>(align_up(static_cast<size_t>(f.S) * f.rows_max * f.Np * 4, 16));
   f.off_ts = f.off_rt + static_cast<uint32_t>(static_cast<size_t>(f.S) * f.N * f.rb * 4);
   const size_t alias_end = f.off_ts + static_cast<size_t>(f.N) * (f.rb + 4) * 4;
-  return f.smem <= 227 * 1024 && alias_end <= f.off_g;
+  // tensor memory: 2 weight buffers of 128 columns, D1 twice (N), Dt twice (rb)
+  const bool tmem_ok = 256 + 2 * f.N + 2 * f.rb <= static_cast<int>(kTmemCols);
+  return tmem_ok && f.smem <= 227 * 1024 && alias_end <= f.off_gw;
 }
 
 int max_active_clusters(size_t smem, int cs) {
@@ -687,13 +862,16 @@ cudaError_t launch_linear_fused(const LinearArgs& a, cudaStream_t stream) {
   p.d_o = a.d_o;
   p.N = f.N;
   p.Np = f.Np;
+  p.Mp = static_cast<int>((a.M + 3) / 4 * 4);
   p.rb = f.rb;
   p.r = a.r;
   p.S = f.S;
   p.kc = f.kc;
   p.rows_max = f.rows_max;
+  p.nbuf = 384 + 2 * f.N + 2 * f.rb <= static_cast<int>(kTmemCols) ? 3 : 2;
   p.lambda = a.lambda;
   p.eps = a.eps;
+  p.inv_d = 1.0f / static_cast<float>(a.d_i);
   p.s_g = a.s_g;
   p.w_norm = a.w_norm;
   p.z = a.z;
@@ -703,7 +881,8 @@ cudaError_t launch_linear_fused(const LinearArgs& a, cudaStream_t stream) {
   p.off_scales = f.off_scales;
   p.off_x = f.off_x;
   p.off_a = f.off_a;
-  p.off_g = f.off_g;
+  p.off_gw = f.off_gw;
+  p.off_gz = f.off_gz;
   p.off_bt = f.off_bt;
   p.off_q = f.off_q;
   p.off_ctrl = f.off_ctrl;
@@ -726,6 +905,13 @@ cudaError_t launch_linear_fused(const LinearArgs& a, cudaStream_t stream) {
   c.numAttrs = 2;
   return cudaLaunchKernelEx(&c, k_fused_decode, maps, p);
 }
+
+#ifdef PL_TIMELINE
+extern "C" int pl_debug_read_timeline_fused(unsigned long long* out) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return 1;
+  return cudaMemcpyFromSymbol(out, g_tl_fused, sizeof(g_tl_fused)) != cudaSuccess ? 2 : 0;
+}
+#endif
 
 uint32_t fused_read_and_clear_status() {
   uint32_t v = 0, zero = 0;
