@@ -324,6 +324,15 @@ def run_ours(args, world, rank, local):
         e2e = {"value": round(step_bytes * args.steps * world / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": round(ms_e2e / args.steps, 4)}
 
+    prefill = None
+    if not args.no_prefill:
+        prefill = bench_prefill(dev, stream)
+        _, bf16_peak, bf16_kind = measured_peaks()
+        prefill["roofline"] = {"bound": "tensor", "kernel": "row prologue + LoRA down + k_gemm_nvfp4 (whole call)",
+                               "achieved": prefill["layer_TFLOPs"], "peak": bf16_peak, "unit": "TFLOP/s",
+                               "frac": round(prefill["layer_TFLOPs"] / bf16_peak, 4), "peak_kind": bf16_kind,
+                               "peak_note": "dense BF16 cuBLAS burst; the path computes in f16 (same tensor rate)"}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args, budget_s=args.cpu_seconds)
@@ -348,10 +357,63 @@ def run_ours(args, world, rank, local):
                          "frac": round(achieved / hbm_peak, 4), "peak_kind": peak_kind,
                          "traffic": profile_traffic("k_fused_decode" if paths[int(dom)] == 2 else "k_tc_decode",
                                                     f"{args.workload}/M{dom}")},
-            "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
+            "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, "prefill": prefill,
             "gpu_launches": sum(launches_per_call.values()) * args.steps,
         }
         print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------- large-M path
+def bench_prefill(dev, stream, reps: int = 5):
+    """The Qwen2.5-7B-shaped layer set at M = 4096 (log-prob recompute): every
+    projection through the large-M tensor-core path, timed with CUDA events on the
+    launching stream; returns per-projection and whole-layer TFLOPS."""
+    import torch
+
+    from precision_linear_gb300 import binding as pl
+    from precision_linear_gb300 import synthetic
+
+    wl = synthetic.WORKLOADS["prefill_7b"]
+    M, r = wl.Ms[0], wl.r
+    ws = pl.Workspace(dev)
+    out, tot_flops, tot_ms = {}, 0, 0.0
+    with torch.cuda.stream(stream):
+        for i, p in enumerate(wl.projs):
+            c = synthetic.projection_case(p.d_o, p.d_i, M, r, wl.sigma, synthetic.proj_seed(wl, 0, i), 0.0,
+                                          device="cpu")
+            W = c["W"].to(dev)
+            codes, scales, s_g = pl.nvfp4_quantize(W)
+            del W
+            x, A, B = c["x"].to(dev), c["A"].to(dev), c["B"].to(dev)
+            norm = p.norm is not None
+            w_norm = c["w_norm"].to(dev) if norm else None
+            z = c["z"].to(dev) if norm else None
+            y = torch.empty(M, p.d_o, dtype=torch.bfloat16, device=dev)
+            ws.get(pl.workspace_bytes(M, p.d_i, p.d_o, r))
+
+            def call():
+                pl.nvfp4_lora_linear(x, codes, scales, s_g, A, B, wl.lam, w_norm, z, synthetic.EPS, out=y, workspace=ws)
+
+            for _ in range(2):
+                call()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                call()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / reps
+            fl = algorithmic_flops(M, p.d_i, p.d_o, r)
+            out[p.name] = {"d_i": p.d_i, "d_o": p.d_o, "us_per_call": round(ms * 1e3, 1),
+                           "TFLOPs": round(fl / (ms * 1e-3) / 1e12, 1), "path": pl.linear_path(M, p.d_i, p.d_o, r)}
+            tot_flops += fl
+            tot_ms += ms
+            del codes, scales, s_g, x, A, B, w_norm, z, y
+    torch.cuda.synchronize()
+    return {"workload": "prefill_7b (Qwen2.5-7B layer set, M=4096, r=32)", "M": M,
+            "layer_us": round(tot_ms * 1e3, 1), "layer_TFLOPs": round(tot_flops / (tot_ms * 1e-3) / 1e12, 1),
+            "per_proj": out, "timing": f"CUDA events, {reps} calls per projection after 2 warm-up calls"}
 
 
 # ------------------------------------------------------------------------- oracle timing
@@ -429,6 +491,7 @@ def main():
     ap.add_argument("--workload", default="decode_proj_7b")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the M=4096 layer-set measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

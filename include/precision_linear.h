@@ -177,8 +177,9 @@ pl_status pl_last_device_status(pl_stream_t stream);
 
 /* Test hook: which kernel path pl_nvfp4_lora_linear takes for this shape on the
  * current device: 2 = one fused tcgen05 kernel (every CTA's K slice on chip),
- * 1 = tcgen05 prologue + main kernel, 0 = generic CUDA-core kernels, -1 = invalid
- * shape or unsupported device.  Launches nothing. */
+ * 1 = tcgen05 prologue + main kernel (M <= 64), 3 = large-M tcgen05 path (row
+ * prologue, LoRA down-projection, persistent NVFP4 GEMM), 0 = generic CUDA-core
+ * kernels, -1 = invalid shape or unsupported device.  Launches nothing. */
 int pl_debug_linear_path(int64_t M, int64_t d_i, int64_t d_o, int r);
 
 /* Test hook: when `armed` is non-zero the next launch-checking step of any call

@@ -88,6 +88,8 @@ size_t pl_workspace_bytes(int64_t M, int64_t d_i, int64_t d_o, int r) {
   if (M < 1 || d_o < 1 || d_i < 16 || d_i % 16 != 0 || r < 0 || r > 64) return 0;
   size_t g = pl::generic_workspace_bytes(M, d_i, d_o, r);
   size_t t = pl::tc_supported(M, d_i, d_o, r) ? pl::tc_workspace_bytes(M, d_i, d_o, r) : 0;
+  const size_t f = pl::prefill_supported(M, d_i, d_o, r) ? pl::prefill_workspace_bytes(M, d_i, d_o, r) : 0;
+  t = t > f ? t : f;
   return g > t ? g : t;
 }
 
@@ -141,12 +143,14 @@ pl_status pl_nvfp4_lora_linear(const void* x, int64_t M, int64_t d_i, int64_t d_
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (pl::fused_supported(M, d_i, d_o, a.r)) return check_launch(pl::launch_linear_fused(a, s));
   if (pl::tc_supported(M, d_i, d_o, a.r)) return check_launch(pl::launch_linear_tc(a, s));
+  if (pl::prefill_supported(M, d_i, d_o, a.r)) return check_launch(pl::launch_linear_prefill(a, s));
   return check_launch(pl::launch_linear_generic(a, s));
 }
 
 pl_status pl_last_device_status(pl_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return PL_ERR_CUDA;
-  uint32_t bits = pl::tc_read_and_clear_status() | pl::fused_read_and_clear_status();
+  uint32_t bits = pl::tc_read_and_clear_status() | pl::fused_read_and_clear_status() |
+                  pl::prefill_read_and_clear_status();
   return (bits & pl::kStatusTimeout) ? PL_ERR_TIMEOUT : PL_OK;
 }
 
@@ -154,6 +158,7 @@ int pl_debug_linear_path(int64_t M, int64_t d_i, int64_t d_o, int r) {
   if (M < 1 || d_o < 1 || d_i < 16 || d_i % 16 != 0 || r < 0 || r > 64 || device_check() != PL_OK) return -1;
   if (pl::fused_supported(M, d_i, d_o, r)) return 2;
   if (pl::tc_supported(M, d_i, d_o, r)) return 1;
+  if (pl::prefill_supported(M, d_i, d_o, r)) return 3;
   return 0;
 }
 

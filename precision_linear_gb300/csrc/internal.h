@@ -1,6 +1,7 @@
 // Internal host-side interface between the C ABI (api.cu) and the kernel files.
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -48,11 +49,21 @@ size_t tc_workspace_bytes(int64_t M, int64_t d_i, int64_t d_o, int r);
 cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream);
 uint32_t tc_read_and_clear_status();
 cudaError_t launch_wait_timeout_probe(cudaStream_t stream);
+// The row prologue on its own: hq = f16(RMSNorm_AQN(x) / rowscale) [M][d_i], rowscale
+// [M] (powers of two), A16 = f16(A) [r][d_i], and n_zero zeros (a multiple of 4) at zero.
+cudaError_t launch_act_prologue(const LinearArgs& a, __half* hq, float* rowscale, __half* A16, float* zero,
+                                int64_t n_zero, cudaStream_t stream);
 
 // ---- linear_fused.cu (tcgen05, one kernel; M <= 64 and at most 3 K chunks of 256 per CTA)
 bool fused_supported(int64_t M, int64_t d_i, int64_t d_o, int r);
 cudaError_t launch_linear_fused(const LinearArgs& a, cudaStream_t stream);
 uint32_t fused_read_and_clear_status();
+
+// ---- linear_prefill.cu (tcgen05 persistent GEMM; M > 64, d_i % 256 == 0, r <= 32)
+bool prefill_supported(int64_t M, int64_t d_i, int64_t d_o, int r);
+size_t prefill_workspace_bytes(int64_t M, int64_t d_i, int64_t d_o, int r);
+cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream);
+uint32_t prefill_read_and_clear_status();
 
 // ---- api.cu
 int sm_count();  // SMs of the current device (cached)

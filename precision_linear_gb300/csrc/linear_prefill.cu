@@ -1,0 +1,655 @@
+// tcgen05 NVFP4 + LoRA linear for large M (log-prob recompute, prefill), sm_103a.
+//
+// Computes the forward map of "QeRL: When Quantized Weights Help Reinforcement
+// Learning, and Where the Evidence Stops", section 2.1 (y = W_hat h + lambda B (A h)),
+// on the section 3.1 NVFP4 backbone (w_hat = s_g s_b q), with h the section 5.1
+// RMSNorm-AQN of x.  Three kernels, chained by programmatic dependent launch:
+//
+//   k_act (linear_tc.cu)  per token row: hq = f16(h / rowscale) with rowscale a power of
+//                         two (max |hq| in [2^13, 2^14)); A -> f16; split counters := 0.
+//   k_lora_down           t[m, :] = rowscale[m] sum_k A[:, k] hq[m, k]: each CTA one K split
+//                         of 128 tokens (tcgen05.mma, 128 x r, K = 16 steps, from TMA-staged
+//                         hq and f16 A tiles, FP32 accumulator in tensor memory) into its
+//                         partial; the last split of a token tile to finish adds the partials
+//                         up in split order (deterministic) into t32.
+//   k_gemm_nvfp4          the dense contraction, persistent over 128 (weight rows) x 192
+//                         (tokens) tiles, o-tiles fastest so that concurrent CTAs share
+//                         their hq tiles in L2:
+//     warp 0      TMA: per 64-wide K step the hq tile (192 x 64 f16, 128-byte swizzle) and
+//                 the packed codes (128 x 32 B); every 4th step the E4M3 scales of the next
+//                 256 K (128 x 16 B); per tile the t32 rows and row scales of its tokens;
+//     warps 2-5   dequantise each K step into a 32-column tensor-memory slot (E2M1 -> f16
+//                 conversion times the f16 block scale: exact), one weight row per thread;
+//     warp 1      tcgen05.mma kind::f16, M = 128, N = 192, K = 16: D (tensor memory, two
+//                 buffers of 192 columns) += W_hat / s_g x hq^T;
+//     warps 6-13  epilogue of the previous tile while the next one accumulates:
+//                 y[m, o] = s_g rowscale[m] D[o, m] + lambda sum_j B[o, j] t32[m, j] (FP32),
+//                 stored as BF16 or FP32.
+//
+// Every mbarrier wait is bounded (200 ms); a wait that gives up sets the status word,
+// the CTA stops issuing work, drains its copies, frees its tensor memory and returns.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace pl {
+
+__device__ uint32_t g_pf_status = 0;
+
+namespace {
+
+constexpr int kTO = 128;  // weight rows per tile
+constexpr int kTN = 192;  // tokens per tile
+constexpr int kKS = 64;   // K per pipeline step (one 128-byte row of f16)
+constexpr int kMaxStages = 5;
+constexpr int kASlots = 4;
+constexpr uint32_t kHBytes = kTN * kKS * 2;     // 24 KB
+constexpr uint32_t kCodeBytes = kTO * kKS / 2;  // 4 KB
+constexpr uint32_t kStageBytes = kHBytes + kCodeBytes;
+constexpr uint32_t kScaleBytes = kTO * 16;      // scales of 256 K
+constexpr int kDeqWarps = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = (2 + kDeqWarps + kEpiWarps) * 32;  // 448
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColD0 = 128;  // D buffer b at columns [128 + 192 b, 320 + 192 b); weight slots below
+constexpr int kMaxR = 32;
+
+struct GParams {
+  int64_t M, d_i, d_o;
+  int r, R4, n_ot, n_tiles, n_ks, stages;
+  float lambda;
+  const float* s_g;
+  const __nv_bfloat16* B;
+  const float* rowscale;  // [M_pad]
+  const float* t32;       // [M_pad][R4]
+  void* y;
+  int y_f32;
+  uint32_t off_scales, off_t, t_slot_bytes, off_ctrl;
+};
+
+struct GMaps {
+  CUtensorMap codes, scales, hq;
+};
+
+struct GCtrl {
+  uint64_t full[kMaxStages], empty[kMaxStages];
+  uint64_t afull[kASlots], aempty[kASlots];
+  uint64_t dfull[2], dempty[2];
+  uint64_t tfull[2], tempty[2];
+  uint64_t mma_done;  // every MMA this CTA issued has completed
+  uint32_t tmem_base;
+  int abort_flag;
+  float s_g;
+};
+
+PL_DEVINL bool wait_p(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  return wait_or_abort_status(bar, parity, abort_flag, &g_pf_status);
+}
+PL_DEVINL void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+// ------------------------------------------------------------------ main contraction
+__global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constant__ GMaps maps, const GParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  GCtrl& C = *reinterpret_cast<GCtrl*>(smem + p.off_ctrl);
+  volatile int* abort_flag = &C.abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = smem_u32(smem);
+  const int nst = p.stages, n_ks = p.n_ks;
+  const bool lora = p.r > 0;
+
+  if (threadIdx.x == 0) {
+    pdl_launch_dependents();
+    for (int s = 0; s < nst; ++s) {
+      mbar_init(smem_u32(&C.full[s]), 1);
+      mbar_init(smem_u32(&C.empty[s]), kDeqWarps + 1);
+    }
+    for (int a = 0; a < kASlots; ++a) {
+      mbar_init(smem_u32(&C.afull[a]), kDeqWarps);
+      mbar_init(smem_u32(&C.aempty[a]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&C.dfull[b]), 1);
+      mbar_init(smem_u32(&C.dempty[b]), kEpiWarps);
+      mbar_init(smem_u32(&C.tfull[b]), 1);
+      mbar_init(smem_u32(&C.tempty[b]), kEpiWarps);
+    }
+    mbar_init(smem_u32(&C.mma_done), 1);
+    C.abort_flag = 0;
+    C.s_g = *p.s_g;  // a weight input: not written by the preceding kernel
+    fence_mbar_init();
+    tma_prefetch_desc(&maps.codes);
+    tma_prefetch_desc(&maps.scales);
+    tma_prefetch_desc(&maps.hq);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&C.tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = C.tmem_base;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      pdl_wait();  // hq, row scales and t32 come from the preceding kernels
+      const uint64_t pol_w = policy_evict_first();  // each weight tile is read by 1/n_mt of the CTAs at a time
+      const uint32_t tbytes = static_cast<uint32_t>(kTN) * (lora ? p.R4 * 4 + 4 : 4);
+      bool ok = true;
+      int64_t gs = 0;
+      int it = 0, t_issued = 0;
+      for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x, ++it) {
+        const int mt = tile / p.n_ot, ot = tile % p.n_ot;
+        const int32_t m0 = mt * kTN, o0 = ot * kTO;
+        {  // this tile's t32 rows and row scales
+          const int tb = it & 1;
+          if (it >= 2) ok = wait_p(smem_u32(&C.tempty[tb]), ((it >> 1) - 1) & 1, abort_flag);
+          if (!ok) break;
+          const uint32_t tb_bar = smem_u32(&C.tfull[tb]);
+          const uint32_t dst = sbase + p.off_t + tb * p.t_slot_bytes;
+          mbar_arrive_expect_tx(tb_bar, tbytes);
+          if (lora) bulk_g2s(dst, p.t32 + static_cast<int64_t>(m0) * p.R4, kTN * p.R4 * 4, tb_bar);
+          bulk_g2s(dst + (lora ? kTN * p.R4 * 4 : 0), p.rowscale + m0, kTN * 4, tb_bar);
+          ++t_issued;
+        }
+        for (int s = 0; s < n_ks && ok; ++s, ++gs) {
+          const int st = static_cast<int>(gs % nst);
+          if (gs >= nst) ok = wait_p(smem_u32(&C.empty[st]), static_cast<uint32_t>((gs / nst) - 1) & 1, abort_flag);
+          if (!ok) break;
+          const uint32_t fb = smem_u32(&C.full[st]);
+          const bool scl = (s & 3) == 0;
+          mbar_arrive_expect_tx(fb, kStageBytes + (scl ? kScaleBytes : 0));
+          const uint32_t stage = sbase + st * kStageBytes;
+          tma_load_2d(stage, &maps.hq, s * kKS, m0, fb);
+          tma_load_2d_hint(stage + kHBytes, &maps.codes, s * (kKS / 2), o0, fb, pol_w);
+          if (scl) {
+            const int64_t grp = static_cast<int64_t>(it) * (n_ks / 4) + s / 4;
+            tma_load_2d_hint(sbase + p.off_scales + static_cast<uint32_t>(grp & 1) * kScaleBytes, &maps.scales,
+                             s * (kKS / 16), o0, fb, pol_w);
+          }
+        }
+      }
+      if (*abort_flag) {  // every issued copy lands before this CTA exits
+        for (int64_t d = gs - nst > 0 ? gs - nst : 0; d < gs; ++d)
+          drain(smem_u32(&C.full[d % nst]), static_cast<uint32_t>(d / nst) & 1);
+        for (int d = t_issued - 2 > 0 ? t_issued - 2 : 0; d < t_issued; ++d)
+          drain(smem_u32(&C.tfull[d & 1]), (d >> 1) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(kTO, kTN, 0);
+      bool ok = true;
+      int64_t gs = 0;
+      int it = 0;
+      for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x, ++it) {
+        const int b = it & 1;
+        if (it >= 2) ok = wait_p(smem_u32(&C.dempty[b]), ((it >> 1) - 1) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (kColD0 + 192u * b);
+        for (int s = 0; s < n_ks && ok; ++s, ++gs) {
+          const int st = static_cast<int>(gs % nst), a = static_cast<int>(gs % kASlots);
+          ok = wait_p(smem_u32(&C.full[st]), static_cast<uint32_t>(gs / nst) & 1, abort_flag) &&
+               wait_p(smem_u32(&C.afull[a]), static_cast<uint32_t>(gs / kASlots) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t hdesc = smem_desc_sw128(sbase + st * kStageBytes, 1024);
+          const uint32_t acol = tmem + 32u * a;
+#pragma unroll
+          for (int kk = 0; kk < kKS / 16; ++kk)
+            mma_ts(d, acol + 8u * kk, hdesc + 2u * kk, idesc, (s > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(smem_u32(&C.empty[st]));
+          tc_commit(smem_u32(&C.aempty[a]));
+        }
+        tc_commit(smem_u32(&C.dfull[b]));
+      }
+      tc_commit(smem_u32(&C.mma_done));
+      drain(smem_u32(&C.mma_done), 0);  // tensor memory is freed only after the last MMA
+    }
+  } else if (warp < 2 + kDeqWarps) {
+    // ---------------------------------------------------------------- dequant
+    const int quarter = warp & 3, row = quarter * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    bool ok = true;
+    int64_t gs = 0;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x, ++it) {
+      for (int s = 0; s < n_ks && ok; ++s, ++gs) {
+        const int st = static_cast<int>(gs % nst), a = static_cast<int>(gs % kASlots);
+        ok = wait_p(smem_u32(&C.full[st]), static_cast<uint32_t>(gs / nst) & 1, abort_flag) &&
+             (gs < kASlots || wait_p(smem_u32(&C.aempty[a]), static_cast<uint32_t>((gs / kASlots) - 1) & 1, abort_flag));
+        if (!ok) break;
+        const uint8_t* stage = smem + st * kStageBytes;
+        const uint4 c0 = *reinterpret_cast<const uint4*>(stage + kHBytes + row * 32);
+        const uint4 c1 = *reinterpret_cast<const uint4*>(stage + kHBytes + row * 32 + 16);
+        const int64_t grp = static_cast<int64_t>(it) * (n_ks / 4) + s / 4;
+        const uint32_t sw = *reinterpret_cast<const uint32_t*>(smem + p.off_scales + static_cast<uint32_t>(grp & 1) * kScaleBytes +
+                                                                row * 16 + (s & 3) * 4);
+        const uint32_t s01 = cvt_e4m3x2_to_f16x2(sw & 0xFFFFu), s23 = cvt_e4m3x2_to_f16x2(sw >> 16);
+        const uint32_t sc[4] = {prmt(s01, s01, 0x1010u), prmt(s01, s01, 0x3232u), prmt(s23, s23, 0x1010u),
+                                prmt(s23, s23, 0x3232u)};
+        const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // 32 weights (2 scale blocks) per tensor-memory store
+          uint32_t v[16];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) e2m1x8_to_f16x8(cw[4 * h + q], v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = hmul2_u32(v[i], sc[2 * h + (i >> 3)]);
+          tmem_st16(tmem + lane_addr + 32u * a + 16u * h, v);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&C.afull[a]));
+          mbar_arrive(smem_u32(&C.empty[st]));
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int quarter = warp & 3, half = (warp - 2 - kDeqWarps) >> 2;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    const float s_g = C.s_g;
+    bool ok = true;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x, ++it) {
+      const int mt = tile / p.n_ot, ot = tile % p.n_ot;
+      const int b = it & 1;
+      const int64_t o = static_cast<int64_t>(ot) * kTO + row;
+      float bo[kMaxR];
+#pragma unroll
+      for (int j = 0; j < kMaxR; ++j) bo[j] = (lora && j < p.r && o < p.d_o) ? __bfloat162float(p.B[o * p.r + j]) : 0.f;
+      ok = wait_p(smem_u32(&C.dfull[b]), (it >> 1) & 1, abort_flag) &&
+           wait_p(smem_u32(&C.tfull[b]), (it >> 1) & 1, abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      const float* ts = reinterpret_cast<const float*>(smem + p.off_t + b * p.t_slot_bytes);
+      const float* rsc = ts + (lora ? kTN * p.R4 : 0);
+      for (int cb = 0; cb < kTN / 2 / 16; ++cb) {
+        const int col = half * (kTN / 2) + cb * 16;  // token columns [col, col + 16) of the tile
+        uint32_t dv[16];
+        tmem_ld16(tmem + lane_addr + (kColD0 + 192u * b) + col, dv);
+        tmem_ld_wait();
+#pragma unroll 4
+        for (int i = 0; i < 16; ++i) {
+          const int ml = col + i;
+          const int64_t m = static_cast<int64_t>(mt) * kTN + ml;
+          float v = s_g * rsc[ml] * __uint_as_float(dv[i]);
+          if (lora) {
+            const float4* t4 = reinterpret_cast<const float4*>(ts + ml * p.R4);
+            float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+            for (int j4 = 0; j4 < kMaxR / 4; ++j4) {
+              if (4 * j4 < p.r) {
+                const float4 t = t4[j4];
+                l0 = fmaf(bo[4 * j4], t.x, fmaf(bo[4 * j4 + 1], t.y, l0));
+                l1 = fmaf(bo[4 * j4 + 2], t.z, fmaf(bo[4 * j4 + 3], t.w, l1));
+              }
+            }
+            v = fmaf(p.lambda, l0 + l1, v);
+          }
+          if (m < p.M && o < p.d_o) {
+            if (p.y_f32) static_cast<float*>(p.y)[m * p.d_o + o] = v;
+            else static_cast<__nv_bfloat16*>(p.y)[m * p.d_o + o] = __float2bfloat16_rn(v);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&C.dempty[b]));
+        mbar_arrive(smem_u32(&C.tempty[b]));
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ LoRA down-projection
+constexpr int kLdStages = 4;
+constexpr int kLdThreads = 6 * 32;  // TMA, MMA, 4 epilogue warps
+constexpr uint32_t kLdH = 128 * kKS * 2;  // 16 KB
+
+struct LParams {
+  int64_t M, d_i, Mp;
+  int r, R4, rb, n_ks, splits;
+  const float* rowscale;
+  float* t_part;  // [splits][Mp][R4]
+  float* t32;     // [Mp][R4]
+  int* counters;  // [token tiles], zero on entry
+};
+struct LMaps {
+  CUtensorMap hq, a16;
+};
+struct LCtrl {
+  uint64_t full[kLdStages], empty[kLdStages], dfull;
+  uint32_t tmem_base;
+  int abort_flag;
+  int last;  // this CTA is the last split of its token tile to finish
+};
+
+__global__ void __launch_bounds__(kLdThreads, 1) k_lora_down(const __grid_constant__ LMaps maps, const LParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t abytes = static_cast<uint32_t>(p.rb) * kKS * 2;
+  const uint32_t stage_bytes = kLdH + abytes;
+  LCtrl& C = *reinterpret_cast<LCtrl*>(smem + kLdStages * stage_bytes);
+  volatile int* abort_flag = &C.abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = smem_u32(smem);
+  const int mtile = blockIdx.x / p.splits, sp = blockIdx.x % p.splits;
+  const int s0 = (sp * p.n_ks) / p.splits, s1 = ((sp + 1) * p.n_ks) / p.splits;
+  const int32_t m0 = mtile * 128;
+  if (threadIdx.x == 0) {
+    pdl_launch_dependents();
+    for (int s = 0; s < kLdStages; ++s) {
+      mbar_init(smem_u32(&C.full[s]), 1);
+      mbar_init(smem_u32(&C.empty[s]), 1);
+    }
+    mbar_init(smem_u32(&C.dfull), 1);
+    C.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&C.tmem_base), 32);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = C.tmem_base;
+  if (warp == 0) {
+    if (lane == 0) {
+      pdl_wait();  // hq and A16 come from the row prologue
+      bool ok = true;
+      int i = 0;
+      for (int s = s0; s < s1 && ok; ++s, ++i) {
+        const int st = i % kLdStages;
+        if (i >= kLdStages) ok = wait_p(smem_u32(&C.empty[st]), ((i / kLdStages) - 1) & 1, abort_flag);
+        if (!ok) break;
+        const uint32_t fb = smem_u32(&C.full[st]);
+        mbar_arrive_expect_tx(fb, stage_bytes);
+        tma_load_2d(sbase + st * stage_bytes, &maps.hq, s * kKS, m0, fb);
+        tma_load_2d(sbase + st * stage_bytes + kLdH, &maps.a16, s * kKS, 0, fb);
+      }
+      if (*abort_flag)
+        for (int d = i - kLdStages > 0 ? i - kLdStages : 0; d < i; ++d)
+          drain(smem_u32(&C.full[d % kLdStages]), (d / kLdStages) & 1);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(128, p.rb, 0);
+      bool ok = true;
+      int i = 0;
+      for (int s = s0; s < s1 && ok; ++s, ++i) {
+        const int st = i % kLdStages;
+        ok = wait_p(smem_u32(&C.full[st]), (i / kLdStages) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t hd = smem_desc_sw128(sbase + st * stage_bytes, 1024);
+        const uint64_t ad = smem_desc_sw128(sbase + st * stage_bytes + kLdH, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kKS / 16; ++kk) mma_ss(tmem, hd + 2u * kk, ad + 2u * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(smem_u32(&C.empty[st]));
+      }
+      tc_commit(smem_u32(&C.dfull));
+    }
+  } else {
+    const int quarter = warp & 3;
+    const int64_t m = static_cast<int64_t>(m0) + quarter * 32 + lane;  // < Mp
+    const bool ok = wait_p(smem_u32(&C.dfull), 0, abort_flag) && !*abort_flag && s1 > s0;
+    tc_fence_after();
+    float* part = p.t_part + (static_cast<int64_t>(sp) * p.Mp + m) * p.R4;
+    uint32_t v[16];
+    for (int jb = 0; jb < p.rb; jb += 16) {
+      tmem_ld16(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + jb, v);
+      tmem_ld_wait();
+      const float rs = (ok && m < p.M) ? p.rowscale[m] : 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (jb + j < p.R4) part[jb + j] = rs * __uint_as_float(v[j]);
+    }
+    __threadfence();
+    named_bar(1, 128);
+    if (threadIdx.x == 64) C.last = atomicAdd(&p.counters[mtile], 1) == p.splits - 1;
+    named_bar(1, 128);
+    if (C.last) {  // every split of this token tile is in memory: add them up in split order
+      __threadfence();
+      float* dst = p.t32 + m * p.R4;
+      for (int j = 0; j < p.R4; ++j) {
+        float acc = 0.f;
+        for (int q = 0; q < p.splits; ++q) acc += __ldcg(p.t_part + (static_cast<int64_t>(q) * p.Mp + m) * p.R4 + j);
+        dst[j] = acc;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 32);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void* base, uint64_t inner,
+               uint64_t outer, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  auto fn = get_encode();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * esize};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Rows of the per-token arrays (row scales, t): a multiple of both token tiles (192 for
+// the GEMM, 128 for the down-projection), so that whole tiles can be read and written.
+int64_t m_pad(int64_t M) { return (M + 383) / 384 * 384; }
+int r4(int r) { return r > 0 ? (r + 3) / 4 * 4 : 0; }
+
+constexpr int kMaxLdSplits = 8;
+
+struct PfWs {
+  __half* hq;
+  float* rowscale;
+  __half* A16;
+  float* t32;
+  float* t_part;
+  int* counters;
+  size_t bytes;
+};
+
+PfWs carve(void* ws, int64_t M, int64_t d_i, int r) {
+  PfWs w{};
+  const uintptr_t b = reinterpret_cast<uintptr_t>(ws);
+  size_t off = 0;
+  const int64_t Mp = m_pad(M);
+  w.hq = reinterpret_cast<__half*>(b + off);
+  off += align_up(static_cast<size_t>(M) * d_i * 2, 256);
+  w.rowscale = reinterpret_cast<float*>(b + off);
+  off += align_up(static_cast<size_t>(Mp) * 4, 256);
+  w.A16 = reinterpret_cast<__half*>(b + off);
+  off += align_up(static_cast<size_t>(r) * d_i * 2, 256);
+  w.t32 = reinterpret_cast<float*>(b + off);
+  off += align_up(static_cast<size_t>(Mp) * r4(r) * 4, 256);
+  w.t_part = reinterpret_cast<float*>(b + off);
+  off += align_up(static_cast<size_t>(kMaxLdSplits) * Mp * r4(r) * 4, 256);
+  w.counters = reinterpret_cast<int*>(b + off);
+  off += align_up(static_cast<size_t>((M + 127) / 128 + 4) * 4, 256);
+  w.bytes = off;
+  return w;
+}
+
+struct GPlan {
+  int stages;
+  uint32_t off_scales, off_t, t_slot_bytes, off_ctrl;
+  size_t smem;
+};
+
+GPlan gplan(int r) {
+  GPlan g{};
+  g.t_slot_bytes = static_cast<uint32_t>(align_up(static_cast<size_t>(kTN) * (r > 0 ? r4(r) * 4 + 4 : 4), 128));
+  const size_t fixed = 2 * kScaleBytes + 2 * static_cast<size_t>(g.t_slot_bytes) + sizeof(GCtrl) + 128 + 1024;
+  int st = static_cast<int>((227 * 1024 - fixed) / kStageBytes);
+  g.stages = st > kMaxStages ? kMaxStages : st;
+  g.off_scales = g.stages * kStageBytes;
+  g.off_t = g.off_scales + 2 * kScaleBytes;
+  g.off_ctrl = static_cast<uint32_t>(align_up(g.off_t + 2 * static_cast<size_t>(g.t_slot_bytes), 128));
+  g.smem = g.off_ctrl + sizeof(GCtrl) + 1024;
+  return g;
+}
+
+cudaError_t set_attributes() {
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    err = cudaFuncSetAttribute(k_gemm_nvfp4, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(k_lora_down, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  });
+  return err;
+}
+
+}  // namespace
+
+bool prefill_supported(int64_t M, int64_t d_i, int64_t d_o, int r) {
+  return M > 64 && d_i >= 256 && d_i % 256 == 0 && d_i <= 49152 && d_o >= 1 && r >= 0 && r <= kMaxR &&
+         gplan(r).stages >= 3;
+}
+
+size_t prefill_workspace_bytes(int64_t M, int64_t d_i, int64_t, int r) { return carve(nullptr, M, d_i, r).bytes; }
+
+cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream) {
+  cudaError_t e = set_attributes();
+  if (e != cudaSuccess) return e;
+  const PfWs w = carve(a.ws, a.M, a.d_i, a.r);
+  const int64_t Mp = m_pad(a.M);
+  const int R4 = r4(a.r);
+  const bool lora = a.r > 0;
+  const int mtiles = static_cast<int>((a.M + 127) / 128);  // token tiles of the LoRA down-projection
+  e = launch_act_prologue(a, w.hq, w.rowscale, w.A16, lora ? reinterpret_cast<float*>(w.counters) : nullptr,
+                          lora ? (mtiles + 3) / 4 * 4 : 0, stream);
+  if (e != cudaSuccess) return e;
+
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  const int n_ks = static_cast<int>(a.d_i / kKS);
+  const int sms = sm_count();
+
+  if (lora) {
+    LMaps lm;
+    const int rb = (a.r + 15) / 16 * 16;
+    bool ok = encode_2d(&lm.hq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.hq, a.d_i, a.M, 64, 128,
+                        CU_TENSOR_MAP_SWIZZLE_128B) &&
+              encode_2d(&lm.a16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.A16, a.d_i, a.r, 64, rb,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!ok) return cudaErrorInvalidValue;
+    LParams lp{};
+    lp.M = a.M;
+    lp.d_i = a.d_i;
+    lp.Mp = Mp;
+    lp.r = a.r;
+    lp.R4 = R4;
+    lp.rb = rb;
+    lp.n_ks = n_ks;
+    int splits = (sms + mtiles - 1) / mtiles;
+    splits = splits > kMaxLdSplits ? kMaxLdSplits : splits;
+    splits = splits > n_ks ? n_ks : (splits < 1 ? 1 : splits);  // every split has at least one K step
+    lp.splits = splits;
+    lp.rowscale = w.rowscale;
+    lp.t_part = w.t_part;
+    lp.t32 = w.t32;
+    lp.counters = w.counters;
+    cudaLaunchConfig_t c{};
+    c.gridDim = dim3(static_cast<unsigned>(mtiles * splits));
+    c.blockDim = dim3(kLdThreads);
+    c.dynamicSmemBytes = kLdStages * (kLdH + static_cast<size_t>(rb) * kKS * 2) + sizeof(LCtrl) + 1024;
+    c.stream = stream;
+    c.attrs = pdl;
+    c.numAttrs = 1;
+    e = cudaLaunchKernelEx(&c, k_lora_down, lm, lp);
+    if (e != cudaSuccess) return e;
+  }
+
+  GMaps gm;
+  bool ok = encode_2d(&gm.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.codes, a.d_i / 2, a.d_o, kKS / 2, kTO,
+                      CU_TENSOR_MAP_SWIZZLE_NONE) &&
+            encode_2d(&gm.scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.scales, a.d_i / 16, a.d_o, 16, kTO,
+                      CU_TENSOR_MAP_SWIZZLE_NONE) &&
+            encode_2d(&gm.hq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.hq, a.d_i, a.M, 64, kTN,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return cudaErrorInvalidValue;
+  const GPlan g = gplan(a.r);
+  GParams p{};
+  p.M = a.M;
+  p.d_i = a.d_i;
+  p.d_o = a.d_o;
+  p.r = a.r;
+  p.R4 = R4;
+  p.n_ot = static_cast<int>((a.d_o + kTO - 1) / kTO);
+  p.n_tiles = static_cast<int>(p.n_ot * ((a.M + kTN - 1) / kTN));
+  p.n_ks = n_ks;
+  p.stages = g.stages;
+  p.lambda = a.lambda;
+  p.s_g = a.s_g;
+  p.B = static_cast<const __nv_bfloat16*>(a.B);
+  p.rowscale = w.rowscale;
+  p.t32 = w.t32;
+  p.y = a.y;
+  p.y_f32 = a.y_f32 ? 1 : 0;
+  p.off_scales = g.off_scales;
+  p.off_t = g.off_t;
+  p.t_slot_bytes = g.t_slot_bytes;
+  p.off_ctrl = g.off_ctrl;
+  cudaLaunchConfig_t c{};
+  c.gridDim = dim3(static_cast<unsigned>(p.n_tiles < sms ? p.n_tiles : sms));
+  c.blockDim = dim3(kThreads);
+  c.dynamicSmemBytes = g.smem;
+  c.stream = stream;
+  c.attrs = pdl;
+  c.numAttrs = 1;
+  return cudaLaunchKernelEx(&c, k_gemm_nvfp4, gm, p);
+}
+
+uint32_t prefill_read_and_clear_status() {
+  uint32_t v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_pf_status, sizeof(v)) != cudaSuccess) return 0;
+  if (v) cudaMemcpyToSymbol(g_pf_status, &zero, sizeof(zero));
+  return v;
+}
+
+}  // namespace pl

@@ -129,13 +129,16 @@ constexpr int kActUnroll = 4;  // 16-byte slots per thread in flight
 
 // CTAs 0 .. M-1: one token row m each.  hz = x (.) (w + z) is kept in shared memory
 // (FP32) while sum(x^2) and max |hz| are reduced; then hq = f16(hz * inv / c_m).
-// CTAs M and up: the f16 copy of A (r x d_i), 8 elements per thread and slot.
+// CTAs M and up: the f16 copy of A (r x d_i), 8 elements per thread and slot, and
+// zeros into `zero` (n_zero floats, a multiple of 4; the accumulator of the large-M
+// LoRA down-projection), 4 per thread and slot.
 __global__ void __launch_bounds__(kActThreads) k_act(const __nv_bfloat16* __restrict__ x, int64_t M, int64_t d_i,
                                                      const float* __restrict__ w_norm,
                                                      const float* __restrict__ z, float eps,
                                                      __half* __restrict__ hq, float* __restrict__ rowscale,
                                                      const __nv_bfloat16* __restrict__ A, int r,
-                                                     __half* __restrict__ A16) {
+                                                     __half* __restrict__ A16, float* __restrict__ zero,
+                                                     int64_t n_zero) {
   extern __shared__ float4 hz4[];  // [d_i / 4]
   __shared__ float red_s[kActThreads / 32], red_m[kActThreads / 32];
   if (threadIdx.x == 0) {
@@ -155,6 +158,8 @@ __global__ void __launch_bounds__(kActThreads) k_act(const __nv_bfloat16* __rest
                      f32x2_to_f16x2(bf16lo_to_f32(v.z), bf16hi_to_f32(v.z)),
                      f32x2_to_f16x2(bf16lo_to_f32(v.w), bf16hi_to_f32(v.w)));
     }
+    for (int64_t sl = (blockIdx.x - M) * kActThreads + threadIdx.x; sl < n_zero / 4; sl += stride)
+      reinterpret_cast<float4*>(zero)[sl] = make_float4(0.f, 0.f, 0.f, 0.f);
     return;
   }
   const int64_t m = blockIdx.x;
@@ -810,7 +815,8 @@ cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   c1.attrs = attrs;
   c1.numAttrs = 1;
   e = cudaLaunchKernelEx(&c1, k_act, static_cast<const __nv_bfloat16*>(a.x), a.M, a.d_i, a.w_norm, a.z, a.eps,
-                         w.hq, w.rowscale, static_cast<const __nv_bfloat16*>(a.A), a.r, w.A16);
+                         w.hq, w.rowscale, static_cast<const __nv_bfloat16*>(a.A), a.r, w.A16,
+                         static_cast<float*>(nullptr), static_cast<int64_t>(0));
   if (e != cudaSuccess) return e;
 
   TcParams p{};
@@ -840,6 +846,27 @@ cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   c2.attrs = attrs;
   c2.numAttrs = 2;
   return cudaLaunchKernelEx(&c2, k_tc_decode, maps, p);
+}
+
+cudaError_t launch_act_prologue(const LinearArgs& a, __half* hq, float* rowscale, __half* A16, float* zero,
+                                int64_t n_zero, cudaStream_t stream) {
+  cudaError_t e = set_kernel_attributes();
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  const int64_t a_slots = static_cast<int64_t>(a.r) * a.d_i / 8 + n_zero / 4;
+  int nconv = static_cast<int>((a_slots + kActThreads * 4 - 1) / (kActThreads * 4));
+  nconv = a_slots > 0 ? (nconv < 1 ? 1 : (nconv > 64 ? 64 : nconv)) : 0;
+  cudaLaunchConfig_t c{};
+  c.gridDim = dim3(static_cast<unsigned>(a.M + nconv));
+  c.blockDim = dim3(kActThreads);
+  c.dynamicSmemBytes = static_cast<size_t>(a.d_i) * 4;
+  c.stream = stream;
+  c.attrs = attr;
+  c.numAttrs = 1;
+  return cudaLaunchKernelEx(&c, k_act, static_cast<const __nv_bfloat16*>(a.x), a.M, a.d_i, a.w_norm, a.z, a.eps, hq,
+                            rowscale, static_cast<const __nv_bfloat16*>(a.A), a.r, A16, zero, n_zero);
 }
 
 cudaError_t launch_wait_timeout_probe(cudaStream_t stream) {
