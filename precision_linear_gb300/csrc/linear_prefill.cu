@@ -18,11 +18,12 @@
 //     warp 0      TMA: per 64-wide K step the hq tile (192 x 64 f16, 128-byte swizzle) and
 //                 the packed codes (128 x 32 B); every 4th step the E4M3 scales of the next
 //                 256 K (128 x 16 B); per tile the t32 rows and row scales of its tokens;
-//     warps 2-5   dequantise each K step into a 32-column tensor-memory slot (E2M1 -> f16
-//                 conversion times the f16 block scale: exact), one weight row per thread;
+//     warps 2-9   dequantise each K step into a 32-column tensor-memory slot (E2M1 -> f16
+//                 conversion times the f16 block scale: exact), one weight row and half
+//                 of the step per thread;
 //     warp 1      tcgen05.mma kind::f16, M = 128, N = 192, K = 16: D (tensor memory, two
 //                 buffers of 192 columns) += W_hat / s_g x hq^T;
-//     warps 6-13  epilogue of the previous tile while the next one accumulates:
+//     warps 10-13 epilogue of the previous tile while the next one accumulates:
 //                 y[m, o] = s_g rowscale[m] D[o, m] + lambda sum_j B[o, j] t32[m, j] (FP32),
 //                 stored as BF16 or FP32.
 //
@@ -38,6 +39,16 @@ namespace pl {
 
 __device__ uint32_t g_pf_status = 0;
 
+// Per-CTA wait accounting for development builds (-DPL_TIMELINE); compiled out otherwise.
+#ifdef PL_TIMELINE
+__device__ unsigned long long g_pf_wait[1024][12];
+#define PF_T0() const uint64_t pf_t0_ = globaltimer_ns()
+#define PF_ACC(slot) do { if (blockIdx.x < 1024) atomicAdd(&g_pf_wait[blockIdx.x][slot], globaltimer_ns() - pf_t0_); } while (0)
+#else
+#define PF_T0() do { } while (0)
+#define PF_ACC(slot) do { } while (0)
+#endif
+
 namespace {
 
 constexpr int kTO = 128;  // weight rows per tile
@@ -49,8 +60,8 @@ constexpr uint32_t kHBytes = kTN * kKS * 2;     // 24 KB
 constexpr uint32_t kCodeBytes = kTO * kKS / 2;  // 4 KB
 constexpr uint32_t kStageBytes = kHBytes + kCodeBytes;
 constexpr uint32_t kScaleBytes = kTO * 16;      // scales of 256 K
-constexpr int kDeqWarps = 4;
-constexpr int kEpiWarps = 8;
+constexpr int kDeqWarps = 8;  // two per tensor-memory lane quarter: each dequantises half of a K step
+constexpr int kEpiWarps = 4;
 constexpr int kThreads = (2 + kDeqWarps + kEpiWarps) * 32;  // 448
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColD0 = 128;  // D buffer b at columns [128 + 192 b, 320 + 192 b); weight slots below
@@ -104,6 +115,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
   const bool lora = p.r > 0;
 
   if (threadIdx.x == 0) {
+#ifdef PL_TIMELINE
+    if (blockIdx.x < 1024) g_pf_wait[blockIdx.x][10] = globaltimer_ns();
+#endif
     pdl_launch_dependents();
     for (int s = 0; s < nst; ++s) {
       mbar_init(smem_u32(&C.full[s]), 1);
@@ -140,7 +154,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       pdl_wait();  // hq, row scales and t32 come from the preceding kernels
-      const uint64_t pol_w = policy_evict_first();  // each weight tile is read by 1/n_mt of the CTAs at a time
       const uint32_t tbytes = static_cast<uint32_t>(kTN) * (lora ? p.R4 * 4 + 4 : 4);
       bool ok = true;
       int64_t gs = 0;
@@ -150,7 +163,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
         const int32_t m0 = mt * kTN, o0 = ot * kTO;
         {  // this tile's t32 rows and row scales
           const int tb = it & 1;
-          if (it >= 2) ok = wait_p(smem_u32(&C.tempty[tb]), ((it >> 1) - 1) & 1, abort_flag);
+          {
+            PF_T0();
+            if (it >= 2) ok = wait_p(smem_u32(&C.tempty[tb]), ((it >> 1) - 1) & 1, abort_flag);
+            PF_ACC(1);
+          }
           if (!ok) break;
           const uint32_t tb_bar = smem_u32(&C.tfull[tb]);
           const uint32_t dst = sbase + p.off_t + tb * p.t_slot_bytes;
@@ -161,18 +178,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
         }
         for (int s = 0; s < n_ks && ok; ++s, ++gs) {
           const int st = static_cast<int>(gs % nst);
-          if (gs >= nst) ok = wait_p(smem_u32(&C.empty[st]), static_cast<uint32_t>((gs / nst) - 1) & 1, abort_flag);
+          {
+            PF_T0();
+            if (gs >= nst) ok = wait_p(smem_u32(&C.empty[st]), static_cast<uint32_t>((gs / nst) - 1) & 1, abort_flag);
+            PF_ACC(0);
+          }
           if (!ok) break;
           const uint32_t fb = smem_u32(&C.full[st]);
           const bool scl = (s & 3) == 0;
           mbar_arrive_expect_tx(fb, kStageBytes + (scl ? kScaleBytes : 0));
           const uint32_t stage = sbase + st * kStageBytes;
           tma_load_2d(stage, &maps.hq, s * kKS, m0, fb);
-          tma_load_2d_hint(stage + kHBytes, &maps.codes, s * (kKS / 2), o0, fb, pol_w);
+          // weights and hq both stay in L2: every weight tile is read once per token tile
+          tma_load_2d(stage + kHBytes, &maps.codes, s * (kKS / 2), o0, fb);
           if (scl) {
             const int64_t grp = static_cast<int64_t>(it) * (n_ks / 4) + s / 4;
-            tma_load_2d_hint(sbase + p.off_scales + static_cast<uint32_t>(grp & 1) * kScaleBytes, &maps.scales,
-                             s * (kKS / 16), o0, fb, pol_w);
+            tma_load_2d(sbase + p.off_scales + static_cast<uint32_t>(grp & 1) * kScaleBytes, &maps.scales,
+                        s * (kKS / 16), o0, fb);
           }
         }
       }
@@ -192,14 +214,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
       int it = 0;
       for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x, ++it) {
         const int b = it & 1;
-        if (it >= 2) ok = wait_p(smem_u32(&C.dempty[b]), ((it >> 1) - 1) & 1, abort_flag);
+        {
+          PF_T0();
+          if (it >= 2) ok = wait_p(smem_u32(&C.dempty[b]), ((it >> 1) - 1) & 1, abort_flag);
+          PF_ACC(2);
+        }
         if (!ok) break;
         tc_fence_after();
         const uint32_t d = tmem + (kColD0 + 192u * b);
         for (int s = 0; s < n_ks && ok; ++s, ++gs) {
           const int st = static_cast<int>(gs % nst), a = static_cast<int>(gs % kASlots);
-          ok = wait_p(smem_u32(&C.full[st]), static_cast<uint32_t>(gs / nst) & 1, abort_flag) &&
-               wait_p(smem_u32(&C.afull[a]), static_cast<uint32_t>(gs / kASlots) & 1, abort_flag);
+          {
+            PF_T0();
+            ok = wait_p(smem_u32(&C.full[st]), static_cast<uint32_t>(gs / nst) & 1, abort_flag);
+            PF_ACC(3);
+          }
+          {
+            PF_T0();
+            ok = ok && wait_p(smem_u32(&C.afull[a]), static_cast<uint32_t>(gs / kASlots) & 1, abort_flag);
+            PF_ACC(4);
+          }
           if (!ok) break;
           tc_fence_after();
           const uint64_t hdesc = smem_desc_sw128(sbase + st * kStageBytes, 1024);
@@ -217,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
     }
   } else if (warp < 2 + kDeqWarps) {
     // ---------------------------------------------------------------- dequant
-    const int quarter = warp & 3, row = quarter * 32 + lane;
+    const int quarter = warp & 3, row = quarter * 32 + lane, g = (warp - 2) >> 2;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     bool ok = true;
     int64_t gs = 0;
@@ -225,28 +259,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
     for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x, ++it) {
       for (int s = 0; s < n_ks && ok; ++s, ++gs) {
         const int st = static_cast<int>(gs % nst), a = static_cast<int>(gs % kASlots);
-        ok = wait_p(smem_u32(&C.full[st]), static_cast<uint32_t>(gs / nst) & 1, abort_flag) &&
-             (gs < kASlots || wait_p(smem_u32(&C.aempty[a]), static_cast<uint32_t>((gs / kASlots) - 1) & 1, abort_flag));
+        {
+          PF_T0();
+          ok = wait_p(smem_u32(&C.full[st]), static_cast<uint32_t>(gs / nst) & 1, abort_flag);
+          if (lane == 0 && warp == 2) PF_ACC(5);
+        }
+        {
+          PF_T0();
+          ok = ok && (gs < kASlots || wait_p(smem_u32(&C.aempty[a]), static_cast<uint32_t>((gs / kASlots) - 1) & 1, abort_flag));
+          if (lane == 0 && warp == 2) PF_ACC(6);
+        }
         if (!ok) break;
         const uint8_t* stage = smem + st * kStageBytes;
-        const uint4 c0 = *reinterpret_cast<const uint4*>(stage + kHBytes + row * 32);
-        const uint4 c1 = *reinterpret_cast<const uint4*>(stage + kHBytes + row * 32 + 16);
+        const uint4 cw = *reinterpret_cast<const uint4*>(stage + kHBytes + row * 32 + g * 16);  // 32 codes
         const int64_t grp = static_cast<int64_t>(it) * (n_ks / 4) + s / 4;
-        const uint32_t sw = *reinterpret_cast<const uint32_t*>(smem + p.off_scales + static_cast<uint32_t>(grp & 1) * kScaleBytes +
-                                                                row * 16 + (s & 3) * 4);
-        const uint32_t s01 = cvt_e4m3x2_to_f16x2(sw & 0xFFFFu), s23 = cvt_e4m3x2_to_f16x2(sw >> 16);
-        const uint32_t sc[4] = {prmt(s01, s01, 0x1010u), prmt(s01, s01, 0x3232u), prmt(s23, s23, 0x1010u),
-                                prmt(s23, s23, 0x3232u)};
-        const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        const uint32_t sw = *reinterpret_cast<const uint16_t*>(smem + p.off_scales + static_cast<uint32_t>(grp & 1) * kScaleBytes +
+                                                                row * 16 + (s & 3) * 4 + g * 2);
+        const uint32_t s01 = cvt_e4m3x2_to_f16x2(sw);
+        const uint32_t sa = prmt(s01, s01, 0x1010u), sb = prmt(s01, s01, 0x3232u);
+        uint32_t v[16];
+        e2m1x8_to_f16x8(cw.x, v[0], v[1], v[2], v[3]);
+        e2m1x8_to_f16x8(cw.y, v[4], v[5], v[6], v[7]);
+        e2m1x8_to_f16x8(cw.z, v[8], v[9], v[10], v[11]);
+        e2m1x8_to_f16x8(cw.w, v[12], v[13], v[14], v[15]);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {  // 32 weights (2 scale blocks) per tensor-memory store
-          uint32_t v[16];
+        for (int i = 0; i < 8; ++i) v[i] = hmul2_u32(v[i], sa);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) e2m1x8_to_f16x8(cw[4 * h + q], v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = hmul2_u32(v[i], sc[2 * h + (i >> 3)]);
-          tmem_st16(tmem + lane_addr + 32u * a + 16u * h, v);
-        }
+        for (int i = 8; i < 16; ++i) v[i] = hmul2_u32(v[i], sb);
+        tmem_st16(tmem + lane_addr + 32u * a + 16u * g, v);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -258,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
     }
   } else {
     // ---------------------------------------------------------------- epilogue
-    const int quarter = warp & 3, half = (warp - 2 - kDeqWarps) >> 2;
+    const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const float s_g = C.s_g;
@@ -271,14 +311,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
       float bo[kMaxR];
 #pragma unroll
       for (int j = 0; j < kMaxR; ++j) bo[j] = (lora && j < p.r && o < p.d_o) ? __bfloat162float(p.B[o * p.r + j]) : 0.f;
-      ok = wait_p(smem_u32(&C.dfull[b]), (it >> 1) & 1, abort_flag) &&
-           wait_p(smem_u32(&C.tfull[b]), (it >> 1) & 1, abort_flag);
+      {
+        PF_T0();
+        ok = wait_p(smem_u32(&C.dfull[b]), (it >> 1) & 1, abort_flag) &&
+             wait_p(smem_u32(&C.tfull[b]), (it >> 1) & 1, abort_flag);
+        if (lane == 0 && warp == 10) PF_ACC(7);
+      }
       if (!ok) break;
       tc_fence_after();
       const float* ts = reinterpret_cast<const float*>(smem + p.off_t + b * p.t_slot_bytes);
       const float* rsc = ts + (lora ? kTN * p.R4 : 0);
-      for (int cb = 0; cb < kTN / 2 / 16; ++cb) {
-        const int col = half * (kTN / 2) + cb * 16;  // token columns [col, col + 16) of the tile
+      for (int cb = 0; cb < kTN / 16; ++cb) {
+        const int col = cb * 16;  // token columns [col, col + 16) of the tile
         uint32_t dv[16];
         tmem_ld16(tmem + lane_addr + (kColD0 + 192u * b) + col, dv);
         tmem_ld_wait();
@@ -320,6 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+#ifdef PL_TIMELINE
+  if (threadIdx.x == 0 && blockIdx.x < 1024) g_pf_wait[blockIdx.x][11] = globaltimer_ns();
+#endif
 }
 
 // ------------------------------------------------------------------ LoRA down-projection
@@ -644,6 +691,15 @@ cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream) {
   c.numAttrs = 1;
   return cudaLaunchKernelEx(&c, k_gemm_nvfp4, gm, p);
 }
+
+#ifdef PL_TIMELINE
+extern "C" int pl_debug_read_prefill_waits(unsigned long long* out) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return 1;
+  if (cudaMemcpyFromSymbol(out, g_pf_wait, sizeof(g_pf_wait)) != cudaSuccess) return 2;
+  static unsigned long long zero[1024][12];
+  return cudaMemcpyToSymbol(g_pf_wait, zero, sizeof(zero)) != cudaSuccess ? 3 : 0;
+}
+#endif
 
 uint32_t prefill_read_and_clear_status() {
   uint32_t v = 0, zero = 0;
