@@ -72,6 +72,7 @@ const char* pl_status_string(pl_status s) {
     case PL_ERR_CUDA: return "PL_ERR_CUDA: CUDA launch or runtime call failed";
     case PL_ERR_WORKSPACE: return "PL_ERR_WORKSPACE: workspace missing, misaligned or too small";
     case PL_ERR_TIMEOUT: return "PL_ERR_TIMEOUT: a bounded device-side wait gave up";
+    case PL_ERR_RANGE: return "PL_ERR_RANGE: the large-M LoRA operands left the f16 range";
   }
   return "unknown pl_status";
 }
@@ -151,7 +152,8 @@ pl_status pl_last_device_status(pl_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return PL_ERR_CUDA;
   uint32_t bits = pl::tc_read_and_clear_status() | pl::fused_read_and_clear_status() |
                   pl::prefill_read_and_clear_status();
-  return (bits & pl::kStatusTimeout) ? PL_ERR_TIMEOUT : PL_OK;
+  if (bits & pl::kStatusTimeout) return PL_ERR_TIMEOUT;
+  return (bits & pl::kStatusRange) ? PL_ERR_RANGE : PL_OK;
 }
 
 int pl_debug_linear_path(int64_t M, int64_t d_i, int64_t d_o, int r) {

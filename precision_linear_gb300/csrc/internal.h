@@ -9,7 +9,7 @@
 namespace pl {
 
 // Device-side status bits set by bounded waits that gave up.
-enum : uint32_t { kStatusTimeout = 1u };
+enum : uint32_t { kStatusTimeout = 1u, kStatusRange = 2u };
 
 // ---- quantize.cu
 cudaError_t launch_quantize(const void* W, int64_t d_o, int64_t d_i, uint8_t* codes,

@@ -6,26 +6,33 @@
 // RMSNorm-AQN of x.  Three kernels, chained by programmatic dependent launch:
 //
 //   k_act (linear_tc.cu)  per token row: hq = f16(h / rowscale) with rowscale a power of
-//                         two (max |hq| in [2^13, 2^14)); A -> f16; split counters := 0.
-//   k_lora_down           t[m, :] = rowscale[m] sum_k A[:, k] hq[m, k]: each CTA one K split
-//                         of 128 tokens (tcgen05.mma, 128 x r, K = 16 steps, from TMA-staged
-//                         hq and f16 A tiles, FP32 accumulator in tensor memory) into its
-//                         partial; the last split of a token tile to finish adds the partials
-//                         up in split order (deterministic) into t32.
+//                         two (max |hq| in [2^13, 2^14)); A -> f16; split counters and the
+//                         two maxima below := 0.
+//   k_lora_down           T[m, :] = (lambda / s_g) sum_k A[:, k] hq[m, k]: each CTA one K
+//                         split of 128 tokens (tcgen05.mma, 128 x r, K = 16 steps, from
+//                         TMA-staged hq and f16 A tiles, FP32 accumulator in tensor memory)
+//                         into its partial; the last split of a token tile to finish adds
+//                         the partials up in split order (deterministic).  Also max |T| and
+//                         max |B| over the whole call.
+//   k_lora_pack           the LoRA up-projection as 64 more K columns of the contraction:
+//                         Bq = f16(B 2^beta) [d_o][64] and Tq = f16(T 2^-beta) [M][64] (zero
+//                         beyond r), beta a power of two that puts both maxima at the same
+//                         magnitude, so that s_g rowscale[m] sum_j Bq[o, j] Tq[m, j] =
+//                         lambda sum_j B[o, j] t[m, j] with t = A h.
 //   k_gemm_nvfp4          the dense contraction, persistent over 128 (weight rows) x 192
 //                         (tokens) tiles, o-tiles fastest so that concurrent CTAs share
 //                         their hq tiles in L2:
 //     warp 0      TMA: per 64-wide K step the hq tile (192 x 64 f16, 128-byte swizzle) and
 //                 the packed codes (128 x 32 B); every 4th step the E4M3 scales of the next
-//                 256 K (128 x 16 B); per tile the t32 rows and row scales of its tokens;
+//                 256 K (128 x 16 B); one more step per tile with the Tq rows of its
+//                 tokens; per tile the row scales of its tokens;
 //     warps 2-9   dequantise each K step into a 32-column tensor-memory slot (E2M1 -> f16
 //                 conversion times the f16 block scale: exact), one weight row and half
-//                 of the step per thread;
+//                 of the step per thread; the LoRA step gets the Bq rows instead;
 //     warp 1      tcgen05.mma kind::f16, M = 128, N = 192, K = 16: D (tensor memory, two
-//                 buffers of 192 columns) += W_hat / s_g x hq^T;
+//                 buffers of 192 columns) += W_hat / s_g x hq^T + Bq x Tq^T;
 //     warps 10-13 epilogue of the previous tile while the next one accumulates:
-//                 y[m, o] = s_g rowscale[m] D[o, m] + lambda sum_j B[o, j] t32[m, j] (FP32),
-//                 stored as BF16 or FP32.
+//                 y[m, o] = s_g rowscale[m] D[o, m], stored as BF16 or FP32.
 //
 // Every mbarrier wait is bounded (200 ms); a wait that gives up sets the status word,
 // the CTA stops issuing work, drains its copies, frees its tensor memory and returns.
@@ -66,22 +73,21 @@ constexpr int kThreads = (2 + kDeqWarps + kEpiWarps) * 32;  // 448
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColD0 = 128;  // D buffer b at columns [128 + 192 b, 320 + 192 b); weight slots below
 constexpr int kMaxR = 32;
+constexpr int kLoraK = 64;  // K columns the LoRA step adds (r <= 32 of them nonzero)
 
 struct GParams {
   int64_t M, d_i, d_o;
-  int r, R4, n_ot, n_tiles, n_ks, stages;
-  float lambda;
+  int r, n_ot, n_tiles, n_ks, stages;
   const float* s_g;
-  const __nv_bfloat16* B;
+  const __half* Bq;       // [d_o][64]
   const float* rowscale;  // [M_pad]
-  const float* t32;       // [M_pad][R4]
   void* y;
   int y_f32;
   uint32_t off_scales, off_t, t_slot_bytes, off_ctrl;
 };
 
 struct GMaps {
-  CUtensorMap codes, scales, hq;
+  CUtensorMap codes, scales, hq, tq;
 };
 
 struct GCtrl {
@@ -113,6 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
   const uint32_t sbase = smem_u32(smem);
   const int nst = p.stages, n_ks = p.n_ks;
   const bool lora = p.r > 0;
+  const int n_steps = n_ks + (lora ? 1 : 0);  // K steps per tile, the LoRA step last
 
   if (threadIdx.x == 0) {
 #ifdef PL_TIMELINE
@@ -154,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       pdl_wait();  // hq, row scales and t32 come from the preceding kernels
-      const uint32_t tbytes = static_cast<uint32_t>(kTN) * (lora ? p.R4 * 4 + 4 : 4);
+      const uint32_t tbytes = static_cast<uint32_t>(kTN) * 4;
       bool ok = true;
       int64_t gs = 0;
       int it = 0, t_issued = 0;
@@ -172,11 +179,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
           const uint32_t tb_bar = smem_u32(&C.tfull[tb]);
           const uint32_t dst = sbase + p.off_t + tb * p.t_slot_bytes;
           mbar_arrive_expect_tx(tb_bar, tbytes);
-          if (lora) bulk_g2s(dst, p.t32 + static_cast<int64_t>(m0) * p.R4, kTN * p.R4 * 4, tb_bar);
-          bulk_g2s(dst + (lora ? kTN * p.R4 * 4 : 0), p.rowscale + m0, kTN * 4, tb_bar);
+          bulk_g2s(dst, p.rowscale + m0, kTN * 4, tb_bar);
           ++t_issued;
         }
-        for (int s = 0; s < n_ks && ok; ++s, ++gs) {
+        for (int s = 0; s < n_steps && ok; ++s, ++gs) {
           const int st = static_cast<int>(gs % nst);
           {
             PF_T0();
@@ -185,6 +191,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
           }
           if (!ok) break;
           const uint32_t fb = smem_u32(&C.full[st]);
+          if (s == n_ks) {  // the LoRA step: Tq rows of this token tile
+            mbar_arrive_expect_tx(fb, kHBytes);
+            tma_load_2d(sbase + st * kStageBytes, &maps.tq, 0, m0, fb);
+            continue;
+          }
           const bool scl = (s & 3) == 0;
           mbar_arrive_expect_tx(fb, kStageBytes + (scl ? kScaleBytes : 0));
           const uint32_t stage = sbase + st * kStageBytes;
@@ -222,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
         if (!ok) break;
         tc_fence_after();
         const uint32_t d = tmem + (kColD0 + 192u * b);
-        for (int s = 0; s < n_ks && ok; ++s, ++gs) {
+        for (int s = 0; s < n_steps && ok; ++s, ++gs) {
           const int st = static_cast<int>(gs % nst), a = static_cast<int>(gs % kASlots);
           {
             PF_T0();
@@ -253,11 +264,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
     // ---------------------------------------------------------------- dequant
     const int quarter = warp & 3, row = quarter * 32 + lane, g = (warp - 2) >> 2;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    if (lora) pdl_wait();  // Bq comes from the preceding kernel
     bool ok = true;
     int64_t gs = 0;
     int it = 0;
     for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x, ++it) {
-      for (int s = 0; s < n_ks && ok; ++s, ++gs) {
+      const int ot = tile % p.n_ot;
+      const int64_t o = static_cast<int64_t>(ot) * kTO + row;
+      uint4 bq[4] = {};  // this thread's half of its Bq row, for the LoRA step
+      if (lora && o < p.d_o) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.Bq + o * kLoraK + 32 * g);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) bq[q] = src[q];
+      }
+      for (int s = 0; s < n_steps && ok; ++s, ++gs) {
         const int st = static_cast<int>(gs % nst), a = static_cast<int>(gs % kASlots);
         {
           PF_T0();
@@ -270,22 +290,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
           if (lane == 0 && warp == 2) PF_ACC(6);
         }
         if (!ok) break;
-        const uint8_t* stage = smem + st * kStageBytes;
-        const uint4 cw = *reinterpret_cast<const uint4*>(stage + kHBytes + row * 32 + g * 16);  // 32 codes
-        const int64_t grp = static_cast<int64_t>(it) * (n_ks / 4) + s / 4;
-        const uint32_t sw = *reinterpret_cast<const uint16_t*>(smem + p.off_scales + static_cast<uint32_t>(grp & 1) * kScaleBytes +
-                                                                row * 16 + (s & 3) * 4 + g * 2);
-        const uint32_t s01 = cvt_e4m3x2_to_f16x2(sw);
-        const uint32_t sa = prmt(s01, s01, 0x1010u), sb = prmt(s01, s01, 0x3232u);
         uint32_t v[16];
-        e2m1x8_to_f16x8(cw.x, v[0], v[1], v[2], v[3]);
-        e2m1x8_to_f16x8(cw.y, v[4], v[5], v[6], v[7]);
-        e2m1x8_to_f16x8(cw.z, v[8], v[9], v[10], v[11]);
-        e2m1x8_to_f16x8(cw.w, v[12], v[13], v[14], v[15]);
+        if (s == n_ks) {
+          const uint32_t w16[16] = {bq[0].x, bq[0].y, bq[0].z, bq[0].w, bq[1].x, bq[1].y, bq[1].z, bq[1].w,
+                                    bq[2].x, bq[2].y, bq[2].z, bq[2].w, bq[3].x, bq[3].y, bq[3].z, bq[3].w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = hmul2_u32(v[i], sa);
+          for (int i = 0; i < 16; ++i) v[i] = w16[i];
+        } else {
+          const uint8_t* stage = smem + st * kStageBytes;
+          const uint4 cw = *reinterpret_cast<const uint4*>(stage + kHBytes + row * 32 + g * 16);  // 32 codes
+          const int64_t grp = static_cast<int64_t>(it) * (n_ks / 4) + s / 4;
+          const uint32_t sw = *reinterpret_cast<const uint16_t*>(smem + p.off_scales + static_cast<uint32_t>(grp & 1) * kScaleBytes +
+                                                                  row * 16 + (s & 3) * 4 + g * 2);
+          const uint32_t s01 = cvt_e4m3x2_to_f16x2(sw);
+          const uint32_t sa = prmt(s01, s01, 0x1010u), sb = prmt(s01, s01, 0x3232u);
+          e2m1x8_to_f16x8(cw.x, v[0], v[1], v[2], v[3]);
+          e2m1x8_to_f16x8(cw.y, v[4], v[5], v[6], v[7]);
+          e2m1x8_to_f16x8(cw.z, v[8], v[9], v[10], v[11]);
+          e2m1x8_to_f16x8(cw.w, v[12], v[13], v[14], v[15]);
 #pragma unroll
-        for (int i = 8; i < 16; ++i) v[i] = hmul2_u32(v[i], sb);
+          for (int i = 0; i < 8; ++i) v[i] = hmul2_u32(v[i], sa);
+#pragma unroll
+          for (int i = 8; i < 16; ++i) v[i] = hmul2_u32(v[i], sb);
+        }
         tmem_st16(tmem + lane_addr + 32u * a + 16u * g, v);
         tmem_st_wait();
         tc_fence_before();
@@ -308,9 +335,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
       const int mt = tile / p.n_ot, ot = tile % p.n_ot;
       const int b = it & 1;
       const int64_t o = static_cast<int64_t>(ot) * kTO + row;
-      float bo[kMaxR];
-#pragma unroll
-      for (int j = 0; j < kMaxR; ++j) bo[j] = (lora && j < p.r && o < p.d_o) ? __bfloat162float(p.B[o * p.r + j]) : 0.f;
       {
         PF_T0();
         ok = wait_p(smem_u32(&C.dfull[b]), (it >> 1) & 1, abort_flag) &&
@@ -319,34 +343,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
       }
       if (!ok) break;
       tc_fence_after();
-      const float* ts = reinterpret_cast<const float*>(smem + p.off_t + b * p.t_slot_bytes);
-      const float* rsc = ts + (lora ? kTN * p.R4 : 0);
+      const float* rsc = reinterpret_cast<const float*>(smem + p.off_t + b * p.t_slot_bytes);
       for (int cb = 0; cb < kTN / 16; ++cb) {
         const int col = cb * 16;  // token columns [col, col + 16) of the tile
         uint32_t dv[16];
         tmem_ld16(tmem + lane_addr + (kColD0 + 192u * b) + col, dv);
         tmem_ld_wait();
-#pragma unroll 4
-        for (int i = 0; i < 16; ++i) {
-          const int ml = col + i;
-          const int64_t m = static_cast<int64_t>(mt) * kTN + ml;
-          float v = s_g * rsc[ml] * __uint_as_float(dv[i]);
-          if (lora) {
-            const float4* t4 = reinterpret_cast<const float4*>(ts + ml * p.R4);
-            float l0 = 0.f, l1 = 0.f;
+        if (o < p.d_o) {
 #pragma unroll
-            for (int j4 = 0; j4 < kMaxR / 4; ++j4) {
-              if (4 * j4 < p.r) {
-                const float4 t = t4[j4];
-                l0 = fmaf(bo[4 * j4], t.x, fmaf(bo[4 * j4 + 1], t.y, l0));
-                l1 = fmaf(bo[4 * j4 + 2], t.z, fmaf(bo[4 * j4 + 3], t.w, l1));
-              }
+          for (int i = 0; i < 16; ++i) {
+            const int64_t m = static_cast<int64_t>(mt) * kTN + col + i;
+            const float v = s_g * rsc[col + i] * __uint_as_float(dv[i]);
+            if (m < p.M) {
+              if (p.y_f32) static_cast<float*>(p.y)[m * p.d_o + o] = v;
+              else static_cast<__nv_bfloat16*>(p.y)[m * p.d_o + o] = __float2bfloat16_rn(v);
             }
-            v = fmaf(p.lambda, l0 + l1, v);
-          }
-          if (m < p.M && o < p.d_o) {
-            if (p.y_f32) static_cast<float*>(p.y)[m * p.d_o + o] = v;
-            else static_cast<__nv_bfloat16*>(p.y)[m * p.d_o + o] = __float2bfloat16_rn(v);
           }
         }
       }
@@ -375,12 +386,15 @@ constexpr int kLdThreads = 6 * 32;  // TMA, MMA, 4 epilogue warps
 constexpr uint32_t kLdH = 128 * kKS * 2;  // 16 KB
 
 struct LParams {
-  int64_t M, d_i, Mp;
+  int64_t M, d_i, Mp, n_b;
   int r, R4, rb, n_ks, splits;
-  const float* rowscale;
-  float* t_part;  // [splits][Mp][R4]
-  float* t32;     // [Mp][R4]
-  int* counters;  // [token tiles], zero on entry
+  float lambda;
+  const float* s_g;
+  const __nv_bfloat16* B;  // [d_o][r]: n_b elements, for max |B|
+  float* t_part;           // [splits][Mp][R4]
+  float* t32;              // [Mp][R4]: T = (lambda / s_g) A hq
+  int* counters;           // [token tiles], then max |T| and max |B| (FP32 bits); zero on entry
+  int mtiles;
 };
 struct LMaps {
   CUtensorMap hq, a16;
@@ -460,18 +474,27 @@ __global__ void __launch_bounds__(kLdThreads, 1) k_lora_down(const __grid_consta
     }
   } else {
     const int quarter = warp & 3;
+    const int et = threadIdx.x - 64;  // 0 .. 127
     const int64_t m = static_cast<int64_t>(m0) + quarter * 32 + lane;  // < Mp
     const bool ok = wait_p(smem_u32(&C.dfull), 0, abort_flag) && !*abort_flag && s1 > s0;
     tc_fence_after();
+    unsigned int* maxima = reinterpret_cast<unsigned int*>(p.counters + p.mtiles);  // [0] max |T|, [1] max |B|
+    {  // max |B| over this CTA's share of B (after the wait: the maxima were zeroed by the prologue)
+      float mb = 0.f;
+      for (int64_t i = static_cast<int64_t>(blockIdx.x) * 128 + et; i < p.n_b; i += static_cast<int64_t>(gridDim.x) * 128)
+        mb = fmaxf(mb, fabsf(__bfloat162float(p.B[i])));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, o));
+      if (lane == 0) atomicMax(&maxima[1], __float_as_uint(mb));
+    }
     float* part = p.t_part + (static_cast<int64_t>(sp) * p.Mp + m) * p.R4;
     uint32_t v[16];
     for (int jb = 0; jb < p.rb; jb += 16) {
       tmem_ld16(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + jb, v);
       tmem_ld_wait();
-      const float rs = (ok && m < p.M) ? p.rowscale[m] : 0.f;
 #pragma unroll
       for (int j = 0; j < 16; ++j)
-        if (jb + j < p.R4) part[jb + j] = rs * __uint_as_float(v[j]);
+        if (jb + j < p.R4) part[jb + j] = (ok && m < p.M) ? __uint_as_float(v[j]) : 0.f;
     }
     __threadfence();
     named_bar(1, 128);
@@ -479,12 +502,36 @@ __global__ void __launch_bounds__(kLdThreads, 1) k_lora_down(const __grid_consta
     named_bar(1, 128);
     if (C.last) {  // every split of this token tile is in memory: add them up in split order
       __threadfence();
-      float* dst = p.t32 + m * p.R4;
-      for (int j = 0; j < p.R4; ++j) {
-        float acc = 0.f;
-        for (int q = 0; q < p.splits; ++q) acc += __ldcg(p.t_part + (static_cast<int64_t>(q) * p.Mp + m) * p.R4 + j);
-        dst[j] = acc;
+      const float f = p.lambda / *p.s_g;
+      float acc[kMaxR];
+#pragma unroll
+      for (int j = 0; j < kMaxR; ++j) acc[j] = 0.f;
+      for (int q = 0; q < p.splits; ++q) {  // all loads of one split issued together
+        const float4* src = reinterpret_cast<const float4*>(p.t_part + (static_cast<int64_t>(q) * p.Mp + m) * p.R4);
+        float4 v[kMaxR / 4];
+#pragma unroll
+        for (int j4 = 0; j4 < kMaxR / 4; ++j4) v[j4] = 4 * j4 < p.R4 ? __ldcg(src + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j4 = 0; j4 < kMaxR / 4; ++j4) {
+          acc[4 * j4] += v[j4].x;
+          acc[4 * j4 + 1] += v[j4].y;
+          acc[4 * j4 + 2] += v[j4].z;
+          acc[4 * j4 + 3] += v[j4].w;
+        }
       }
+      float4* dst = reinterpret_cast<float4*>(p.t32 + m * p.R4);
+      float mt = 0.f;
+#pragma unroll
+      for (int j4 = 0; j4 < kMaxR / 4; ++j4) {
+        if (4 * j4 < p.R4) {
+          const float4 t = make_float4(f * acc[4 * j4], f * acc[4 * j4 + 1], f * acc[4 * j4 + 2], f * acc[4 * j4 + 3]);
+          dst[j4] = t;
+          mt = fmaxf(mt, fmaxf(fmaxf(fabsf(t.x), fabsf(t.y)), fmaxf(fabsf(t.z), fabsf(t.w))));
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, o));
+      if (lane == 0) atomicMax(&maxima[0], __float_as_uint(mt));
     }
   }
   tc_fence_before();
@@ -492,6 +539,44 @@ __global__ void __launch_bounds__(kLdThreads, 1) k_lora_down(const __grid_consta
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 32);
+  }
+}
+
+// ------------------------------------------------------------------ LoRA operands of the contraction
+// beta from the two maxima: Bq max ~ max|B| 2^beta and Tq max ~ max|T| 2^-beta meet at
+// 2^((e_T + e_B) / 2); past the f16 range the call reports a range error.
+__global__ void __launch_bounds__(256) k_lora_pack(const float* __restrict__ t32, int64_t Mp, int R4,
+                                                   const __nv_bfloat16* __restrict__ B, int64_t d_o, int r,
+                                                   const unsigned int* __restrict__ maxima, __half* __restrict__ Tq,
+                                                   __half* __restrict__ Bq) {
+  pdl_launch_dependents();
+  pdl_wait();  // T and the maxima come from the down-projection
+  const float tmax = __uint_as_float(maxima[0]), bmax = __uint_as_float(maxima[1]);
+  int beta = 0;
+  if (tmax > 0.f && bmax > 0.f) {
+    const int et = static_cast<int>((__float_as_uint(tmax) >> 23) & 0xFFu) - 127;
+    const int eb = static_cast<int>((__float_as_uint(bmax) >> 23) & 0xFFu) - 127;
+    const int d = et - eb;
+    beta = d >= 0 ? d / 2 : -((1 - d) / 2);  // floor(d / 2)
+    if (((et + eb) >> 1) >= 14 && blockIdx.x == 0 && threadIdx.x == 0) atomicOr(&g_pf_status, kStatusRange);
+  }
+  const float up = ldexpf(1.0f, beta), down = ldexpf(1.0f, -beta);
+  // 8 consecutive f16 (16 bytes) per thread and step: rows of 64 are 8 such pieces
+  const int64_t nt = Mp * (kLoraK / 8), nb = d_o * (kLoraK / 8);
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nt + nb;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const bool tpart = i < nt;
+    const int64_t k = tpart ? i : i - nt, row = k >> 3;
+    const int j0 = static_cast<int>(k & 7) * 8;
+    float v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int j = j0 + q;
+      v[q] = j >= r ? 0.f : (tpart ? t32[row * R4 + j] * down : __bfloat162float(B[row * r + j]) * up);
+    }
+    const uint4 h = make_uint4(f32x2_to_f16x2(v[0], v[1]), f32x2_to_f16x2(v[2], v[3]), f32x2_to_f16x2(v[4], v[5]),
+                               f32x2_to_f16x2(v[6], v[7]));
+    reinterpret_cast<uint4*>(tpart ? Tq : Bq)[k] = h;
   }
 }
 
@@ -535,11 +620,13 @@ struct PfWs {
   __half* A16;
   float* t32;
   float* t_part;
-  int* counters;
+  int* counters;  // [token tiles of the down-projection], max |T|, max |B|
+  __half* Tq;     // [Mp][64]
+  __half* Bq;     // [d_o][64]
   size_t bytes;
 };
 
-PfWs carve(void* ws, int64_t M, int64_t d_i, int r) {
+PfWs carve(void* ws, int64_t M, int64_t d_i, int64_t d_o, int r) {
   PfWs w{};
   const uintptr_t b = reinterpret_cast<uintptr_t>(ws);
   size_t off = 0;
@@ -555,7 +642,11 @@ PfWs carve(void* ws, int64_t M, int64_t d_i, int r) {
   w.t_part = reinterpret_cast<float*>(b + off);
   off += align_up(static_cast<size_t>(kMaxLdSplits) * Mp * r4(r) * 4, 256);
   w.counters = reinterpret_cast<int*>(b + off);
-  off += align_up(static_cast<size_t>((M + 127) / 128 + 4) * 4, 256);
+  off += align_up(static_cast<size_t>((M + 127) / 128 + 6) * 4, 256);
+  w.Tq = reinterpret_cast<__half*>(b + off);
+  off += align_up(static_cast<size_t>(Mp) * kLoraK * 2, 256);
+  w.Bq = reinterpret_cast<__half*>(b + off);
+  off += align_up(static_cast<size_t>(d_o) * kLoraK * 2, 256);
   w.bytes = off;
   return w;
 }
@@ -568,7 +659,7 @@ struct GPlan {
 
 GPlan gplan(int r) {
   GPlan g{};
-  g.t_slot_bytes = static_cast<uint32_t>(align_up(static_cast<size_t>(kTN) * (r > 0 ? r4(r) * 4 + 4 : 4), 128));
+  g.t_slot_bytes = static_cast<uint32_t>(align_up(static_cast<size_t>(kTN) * 4, 128));  // row scales of a tile
   const size_t fixed = 2 * kScaleBytes + 2 * static_cast<size_t>(g.t_slot_bytes) + sizeof(GCtrl) + 128 + 1024;
   int st = static_cast<int>((227 * 1024 - fixed) / kStageBytes);
   g.stages = st > kMaxStages ? kMaxStages : st;
@@ -597,18 +688,20 @@ bool prefill_supported(int64_t M, int64_t d_i, int64_t d_o, int r) {
          gplan(r).stages >= 3;
 }
 
-size_t prefill_workspace_bytes(int64_t M, int64_t d_i, int64_t, int r) { return carve(nullptr, M, d_i, r).bytes; }
+size_t prefill_workspace_bytes(int64_t M, int64_t d_i, int64_t d_o, int r) {
+  return carve(nullptr, M, d_i, d_o, r).bytes;
+}
 
 cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream) {
   cudaError_t e = set_attributes();
   if (e != cudaSuccess) return e;
-  const PfWs w = carve(a.ws, a.M, a.d_i, a.r);
+  const PfWs w = carve(a.ws, a.M, a.d_i, a.d_o, a.r);
   const int64_t Mp = m_pad(a.M);
   const int R4 = r4(a.r);
   const bool lora = a.r > 0;
   const int mtiles = static_cast<int>((a.M + 127) / 128);  // token tiles of the LoRA down-projection
   e = launch_act_prologue(a, w.hq, w.rowscale, w.A16, lora ? reinterpret_cast<float*>(w.counters) : nullptr,
-                          lora ? (mtiles + 3) / 4 * 4 : 0, stream);
+                          lora ? (mtiles + 2 + 3) / 4 * 4 : 0, stream);
   if (e != cudaSuccess) return e;
 
   cudaLaunchAttribute pdl[1];
@@ -637,10 +730,14 @@ cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream) {
     splits = splits > kMaxLdSplits ? kMaxLdSplits : splits;
     splits = splits > n_ks ? n_ks : (splits < 1 ? 1 : splits);  // every split has at least one K step
     lp.splits = splits;
-    lp.rowscale = w.rowscale;
+    lp.n_b = a.d_o * a.r;
+    lp.lambda = a.lambda;
+    lp.s_g = a.s_g;
+    lp.B = static_cast<const __nv_bfloat16*>(a.B);
     lp.t_part = w.t_part;
     lp.t32 = w.t32;
     lp.counters = w.counters;
+    lp.mtiles = mtiles;
     cudaLaunchConfig_t c{};
     c.gridDim = dim3(static_cast<unsigned>(mtiles * splits));
     c.blockDim = dim3(kLdThreads);
@@ -649,6 +746,16 @@ cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream) {
     c.attrs = pdl;
     c.numAttrs = 1;
     e = cudaLaunchKernelEx(&c, k_lora_down, lm, lp);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t c2{};
+    c2.gridDim = dim3(static_cast<unsigned>(2 * sms));
+    c2.blockDim = dim3(256);
+    c2.stream = stream;
+    c2.attrs = pdl;
+    c2.numAttrs = 1;
+    e = cudaLaunchKernelEx(&c2, k_lora_pack, static_cast<const float*>(w.t32), Mp, R4,
+                           static_cast<const __nv_bfloat16*>(a.B), a.d_o, a.r,
+                           reinterpret_cast<const unsigned int*>(w.counters + mtiles), w.Tq, w.Bq);
     if (e != cudaSuccess) return e;
   }
 
@@ -659,6 +766,10 @@ cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream) {
                       CU_TENSOR_MAP_SWIZZLE_NONE) &&
             encode_2d(&gm.hq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.hq, a.d_i, a.M, 64, kTN,
                       CU_TENSOR_MAP_SWIZZLE_128B);
+  if (ok && lora)
+    ok = encode_2d(&gm.tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.Tq, kLoraK, Mp, 64, kTN, CU_TENSOR_MAP_SWIZZLE_128B);
+  else
+    gm.tq = gm.hq;  // unused
   if (!ok) return cudaErrorInvalidValue;
   const GPlan g = gplan(a.r);
   GParams p{};
@@ -666,16 +777,13 @@ cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream) {
   p.d_i = a.d_i;
   p.d_o = a.d_o;
   p.r = a.r;
-  p.R4 = R4;
   p.n_ot = static_cast<int>((a.d_o + kTO - 1) / kTO);
   p.n_tiles = static_cast<int>(p.n_ot * ((a.M + kTN - 1) / kTN));
   p.n_ks = n_ks;
   p.stages = g.stages;
-  p.lambda = a.lambda;
   p.s_g = a.s_g;
-  p.B = static_cast<const __nv_bfloat16*>(a.B);
+  p.Bq = w.Bq;
   p.rowscale = w.rowscale;
-  p.t32 = w.t32;
   p.y = a.y;
   p.y_f32 = a.y_f32 ? 1 : 0;
   p.off_scales = g.off_scales;

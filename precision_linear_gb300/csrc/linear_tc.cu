@@ -125,14 +125,14 @@ __global__ void k_wait_timeout_probe(uint64_t limit_ns) {
 
 // ------------------------------------------------------------------ activation prologue
 constexpr int kActThreads = 256;
-constexpr int kActUnroll = 4;  // 16-byte slots per thread in flight
+constexpr int kActUnroll = 2;  // 16-byte slots per thread in flight (a 3584 row is 448 slots)
 
 // CTAs 0 .. M-1: one token row m each.  hz = x (.) (w + z) is kept in shared memory
 // (FP32) while sum(x^2) and max |hz| are reduced; then hq = f16(hz * inv / c_m).
 // CTAs M and up: the f16 copy of A (r x d_i), 8 elements per thread and slot, and
 // zeros into `zero` (n_zero floats, a multiple of 4; the accumulator of the large-M
 // LoRA down-projection), 4 per thread and slot.
-__global__ void __launch_bounds__(kActThreads) k_act(const __nv_bfloat16* __restrict__ x, int64_t M, int64_t d_i,
+__global__ void __launch_bounds__(kActThreads, 4) k_act(const __nv_bfloat16* __restrict__ x, int64_t M, int64_t d_i,
                                                      const float* __restrict__ w_norm,
                                                      const float* __restrict__ z, float eps,
                                                      __half* __restrict__ hq, float* __restrict__ rowscale,

@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_status_strings_and_version(L):
-    for s in range(9):
+    for s in range(10):
         txt = L.pl_status_string(s).decode()
         assert txt.startswith("PL_")
     assert L.pl_status_string(99).decode() == "unknown pl_status"
