@@ -19,9 +19,10 @@
 //                         beyond r), beta a power of two that puts both maxima at the same
 //                         magnitude, so that s_g rowscale[m] sum_j Bq[o, j] Tq[m, j] =
 //                         lambda sum_j B[o, j] t[m, j] with t = A h.
-//   k_gemm_nvfp4          the dense contraction, persistent over 128 (weight rows) x 192
-//                         (tokens) tiles, o-tiles fastest so that concurrent CTAs share
-//                         their hq tiles in L2:
+//   k_gemm_nvfp4          the dense contraction, persistent over 128 (weight rows) x TN
+//                         (tokens; 128, 160 or 192, whichever needs the fewest rounds)
+//                         tiles, o-tiles fastest so that concurrent CTAs share their hq
+//                         tiles in L2:
 //     warp 0      TMA: per 64-wide K step the hq tile (192 x 64 f16, 128-byte swizzle) and
 //                 the packed codes (128 x 32 B); every 4th step the E4M3 scales of the next
 //                 256 K (128 x 16 B); one more step per tile with the Tq rows of its
@@ -59,19 +60,18 @@ __device__ unsigned long long g_pf_wait[1024][12];
 namespace {
 
 constexpr int kTO = 128;  // weight rows per tile
-constexpr int kTN = 192;  // tokens per tile
+constexpr int kTN = 192;  // tokens per tile, at most (the GEMM is instantiated for 128, 160 and 192)
 constexpr int kKS = 64;   // K per pipeline step (one 128-byte row of f16)
-constexpr int kMaxStages = 5;
+constexpr int kMaxStages = 7;
 constexpr int kASlots = 4;
-constexpr uint32_t kHBytes = kTN * kKS * 2;     // 24 KB
 constexpr uint32_t kCodeBytes = kTO * kKS / 2;  // 4 KB
-constexpr uint32_t kStageBytes = kHBytes + kCodeBytes;
+__host__ __device__ constexpr uint32_t stage_bytes_of(int tn) { return static_cast<uint32_t>(tn) * kKS * 2 + kCodeBytes; }
 constexpr uint32_t kScaleBytes = kTO * 16;      // scales of 256 K
 constexpr int kDeqWarps = 8;  // two per tensor-memory lane quarter: each dequantises half of a K step
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = (2 + kDeqWarps + kEpiWarps) * 32;  // 448
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColD0 = 128;  // D buffer b at columns [128 + 192 b, 320 + 192 b); weight slots below
+constexpr uint32_t kColD0 = 128;  // D buffer b at columns [128 + TN b, 128 + TN (b + 1)); weight slots below
 constexpr int kMaxR = 32;
 constexpr int kLoraK = 64;  // K columns the LoRA step adds (r <= 32 of them nonzero)
 
@@ -110,7 +110,9 @@ PL_DEVINL void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t 
 }
 
 // ------------------------------------------------------------------ main contraction
+template <int TN>
 __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constant__ GMaps maps, const GParams p) {
+  constexpr uint32_t kHBytesT = TN * kKS * 2, kStageBytes = stage_bytes_of(TN);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   GCtrl& C = *reinterpret_cast<GCtrl*>(smem + p.off_ctrl);
@@ -161,13 +163,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       pdl_wait();  // hq, row scales and t32 come from the preceding kernels
-      const uint32_t tbytes = static_cast<uint32_t>(kTN) * 4;
+      const uint32_t tbytes = static_cast<uint32_t>(TN) * 4;
       bool ok = true;
       int64_t gs = 0;
       int it = 0, t_issued = 0;
       for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x, ++it) {
         const int mt = tile / p.n_ot, ot = tile % p.n_ot;
-        const int32_t m0 = mt * kTN, o0 = ot * kTO;
+        const int32_t m0 = mt * TN, o0 = ot * kTO;
         {  // this tile's t32 rows and row scales
           const int tb = it & 1;
           {
@@ -179,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
           const uint32_t tb_bar = smem_u32(&C.tfull[tb]);
           const uint32_t dst = sbase + p.off_t + tb * p.t_slot_bytes;
           mbar_arrive_expect_tx(tb_bar, tbytes);
-          bulk_g2s(dst, p.rowscale + m0, kTN * 4, tb_bar);
+          bulk_g2s(dst, p.rowscale + m0, TN * 4, tb_bar);
           ++t_issued;
         }
         for (int s = 0; s < n_steps && ok; ++s, ++gs) {
@@ -192,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
           if (!ok) break;
           const uint32_t fb = smem_u32(&C.full[st]);
           if (s == n_ks) {  // the LoRA step: Tq rows of this token tile
-            mbar_arrive_expect_tx(fb, kHBytes);
+            mbar_arrive_expect_tx(fb, kHBytesT);
             tma_load_2d(sbase + st * kStageBytes, &maps.tq, 0, m0, fb);
             continue;
           }
@@ -201,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
           const uint32_t stage = sbase + st * kStageBytes;
           tma_load_2d(stage, &maps.hq, s * kKS, m0, fb);
           // weights and hq both stay in L2: every weight tile is read once per token tile
-          tma_load_2d(stage + kHBytes, &maps.codes, s * (kKS / 2), o0, fb);
+          tma_load_2d(stage + kHBytesT, &maps.codes, s * (kKS / 2), o0, fb);
           if (scl) {
             const int64_t grp = static_cast<int64_t>(it) * (n_ks / 4) + s / 4;
             tma_load_2d(sbase + p.off_scales + static_cast<uint32_t>(grp & 1) * kScaleBytes, &maps.scales,
@@ -219,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_f16(kTO, kTN, 0);
+      const uint32_t idesc = idesc_f16(kTO, TN, 0);
       bool ok = true;
       int64_t gs = 0;
       int it = 0;
@@ -232,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
         }
         if (!ok) break;
         tc_fence_after();
-        const uint32_t d = tmem + (kColD0 + 192u * b);
+        const uint32_t d = tmem + (kColD0 + static_cast<uint32_t>(TN) * b);
         for (int s = 0; s < n_steps && ok; ++s, ++gs) {
           const int st = static_cast<int>(gs % nst), a = static_cast<int>(gs % kASlots);
           {
@@ -298,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
           for (int i = 0; i < 16; ++i) v[i] = w16[i];
         } else {
           const uint8_t* stage = smem + st * kStageBytes;
-          const uint4 cw = *reinterpret_cast<const uint4*>(stage + kHBytes + row * 32 + g * 16);  // 32 codes
+          const uint4 cw = *reinterpret_cast<const uint4*>(stage + kHBytesT + row * 32 + g * 16);  // 32 codes
           const int64_t grp = static_cast<int64_t>(it) * (n_ks / 4) + s / 4;
           const uint32_t sw = *reinterpret_cast<const uint16_t*>(smem + p.off_scales + static_cast<uint32_t>(grp & 1) * kScaleBytes +
                                                                   row * 16 + (s & 3) * 4 + g * 2);
@@ -344,15 +346,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
       if (!ok) break;
       tc_fence_after();
       const float* rsc = reinterpret_cast<const float*>(smem + p.off_t + b * p.t_slot_bytes);
-      for (int cb = 0; cb < kTN / 16; ++cb) {
+      for (int cb = 0; cb < TN / 16; ++cb) {
         const int col = cb * 16;  // token columns [col, col + 16) of the tile
         uint32_t dv[16];
-        tmem_ld16(tmem + lane_addr + (kColD0 + 192u * b) + col, dv);
+        tmem_ld16(tmem + lane_addr + (kColD0 + static_cast<uint32_t>(TN) * b) + col, dv);
         tmem_ld_wait();
         if (o < p.d_o) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const int64_t m = static_cast<int64_t>(mt) * kTN + col + i;
+            const int64_t m = static_cast<int64_t>(mt) * TN + col + i;
             const float v = s_g * rsc[col + i] * __uint_as_float(dv[i]);
             if (m < p.M) {
               if (p.y_f32) static_cast<float*>(p.y)[m * p.d_o + o] = v;
@@ -607,9 +609,10 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void*
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Rows of the per-token arrays (row scales, t): a multiple of both token tiles (192 for
-// the GEMM, 128 for the down-projection), so that whole tiles can be read and written.
-int64_t m_pad(int64_t M) { return (M + 383) / 384 * 384; }
+// Rows of the per-token arrays (row scales, t): a multiple of every token tile (128, 160
+// or 192 for the GEMM, 128 for the down-projection), so that whole tiles can be read and
+// written.
+int64_t m_pad(int64_t M) { return (M + 1919) / 1920 * 1920; }
 int r4(int r) { return r > 0 ? (r + 3) / 4 * 4 : 0; }
 
 constexpr int kMaxLdSplits = 8;
@@ -657,9 +660,10 @@ struct GPlan {
   size_t smem;
 };
 
-GPlan gplan(int r) {
+GPlan gplan(int r, int tn) {
   GPlan g{};
-  g.t_slot_bytes = static_cast<uint32_t>(align_up(static_cast<size_t>(kTN) * 4, 128));  // row scales of a tile
+  const uint32_t kStageBytes = stage_bytes_of(tn);
+  g.t_slot_bytes = static_cast<uint32_t>(align_up(static_cast<size_t>(tn) * 4, 128));  // row scales of a tile
   const size_t fixed = 2 * kScaleBytes + 2 * static_cast<size_t>(g.t_slot_bytes) + sizeof(GCtrl) + 128 + 1024;
   int st = static_cast<int>((227 * 1024 - fixed) / kStageBytes);
   g.stages = st > kMaxStages ? kMaxStages : st;
@@ -674,7 +678,11 @@ cudaError_t set_attributes() {
   static std::once_flag once;
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
-    err = cudaFuncSetAttribute(k_gemm_nvfp4, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    err = cudaFuncSetAttribute(k_gemm_nvfp4<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(k_gemm_nvfp4<160>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(k_gemm_nvfp4<192>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (err == cudaSuccess)
       err = cudaFuncSetAttribute(k_lora_down, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   });
@@ -685,7 +693,7 @@ cudaError_t set_attributes() {
 
 bool prefill_supported(int64_t M, int64_t d_i, int64_t d_o, int r) {
   return M > 64 && d_i >= 256 && d_i % 256 == 0 && d_i <= 49152 && d_o >= 1 && r >= 0 && r <= kMaxR &&
-         gplan(r).stages >= 3;
+         gplan(r, kTN).stages >= 3;
 }
 
 size_t prefill_workspace_bytes(int64_t M, int64_t d_i, int64_t d_o, int r) {
@@ -759,26 +767,35 @@ cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
   }
 
+  // token tile: 192 (the widest MMA the two accumulator buffers allow, and the most
+  // efficient per instruction) unless that leaves SMs idle, then the narrower tile that
+  // fills the most of them
+  const int64_t n_ot64 = (a.d_o + kTO - 1) / kTO;
+  int tn = kTN;
+  for (int cand : {160, 128}) {
+    if (n_ot64 * ((a.M + tn - 1) / tn) >= sms) break;
+    tn = cand;
+  }
   GMaps gm;
   bool ok = encode_2d(&gm.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.codes, a.d_i / 2, a.d_o, kKS / 2, kTO,
                       CU_TENSOR_MAP_SWIZZLE_NONE) &&
             encode_2d(&gm.scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.scales, a.d_i / 16, a.d_o, 16, kTO,
                       CU_TENSOR_MAP_SWIZZLE_NONE) &&
-            encode_2d(&gm.hq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.hq, a.d_i, a.M, 64, kTN,
+            encode_2d(&gm.hq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.hq, a.d_i, a.M, 64, tn,
                       CU_TENSOR_MAP_SWIZZLE_128B);
   if (ok && lora)
-    ok = encode_2d(&gm.tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.Tq, kLoraK, Mp, 64, kTN, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = encode_2d(&gm.tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.Tq, kLoraK, Mp, 64, tn, CU_TENSOR_MAP_SWIZZLE_128B);
   else
     gm.tq = gm.hq;  // unused
   if (!ok) return cudaErrorInvalidValue;
-  const GPlan g = gplan(a.r);
+  const GPlan g = gplan(a.r, tn);
   GParams p{};
   p.M = a.M;
   p.d_i = a.d_i;
   p.d_o = a.d_o;
   p.r = a.r;
   p.n_ot = static_cast<int>((a.d_o + kTO - 1) / kTO);
-  p.n_tiles = static_cast<int>(p.n_ot * ((a.M + kTN - 1) / kTN));
+  p.n_tiles = static_cast<int>(p.n_ot * ((a.M + tn - 1) / tn));
   p.n_ks = n_ks;
   p.stages = g.stages;
   p.s_g = a.s_g;
@@ -797,7 +814,9 @@ cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream) {
   c.stream = stream;
   c.attrs = pdl;
   c.numAttrs = 1;
-  return cudaLaunchKernelEx(&c, k_gemm_nvfp4, gm, p);
+  if (tn == 128) return cudaLaunchKernelEx(&c, k_gemm_nvfp4<128>, gm, p);
+  if (tn == 160) return cudaLaunchKernelEx(&c, k_gemm_nvfp4<160>, gm, p);
+  return cudaLaunchKernelEx(&c, k_gemm_nvfp4<192>, gm, p);
 }
 
 #ifdef PL_TIMELINE
