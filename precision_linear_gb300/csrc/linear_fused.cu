@@ -20,22 +20,30 @@
 //                (weights; they do not depend on the preceding kernel), then, after
 //                the programmatic-dependent-launch wait, the x slice and the w_norm
 //                and z slices;
-//   warps 10-13  B rows of the CTA's output share into shared memory; w_norm + z;
-//                A bf16 -> f16 in place; token rows of x from a shared queue (sum of
-//                squares and max |u| of the row, then u c -> f16 in place; the row
-//                sums go to every CTA of the cluster); then lane 0 of each issues
+//   warps 10-13  w_norm + z; A bf16 -> f16 in place; token rows of x from a shared
+//                queue (sum of squares and max |u| of the row, then u c -> f16 in
+//                place; the row sums go to every CTA of the cluster); then lane 0 of
+//                each issues
 //                tcgen05.mma kind::f16 into its own accumulator (a single issuing
 //                thread is latency-bound on these small MMAs): D1 += W_hat/s_g (tensor
-//                memory) x u^T over even / odd K steps, and Dt^T += u x A^T (shared
-//                memory) over even / odd K steps;
-//   warps 2-9    dequantise chunks into two tensor-memory buffers (E2M1 -> f16
-//                conversion, times the block scale: exact in f16), take token rows
-//                from the queue when the second buffer is full, then the epilogue;
+//                memory) x u^T over even / odd K steps as the chunks are dequantised,
+//                and Dt^T += u x A^T (shared memory) over even / odd K steps at once;
+//                warps 12-13 then round t = Dt lambda / s_g to bf16 into shared memory
+//                and the D1 issuer adds the up-projection as one more K step,
+//                D1 += B t^T (bf16 operands, B as stored);
+//   warps 2-9    B rows of the tile into shared memory (bf16); dequantise chunks
+//                into two or three tensor-memory buffers (E2M1 -> f16 conversion,
+//                times the block scale: exact in f16), take token rows from the
+//                queue when the buffers are full, then the epilogue;
 //   warp 1       tensor-memory allocation.
-// Epilogue: each CTA sends, with st.async into its peers' shared memory, the rows of
-// s_g / c D1 that each peer owns (peer p owns rows [128 p / S, 128 (p+1) / S)) and its
-// whole t slice Dt^T / c to every peer.  Each CTA sums what it owns in split order
-// (deterministic), adds lambda B t on CUDA cores, scales by rs and writes y.
+// Epilogue: each CTA's partial P = s_g D1 / c already holds its share of the LoRA
+// path (by linearity the splits' B t_s add up to B t); it sends with st.async into
+// its peers' shared memory the rows of P that each peer owns (peer p owns rows
+// [128 p / S, 128 (p+1) / S)).  Each CTA sums what it owns in split order
+// (deterministic), scales by rs and writes y.
+// The receive buffers have a region of their own when shared memory allows (then no
+// cluster barrier comes between the MMAs and the exchange), else they lie over the
+// stage region, after a cluster barrier.
 //
 // Every mbarrier wait is bounded (200 ms).  A wait that gives up sets the status word;
 // the CTA still takes part in every cluster barrier and still sends its (then
@@ -68,7 +76,7 @@ constexpr int kScaleBytes = kTileO * kChunkK / 16;  // 2 KB
 constexpr int kMaxChunks = 3;
 constexpr int kMaxSplit = 8;
 constexpr int kMaxN = 64;
-constexpr int kMaxR = 64;
+constexpr int kMaxRFused = 32;  // LoRA rank this kernel takes (B rows are held in registers)
 constexpr int kDeqWarps = 8;
 constexpr int kConvWarps = 4;
 constexpr int kConvThreads = kConvWarps * 32;
@@ -89,8 +97,11 @@ struct FParams {
   void* y;
   int y_f32;
   // shared-memory layout (byte offsets from the 1 KB-aligned base)
-  uint32_t off_scales, off_x, off_a, off_gw, off_gz, off_bt, off_q, off_ctrl;
-  uint32_t off_rt, off_ts;  // receive buffers, over the dead stage region (receive P at 0)
+  uint32_t off_scales, off_x, off_a, off_gw, off_gz, off_q, off_ctrl;
+  uint32_t off_rp;          // partial-output receive buffers
+  uint32_t off_bq, off_tq;  // LoRA up-projection operands: B of the tile [128][64], t [N][64] (bf16, SW128)
+  int alias_recv;           // 1: the receive buffers lie over the stage region (cluster barrier first)
+  int lora_in_a;            // 1: the up-projection operands lie over the A slabs (written once Dt is done)
 };
 
 struct FMaps {
@@ -104,6 +115,8 @@ struct Ctrl {
   uint64_t a_in, x_in, g_in;   // LoRA A slice, x slice, w_norm / z slices landed
   uint64_t g_ready;            // w_norm + z formed
   uint64_t act_ready;          // every token row converted
+  uint64_t dt_full;            // the LoRA down-projection MMAs done
+  uint64_t lora_ready;         // B and t of the up-projection in shared memory
   uint64_t d_full;             // every MMA done
   uint64_t recv;               // the peers' shares arrived
   uint32_t tmem_base;
@@ -128,6 +141,7 @@ PL_DEVINL uint32_t cluster_rank() {
 }
 PL_DEVINL void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
 PL_DEVINL void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+PL_DEVINL void cluster_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory"); }
 PL_DEVINL void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 // 16 bytes into a peer's shared memory, completing 16 bytes of its mbarrier's transaction.
 PL_DEVINL void st_async_f32x4(uint32_t addr, float4 v, uint32_t bar) {
@@ -274,13 +288,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
       mbar_init(smem_u32(&C.wfull[c]), 1);
       mbar_init(smem_u32(&C.a_full[c]), kDeqWarps);
     }
-    for (int b = 0; b < kMaxChunks; ++b) mbar_init(smem_u32(&C.a_empty[b]), kConvWarps);
+    for (int b = 0; b < kMaxChunks; ++b) mbar_init(smem_u32(&C.a_empty[b]), 2);  // the D1 issuers
     mbar_init(smem_u32(&C.a_in), 1);
     mbar_init(smem_u32(&C.x_in), 1);
     mbar_init(smem_u32(&C.g_in), 1);
     mbar_init(smem_u32(&C.g_ready), kConvWarps);
     mbar_init(smem_u32(&C.act_ready), kDeqWarps + kConvWarps + 1);  // + warp 1 (its share of A)
-    mbar_init(smem_u32(&C.d_full), kConvWarps);
+    mbar_init(smem_u32(&C.dt_full), 2);
+    mbar_init(smem_u32(&C.lora_ready), 4 + 2);  // 4 dequant warps (B), 2 conversion warps (t)
+    mbar_init(smem_u32(&C.d_full), 2);
     mbar_init(smem_u32(&C.recv), 1);
     fence_mbar_init();
     PL_TLF(16);
@@ -350,39 +366,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
       drain(xb, 0);
     }
     __syncwarp();
-    cluster_arrive();
-    cluster_wait();
+    if (p.alias_recv) {
+      cluster_arrive();
+      cluster_wait();
+    }
+    cluster_arrive_relaxed();
   } else if (warp == 1) {
     if (lora) convert_a(smem + p.off_a, a_bytes, kConvThreads + lane, kConvThreads + 32, smem_u32(&C.a_in), abort_flag);
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&C.act_ready));
-    cluster_arrive();
-    cluster_wait();
+    if (p.alias_recv) {
+      cluster_arrive();
+      cluster_wait();
+    }
+    cluster_arrive_relaxed();
   } else if (warp >= kConvWarp0) {
     // ---------------------------------------------------------------- activations, then MMA issue
     const int cw = warp - kConvWarp0;              // 0..3
     const int ct = threadIdx.x - kConvWarp0 * 32;  // 0..127
-    float* bt = reinterpret_cast<float*>(smem + p.off_bt);  // [j][rows_max]: B of the owned rows
-    if (lora) {
-      // B is a weight: read before the wait on the preceding kernel
-      const int nb = rows_own * p.r;
-      for (int i0 = 0; i0 < nb; i0 += 8 * kConvThreads) {
-        float b[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int i = i0 + u * kConvThreads + ct;
-          const int rl = i / p.r, j = i % p.r;
-          const int64_t o = static_cast<int64_t>(row0) + R0 + rl;
-          b[u] = (i < nb && o < p.d_o) ? __bfloat162float(p.B[o * p.r + j]) : 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int i = i0 + u * kConvThreads + ct;
-          if (i < nb) bt[(i % p.r) * p.rows_max + i / p.r] = b[u];
-        }
-      }
-    }
+    static_assert((kConvWarp0 + 2) % 4 == 0, "warps kConvWarp0 + 2, + 3 hold tensor-memory lanes 0-63");
     bool ok = true;
     if (lora)  // A lands early (a weight): convert it while x is still on its way
       ok = convert_a(smem + p.off_a, a_bytes, ct, kConvThreads + 32, smem_u32(&C.a_in), abort_flag);
@@ -407,52 +410,100 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
     if (ct == 0) PL_TLF(4);
     convert_rows();  // also fences and arrives on act_ready
     if (ct == 0) PL_TLF(5);
+    const bool tpart = cw >= 2;
     if (lane == 0) {
       // issuer cw: accumulator D1a / D1b (cw 0 / 1) or Dta / Dtb (cw 2 / 3), even / odd K steps
-      const bool tpart = cw >= 2, issue = !tpart || lora;
       const int par = cw & 1;
-      const uint32_t idesc = tpart ? idesc_f16(kTileO, p.rb, 0) : idesc_f16(kTileO, N, 0);
       const uint32_t dcol = cw == 0 ? colD1a : (cw == 1 ? colD1b : (cw == 2 ? colDta : colDtb));
       // Descriptors advance by constants: one K step is 32 bytes (2 units of 16 B), one
       // 64-element slab N * 128 bytes (x) or rb * 128 bytes (A).  A single issuing thread
       // spends most of its time on the arithmetic between MMAs, so none is left there.
       const uint64_t xd0 = smem_desc_sw128(sbase + p.off_x, 1024) + 2u * par;
-      const uint64_t ad0 = smem_desc_sw128(sbase + p.off_a, 1024) + 2u * par;
       const uint32_t xslab = static_cast<uint32_t>(N) * 8u, aslab = static_cast<uint32_t>(p.rb) * 8u;
       const uint32_t dtm = tmem + dcol;
       bool go = wait_f(smem_u32(&C.act_ready), 0, abort_flag);
       if (cw == 0) PL_TLF(15);
-      for (int c = 0; c < nch && go; ++c) {
-        go = wait_f(smem_u32(&C.a_full[c]), 0, abort_flag);
-        if (!go) break;
-        if (cw == 0) PL_TLF(23 + c);
-        tc_fence_after();
-        if (issue) {
+      if (!tpart) {
+        const uint32_t idesc = idesc_f16(kTileO, N, 0);
+        for (int c = 0; c < nch && go; ++c) {
+          go = wait_f(smem_u32(&C.a_full[c]), 0, abort_flag);
+          if (!go) break;
+          if (cw == 0) PL_TLF(23 + c);
+          tc_fence_after();
           const uint64_t xc = xd0 + static_cast<uint64_t>(4u * c * xslab);
-          if (!tpart) {
-            const uint32_t ac = tmem + 128u * (c % nbuf) + 8u * par;  // K step kk = 2 h + par
+          const uint32_t ac = tmem + 128u * (c % nbuf) + 8u * par;  // K step kk = 2 h + par
 #pragma unroll
-            for (int h = 0; h < kChunkK / 32; ++h)
-              mma_ts(dtm, ac + 16u * h, xc + (h >> 1) * xslab + 4u * (h & 1), idesc, (c > 0 || h > 0) ? 1u : 0u);
-          } else {
-            // A operand: 128 rows of u (rows >= N read bytes of the following slabs and
-            // regions, inside this CTA's allocation; they only feed unread lanes)
-            const uint64_t acd = ad0 + static_cast<uint64_t>(4u * c * aslab);
-#pragma unroll
-            for (int h = 0; h < kChunkK / 32; ++h)
-              mma_ss(dtm, xc + (h >> 1) * xslab + 4u * (h & 1), acd + (h >> 1) * aslab + 4u * (h & 1), idesc,
-                     (c > 0 || h > 0) ? 1u : 0u);
+          for (int h = 0; h < kChunkK / 32; ++h)
+            mma_ts(dtm, ac + 16u * h, xc + (h >> 1) * xslab + 4u * (h & 1), idesc, (c > 0 || h > 0) ? 1u : 0u);
+          if (cw == 0) PL_TLF(26 + c);
+          if (c + nbuf < nch) tc_commit(smem_u32(&C.a_empty[c % nbuf]));  // buffer reused by chunk c + nbuf
+        }
+        if (lora && cw == 0 && go) {
+          // the LoRA up-projection as one more K step of D1a: B (bf16, as stored) times
+          // t = Dt lambda / s_g (bf16), which is lambda B A u in the units of D1
+          go = wait_f(smem_u32(&C.lora_ready), 0, abort_flag);
+          if (go) {
+            tc_fence_after();
+            const uint32_t idesc_l = idesc_f16(kTileO, N, 1);
+            const uint64_t bd = smem_desc_sw128(sbase + p.off_bq, 1024);
+            const uint64_t td = smem_desc_sw128(sbase + p.off_tq, 1024);
+            for (int k = 0; k < p.rb / 16; ++k) mma_ss(dtm, bd + 2u * k, td + 2u * k, idesc_l, 1u);
           }
         }
-        if (cw == 0) PL_TLF(26 + c);
-        if (c + nbuf < nch) tc_commit(smem_u32(&C.a_empty[c % nbuf]));  // buffer reused by chunk c + nbuf
+        tc_commit(smem_u32(&C.d_full));  // also reached on abort: tracks every MMA issued
+        if (cw == 0) PL_TLF(8);
+      } else if (lora) {
+        // the LoRA down-projection needs no weight buffer: all of it at once
+        const uint32_t idesc = idesc_f16(kTileO, p.rb, 0);
+        const uint64_t ad0 = smem_desc_sw128(sbase + p.off_a, 1024) + 2u * par;
+        for (int c = 0; c < nch && go; ++c) {
+          // A operand: 128 rows of u (rows >= N read bytes of the following slabs and
+          // regions, inside this CTA's allocation; they only feed unread lanes)
+          const uint64_t xc = xd0 + static_cast<uint64_t>(4u * c * xslab);
+          const uint64_t acd = ad0 + static_cast<uint64_t>(4u * c * aslab);
+#pragma unroll
+          for (int h = 0; h < kChunkK / 32; ++h)
+            mma_ss(dtm, xc + (h >> 1) * xslab + 4u * (h & 1), acd + (h >> 1) * aslab + 4u * (h & 1), idesc,
+                   (c > 0 || h > 0) ? 1u : 0u);
+        }
+        tc_commit(smem_u32(&C.dt_full));
       }
-      tc_commit(smem_u32(&C.d_full));  // also reached on abort: tracks every MMA issued
-      if (cw == 0) PL_TLF(8);
     }
     __syncwarp();
-    cluster_arrive();
-    cluster_wait();
+    if (tpart && lora) {
+      // t = (Dta + Dtb) lambda / s_g -> bf16, one token row per lane (warps 12 / 13 hold
+      // tensor-memory lanes 0-31 / 32-63), K-major 128-byte swizzled rows of 64 elements
+      bool tok = wait_f(smem_u32(&C.dt_full), 0, abort_flag);
+      tc_fence_after();
+      const int n = (cw - 2) * 32 + lane;
+      const float lam_sg = p.lambda / *p.s_g;
+      uint8_t* tq = smem + p.off_tq + n * 128;
+      const uint32_t la = static_cast<uint32_t>((cw - 2) * 32) << 16;
+#pragma unroll
+      for (int j8 = 0; j8 < kMaxRFused / 8; ++j8) {
+        if (j8 * 8 < p.rb) {
+          uint32_t a8[8], b8[8];
+          tmem_ld8(tmem + la + colDta + j8 * 8, a8);
+          tmem_ld8(tmem + la + colDtb + j8 * 8, b8);
+          tmem_ld_wait();
+          uint32_t w[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            w[q] = f32x2_to_bf16x2((__uint_as_float(a8[2 * q]) + __uint_as_float(b8[2 * q])) * lam_sg,
+                                   (__uint_as_float(a8[2 * q + 1]) + __uint_as_float(b8[2 * q + 1])) * lam_sg);
+          if (n < N && tok) *reinterpret_cast<uint4*>(tq + ((j8 ^ (n & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&C.lora_ready));
+    }
+    __syncwarp();
+    if (p.alias_recv) {
+      cluster_arrive();
+      cluster_wait();
+    }
+    cluster_arrive_relaxed();
   } else {
     // ---------------------------------------------------------------- dequant + epilogue
     const int dw = warp - 2;              // 0..7
@@ -461,6 +512,43 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
     const int row = quarter * 32 + lane;  // weight row within the tile
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const int et = threadIdx.x - 64;      // 0 .. 255
+    // B row of this thread's weight row, bf16 pairs (a weight: read before any data wait;
+    // the g == 0 threads cover the 128 rows)
+    uint32_t bq[kMaxRFused / 2];
+#pragma unroll
+    for (int j = 0; j < kMaxRFused / 2; ++j) bq[j] = 0u;
+    if (lora && g == 0 && static_cast<int64_t>(row0) + row < p.d_o) {
+      const int64_t o = static_cast<int64_t>(row0) + row;
+      if ((p.r & 7) == 0) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.B + o * p.r);
+#pragma unroll
+        for (int q = 0; q < kMaxRFused / 8; ++q)
+          if (8 * q < p.r) {
+            const uint4 v = src[q];
+            bq[4 * q] = v.x; bq[4 * q + 1] = v.y; bq[4 * q + 2] = v.z; bq[4 * q + 3] = v.w;
+          }
+      } else {
+        const uint16_t* src = reinterpret_cast<const uint16_t*>(p.B + o * p.r);
+#pragma unroll
+        for (int j = 0; j < kMaxRFused; ++j)
+          if (j < p.r) bq[j >> 1] |= static_cast<uint32_t>(src[j]) << (16 * (j & 1));
+      }
+    }
+    // B rows of the up-projection operand (K-major, 128-byte swizzled; columns >= r are 0)
+    auto write_bq = [&]() {
+      if (g == 0) {
+        uint8_t* bqs = smem + p.off_bq + row * 128;
+#pragma unroll
+        for (int j8 = 0; j8 < kMaxRFused / 8; ++j8)
+          if (j8 * 8 < p.rb)
+            *reinterpret_cast<uint4*>(bqs + ((j8 ^ (row & 7)) << 4)) =
+                make_uint4(bq[4 * j8], bq[4 * j8 + 1], bq[4 * j8 + 2], bq[4 * j8 + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&C.lora_ready));
+      }
+    };
+    if (lora && !p.lora_in_a) write_bq();
     bool ok = true, converted = false;
     for (int c = 0; c < nch; ++c) {
       if (c == nbuf) {  // buffer 0 is needed again: help with the activations first
@@ -505,19 +593,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
       ok = wait_f(smem_u32(&C.g_ready), 0, abort_flag) && wait_f(smem_u32(&C.x_in), 0, abort_flag) && ok;
       convert_rows();
     }
+    if (lora && p.lora_in_a) {  // the A slabs are free once the down-projection is done
+      ok = wait_f(smem_u32(&C.dt_full), 0, abort_flag) && ok;
+      write_bq();
+    }
     if (et == 0) C.s_g = *p.s_g;  // a weight input: not written by the preceding kernel
     // ---------------------------------------------------------------- epilogue: gather
     ok = wait_f(smem_u32(&C.d_full), 0, abort_flag) && ok;
     if (et == 0) PL_TLF(9);
     tc_fence_after();
     const int half = N / 2, n0 = g * half;  // tokens [n0, n0 + half) of D1 for this thread
-    const int thalf = p.rb / 2, j0 = g * thalf;
-    const bool trow = lora && quarter * 32 < M && quarter < 2;  // lanes 0..63: token rows of Dt^T
-    // accumulators into registers first (their latency hides behind the cluster barrier)
-    float d1[32], dt[32];
+    const int Mp = p.Mp;
+    float d1[32];
 #pragma unroll
     for (int cb = 0; cb < 4; ++cb) {
-      if (cb * 8 < half && n0 + cb * 8 < p.Mp) {
+      if (cb * 8 < half && n0 + cb * 8 < Mp) {
         uint32_t a8[8], b8[8];
         tmem_ld8(tmem + lane_addr + colD1a + n0 + cb * 8, a8);
         tmem_ld8(tmem + lane_addr + colD1b + n0 + cb * 8, b8);
@@ -525,83 +615,46 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
 #pragma unroll
         for (int i = 0; i < 8; ++i) d1[cb * 8 + i] = __uint_as_float(a8[i]) + __uint_as_float(b8[i]);
       }
-      if (trow && cb * 8 < thalf) {
-        uint32_t a8[8], b8[8];
-        tmem_ld8(tmem + lane_addr + colDta + j0 + cb * 8, a8);
-        tmem_ld8(tmem + lane_addr + colDtb + j0 + cb * 8, b8);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 8; ++i) dt[cb * 8 + i] = __uint_as_float(a8[i]) + __uint_as_float(b8[i]);
-      }
     }
     const bool good = ok && !*abort_flag;
-    cluster_arrive();  // this CTA no longer reads its stage region
-    cluster_wait();
+    // P[row, n] = s_g D1[row, n] / c_n: this split's share of W_hat u + lambda B A u
+    const float s_g = C.s_g;
+    float pv[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < half && n0 + i < Mp) pv[i] = good ? C.cinv[n0 + i] * s_g * d1[i] : 0.f;
+    if (p.alias_recv) {  // the receive buffers lie over the stage region: every CTA is done with it
+      cluster_arrive();
+      cluster_wait();
+    }
     if (et == 0) PL_TLF(10);
     // ---------------------------------------------------------------- epilogue: exchange
     const uint32_t recv_bar = smem_u32(&C.recv);
-    const float s_g = C.s_g;
-    const int Mp = p.Mp;
     {
       int o = S - 1;
       while (o > 0 && owner_row0(o, S) > row) --o;
       const int rl = row - owner_row0(o, S);
-      const uint32_t dst = sbase + static_cast<uint32_t>(((me * p.rows_max + rl) * p.Np + n0) * 4);
+      const uint32_t dst = sbase + p.off_rp + static_cast<uint32_t>(((me * p.rows_max + rl) * p.Np + n0) * 4);
       const uint32_t rdst = mapa_shared(dst, static_cast<uint32_t>(o)), rbar = mapa_shared(recv_bar, o);
 #pragma unroll
       for (int i = 0; i < 32; i += 4) {
         if (i < half && n0 + i < Mp) {
-          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (good) {
-            const float4 ci = *reinterpret_cast<const float4*>(&C.cinv[n0 + i]);
-            v = make_float4(s_g * ci.x * d1[i], s_g * ci.y * d1[i + 1], s_g * ci.z * d1[i + 2], s_g * ci.w * d1[i + 3]);
-          }
+          const float4 v = make_float4(pv[i], pv[i + 1], pv[i + 2], pv[i + 3]);
           if (o == me) *reinterpret_cast<float4*>(smem + (dst - sbase) + 4 * i) = v;
           else st_async_f32x4(rdst + 4 * i, v, rbar);
         }
       }
     }
-    if (et == 0) PL_TLF(48);
-    float* rtw = reinterpret_cast<float*>(smem + p.off_rt);
-    if (trow && quarter * 32 + lane < M) {  // this split's t slice, local copy first
-      const int n = quarter * 32 + lane;
-      const float ci = C.cinv[n];
-      float* dst = rtw + (me * N + n) * p.rb + j0;
-#pragma unroll
-      for (int i = 0; i < 32; i += 4) {
-        if (i < thalf) {
-          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (good) v = make_float4(ci * dt[i], ci * dt[i + 1], ci * dt[i + 2], ci * dt[i + 3]);
-          *reinterpret_cast<float4*>(dst + i) = v;
-        }
-      }
-    }
-    if (et == 0) PL_TLF(49);
-    if (lora && S > 1) {  // then from there to every peer, spread over all epilogue threads
-      named_bar(1, kEpiThreads);
-      if (et == 0) PL_TLF(50);
-      const int per = M * p.rb / 4;  // 16-byte pieces of the slice
-      const uint32_t src = sbase + p.off_rt + static_cast<uint32_t>(me * N * p.rb * 4);
-      for (int i = et; i < per * (S - 1); i += kEpiThreads) {
-        const int d = 1 + i / per, k = i % per;
-        const uint32_t o = static_cast<uint32_t>((me + d) % S);
-        const float4 v = *reinterpret_cast<const float4*>(smem + (src - sbase) + 16 * k);
-        st_async_f32x4(mapa_shared(src + 16 * k, o), v, mapa_shared(recv_bar, o));
-      }
-    }
     if (et == 0) {
-      const uint32_t per_peer =
-          static_cast<uint32_t>(rows_own * Mp * 4 + (lora ? M * p.rb * 4 : 0) + (norm ? M * 4 : 0));
+      const uint32_t per_peer = static_cast<uint32_t>(rows_own * Mp * 4 + (norm ? M * 4 : 0));
       mbar_arrive_expect_tx(recv_bar, per_peer * static_cast<uint32_t>(S - 1));
       PL_TLF(11);
     }
     named_bar(1, kEpiThreads);  // this CTA's own shares are in place
     ok = wait_f(recv_bar, 0, abort_flag) && good;
+    cluster_arrive_relaxed();  // nothing more lands here (released at the exit barrier)
     if (et == 0) PL_TLF(12);
     // ---------------------------------------------------------------- epilogue: combine
-    const float* rt = rtw;
-    float* ts = reinterpret_cast<float*>(smem + p.off_ts);  // [N][rb + 4]: lambda t
-    const int tstr = p.rb + 4;
     if (et < M) {
       float rs = 1.f;
       if (norm) {
@@ -611,21 +664,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
       }
       C.rs[et] = rs;
     }
-    if (et == 0) PL_TLF(51);
-    if (lora) {
-      for (int i = et; i < M * p.rb; i += kEpiThreads) {
-        const int n = i / p.rb, j = i % p.rb;
-        float acc = 0.f;
-        for (int s = 0; s < S; ++s) acc += rt[(s * N + n) * p.rb + j];
-        ts[n * tstr + j] = p.lambda * acc;
-      }
-    }
-    if (et == 0) PL_TLF(52);
     named_bar(1, kEpiThreads);
     if (et == 0) PL_TLF(22);
     if (ok) {
-      const float* rp = reinterpret_cast<const float*>(smem);
-      const float* bt = reinterpret_cast<const float*>(smem + p.off_bt);
+      const float* rp = reinterpret_cast<const float*>(smem + p.off_rp);
       const int items = rows_own * (Mp / 4);
       for (int e = et; e < items; e += kEpiThreads) {
         const int rl = e % rows_own, n4 = 4 * (e / rows_own);
@@ -633,23 +675,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
         for (int s = 0; s < S; ++s) {
           const float4 v = *reinterpret_cast<const float4*>(rp + (s * p.rows_max + rl) * p.Np + n4);
           acc[0] += v.x; acc[1] += v.y; acc[2] += v.z; acc[3] += v.w;
-        }
-        if (lora) {
-          const int nq = M - n4 < 4 ? M - n4 : 4;
-#pragma unroll 2
-          for (int j = 0; j < p.r; j += 4) {
-            const float b0 = bt[j * p.rows_max + rl];
-            const float b1 = j + 1 < p.r ? bt[(j + 1) * p.rows_max + rl] : 0.f;
-            const float b2 = j + 2 < p.r ? bt[(j + 2) * p.rows_max + rl] : 0.f;
-            const float b3 = j + 3 < p.r ? bt[(j + 3) * p.rows_max + rl] : 0.f;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              if (q < nq) {
-                const float4 t = *reinterpret_cast<const float4*>(ts + (n4 + q) * tstr + j);
-                acc[q] = fmaf(b0, t.x, fmaf(b1, t.y, fmaf(b2, t.z, fmaf(b3, t.w, acc[q]))));
-              }
-            }
-          }
         }
         const int64_t oo = static_cast<int64_t>(row0) + R0 + rl;
         if (oo < p.d_o) {
@@ -667,6 +692,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
     }
   }
   if (threadIdx.x == 64) PL_TLF(13);
+  // no CTA leaves while a peer may still write into its shared memory (also when a
+  // bounded wait gave up: every CTA reaches this barrier)
+  __syncwarp();
+  cluster_wait();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -704,8 +733,8 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void*
 }
 
 struct FPlan {
-  int N, Np, rb, S, kc, tiles, rows_max, nchmax;
-  uint32_t off_scales, off_x, off_a, off_gw, off_gz, off_bt, off_q, off_ctrl, off_rt, off_ts;
+  int N, Np, rb, S, kc, tiles, rows_max, nchmax, alias_recv, lora_in_a;
+  uint32_t off_scales, off_x, off_a, off_gw, off_gz, off_q, off_ctrl, off_rp, off_bq, off_tq;
   size_t smem;
 };
 
@@ -719,23 +748,48 @@ bool layout(FPlan& f, int r) {
   f.off_a = al1k(f.off_x + static_cast<size_t>(nslab) * f.N * 128);
   f.off_gw = al1k(f.off_a + static_cast<size_t>(nslab) * f.rb * 128);
   f.off_gz = f.off_gw + f.nchmax * kChunkK * 4;
-  f.off_bt = f.off_gz + f.nchmax * kChunkK * 4;
-  f.off_q = f.off_bt + static_cast<uint32_t>(align_up(static_cast<size_t>(r > 0 ? r : 1) * f.rows_max * 4, 16));
+  f.off_q = f.off_gz + f.nchmax * kChunkK * 4;
   f.off_ctrl = f.off_q + static_cast<uint32_t>(align_up(static_cast<size_t>(f.S) * f.N * 4, 16));
   f.off_ctrl = static_cast<uint32_t>(align_up(f.off_ctrl, 128));
   size_t end = f.off_ctrl + sizeof(Ctrl);
   // the LoRA-down MMA reads 128 rows of every u slab (rows >= N are don't-care)
   const size_t read_end = f.off_x + static_cast<size_t>(nslab - 1) * f.N * 128 + 128 * 128;
   if (end < read_end) end = read_end;
-  f.smem = end + 1024;  // alignment slack
-  if (f.smem < kMinSmem) f.smem = kMinSmem;
-  // receive buffers over the dead stages: P [S][rows_max][Np], T [S][N][rb], lambda t [N][rb + 4]
-  f.off_rt = static_cast<uint32_t>(align_up(static_cast<size_t>(f.S) * f.rows_max * f.Np * 4, 16));
-  f.off_ts = f.off_rt + static_cast<uint32_t>(static_cast<size_t>(f.S) * f.N * f.rb * 4);
-  const size_t alias_end = f.off_ts + static_cast<size_t>(f.N) * (f.rb + 4) * 4;
+  // Two buffers may have a region of their own or share one:
+  //  - the LoRA up-projection operands (B [128][64] and t [N][64], bf16): own region, or
+  //    over the A slabs, which are free once the down-projection is done;
+  //  - the partial-output receive buffers P [S][rows_max][Np]: own region (peers may send
+  //    as soon as they are done), or over the stage region, which every CTA of the
+  //    cluster must have finished with first.
+  const size_t base = align_up(end, 1024);
+  const size_t lora_bytes = r > 0 ? static_cast<size_t>(kTileO) * 128 + align_up(static_cast<size_t>(f.N) * 128, 1024) : 0;
+  const size_t a_region = f.off_gw - f.off_a;
+  const size_t rp_bytes = static_cast<size_t>(f.S) * f.rows_max * f.Np * 4;
+  bool placed = false;
+  for (int opt = 0; opt < 4 && !placed; ++opt) {
+    const bool l_in_a = opt == 1 || opt == 2, rp_alias = opt >= 2;
+    if (l_in_a && (r == 0 || lora_bytes > a_region)) continue;
+    if (rp_alias && rp_bytes > f.off_gw) continue;
+    size_t e = base;
+    f.off_bq = f.off_tq = 0;
+    if (r > 0) {
+      const size_t lb = l_in_a ? f.off_a : e;
+      f.off_bq = static_cast<uint32_t>(lb);
+      f.off_tq = static_cast<uint32_t>(lb + static_cast<size_t>(kTileO) * 128);
+      if (!l_in_a) e += lora_bytes;
+    }
+    f.off_rp = rp_alias ? 0u : static_cast<uint32_t>(e);
+    if (!rp_alias) e += rp_bytes;
+    if (e + 1024 > 227 * 1024) continue;  // + alignment slack
+    f.lora_in_a = l_in_a ? 1 : 0;
+    f.alias_recv = rp_alias ? 1 : 0;
+    f.smem = e + 1024;
+    if (f.smem < kMinSmem) f.smem = kMinSmem;
+    placed = true;
+  }
   // tensor memory: 2 weight buffers of 128 columns, D1 twice (N), Dt twice (rb)
   const bool tmem_ok = 256 + 2 * f.N + 2 * f.rb <= static_cast<int>(kTmemCols);
-  return tmem_ok && f.smem <= 227 * 1024 && alias_end <= f.off_gw;
+  return placed && tmem_ok;
 }
 
 int max_active_clusters(size_t smem, int cs) {
@@ -771,7 +825,7 @@ cudaError_t set_attributes() {
 // every CTA's slice is at most 3 chunks, shared memory fits and all clusters can be
 // resident at once; none -> this path does not apply.
 bool make_plan(int64_t M, int64_t d_i, int64_t d_o, int r, FPlan& out) {
-  if (M < 1 || M > kMaxN || d_i < kChunkK || d_i % kChunkK != 0 || r < 0 || r > kMaxR || d_o < 1) return false;
+  if (M < 1 || M > kMaxN || d_i < kChunkK || d_i % kChunkK != 0 || r < 0 || r > kMaxRFused || d_o < 1) return false;
   FPlan f{};
   f.N = static_cast<int>((M + 15) / 16 * 16);
   f.Np = f.N + 4;
@@ -883,11 +937,13 @@ cudaError_t launch_linear_fused(const LinearArgs& a, cudaStream_t stream) {
   p.off_a = f.off_a;
   p.off_gw = f.off_gw;
   p.off_gz = f.off_gz;
-  p.off_bt = f.off_bt;
   p.off_q = f.off_q;
   p.off_ctrl = f.off_ctrl;
-  p.off_rt = f.off_rt;
-  p.off_ts = f.off_ts;
+  p.off_rp = f.off_rp;
+  p.off_bq = f.off_bq;
+  p.off_tq = f.off_tq;
+  p.alias_recv = f.alias_recv;
+  p.lora_in_a = f.lora_in_a;
 
   cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
