@@ -88,7 +88,7 @@ constexpr size_t kMinSmem = 120 * 1024;  // > half an SM: one CTA per SM, so its
 
 struct FParams {
   int64_t M, d_i, d_o;
-  int N, Np, Mp, rb, r, S, kc, rows_max, nbuf;
+  int N, Np, Mp, rb, r, S, kc, rows_max, nbuf, nacc;
   float lambda, eps, inv_d;
   const float* s_g;
   const float* w_norm;
@@ -114,7 +114,8 @@ struct Ctrl {
   uint64_t a_empty[kMaxChunks]; // the MMAs reading buffer b are done
   uint64_t a_in, x_in, g_in;   // LoRA A slice, x slice, w_norm / z slices landed
   uint64_t g_ready;            // w_norm + z formed
-  uint64_t act_ready;          // every token row converted
+  uint64_t rows_ready;         // every token row converted (one arrival per row)
+  uint64_t a16_ready;          // the LoRA A slice converted to f16
   uint64_t dt_full;            // the LoRA down-projection MMAs done
   uint64_t lora_ready;         // B and t of the up-projection in shared memory
   uint64_t d_full;             // every MMA done
@@ -122,7 +123,6 @@ struct Ctrl {
   uint32_t tmem_base;
   int abort_flag;
   int next_row;                // token-row queue of the conversion
-  float s_g;
   alignas(16) float cinv[kMaxN];  // 1 / c of this split, per token row
   float rs[kMaxN];
 };
@@ -161,86 +161,161 @@ PL_DEVINL void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t 
 PL_DEVINL int owner_row0(int s, int S) { return (s * kTileO) / S; }
 
 // Token rows of x (one warp): sum of squares and max |u| over this CTA's slice, then
-// u c -> f16 in place.  Rows come from a queue shared by the conversion and dequant
-// warps, 32 / L at a time: lanes L i .. L i + L - 1 take row base + i, lane L i + l the
-// 16-byte pieces l, l + L, ... of the row (piece q: slab q / 8, column q % 8).  L is 32
-// for few rows (short chains per lane), 8 for many (more rows in flight).  Out of line:
-// it is called from two roles.
+// u c -> f16 in place.  Rows come two at a time from a queue shared by the conversion
+// and dequant warps.  Lane l takes the 16-byte pieces l, l + 32, ... of a row (piece q:
+// slab q / 8, column q % 8; one piece per lane per chunk), so its eight values of
+// w_norm + z per piece stay in registers for every row, and the row's pieces stay in
+// registers between the two passes.  Out of line: it is called from two roles.
 __device__ __noinline__ void convert_rows_warp(uint8_t* smem, uint32_t off_x, const float* gsh, float* qrecv, Ctrl* C,
                                                int N, int nslab, int M, int S, int me, bool norm,
                                                volatile int* abort_flag) {
-  const int L = M <= 12 ? 32 : (M <= 24 ? 16 : 8);
-  const int lane = threadIdx.x & 31, gi = lane / L, sl = lane % L, step = 32 / L;
-  const int npieces = nslab * 8;
+  constexpr int kRows = 1;
+  const int lane = threadIdx.x & 31;
+  const int nk = nslab / 4;  // pieces per lane: one per chunk
+  const int ch = lane & 7;
+  float g[kMaxChunks][8];
+#pragma unroll
+  for (int k = 0; k < kMaxChunks; ++k) {
+    float4 ga = make_float4(1.f, 1.f, 1.f, 1.f), gb = ga;
+    if (norm && k < nk) {
+      const float4* g4 = reinterpret_cast<const float4*>(gsh) + (lane + 32 * k) * 2;
+      ga = g4[0];
+      gb = g4[1];
+    }
+    g[k][0] = ga.x; g[k][1] = ga.y; g[k][2] = ga.z; g[k][3] = ga.w;
+    g[k][4] = gb.x; g[k][5] = gb.y; g[k][6] = gb.z; g[k][7] = gb.w;
+  }
+  // byte offset of this lane's piece k within a row n: slab (lane + 32 k) / 8, column ch
+  auto piece = [&](int n, int k) {
+    return off_x + static_cast<uint32_t>(n * 128 + ((lane >> 3) + 4 * k) * N * 128 + ((ch ^ (n & 7)) << 4));
+  };
   const uint32_t recv_bar = smem_u32(&C->recv);
   for (;;) {
     int base = 0;
-    if (lane == 0) base = atomicAdd(&C->next_row, step);
+    if (lane == 0) base = atomicAdd(&C->next_row, kRows);
     base = __shfl_sync(0xFFFFFFFFu, base, 0);
     if (base >= M || *abort_flag) break;
-    const int n = base + gi;
-    const bool live = n < M;
-    uint8_t* rowp = smem + off_x + n * 128;
-    const float4* g4 = reinterpret_cast<const float4*>(gsh);
-    float ss = 0.f, mx = 0.f;
-    if (live) {
-#pragma unroll 2
-      for (int q = sl; q < npieces; q += L) {
-        const int slab = q >> 3, ch = q & 7;
-        const uint4 v = *reinterpret_cast<const uint4*>(rowp + slab * N * 128 + ((ch ^ (n & 7)) << 4));
-        float4 ga = make_float4(1.f, 1.f, 1.f, 1.f), gb = ga;
-        if (norm) {
-          ga = g4[slab * 16 + ch * 2];
-          gb = g4[slab * 16 + ch * 2 + 1];
+    uint4 v[kRows][kMaxChunks];
+    float ss[kRows], mx[kRows];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+      const int n = base + r;
+      ss[r] = 0.f;
+      mx[r] = 0.f;
+#pragma unroll
+      for (int k = 0; k < kMaxChunks; ++k) {
+        v[r][k] = make_uint4(0u, 0u, 0u, 0u);
+        if (k < nk && n < M) v[r][k] = *reinterpret_cast<const uint4*>(smem + piece(n, k));
+        const uint32_t w[4] = {v[r][k].x, v[r][k].y, v[r][k].z, v[r][k].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float x0 = bf16lo_to_f32(w[i]), x1 = bf16hi_to_f32(w[i]);
+          ss[r] = fmaf(x0, x0, fmaf(x1, x1, ss[r]));
+          mx[r] = fmaxf(mx[r], fmaxf(fabsf(x0 * g[k][2 * i]), fabsf(x1 * g[k][2 * i + 1])));
         }
-        const float x0 = bf16lo_to_f32(v.x), x1 = bf16hi_to_f32(v.x), x2 = bf16lo_to_f32(v.y), x3 = bf16hi_to_f32(v.y);
-        const float x4 = bf16lo_to_f32(v.z), x5 = bf16hi_to_f32(v.z), x6 = bf16lo_to_f32(v.w), x7 = bf16hi_to_f32(v.w);
-        ss = fmaf(x0, x0, fmaf(x1, x1, fmaf(x2, x2, fmaf(x3, x3, ss))));
-        ss = fmaf(x4, x4, fmaf(x5, x5, fmaf(x6, x6, fmaf(x7, x7, ss))));
-        mx = fmaxf(fmaxf(fmaxf(fabsf(x0 * ga.x), fabsf(x1 * ga.y)), fmaxf(fabsf(x2 * ga.z), fabsf(x3 * ga.w))),
-                   fmaxf(fmaxf(fabsf(x4 * gb.x), fabsf(x5 * gb.y)), fmaxf(fabsf(x6 * gb.z), fmaxf(fabsf(x7 * gb.w), mx))));
       }
     }
-    for (int o = L / 2; o > 0; o >>= 1) {
-      ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
-      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-    }
-    // c = 2^e with max |u| c in [2^13, 2^14): e from the exponent field of max |u|
-    const int ex = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu) - 127;
-    int e = mx > 0.f ? 13 - ex : 0;
-    e = e < -100 ? -100 : (e > 100 ? 100 : e);
-    const float cs = __int_as_float((127 + e) << 23);
-    if (live) {
-#pragma unroll 2
-      for (int q = sl; q < npieces; q += L) {
-        const int slab = q >> 3, ch = q & 7;
-        uint4* pv = reinterpret_cast<uint4*>(rowp + slab * N * 128 + ((ch ^ (n & 7)) << 4));
-        const uint4 v = *pv;
-        float4 ga = make_float4(cs, cs, cs, cs), gb = ga;
-        if (norm) {
-          ga = g4[slab * 16 + ch * 2];
-          gb = g4[slab * 16 + ch * 2 + 1];
-          ga.x *= cs; ga.y *= cs; ga.z *= cs; ga.w *= cs;
-          gb.x *= cs; gb.y *= cs; gb.z *= cs; gb.w *= cs;
-        }
-        *pv = make_uint4(f32x2_to_f16x2(bf16lo_to_f32(v.x) * ga.x, bf16hi_to_f32(v.x) * ga.y),
-                         f32x2_to_f16x2(bf16lo_to_f32(v.y) * ga.z, bf16hi_to_f32(v.y) * ga.w),
-                         f32x2_to_f16x2(bf16lo_to_f32(v.z) * gb.x, bf16hi_to_f32(v.z) * gb.y),
-                         f32x2_to_f16x2(bf16lo_to_f32(v.w) * gb.z, bf16hi_to_f32(v.w) * gb.w));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+      for (int r = 0; r < kRows; ++r) {
+        ss[r] += __shfl_xor_sync(0xFFFFFFFFu, ss[r], o);
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xFFFFFFFFu, mx[r], o));
       }
-      if (sl == 0) {
+    }
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+      const int n = base + r;
+      if (n >= M) continue;
+      // c = 2^e with max |u| c in [2^13, 2^14): e from the exponent field of max |u|
+      const int ex = static_cast<int>((__float_as_uint(mx[r]) >> 23) & 0xFFu) - 127;
+      int e = mx[r] > 0.f ? 13 - ex : 0;
+      e = e < -100 ? -100 : (e > 100 ? 100 : e);
+      const float cs = __int_as_float((127 + e) << 23);
+#pragma unroll
+      for (int k = 0; k < kMaxChunks; ++k) {
+        if (k < nk) {
+          const uint32_t w[4] = {v[r][k].x, v[r][k].y, v[r][k].z, v[r][k].w};
+          uint32_t o[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            o[i] = f32x2_to_f16x2(bf16lo_to_f32(w[i]) * (g[k][2 * i] * cs), bf16hi_to_f32(w[i]) * (g[k][2 * i + 1] * cs));
+          *reinterpret_cast<uint4*>(smem + piece(n, k)) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+      if (lane == 0) {
         C->cinv[n] = __int_as_float((127 - e) << 23);
-        if (norm) qrecv[me * N + n] = ss;
-      } else if (norm && sl < S) {  // the row's sum of squares to every peer
-        const uint32_t dst = static_cast<uint32_t>((me + sl) % S);
-        st_async_f32(mapa_shared(smem_u32(&qrecv[me * N + n]), dst), ss, mapa_shared(recv_bar, dst));
+        if (norm) qrecv[me * N + n] = ss[r];
+      } else if (norm && lane < S) {  // the row's sum of squares to every peer
+        const uint32_t dst = static_cast<uint32_t>((me + lane) % S);
+        st_async_f32(mapa_shared(smem_u32(&qrecv[me * N + n]), dst), ss[r], mapa_shared(recv_bar, dst));
       }
+    }
+    fence_proxy_async_smem();  // the f16 operands are read by the tensor cores
+    __syncwarp();
+    if (lane == 0) {
+      const int live = M - base < kRows ? M - base : kRows;
+      for (int r = 0; r < live; ++r) mbar_arrive(smem_u32(&C->rows_ready));
     }
   }
-  fence_proxy_async_smem();  // the f16 operands are read by the tensor cores
-  __syncwarp();
-  if (lane == 0) mbar_arrive(smem_u32(&C->act_ready));
   if (lane == 0) PL_TLF(32 + (threadIdx.x >> 5));
+}
+
+// The K steps q, q + Q, ... of one chunk (16 steps of 16): D (+)= W_hat/s_g (tensor
+// memory, 8 columns per step) x u^T (shared memory; 2 units of 16 B per step, one slab
+// per 4 steps).
+template <int Q>
+PL_DEVINL void mma_d1_chunk(uint32_t dtm, uint32_t abuf, uint64_t xc, uint32_t xslab, uint32_t idesc, int q,
+                            bool first) {
+#pragma unroll
+  for (int i = 0; i < (kChunkK / 16 + Q - 1) / Q; ++i) {
+    const int kk = q + Q * i;
+    if (kk < kChunkK / 16)
+      mma_ts(dtm, abuf + 8u * kk, xc + static_cast<uint64_t>((kk >> 2) * xslab + 2u * (kk & 3)), idesc,
+             (!first || i > 0) ? 1u : 0u);
+  }
+}
+
+// D1 issuer q of nacc (one thread): K steps q, q + nacc, ... of every chunk as it is
+// dequantised, into accumulator q (a single issuing thread is latency-bound on these
+// small MMAs); issuer 0 then adds the LoRA up-projection (rank rb, 0 for none) as one
+// more K step.  Out of line: it is called from four roles.
+__device__ __noinline__ void issue_d1_thread(Ctrl& C, int q, int nacc, int nch, int nbuf, int N, int rb,
+                                             uint32_t tmem, uint32_t col_d1, uint32_t x_addr, uint32_t bq_addr,
+                                             uint32_t tq_addr, volatile int* abort_flag) {
+  const uint32_t dtm = tmem + col_d1 + static_cast<uint32_t>(q * N);
+  const uint64_t xd0 = smem_desc_sw128(x_addr, 1024);
+  const uint32_t xslab = static_cast<uint32_t>(N) * 8u;  // one 64-element slab of u, in 16-byte units
+  const uint32_t idesc = idesc_f16(kTileO, N, 0);
+  bool go = wait_f(smem_u32(&C.rows_ready), 0, abort_flag);
+  if (q == 0) PL_TLF(15);
+  for (int c = 0; c < nch && go; ++c) {
+    go = wait_f(smem_u32(&C.a_full[c]), 0, abort_flag);
+    if (!go) break;
+    if (q == 0) PL_TLF(23 + c);
+    tc_fence_after();
+    const uint64_t xc = xd0 + static_cast<uint64_t>(4u * c * xslab);
+    const uint32_t ab = tmem + 128u * (c % nbuf);
+    if (nacc == 4) mma_d1_chunk<4>(dtm, ab, xc, xslab, idesc, q, c == 0);
+    else if (nacc == 3) mma_d1_chunk<3>(dtm, ab, xc, xslab, idesc, q, c == 0);
+    else mma_d1_chunk<2>(dtm, ab, xc, xslab, idesc, q, c == 0);
+    if (q == 0) PL_TLF(26 + c);
+    if (c + nbuf < nch) tc_commit(smem_u32(&C.a_empty[c % nbuf]));  // buffer reused by chunk c + nbuf
+  }
+  if (rb > 0 && q == 0 && go) {
+    // the LoRA up-projection as one more K step: B (bf16, as stored) times
+    // t = Dt lambda / s_g (bf16), which is lambda B A u in the units of D1
+    go = wait_f(smem_u32(&C.lora_ready), 0, abort_flag);
+    if (go) {
+      tc_fence_after();
+      const uint32_t idesc_l = idesc_f16(kTileO, N, 1);
+      const uint64_t bd = smem_desc_sw128(bq_addr, 1024);
+      const uint64_t td = smem_desc_sw128(tq_addr, 1024);
+      for (int k = 0; k < rb / 16; ++k) mma_ss(dtm, bd + 2u * k, td + 2u * k, idesc_l, 1u);
+    }
+  }
+  tc_commit(smem_u32(&C.d_full));  // also reached on abort: tracks every MMA issued
+  if (q == 0) PL_TLF(8);
 }
 
 // The staged LoRA A slice, bf16 -> f16 in place (16 bytes per step; `who` of `nthreads`).
@@ -279,7 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
   const uint32_t a_bytes = static_cast<uint32_t>(nslab) * p.rb * 128u;
   const uint32_t g_bytes = static_cast<uint32_t>(nch) * kChunkK * 4u;
   const int nbuf = p.nbuf;  // tensor-memory weight buffers (2 or 3) of 128 columns
-  const uint32_t colD1a = 128u * nbuf, colD1b = colD1a + N, colDta = colD1a + 2 * N, colDtb = colDta + p.rb;
+  const int nacc = p.nacc;  // D1 accumulators (2 to 4), one per issuing thread
+  const uint32_t colD1 = 128u * nbuf, colDta = colD1 + nacc * N, colDtb = colDta + p.rb;
 
   if (threadIdx.x == 0) {
     PL_TLF(0);
@@ -288,15 +364,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
       mbar_init(smem_u32(&C.wfull[c]), 1);
       mbar_init(smem_u32(&C.a_full[c]), kDeqWarps);
     }
-    for (int b = 0; b < kMaxChunks; ++b) mbar_init(smem_u32(&C.a_empty[b]), 2);  // the D1 issuers
+    for (int b = 0; b < kMaxChunks; ++b) mbar_init(smem_u32(&C.a_empty[b]), nacc);  // the D1 issuers
     mbar_init(smem_u32(&C.a_in), 1);
     mbar_init(smem_u32(&C.x_in), 1);
     mbar_init(smem_u32(&C.g_in), 1);
     mbar_init(smem_u32(&C.g_ready), kConvWarps);
-    mbar_init(smem_u32(&C.act_ready), kDeqWarps + kConvWarps + 1);  // + warp 1 (its share of A)
+    mbar_init(smem_u32(&C.rows_ready), M);
+    mbar_init(smem_u32(&C.a16_ready), kConvWarps + 1);  // + warp 1 (its share of A)
     mbar_init(smem_u32(&C.dt_full), 2);
     mbar_init(smem_u32(&C.lora_ready), 4 + 2);  // 4 dequant warps (B), 2 conversion warps (t)
-    mbar_init(smem_u32(&C.d_full), 2);
+    mbar_init(smem_u32(&C.d_full), nacc);
     mbar_init(smem_u32(&C.recv), 1);
     fence_mbar_init();
     PL_TLF(16);
@@ -344,6 +421,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
     convert_rows_warp(smem, p.off_x, gsh, qrecv, &C, N, nslab, M, S, me, norm, abort_flag);
   };
 
+  auto issue_d1 = [&](int q) {
+    issue_d1_thread(C, q, nacc, nch, nbuf, N, lora ? p.rb : 0, tmem, colD1, sbase + p.off_x, sbase + p.off_bq,
+                    sbase + p.off_tq, abort_flag);
+  };
+
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
@@ -364,6 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
       if (lora) drain(smem_u32(&C.a_in), 0);
       if (norm) drain(smem_u32(&C.g_in), 0);
       drain(xb, 0);
+      if (nacc > 3) issue_d1(3);
     }
     __syncwarp();
     if (p.alias_recv) {
@@ -375,7 +458,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
     if (lora) convert_a(smem + p.off_a, a_bytes, kConvThreads + lane, kConvThreads + 32, smem_u32(&C.a_in), abort_flag);
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&C.act_ready));
+    if (lane == 0) mbar_arrive(smem_u32(&C.a16_ready));
+    if (lane == 0 && nacc > 2) issue_d1(2);
+    __syncwarp();
     if (p.alias_recv) {
       cluster_arrive();
       cluster_wait();
@@ -389,6 +474,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
     bool ok = true;
     if (lora)  // A lands early (a weight): convert it while x is still on its way
       ok = convert_a(smem + p.off_a, a_bytes, ct, kConvThreads + 32, smem_u32(&C.a_in), abort_flag);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&C.a16_ready));
     if (ct == 0) PL_TLF(21);
     if (norm) {
       ok = wait_f(smem_u32(&C.g_in), 0, abort_flag) && ok;
@@ -408,52 +496,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
     if (ct == 0) PL_TLF(3);
     ok = wait_f(smem_u32(&C.g_ready), 0, abort_flag) && wait_f(smem_u32(&C.x_in), 0, abort_flag) && ok;
     if (ct == 0) PL_TLF(4);
-    convert_rows();  // also fences and arrives on act_ready
+    convert_rows();  // also fences and arrives on rows_ready
     if (ct == 0) PL_TLF(5);
     const bool tpart = cw >= 2;
     if (lane == 0) {
-      // issuer cw: accumulator D1a / D1b (cw 0 / 1) or Dta / Dtb (cw 2 / 3), even / odd K steps
-      const int par = cw & 1;
-      const uint32_t dcol = cw == 0 ? colD1a : (cw == 1 ? colD1b : (cw == 2 ? colDta : colDtb));
-      // Descriptors advance by constants: one K step is 32 bytes (2 units of 16 B), one
-      // 64-element slab N * 128 bytes (x) or rb * 128 bytes (A).  A single issuing thread
-      // spends most of its time on the arithmetic between MMAs, so none is left there.
-      const uint64_t xd0 = smem_desc_sw128(sbase + p.off_x, 1024) + 2u * par;
-      const uint32_t xslab = static_cast<uint32_t>(N) * 8u, aslab = static_cast<uint32_t>(p.rb) * 8u;
-      const uint32_t dtm = tmem + dcol;
-      bool go = wait_f(smem_u32(&C.act_ready), 0, abort_flag);
-      if (cw == 0) PL_TLF(15);
       if (!tpart) {
-        const uint32_t idesc = idesc_f16(kTileO, N, 0);
-        for (int c = 0; c < nch && go; ++c) {
-          go = wait_f(smem_u32(&C.a_full[c]), 0, abort_flag);
-          if (!go) break;
-          if (cw == 0) PL_TLF(23 + c);
-          tc_fence_after();
-          const uint64_t xc = xd0 + static_cast<uint64_t>(4u * c * xslab);
-          const uint32_t ac = tmem + 128u * (c % nbuf) + 8u * par;  // K step kk = 2 h + par
-#pragma unroll
-          for (int h = 0; h < kChunkK / 32; ++h)
-            mma_ts(dtm, ac + 16u * h, xc + (h >> 1) * xslab + 4u * (h & 1), idesc, (c > 0 || h > 0) ? 1u : 0u);
-          if (cw == 0) PL_TLF(26 + c);
-          if (c + nbuf < nch) tc_commit(smem_u32(&C.a_empty[c % nbuf]));  // buffer reused by chunk c + nbuf
-        }
-        if (lora && cw == 0 && go) {
-          // the LoRA up-projection as one more K step of D1a: B (bf16, as stored) times
-          // t = Dt lambda / s_g (bf16), which is lambda B A u in the units of D1
-          go = wait_f(smem_u32(&C.lora_ready), 0, abort_flag);
-          if (go) {
-            tc_fence_after();
-            const uint32_t idesc_l = idesc_f16(kTileO, N, 1);
-            const uint64_t bd = smem_desc_sw128(sbase + p.off_bq, 1024);
-            const uint64_t td = smem_desc_sw128(sbase + p.off_tq, 1024);
-            for (int k = 0; k < p.rb / 16; ++k) mma_ss(dtm, bd + 2u * k, td + 2u * k, idesc_l, 1u);
-          }
-        }
-        tc_commit(smem_u32(&C.d_full));  // also reached on abort: tracks every MMA issued
-        if (cw == 0) PL_TLF(8);
+        issue_d1(cw);  // D1 issuers 0 and 1
       } else if (lora) {
-        // the LoRA down-projection needs no weight buffer: all of it at once
+        // the LoRA down-projection needs no weight buffer: all of it at once, even / odd
+        // K steps into Dta / Dtb (cw 2 / 3)
+        const int par = cw & 1;
+        const uint32_t dtm = tmem + (cw == 2 ? colDta : colDtb);
+        const uint64_t xd0 = smem_desc_sw128(sbase + p.off_x, 1024) + 2u * par;
+        const uint32_t xslab = static_cast<uint32_t>(N) * 8u, aslab = static_cast<uint32_t>(p.rb) * 8u;
+        bool go = wait_f(smem_u32(&C.rows_ready), 0, abort_flag) && wait_f(smem_u32(&C.a16_ready), 0, abort_flag);
         const uint32_t idesc = idesc_f16(kTileO, p.rb, 0);
         const uint64_t ad0 = smem_desc_sw128(sbase + p.off_a, 1024) + 2u * par;
         for (int c = 0; c < nch && go; ++c) {
@@ -512,35 +568,37 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
     const int row = quarter * 32 + lane;  // weight row within the tile
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const int et = threadIdx.x - 64;      // 0 .. 255
-    // B row of this thread's weight row, bf16 pairs (a weight: read before any data wait;
-    // the g == 0 threads cover the 128 rows)
-    uint32_t bq[kMaxRFused / 2];
-#pragma unroll
-    for (int j = 0; j < kMaxRFused / 2; ++j) bq[j] = 0u;
-    if (lora && g == 0 && static_cast<int64_t>(row0) + row < p.d_o) {
-      const int64_t o = static_cast<int64_t>(row0) + row;
-      if ((p.r & 7) == 0) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.B + o * p.r);
-#pragma unroll
-        for (int q = 0; q < kMaxRFused / 8; ++q)
-          if (8 * q < p.r) {
-            const uint4 v = src[q];
-            bq[4 * q] = v.x; bq[4 * q + 1] = v.y; bq[4 * q + 2] = v.z; bq[4 * q + 3] = v.w;
-          }
-      } else {
-        const uint16_t* src = reinterpret_cast<const uint16_t*>(p.B + o * p.r);
-#pragma unroll
-        for (int j = 0; j < kMaxRFused; ++j)
-          if (j < p.r) bq[j >> 1] |= static_cast<uint32_t>(src[j]) << (16 * (j & 1));
-      }
-    }
-    // B rows of the up-projection operand (K-major, 128-byte swizzled; columns >= r are 0)
-    auto write_bq = [&]() {
+    const float s_g = *p.s_g;             // a weight input: not written by the preceding kernel
+    // B rows of the up-projection operand (K-major, 128-byte swizzled; columns >= r are
+    // 0), one row per g == 0 thread, from global memory (a weight)
+    auto write_bq = [&](bool wait_dt) {
       if (g == 0) {
+        uint32_t bq[kMaxRFused / 2];
+#pragma unroll
+        for (int j = 0; j < kMaxRFused / 2; ++j) bq[j] = 0u;
+        const int64_t o = static_cast<int64_t>(row0) + row;
+        if (o < p.d_o) {
+          if ((p.r & 7) == 0) {
+            const uint4* src = reinterpret_cast<const uint4*>(p.B + o * p.r);
+#pragma unroll
+            for (int q = 0; q < kMaxRFused / 8; ++q)
+              if (8 * q < p.r) {
+                const uint4 v = src[q];
+                bq[4 * q] = v.x; bq[4 * q + 1] = v.y; bq[4 * q + 2] = v.z; bq[4 * q + 3] = v.w;
+              }
+          } else {
+            const uint16_t* src = reinterpret_cast<const uint16_t*>(p.B + o * p.r);
+#pragma unroll
+            for (int j = 0; j < kMaxRFused; ++j)
+              if (j < p.r) bq[j >> 1] |= static_cast<uint32_t>(src[j]) << (16 * (j & 1));
+          }
+        }
+        // over the A slabs: only once the down-projection is done with them
+        const bool w_ok = !wait_dt || wait_f(smem_u32(&C.dt_full), 0, abort_flag);
         uint8_t* bqs = smem + p.off_bq + row * 128;
 #pragma unroll
         for (int j8 = 0; j8 < kMaxRFused / 8; ++j8)
-          if (j8 * 8 < p.rb)
+          if (j8 * 8 < p.rb && w_ok)
             *reinterpret_cast<uint4*>(bqs + ((j8 ^ (row & 7)) << 4)) =
                 make_uint4(bq[4 * j8], bq[4 * j8 + 1], bq[4 * j8 + 2], bq[4 * j8 + 3]);
         fence_proxy_async_smem();
@@ -548,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
         if (lane == 0) mbar_arrive(smem_u32(&C.lora_ready));
       }
     };
-    if (lora && !p.lora_in_a) write_bq();
+    if (lora && !p.lora_in_a) write_bq(false);
     bool ok = true, converted = false;
     for (int c = 0; c < nch; ++c) {
       if (c == nbuf) {  // buffer 0 is needed again: help with the activations first
@@ -593,11 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
       ok = wait_f(smem_u32(&C.g_ready), 0, abort_flag) && wait_f(smem_u32(&C.x_in), 0, abort_flag) && ok;
       convert_rows();
     }
-    if (lora && p.lora_in_a) {  // the A slabs are free once the down-projection is done
-      ok = wait_f(smem_u32(&C.dt_full), 0, abort_flag) && ok;
-      write_bq();
-    }
-    if (et == 0) C.s_g = *p.s_g;  // a weight input: not written by the preceding kernel
+    if (lora && p.lora_in_a) write_bq(true);
     // ---------------------------------------------------------------- epilogue: gather
     ok = wait_f(smem_u32(&C.d_full), 0, abort_flag) && ok;
     if (et == 0) PL_TLF(9);
@@ -608,21 +662,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
 #pragma unroll
     for (int cb = 0; cb < 4; ++cb) {
       if (cb * 8 < half && n0 + cb * 8 < Mp) {
-        uint32_t a8[8], b8[8];
-        tmem_ld8(tmem + lane_addr + colD1a + n0 + cb * 8, a8);
-        tmem_ld8(tmem + lane_addr + colD1b + n0 + cb * 8, b8);
+        uint32_t t8[4][8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (q < nacc) tmem_ld8(tmem + lane_addr + colD1 + q * N + n0 + cb * 8, t8[q]);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 8; ++i) d1[cb * 8 + i] = __uint_as_float(a8[i]) + __uint_as_float(b8[i]);
+        for (int i = 0; i < 8; ++i) {
+          float v = __uint_as_float(t8[0][i]) + __uint_as_float(t8[1][i]);
+          if (nacc > 2) v += __uint_as_float(t8[2][i]);
+          if (nacc > 3) v += __uint_as_float(t8[3][i]);
+          d1[cb * 8 + i] = v;
+        }
       }
     }
+    if (et == 0) PL_TLF(29);
+    ok = wait_f(smem_u32(&C.rows_ready), 0, abort_flag) && ok;  // orders the reads of 1 / c
     const bool good = ok && !*abort_flag;
     // P[row, n] = s_g D1[row, n] / c_n: this split's share of W_hat u + lambda B A u
-    const float s_g = C.s_g;
-    float pv[32];
+    float* pv = d1;  // in place
 #pragma unroll
     for (int i = 0; i < 32; ++i)
       if (i < half && n0 + i < Mp) pv[i] = good ? C.cinv[n0 + i] * s_g * d1[i] : 0.f;
+    if (et == 0) PL_TLF(30);
     if (p.alias_recv) {  // the receive buffers lie over the stage region: every CTA is done with it
       cluster_arrive();
       cluster_wait();
@@ -922,7 +984,10 @@ cudaError_t launch_linear_fused(const LinearArgs& a, cudaStream_t stream) {
   p.S = f.S;
   p.kc = f.kc;
   p.rows_max = f.rows_max;
+  // tensor memory: nbuf weight buffers of 128 columns, nacc D1 accumulators of N, Dt twice (rb)
   p.nbuf = 384 + 2 * f.N + 2 * f.rb <= static_cast<int>(kTmemCols) ? 3 : 2;
+  p.nacc = 2;
+  while (p.nacc < 4 && 128 * p.nbuf + (p.nacc + 1) * f.N + 2 * f.rb <= static_cast<int>(kTmemCols)) ++p.nacc;
   p.lambda = a.lambda;
   p.eps = a.eps;
   p.inv_d = 1.0f / static_cast<float>(a.d_i);
