@@ -23,9 +23,8 @@
 //   warps 10-13  w_norm + z; A bf16 -> f16 in place; token rows of x from a shared
 //                queue (sum of squares and max |u| of the row, then u c -> f16 in
 //                place; the row sums go to every CTA of the cluster); then lane 0 of
-//                each issues
-//                tcgen05.mma kind::f16 into its own accumulator (a single issuing
-//                thread is latency-bound on these small MMAs): D1 += W_hat/s_g (tensor
+//                each issues tcgen05.mma kind::f16 into its own accumulator (a single
+//                issuing thread is latency-bound on these small MMAs): D1 += W_hat/s_g (tensor
 //                memory) x u^T over even / odd K steps as the chunks are dequantised,
 //                and Dt^T += u x A^T (shared memory) over even / odd K steps at once;
 //                warps 12-13 then round t = Dt lambda / s_g to bf16 into shared memory
@@ -78,6 +77,7 @@ constexpr int kMaxSplit = 8;
 constexpr int kMaxN = 64;
 constexpr int kMaxRFused = 32;  // LoRA rank this kernel takes (B rows are held in registers)
 constexpr int kDeqWarps = 8;
+constexpr int kAcc = 2;  // D1 accumulators, each with its own issuing thread (even / odd K steps)
 constexpr int kConvWarps = 4;
 constexpr int kConvThreads = kConvWarps * 32;
 constexpr int kEpiThreads = kDeqWarps * 32;
@@ -88,7 +88,7 @@ constexpr size_t kMinSmem = 120 * 1024;  // > half an SM: one CTA per SM, so its
 
 struct FParams {
   int64_t M, d_i, d_o;
-  int N, Np, Mp, rb, r, S, kc, rows_max, nbuf, nacc;
+  int N, Np, Mp, rb, r, S, kc, rows_max, nbuf;
   float lambda, eps, inv_d;
   const float* s_g;
   const float* w_norm;
@@ -119,7 +119,9 @@ struct Ctrl {
   uint64_t dt_full;            // the LoRA down-projection MMAs done
   uint64_t lora_ready;         // B and t of the up-projection in shared memory
   uint64_t d_full;             // every MMA done
-  uint64_t recv;               // the peers' shares arrived
+  uint64_t recv;               // the peers' partial outputs arrived
+  uint64_t q_full;             // the peers' row sums of x^2 arrived
+  uint64_t rs_ready;           // rs of every token row formed
   uint32_t tmem_base;
   int abort_flag;
   int next_row;                // token-row queue of the conversion
@@ -189,7 +191,7 @@ __device__ __noinline__ void convert_rows_warp(uint8_t* smem, uint32_t off_x, co
   auto piece = [&](int n, int k) {
     return off_x + static_cast<uint32_t>(n * 128 + ((lane >> 3) + 4 * k) * N * 128 + ((ch ^ (n & 7)) << 4));
   };
-  const uint32_t recv_bar = smem_u32(&C->recv);
+  const uint32_t q_bar = smem_u32(&C->q_full);
   for (;;) {
     int base = 0;
     if (lane == 0) base = atomicAdd(&C->next_row, kRows);
@@ -248,7 +250,7 @@ __device__ __noinline__ void convert_rows_warp(uint8_t* smem, uint32_t off_x, co
         if (norm) qrecv[me * N + n] = ss[r];
       } else if (norm && lane < S) {  // the row's sum of squares to every peer
         const uint32_t dst = static_cast<uint32_t>((me + lane) % S);
-        st_async_f32(mapa_shared(smem_u32(&qrecv[me * N + n]), dst), ss[r], mapa_shared(recv_bar, dst));
+        st_async_f32(mapa_shared(smem_u32(&qrecv[me * N + n]), dst), ss[r], mapa_shared(q_bar, dst));
       }
     }
     fence_proxy_async_smem();  // the f16 operands are read by the tensor cores
@@ -276,11 +278,11 @@ PL_DEVINL void mma_d1_chunk(uint32_t dtm, uint32_t abuf, uint64_t xc, uint32_t x
   }
 }
 
-// D1 issuer q of nacc (one thread): K steps q, q + nacc, ... of every chunk as it is
+// D1 issuer q of kAcc (one thread): K steps q, q + kAcc, ... of every chunk as it is
 // dequantised, into accumulator q (a single issuing thread is latency-bound on these
 // small MMAs); issuer 0 then adds the LoRA up-projection (rank rb, 0 for none) as one
-// more K step.  Out of line: it is called from four roles.
-__device__ __noinline__ void issue_d1_thread(Ctrl& C, int q, int nacc, int nch, int nbuf, int N, int rb,
+// more K step.  Out of line: it is called from two warps.
+__device__ __noinline__ void issue_d1_thread(Ctrl& C, int q, int nch, int nbuf, int N, int rb,
                                              uint32_t tmem, uint32_t col_d1, uint32_t x_addr, uint32_t bq_addr,
                                              uint32_t tq_addr, volatile int* abort_flag) {
   const uint32_t dtm = tmem + col_d1 + static_cast<uint32_t>(q * N);
@@ -296,9 +298,7 @@ __device__ __noinline__ void issue_d1_thread(Ctrl& C, int q, int nacc, int nch, 
     tc_fence_after();
     const uint64_t xc = xd0 + static_cast<uint64_t>(4u * c * xslab);
     const uint32_t ab = tmem + 128u * (c % nbuf);
-    if (nacc == 4) mma_d1_chunk<4>(dtm, ab, xc, xslab, idesc, q, c == 0);
-    else if (nacc == 3) mma_d1_chunk<3>(dtm, ab, xc, xslab, idesc, q, c == 0);
-    else mma_d1_chunk<2>(dtm, ab, xc, xslab, idesc, q, c == 0);
+    mma_d1_chunk<kAcc>(dtm, ab, xc, xslab, idesc, q, c == 0);
     if (q == 0) PL_TLF(26 + c);
     if (c + nbuf < nch) tc_commit(smem_u32(&C.a_empty[c % nbuf]));  // buffer reused by chunk c + nbuf
   }
@@ -354,8 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
   const uint32_t a_bytes = static_cast<uint32_t>(nslab) * p.rb * 128u;
   const uint32_t g_bytes = static_cast<uint32_t>(nch) * kChunkK * 4u;
   const int nbuf = p.nbuf;  // tensor-memory weight buffers (2 or 3) of 128 columns
-  const int nacc = p.nacc;  // D1 accumulators (2 to 4), one per issuing thread
-  const uint32_t colD1 = 128u * nbuf, colDta = colD1 + nacc * N, colDtb = colDta + p.rb;
+  const uint32_t colD1 = 128u * nbuf, colDta = colD1 + kAcc * N, colDtb = colDta + p.rb;
 
   if (threadIdx.x == 0) {
     PL_TLF(0);
@@ -364,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
       mbar_init(smem_u32(&C.wfull[c]), 1);
       mbar_init(smem_u32(&C.a_full[c]), kDeqWarps);
     }
-    for (int b = 0; b < kMaxChunks; ++b) mbar_init(smem_u32(&C.a_empty[b]), nacc);  // the D1 issuers
+    for (int b = 0; b < kMaxChunks; ++b) mbar_init(smem_u32(&C.a_empty[b]), kAcc);  // the D1 issuers
     mbar_init(smem_u32(&C.a_in), 1);
     mbar_init(smem_u32(&C.x_in), 1);
     mbar_init(smem_u32(&C.g_in), 1);
@@ -373,9 +372,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
     mbar_init(smem_u32(&C.a16_ready), kConvWarps + 1);  // + warp 1 (its share of A)
     mbar_init(smem_u32(&C.dt_full), 2);
     mbar_init(smem_u32(&C.lora_ready), 4 + 2);  // 4 dequant warps (B), 2 conversion warps (t)
-    mbar_init(smem_u32(&C.d_full), nacc);
+    mbar_init(smem_u32(&C.d_full), kAcc);
     mbar_init(smem_u32(&C.recv), 1);
+    mbar_init(smem_u32(&C.q_full), 1);
+    mbar_init(smem_u32(&C.rs_ready), 2);  // warps kConvWarp0 + 2, + 3
     fence_mbar_init();
+    mbar_arrive_expect_tx(smem_u32(&C.q_full), norm ? static_cast<uint32_t>((S - 1) * M * 4) : 0u);
     PL_TLF(16);
     const uint64_t pol = policy_evict_first();  // weights are streamed once
     for (int c = 0; c < nch; ++c) {
@@ -422,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
   };
 
   auto issue_d1 = [&](int q) {
-    issue_d1_thread(C, q, nacc, nch, nbuf, N, lora ? p.rb : 0, tmem, colD1, sbase + p.off_x, sbase + p.off_bq,
+    issue_d1_thread(C, q, nch, nbuf, N, lora ? p.rb : 0, tmem, colD1, sbase + p.off_x, sbase + p.off_bq,
                     sbase + p.off_tq, abort_flag);
   };
 
@@ -446,7 +448,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
       if (lora) drain(smem_u32(&C.a_in), 0);
       if (norm) drain(smem_u32(&C.g_in), 0);
       drain(xb, 0);
-      if (nacc > 3) issue_d1(3);
     }
     __syncwarp();
     if (p.alias_recv) {
@@ -459,8 +460,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&C.a16_ready));
-    if (lane == 0 && nacc > 2) issue_d1(2);
-    __syncwarp();
     if (p.alias_recv) {
       cluster_arrive();
       cluster_wait();
@@ -553,6 +552,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&C.lora_ready));
+    }
+    if (tpart) {
+      // rs_n = 1 / sqrt(sum over the splits of sum_k x[n, k]^2 / d_i + eps), one token row
+      // per lane, once every split's row sums are in (the local ones: rows_ready)
+      const bool qok = wait_f(smem_u32(&C.rows_ready), 0, abort_flag) && wait_f(smem_u32(&C.q_full), 0, abort_flag);
+      const int n = (cw - 2) * 32 + lane;
+      if (n < M) {
+        float rs = 1.f;
+        if (norm && qok) {
+          float tot = 0.f;
+          for (int s = 0; s < S; ++s) tot += qrecv[s * N + n];
+          rs = rsqrtf(tot * p.inv_d + p.eps);
+        }
+        C.rs[n] = rs;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&C.rs_ready));
     }
     __syncwarp();
     if (p.alias_recv) {
@@ -658,57 +674,48 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
     tc_fence_after();
     const int half = N / 2, n0 = g * half;  // tokens [n0, n0 + half) of D1 for this thread
     const int Mp = p.Mp;
-    float d1[32];
-#pragma unroll
-    for (int cb = 0; cb < 4; ++cb) {
-      if (cb * 8 < half && n0 + cb * 8 < Mp) {
-        uint32_t t8[4][8];
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (q < nacc) tmem_ld8(tmem + lane_addr + colD1 + q * N + n0 + cb * 8, t8[q]);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          float v = __uint_as_float(t8[0][i]) + __uint_as_float(t8[1][i]);
-          if (nacc > 2) v += __uint_as_float(t8[2][i]);
-          if (nacc > 3) v += __uint_as_float(t8[3][i]);
-          d1[cb * 8 + i] = v;
-        }
-      }
-    }
-    if (et == 0) PL_TLF(29);
-    ok = wait_f(smem_u32(&C.rows_ready), 0, abort_flag) && ok;  // orders the reads of 1 / c
+    // rs_ready also orders the reads of 1 / c: its arrivals follow a wait on rows_ready
+    ok = wait_f(smem_u32(&C.rs_ready), 0, abort_flag) && ok;
     const bool good = ok && !*abort_flag;
-    // P[row, n] = s_g D1[row, n] / c_n: this split's share of W_hat u + lambda B A u
-    float* pv = d1;  // in place
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (i < half && n0 + i < Mp) pv[i] = good ? C.cinv[n0 + i] * s_g * d1[i] : 0.f;
-    if (et == 0) PL_TLF(30);
     if (p.alias_recv) {  // the receive buffers lie over the stage region: every CTA is done with it
       cluster_arrive();
       cluster_wait();
     }
     if (et == 0) PL_TLF(10);
     // ---------------------------------------------------------------- epilogue: exchange
+    // P[row, n] = rs_n s_g D1[row, n] / c_n (this split's share of y), 8 tokens at a time,
+    // straight into the shared memory of the CTA that owns the row
     const uint32_t recv_bar = smem_u32(&C.recv);
     {
-      int o = S - 1;
-      while (o > 0 && owner_row0(o, S) > row) --o;
+      const int o = ((row + 1) * S - 1) >> 7;  // the owner: owner_row0(o, S) <= row < owner_row0(o + 1, S)
       const int rl = row - owner_row0(o, S);
       const uint32_t dst = sbase + p.off_rp + static_cast<uint32_t>(((me * p.rows_max + rl) * p.Np + n0) * 4);
       const uint32_t rdst = mapa_shared(dst, static_cast<uint32_t>(o)), rbar = mapa_shared(recv_bar, o);
+#pragma unroll 1
+      for (int i = 0; i < half && n0 + i < Mp; i += 8) {
+        uint32_t a8[8], b8[8];
+        tmem_ld8(tmem + lane_addr + colD1 + n0 + i, a8);
+        tmem_ld8(tmem + lane_addr + colD1 + N + n0 + i, b8);
+        tmem_ld_wait();
+        float v[8];
 #pragma unroll
-      for (int i = 0; i < 32; i += 4) {
-        if (i < half && n0 + i < Mp) {
-          const float4 v = make_float4(pv[i], pv[i + 1], pv[i + 2], pv[i + 3]);
-          if (o == me) *reinterpret_cast<float4*>(smem + (dst - sbase) + 4 * i) = v;
-          else st_async_f32x4(rdst + 4 * i, v, rbar);
+        for (int j = 0; j < 8; ++j) {
+          const int n = n0 + i + j;
+          v[j] = good ? C.rs[n] * C.cinv[n] * s_g * (__uint_as_float(a8[j]) + __uint_as_float(b8[j])) : 0.f;
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (n0 + i + 4 * h < Mp) {
+            const float4 f = make_float4(v[4 * h], v[4 * h + 1], v[4 * h + 2], v[4 * h + 3]);
+            const uint32_t off = static_cast<uint32_t>(4 * (i + 4 * h));
+            if (o == me) *reinterpret_cast<float4*>(smem + (dst - sbase) + off) = f;
+            else st_async_f32x4(rdst + off, f, rbar);
+          }
         }
       }
     }
     if (et == 0) {
-      const uint32_t per_peer = static_cast<uint32_t>(rows_own * Mp * 4 + (norm ? M * 4 : 0));
+      const uint32_t per_peer = static_cast<uint32_t>(rows_own * Mp * 4);
       mbar_arrive_expect_tx(recv_bar, per_peer * static_cast<uint32_t>(S - 1));
       PL_TLF(11);
     }
@@ -717,17 +724,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
     cluster_arrive_relaxed();  // nothing more lands here (released at the exit barrier)
     if (et == 0) PL_TLF(12);
     // ---------------------------------------------------------------- epilogue: combine
-    if (et < M) {
-      float rs = 1.f;
-      if (norm) {
-        float tot = 0.f;
-        for (int s = 0; s < S; ++s) tot += qrecv[s * N + et];
-        rs = rsqrtf(tot * p.inv_d + p.eps);
-      }
-      C.rs[et] = rs;
-    }
-    named_bar(1, kEpiThreads);
-    if (et == 0) PL_TLF(22);
     if (ok) {
       const float* rp = reinterpret_cast<const float*>(smem + p.off_rp);
       const int items = rows_own * (Mp / 4);
@@ -744,7 +740,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
           for (int q = 0; q < 4; ++q) {
             const int n = n4 + q;
             if (n < M) {
-              const float v = C.rs[n] * acc[q];
+              const float v = acc[q];
               if (p.y_f32) static_cast<float*>(p.y)[static_cast<int64_t>(n) * p.d_o + oo] = v;
               else static_cast<__nv_bfloat16*>(p.y)[static_cast<int64_t>(n) * p.d_o + oo] = __float2bfloat16_rn(v);
             }
@@ -984,10 +980,8 @@ cudaError_t launch_linear_fused(const LinearArgs& a, cudaStream_t stream) {
   p.S = f.S;
   p.kc = f.kc;
   p.rows_max = f.rows_max;
-  // tensor memory: nbuf weight buffers of 128 columns, nacc D1 accumulators of N, Dt twice (rb)
+  // tensor memory: nbuf weight buffers of 128 columns, D1 twice (N), Dt twice (rb)
   p.nbuf = 384 + 2 * f.N + 2 * f.rb <= static_cast<int>(kTmemCols) ? 3 : 2;
-  p.nacc = 2;
-  while (p.nacc < 4 && 128 * p.nbuf + (p.nacc + 1) * f.N + 2 * f.rb <= static_cast<int>(kTmemCols)) ++p.nacc;
   p.lambda = a.lambda;
   p.eps = a.eps;
   p.inv_d = 1.0f / static_cast<float>(a.d_i);
