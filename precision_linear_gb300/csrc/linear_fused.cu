@@ -35,11 +35,12 @@
 //                times the block scale: exact in f16), take token rows from the
 //                queue when the buffers are full, then the epilogue;
 //   warp 1       tensor-memory allocation.
-// Epilogue: each CTA's partial P = s_g D1 / c already holds its share of the LoRA
-// path (by linearity the splits' B t_s add up to B t); it sends with st.async into
-// its peers' shared memory the rows of P that each peer owns (peer p owns rows
-// [128 p / S, 128 (p+1) / S)).  Each CTA sums what it owns in split order
-// (deterministic), scales by rs and writes y.
+// Epilogue: each CTA's partial P = rs s_g D1 / c already holds its share of the LoRA
+// path (by linearity the splits' B t_s add up to B t; rs is formed by warps 12-13 from
+// every split's row sums, which arrive during the row conversion); it sends P, eight
+// tokens at a time, with st.async into the shared memory of the peer that owns the
+// row (peer p owns rows [128 p / S, 128 (p+1) / S)).  Each CTA sums what it owns in
+// split order (deterministic) and writes y.
 // The receive buffers have a region of their own when shared memory allows (then no
 // cluster barrier comes between the MMAs and the exchange), else they lie over the
 // stage region, after a cluster barrier.
