@@ -532,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
       bool tok = wait_f(smem_u32(&C.dt_full), 0, abort_flag);
       tc_fence_after();
       const int n = (cw - 2) * 32 + lane;
-      const float lam_sg = p.lambda / *p.s_g;
+      const float lam_sg = __fdividef(p.lambda, *p.s_g);
       uint8_t* tq = smem + p.off_tq + n * 128;
       const uint32_t la = static_cast<uint32_t>((cw - 2) * 32) << 16;
 #pragma unroll
@@ -564,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
         if (norm && qok) {
           float tot = 0.f;
           for (int s = 0; s < S; ++s) tot += qrecv[s * N + n];
-          rs = rsqrtf(tot * p.inv_d + p.eps);
+          asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(rs) : "f"(tot * p.inv_d + p.eps));
         }
         C.rs[n] = rs;
       }
