@@ -19,19 +19,26 @@
 //                         beyond r), beta a power of two that puts both maxima at the same
 //                         magnitude, so that s_g rowscale[m] sum_j Bq[o, j] Tq[m, j] =
 //                         lambda sum_j B[o, j] t[m, j] with t = A h.
-//   k_gemm_nvfp4          the dense contraction, persistent over 128 (weight rows) x TN
-//                         (tokens; 128, 160 or 192, whichever needs the fewest rounds)
-//                         tiles, o-tiles fastest so that concurrent CTAs share their hq
-//                         tiles in L2:
-//     warp 0      TMA: per 64-wide K step the hq tile (192 x 64 f16, 128-byte swizzle) and
-//                 the packed codes (128 x 32 B); every 4th step the E4M3 scales of the next
-//                 256 K (128 x 16 B); one more step per tile with the Tq rows of its
-//                 tokens; per tile the row scales of its tokens;
+//   k_gemm_nvfp4          the dense contraction on CTA pairs (clusters of two, the
+//                         tcgen05 cta_group::2 form), persistent over 256 (weight rows) x
+//                         TN (tokens; 192, or 128 when 192 leaves pairs idle) tiles,
+//                         o-tiles fastest so that concurrent pairs share their hq tiles in
+//                         L2.  Each CTA of a pair owns 128 of the weight rows and half of
+//                         the tokens:
+//     warp 0      TMA: per 64-wide K step this CTA's half of the hq tile (TN/2 x 64 f16,
+//                 128-byte swizzle) and the packed codes of its rows (128 x 32 B); every
+//                 4th step the E4M3 scales of the next 256 K (128 x 16 B); one more step
+//                 per tile with the Tq rows of its tokens; per tile the row scales of
+//                 all TN tokens;
 //     warps 2-9   dequantise each K step into a 32-column tensor-memory slot (E2M1 -> f16
 //                 conversion times the f16 block scale: exact), one weight row and half
-//                 of the step per thread; the LoRA step gets the Bq rows instead;
-//     warp 1      tcgen05.mma kind::f16, M = 128, N = 192, K = 16: D (tensor memory, two
-//                 buffers of 192 columns) += W_hat / s_g x hq^T + Bq x Tq^T;
+//                 of the step per thread; the LoRA step gets the Bq rows instead; the odd
+//                 CTA's warps signal the even CTA's barrier;
+//     warp 1      in the even CTA: tcgen05.mma.cta_group::2 kind::f16, M = 256, N = TN,
+//                 K = 16: D (each CTA's 128 rows in its own tensor memory, two buffers of
+//                 TN columns) += W_hat / s_g x hq^T + Bq x Tq^T, the A rows from both
+//                 CTAs' tensor memory and the B rows from both CTAs' shared memory, so
+//                 each SM stages and reads only half of the token tile;
 //     warps 10-13 epilogue of the previous tile while the next one accumulates:
 //                 y[m, o] = s_g rowscale[m] D[o, m], stored as BF16 or FP32.
 //
@@ -60,18 +67,27 @@ __device__ unsigned long long g_pf_wait[1024][12];
 namespace {
 
 constexpr int kTO = 128;  // weight rows per tile
-constexpr int kTN = 192;  // tokens per tile, at most (the GEMM is instantiated for 128, 160 and 192)
+constexpr int kTN = 192;  // tokens per pair tile, at most (the GEMM is instantiated for 128 and 192)
 constexpr int kKS = 64;   // K per pipeline step (one 128-byte row of f16)
-constexpr int kMaxStages = 7;
-constexpr int kASlots = 4;
+constexpr int kMaxStages = 10;
+constexpr int kMaxASlots = 8;
+// Tensor-memory weight slots (32 columns: one 64-wide K step of 128 rows) beside the two
+// accumulator buffers of TN columns: 4 at TN = 192, 6 at 160, 8 at 128.
+__host__ __device__ constexpr int a_slots_of(int tn) { return (512 - 2 * tn) / 32 < kMaxASlots ? (512 - 2 * tn) / 32 : kMaxASlots; }
 constexpr uint32_t kCodeBytes = kTO * kKS / 2;  // 4 KB
-__host__ __device__ constexpr uint32_t stage_bytes_of(int tn) { return static_cast<uint32_t>(tn) * kKS * 2 + kCodeBytes; }
+// one pipeline stage of a CTA: its half of the tile's tokens (tn / 2 rows of hq) and its codes
+__host__ __device__ constexpr uint32_t stage_bytes_of(int tn) { return static_cast<uint32_t>(tn / 2) * kKS * 2 + kCodeBytes; }
 constexpr uint32_t kScaleBytes = kTO * 16;      // scales of 256 K
+// Scale slots: the group of step 4G is loaded once the stage of step 4G - stages is free, so
+// the dequant warps may still read groups down to (4G - stages + 1) / 4: ceil((stages - 1) / 4)
+// of them besides G.
+constexpr int kScaleSlots = 4;
+static_assert(kMaxStages <= 4 * (kScaleSlots - 1) + 1, "scale slots too few for the stage count");
 constexpr int kDeqWarps = 8;  // two per tensor-memory lane quarter: each dequantises half of a K step
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = (2 + kDeqWarps + kEpiWarps) * 32;  // 448
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColD0 = 128;  // D buffer b at columns [128 + TN b, 128 + TN (b + 1)); weight slots below
+
 constexpr int kMaxR = 32;
 constexpr int kLoraK = 64;  // K columns the LoRA step adds (r <= 32 of them nonzero)
 
@@ -92,7 +108,7 @@ struct GMaps {
 
 struct GCtrl {
   uint64_t full[kMaxStages], empty[kMaxStages];
-  uint64_t afull[kASlots], aempty[kASlots];
+  uint64_t afull[kMaxASlots], aempty[kMaxASlots];
   uint64_t dfull[2], dempty[2];
   uint64_t tfull[2], tempty[2];
   uint64_t mma_done;  // every MMA this CTA issued has completed
@@ -101,18 +117,72 @@ struct GCtrl {
   float s_g;
 };
 
-PL_DEVINL bool wait_p(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __noinline__ bool wait_p_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   return wait_or_abort_status(bar, parity, abort_flag, &g_pf_status);
 }
+// Bounded wait: the common case (already complete) inline, the polling loop out of line.
+PL_DEVINL bool wait_p(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  return mbar_try_wait(bar, parity) || wait_p_slow(bar, parity, abort_flag);
+}
+// Position and phase of a ring of n barriers (no division on the issue paths).
+struct Ring {
+  int i = 0;
+  uint32_t ph = 0;
+  PL_DEVINL void next(int n) {
+    if (++i == n) {
+      i = 0;
+      ph ^= 1u;
+    }
+  }
+};
 PL_DEVINL void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
 
+// ---- CTA-pair (cta_group::2) forms: the even CTA of a cluster of two issues M = 256 MMAs
+// whose A rows 0-127 / 128-255 come from the even / odd CTA's tensor memory, whose B rows
+// [0, N/2) / [N/2, N) come from the even / odd CTA's shared memory (same offsets), and
+// whose D rows 0-127 / 128-255 land in the even / odd CTA's tensor memory.
+PL_DEVINL void tmem_alloc2(uint32_t dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" :: "r"(dst), "r"(ncols) : "memory");
+}
+PL_DEVINL void tmem_relinquish2() { asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory"); }
+PL_DEVINL void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
+}
+PL_DEVINL void mma2_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc, uint32_t accum) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+               :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accum) : "memory");
+}
+// Arrival on the barrier at this offset in both CTAs of the pair once every MMA issued so far
+// has completed.
+PL_DEVINL void tc_commit2(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+               :: "r"(bar), "h"(static_cast<uint16_t>(3)) : "memory");
+}
+PL_DEVINL uint32_t cta_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Arrival on the barrier at this offset in the even CTA (default semantics: the data it
+// orders is tensor memory, ordered by the tcgen05 fences around the arrival and the wait;
+// a cluster-scope release would cost about a microsecond per arrival).
+PL_DEVINL void mbar_arrive_leader(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" :: "r"(mapa_shared(bar, 0)) : "memory");
+}
 // ------------------------------------------------------------------ main contraction
+// A cluster of two CTAs (a pair) per 256 (weight rows) x TN (tokens) tile: each CTA
+// dequantises its own 128 weight rows into its tensor memory and stages its own half of the
+// tile's tokens in shared memory; the even CTA issues the M = 256 MMAs for both.
 template <int TN>
 __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constant__ GMaps maps, const GParams p) {
-  constexpr uint32_t kHBytesT = TN * kKS * 2, kStageBytes = stage_bytes_of(TN);
+  constexpr int kTH = TN / 2;  // token rows of the B operand this CTA stages
+  constexpr int kASlots = a_slots_of(TN);
+  constexpr uint32_t kColD0 = 32u * kASlots;  // D buffer b at columns [kColD0 + TN b, kColD0 + TN (b + 1))
+  constexpr uint32_t kHBytesT = kTH * kKS * 2, kStageBytes = stage_bytes_of(TN);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   GCtrl& C = *reinterpret_cast<GCtrl*>(smem + p.off_ctrl);
@@ -122,6 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
   const int nst = p.stages, n_ks = p.n_ks;
   const bool lora = p.r > 0;
   const int n_steps = n_ks + (lora ? 1 : 0);  // K steps per tile, the LoRA step last
+  const int rank = static_cast<int>(cta_rank());  // 0: issues the MMAs of the pair
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
 #ifdef PL_TIMELINE
@@ -130,15 +202,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
     pdl_launch_dependents();
     for (int s = 0; s < nst; ++s) {
       mbar_init(smem_u32(&C.full[s]), 1);
-      mbar_init(smem_u32(&C.empty[s]), kDeqWarps + 1);
+      mbar_init(smem_u32(&C.empty[s]), kDeqWarps + 1);  // + the pair's MMA commit
     }
     for (int a = 0; a < kASlots; ++a) {
-      mbar_init(smem_u32(&C.afull[a]), kDeqWarps);
+      mbar_init(smem_u32(&C.afull[a]), 2 * kDeqWarps);  // both CTAs' dequant warps (waited on in the even one)
       mbar_init(smem_u32(&C.aempty[a]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&C.dfull[b]), 1);
-      mbar_init(smem_u32(&C.dempty[b]), kEpiWarps);
+      mbar_init(smem_u32(&C.dempty[b]), 2 * kEpiWarps);  // both CTAs' epilogue warps (waited on in the even one)
       mbar_init(smem_u32(&C.tfull[b]), 1);
       mbar_init(smem_u32(&C.tempty[b]), kEpiWarps);
     }
@@ -151,11 +223,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
     tma_prefetch_desc(&maps.hq);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&C.tmem_base), kTmemCols);
-    tmem_relinquish();
+    tmem_alloc2(smem_u32(&C.tmem_base), kTmemCols);
+    tmem_relinquish2();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // both CTAs' barriers and tensor memory exist before either touches the other's
   tc_fence_after();
   const uint32_t tmem = C.tmem_base;
 
@@ -166,11 +239,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
       const uint32_t tbytes = static_cast<uint32_t>(TN) * 4;
       bool ok = true;
       int64_t gs = 0;
+      Ring rs;            // stage ring
+      uint32_t grp = ~0u;  // scale groups loaded so far - 1
       int it = 0, t_issued = 0;
-      for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x, ++it) {
+      for (int tile = pair; tile < p.n_tiles && ok; tile += npairs, ++it) {
         const int mt = tile / p.n_ot, ot = tile % p.n_ot;
-        const int32_t m0 = mt * TN, o0 = ot * kTO;
-        {  // this tile's t32 rows and row scales
+        const int32_t m0 = mt * TN, o0 = ot * 2 * kTO + rank * kTO, mh = m0 + rank * kTH;
+        {  // the row scales of this tile's tokens (all TN: this CTA's accumulator spans them)
           const int tb = it & 1;
           {
             PF_T0();
@@ -184,29 +259,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
           bulk_g2s(dst, p.rowscale + m0, TN * 4, tb_bar);
           ++t_issued;
         }
-        for (int s = 0; s < n_steps && ok; ++s, ++gs) {
-          const int st = static_cast<int>(gs % nst);
+        for (int s = 0; s < n_steps && ok; ++s, ++gs, rs.next(nst)) {
+          const int st = rs.i;
           {
             PF_T0();
-            if (gs >= nst) ok = wait_p(smem_u32(&C.empty[st]), static_cast<uint32_t>((gs / nst) - 1) & 1, abort_flag);
+            if (gs >= nst) ok = wait_p(smem_u32(&C.empty[st]), rs.ph ^ 1u, abort_flag);
             PF_ACC(0);
           }
           if (!ok) break;
           const uint32_t fb = smem_u32(&C.full[st]);
-          if (s == n_ks) {  // the LoRA step: Tq rows of this token tile
+          if (s == n_ks) {  // the LoRA step: Tq rows of this CTA's half of the tokens
             mbar_arrive_expect_tx(fb, kHBytesT);
-            tma_load_2d(sbase + st * kStageBytes, &maps.tq, 0, m0, fb);
+            tma_load_2d(sbase + st * kStageBytes, &maps.tq, 0, mh, fb);
             continue;
           }
           const bool scl = (s & 3) == 0;
           mbar_arrive_expect_tx(fb, kStageBytes + (scl ? kScaleBytes : 0));
           const uint32_t stage = sbase + st * kStageBytes;
-          tma_load_2d(stage, &maps.hq, s * kKS, m0, fb);
+          tma_load_2d(stage, &maps.hq, s * kKS, mh, fb);
           // weights and hq both stay in L2: every weight tile is read once per token tile
           tma_load_2d(stage + kHBytesT, &maps.codes, s * (kKS / 2), o0, fb);
           if (scl) {
-            const int64_t grp = static_cast<int64_t>(it) * (n_ks / 4) + s / 4;
-            tma_load_2d(sbase + p.off_scales + static_cast<uint32_t>(grp & 1) * kScaleBytes, &maps.scales,
+            ++grp;
+            tma_load_2d(sbase + p.off_scales + (grp % kScaleSlots) * kScaleBytes, &maps.scales,
                         s * (kKS / 16), o0, fb);
           }
         }
@@ -219,13 +294,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
       }
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_f16(kTO, TN, 0);
+    // ---------------------------------------------------------------- MMA issuer (even CTA)
+    if (lane == 0 && rank == 0) {
+      const uint32_t idesc = idesc_f16(2 * kTO, TN, 0);
       bool ok = true;
-      int64_t gs = 0;
+      Ring rs, ra;  // stage and slot rings
+      const uint64_t hdesc0 = smem_desc_sw128(sbase, 1024);
       int it = 0;
-      for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x, ++it) {
+      for (int tile = pair; tile < p.n_tiles && ok; tile += npairs, ++it) {
         const int b = it & 1;
         {
           PF_T0();
@@ -235,31 +311,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
         if (!ok) break;
         tc_fence_after();
         const uint32_t d = tmem + (kColD0 + static_cast<uint32_t>(TN) * b);
-        for (int s = 0; s < n_steps && ok; ++s, ++gs) {
-          const int st = static_cast<int>(gs % nst), a = static_cast<int>(gs % kASlots);
+        for (int s = 0; s < n_steps && ok; ++s, rs.next(nst), ra.next(kASlots)) {
+          const int st = rs.i, a = ra.i;
           {
+            // both CTAs' slot a is dequantised; each dequant warp waited for its CTA's stage
+            // st first, so both halves of the token tile have landed too
             PF_T0();
-            ok = wait_p(smem_u32(&C.full[st]), static_cast<uint32_t>(gs / nst) & 1, abort_flag);
-            PF_ACC(3);
-          }
-          {
-            PF_T0();
-            ok = ok && wait_p(smem_u32(&C.afull[a]), static_cast<uint32_t>(gs / kASlots) & 1, abort_flag);
+            ok = wait_p(smem_u32(&C.afull[a]), ra.ph, abort_flag);
             PF_ACC(4);
           }
           if (!ok) break;
           tc_fence_after();
-          const uint64_t hdesc = smem_desc_sw128(sbase + st * kStageBytes, 1024);
+          const uint64_t hdesc = hdesc0 + static_cast<uint64_t>(static_cast<uint32_t>(st) * (kStageBytes >> 4));
           const uint32_t acol = tmem + 32u * a;
 #pragma unroll
           for (int kk = 0; kk < kKS / 16; ++kk)
-            mma_ts(d, acol + 8u * kk, hdesc + 2u * kk, idesc, (s > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(smem_u32(&C.empty[st]));
-          tc_commit(smem_u32(&C.aempty[a]));
+            mma2_ts(d, acol + 8u * kk, hdesc + 2u * kk, idesc, (s > 0 || kk > 0) ? 1u : 0u);
+          tc_commit2(smem_u32(&C.empty[st]));
+          tc_commit2(smem_u32(&C.aempty[a]));
         }
-        tc_commit(smem_u32(&C.dfull[b]));
+        tc_commit2(smem_u32(&C.dfull[b]));
       }
-      tc_commit(smem_u32(&C.mma_done));
+      tc_commit2(smem_u32(&C.mma_done));
       drain(smem_u32(&C.mma_done), 0);  // tensor memory is freed only after the last MMA
     }
   } else if (warp < 2 + kDeqWarps) {
@@ -269,26 +342,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
     if (lora) pdl_wait();  // Bq comes from the preceding kernel
     bool ok = true;
     int64_t gs = 0;
+    Ring rs, ra;         // stage and slot rings
+    uint32_t grp = ~0u;  // scale groups used so far - 1
     int it = 0;
-    for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x, ++it) {
+    for (int tile = pair; tile < p.n_tiles && ok; tile += npairs, ++it) {
       const int ot = tile % p.n_ot;
-      const int64_t o = static_cast<int64_t>(ot) * kTO + row;
+      const int64_t o = static_cast<int64_t>(ot) * 2 * kTO + rank * kTO + row;
       uint4 bq[4] = {};  // this thread's half of its Bq row, for the LoRA step
       if (lora && o < p.d_o) {
         const uint4* src = reinterpret_cast<const uint4*>(p.Bq + o * kLoraK + 32 * g);
 #pragma unroll
         for (int q = 0; q < 4; ++q) bq[q] = src[q];
       }
-      for (int s = 0; s < n_steps && ok; ++s, ++gs) {
-        const int st = static_cast<int>(gs % nst), a = static_cast<int>(gs % kASlots);
+      for (int s = 0; s < n_steps && ok; ++s, ++gs, rs.next(nst), ra.next(kASlots)) {
+        const int st = rs.i, a = ra.i;
         {
           PF_T0();
-          ok = wait_p(smem_u32(&C.full[st]), static_cast<uint32_t>(gs / nst) & 1, abort_flag);
+          ok = wait_p(smem_u32(&C.full[st]), rs.ph, abort_flag);
           if (lane == 0 && warp == 2) PF_ACC(5);
         }
         {
           PF_T0();
-          ok = ok && (gs < kASlots || wait_p(smem_u32(&C.aempty[a]), static_cast<uint32_t>((gs / kASlots) - 1) & 1, abort_flag));
+          ok = ok && (gs < kASlots || wait_p(smem_u32(&C.aempty[a]), ra.ph ^ 1u, abort_flag));
           if (lane == 0 && warp == 2) PF_ACC(6);
         }
         if (!ok) break;
@@ -301,8 +376,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
         } else {
           const uint8_t* stage = smem + st * kStageBytes;
           const uint4 cw = *reinterpret_cast<const uint4*>(stage + kHBytesT + row * 32 + g * 16);  // 32 codes
-          const int64_t grp = static_cast<int64_t>(it) * (n_ks / 4) + s / 4;
-          const uint32_t sw = *reinterpret_cast<const uint16_t*>(smem + p.off_scales + static_cast<uint32_t>(grp & 1) * kScaleBytes +
+          if ((s & 3) == 0) ++grp;
+          const uint32_t sw = *reinterpret_cast<const uint16_t*>(smem + p.off_scales + (grp % kScaleSlots) * kScaleBytes +
                                                                   row * 16 + (s & 3) * 4 + g * 2);
           const uint32_t s01 = cvt_e4m3x2_to_f16x2(sw);
           const uint32_t sa = prmt(s01, s01, 0x1010u), sb = prmt(s01, s01, 0x3232u);
@@ -320,7 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(smem_u32(&C.afull[a]));
+          if (rank == 0) mbar_arrive(smem_u32(&C.afull[a]));
+          else mbar_arrive_leader(smem_u32(&C.afull[a]));
           mbar_arrive(smem_u32(&C.empty[st]));
         }
       }
@@ -333,10 +409,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
     const float s_g = C.s_g;
     bool ok = true;
     int it = 0;
-    for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x, ++it) {
+    for (int tile = pair; tile < p.n_tiles && ok; tile += npairs, ++it) {
       const int mt = tile / p.n_ot, ot = tile % p.n_ot;
       const int b = it & 1;
-      const int64_t o = static_cast<int64_t>(ot) * kTO + row;
+      const int64_t o = static_cast<int64_t>(ot) * 2 * kTO + rank * kTO + row;
       {
         PF_T0();
         ok = wait_p(smem_u32(&C.dfull[b]), (it >> 1) & 1, abort_flag) &&
@@ -366,16 +442,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(smem_u32(&C.dempty[b]));
+        if (rank == 0) mbar_arrive(smem_u32(&C.dempty[b]));
+        else mbar_arrive_leader(smem_u32(&C.dempty[b]));
         mbar_arrive(smem_u32(&C.tempty[b]));
       }
     }
   }
+  // both CTAs are done (the even CTA's last MMA has completed) before either frees its
+  // tensor memory or leaves while the other may still signal it
   tc_fence_before();
   __syncthreads();
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc2(tmem, kTmemCols);
   }
 #ifdef PL_TIMELINE
   if (threadIdx.x == 0 && blockIdx.x < 1024) g_pf_wait[blockIdx.x][11] = globaltimer_ns();
@@ -664,11 +744,11 @@ GPlan gplan(int r, int tn) {
   GPlan g{};
   const uint32_t kStageBytes = stage_bytes_of(tn);
   g.t_slot_bytes = static_cast<uint32_t>(align_up(static_cast<size_t>(tn) * 4, 128));  // row scales of a tile
-  const size_t fixed = 2 * kScaleBytes + 2 * static_cast<size_t>(g.t_slot_bytes) + sizeof(GCtrl) + 128 + 1024;
+  const size_t fixed = kScaleSlots * kScaleBytes + 2 * static_cast<size_t>(g.t_slot_bytes) + sizeof(GCtrl) + 128 + 1024;
   int st = static_cast<int>((227 * 1024 - fixed) / kStageBytes);
   g.stages = st > kMaxStages ? kMaxStages : st;
   g.off_scales = g.stages * kStageBytes;
-  g.off_t = g.off_scales + 2 * kScaleBytes;
+  g.off_t = g.off_scales + kScaleSlots * kScaleBytes;
   g.off_ctrl = static_cast<uint32_t>(align_up(g.off_t + 2 * static_cast<size_t>(g.t_slot_bytes), 128));
   g.smem = g.off_ctrl + sizeof(GCtrl) + 1024;
   return g;
@@ -767,24 +847,22 @@ cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
   }
 
-  // token tile: 192 (the widest MMA the two accumulator buffers allow, and the most
-  // efficient per instruction) unless that leaves SMs idle, then the narrower tile that
-  // fills the most of them
-  const int64_t n_ot64 = (a.d_o + kTO - 1) / kTO;
+  // pair tiles of 256 weight rows x tn tokens; tn = 192 (the widest MMA the two
+  // accumulator buffers allow) unless that leaves pairs idle, then 128
+  const int pairs = sms / 2;
+  const int64_t n_ot64 = (a.d_o + 2 * kTO - 1) / (2 * kTO);
   int tn = kTN;
-  for (int cand : {160, 128}) {
-    if (n_ot64 * ((a.M + tn - 1) / tn) >= sms) break;
-    tn = cand;
-  }
+  if (n_ot64 * ((a.M + tn - 1) / tn) < pairs) tn = 128;
   GMaps gm;
   bool ok = encode_2d(&gm.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.codes, a.d_i / 2, a.d_o, kKS / 2, kTO,
                       CU_TENSOR_MAP_SWIZZLE_NONE) &&
             encode_2d(&gm.scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.scales, a.d_i / 16, a.d_o, 16, kTO,
                       CU_TENSOR_MAP_SWIZZLE_NONE) &&
-            encode_2d(&gm.hq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.hq, a.d_i, a.M, 64, tn,
+            encode_2d(&gm.hq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.hq, a.d_i, a.M, 64, tn / 2,
                       CU_TENSOR_MAP_SWIZZLE_128B);
   if (ok && lora)
-    ok = encode_2d(&gm.tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.Tq, kLoraK, Mp, 64, tn, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = encode_2d(&gm.tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.Tq, kLoraK, Mp, 64, tn / 2,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
   else
     gm.tq = gm.hq;  // unused
   if (!ok) return cudaErrorInvalidValue;
@@ -794,7 +872,7 @@ cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream) {
   p.d_i = a.d_i;
   p.d_o = a.d_o;
   p.r = a.r;
-  p.n_ot = static_cast<int>((a.d_o + kTO - 1) / kTO);
+  p.n_ot = static_cast<int>(n_ot64);
   p.n_tiles = static_cast<int>(p.n_ot * ((a.M + tn - 1) / tn));
   p.n_ks = n_ks;
   p.stages = g.stages;
@@ -807,13 +885,19 @@ cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream) {
   p.off_t = g.off_t;
   p.t_slot_bytes = g.t_slot_bytes;
   p.off_ctrl = g.off_ctrl;
+  cudaLaunchAttribute gattrs[2];
+  gattrs[0] = pdl[0];
+  gattrs[1].id = cudaLaunchAttributeClusterDimension;
+  gattrs[1].val.clusterDim.x = 2;
+  gattrs[1].val.clusterDim.y = 1;
+  gattrs[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t c{};
-  c.gridDim = dim3(static_cast<unsigned>(p.n_tiles < sms ? p.n_tiles : sms));
+  c.gridDim = dim3(static_cast<unsigned>(2 * (p.n_tiles < pairs ? p.n_tiles : pairs)));
   c.blockDim = dim3(kThreads);
   c.dynamicSmemBytes = g.smem;
   c.stream = stream;
-  c.attrs = pdl;
-  c.numAttrs = 1;
+  c.attrs = gattrs;
+  c.numAttrs = 2;
   if (tn == 128) return cudaLaunchKernelEx(&c, k_gemm_nvfp4<128>, gm, p);
   if (tn == 160) return cudaLaunchKernelEx(&c, k_gemm_nvfp4<160>, gm, p);
   return cudaLaunchKernelEx(&c, k_gemm_nvfp4<192>, gm, p);
