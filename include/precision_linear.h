@@ -71,8 +71,8 @@ typedef enum pl_status {
   PL_ERR_CUDA = 6,      /* a CUDA runtime call or kernel launch failed        */
   PL_ERR_WORKSPACE = 7, /* workspace NULL, misaligned or smaller than needed  */
   PL_ERR_TIMEOUT = 8,   /* a bounded device-side wait gave up                 */
-  PL_ERR_RANGE = 9      /* an intermediate of the large-M LoRA step left the f16
-                           range (|lambda t / (s_g rowscale)| x max|B| >= 2^28) */
+  PL_ERR_RANGE = 9      /* reserved: an intermediate left its number format's
+                           range (no current path raises it)                  */
 } pl_status;
 
 /* Static, human-readable name of a status code.  Never NULL. */
@@ -174,8 +174,8 @@ pl_status pl_nvfp4_lora_linear_static_ws(const void* x_bf16, int64_t M, int64_t 
                                          void* y, int y_dtype, pl_stream_t stream);
 
 /* Synchronises `stream`, then returns and clears the device status word: set by
- * bounded device-side waits that gave up (PL_ERR_TIMEOUT) and by a large-M call whose
- * LoRA operands did not fit f16 (PL_ERR_RANGE; its y is then not valid), else PL_OK. */
+ * bounded device-side waits that gave up (PL_ERR_TIMEOUT; that call's y is then not
+ * valid), else PL_OK. */
 pl_status pl_last_device_status(pl_stream_t stream);
 
 /* Test hook: which kernel path pl_nvfp4_lora_linear takes for this shape on the

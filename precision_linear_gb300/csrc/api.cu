@@ -72,7 +72,7 @@ const char* pl_status_string(pl_status s) {
     case PL_ERR_CUDA: return "PL_ERR_CUDA: CUDA launch or runtime call failed";
     case PL_ERR_WORKSPACE: return "PL_ERR_WORKSPACE: workspace missing, misaligned or too small";
     case PL_ERR_TIMEOUT: return "PL_ERR_TIMEOUT: a bounded device-side wait gave up";
-    case PL_ERR_RANGE: return "PL_ERR_RANGE: the large-M LoRA operands left the f16 range";
+    case PL_ERR_RANGE: return "PL_ERR_RANGE: an intermediate left its number format's range";
   }
   return "unknown pl_status";
 }

@@ -6,19 +6,16 @@
 // RMSNorm-AQN of x.  Three kernels, chained by programmatic dependent launch:
 //
 //   k_act (linear_tc.cu)  per token row: hq = f16(h / rowscale) with rowscale a power of
-//                         two (max |hq| in [2^13, 2^14)); A -> f16; split counters and the
-//                         two maxima below := 0.
+//                         two (max |hq| in [2^13, 2^14)); A -> f16; split counters := 0.
 //   k_lora_down           T[m, :] = (lambda / s_g) sum_k A[:, k] hq[m, k]: each CTA one K
 //                         split of 128 tokens (tcgen05.mma, 128 x r, K = 16 steps, from
 //                         TMA-staged hq and f16 A tiles, FP32 accumulator in tensor memory)
 //                         into its partial; the last split of a token tile to finish adds
-//                         the partials up in split order (deterministic).  Also max |T| and
-//                         max |B| over the whole call.
-//   k_lora_pack           the LoRA up-projection as 64 more K columns of the contraction:
-//                         Bq = f16(B 2^beta) [d_o][64] and Tq = f16(T 2^-beta) [M][64] (zero
-//                         beyond r), beta a power of two that puts both maxima at the same
-//                         magnitude, so that s_g rowscale[m] sum_j Bq[o, j] Tq[m, j] =
-//                         lambda sum_j B[o, j] t[m, j] with t = A h.
+//                         the partials up in split order (deterministic) and writes
+//                         Tq = bf16(T) [M][64] (zero beyond r).  The LoRA up-projection is
+//                         then 64 more K columns of the contraction: since t = A h = rowscale
+//                         A hq, s_g rowscale[m] sum_j B[o, j] Tq[m, j] = lambda sum_j B[o, j]
+//                         t[m, j], with B (bf16, as stored) the A operand of that step.
 //   k_gemm_nvfp4          the dense contraction on CTA pairs (clusters of two, the
 //                         tcgen05 cta_group::2 form), persistent over 256 (weight rows) x
 //                         TN (tokens; 192, or 128 when 192 leaves pairs idle) tiles,
@@ -32,11 +29,11 @@
 //                 all TN tokens;
 //     warps 2-9   dequantise each K step into a 32-column tensor-memory slot (E2M1 -> f16
 //                 conversion times the f16 block scale: exact), one weight row and half
-//                 of the step per thread; the LoRA step gets the Bq rows instead; the odd
-//                 CTA's warps signal the even CTA's barrier;
+//                 of the step per thread; the LoRA step gets the B rows (bf16) instead;
+//                 the odd CTA's warps signal the even CTA's barrier;
 //     warp 1      in the even CTA: tcgen05.mma.cta_group::2 kind::f16, M = 256, N = TN,
 //                 K = 16: D (each CTA's 128 rows in its own tensor memory, two buffers of
-//                 TN columns) += W_hat / s_g x hq^T + Bq x Tq^T, the A rows from both
+//                 TN columns) += W_hat / s_g x hq^T (f16) + B x Tq^T (bf16), the A rows from both
 //                 CTAs' tensor memory and the B rows from both CTAs' shared memory, so
 //                 each SM stages and reads only half of the token tile;
 //     warps 10-13 epilogue of the previous tile while the next one accumulates:
@@ -95,7 +92,7 @@ struct GParams {
   int64_t M, d_i, d_o;
   int r, n_ot, n_tiles, n_ks, stages;
   const float* s_g;
-  const __half* Bq;       // [d_o][64]
+  const __nv_bfloat16* B; // [d_o][r], as stored: the A operand of the LoRA step
   const float* rowscale;  // [M_pad]
   void* y;
   int y_f32;
@@ -235,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
-      pdl_wait();  // hq, row scales and t32 come from the preceding kernels
+      pdl_wait();  // hq, row scales and Tq come from the preceding kernels
       const uint32_t tbytes = static_cast<uint32_t>(TN) * 4;
       bool ok = true;
       int64_t gs = 0;
@@ -297,6 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
     // ---------------------------------------------------------------- MMA issuer (even CTA)
     if (lane == 0 && rank == 0) {
       const uint32_t idesc = idesc_f16(2 * kTO, TN, 0);
+      const uint32_t idesc_l = idesc_f16(2 * kTO, TN, 1);  // the LoRA step: bf16 B and T
+      const int l_sub = (p.r + 15) / 16;                      // its K sub-steps of 16
       bool ok = true;
       Ring rs, ra;  // stage and slot rings
       const uint64_t hdesc0 = smem_desc_sw128(sbase, 1024);
@@ -311,7 +310,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
         if (!ok) break;
         tc_fence_after();
         const uint32_t d = tmem + (kColD0 + static_cast<uint32_t>(TN) * b);
-        for (int s = 0; s < n_steps && ok; ++s, rs.next(nst), ra.next(kASlots)) {
+        // main K steps (the first one starts the accumulator), then the LoRA step: kept out
+        // of the loop, whose single issuing thread bounds the kernel
+        for (int s = 0; s < n_ks && ok; ++s) {
           const int st = rs.i, a = ra.i;
           {
             // both CTAs' slot a is dequantised; each dequant warp waited for its CTA's stage
@@ -324,11 +325,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
           tc_fence_after();
           const uint64_t hdesc = hdesc0 + static_cast<uint64_t>(static_cast<uint32_t>(st) * (kStageBytes >> 4));
           const uint32_t acol = tmem + 32u * a;
-#pragma unroll
-          for (int kk = 0; kk < kKS / 16; ++kk)
-            mma2_ts(d, acol + 8u * kk, hdesc + 2u * kk, idesc, (s > 0 || kk > 0) ? 1u : 0u);
+          mma2_ts(d, acol, hdesc, idesc, s > 0 ? 1u : 0u);
+          mma2_ts(d, acol + 8u, hdesc + 2u, idesc, 1u);
+          mma2_ts(d, acol + 16u, hdesc + 4u, idesc, 1u);
+          mma2_ts(d, acol + 24u, hdesc + 6u, idesc, 1u);
           tc_commit2(smem_u32(&C.empty[st]));
           tc_commit2(smem_u32(&C.aempty[a]));
+          rs.next(nst);
+          ra.next(kASlots);
+        }
+        if (lora && ok) {
+          const int st = rs.i, a = ra.i;
+          ok = wait_p(smem_u32(&C.afull[a]), ra.ph, abort_flag);
+          if (ok) {
+            tc_fence_after();
+            const uint64_t hdesc = hdesc0 + static_cast<uint64_t>(static_cast<uint32_t>(st) * (kStageBytes >> 4));
+            const uint32_t acol = tmem + 32u * a;
+            for (int kk = 0; kk < l_sub; ++kk) mma2_ts(d, acol + 8u * kk, hdesc + 2u * kk, idesc_l, 1u);
+            tc_commit2(smem_u32(&C.empty[st]));
+            tc_commit2(smem_u32(&C.aempty[a]));
+            rs.next(nst);
+            ra.next(kASlots);
+          }
         }
         tc_commit2(smem_u32(&C.dfull[b]));
       }
@@ -339,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
     // ---------------------------------------------------------------- dequant
     const int quarter = warp & 3, row = quarter * 32 + lane, g = (warp - 2) >> 2;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    if (lora) pdl_wait();  // Bq comes from the preceding kernel
+
     bool ok = true;
     int64_t gs = 0;
     Ring rs, ra;         // stage and slot rings
@@ -348,11 +366,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
     for (int tile = pair; tile < p.n_tiles && ok; tile += npairs, ++it) {
       const int ot = tile % p.n_ot;
       const int64_t o = static_cast<int64_t>(ot) * 2 * kTO + rank * kTO + row;
-      uint4 bq[4] = {};  // this thread's half of its Bq row, for the LoRA step
-      if (lora && o < p.d_o) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.Bq + o * kLoraK + 32 * g);
+      // this thread's half of the LoRA step's 64 K columns of its row: B[o][32 g .. 32 g + 32),
+      // bf16 as stored, zero beyond r (r <= 32: the g = 1 half is all zero)
+      uint4 bq[4] = {};
+      if (lora && g == 0 && o < p.d_o) {
+        if ((p.r & 7) == 0) {
+          const uint4* src = reinterpret_cast<const uint4*>(p.B + o * p.r);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) bq[q] = src[q];
+          for (int q = 0; q < 4; ++q)
+            if (8 * q < p.r) bq[q] = src[q];
+        } else {
+          const uint16_t* src = reinterpret_cast<const uint16_t*>(p.B + o * p.r);
+          uint32_t w[16];
+#pragma unroll
+          for (int j2 = 0; j2 < 16; ++j2) {
+            const uint32_t lo = 2 * j2 < p.r ? src[2 * j2] : 0u, hi = 2 * j2 + 1 < p.r ? src[2 * j2 + 1] : 0u;
+            w[j2] = lo | (hi << 16);
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) bq[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        }
       }
       for (int s = 0; s < n_steps && ok; ++s, ++gs, rs.next(nst), ra.next(kASlots)) {
         const int st = rs.i, a = ra.i;
@@ -468,14 +501,13 @@ constexpr int kLdThreads = 6 * 32;  // TMA, MMA, 4 epilogue warps
 constexpr uint32_t kLdH = 128 * kKS * 2;  // 16 KB
 
 struct LParams {
-  int64_t M, d_i, Mp, n_b;
+  int64_t M, d_i, Mp;
   int r, R4, rb, n_ks, splits;
   float lambda;
   const float* s_g;
-  const __nv_bfloat16* B;  // [d_o][r]: n_b elements, for max |B|
   float* t_part;           // [splits][Mp][R4]
-  float* t32;              // [Mp][R4]: T = (lambda / s_g) A hq
-  int* counters;           // [token tiles], then max |T| and max |B| (FP32 bits); zero on entry
+  __nv_bfloat16* Tq;       // [Mp][64]: bf16(T), T = (lambda / s_g) A hq, zero beyond r
+  int* counters;           // [token tiles]; zero on entry
   int mtiles;
 };
 struct LMaps {
@@ -556,19 +588,9 @@ __global__ void __launch_bounds__(kLdThreads, 1) k_lora_down(const __grid_consta
     }
   } else {
     const int quarter = warp & 3;
-    const int et = threadIdx.x - 64;  // 0 .. 127
     const int64_t m = static_cast<int64_t>(m0) + quarter * 32 + lane;  // < Mp
     const bool ok = wait_p(smem_u32(&C.dfull), 0, abort_flag) && !*abort_flag && s1 > s0;
     tc_fence_after();
-    unsigned int* maxima = reinterpret_cast<unsigned int*>(p.counters + p.mtiles);  // [0] max |T|, [1] max |B|
-    {  // max |B| over this CTA's share of B (after the wait: the maxima were zeroed by the prologue)
-      float mb = 0.f;
-      for (int64_t i = static_cast<int64_t>(blockIdx.x) * 128 + et; i < p.n_b; i += static_cast<int64_t>(gridDim.x) * 128)
-        mb = fmaxf(mb, fabsf(__bfloat162float(p.B[i])));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, o));
-      if (lane == 0) atomicMax(&maxima[1], __float_as_uint(mb));
-    }
     float* part = p.t_part + (static_cast<int64_t>(sp) * p.Mp + m) * p.R4;
     uint32_t v[16];
     for (int jb = 0; jb < p.rb; jb += 16) {
@@ -601,19 +623,20 @@ __global__ void __launch_bounds__(kLdThreads, 1) k_lora_down(const __grid_consta
           acc[4 * j4 + 3] += v[j4].w;
         }
       }
-      float4* dst = reinterpret_cast<float4*>(p.t32 + m * p.R4);
-      float mt = 0.f;
+      // the LoRA step's B operand row: 64 bf16, T in the first r, zero beyond
+      uint4* dst = reinterpret_cast<uint4*>(p.Tq + m * kLoraK);
 #pragma unroll
-      for (int j4 = 0; j4 < kMaxR / 4; ++j4) {
-        if (4 * j4 < p.R4) {
-          const float4 t = make_float4(f * acc[4 * j4], f * acc[4 * j4 + 1], f * acc[4 * j4 + 2], f * acc[4 * j4 + 3]);
-          dst[j4] = t;
-          mt = fmaxf(mt, fmaxf(fmaxf(fabsf(t.x), fabsf(t.y)), fmaxf(fabsf(t.z), fabsf(t.w))));
+      for (int q = 0; q < kLoraK / 8; ++q) {
+        uint32_t w[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const int j = 8 * q + 2 * h;
+          const float lo = j < p.r && j < kMaxR ? f * acc[j < kMaxR ? j : 0] : 0.f;
+          const float hi = j + 1 < p.r && j + 1 < kMaxR ? f * acc[j + 1 < kMaxR ? j + 1 : 0] : 0.f;
+          w[h] = f32x2_to_bf16x2(lo, hi);
         }
+        dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, o));
-      if (lane == 0) atomicMax(&maxima[0], __float_as_uint(mt));
     }
   }
   tc_fence_before();
@@ -624,43 +647,6 @@ __global__ void __launch_bounds__(kLdThreads, 1) k_lora_down(const __grid_consta
   }
 }
 
-// ------------------------------------------------------------------ LoRA operands of the contraction
-// beta from the two maxima: Bq max ~ max|B| 2^beta and Tq max ~ max|T| 2^-beta meet at
-// 2^((e_T + e_B) / 2); past the f16 range the call reports a range error.
-__global__ void __launch_bounds__(256) k_lora_pack(const float* __restrict__ t32, int64_t Mp, int R4,
-                                                   const __nv_bfloat16* __restrict__ B, int64_t d_o, int r,
-                                                   const unsigned int* __restrict__ maxima, __half* __restrict__ Tq,
-                                                   __half* __restrict__ Bq) {
-  pdl_launch_dependents();
-  pdl_wait();  // T and the maxima come from the down-projection
-  const float tmax = __uint_as_float(maxima[0]), bmax = __uint_as_float(maxima[1]);
-  int beta = 0;
-  if (tmax > 0.f && bmax > 0.f) {
-    const int et = static_cast<int>((__float_as_uint(tmax) >> 23) & 0xFFu) - 127;
-    const int eb = static_cast<int>((__float_as_uint(bmax) >> 23) & 0xFFu) - 127;
-    const int d = et - eb;
-    beta = d >= 0 ? d / 2 : -((1 - d) / 2);  // floor(d / 2)
-    if (((et + eb) >> 1) >= 14 && blockIdx.x == 0 && threadIdx.x == 0) atomicOr(&g_pf_status, kStatusRange);
-  }
-  const float up = ldexpf(1.0f, beta), down = ldexpf(1.0f, -beta);
-  // 8 consecutive f16 (16 bytes) per thread and step: rows of 64 are 8 such pieces
-  const int64_t nt = Mp * (kLoraK / 8), nb = d_o * (kLoraK / 8);
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nt + nb;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const bool tpart = i < nt;
-    const int64_t k = tpart ? i : i - nt, row = k >> 3;
-    const int j0 = static_cast<int>(k & 7) * 8;
-    float v[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int j = j0 + q;
-      v[q] = j >= r ? 0.f : (tpart ? t32[row * R4 + j] * down : __bfloat162float(B[row * r + j]) * up);
-    }
-    const uint4 h = make_uint4(f32x2_to_f16x2(v[0], v[1]), f32x2_to_f16x2(v[2], v[3]), f32x2_to_f16x2(v[4], v[5]),
-                               f32x2_to_f16x2(v[6], v[7]));
-    reinterpret_cast<uint4*>(tpart ? Tq : Bq)[k] = h;
-  }
-}
 
 // ------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -701,11 +687,9 @@ struct PfWs {
   __half* hq;
   float* rowscale;
   __half* A16;
-  float* t32;
   float* t_part;
-  int* counters;  // [token tiles of the down-projection], max |T|, max |B|
-  __half* Tq;     // [Mp][64]
-  __half* Bq;     // [d_o][64]
+  int* counters;          // [token tiles of the down-projection]
+  __nv_bfloat16* Tq;      // [Mp][64]: bf16(T), zero beyond r
   size_t bytes;
 };
 
@@ -720,16 +704,12 @@ PfWs carve(void* ws, int64_t M, int64_t d_i, int64_t d_o, int r) {
   off += align_up(static_cast<size_t>(Mp) * 4, 256);
   w.A16 = reinterpret_cast<__half*>(b + off);
   off += align_up(static_cast<size_t>(r) * d_i * 2, 256);
-  w.t32 = reinterpret_cast<float*>(b + off);
-  off += align_up(static_cast<size_t>(Mp) * r4(r) * 4, 256);
   w.t_part = reinterpret_cast<float*>(b + off);
   off += align_up(static_cast<size_t>(kMaxLdSplits) * Mp * r4(r) * 4, 256);
   w.counters = reinterpret_cast<int*>(b + off);
   off += align_up(static_cast<size_t>((M + 127) / 128 + 6) * 4, 256);
-  w.Tq = reinterpret_cast<__half*>(b + off);
+  w.Tq = reinterpret_cast<__nv_bfloat16*>(b + off);
   off += align_up(static_cast<size_t>(Mp) * kLoraK * 2, 256);
-  w.Bq = reinterpret_cast<__half*>(b + off);
-  off += align_up(static_cast<size_t>(d_o) * kLoraK * 2, 256);
   w.bytes = off;
   return w;
 }
@@ -789,7 +769,7 @@ cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream) {
   const bool lora = a.r > 0;
   const int mtiles = static_cast<int>((a.M + 127) / 128);  // token tiles of the LoRA down-projection
   e = launch_act_prologue(a, w.hq, w.rowscale, w.A16, lora ? reinterpret_cast<float*>(w.counters) : nullptr,
-                          lora ? (mtiles + 2 + 3) / 4 * 4 : 0, stream);
+                          lora ? (mtiles + 3) / 4 * 4 : 0, stream);
   if (e != cudaSuccess) return e;
 
   cudaLaunchAttribute pdl[1];
@@ -818,12 +798,10 @@ cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream) {
     splits = splits > kMaxLdSplits ? kMaxLdSplits : splits;
     splits = splits > n_ks ? n_ks : (splits < 1 ? 1 : splits);  // every split has at least one K step
     lp.splits = splits;
-    lp.n_b = a.d_o * a.r;
     lp.lambda = a.lambda;
     lp.s_g = a.s_g;
-    lp.B = static_cast<const __nv_bfloat16*>(a.B);
     lp.t_part = w.t_part;
-    lp.t32 = w.t32;
+    lp.Tq = w.Tq;
     lp.counters = w.counters;
     lp.mtiles = mtiles;
     cudaLaunchConfig_t c{};
@@ -835,15 +813,6 @@ cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream) {
     c.numAttrs = 1;
     e = cudaLaunchKernelEx(&c, k_lora_down, lm, lp);
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t c2{};
-    c2.gridDim = dim3(static_cast<unsigned>(2 * sms));
-    c2.blockDim = dim3(256);
-    c2.stream = stream;
-    c2.attrs = pdl;
-    c2.numAttrs = 1;
-    e = cudaLaunchKernelEx(&c2, k_lora_pack, static_cast<const float*>(w.t32), Mp, R4,
-                           static_cast<const __nv_bfloat16*>(a.B), a.d_o, a.r,
-                           reinterpret_cast<const unsigned int*>(w.counters + mtiles), w.Tq, w.Bq);
     if (e != cudaSuccess) return e;
   }
 
@@ -861,7 +830,7 @@ cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream) {
             encode_2d(&gm.hq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.hq, a.d_i, a.M, 64, tn / 2,
                       CU_TENSOR_MAP_SWIZZLE_128B);
   if (ok && lora)
-    ok = encode_2d(&gm.tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.Tq, kLoraK, Mp, 64, tn / 2,
+    ok = encode_2d(&gm.tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w.Tq, kLoraK, Mp, 64, tn / 2,
                    CU_TENSOR_MAP_SWIZZLE_128B);
   else
     gm.tq = gm.hq;  // unused
@@ -877,7 +846,7 @@ cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream) {
   p.n_ks = n_ks;
   p.stages = g.stages;
   p.s_g = a.s_g;
-  p.Bq = w.Bq;
+  p.B = static_cast<const __nv_bfloat16*>(a.B);
   p.rowscale = w.rowscale;
   p.y = a.y;
   p.y_f32 = a.y_f32 ? 1 : 0;
