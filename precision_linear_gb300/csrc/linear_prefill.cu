@@ -794,7 +794,7 @@ cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream) {
     lp.R4 = R4;
     lp.rb = rb;
     lp.n_ks = n_ks;
-    int splits = (sms + mtiles - 1) / mtiles;
+    int splits = sms / mtiles;  // one wave: every split of every token tile resident at once
     splits = splits > kMaxLdSplits ? kMaxLdSplits : splits;
     splits = splits > n_ks ? n_ks : (splits < 1 ? 1 : splits);  // every split has at least one K step
     lp.splits = splits;

@@ -7,7 +7,7 @@
 //
 // Two kernels per call, chained by programmatic dependent launch:
 //
-// k_act (one CTA per token row): h = x / rms (.) (w_norm + z) in FP32, a power-of-two
+// k_act (a group of warps per token row): h = x / rms (.) (w_norm + z) in FP32, a power-of-two
 //   c_m with max|h| / c_m in [2^13, 2^14), and the f16 activations h / c_m (11-bit
 //   significand, no overflow) into the workspace; a few more CTAs copy the LoRA matrix
 //   A into the workspace as f16.
@@ -125,32 +125,32 @@ __global__ void k_wait_timeout_probe(uint64_t limit_ns) {
 
 // ------------------------------------------------------------------ activation prologue
 constexpr int kActThreads = 256;
-constexpr int kActUnroll = 2;  // 16-byte slots per thread in flight (a 3584 row is 448 slots)
+constexpr int kActWarps = kActThreads / 32;  // token rows in flight per CTA
 
 // CTAs 0 .. M-1: one token row m each.  hz = x (.) (w + z) is kept in shared memory
 // (FP32) while sum(x^2) and max |hz| are reduced; then hq = f16(hz * inv / c_m).
 // CTAs M and up: the f16 copy of A (r x d_i), 8 elements per thread and slot, and
 // zeros into `zero` (n_zero floats, a multiple of 4; the accumulator of the large-M
 // LoRA down-projection), 4 per thread and slot.
-__global__ void __launch_bounds__(kActThreads, 4) k_act(const __nv_bfloat16* __restrict__ x, int64_t M, int64_t d_i,
+__global__ void __launch_bounds__(kActThreads, 2) k_act(const __nv_bfloat16* __restrict__ x, int64_t M, int64_t d_i,
                                                      const float* __restrict__ w_norm,
                                                      const float* __restrict__ z, float eps,
                                                      __half* __restrict__ hq, float* __restrict__ rowscale,
                                                      const __nv_bfloat16* __restrict__ A, int r,
                                                      __half* __restrict__ A16, float* __restrict__ zero,
-                                                     int64_t n_zero) {
-  extern __shared__ float4 hz4[];  // [d_i / 4]
-  __shared__ float red_s[kActThreads / 32], red_m[kActThreads / 32];
+                                                     int64_t n_zero, int n_row_ctas, int wpr) {
+  extern __shared__ float4 g4[];  // [d_i / 4]: w_norm + z of the whole row (1 without the norm)
+  __shared__ float red_s[kActWarps], red_m[kActWarps];
   if (threadIdx.x == 0) {
     PL_TLP(0);
     pdl_launch_dependents();
   }
   pdl_wait();  // x may come from the preceding kernel, which may also still read the workspace
   if (threadIdx.x == 0) PL_TLP(1);
-  if (static_cast<int64_t>(blockIdx.x) >= M) {
+  if (static_cast<int>(blockIdx.x) >= n_row_ctas) {
     const int64_t nslot = static_cast<int64_t>(r) * d_i / 8;
-    const int64_t stride = static_cast<int64_t>(gridDim.x - M) * kActThreads;
-    for (int64_t sl = (blockIdx.x - M) * kActThreads + threadIdx.x; sl < nslot; sl += stride) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x - n_row_ctas) * kActThreads;
+    for (int64_t sl = (blockIdx.x - n_row_ctas) * kActThreads + threadIdx.x; sl < nslot; sl += stride) {
       const uint4 v = reinterpret_cast<const uint4*>(A)[sl];
       reinterpret_cast<uint4*>(A16)[sl] =
           make_uint4(f32x2_to_f16x2(bf16lo_to_f32(v.x), bf16hi_to_f32(v.x)),
@@ -158,92 +158,85 @@ __global__ void __launch_bounds__(kActThreads, 4) k_act(const __nv_bfloat16* __r
                      f32x2_to_f16x2(bf16lo_to_f32(v.z), bf16hi_to_f32(v.z)),
                      f32x2_to_f16x2(bf16lo_to_f32(v.w), bf16hi_to_f32(v.w)));
     }
-    for (int64_t sl = (blockIdx.x - M) * kActThreads + threadIdx.x; sl < n_zero / 4; sl += stride)
+    for (int64_t sl = (blockIdx.x - n_row_ctas) * kActThreads + threadIdx.x; sl < n_zero / 4; sl += stride)
       reinterpret_cast<float4*>(zero)[sl] = make_float4(0.f, 0.f, 0.f, 0.f);
     return;
   }
-  const int64_t m = blockIdx.x;
-  const int64_t nv8 = d_i / 8;
   const bool norm = w_norm != nullptr, noise = norm && z != nullptr;
-  const uint4* xr = reinterpret_cast<const uint4*>(x + m * d_i);
-  float ss = 0.f, mx = 0.f;
-  for (int64_t base = threadIdx.x; base < nv8; base += kActThreads * kActUnroll) {
-    uint4 xv[kActUnroll];
-    float4 wv[kActUnroll][2], zv[kActUnroll][2];
-#pragma unroll
-    for (int u = 0; u < kActUnroll; ++u) {
-      const int64_t sl = base + u * kActThreads;
-      if (sl < nv8) {
-        xv[u] = xr[sl];
-        if (norm) {
-          wv[u][0] = reinterpret_cast<const float4*>(w_norm)[2 * sl];
-          wv[u][1] = reinterpret_cast<const float4*>(w_norm)[2 * sl + 1];
-        }
-        if (noise) {
-          zv[u][0] = reinterpret_cast<const float4*>(z)[2 * sl];
-          zv[u][1] = reinterpret_cast<const float4*>(z)[2 * sl + 1];
-        }
-      }
+  for (int64_t i = threadIdx.x; i < d_i / 4; i += kActThreads) {
+    float4 g = make_float4(1.f, 1.f, 1.f, 1.f);
+    if (norm) g = reinterpret_cast<const float4*>(w_norm)[i];
+    if (noise) {
+      const float4 zz = reinterpret_cast<const float4*>(z)[i];
+      g.x += zz.x; g.y += zz.y; g.z += zz.z; g.w += zz.w;
     }
-#pragma unroll
-    for (int u = 0; u < kActUnroll; ++u) {
-      const int64_t sl = base + u * kActThreads;
-      if (sl < nv8) {
-        float sc[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
-        if (norm) {
-          sc[0] = wv[u][0].x; sc[1] = wv[u][0].y; sc[2] = wv[u][0].z; sc[3] = wv[u][0].w;
-          sc[4] = wv[u][1].x; sc[5] = wv[u][1].y; sc[6] = wv[u][1].z; sc[7] = wv[u][1].w;
-        }
-        if (noise) {
-          sc[0] += zv[u][0].x; sc[1] += zv[u][0].y; sc[2] += zv[u][0].z; sc[3] += zv[u][0].w;
-          sc[4] += zv[u][1].x; sc[5] += zv[u][1].y; sc[6] += zv[u][1].z; sc[7] += zv[u][1].w;
-        }
-        const uint32_t w4[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
-        float h[8];
+    g4[i] = g;
+  }
+  __syncthreads();
+  // a group of wpr warps per token row (wpr = 1 for rows up to 16 KB): thread t of the group
+  // takes the 16-byte pieces t, t + 32 wpr, ... of x; two passes (row statistics, then the
+  // scaled f16 row: the second pass reads x from L2)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rows_cta = kActWarps / wpr, grp = warp / wpr, gt = (warp % wpr) * 32 + lane, gstride = 32 * wpr;
+  const int64_t nv8 = d_i / 8;
+  const int64_t per_round = static_cast<int64_t>(n_row_ctas) * rows_cta;
+  const int64_t rounds = (M + per_round - 1) / per_round;
+  for (int64_t rd = 0; rd < rounds; ++rd) {
+    const int64_t m = rd * per_round + static_cast<int64_t>(blockIdx.x) * rows_cta + grp;
+    const bool live = m < M;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (live ? m : 0) * d_i);
+    float ss = 0.f, mx = 0.f;
+    if (live) {
+#pragma unroll 4
+      for (int64_t q = gt; q < nv8; q += gstride) {
+        const uint4 v = xr[q];
+        const float4 ga = g4[2 * q], gb = g4[2 * q + 1];
+        const float g8[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const float a0 = bf16lo_to_f32(w4[j]), a1 = bf16hi_to_f32(w4[j]);
-          ss = fmaf(a0, a0, ss);
-          ss = fmaf(a1, a1, ss);
-          h[2 * j] = a0 * sc[2 * j];
-          h[2 * j + 1] = a1 * sc[2 * j + 1];
+          ss = fmaf(a0, a0, fmaf(a1, a1, ss));
+          mx = fmaxf(mx, fmaxf(fabsf(a0 * g8[2 * j]), fabsf(a1 * g8[2 * j + 1])));
         }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx = fmaxf(mx, fabsf(h[i]));
-        hz4[2 * sl] = make_float4(h[0], h[1], h[2], h[3]);
-        hz4[2 * sl + 1] = make_float4(h[4], h[5], h[6], h[7]);
       }
     }
-  }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
-    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-  }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) {
-    red_s[warp] = ss;
-    red_m[warp] = mx;
-  }
-  __syncthreads();
-  float tot = 0.f, hm = 0.f;
-#pragma unroll
-  for (int w = 0; w < kActThreads / 32; ++w) {
-    tot += red_s[w];
-    hm = fmaxf(hm, red_m[w]);
-  }
-  if (threadIdx.x == 0) PL_TLP(2);
-  const float inv = norm ? 1.0f / sqrtf(tot / static_cast<float>(d_i) + eps) : 1.0f;
-  const float hmax = inv * hm;
-  int e = hmax > 0.f ? ilogbf(hmax) - 13 : 0;  // max |h| / c_m in [2^13, 2^14)
-  e = e < -100 ? -100 : (e > 100 ? 100 : e);
-  const float f = inv * ldexpf(1.0f, -e);
-  if (threadIdx.x == 0) rowscale[m] = ldexpf(1.0f, e);
-  uint4* hr = reinterpret_cast<uint4*>(hq + m * d_i);
-  for (int64_t sl = threadIdx.x; sl < nv8; sl += kActThreads) {
-    const float4 a = hz4[2 * sl], b = hz4[2 * sl + 1];
-    hr[sl] = make_uint4(f32x2_to_f16x2(a.x * f, a.y * f), f32x2_to_f16x2(a.z * f, a.w * f),
-                        f32x2_to_f16x2(b.x * f, b.y * f), f32x2_to_f16x2(b.z * f, b.w * f));
+    for (int o = 16; o > 0; o >>= 1) {
+      ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    }
+    if (wpr > 1) {  // the group's warps add up through shared memory
+      if (lane == 0) {
+        red_s[warp] = ss;
+        red_m[warp] = mx;
+      }
+      __syncthreads();
+      ss = 0.f;
+      mx = 0.f;
+      for (int w = grp * wpr; w < (grp + 1) * wpr; ++w) {
+        ss += red_s[w];
+        mx = fmaxf(mx, red_m[w]);
+      }
+      __syncthreads();
+    }
+    if (!live) continue;
+    const float inv = norm ? 1.0f / sqrtf(ss / static_cast<float>(d_i) + eps) : 1.0f;
+    const float hmax = inv * mx;
+    int e = hmax > 0.f ? ilogbf(hmax) - 13 : 0;  // max |h| / c_m in [2^13, 2^14)
+    e = e < -100 ? -100 : (e > 100 ? 100 : e);
+    const float f = inv * ldexpf(1.0f, -e);
+    if (gt == 0) rowscale[m] = ldexpf(1.0f, e);
+    uint4* hr = reinterpret_cast<uint4*>(hq + m * d_i);
+#pragma unroll 4
+    for (int64_t q = gt; q < nv8; q += gstride) {
+      const uint4 v = xr[q];
+      const float4 ga = g4[2 * q], gb = g4[2 * q + 1];
+      hr[q] = make_uint4(f32x2_to_f16x2(bf16lo_to_f32(v.x) * ga.x * f, bf16hi_to_f32(v.x) * ga.y * f),
+                         f32x2_to_f16x2(bf16lo_to_f32(v.y) * ga.z * f, bf16hi_to_f32(v.y) * ga.w * f),
+                         f32x2_to_f16x2(bf16lo_to_f32(v.z) * gb.x * f, bf16hi_to_f32(v.z) * gb.y * f),
+                         f32x2_to_f16x2(bf16lo_to_f32(v.w) * gb.z * f, bf16hi_to_f32(v.w) * gb.w * f));
+    }
   }
   if (threadIdx.x == 0) PL_TLP(5);
 }
@@ -803,20 +796,7 @@ cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   attrs[1].val.clusterDim.y = 1;
   attrs[1].val.clusterDim.z = 1;
 
-  // extra prologue CTAs copy A to f16 (about 2048 elements per thread and CTA at most 32)
-  const int64_t a_slots = static_cast<int64_t>(a.r) * a.d_i / 8;
-  int nconv = static_cast<int>((a_slots + kActThreads * 4 - 1) / (kActThreads * 4));
-  nconv = a.r > 0 ? (nconv < 1 ? 1 : (nconv > 32 ? 32 : nconv)) : 0;
-  cudaLaunchConfig_t c1{};
-  c1.gridDim = dim3(static_cast<unsigned>(a.M + nconv));
-  c1.blockDim = dim3(kActThreads);
-  c1.dynamicSmemBytes = pl.act_smem;
-  c1.stream = stream;
-  c1.attrs = attrs;
-  c1.numAttrs = 1;
-  e = cudaLaunchKernelEx(&c1, k_act, static_cast<const __nv_bfloat16*>(a.x), a.M, a.d_i, a.w_norm, a.z, a.eps,
-                         w.hq, w.rowscale, static_cast<const __nv_bfloat16*>(a.A), a.r, w.A16,
-                         static_cast<float*>(nullptr), static_cast<int64_t>(0));
+  e = launch_act_prologue(a, w.hq, w.rowscale, w.A16, nullptr, 0, stream);
   if (e != cudaSuccess) return e;
 
   TcParams p{};
@@ -858,15 +838,24 @@ cudaError_t launch_act_prologue(const LinearArgs& a, __half* hq, float* rowscale
   const int64_t a_slots = static_cast<int64_t>(a.r) * a.d_i / 8 + n_zero / 4;
   int nconv = static_cast<int>((a_slots + kActThreads * 4 - 1) / (kActThreads * 4));
   nconv = a_slots > 0 ? (nconv < 1 ? 1 : (nconv > 64 ? 64 : nconv)) : 0;
+  // row CTAs, at most two per SM (each holds w_norm + z): a group of wpr warps per row,
+  // wpr the power of two that gives each thread at most 16 pieces of 16 bytes
+  const int64_t nv8 = a.d_i / 8;
+  int wpr = 1;
+  while (wpr < kActWarps && nv8 > 16 * 32 * wpr) wpr *= 2;
+  const int rows_cta = kActWarps / wpr;
+  const int64_t want = (a.M + rows_cta - 1) / rows_cta;
+  const int n_row_ctas = static_cast<int>(want < 2 * sm_count() ? want : 2 * sm_count());
   cudaLaunchConfig_t c{};
-  c.gridDim = dim3(static_cast<unsigned>(a.M + nconv));
+  c.gridDim = dim3(static_cast<unsigned>(n_row_ctas + nconv));
   c.blockDim = dim3(kActThreads);
   c.dynamicSmemBytes = static_cast<size_t>(a.d_i) * 4;
   c.stream = stream;
   c.attrs = attr;
   c.numAttrs = 1;
   return cudaLaunchKernelEx(&c, k_act, static_cast<const __nv_bfloat16*>(a.x), a.M, a.d_i, a.w_norm, a.z, a.eps, hq,
-                            rowscale, static_cast<const __nv_bfloat16*>(a.A), a.r, A16, zero, n_zero);
+                            rowscale, static_cast<const __nv_bfloat16*>(a.A), a.r, A16, zero, n_zero, n_row_ctas,
+                            wpr);
 }
 
 cudaError_t launch_wait_timeout_probe(cudaStream_t stream) {
