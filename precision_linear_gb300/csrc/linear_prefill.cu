@@ -496,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
 }
 
 // ------------------------------------------------------------------ LoRA down-projection
-constexpr int kLdStages = 4;
+constexpr int kLdStages = 8;
 constexpr int kLdThreads = 6 * 32;  // TMA, MMA, 4 epilogue warps
 constexpr uint32_t kLdH = 128 * kKS * 2;  // 16 KB
 
