@@ -213,5 +213,6 @@ def last_device_status(device=None) -> int:
 
 def linear_path(M: int, d_i: int, d_o: int, r: int) -> int:
     """Kernel path the linear takes for this shape on the current device: 2 fused
-    tcgen05 kernel, 1 tcgen05 prologue + main kernel, 0 CUDA-core kernels, -1 invalid."""
+    tcgen05 kernel, 1 tcgen05 prologue + main kernel, 3 large-M CTA-pair contraction,
+    0 CUDA-core kernels, -1 invalid."""
     return int(lib().pl_debug_linear_path(M, d_i, d_o, r))

@@ -64,6 +64,16 @@ def test_ragged_shapes(cuda_ok, d_o, d_i, M):
     _check(d_o, d_i, M, 8, seed=d_o * 7 + M)
 
 
+# Large-M shapes of the CTA-pair contraction: an odd rank (B rows read element-wise), d_o
+# not a multiple of the 256-row pair tile, M not a multiple of the token tile, several tiles
+# per pair (persistent rounds), and the narrow-tile choice when tiles are fewer than pairs.
+@pytest.mark.parametrize("d_o,d_i,M,r", [(1000, 1024, 700, 5), (4000, 2048, 1500, 32), (2304, 512, 4096, 16),
+                                         (520, 768, 3000, 1)])
+def test_large_m_shapes(cuda_ok, d_o, d_i, M, r):
+    assert pl.linear_path(M, d_i, d_o, r) == 3
+    _check(d_o, d_i, M, r, seed=d_o + M + r)
+
+
 @pytest.mark.parametrize("M", [8, 32, 64])
 def test_7b_layer_set(cuda_ok, M):
     wl = synthetic.WORKLOADS["layer_7b"]
