@@ -750,7 +750,7 @@ cudaError_t set_attributes() {
 }  // namespace
 
 bool prefill_supported(int64_t M, int64_t d_i, int64_t d_o, int r) {
-  return M > 64 && d_i >= 256 && d_i % 256 == 0 && d_i <= 49152 && d_o >= 1 && r >= 0 && r <= kMaxR &&
+  return M > 64 && d_i >= 256 && d_i % 256 == 0 && d_i <= 32768 && d_o >= 1 && r >= 0 && r <= kMaxR &&
          gplan(r, kTN).stages >= 3;
 }
 

@@ -126,6 +126,7 @@ __global__ void k_wait_timeout_probe(uint64_t limit_ns) {
 // ------------------------------------------------------------------ activation prologue
 constexpr int kActThreads = 256;
 constexpr int kActWarps = kActThreads / 32;  // token rows in flight per CTA
+constexpr int kActPieces = 16;               // 16-byte pieces of x per thread, held in registers
 
 // CTAs 0 .. M-1: one token row m each.  hz = x (.) (w + z) is kept in shared memory
 // (FP32) while sum(x^2) and max |hz| are reduced; then hq = f16(hz * inv / c_m).
@@ -173,9 +174,9 @@ __global__ void __launch_bounds__(kActThreads, 2) k_act(const __nv_bfloat16* __r
     g4[i] = g;
   }
   __syncthreads();
-  // a group of wpr warps per token row (wpr = 1 for rows up to 16 KB): thread t of the group
-  // takes the 16-byte pieces t, t + 32 wpr, ... of x; two passes (row statistics, then the
-  // scaled f16 row: the second pass reads x from L2)
+  // a group of wpr warps per token row (wpr = 1 for rows up to 8 KB): thread t of the group
+  // holds the 16-byte pieces t, t + 32 wpr, ... of x in registers (at most kActPieces: the
+  // host picks wpr so), for the row statistics and then the scaled f16 row
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rows_cta = kActWarps / wpr, grp = warp / wpr, gt = (warp % wpr) * 32 + lane, gstride = 32 * wpr;
   const int64_t nv8 = d_i / 8;
@@ -185,14 +186,20 @@ __global__ void __launch_bounds__(kActThreads, 2) k_act(const __nv_bfloat16* __r
     const int64_t m = rd * per_round + static_cast<int64_t>(blockIdx.x) * rows_cta + grp;
     const bool live = m < M;
     const uint4* xr = reinterpret_cast<const uint4*>(x + (live ? m : 0) * d_i);
+    uint4 xv[kActPieces];
+#pragma unroll
+    for (int i = 0; i < kActPieces; ++i) {
+      const int64_t q = gt + static_cast<int64_t>(i) * gstride;
+      xv[i] = live && q < nv8 ? xr[q] : make_uint4(0u, 0u, 0u, 0u);  // every load of the row in flight
+    }
     float ss = 0.f, mx = 0.f;
-    if (live) {
-#pragma unroll 4
-      for (int64_t q = gt; q < nv8; q += gstride) {
-        const uint4 v = xr[q];
+#pragma unroll
+    for (int i = 0; i < kActPieces; ++i) {
+      const int64_t q = gt + static_cast<int64_t>(i) * gstride;
+      if (q < nv8) {
         const float4 ga = g4[2 * q], gb = g4[2 * q + 1];
         const float g8[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+        const uint32_t w4[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const float a0 = bf16lo_to_f32(w4[j]), a1 = bf16hi_to_f32(w4[j]);
@@ -228,14 +235,17 @@ __global__ void __launch_bounds__(kActThreads, 2) k_act(const __nv_bfloat16* __r
     const float f = inv * ldexpf(1.0f, -e);
     if (gt == 0) rowscale[m] = ldexpf(1.0f, e);
     uint4* hr = reinterpret_cast<uint4*>(hq + m * d_i);
-#pragma unroll 4
-    for (int64_t q = gt; q < nv8; q += gstride) {
-      const uint4 v = xr[q];
-      const float4 ga = g4[2 * q], gb = g4[2 * q + 1];
-      hr[q] = make_uint4(f32x2_to_f16x2(bf16lo_to_f32(v.x) * ga.x * f, bf16hi_to_f32(v.x) * ga.y * f),
-                         f32x2_to_f16x2(bf16lo_to_f32(v.y) * ga.z * f, bf16hi_to_f32(v.y) * ga.w * f),
-                         f32x2_to_f16x2(bf16lo_to_f32(v.z) * gb.x * f, bf16hi_to_f32(v.z) * gb.y * f),
-                         f32x2_to_f16x2(bf16lo_to_f32(v.w) * gb.z * f, bf16hi_to_f32(v.w) * gb.w * f));
+#pragma unroll
+    for (int i = 0; i < kActPieces; ++i) {
+      const int64_t q = gt + static_cast<int64_t>(i) * gstride;
+      if (q < nv8) {
+        const uint4 v = xv[i];
+        const float4 ga = g4[2 * q], gb = g4[2 * q + 1];
+        hr[q] = make_uint4(f32x2_to_f16x2(bf16lo_to_f32(v.x) * ga.x * f, bf16hi_to_f32(v.x) * ga.y * f),
+                           f32x2_to_f16x2(bf16lo_to_f32(v.y) * ga.z * f, bf16hi_to_f32(v.y) * ga.w * f),
+                           f32x2_to_f16x2(bf16lo_to_f32(v.z) * gb.x * f, bf16hi_to_f32(v.z) * gb.y * f),
+                           f32x2_to_f16x2(bf16lo_to_f32(v.w) * gb.z * f, bf16hi_to_f32(v.w) * gb.w * f));
+      }
     }
   }
   if (threadIdx.x == 0) PL_TLP(5);
@@ -763,8 +773,8 @@ TcWs carve(void* ws, int64_t M, int64_t d_i, int r) {
 }  // namespace
 
 bool tc_supported(int64_t M, int64_t d_i, int64_t, int r) {
-  // k_act keeps one FP32 row in shared memory (<= 192 KB)
-  return M >= 1 && M <= kMaxN && d_i >= kChunkK && d_i % kChunkK == 0 && d_i <= 49152 && r >= 0 && r <= kMaxR;
+  // k_act holds a token row of at most 32768 elements in the registers of one CTA
+  return M >= 1 && M <= kMaxN && d_i >= kChunkK && d_i % kChunkK == 0 && d_i <= 32768 && r >= 0 && r <= kMaxR;
 }
 
 size_t tc_workspace_bytes(int64_t M, int64_t d_i, int64_t, int r) { return carve(nullptr, M, d_i, r).bytes; }
@@ -839,10 +849,11 @@ cudaError_t launch_act_prologue(const LinearArgs& a, __half* hq, float* rowscale
   int nconv = static_cast<int>((a_slots + kActThreads * 4 - 1) / (kActThreads * 4));
   nconv = a_slots > 0 ? (nconv < 1 ? 1 : (nconv > 64 ? 64 : nconv)) : 0;
   // row CTAs, at most two per SM (each holds w_norm + z): a group of wpr warps per row,
-  // wpr the power of two that gives each thread at most 16 pieces of 16 bytes
+  // wpr the power of two that gives each thread at most kActPieces pieces of 16 bytes
   const int64_t nv8 = a.d_i / 8;
   int wpr = 1;
-  while (wpr < kActWarps && nv8 > 16 * 32 * wpr) wpr *= 2;
+  while (wpr < kActWarps && nv8 > kActPieces * 32 * wpr) wpr *= 2;
+  if (nv8 > static_cast<int64_t>(kActPieces) * 32 * wpr) return cudaErrorInvalidValue;  // d_i > 32768
   const int rows_cta = kActWarps / wpr;
   const int64_t want = (a.M + rows_cta - 1) / rows_cta;
   const int n_row_ctas = static_cast<int>(want < 2 * sm_count() ? want : 2 * sm_count());
