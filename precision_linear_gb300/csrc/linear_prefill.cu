@@ -18,7 +18,8 @@
 //                         t[m, j], with B (bf16, as stored) the A operand of that step.
 //   k_gemm_nvfp4          the dense contraction on CTA pairs (clusters of two, the
 //                         tcgen05 cta_group::2 form), persistent over 256 (weight rows) x
-//                         TN (tokens; 192, or 128 when 192 leaves pairs idle) tiles,
+//                         TN (tokens; 192 or 160 by the rounds they need, 128 when 192 leaves
+//                         pairs idle) tiles,
 //                         o-tiles fastest so that concurrent pairs share their hq tiles in
 //                         L2.  Each CTA of a pair owns 128 of the weight rows and half of
 //                         the tokens:
@@ -69,7 +70,7 @@ constexpr int kKS = 64;   // K per pipeline step (one 128-byte row of f16)
 constexpr int kMaxStages = 10;
 constexpr int kMaxASlots = 8;
 // Tensor-memory weight slots (32 columns: one 64-wide K step of 128 rows) beside the two
-// accumulator buffers of TN columns: 4 at TN = 192, 8 at 128.
+// accumulator buffers of TN columns: 4 at TN = 192, 6 at 160, 8 at 128.
 __host__ __device__ constexpr int a_slots_of(int tn) { return (512 - 2 * tn) / 32 < kMaxASlots ? (512 - 2 * tn) / 32 : kMaxASlots; }
 constexpr uint32_t kCodeBytes = kTO * kKS / 2;  // 4 KB
 // one pipeline stage of a CTA: its half of the tile's tokens (tn / 2 rows of hq) and its codes
@@ -675,10 +676,10 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void*
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Rows of the per-token arrays (row scales, Tq): a multiple of every token tile (128 or
-// 192 for the GEMM, 128 for the down-projection), so that whole tiles can be read and
+// Rows of the per-token arrays (row scales, Tq): a multiple of every token tile (128, 160
+// or 192 for the GEMM, 128 for the down-projection), so that whole tiles can be read and
 // written.
-int64_t m_pad(int64_t M) { return (M + 383) / 384 * 384; }
+int64_t m_pad(int64_t M) { return (M + 1919) / 1920 * 1920; }
 int r4(int r) { return r > 0 ? (r + 3) / 4 * 4 : 0; }
 
 constexpr int kMaxLdSplits = 8;
@@ -739,6 +740,8 @@ cudaError_t set_attributes() {
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
     err = cudaFuncSetAttribute(k_gemm_nvfp4<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(k_gemm_nvfp4<160>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (err == cudaSuccess)
       err = cudaFuncSetAttribute(k_gemm_nvfp4<192>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (err == cudaSuccess)
@@ -814,12 +817,15 @@ cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
   }
 
-  // pair tiles of 256 weight rows x tn tokens; tn = 192 (the widest MMA the two
-  // accumulator buffers allow) unless that leaves pairs idle, then 128
+  // pair tiles of 256 weight rows x tn tokens: 128 when 192 leaves pairs idle; else 192 (the
+  // widest MMA the two accumulator buffers allow) or 160, whichever needs fewer rounds of
+  // the pairs, a round of 160-token tiles costing 0.966 of one of 192 (measured)
   const int pairs = sms / 2;
   const int64_t n_ot64 = (a.d_o + 2 * kTO - 1) / (2 * kTO);
+  auto rounds = [&](int t) { return (n_ot64 * ((a.M + t - 1) / t) + pairs - 1) / pairs; };
   int tn = kTN;
   if (n_ot64 * ((a.M + tn - 1) / tn) < pairs) tn = 128;
+  else if (0.966 * static_cast<double>(rounds(160)) < static_cast<double>(rounds(192))) tn = 160;
   GMaps gm;
   bool ok = encode_2d(&gm.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.codes, a.d_i / 2, a.d_o, kKS / 2, kTO,
                       CU_TENSOR_MAP_SWIZZLE_NONE) &&
@@ -866,6 +872,7 @@ cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream) {
   c.attrs = gattrs;
   c.numAttrs = 2;
   if (tn == 128) return cudaLaunchKernelEx(&c, k_gemm_nvfp4<128>, gm, p);
+  if (tn == 160) return cudaLaunchKernelEx(&c, k_gemm_nvfp4<160>, gm, p);
   return cudaLaunchKernelEx(&c, k_gemm_nvfp4<192>, gm, p);
 }
 
