@@ -182,13 +182,23 @@ def run_ours(args, world, rank, local):
     W_dev = base["W"].to(dev)
     codes0, scales0, sg0 = pl.nvfp4_quantize(W_dev)
     torch.cuda.synchronize()
+    # each step's inputs and results sit in one device buffer apiece (views per call), so the
+    # end-to-end leg moves a step's inputs and results with one copy each way
+    x_off = [sum(Ms[:j]) for j in range(len(Ms))]
+    x_bufs, y_bufs = [], []
     for i in range(n_sets):
+        xb = torch.empty(sum(Ms), d_i, dtype=torch.bfloat16, device=dev)
+        yb = torch.empty(sum(Ms), d_o, dtype=torch.bfloat16, device=dev)
+        x_bufs.append(xb)
+        y_bufs.append(yb)
         calls = []
-        for M in Ms:
+        for j, M in enumerate(Ms):
+            xv = xb[x_off[j]:x_off[j] + M]
+            xv.copy_(base["x"][:M])
             calls.append(dict(M=M, codes=codes0.clone(), scales=scales0.clone(), s_g=sg0.clone(),
-                              x=base["x"][:M].contiguous().to(dev), A=base["A"].to(dev), B=base["B"].to(dev),
+                              x=xv, A=base["A"].to(dev), B=base["B"].to(dev),
                               w_norm=base["w_norm"].to(dev), z=base["z"].to(dev),
-                              y=torch.empty(M, d_o, dtype=torch.bfloat16, device=dev)))
+                              y=yb[x_off[j]:x_off[j] + M]))
         sets.append(calls)
     ws = pl.Workspace(dev)
     ws.get(max(pl.workspace_bytes(M, d_i, d_o, r) for M in Ms))
@@ -285,30 +295,30 @@ def run_ours(args, world, rank, local):
     # ---- end to end through the public API with host buffers
     e2e = None
     if rank == 0 or world > 1:
-        hx = [torch.empty(M, d_i, dtype=torch.bfloat16).pin_memory() for M in Ms]
-        hy = [torch.empty(M, d_o, dtype=torch.bfloat16).pin_memory() for M in Ms]
-        for h, M in zip(hx, Ms):
-            h.copy_(base["x"][:M])
+        hx = torch.empty(sum(Ms), d_i, dtype=torch.bfloat16).pin_memory()  # a step's inputs, packed
+        hy = torch.empty(sum(Ms), d_o, dtype=torch.bfloat16).pin_memory()  # a step's results, packed
+        for j, M in enumerate(Ms):
+            hx[x_off[j]:x_off[j] + M].copy_(base["x"][:M])
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         bi = sum(2 * M * d_i for M in Ms)
         bo = sum(2 * M * d_o for M in Ms)
 
-        def e2e_step(calls):
-            for j, c in enumerate(calls):
-                c["x"].copy_(hx[j], non_blocking=True)  # H2D of this call's input
+        def e2e_step(k):
+            x_bufs[k].copy_(hx, non_blocking=True)  # H2D of the step's inputs
+            for c in sets[k]:
                 one_call(c)
-                hy[j].copy_(c["y"], non_blocking=True)  # D2H of its result
+            hy.copy_(y_bufs[k], non_blocking=True)  # D2H of the step's results
 
         with torch.cuda.stream(stream):
             eg = torch.cuda.CUDAGraph()
             with torch.cuda.graph(eg, stream=stream):
-                for calls in sets:
-                    e2e_step(calls)
+                for k in range(len(sets)):
+                    e2e_step(k)
             e1g = []
-            for calls in sets:
+            for k in range(len(sets)):
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, stream=stream):
-                    e2e_step(calls)
+                    e2e_step(k)
                 e1g.append(g)
             for _ in range(max(1, args.warmup // n_round)):
                 eg.replay()
