@@ -334,6 +334,10 @@ def run_ours(args, world, rank, local):
         e2e = {"value": round(step_bytes * args.steps * world / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": round(ms_e2e / args.steps, 4)}
 
+    layer_dec = None
+    if not args.no_layer:
+        layer_dec = bench_layer_decode(dev, stream)
+
     prefill = None
     if not args.no_prefill:
         prefill = bench_prefill(dev, stream)
@@ -367,10 +371,73 @@ def run_ours(args, world, rank, local):
                          "frac": round(achieved / hbm_peak, 4), "peak_kind": peak_kind,
                          "traffic": profile_traffic("k_fused_decode" if paths[int(dom)] == 2 else "k_tc_decode",
                                                     f"{args.workload}/M{dom}")},
-            "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, "prefill": prefill,
+            "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, "layer_decode": layer_dec, "prefill": prefill,
             "gpu_launches": sum(launches_per_call.values()) * args.steps,
         }
         print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------- 7B layer decode
+def bench_layer_decode(dev, stream, replays: int = 20):
+    """The Qwen2.5-7B-shaped decoder-layer projection set at decode batch sizes: the seven
+    projections of one layer back to back (q/k/v on norm 1, gate/up on norm 2, o and down
+    plain), two weight copies of the layer alternating (262 MB > L2), CUDA graphs; per M
+    the layer's time and HBM GB/s of its algorithmic bytes."""
+    import torch
+
+    from precision_linear_gb300 import binding as pl
+    from precision_linear_gb300 import synthetic
+
+    wl = synthetic.WORKLOADS["layer_7b"]
+    r = wl.r
+    Mmax = max(wl.Ms)
+    ws = pl.Workspace(dev)
+    ws.get(max(pl.workspace_bytes(M, p.d_i, p.d_o, r) for M in wl.Ms for p in wl.projs))
+    projs = []
+    for i, p in enumerate(wl.projs):
+        c = synthetic.projection_case(p.d_o, p.d_i, Mmax, r, wl.sigma, synthetic.proj_seed(wl, 0, i), 0.0,
+                                      device="cpu")
+        W = c["W"].to(dev)
+        codes, scales, s_g = pl.nvfp4_quantize(W)
+        del W
+        norm = p.norm is not None
+        projs.append(dict(p=p, norm=norm, copies=[(codes, scales, s_g), (codes.clone(), scales.clone(), s_g.clone())],
+                          x=c["x"].to(dev), A=c["A"].to(dev), B=c["B"].to(dev),
+                          w_norm=c["w_norm"].to(dev) if norm else None, z=c["z"].to(dev) if norm else None))
+    torch.cuda.synchronize()
+    out = {}
+    with torch.cuda.stream(stream):
+        for M in wl.Ms:
+            ys = [torch.empty(M, q["p"].d_o, dtype=torch.bfloat16, device=dev) for q in projs]
+
+            def layer(k):
+                for q, y in zip(projs, ys):
+                    codes, scales, s_g = q["copies"][k]
+                    pl.nvfp4_lora_linear(q["x"][:M], codes, scales, s_g, q["A"], q["B"], wl.lam, q["w_norm"], q["z"],
+                                         synthetic.EPS, out=y, workspace=ws)
+
+            layer(0)
+            layer(1)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                layer(0)
+                layer(1)
+            g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(replays):
+                g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / (2 * replays)
+            nbytes = sum(algorithmic_bytes(M, q["p"].d_i, q["p"].d_o, r) for q in projs)
+            out[str(M)] = {"us_per_layer": round(us, 1), "GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
+                           "paths": {q["p"].name: pl.linear_path(M, q["p"].d_i, q["p"].d_o, r) for q in projs}}
+    torch.cuda.synchronize()
+    return {"workload": "layer_7b (Qwen2.5-7B decoder-layer projection set, r=32)", "per_M": out,
+            "timing": f"CUDA events around {replays} replays of a CUDA graph of two layers (two weight copies)"}
 
 
 # ------------------------------------------------------------------------- large-M path
@@ -510,6 +577,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the M=4096 layer-set measurement")
+    ap.add_argument("--no-layer", action="store_true", help="skip the 7B decoder-layer decode measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
