@@ -22,12 +22,14 @@
 //     8 codes per 32-bit word into 4 f16x2 words with the hardware E2M1 conversion,
 //     multiplies by the block scale (q * s_b is exact in f16) and stores them into
 //     tensor memory, where they are the MMA's A operand;
-//   * warp 1 issues tcgen05.mma kind::f16 (K = 16 each): weights (tensor memory) x
+//   * four warps issue tcgen05.mma kind::f16 (K = 16 each; one thread issues one only
+//     every few tens of ns, so the work is shared): weights (tensor memory) x
 //     activations^T into accumulator D1, and A (shared memory, 128-row operand whose
 //     rows >= r are don't-care) x activations^T into accumulator Dt, whose lanes < r are
-//     this CTA's K slice of t = A h;
-//   * epilogue (warps 2..9): every CTA puts s_g c_m D1 and its Dt slice in shared
-//     memory; after a cluster barrier CTA s sums, over DSMEM and in split order
+//     this CTA's K slice of t = A h -- each of D1 and Dt as two partial sums over the two
+//     halves of every chunk's K steps;
+//   * epilogue (warps 2..9): every CTA adds the partial sums and puts s_g c_m D1 and its
+//     Dt slice in shared memory; after a cluster barrier CTA s sums, over DSMEM and in split order
 //     (deterministic), the t slices of all S CTAs into t, and the D1 partials of its
 //     share of the 128 rows; it adds the LoRA up-projection lambda B t on CUDA cores
 //     and writes y.
@@ -49,12 +51,15 @@ __device__ uint32_t g_tc_status = 0;
 #ifdef PL_TIMELINE
 __device__ unsigned long long g_tl_main[1024][16];
 __device__ unsigned long long g_tl_pro[256][8];
+__device__ unsigned long long g_tl_chunk[1024][4][32];  // per chunk: W issued, MMA ready, A ready, dequant start
+#define PL_TLC(kind, c) do { if (blockIdx.x < 1024 && (c) < 32) g_tl_chunk[blockIdx.x][kind][c] = globaltimer_ns(); } while (0)
 #define PL_TL(slot) do { if (blockIdx.x < 1024) g_tl_main[blockIdx.x][slot] = globaltimer_ns(); } while (0)
 #define PL_TLP(slot) do { const unsigned b_ = blockIdx.x + gridDim.x * blockIdx.y; \
                           if (b_ < 256) g_tl_pro[b_][slot] = globaltimer_ns(); } while (0)
 #else
 #define PL_TL(slot) do { } while (0)
 #define PL_TLP(slot) do { } while (0)
+#define PL_TLC(kind, c) do { } while (0)
 #endif
 
 namespace {
@@ -64,22 +69,27 @@ constexpr int kChunkK = 256;
 constexpr int kCodesBytes = kTileO * kChunkK / 2;   // 16 KB
 constexpr int kScaleBytes = kTileO * kChunkK / 16;  // 2 KB
 constexpr int kDeqWarps = 8;
-constexpr int kThreads = 10 * 32;  // producer, MMA, 8 dequant/epilogue warps
+constexpr int kIssuers = 4;        // MMA-issuing warps: D1 and Dt, each in two K halves
+constexpr int kThreads = (2 + kDeqWarps + kIssuers - 1) * 32;  // producer, issuer 0, dequant/epilogue, issuers 1..3
 constexpr int kEpiThreads = kDeqWarps * 32;
 constexpr int kMaxStages = 8;
 constexpr int kMaxSplit = 8;
+constexpr int kMaxLa = 3;  // slots of the shared-memory ring of A chunks
 constexpr int kMaxN = 64;
 constexpr int kMaxR = 64;
 constexpr uint32_t kTmemCols = 512;
-// tensor-memory columns: A buffers [0,128) and [128,256), D1 [256,256+N), Dt [320,320+N)
+// tensor-memory columns: kAbuf weight (MMA A operand) buffers of 128 columns from 0, then
+// the accumulators of the four issuers, N <= 64 columns each: D1 over the first and the
+// second half of every chunk's K steps, and Dt likewise
+constexpr int kAbuf = 2;
 constexpr uint32_t kColA0 = 0;
-constexpr uint32_t kColD1 = 256;
-constexpr uint32_t kColDt = 320;
+constexpr uint32_t kColAcc = 256;  // issuer q accumulates at kColAcc + 64 q
+static_assert(kAbuf * 128 <= kColAcc && kColAcc + kIssuers * kMaxN <= kTmemCols, "TMEM columns");
 constexpr int kTStride = kMaxR + 4;  // floats per token row of the t buffers (16-byte rows, spread banks)
 
 struct TcParams {
   int64_t M, d_i, d_o;
-  int N, r, rb, tiles, splits, kc, stages;
+  int N, r, rb, tiles, splits, kc, stages, la;
   uint32_t stage_bytes;
   float lambda;
   const float* s_g;
@@ -95,8 +105,8 @@ struct TcMaps {
 
 struct Smem {
   uint64_t wfull[kMaxStages], hfull[kMaxStages], empty[kMaxStages];
-  uint64_t a_full[2], a_empty[2];
-  uint64_t lfull[2], lempty[2];  // shared-memory ring of A chunks
+  uint64_t a_full[kAbuf], a_empty[kAbuf];
+  uint64_t lfull[kMaxLa], lempty[kMaxLa];  // shared-memory ring of A chunks
   uint64_t d_full;
   uint32_t tmem_base;
   int abort_flag;
@@ -127,6 +137,7 @@ __global__ void k_wait_timeout_probe(uint64_t limit_ns) {
 constexpr int kActThreads = 256;
 constexpr int kActWarps = kActThreads / 32;  // token rows in flight per CTA
 constexpr int kActPieces = 16;               // 16-byte pieces of x per thread, held in registers
+constexpr int kActUnroll = 4;                // loads per thread in flight in the copy loops
 
 // CTAs 0 .. M-1: one token row m each.  hz = x (.) (w + z) is kept in shared memory
 // (FP32) while sum(x^2) and max |hz| are reduced; then hq = f16(hz * inv / c_m).
@@ -151,27 +162,48 @@ __global__ void __launch_bounds__(kActThreads, 2) k_act(const __nv_bfloat16* __r
   if (static_cast<int>(blockIdx.x) >= n_row_ctas) {
     const int64_t nslot = static_cast<int64_t>(r) * d_i / 8;
     const int64_t stride = static_cast<int64_t>(gridDim.x - n_row_ctas) * kActThreads;
-    for (int64_t sl = (blockIdx.x - n_row_ctas) * kActThreads + threadIdx.x; sl < nslot; sl += stride) {
-      const uint4 v = reinterpret_cast<const uint4*>(A)[sl];
-      reinterpret_cast<uint4*>(A16)[sl] =
-          make_uint4(f32x2_to_f16x2(bf16lo_to_f32(v.x), bf16hi_to_f32(v.x)),
-                     f32x2_to_f16x2(bf16lo_to_f32(v.y), bf16hi_to_f32(v.y)),
-                     f32x2_to_f16x2(bf16lo_to_f32(v.z), bf16hi_to_f32(v.z)),
-                     f32x2_to_f16x2(bf16lo_to_f32(v.w), bf16hi_to_f32(v.w)));
+    // kActUnroll slots per thread and round, every load of the round in flight before the stores
+    for (int64_t s0 = (blockIdx.x - n_row_ctas) * kActThreads + threadIdx.x; s0 < nslot; s0 += kActUnroll * stride) {
+      uint4 v[kActUnroll];
+#pragma unroll
+      for (int u = 0; u < kActUnroll; ++u) {
+        const int64_t sl = s0 + u * stride;
+        if (sl < nslot) v[u] = reinterpret_cast<const uint4*>(A)[sl];
+      }
+#pragma unroll
+      for (int u = 0; u < kActUnroll; ++u) {
+        const int64_t sl = s0 + u * stride;
+        if (sl < nslot)
+          reinterpret_cast<uint4*>(A16)[sl] =
+              make_uint4(f32x2_to_f16x2(bf16lo_to_f32(v[u].x), bf16hi_to_f32(v[u].x)),
+                         f32x2_to_f16x2(bf16lo_to_f32(v[u].y), bf16hi_to_f32(v[u].y)),
+                         f32x2_to_f16x2(bf16lo_to_f32(v[u].z), bf16hi_to_f32(v[u].z)),
+                         f32x2_to_f16x2(bf16lo_to_f32(v[u].w), bf16hi_to_f32(v[u].w)));
+      }
     }
     for (int64_t sl = (blockIdx.x - n_row_ctas) * kActThreads + threadIdx.x; sl < n_zero / 4; sl += stride)
       reinterpret_cast<float4*>(zero)[sl] = make_float4(0.f, 0.f, 0.f, 0.f);
     return;
   }
   const bool norm = w_norm != nullptr, noise = norm && z != nullptr;
-  for (int64_t i = threadIdx.x; i < d_i / 4; i += kActThreads) {
-    float4 g = make_float4(1.f, 1.f, 1.f, 1.f);
-    if (norm) g = reinterpret_cast<const float4*>(w_norm)[i];
-    if (noise) {
-      const float4 zz = reinterpret_cast<const float4*>(z)[i];
-      g.x += zz.x; g.y += zz.y; g.z += zz.z; g.w += zz.w;
+  const int64_t n4 = d_i / 4;
+  for (int64_t i0 = threadIdx.x; i0 < n4; i0 += kActUnroll * kActThreads) {
+    float4 g[kActUnroll], zz[kActUnroll];
+#pragma unroll
+    for (int u = 0; u < kActUnroll; ++u) {  // every load of the round in flight
+      const int64_t i = i0 + u * kActThreads;
+      g[u] = make_float4(1.f, 1.f, 1.f, 1.f);
+      zz[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < n4) {
+        if (norm) g[u] = reinterpret_cast<const float4*>(w_norm)[i];
+        if (noise) zz[u] = reinterpret_cast<const float4*>(z)[i];
+      }
     }
-    g4[i] = g;
+#pragma unroll
+    for (int u = 0; u < kActUnroll; ++u) {
+      const int64_t i = i0 + u * kActThreads;
+      if (i < n4) g4[i] = make_float4(g[u].x + zz[u].x, g[u].y + zz[u].y, g[u].z + zz[u].z, g[u].w + zz[u].w);
+    }
   }
   __syncthreads();
   // a group of wpr warps per token row (wpr = 1 for rows up to 8 KB): thread t of the group
@@ -256,11 +288,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
                                                            const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int N = p.N, stages = p.stages;
+  const int N = p.N, stages = p.stages, la = p.la;
   const uint32_t h_bytes = static_cast<uint32_t>(N) * 512u;
   const uint32_t l_bytes = static_cast<uint32_t>(p.rb) * 512u;  // one A chunk (rb rows x 256 bf16)
-  uint8_t* lring = smem + static_cast<size_t>(stages) * p.stage_bytes;          // 2 A chunks
-  __nv_bfloat16* sBt = reinterpret_cast<__nv_bfloat16*>(lring + 2 * l_bytes);  // [kMaxR][128]: B^T of the tile
+  uint8_t* lring = smem + static_cast<size_t>(stages) * p.stage_bytes;           // la A chunks
+  __nv_bfloat16* sBt = reinterpret_cast<__nv_bfloat16*>(lring + la * l_bytes);  // [kMaxR][128]: B^T of the tile
   Smem& S = *reinterpret_cast<Smem*>(reinterpret_cast<uint8_t*>(sBt) + kTileO * kMaxR * 2);
   volatile int* abort_flag = &S.abort_flag;
 
@@ -270,6 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
   const int c1 = static_cast<int>((static_cast<int64_t>(split + 1) * p.kc) / p.splits);
   const int nch = c1 - c0;
   const bool lora = p.r > 0;
+  const int n_iss = lora ? kIssuers : 2;  // the Dt issuers idle without an adapter
   bool go = false;  // epilogue threads: this CTA's accumulators are valid
 
   const uint64_t pol_w = policy_evict_first();  // weights are streamed once
@@ -281,15 +314,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
     for (int s = 0; s < stages; ++s) {
       mbar_init(smem_u32(&S.wfull[s]), 1);
       mbar_init(smem_u32(&S.hfull[s]), 1);
-      mbar_init(smem_u32(&S.empty[s]), kDeqWarps + 1);
+      mbar_init(smem_u32(&S.empty[s]), kDeqWarps + n_iss);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kAbuf; ++b) {
       mbar_init(smem_u32(&S.a_full[b]), kDeqWarps);
-      mbar_init(smem_u32(&S.a_empty[b]), 1);
-      mbar_init(smem_u32(&S.lfull[b]), 1);
-      mbar_init(smem_u32(&S.lempty[b]), 1);
+      mbar_init(smem_u32(&S.a_empty[b]), 2);
     }
-    mbar_init(smem_u32(&S.d_full), 1);
+    for (int b = 0; b < la; ++b) {
+      mbar_init(smem_u32(&S.lfull[b]), 1);
+      mbar_init(smem_u32(&S.lempty[b]), 2);
+    }
+    mbar_init(smem_u32(&S.d_full), n_iss);
     S.abort_flag = 0;
     fence_mbar_init();
     // the first stages of weights do not depend on the prologue: issue them at once
@@ -298,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
       const uint32_t wb = smem_u32(&S.wfull[c]);
       mbar_arrive_expect_tx(wb, kCodesBytes + kScaleBytes);
       const int kc = c0 + c;
+      PL_TLC(0, c);
       tma_load_2d_hint(smem_u32(st), &maps.codes, kc * (kChunkK / 2), row0, wb, pol_w);
       tma_load_2d_hint(smem_u32(st + kCodesBytes + h_bytes), &maps.scales, kc * (kChunkK / 16), row0, wb, pol_w);
     }
@@ -317,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
-      const int lpre = lora ? (nch < 2 ? nch : 2) : 0;
+      const int lpre = lora ? (nch < la ? nch : la) : 0;
       PL_TL(2);
       pdl_wait();  // activations and the f16 copy of A come from the prologue
       PL_TL(3);
@@ -338,10 +374,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
       int c = pre, lc = lpre;
       bool ok = true;
       while (ok && (c < nch || lc < (lora ? nch : 0))) {
-        // A chunks run at most 2 ahead of the weights; weights `stages` ahead
-        if (lora && lc < nch && lc < c + 2) {
-          const int b = lc & 1;
-          ok = wait_or_abort(smem_u32(&S.lempty[b]), ((lc >> 1) - 1) & 1, abort_flag);
+        // Issue in the order the MMA frees the buffers: A chunk lc reuses the ring slot of
+        // chunk lc - la, weight chunk c the stage of chunk c - stages.  (Taking A first
+        // whenever it is behind would wait on the MMA of the chunk just issued and leave
+        // the weight stream one chunk deep.)
+        if (lora && lc < nch && (c >= nch || lc - la <= c - stages)) {
+          const int b = lc % la;
+          ok = wait_or_abort(smem_u32(&S.lempty[b]), ((lc / la) - 1) & 1, abort_flag);
           if (!ok) break;
           const uint32_t lb = smem_u32(&S.lfull[b]);
           mbar_arrive_expect_tx(lb, l_bytes);
@@ -358,6 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
         uint8_t* st = smem + static_cast<size_t>(s) * p.stage_bytes;
         const uint32_t wb = smem_u32(&S.wfull[s]), hb = smem_u32(&S.hfull[s]);
         const int kc = c0 + c;
+        PL_TLC(0, c);
         mbar_arrive_expect_tx(wb, kCodesBytes + kScaleBytes);
         tma_load_2d_hint(smem_u32(st), &maps.codes, kc * (kChunkK / 2), row0, wb, pol_w);
         tma_load_2d_hint(smem_u32(st + kCodesBytes + h_bytes), &maps.scales, kc * (kChunkK / 16), row0, wb, pol_w);
@@ -371,47 +411,57 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
           drain(smem_u32(&S.wfull[d % stages]), (d / stages) & 1);
           drain(smem_u32(&S.hfull[d % stages]), (d / stages) & 1);
         }
-        for (int d = (lc - 2 > 0 ? lc - 2 : 0); d < lc; ++d) drain(smem_u32(&S.lfull[d & 1]), (d >> 1) & 1);
+        for (int d = (lc - la > 0 ? lc - la : 0); d < lc; ++d) drain(smem_u32(&S.lfull[d % la]), (d / la) & 1);
       }
     }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+  } else if (warp == 1 || warp >= 2 + kDeqWarps) {
+    // ---------------------------------------------------------------- MMA issuers
+    // One thread can issue a tcgen05.mma only every few tens of ns, so four warps share the
+    // work: issuer q takes K steps [8 (q & 1), 8 (q & 1) + 8) of every chunk, q < 2 the
+    // weights (tensor memory) x activations^T into D1 half q, q >= 2 the adapter A (shared
+    // memory, a 128-row operand whose rows >= r are don't-care) x activations^T into Dt
+    // half q - 2.  Each accumulator is a partial sum; the epilogue adds the two halves.
+    const int q = warp == 1 ? 0 : warp - (1 + kDeqWarps);
+    if (lane == 0 && q < n_iss) {
       const uint32_t idesc = idesc_f16(kTileO, N, 0);
+      const uint32_t dcol = tmem + kColAcc + 64u * static_cast<uint32_t>(q);
+      const int k0 = 8 * (q & 1);
+      const bool wq = q < 2;
       bool ok = true;
       for (int c = 0; c < nch && ok; ++c) {
-        const int s = c % stages, b = c & 1;
-        ok = wait_or_abort(smem_u32(&S.a_full[b]), (c >> 1) & 1, abort_flag) &&
+        const int s = c % stages, b = c % kAbuf, lb = c % la;
+        ok = (wq ? wait_or_abort(smem_u32(&S.a_full[b]), (c / kAbuf) & 1, abort_flag)
+                 : wait_or_abort(smem_u32(&S.lfull[lb]), (c / la) & 1, abort_flag)) &&
              wait_or_abort(smem_u32(&S.hfull[s]), (c / stages) & 1, abort_flag);
         if (!ok) break;
+        PL_TLC(wq ? 1 : 2, c);
         tc_fence_after();
         const uint32_t hbase = smem_u32(smem + static_cast<size_t>(s) * p.stage_bytes + kCodesBytes);
+        if (wq) {
 #pragma unroll
-        for (int kk = 0; kk < kChunkK / 16; ++kk) {
-          const uint64_t bdesc = smem_desc_sw128(hbase + (kk >> 2) * N * 128 + (kk & 3) * 32, 1024);
-          mma_ts(tmem + kColD1, tmem + kColA0 + 128u * b + kk * 8, bdesc, idesc, (c > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc_commit(smem_u32(&S.a_empty[b]));
-        if (lora) {
-          // A operand from shared memory: 128 rows at 1 KB per 8 rows; rows >= rb read
-          // bytes that follow the chunk (still inside this CTA's allocation) and only
-          // feed accumulator lanes >= r, which are never read
-          ok = wait_or_abort(smem_u32(&S.lfull[c & 1]), (c >> 1) & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t abase = smem_u32(lring + (c & 1) * l_bytes);
+          for (int i = 0; i < 8; ++i) {
+            const int kk = k0 + i;
+            const uint64_t bdesc = smem_desc_sw128(hbase + (kk >> 2) * N * 128 + (kk & 3) * 32, 1024);
+            mma_ts(dcol, tmem + kColA0 + 128u * b + kk * 8, bdesc, idesc, (c > 0 || i > 0) ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&S.a_empty[b]));
+        } else {
+          // rows >= rb of the A operand read bytes that follow the chunk (still inside this
+          // CTA's allocation) and only feed accumulator lanes >= r, which are never used
+          const uint32_t abase = smem_u32(lring + lb * l_bytes);
 #pragma unroll
-          for (int kk = 0; kk < kChunkK / 16; ++kk) {
+          for (int i = 0; i < 8; ++i) {
+            const int kk = k0 + i;
             const uint64_t adesc = smem_desc_sw128(abase + (kk >> 2) * p.rb * 128 + (kk & 3) * 32, 1024);
             const uint64_t bdesc = smem_desc_sw128(hbase + (kk >> 2) * N * 128 + (kk & 3) * 32, 1024);
-            mma_ss(tmem + kColDt, adesc, bdesc, idesc, (c > 0 || kk > 0) ? 1u : 0u);
+            mma_ss(dcol, adesc, bdesc, idesc, (c > 0 || i > 0) ? 1u : 0u);
           }
-          tc_commit(smem_u32(&S.lempty[c & 1]));
+          tc_commit(smem_u32(&S.lempty[lb]));
         }
         tc_commit(smem_u32(&S.empty[s]));
       }
       tc_commit(smem_u32(&S.d_full));  // also reached on abort: tracks every MMA issued
-      PL_TL(6);
+      if (q == 0) PL_TL(6);
     }
   } else {
     // ---------------------------------------------------------------- dequant + epilogue
@@ -450,11 +500,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
       }
     }
     for (int c = 0; c < nch; ++c) {
-      const int s = c % stages, b = c & 1;
+      const int s = c % stages, b = c % kAbuf;
       ok = wait_or_abort(smem_u32(&S.wfull[s]), (c / stages) & 1, abort_flag) &&
-           (c < 2 || wait_or_abort(smem_u32(&S.a_empty[b]), ((c >> 1) - 1) & 1, abort_flag));
+           (c < kAbuf || wait_or_abort(smem_u32(&S.a_empty[b]), ((c / kAbuf) - 1) & 1, abort_flag));
       if (!ok) break;
       if (c == 0 && threadIdx.x == 64) PL_TL(4);
+      if (threadIdx.x == 64) PL_TLC(3, c);
       const uint8_t* st = smem + static_cast<size_t>(s) * p.stage_bytes;
       const uint8_t* crow = st + row * 128;
       const uint2 sc8 = *reinterpret_cast<const uint2*>(st + kCodesBytes + h_bytes + row * 16 + g * 8);
@@ -501,23 +552,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
       const float s_g = S.s_g;
       const int half = N / 2;  // 8, 16, 24 or 32 tokens per thread
       const int n0 = g * half;
-      uint32_t d1[32], dt[32];
       const bool trow = lora && quarter < 2;  // lanes 0..63 hold rows of t
+      const uint32_t acc = tmem + lane_addr + kColAcc + static_cast<uint32_t>(n0);
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) {
-        if (cb * 8 < half) {
-          tmem_ld8(tmem + lane_addr + kColD1 + n0 + cb * 8, &d1[cb * 8]);
-          if (trow) tmem_ld8(tmem + lane_addr + kColDt + n0 + cb * 8, &dt[cb * 8]);
-        }
-      }
-      tmem_ld_wait();
-      const int jt = row;
+        if (cb * 8 < half) {  // 8 tokens at a time: the two halves of D1 (and of Dt)
+          uint32_t da[8], db[8], ta[8], tb[8];
+          tmem_ld8(acc + cb * 8, da);
+          tmem_ld8(acc + 64 + cb * 8, db);
+          if (trow) {
+            tmem_ld8(acc + 128 + cb * 8, ta);
+            tmem_ld8(acc + 192 + cb * 8, tb);
+          }
+          tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        if (i < half) {
-          const int n = n0 + i;
-          red[n * kTileO + row] = s_g * S.rowscale[n] * __uint_as_float(d1[i]);
-          if (trow) tred[n * kTStride + jt] = S.rowscale[n] * __uint_as_float(dt[i]);
+          for (int i = 0; i < 8; ++i) {
+            const int n = n0 + cb * 8 + i;
+            red[n * kTileO + row] = s_g * S.rowscale[n] * (__uint_as_float(da[i]) + __uint_as_float(db[i]));
+            if (trow) tred[n * kTStride + row] = S.rowscale[n] * (__uint_as_float(ta[i]) + __uint_as_float(tb[i]));
+          }
         }
       }
     }
@@ -556,65 +609,70 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
             acc.z += part[sp].z;
             acc.w += part[sp].w;
           }
+        // adapter rows past r (accumulator lanes that hold don't-care sums) become zeros
         reinterpret_cast<float4*>(tful + n * kTStride + jj)[0] =
-            make_float4(p.lambda * acc.x, p.lambda * acc.y, p.lambda * acc.z, p.lambda * acc.w);
+            make_float4(jj < p.r ? p.lambda * acc.x : 0.f, jj + 1 < p.r ? p.lambda * acc.y : 0.f,
+                        jj + 2 < p.r ? p.lambda * acc.z : 0.f, jj + 3 < p.r ? p.lambda * acc.w : 0.f);
       }
       named_bar(1, kEpiThreads);
     }
+    // This CTA's share of the tile's rows: groups of 4 rows [g0, g1) of 32.  Thread et takes
+    // row r0 + et % nrows and every ngrp-th token from et / nrows; it holds the row of B in
+    // registers, sums the D1 partials of the S CTAs (split order) and adds B (lambda t).
     const int g0 = (split * (kTileO / 4)) / p.splits, g1 = ((split + 1) * (kTileO / 4)) / p.splits;
-    const int ng = g1 - g0;
-    // work item = (token n, row group rr, quarter jp of the adapter rows): the 4 lanes
-    // of one (n, rr) are neighbours in a warp and combine their LoRA sums by shuffles;
-    // lane jp == 0 also sums the D1 partials and writes the 4 outputs
-    const int items = ng * mt * 4;
-    const int jq = (p.r + 3) / 4;
-    for (int base = et - (et & 31); base < items; base += kEpiThreads) {
-      const int e = base + (et & 31);
-      const bool valid = e < items;
-      const int gi = e >> 2, jp = e & 3;
-      const int n = valid ? gi / ng : 0, rr = valid ? 4 * (g0 + gi % ng) : 0;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      if (valid && lora) {
-        const float* tn = tful + n * kTStride;
-        const int ja = jp * jq, jb = (jp + 1) * jq < p.r ? (jp + 1) * jq : p.r;
-        for (int jj = ja; jj < jb; ++jj) {
-          const float tj = tn[jj];
-          const uint2 b4 = *reinterpret_cast<const uint2*>(sBt + jj * kTileO + rr);  // B[rr..rr+3][jj]
-          acc[0] = fmaf(bf16lo_to_f32(b4.x), tj, acc[0]);
-          acc[1] = fmaf(bf16hi_to_f32(b4.x), tj, acc[1]);
-          acc[2] = fmaf(bf16lo_to_f32(b4.y), tj, acc[2]);
-          acc[3] = fmaf(bf16hi_to_f32(b4.y), tj, acc[3]);
+    const int r0 = 4 * g0, nrows = 4 * (g1 - g0);
+    const int ngrp = kEpiThreads / nrows;  // >= 2: a share has at most 128 rows
+    const int rl = et % nrows, tg = et / nrows;
+    if (tg < ngrp) {
+      const int rr = r0 + rl;
+      const int64_t oo = static_cast<int64_t>(tile) * kTileO + rr;
+      const int r4 = lora ? (p.r + 3) / 4 : 0;
+      // y[n][rr] = (sum over splits of the D1 partials) + lora, stored as FP32 or BF16
+      auto finish = [&](int n, float lora_sum) {
+        float d = 0.f;
+        if (p.splits == 1) {
+          d = red[n * kTileO + rr];
+        } else {
+          const uint32_t addr = red_addr + static_cast<uint32_t>((n * kTileO + rr) * 4);
+          float part[kMaxSplit];
+#pragma unroll
+          for (int sp = 0; sp < kMaxSplit; ++sp)
+            if (sp < p.splits) part[sp] = ld_dsmem_f32(mapa_shared(addr, sp));
+#pragma unroll
+          for (int sp = 0; sp < kMaxSplit; ++sp)
+            if (sp < p.splits) d += part[sp];
         }
-      }
+        const float v = d + lora_sum;
+        if (oo < p.d_o) {
+          if (p.y_f32) static_cast<float*>(p.y)[n * p.d_o + oo] = v;
+          else static_cast<__nv_bfloat16*>(p.y)[n * p.d_o + oo] = __float2bfloat16_rn(v);
+        }
+      };
+      // four tokens per round (n + i ngrp): independent FMA chains in flight; B[rr][j] comes
+      // from sBt[j][rr] (zeros past r), 32 neighbouring rows of one row of sBt per warp
+      constexpr int kTok = 4;
+      for (int n = tg; n < mt; n += kTok * ngrp) {
+        float acc[kTok] = {0.f, 0.f, 0.f, 0.f};
+        const float4* tn[kTok];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        acc[q] += __shfl_xor_sync(0xFFFFFFFFu, acc[q], 1);
-        acc[q] += __shfl_xor_sync(0xFFFFFFFFu, acc[q], 2);
-      }
-      if (valid && jp == 0) {
-        const uint32_t addr = red_addr + static_cast<uint32_t>((n * kTileO + rr) * 4);
-        float4 part[kMaxSplit];
+        for (int i = 0; i < kTok; ++i) {
+          const int ni = n + i * ngrp;
+          tn[i] = reinterpret_cast<const float4*>(tful + (ni < mt ? ni : n) * kTStride);
+        }
+        for (int j4 = 0; j4 < r4; ++j4) {
+          const float w0 = __bfloat162float(sBt[(4 * j4) * kTileO + rr]);
+          const float w1 = __bfloat162float(sBt[(4 * j4 + 1) * kTileO + rr]);
+          const float w2 = __bfloat162float(sBt[(4 * j4 + 2) * kTileO + rr]);
+          const float w3 = __bfloat162float(sBt[(4 * j4 + 3) * kTileO + rr]);
 #pragma unroll
-        for (int sp = 0; sp < kMaxSplit; ++sp)
-          if (sp < p.splits) part[sp] = ld_dsmem_f32x4(mapa_shared(addr, sp));
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int sp = 0; sp < kMaxSplit; ++sp)
-          if (sp < p.splits) {
-            d[0] += part[sp].x;
-            d[1] += part[sp].y;
-            d[2] += part[sp].z;
-            d[3] += part[sp].w;
-          }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int64_t oo = static_cast<int64_t>(tile) * kTileO + rr + q;
-          const float v = d[q] + acc[q];
-          if (oo < p.d_o) {
-            if (p.y_f32) static_cast<float*>(p.y)[n * p.d_o + oo] = v;
-            else static_cast<__nv_bfloat16*>(p.y)[n * p.d_o + oo] = __float2bfloat16_rn(v);
+          for (int i = 0; i < kTok; ++i) {
+            const float4 t4 = tn[i][j4];  // the same address across the warp: a broadcast
+            acc[i] = fmaf(w0, t4.x, fmaf(w1, t4.y, fmaf(w2, t4.z, fmaf(w3, t4.w, acc[i]))));
           }
         }
+#pragma unroll
+        for (int i = 0; i < kTok; ++i)
+          if (n + i * ngrp < mt) finish(n + i * ngrp, acc[i]);
       }
     }
   }
@@ -656,25 +714,31 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void*
 }
 
 struct Plan {
-  int N, rb, tiles, kc, splits, stages;
+  int N, rb, tiles, kc, splits, stages, la;
   uint32_t stage_bytes;
   size_t smem, act_smem;
 };
 
 uint32_t stage_bytes_for(int N) { return kCodesBytes + kScaleBytes + static_cast<uint32_t>(N) * 512u; }
 
-// Shared memory: `stages` stages, the 2-chunk ring of A (rb rows x 512 B each), the B
-// rows of the tile, the control block and 1 KB of alignment slack.  The epilogue
-// reuses the stage region for its partials ([N][128] + 2 x [N][68] FP32 < 1.1 KB x N),
-// which two stages always cover.
-void stage_plan(int N, int rb, int& stages, uint32_t& sb, size_t& total) {
+// Shared memory: `stages` stages, the ring of `la` A chunks (rb rows x 512 B each), the
+// B rows of the tile, the control block and 1 KB of alignment slack.  The ring has a
+// third slot when that costs no weight stage.  The epilogue reuses the stage region for
+// its partials ([N][128] + 2 x [N][68] FP32 < 1.1 KB x N), which two stages always cover.
+void stage_plan(int N, int rb, int& stages, int& la, uint32_t& sb, size_t& total) {
   sb = stage_bytes_for(N);
-  const size_t fixed = 1024 + 2 * static_cast<size_t>(rb) * 512 + kTileO * kMaxR * 2 + sizeof(Smem);
   const size_t limit = 227 * 1024;
-  int st = static_cast<int>((limit - fixed) / sb);
-  st = st > kMaxStages ? kMaxStages : st;
-  stages = st < 2 ? 2 : st;
-  total = fixed + static_cast<size_t>(stages) * sb;
+  auto fit = [&](int l, size_t& fixed) {
+    fixed = 1024 + static_cast<size_t>(l) * rb * 512 + kTileO * kMaxR * 2 + sizeof(Smem);
+    int st = static_cast<int>((limit - fixed) / sb);
+    st = st > kMaxStages ? kMaxStages : st;
+    return st < 2 ? 2 : st;
+  };
+  size_t fixed2, fixed3;
+  const int st2 = fit(2, fixed2), st3 = fit(kMaxLa, fixed3);
+  la = st3 >= st2 && fixed3 + static_cast<size_t>(st3) * sb <= limit ? kMaxLa : 2;
+  stages = la == kMaxLa ? st3 : st2;
+  total = (la == kMaxLa ? fixed3 : fixed2) + static_cast<size_t>(stages) * sb;
 }
 
 cudaError_t set_kernel_attributes() {
@@ -695,10 +759,10 @@ int max_active_clusters(int N, int rb, int cs) {
   std::lock_guard<std::mutex> lk(mu);
   int& c = cache[N / 16][rb / 8][cs];
   if (c == 0) {
-    int st;
+    int st, la;
     uint32_t sb;
     size_t total;
-    stage_plan(N, rb, st, sb, total);
+    stage_plan(N, rb, st, la, sb, total);
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(cs * 64));
     cfg.blockDim = dim3(kThreads);
@@ -744,7 +808,7 @@ Plan make_plan(int64_t M, int64_t d_i, int64_t d_o, int r) {
   pl.tiles = static_cast<int>((d_o + kTileO - 1) / kTileO);
   pl.kc = static_cast<int>(d_i / kChunkK);
   pl.splits = choose_splits(pl.N, pl.rb, pl.tiles, pl.kc);
-  stage_plan(pl.N, pl.rb, pl.stages, pl.stage_bytes, pl.smem);
+  stage_plan(pl.N, pl.rb, pl.stages, pl.la, pl.stage_bytes, pl.smem);
   pl.act_smem = static_cast<size_t>(d_i) * 4;
   return pl;
 }
@@ -820,6 +884,7 @@ cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   p.splits = pl.splits;
   p.kc = pl.kc;
   p.stages = pl.stages;
+  p.la = pl.la;
   p.stage_bytes = pl.stage_bytes;
   p.lambda = a.lambda;
   p.s_g = a.s_g;
@@ -880,6 +945,11 @@ extern "C" int pl_debug_read_timeline(unsigned long long* main_out, unsigned lon
   if (cudaMemcpyFromSymbol(main_out, g_tl_main, sizeof(g_tl_main)) != cudaSuccess) return 2;
   if (cudaMemcpyFromSymbol(pro_out, g_tl_pro, sizeof(g_tl_pro)) != cudaSuccess) return 3;
   return 0;
+}
+
+extern "C" int pl_debug_read_timeline_chunks(unsigned long long* out) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return 1;
+  return cudaMemcpyFromSymbol(out, g_tl_chunk, sizeof(g_tl_chunk)) == cudaSuccess ? 0 : 2;
 }
 #endif
 

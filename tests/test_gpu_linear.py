@@ -74,6 +74,16 @@ def test_large_m_shapes(cuda_ok, d_o, d_i, M, r):
     _check(d_o, d_i, M, r, seed=d_o + M + r)
 
 
+# Decode shapes of the two-kernel tcgen05 path (too many tiles, or too long a K slice, for
+# the fused kernel): one chunk per CTA (fewer than the A ring's slots), no adapter, an odd
+# rank, K split over a cluster with ragged slices, N = 64 with r = 64.
+@pytest.mark.parametrize("d_o,d_i,M,r", [(20000, 256, 1, 0), (20000, 512, 7, 5), (2000, 8192, 3, 5),
+                                         (3000, 9216, 64, 64), (130, 18944, 33, 32)])
+def test_tc_path_shapes(cuda_ok, d_o, d_i, M, r):
+    assert pl.linear_path(M, d_i, d_o, r) == 1
+    _check(d_o, d_i, M, r, seed=d_o + M + r, lora=r > 0)
+
+
 @pytest.mark.parametrize("M", [8, 32, 64])
 def test_7b_layer_set(cuda_ok, M):
     wl = synthetic.WORKLOADS["layer_7b"]
