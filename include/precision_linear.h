@@ -173,6 +173,38 @@ pl_status pl_nvfp4_lora_linear_static_ws(const void* x_bf16, int64_t M, int64_t 
                                          const float* w_norm, const float* z, float eps,
                                          void* y, int y_dtype, pl_stream_t stream);
 
+/* AQN noise state: the staged schedule (section 5.2), its stage (section 6) and the
+ * device draw of z that pl_rmsnorm_aqn and pl_nvfp4_lora_linear take (section 5.1).
+ *
+ * pl_aqn_stage: the schedule stage after `done` of `total` planned updates, ten
+ *   equal parts of the horizon: min(9, floor(10 done / total)); stage 0 is the
+ *   warm-up without noise.  Host only.  Returns -1 when total < 1 or done < 0. */
+int pl_aqn_stage(int64_t done, int64_t total);
+
+/* pl_aqn_sigma: sigma_0 = 0 and, for k = 1 .. 9,
+ *   sigma_k = sigma_start * (sigma_end / sigma_start) ^ ((k - 1) / 8),
+ * so stage 1 is sigma_start and stage 9 sigma_end.  Computed in double, returned
+ * rounded to float.  Host only.  Returns -1 for a stage outside 0 .. 9 or a start or
+ * end that is not positive and finite. */
+float pl_aqn_sigma(int stage, float sigma_start, float sigma_end);
+
+/* pl_aqn_noise: z[s][j] = sigma * n_j(seed, norm_id, scope0 + s), s < n_scopes, j < d.
+ * The state is a pure function of its arguments, so a rollout, a response or a token
+ * (the persistence scope the caller declares through the scope index) replays it
+ * exactly; norm_id names the RMSNorm (one vector per norm, shared by the projections
+ * that read it).  Draws: Philox4x32-10 (Salmon et al., SC 2011) with key = seed (low
+ * word first) and counter = (j / 4, norm_id, scope low word, scope high word); each
+ * output word x gives u = (2 (x >> 9) + 1) * 2^-24; channels 4b, 4b+1 are rho cos(2 pi
+ * u1), rho sin(2 pi u1) with rho = sqrt(-2 ln u0) from words 0..1 of block b, channels
+ * 4b+2, 4b+3 the same from words 2..3; FP32 with the IEEE square root, logf and
+ * sincospif, then times sigma.
+ *  z out: FP32 [n_scopes][d], device, 4-byte aligned (caller-owned).
+ * Requirements: 1 <= d <= 2^31, 1 <= n_scopes <= 2^31, d * n_scopes <= 2^40, sigma
+ * finite and >= 0 (PL_ERR_SHAPE otherwise, nothing launched).  One kernel launch,
+ * asynchronous on `stream`. */
+pl_status pl_aqn_noise(uint64_t seed, uint32_t norm_id, uint64_t scope0, int64_t n_scopes, int64_t d,
+                       float sigma, float* z, pl_stream_t stream);
+
 /* Synchronises `stream`, then returns and clears the device status word: set by
  * bounded device-side waits that gave up (PL_ERR_TIMEOUT; that call's y is then not
  * valid), else PL_OK. */

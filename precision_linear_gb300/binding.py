@@ -47,6 +47,10 @@ _SIGNATURES = {
                                             _c_void_p, _c_void_p, ctypes.c_int, ctypes.c_float,
                                             _c_void_p, _c_void_p, ctypes.c_float, _c_void_p, ctypes.c_int,
                                             _c_void_p, ctypes.c_size_t, _c_void_p]),
+    "pl_aqn_stage": (ctypes.c_int, [_i64, _i64]),
+    "pl_aqn_sigma": (ctypes.c_float, [ctypes.c_int, ctypes.c_float, ctypes.c_float]),
+    "pl_aqn_noise": (ctypes.c_int, [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint64, _i64, _i64, ctypes.c_float,
+                                    _c_void_p, _c_void_p]),
     "pl_last_device_status": (ctypes.c_int, [_c_void_p]),
     "pl_debug_fail_next_launch": (None, [ctypes.c_int]),
     "pl_debug_linear_path": (ctypes.c_int, [_i64, _i64, _i64, ctypes.c_int]),
@@ -202,6 +206,42 @@ def nvfp4_lora_linear(x, codes, scales, s_g, A=None, B=None, lam: float = 0.0, w
                                         _ptr(A), _ptr(B), r, float(lam), _ptr(w_norm), _ptr(z), float(eps),
                                         _ptr(out), _OUT_DTYPES[out.dtype], _ptr(ws), ws.numel(), _stream(dev))
     _check(st, "pl_nvfp4_lora_linear")
+    return out
+
+
+def aqn_stage(done: int, total: int) -> int:
+    """Schedule stage (0 .. 9) after `done` of `total` planned updates."""
+    k = int(lib().pl_aqn_stage(int(done), int(total)))
+    if k < 0:
+        raise ValueError("pl_aqn_stage: need total >= 1 and done >= 0")
+    return k
+
+
+def aqn_sigma(stage: int, sigma_start: float, sigma_end: float) -> float:
+    """sigma of schedule stage `stage` (0 for the warm-up stage)."""
+    v = float(lib().pl_aqn_sigma(int(stage), float(sigma_start), float(sigma_end)))
+    if v < 0:
+        raise ValueError("pl_aqn_sigma: stage outside 0..9 or non-positive endpoints")
+    return v
+
+
+def aqn_noise(d: int, seed: int, norm_id: int = 0, scope0: int = 0, n_scopes: int = 1, sigma: float = 1.0,
+              out: torch.Tensor | None = None, device=None) -> torch.Tensor:
+    """z FP32 [n_scopes, d]: the AQN noise states of scope indices scope0 .. scope0 + n_scopes - 1
+    of norm `norm_id` under `seed` (row 0 is the z the linear and the norm take)."""
+    dev = torch.device(device) if device is not None else (out.device if out is not None else torch.device("cuda"))
+    if dev.type == "cuda" and dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    if out is None:
+        out = torch.empty(n_scopes, d, dtype=torch.float32, device=dev)
+    _need(out, "out", torch.float32, dev, 2)
+    if tuple(out.shape) != (n_scopes, d):
+        raise ValueError(f"out must be [{n_scopes}, {d}]")
+    with torch.cuda.device(dev):
+        st = lib().pl_aqn_noise(int(seed) & 0xFFFFFFFFFFFFFFFF, int(norm_id) & 0xFFFFFFFF,
+                                int(scope0) & 0xFFFFFFFFFFFFFFFF, int(n_scopes), int(d), float(sigma), _ptr(out),
+                                _stream(dev))
+    _check(st, "pl_aqn_noise")
     return out
 
 

@@ -1,6 +1,7 @@
 // C ABI of libprecision_linear: argument checks, device check, dispatch.
 // Declarations and the contract of every entry point are in include/precision_linear.h.
 #include <atomic>
+#include <cmath>
 #include <mutex>
 
 #include "../../include/precision_linear.h"
@@ -146,6 +147,36 @@ pl_status pl_nvfp4_lora_linear(const void* x, int64_t M, int64_t d_i, int64_t d_
   if (pl::tc_supported(M, d_i, d_o, a.r)) return check_launch(pl::launch_linear_tc(a, s));
   if (pl::prefill_supported(M, d_i, d_o, a.r)) return check_launch(pl::launch_linear_prefill(a, s));
   return check_launch(pl::launch_linear_generic(a, s));
+}
+
+int pl_aqn_stage(int64_t done, int64_t total) {
+  if (total < 1 || done < 0) return -1;
+  // ten equal parts of the planned horizon, the product taken in 128 bits
+  if (done >= total) return 9;
+  const int64_t k = static_cast<int64_t>((static_cast<__int128>(10) * done) / total);
+  return k > 9 ? 9 : static_cast<int>(k);
+}
+
+float pl_aqn_sigma(int stage, float sigma_start, float sigma_end) {
+  if (stage < 0 || stage > 9 || !(sigma_start > 0.f) || !(sigma_end > 0.f) || !std::isfinite(sigma_start) ||
+      !std::isfinite(sigma_end))
+    return -1.f;
+  if (stage == 0) return 0.f;
+  const double s0 = sigma_start, s1 = sigma_end;
+  return static_cast<float>(s0 * std::pow(s1 / s0, (stage - 1) / 8.0));
+}
+
+pl_status pl_aqn_noise(uint64_t seed, uint32_t norm_id, uint64_t scope0, int64_t n_scopes, int64_t d,
+                       float sigma, float* z, pl_stream_t stream) {
+  if (!z) return PL_ERR_NULL;
+  if (d < 1 || n_scopes < 1 || d > (1ll << 31) || n_scopes > (1ll << 31) || d * n_scopes > (1ll << 40) ||
+      !(sigma >= 0.f) || !std::isfinite(sigma))
+    return PL_ERR_SHAPE;
+  if (reinterpret_cast<uintptr_t>(z) & 3u) return PL_ERR_ALIGN;
+  pl_status st = device_check();
+  if (st != PL_OK) return st;
+  return check_launch(pl::launch_aqn_noise(seed, norm_id, scope0, n_scopes, d, sigma, z,
+                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
 pl_status pl_last_device_status(pl_stream_t stream) {

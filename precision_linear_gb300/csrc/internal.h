@@ -65,6 +65,10 @@ size_t prefill_workspace_bytes(int64_t M, int64_t d_i, int64_t d_o, int r);
 cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream);
 uint32_t prefill_read_and_clear_status();
 
+// ---- aqn.cu: z [n_scopes][d] = sigma * Philox4x32-10 / Box-Muller normals
+cudaError_t launch_aqn_noise(uint64_t seed, uint32_t norm_id, uint64_t scope0, int64_t n_scopes, int64_t d,
+                             float sigma, float* z, cudaStream_t stream);
+
 // ---- api.cu
 int sm_count();  // SMs of the current device (cached)
 

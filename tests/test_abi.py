@@ -110,10 +110,44 @@ def test_linear_argument_checks(L):
     assert f(*_lin_args(y_dtype=5)) == 2
 
 
+def test_aqn_stage_and_sigma_follow_the_oracle(L):
+    """Host-side schedule of the AQN noise against oracle/aqn.py (FP64, rounded to FP32)."""
+    import numpy as np
+
+    from oracle import aqn
+    for total in (1, 7, 10, 1000, 12345):
+        for done in sorted({0, 1, total // 10, total // 10 + 1, total // 2, total - 1, total, 3 * total}):
+            assert L.pl_aqn_stage(done, total) == aqn.stage(done, total), (done, total)
+    assert L.pl_aqn_stage(1 << 62, (1 << 62) + 1) == 9  # no overflow in 10 * done
+    assert L.pl_aqn_stage(1, 0) == -1 and L.pl_aqn_stage(-1, 10) == -1
+    for start, end in ((0.01, 0.0005), (0.05, 0.0005)):
+        s32, e32 = float(np.float32(start)), float(np.float32(end))
+        for k in range(10):
+            want = np.float32(aqn.sigma(k, s32, e32))
+            got = np.float32(L.pl_aqn_sigma(k, s32, e32))
+            assert abs(int(got.view(np.int32)) - int(want.view(np.int32))) <= 1, (k, got, want)
+        assert L.pl_aqn_sigma(1, s32, e32) == s32 and L.pl_aqn_sigma(9, s32, e32) == e32
+    assert L.pl_aqn_sigma(10, 0.01, 0.0005) == -1.0 and L.pl_aqn_sigma(-1, 0.01, 0.0005) == -1.0
+    assert L.pl_aqn_sigma(3, 0.0, 0.0005) == -1.0 and L.pl_aqn_sigma(3, 0.01, float("inf")) == -1.0
+
+
+def test_aqn_noise_argument_checks(L):
+    f = L.pl_aqn_noise
+    ok = [1, 0, 0, 1, 256, ctypes.c_float(0.01), _p(FAKE), None]
+    a = list(ok); a[6] = None
+    assert f(*a) == 1
+    for i, v in ((4, 0), (3, 0), (4, (1 << 31) + 1), (5, ctypes.c_float(-1.0)), (5, ctypes.c_float(float("nan")))):
+        a = list(ok); a[i] = v
+        assert f(*a) == 2, (i, v)
+    a = list(ok); a[6] = _p(FAKE + 2)
+    assert f(*a) == 3
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
 def test_valid_arguments_without_a_device_report_device_error(L):
     assert L.pl_nvfp4_lora_linear(*_lin_args()) == 5
     assert L.pl_nvfp4_quantize(_p(FAKE), 16, 32, _p(FAKE), _p(FAKE), _p(FAKE), None) == 5
+    assert L.pl_aqn_noise(1, 0, 0, 1, 256, ctypes.c_float(0.01), _p(FAKE), None) == 5
 
 
 def test_product_path_does_not_import_the_oracle():
