@@ -138,9 +138,11 @@ def dist_setup():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
+        import torch
         import torch.distributed as dist
-        backend = "nccl"
-        dist.init_process_group(backend=backend)
+        # NCCL between GPUs; gloo on a host without one (the reference arm's other ranks
+        # and the multi-rank tests on CPU)
+        dist.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo")
     return world, rank, local
 
 
