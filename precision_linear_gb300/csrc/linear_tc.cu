@@ -139,9 +139,11 @@ constexpr int kActWarps = kActThreads / 32;  // token rows in flight per CTA
 constexpr int kActPieces = 16;               // 16-byte pieces of x per thread, held in registers
 constexpr int kActUnroll = 4;                // loads per thread in flight in the copy loops
 
-// CTAs 0 .. M-1: one token row m each.  hz = x (.) (w + z) is kept in shared memory
-// (FP32) while sum(x^2) and max |hz| are reduced; then hq = f16(hz * inv / c_m).
-// CTAs M and up: the f16 copy of A (r x d_i), 8 elements per thread and slot, and
+// CTAs 0 .. n_row_ctas-1: token rows, a group of wpr warps per row (kActWarps / wpr rows
+// per CTA, rows strided over the CTAs).  w + z of the whole row sits in shared memory
+// (FP32); the group holds its row of x in registers while sum(x^2) and max |x (w + z)|
+// are reduced, then writes hq = f16(x (w + z) inv / c_m) and c_m.
+// CTAs n_row_ctas and up: the f16 copy of A (r x d_i), 8 elements per thread and slot, and
 // zeros into `zero` (n_zero floats, a multiple of 4; the accumulator of the large-M
 // LoRA down-projection), 4 per thread and slot.
 __global__ void __launch_bounds__(kActThreads, 2) k_act(const __nv_bfloat16* __restrict__ x, int64_t M, int64_t d_i,
