@@ -111,6 +111,22 @@ pl_status pl_nvfp4_quantize(const void* W_bf16, int64_t d_o, int64_t d_i,
                             uint8_t* codes, uint8_t* scales, float* s_g,
                             pl_stream_t stream);
 
+/* Update-aware quantisation fold ("QuRL: Low-Precision Reinforcement Learning for
+ * Efficient Reasoning", reading notes section 3: a linear layer is invariant under
+ * W X = (W / s)(s X), the factor on X absorbed by the normalisation before it; the
+ * method folds s > 1, once, before training; s = 1.5 in its runs).
+ *
+ * pl_nvfp4_quantize_uaq: pl_nvfp4_quantize of W' = fp32(W / s) (IEEE division of every
+ *   weight): s_g = fp32(max|W'| / 2688), block scales and codes of W' under the same
+ *   contract.  s == 1 is exactly pl_nvfp4_quantize.  Requirements as pl_nvfp4_quantize,
+ *   plus s finite and > 0 (PL_ERR_SHAPE).
+ * pl_uaq_fold_norm: out[i] = fp32(w_norm[i] * s), i < d (FP32 [d] in and out, device,
+ *   4-byte aligned; out may equal w_norm).  The folded pair (W', w') gives the same layer
+ *   up to the quantisation of W'. */
+pl_status pl_nvfp4_quantize_uaq(const void* W_bf16, int64_t d_o, int64_t d_i, float s,
+                                uint8_t* codes, uint8_t* scales, float* s_g, pl_stream_t stream);
+pl_status pl_uaq_fold_norm(const float* w_norm, int64_t d, float s, float* out, pl_stream_t stream);
+
 /* RMSNorm with AQN noise folded into the scale (section 5.1):
  *   h[m, :] = x[m, :] / sqrt(mean_j x[m, j]^2 + eps) (.) (w_norm + z)
  *  x_bf16 in : BF16 [M][d];  w_norm in: FP32 [d];  z in: FP32 [d] or NULL (no

@@ -47,6 +47,9 @@ _SIGNATURES = {
                                             _c_void_p, _c_void_p, ctypes.c_int, ctypes.c_float,
                                             _c_void_p, _c_void_p, ctypes.c_float, _c_void_p, ctypes.c_int,
                                             _c_void_p, ctypes.c_size_t, _c_void_p]),
+    "pl_nvfp4_quantize_uaq": (ctypes.c_int, [_c_void_p, _i64, _i64, ctypes.c_float, _c_void_p, _c_void_p,
+                                             _c_void_p, _c_void_p]),
+    "pl_uaq_fold_norm": (ctypes.c_int, [_c_void_p, _i64, ctypes.c_float, _c_void_p, _c_void_p]),
     "pl_aqn_stage": (ctypes.c_int, [_i64, _i64]),
     "pl_aqn_sigma": (ctypes.c_float, [ctypes.c_int, ctypes.c_float, ctypes.c_float]),
     "pl_aqn_noise": (ctypes.c_int, [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint64, _i64, _i64, ctypes.c_float,
@@ -132,6 +135,37 @@ def nvfp4_quantize(W: torch.Tensor, codes=None, scales=None, s_g=None):
         st = lib().pl_nvfp4_quantize(_ptr(W), d_o, d_i, _ptr(codes), _ptr(scales), _ptr(s_g), _stream(dev))
     _check(st, "pl_nvfp4_quantize")
     return codes, scales, s_g
+
+
+def nvfp4_quantize_uaq(W: torch.Tensor, s: float = 1.5, codes=None, scales=None, s_g=None):
+    """NVFP4 encoding of fp32(W / s) (the UAQ fold's weight half); returns (codes, scales, s_g)."""
+    _need(W, "W", torch.bfloat16, dim=2)
+    d_o, d_i = W.shape
+    dev = W.device
+    if codes is None:
+        codes = torch.empty(d_o, d_i // 2, dtype=torch.uint8, device=dev)
+    if scales is None:
+        scales = torch.empty(d_o, max(d_i // 16, 1), dtype=torch.uint8, device=dev)
+    if s_g is None:
+        s_g = torch.empty(1, dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        st = lib().pl_nvfp4_quantize_uaq(_ptr(W), d_o, d_i, float(s), _ptr(codes), _ptr(scales), _ptr(s_g),
+                                         _stream(dev))
+    _check(st, "pl_nvfp4_quantize_uaq")
+    return codes, scales, s_g
+
+
+def uaq_fold_norm(w_norm: torch.Tensor, s: float = 1.5, out: torch.Tensor | None = None) -> torch.Tensor:
+    """fp32(w_norm * s) (the UAQ fold's norm half)."""
+    _need(w_norm, "w_norm", torch.float32, dim=1)
+    dev = w_norm.device
+    if out is None:
+        out = torch.empty_like(w_norm)
+    _need(out, "out", torch.float32, dev, 1)
+    with torch.cuda.device(dev):
+        st = lib().pl_uaq_fold_norm(_ptr(w_norm), w_norm.numel(), float(s), _ptr(out), _stream(dev))
+    _check(st, "pl_uaq_fold_norm")
+    return out
 
 
 def rmsnorm_aqn(x: torch.Tensor, w_norm: torch.Tensor, z: torch.Tensor | None = None,

@@ -106,6 +106,26 @@ pl_status pl_nvfp4_quantize(const void* W, int64_t d_o, int64_t d_i, uint8_t* co
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
+pl_status pl_nvfp4_quantize_uaq(const void* W, int64_t d_o, int64_t d_i, float s, uint8_t* codes,
+                                uint8_t* scales, float* s_g, pl_stream_t stream) {
+  if (!W || !codes || !scales || !s_g) return PL_ERR_NULL;
+  if (d_o < 1 || d_i < 16 || d_i % 16 != 0 || !(s > 0.f) || !std::isfinite(s)) return PL_ERR_SHAPE;
+  if (!aligned16(W) || !aligned16(codes) || (reinterpret_cast<uintptr_t>(s_g) & 3u)) return PL_ERR_ALIGN;
+  pl_status st = device_check();
+  if (st != PL_OK) return st;
+  return check_launch(pl::launch_quantize(W, d_o, d_i, codes, scales, s_g,
+                                          reinterpret_cast<cudaStream_t>(stream), s));
+}
+
+pl_status pl_uaq_fold_norm(const float* w_norm, int64_t d, float s, float* out, pl_stream_t stream) {
+  if (!w_norm || !out) return PL_ERR_NULL;
+  if (d < 1 || d > (1ll << 40) || !(s > 0.f) || !std::isfinite(s)) return PL_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(w_norm) & 3u) || (reinterpret_cast<uintptr_t>(out) & 3u)) return PL_ERR_ALIGN;
+  pl_status st = device_check();
+  if (st != PL_OK) return st;
+  return check_launch(pl::launch_fold_norm(w_norm, d, s, out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 pl_status pl_rmsnorm_aqn(const void* x, int64_t M, int64_t d, const float* w_norm,
                          const float* z, float eps, void* h, int h_dtype, pl_stream_t stream) {
   if (!x || !w_norm || !h) return PL_ERR_NULL;

@@ -12,8 +12,11 @@ namespace pl {
 enum : uint32_t { kStatusTimeout = 1u, kStatusRange = 2u };
 
 // ---- quantize.cu
+// fold_s != 1 quantises fp32(W / fold_s) (the UAQ fold); 1 is the plain quantiser.
 cudaError_t launch_quantize(const void* W, int64_t d_o, int64_t d_i, uint8_t* codes,
-                            uint8_t* scales, float* s_g, cudaStream_t stream);
+                            uint8_t* scales, float* s_g, cudaStream_t stream, float fold_s = 1.0f);
+// out[i] = fp32(w[i] * s), i < d: the norm-scale half of the UAQ fold.
+cudaError_t launch_fold_norm(const float* w, int64_t d, float s, float* out, cudaStream_t stream);
 
 // ---- norm.cu
 cudaError_t launch_rmsnorm_aqn(const void* x, int64_t M, int64_t d, const float* w_norm,

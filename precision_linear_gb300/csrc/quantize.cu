@@ -18,6 +18,12 @@
 //              codes, 8-byte + 1-byte stores (a warp moves 1 KB in, 288 B out).
 //   k_finalize turns the accumulated amax into s_g in place.
 //
+// The UAQ fold (invariant scaling, "QuRL" reading notes, section 3: W X = (W / s)(s X))
+// quantises W' = fp32(W / s) instead: the same three kernels with kFold, which divide
+// every loaded weight by s (IEEE division) and derive the tensor and block scales from
+// fp32(amax / s) -- equal to the maximum of the divided values, since rounding a quotient
+// by a positive s is monotone.
+//
 // The quotient |w|/S decides a code only through which E2M1 rounding interval it
 // falls in.  k_quant therefore evaluates |w| * (1/S) scaled by (1 -+ 2^-21), a band
 // that provably brackets the correctly rounded quotient (reciprocal and products
@@ -85,11 +91,14 @@ PL_DEVINL void codes16(const float (&f)[16], float y, uint32_t& w0, uint32_t& w1
   w1 = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
 }
 
+template <bool kFold>
 __global__ void __launch_bounds__(kThreads) k_quant(const uint4* __restrict__ W, size_t n_blocks,
                                                     const uint32_t* __restrict__ amax_bits,
                                                     uint2* __restrict__ codes,
-                                                    uint8_t* __restrict__ scales) {
-  const float s_g = tensor_scale_from_amax(__uint_as_float(*amax_bits));
+                                                    uint8_t* __restrict__ scales, float fold_s) {
+  float amax_t = __uint_as_float(*amax_bits);
+  if constexpr (kFold) amax_t = __fdiv_rn(amax_t, fold_s);
+  const float s_g = tensor_scale_from_amax(amax_t);
   const float six_sg = __fmul_rn(6.0f, s_g);
   const size_t stride = static_cast<size_t>(gridDim.x) * kThreads;
   for (size_t b = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x; b < n_blocks; b += stride) {
@@ -103,7 +112,12 @@ __global__ void __launch_bounds__(kThreads) k_quant(const uint4* __restrict__ W,
       f[2 * i + 1] = bf16hi_to_f32(u[i]);
       am = max(am, absmax_bf16x2(u[i]));
     }
-    const float amax_b = __uint_as_float(am << 16);
+    float amax_b = __uint_as_float(am << 16);
+    if constexpr (kFold) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) f[i] = __fdiv_rn(f[i], fold_s);
+      amax_b = __fdiv_rn(amax_b, fold_s);
+    }
     const float t = __fdiv_rn(amax_b, six_sg);
     const uint32_t sb = cvt_e4m3x2(0.0f, t) & 0xFFu;
     const float S = __fmul_rn(s_g, e4m3_to_f32(sb));
@@ -138,17 +152,28 @@ __global__ void __launch_bounds__(kThreads) k_quant(const uint4* __restrict__ W,
   }
 }
 
-__global__ void k_finalize(float* s_g) {
+template <bool kFold>
+__global__ void k_finalize(float* s_g, float fold_s) {
   if (threadIdx.x == 0) {
-    const float amax = __uint_as_float(*reinterpret_cast<const uint32_t*>(s_g));
+    float amax = __uint_as_float(*reinterpret_cast<const uint32_t*>(s_g));
+    if constexpr (kFold) amax = __fdiv_rn(amax, fold_s);
     *s_g = tensor_scale_from_amax(amax);
   }
+}
+
+// The norm-scale half of the fold: w' = fp32(w * s), elementwise.
+__global__ void __launch_bounds__(kThreads) k_fold_norm(const float* __restrict__ w, int64_t d, float s,
+                                                        float* __restrict__ out) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < d; i += stride)
+    out[i] = __fmul_rn(w[i], s);
 }
 
 }  // namespace
 
 cudaError_t launch_quantize(const void* W, int64_t d_o, int64_t d_i, uint8_t* codes,
-                            uint8_t* scales, float* s_g, cudaStream_t stream) {
+                            uint8_t* scales, float* s_g, cudaStream_t stream, float fold_s) {
+  const bool fold = fold_s != 1.0f;  // W / 1 == W exactly: the plain kernels
   const size_t n = static_cast<size_t>(d_o) * static_cast<size_t>(d_i);
   const size_t n_vec = n / 8;        // 16-byte words of 8 bf16
   const size_t n_blocks = n / 16;    // 16-weight blocks
@@ -161,10 +186,24 @@ cudaError_t launch_quantize(const void* W, int64_t d_o, int64_t d_i, uint8_t* co
                                                              reinterpret_cast<uint32_t*>(s_g));
   size_t g2 = (n_blocks + kThreads - 1) / kThreads;
   g2 = g2 < 1 ? 1 : (g2 > static_cast<size_t>(sms) * 16 ? static_cast<size_t>(sms) * 16 : g2);
-  k_quant<<<static_cast<unsigned>(g2), kThreads, 0, stream>>>(
-      static_cast<const uint4*>(W), n_blocks, reinterpret_cast<const uint32_t*>(s_g),
-      reinterpret_cast<uint2*>(codes), scales);
-  k_finalize<<<1, 32, 0, stream>>>(s_g);
+  if (fold) {
+    k_quant<true><<<static_cast<unsigned>(g2), kThreads, 0, stream>>>(
+        static_cast<const uint4*>(W), n_blocks, reinterpret_cast<const uint32_t*>(s_g),
+        reinterpret_cast<uint2*>(codes), scales, fold_s);
+    k_finalize<true><<<1, 32, 0, stream>>>(s_g, fold_s);
+  } else {
+    k_quant<false><<<static_cast<unsigned>(g2), kThreads, 0, stream>>>(
+        static_cast<const uint4*>(W), n_blocks, reinterpret_cast<const uint32_t*>(s_g),
+        reinterpret_cast<uint2*>(codes), scales, 1.0f);
+    k_finalize<false><<<1, 32, 0, stream>>>(s_g, 1.0f);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fold_norm(const float* w, int64_t d, float s, float* out, cudaStream_t stream) {
+  int64_t g = (d + kThreads - 1) / kThreads;
+  g = g > 1024 ? 1024 : g;
+  k_fold_norm<<<static_cast<unsigned>(g), kThreads, 0, stream>>>(w, d, s, out);
   return cudaGetLastError();
 }
 

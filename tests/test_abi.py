@@ -131,6 +131,29 @@ def test_aqn_stage_and_sigma_follow_the_oracle(L):
     assert L.pl_aqn_sigma(3, 0.0, 0.0005) == -1.0 and L.pl_aqn_sigma(3, 0.01, float("inf")) == -1.0
 
 
+def test_uaq_argument_checks(L):
+    q = L.pl_nvfp4_quantize_uaq
+    ok = [_p(FAKE), 16, 32, ctypes.c_float(1.5), _p(FAKE), _p(FAKE), _p(FAKE), None]
+    a = list(ok); a[0] = None
+    assert q(*a) == 1
+    for i, v in ((2, 24), (1, 0), (3, ctypes.c_float(0.0)), (3, ctypes.c_float(-1.5)),
+                 (3, ctypes.c_float(float("inf")))):
+        a = list(ok); a[i] = v
+        assert q(*a) == 2, (i, v)
+    a = list(ok); a[0] = _p(FAKE + 8)
+    assert q(*a) == 3
+    f = L.pl_uaq_fold_norm
+    okf = [_p(FAKE), 256, ctypes.c_float(1.5), _p(FAKE), None]
+    a = list(okf); a[3] = None
+    assert f(*a) == 1
+    a = list(okf); a[1] = 0
+    assert f(*a) == 2
+    a = list(okf); a[2] = ctypes.c_float(float("nan"))
+    assert f(*a) == 2
+    a = list(okf); a[0] = _p(FAKE + 2)
+    assert f(*a) == 3
+
+
 def test_aqn_noise_argument_checks(L):
     f = L.pl_aqn_noise
     ok = [1, 0, 0, 1, 256, ctypes.c_float(0.01), _p(FAKE), None]
@@ -148,6 +171,8 @@ def test_valid_arguments_without_a_device_report_device_error(L):
     assert L.pl_nvfp4_lora_linear(*_lin_args()) == 5
     assert L.pl_nvfp4_quantize(_p(FAKE), 16, 32, _p(FAKE), _p(FAKE), _p(FAKE), None) == 5
     assert L.pl_aqn_noise(1, 0, 0, 1, 256, ctypes.c_float(0.01), _p(FAKE), None) == 5
+    assert L.pl_nvfp4_quantize_uaq(_p(FAKE), 16, 32, ctypes.c_float(1.5), _p(FAKE), _p(FAKE), _p(FAKE), None) == 5
+    assert L.pl_uaq_fold_norm(_p(FAKE), 256, ctypes.c_float(1.5), _p(FAKE), None) == 5
 
 
 def test_product_path_does_not_import_the_oracle():
