@@ -42,3 +42,19 @@ def test_reference_arm_world_2_prints_one_line_from_rank_0():
     assert l["impl"] == "reference" and l["n_gpus"] == 2 and l["steps"] == 2 and l["warmup"] == 3
     assert l["value"] > 0 and l["cpu_baseline"]["kind"] == "oracle"
     assert l["e2e"]["h2d_bytes_per_step"] == 0 and l["scaling"] == "weak"
+
+
+def test_reference_arm_single_process_line_contract():
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="", OMP_NUM_THREADS="1")
+    p = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "2", "--warmup", "3",
+                        "--workload", "tiny"], cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert p.returncode == 0, p.stderr[-4000:]
+    lines = [json.loads(l) for l in p.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    l = lines[0]
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+              "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e", "impl"):
+        assert k in l, k
+    assert l["n_gpus"] == 1 and l["impl"] == "reference" and l["higher_is_better"] is True
+    assert l["config"]["workload"] == "tiny" and l["cpu_baseline"]["value"] == l["value"]
+    assert l["e2e"]["value"] == l["value"] and l["e2e"]["unit"] == l["unit"]
