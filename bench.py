@@ -349,6 +349,13 @@ def run_ours(args, world, rank, local):
                                "frac": round(prefill["layer_TFLOPs"] / bf16_peak, 4), "peak_kind": bf16_kind,
                                "peak_note": "dense BF16 cuBLAS burst; the path computes in f16 (same tensor rate)"}
 
+    extras = None
+    if not args.no_extras:
+        try:
+            extras = bench_noise_and_fold(dev, stream)
+        except Exception as e:  # reported, never allowed to cost the line
+            extras = {"error": f"{type(e).__name__}: {e}"}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args, budget_s=args.cpu_seconds)
@@ -374,9 +381,62 @@ def run_ours(args, world, rank, local):
                          "traffic": profile_traffic("k_fused_decode" if paths[int(dom)] == 2 else "k_tc_decode",
                                                     f"{args.workload}/M{dom}")},
             "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, "layer_decode": layer_dec, "prefill": prefill,
+            "aqn_and_uaq": extras,
             "gpu_launches": sum(launches_per_call.values()) * args.steps,
         }
         print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------- AQN draw, UAQ fold
+def _graph_us(stream, fn, calls: int = 20, replays: int = 10) -> float:
+    """Mean us per call of fn(k) over CUDA graphs of `calls` calls (after one eager pass)."""
+    import torch
+    with torch.cuda.stream(stream):
+        for k in range(3):
+            fn(k)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for k in range(calls):
+                fn(k)
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(replays):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (calls * replays)
+
+
+def bench_noise_and_fold(dev, stream):
+    """The AQN noise draw (per norm state; 64 per-token states; 4096 per-token states of a
+    4096-token batch) and the UAQ-folded quantiser next to the plain one, on the 7B
+    shapes; us per call from CUDA graphs, GB/s of the bytes each writes or moves."""
+    import torch
+
+    from precision_linear_gb300 import binding as pl
+    from precision_linear_gb300 import synthetic
+
+    out = {"noise": {}, "quantize": {}}
+    for n, d in ((1, 3584), (64, 5120), (4096, 3584)):
+        z = torch.empty(n, d, dtype=torch.float32, device=dev)
+        us = _graph_us(stream, lambda k: pl.aqn_noise(d, 1, 0, k * n, n, 0.01, out=z))
+        out["noise"][f"{n}x{d}"] = {"us": round(us, 2), "GBps_written": round(4 * n * d / (us * 1e3), 1)}
+    for d_o, d_i in ((3584, 3584), (18944, 3584)):
+        W = synthetic.weight(d_o, d_i, seed=d_o + d_i).to(dev)
+        bufs = [pl.nvfp4_quantize(W) for _ in range(2)]
+        P = d_o * d_i
+        nbytes = 2 * P + 2 * P + 9 * P // 16  # the amax pass, the block pass, the packed output
+        plain = _graph_us(stream, lambda k: pl.nvfp4_quantize(W, *bufs[k % 2]), calls=10, replays=5)
+        fold = _graph_us(stream, lambda k: pl.nvfp4_quantize_uaq(W, 1.5, *bufs[k % 2]), calls=10, replays=5)
+        out["quantize"][f"{d_o}x{d_i}"] = {"plain_us": round(plain, 2), "uaq_us": round(fold, 2),
+                                           "plain_GBps": round(nbytes / (plain * 1e3), 1),
+                                           "uaq_GBps": round(nbytes / (fold * 1e3), 1)}
+        del W, bufs
+    torch.cuda.synchronize()
+    return out
 
 
 # ------------------------------------------------------------------------- 7B layer decode
@@ -580,6 +640,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the M=4096 layer-set measurement")
     ap.add_argument("--no-layer", action="store_true", help="skip the 7B decoder-layer decode measurement")
+    ap.add_argument("--no-extras", action="store_true", help="skip the AQN draw and UAQ quantiser timings")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
