@@ -17,7 +17,7 @@ Evidence Stops" (zhongzhuzhou.org):
   rollout, per response or per token).
 
 The pages leave open the stage boundaries, the distribution's details and the
-generator.  Readings taken here (each also listed in the design doc):
+generator.  Readings taken here:
 
 * stage = min(9, floor(10 * done / total)): ten stages of equal length, stage 0
   (the warm-up, sigma 0) first;

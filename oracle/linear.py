@@ -11,7 +11,7 @@ Evidence Stops", zhongzhuzhou.org):
   u = x / sqrt(d^-1 sum_j x_j^2 + delta),  h = u (.) w,  h_z = u (.) (w + z),
   and h_z W = h diag(1 + z/w) W  when every w_j != 0.
 
-Readings (listed in the design doc): the adapter acts on the same normalised, noised
+Readings taken here: the adapter acts on the same normalised, noised
 input h_z as the backbone; delta is a caller argument (1e-6 in the workloads);
 w + z is formed before the product, never by dividing by w.
 """

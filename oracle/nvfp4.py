@@ -12,8 +12,7 @@ Evidence Stops" (zhongzhuzhou.org), section 3.1 "What the four bits represent":
 * Storage: P/2 bytes of 4-bit payload + P/16 bytes of block scales = 9P/16.
 
 The pages leave open how s_g and s_b are chosen, the rounding of s_b, the tie
-rule, the nibble order and the block axis.  Readings taken here (each listed in
-the design doc with its reason):
+rule, the nibble order and the block axis.  Readings taken here:
 
 * s_g = fp32(amax_t / 2688) with 2688 = 6 * 448 (largest E2M1 magnitude times
   largest finite E4M3), so the block holding the tensor maximum gets s_b = 448;

@@ -7,7 +7,7 @@ invariant under W X = (W / s)(s X); the factor on the activations is absorbed by
 normalisation before it; the method picks s > 1 on purpose (s = 1.5 in its runs), once,
 before training, so that a weight update grows by s relative to the quantisation step.
 
-Readings (listed in the design doc): the fold divides the weight in FP32, W' = fp32(W / s),
+Readings taken here: the fold divides the weight in FP32, W' = fp32(W / s),
 before the fixed-scale quantiser of oracle.nvfp4, and multiplies the FP32 norm weight,
 w' = fp32(w * s); the AQN noise is drawn on the folded scale as before, h = u (.) (w' + z).
 """

@@ -7,7 +7,7 @@ quantised, theta_hat = Q(theta, b), weights with one scale per output channel an
 activations with one scale per token, in INT8 or FP8, and the rollout runs on INT8 /
 FP8 matrix products; the quantisation error is about |theta| / 2^b.
 
-Readings (listed in the design doc; the notes give no formula for Q):
+Readings taken here (the notes give no formula for Q):
 * symmetric absmax scales, no zero point: INT8 s = fp32(amax / 127), q = clip(RNE(fp32(v / s)),
   -127, 127); FP8 s = fp32(amax / 448), code = E4M3 of fp32(v / s) (round to nearest, ties
   to even, saturating at 448; sign bit separate, +0 for zero); s = 1 for an all-zero row;
