@@ -70,6 +70,14 @@ def test_schedule_values_for_table4_range():
     assert math.isclose(s[2], 0.01 * 0.05 ** 0.125, rel_tol=1e-15)
 
 
+def test_schedule_matches_the_printed_endpoints():
+    rows = [l.split() for l in open(os.path.join(ROOT, "tests", "golden", "aqn_schedule.txt"), encoding="utf-8")
+            if l.strip() and not l.startswith("#")]
+    assert len(rows) == 3
+    for start, end, k, want in rows:
+        assert math.isclose(aqn.sigma(int(k), float(start), float(end)), float(want), rel_tol=1e-15, abs_tol=0)
+
+
 def test_stage_rule():
     assert aqn.stage(0, 1000) == 0
     assert aqn.stage(99, 1000) == 0
