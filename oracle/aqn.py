@@ -112,6 +112,21 @@ def uniform(words) -> np.ndarray:
 # ----------------------------------------------------------------------------
 # Noise state
 # ----------------------------------------------------------------------------
+def box_muller(x0, x1, x2, x3):
+    """The four normals of one block from its four Philox words (arrays or scalars)."""
+    u0, u1, u2, u3 = uniform(x0), uniform(x1), uniform(x2), uniform(x3)
+    rho_a = np.sqrt(-2.0 * np.log(u0))
+    rho_b = np.sqrt(-2.0 * np.log(u2))
+    return (rho_a * np.cos(2.0 * math.pi * u1), rho_a * np.sin(2.0 * math.pi * u1),
+            rho_b * np.cos(2.0 * math.pi * u3), rho_b * np.sin(2.0 * math.pi * u3))
+
+
+def noise_block(seed: int, norm_id: int, scope: int, b: int):
+    """Channels 4b .. 4b+3 of the unit-sigma state of (seed, norm_id, scope), FP64."""
+    x = philox4x32_10((b, norm_id, scope & _MASK32, (scope >> 32) & _MASK32), (seed & _MASK32, (seed >> 32) & _MASK32))
+    return tuple(float(v) for v in box_muller(*(np.uint64(w) for w in x)))
+
+
 def noise(seed: int, norm_id: int, scope0: int, n_scopes: int, d: int, sig: float) -> np.ndarray:
     """z [n_scopes][d] (FP64): row s is the state of scope index scope0 + s of norm `norm_id`."""
     if d < 1 or n_scopes < 1:
@@ -125,11 +140,5 @@ def noise(seed: int, norm_id: int, scope0: int, n_scopes: int, d: int, sig: floa
         x0, x1, x2, x3 = philox4x32_10_array(blocks, np.full(nb, norm_id, np.uint64),
                                              np.full(nb, sc & _MASK32, np.uint64),
                                              np.full(nb, (sc >> 32) & _MASK32, np.uint64), k0, k1)
-        u0, u1, u2, u3 = uniform(x0), uniform(x1), uniform(x2), uniform(x3)
-        rho_a = np.sqrt(-2.0 * np.log(u0))
-        rho_b = np.sqrt(-2.0 * np.log(u2))
-        out[s, 0::4] = rho_a * np.cos(2.0 * math.pi * u1)
-        out[s, 1::4] = rho_a * np.sin(2.0 * math.pi * u1)
-        out[s, 2::4] = rho_b * np.cos(2.0 * math.pi * u3)
-        out[s, 3::4] = rho_b * np.sin(2.0 * math.pi * u3)
+        out[s, 0::4], out[s, 1::4], out[s, 2::4], out[s, 3::4] = box_muller(x0, x1, x2, x3)
     return float(sig) * out[:, :d]

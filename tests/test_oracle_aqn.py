@@ -39,6 +39,26 @@ def test_philox_known_answers():
         assert aqn.philox4x32_10(ctr, key) == want
 
 
+def test_counter_and_key_layout_through_a_known_answer():
+    """The third known-answer vector has six distinct words: read as seed = key (low word
+    first) and counter = (block, norm, scope low, scope high), the state's block must be
+    the Box-Muller transform of the vector's published output words, computed here by
+    hand from the definition (u = (2 (x >> 9) + 1) 2^-24)."""
+    ctr, key, out = _kat()[2]
+    seed = key[0] | (key[1] << 32)
+    scope = ctr[2] | (ctr[3] << 32)
+    got = aqn.noise_block(seed, ctr[1], scope, ctr[0])
+    u = [(2 * (w >> 9) + 1) * 2.0 ** -24 for w in out]
+    ra, rb = math.sqrt(-2 * math.log(u[0])), math.sqrt(-2 * math.log(u[2]))
+    want = (ra * math.cos(2 * math.pi * u[1]), ra * math.sin(2 * math.pi * u[1]),
+            rb * math.cos(2 * math.pi * u[3]), rb * math.sin(2 * math.pi * u[3]))
+    assert all(math.isclose(g, w, rel_tol=1e-14, abs_tol=1e-15) for g, w in zip(got, want))
+    # and the array draw agrees with the one-block form at small block indices
+    z = aqn.noise(seed, ctr[1], scope, 1, 64, 1.0)[0]
+    for b in (0, 5, 15):
+        assert np.allclose(z[4 * b:4 * b + 4], aqn.noise_block(seed, ctr[1], scope, b), rtol=0, atol=1e-15)
+
+
 def test_philox_array_form_matches_scalar_form():
     rng = np.random.default_rng(7)
     c = rng.integers(0, 2 ** 32, size=(4, 64), dtype=np.uint64)
