@@ -121,8 +121,10 @@ pl_status pl_nvfp4_quantize(const void* W_bf16, int64_t d_o, int64_t d_i,
  *   contract.  s == 1 is exactly pl_nvfp4_quantize.  Requirements as pl_nvfp4_quantize,
  *   plus s finite and > 0 (PL_ERR_SHAPE).
  * pl_uaq_fold_norm: out[i] = fp32(w_norm[i] * s), i < d (FP32 [d] in and out, device,
- *   4-byte aligned; out may equal w_norm).  The folded pair (W', w') gives the same layer
- *   up to the quantisation of W'. */
+ *   4-byte aligned; out may equal w_norm).  Requirements: 1 <= d <= 2^40, s finite and > 0
+ *   (PL_ERR_SHAPE), pointers non-NULL (PL_ERR_NULL) and 4-byte aligned (PL_ERR_ALIGN); one
+ *   kernel launch, asynchronous.  The folded pair (W', w') gives the same layer up to the
+ *   quantisation of W'. */
 pl_status pl_nvfp4_quantize_uaq(const void* W_bf16, int64_t d_o, int64_t d_i, float s,
                                 uint8_t* codes, uint8_t* scales, float* s_g, pl_stream_t stream);
 pl_status pl_uaq_fold_norm(const float* w_norm, int64_t d, float s, float* out, pl_stream_t stream);
