@@ -440,6 +440,22 @@ def bench_noise_and_fold(dev, stream):
 
 
 # ------------------------------------------------------------------------- 7B layer decode
+def layer_on_device(cases: dict, dev, keep_weights_on_host: bool = False) -> dict:
+    """synthetic.layer_case moved to the device, each distinct tensor once: the
+    projections that share a norm keep sharing one device copy of its input."""
+    moved = {}
+
+    def mv(t):
+        if t is None:
+            return None
+        if id(t) not in moved:
+            moved[id(t)] = t.to(dev)
+        return moved[id(t)]
+
+    return {name: {k: (v if (k == "W" and keep_weights_on_host) else mv(v)) for k, v in c.items()}
+            for name, c in cases.items()}
+
+
 def bench_layer_decode(dev, stream, replays: int = 20):
     """The Qwen2.5-7B-shaped decoder-layer projection set at decode batch sizes: the seven
     projections of one layer back to back (q/k/v on norm 1, gate/up on norm 2, o and down
@@ -455,17 +471,12 @@ def bench_layer_decode(dev, stream, replays: int = 20):
     Mmax = max(wl.Ms)
     ws = pl.Workspace(dev)
     ws.get(max(pl.workspace_bytes(M, p.d_i, p.d_o, r) for M in wl.Ms for p in wl.projs))
+    cases = layer_on_device(synthetic.layer_case(wl, 0, Mmax), dev)  # q/k/v and gate/up share their norm's input
     projs = []
-    for i, p in enumerate(wl.projs):
-        c = synthetic.projection_case(p.d_o, p.d_i, Mmax, r, wl.sigma, synthetic.proj_seed(wl, 0, i), 0.0,
-                                      device="cpu")
-        W = c["W"].to(dev)
-        codes, scales, s_g = pl.nvfp4_quantize(W)
-        del W
-        norm = p.norm is not None
-        projs.append(dict(p=p, norm=norm, copies=[(codes, scales, s_g), (codes.clone(), scales.clone(), s_g.clone())],
-                          x=c["x"].to(dev), A=c["A"].to(dev), B=c["B"].to(dev),
-                          w_norm=c["w_norm"].to(dev) if norm else None, z=c["z"].to(dev) if norm else None))
+    for p in wl.projs:
+        c = cases[p.name]
+        codes, scales, s_g = pl.nvfp4_quantize(c.pop("W"))
+        projs.append(dict(p=p, copies=[(codes, scales, s_g), (codes.clone(), scales.clone(), s_g.clone())], **c))
     torch.cuda.synchronize()
     out = {}
     with torch.cuda.stream(stream):
@@ -516,17 +527,14 @@ def bench_prefill(dev, stream, reps: int = 5, replays: int = 3):
     M, r = wl.Ms[0], wl.r
     ws = pl.Workspace(dev)
     out, tot_flops, tot_ms = {}, 0, 0.0
+    cases = layer_on_device(synthetic.layer_case(wl, 0, M), dev, keep_weights_on_host=True)
     with torch.cuda.stream(stream):
-        for i, p in enumerate(wl.projs):
-            c = synthetic.projection_case(p.d_o, p.d_i, M, r, wl.sigma, synthetic.proj_seed(wl, 0, i), 0.0,
-                                          device="cpu")
+        for p in wl.projs:
+            c = cases[p.name]
             W = c["W"].to(dev)
             codes, scales, s_g = pl.nvfp4_quantize(W)
             del W
-            x, A, B = c["x"].to(dev), c["A"].to(dev), c["B"].to(dev)
-            norm = p.norm is not None
-            w_norm = c["w_norm"].to(dev) if norm else None
-            z = c["z"].to(dev) if norm else None
+            x, A, B, w_norm, z = c["x"], c["A"], c["B"], c["w_norm"], c["z"]
             y = torch.empty(M, p.d_o, dtype=torch.bfloat16, device=dev)
             ws.get(pl.workspace_bytes(M, p.d_i, p.d_o, r))
 
@@ -556,6 +564,7 @@ def bench_prefill(dev, stream, reps: int = 5, replays: int = 3):
             tot_flops += fl
             tot_ms += ms
             del codes, scales, s_g, x, A, B, w_norm, z, y
+            cases[p.name] = None
     torch.cuda.synchronize()
     return {"workload": "prefill_7b (Qwen2.5-7B layer set, M=4096, r=32)", "M": M,
             "layer_us": round(tot_ms * 1e3, 1), "layer_TFLOPs": round(tot_flops / (tot_ms * 1e-3) / 1e12, 1),

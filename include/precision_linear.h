@@ -78,7 +78,8 @@ typedef enum pl_status {
 /* Static, human-readable name of a status code.  Never NULL. */
 const char* pl_status_string(pl_status status);
 
-/* ABI version of this header (major * 100 + minor). */
+/* ABI version of this header (major * 100 + minor): 200 (z_ld added to
+ * pl_rmsnorm_aqn and pl_nvfp4_lora_linear). */
 int pl_version(void);
 
 /* Bytes of the packed NVFP4 payload plus block scales for a [d_o, d_i] weight:
@@ -129,14 +130,25 @@ pl_status pl_nvfp4_quantize_uaq(const void* W_bf16, int64_t d_o, int64_t d_i, fl
                                 uint8_t* codes, uint8_t* scales, float* s_g, pl_stream_t stream);
 pl_status pl_uaq_fold_norm(const float* w_norm, int64_t d, float s, float* out, pl_stream_t stream);
 
+/* The AQN noise state z of a call (section 5.1 folds it into the norm scale; section 6,
+ * "A training algorithm that exposes the stochastic state", lets the caller declare its
+ * persistence scope: one state per rollout, per response or per token).
+ *  z NULL     : no noise.
+ *  z_ld == 0  : z is one FP32 vector [d], the state of every token row (per-rollout
+ *               scope, or any call whose rows share a state).
+ *  z_ld >= d  : z holds one FP32 vector per token row: row m's state starts at
+ *               z + m * z_ld (per-response or per-token scope in a batched call; e.g.
+ *               the [n_scopes][d] output of pl_aqn_noise with z_ld = d).
+ * z_ld must be 0 or a multiple of 4 that is >= d (else PL_ERR_SHAPE). */
+
 /* RMSNorm with AQN noise folded into the scale (section 5.1):
- *   h[m, :] = x[m, :] / sqrt(mean_j x[m, j]^2 + eps) (.) (w_norm + z)
- *  x_bf16 in : BF16 [M][d];  w_norm in: FP32 [d];  z in: FP32 [d] or NULL (no
- *  noise);  h out: [M][d] of h_dtype (BF16 rounds to nearest even).  w_norm + z
- *  is formed in FP32.  Requirements: M >= 1, d >= 8, d % 8 == 0, x and h 16-byte
- *  aligned, h_dtype a pl_dtype. */
+ *   h[m, :] = x[m, :] / sqrt(mean_j x[m, j]^2 + eps) (.) (w_norm + z_m)
+ *  x_bf16 in : BF16 [M][d];  w_norm in: FP32 [d];  z, z_ld: the noise state (above),
+ *  z_m its vector for row m;  h out: [M][d] of h_dtype (BF16 rounds to nearest even).
+ *  w_norm + z_m is formed in FP32.  Requirements: M >= 1, d >= 8, d % 8 == 0, x and h
+ *  16-byte aligned, z 16-byte aligned, h_dtype a pl_dtype. */
 pl_status pl_rmsnorm_aqn(const void* x_bf16, int64_t M, int64_t d,
-                         const float* w_norm, const float* z, float eps,
+                         const float* w_norm, const float* z, int64_t z_ld, float eps,
                          void* h, int h_dtype, pl_stream_t stream);
 
 /* The quantised-backbone LoRA linear (section 2.1 forward map, with the
@@ -147,7 +159,8 @@ pl_status pl_rmsnorm_aqn(const void* x_bf16, int64_t M, int64_t d,
  *  codes, scales, s_g in: NVFP4 weight [d_o][d_i] (layout above)
  *  A_bf16  in : BF16 [r][d_i], B_bf16 in: BF16 [d_o][r]; both NULL or r == 0
  *               means no adapter.
- *  w_norm, z in: FP32 [d_i] or NULL (z NULL = no noise; w_norm NULL = no norm)
+ *  w_norm  in : FP32 [d_i] or NULL (no norm: z is then ignored)
+ *  z, z_ld in : the noise state (above) over d = d_i
  *  y       out: [M][d_o] of y_dtype (a pl_dtype)
  *  workspace  : device scratch of at least pl_workspace_bytes(M, d_i, d_o, r).
  * Accumulation is FP32.  M <= 64 runs the decode path, larger M the prefill
@@ -157,7 +170,7 @@ pl_status pl_rmsnorm_aqn(const void* x_bf16, int64_t M, int64_t d,
 pl_status pl_nvfp4_lora_linear(const void* x_bf16, int64_t M, int64_t d_i, int64_t d_o,
                                const uint8_t* codes, const uint8_t* scales, const float* s_g,
                                const void* A_bf16, const void* B_bf16, int r, float lambda,
-                               const float* w_norm, const float* z, float eps,
+                               const float* w_norm, const float* z, int64_t z_ld, float eps,
                                void* y, int y_dtype, void* workspace, size_t workspace_bytes,
                                pl_stream_t stream);
 
@@ -176,7 +189,8 @@ pl_status pl_nvfp4_lora_linear(const void* x_bf16, int64_t M, int64_t d_i, int64
  * every device loading this library keeps until the process exits.
  *
  * Arguments, layouts, arithmetic and status codes are those of
- * pl_nvfp4_lora_linear; additionally PL_ERR_WORKSPACE is returned, with nothing
+ * pl_nvfp4_lora_linear with z_ld = 0 (one noise vector for every row); additionally
+ * PL_ERR_WORKSPACE is returned, with nothing
  * launched, when pl_workspace_bytes(M, d_i, d_o, r) exceeds
  * PL_STATIC_WORKSPACE_BYTES (e.g. M = 64 decode fits for d_i up to 28672).
  * The call allocates nothing.  Its first call on a device looks up the array's

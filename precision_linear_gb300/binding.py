@@ -41,11 +41,11 @@ _SIGNATURES = {
     "pl_nvfp4_bytes": (ctypes.c_size_t, [_i64, _i64]),
     "pl_workspace_bytes": (ctypes.c_size_t, [_i64, _i64, _i64, ctypes.c_int]),
     "pl_nvfp4_quantize": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
-    "pl_rmsnorm_aqn": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, ctypes.c_float,
+    "pl_rmsnorm_aqn": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, _i64, ctypes.c_float,
                                       _c_void_p, ctypes.c_int, _c_void_p]),
     "pl_nvfp4_lora_linear": (ctypes.c_int, [_c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p, _c_void_p,
                                             _c_void_p, _c_void_p, ctypes.c_int, ctypes.c_float,
-                                            _c_void_p, _c_void_p, ctypes.c_float, _c_void_p, ctypes.c_int,
+                                            _c_void_p, _c_void_p, _i64, ctypes.c_float, _c_void_p, ctypes.c_int,
                                             _c_void_p, ctypes.c_size_t, _c_void_p]),
     "pl_nvfp4_quantize_uaq": (ctypes.c_int, [_c_void_p, _i64, _i64, ctypes.c_float, _c_void_p, _c_void_p,
                                              _c_void_p, _c_void_p]),
@@ -112,6 +112,23 @@ def _need(t, name, dtype, device=None, dim=None):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _noise(z, M: int, d: int, dev):
+    """(z, z_ld) for the C ABI: a [d] vector is every row's state (z_ld = 0); a [M, d]
+    tensor (row stride a multiple of 4, unit column stride) gives row m its own state."""
+    if z is None:
+        return None, 0
+    if not isinstance(z, torch.Tensor) or z.dtype != torch.float32 or not z.is_cuda or z.device != dev:
+        raise TypeError(f"z must be a float32 tensor on {dev}")
+    if z.dim() == 1:
+        if z.shape[0] != d or not z.is_contiguous():
+            raise ValueError(f"z must be a contiguous vector of {d} elements")
+        return z, 0
+    if z.dim() != 2 or tuple(z.shape) != (M, d) or z.stride(1) != 1 or z.stride(0) < d or z.stride(0) % 4:
+        raise ValueError(f"per-row z must be [{M}, {d}] with unit column stride and a row stride that is a "
+                         "multiple of 4")
+    return z, int(z.stride(0))
+
+
 def nvfp4_bytes(d_o: int, d_i: int) -> int:
     return int(lib().pl_nvfp4_bytes(d_o, d_i))
 
@@ -171,12 +188,12 @@ def uaq_fold_norm(w_norm: torch.Tensor, s: float = 1.5, out: torch.Tensor | None
 def rmsnorm_aqn(x: torch.Tensor, w_norm: torch.Tensor, z: torch.Tensor | None = None,
                 eps: float = 1e-6, out: torch.Tensor | None = None,
                 out_dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
-    """h = x / sqrt(mean(x^2) + eps) * (w_norm + z) per row, BF16 or FP32 output."""
+    """h = x / sqrt(mean(x^2) + eps) * (w_norm + z_m) per row m, BF16 or FP32 output.
+    z: None, one [d] vector for every row, or [M, d] (one noise state per row)."""
     _need(x, "x", torch.bfloat16, dim=2)
     dev = x.device
     _need(w_norm, "w_norm", torch.float32, dev, 1)
-    if z is not None:
-        _need(z, "z", torch.float32, dev, 1)
+    z, z_ld = _noise(z, x.shape[0], x.shape[1], dev)
     if out is None:
         out = torch.empty(x.shape, dtype=out_dtype, device=dev)
     _need(out, "out", out.dtype, dev, 2)
@@ -184,7 +201,7 @@ def rmsnorm_aqn(x: torch.Tensor, w_norm: torch.Tensor, z: torch.Tensor | None = 
         raise TypeError("out must be bfloat16 or float32")
     M, d = x.shape
     with torch.cuda.device(dev):
-        st = lib().pl_rmsnorm_aqn(_ptr(x), M, d, _ptr(w_norm), _ptr(z), float(eps), _ptr(out),
+        st = lib().pl_rmsnorm_aqn(_ptr(x), M, d, _ptr(w_norm), _ptr(z), z_ld, float(eps), _ptr(out),
                                   _OUT_DTYPES[out.dtype], _stream(dev))
     _check(st, "pl_rmsnorm_aqn")
     return out
@@ -209,7 +226,8 @@ _default_ws = {}
 def nvfp4_lora_linear(x, codes, scales, s_g, A=None, B=None, lam: float = 0.0, w_norm=None, z=None,
                       eps: float = 1e-6, out=None, workspace: Workspace | None = None,
                       out_dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
-    """y = W_hat h + lam * B (A h) with h = RMSNorm_AQN(x) when w_norm is given (else x)."""
+    """y = W_hat h + lam * B (A h) with h = RMSNorm_AQN(x) when w_norm is given (else x).
+    z: None, one [d_i] noise vector for every row, or [M, d_i] (one noise state per row)."""
     _need(x, "x", torch.bfloat16, dim=2)
     dev = x.device
     _need(codes, "codes", torch.uint8, dev, 2)
@@ -224,8 +242,7 @@ def nvfp4_lora_linear(x, codes, scales, s_g, A=None, B=None, lam: float = 0.0, w
         r = A.shape[0]
     if w_norm is not None:
         _need(w_norm, "w_norm", torch.float32, dev, 1)
-    if z is not None:
-        _need(z, "z", torch.float32, dev, 1)
+    z, z_ld = _noise(z, M, d_i, dev)
     if out is None:
         out = torch.empty(M, d_o, dtype=out_dtype, device=dev)
     if out.dtype not in _OUT_DTYPES:
@@ -237,7 +254,7 @@ def nvfp4_lora_linear(x, codes, scales, s_g, A=None, B=None, lam: float = 0.0, w
     ws = workspace.get(need)
     with torch.cuda.device(dev):
         st = lib().pl_nvfp4_lora_linear(_ptr(x), M, d_i, d_o, _ptr(codes), _ptr(scales), _ptr(s_g),
-                                        _ptr(A), _ptr(B), r, float(lam), _ptr(w_norm), _ptr(z), float(eps),
+                                        _ptr(A), _ptr(B), r, float(lam), _ptr(w_norm), _ptr(z), z_ld, float(eps),
                                         _ptr(out), _OUT_DTYPES[out.dtype], _ptr(ws), ws.numel(), _stream(dev))
     _check(st, "pl_nvfp4_lora_linear")
     return out

@@ -13,6 +13,13 @@ std::atomic<int> g_fail_next_launch{0};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The noise state's row stride: 0 (one vector for every row) or a multiple of 4 that is
+// at least the row length, with every row's offset representable.
+bool z_ld_ok(int64_t z_ld, int64_t M, int64_t d) {
+  if (z_ld == 0) return true;
+  return z_ld >= d && z_ld % 4 == 0 && z_ld <= (int64_t{1} << 40) / (M > 0 ? M : 1);
+}
+
 pl_status check_launch(cudaError_t e) {
   if (g_fail_next_launch.exchange(0) != 0) return PL_ERR_CUDA;
   return e == cudaSuccess ? PL_OK : PL_ERR_CUDA;
@@ -78,7 +85,7 @@ const char* pl_status_string(pl_status s) {
   return "unknown pl_status";
 }
 
-int pl_version(void) { return 100; }
+int pl_version(void) { return 200; }
 
 size_t pl_nvfp4_bytes(int64_t d_o, int64_t d_i) {
   if (d_o < 1 || d_i < 16 || d_i % 16 != 0) return 0;
@@ -127,21 +134,22 @@ pl_status pl_uaq_fold_norm(const float* w_norm, int64_t d, float s, float* out, 
 }
 
 pl_status pl_rmsnorm_aqn(const void* x, int64_t M, int64_t d, const float* w_norm,
-                         const float* z, float eps, void* h, int h_dtype, pl_stream_t stream) {
+                         const float* z, int64_t z_ld, float eps, void* h, int h_dtype, pl_stream_t stream) {
   if (!x || !w_norm || !h) return PL_ERR_NULL;
   if (M < 1 || d < 8 || d % 8 != 0 || M > 0x7FFFFFFF) return PL_ERR_SHAPE;
   if (h_dtype != PL_DTYPE_BF16 && h_dtype != PL_DTYPE_F32) return PL_ERR_SHAPE;
-  if (!aligned16(x) || !aligned16(h)) return PL_ERR_ALIGN;
+  if (z && !z_ld_ok(z_ld, M, d)) return PL_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(h) || (z && !aligned16(z))) return PL_ERR_ALIGN;
   pl_status st = device_check();
   if (st != PL_OK) return st;
-  return check_launch(pl::launch_rmsnorm_aqn(x, M, d, w_norm, z, eps, h, h_dtype == PL_DTYPE_F32,
+  return check_launch(pl::launch_rmsnorm_aqn(x, M, d, w_norm, z, z ? z_ld : 0, eps, h, h_dtype == PL_DTYPE_F32,
                                              reinterpret_cast<cudaStream_t>(stream)));
 }
 
 pl_status pl_nvfp4_lora_linear(const void* x, int64_t M, int64_t d_i, int64_t d_o,
                                const uint8_t* codes, const uint8_t* scales, const float* s_g,
                                const void* A, const void* B, int r, float lambda,
-                               const float* w_norm, const float* z, float eps, void* y,
+                               const float* w_norm, const float* z, int64_t z_ld, float eps, void* y,
                                int y_dtype, void* workspace, size_t ws_bytes, pl_stream_t stream) {
   if (!x || !codes || !scales || !s_g || !y) return PL_ERR_NULL;
   if (M < 1 || d_o < 1 || d_i < 16 || d_i % 16 != 0 || M > (1ll << 24) || d_o > (1ll << 31) ||
@@ -149,6 +157,7 @@ pl_status pl_nvfp4_lora_linear(const void* x, int64_t M, int64_t d_i, int64_t d_
     return PL_ERR_SHAPE;
   if (y_dtype != PL_DTYPE_BF16 && y_dtype != PL_DTYPE_F32) return PL_ERR_SHAPE;
   if (r < 0 || r > 64) return PL_ERR_RANK;
+  if (w_norm && z && !z_ld_ok(z_ld, M, d_i)) return PL_ERR_SHAPE;
   const bool lora = r > 0 && A != nullptr && B != nullptr;
   if (r > 0 && (A == nullptr) != (B == nullptr)) return PL_ERR_NULL;
   if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || !aligned16(y) ||
@@ -160,7 +169,8 @@ pl_status pl_nvfp4_lora_linear(const void* x, int64_t M, int64_t d_i, int64_t d_
   pl_status st = device_check();
   if (st != PL_OK) return st;
   pl::LinearArgs a{x, M, d_i, d_o, codes, scales, s_g, lora ? A : nullptr, lora ? B : nullptr,
-                   lora ? r : 0, lambda, w_norm, w_norm ? z : nullptr, eps, y, y_dtype == PL_DTYPE_F32,
+                   lora ? r : 0, lambda, w_norm, w_norm ? z : nullptr, (w_norm && z) ? z_ld : 0, eps, y,
+                   y_dtype == PL_DTYPE_F32,
                    workspace, ws_bytes};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (pl::fused_supported(M, d_i, d_o, a.r)) return check_launch(pl::launch_linear_fused(a, s));

@@ -19,8 +19,10 @@ cudaError_t launch_quantize(const void* W, int64_t d_o, int64_t d_i, uint8_t* co
 cudaError_t launch_fold_norm(const float* w, int64_t d, float s, float* out, cudaStream_t stream);
 
 // ---- norm.cu
+// z_ld: 0 = one noise vector for every row, else row m's vector starts at z + m * z_ld.
 cudaError_t launch_rmsnorm_aqn(const void* x, int64_t M, int64_t d, const float* w_norm,
-                               const float* z, float eps, void* h, bool h_f32, cudaStream_t stream);
+                               const float* z, int64_t z_ld, float eps, void* h, bool h_f32,
+                               cudaStream_t stream);
 
 // Arguments of one linear call, shared by every path.
 struct LinearArgs {
@@ -34,7 +36,8 @@ struct LinearArgs {
   int r;
   float lambda;
   const float* w_norm;    // [d_i] or null
-  const float* z;         // [d_i] or null
+  const float* z;         // [d_i] (z_ld == 0) or [M] rows of z_ld floats, or null
+  int64_t z_ld;           // 0: one noise vector for every row; else elements between rows
   float eps;
   void* y;                // [M][d_o], bf16 or fp32
   bool y_f32;

@@ -39,11 +39,12 @@ GenericWs carve(void* ws, int64_t M, int64_t d_i) {
 
 __global__ void __launch_bounds__(kProThreads) k_prologue(const __nv_bfloat16* __restrict__ x, int64_t d_i,
                                                           const float* __restrict__ w_norm,
-                                                          const float* __restrict__ z, float eps,
-                                                          const __nv_bfloat16* __restrict__ A, int r,
-                                                          float* __restrict__ h, float* __restrict__ t) {
+                                                          const float* __restrict__ z, int64_t z_ld,
+                                                          float eps, const __nv_bfloat16* __restrict__ A,
+                                                          int r, float* __restrict__ h, float* __restrict__ t) {
   __shared__ float red[kProThreads / 32];
   const int64_t m = blockIdx.x;
+  if (z != nullptr) z += m * z_ld;  // this row's noise state (z_ld = 0: shared)
   const __nv_bfloat16* xr = x + m * d_i;
   float* hr = h + m * d_i;
   float inv = 1.0f;
@@ -169,7 +170,7 @@ cudaError_t launch_linear_generic(const LinearArgs& a, cudaStream_t stream) {
   GenericWs w = carve(a.ws, a.M, a.d_i);
   const bool lora = a.A != nullptr && a.B != nullptr && a.r > 0;
   k_prologue<<<static_cast<unsigned>(a.M), kProThreads, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(a.x), a.d_i, a.w_norm, a.z, a.eps,
+      static_cast<const __nv_bfloat16*>(a.x), a.d_i, a.w_norm, a.z, a.z_ld, a.eps,
       lora ? static_cast<const __nv_bfloat16*>(a.A) : nullptr, lora ? a.r : 0, w.h, w.t);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

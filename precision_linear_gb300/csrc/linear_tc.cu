@@ -146,9 +146,12 @@ constexpr int kActUnroll = 4;                // loads per thread in flight in th
 // CTAs n_row_ctas and up: the f16 copy of A (r x d_i), 8 elements per thread and slot, and
 // zeros into `zero` (n_zero floats, a multiple of 4; the accumulator of the large-M
 // LoRA down-projection), 4 per thread and slot.
+// kRowZ: z holds one noise vector per token row (z_ld floats apart), added to w_norm as
+// each row is taken; otherwise w_norm + z is formed once, in shared memory.
+template <bool kRowZ>
 __global__ void __launch_bounds__(kActThreads, 2) k_act(const __nv_bfloat16* __restrict__ x, int64_t M, int64_t d_i,
                                                      const float* __restrict__ w_norm,
-                                                     const float* __restrict__ z, float eps,
+                                                     const float* __restrict__ z, int64_t z_ld, float eps,
                                                      __half* __restrict__ hq, float* __restrict__ rowscale,
                                                      const __nv_bfloat16* __restrict__ A, int r,
                                                      __half* __restrict__ A16, float* __restrict__ zero,
@@ -187,7 +190,9 @@ __global__ void __launch_bounds__(kActThreads, 2) k_act(const __nv_bfloat16* __r
       reinterpret_cast<float4*>(zero)[sl] = make_float4(0.f, 0.f, 0.f, 0.f);
     return;
   }
-  const bool norm = w_norm != nullptr, noise = norm && z != nullptr;
+  const bool norm = w_norm != nullptr, noise = !kRowZ && norm && z != nullptr;
+  // one noise vector per token row: added row by row below, w_norm alone in g4
+  const float* zrows = (kRowZ && norm) ? z : nullptr;
   const int64_t n4 = d_i / 4;
   for (int64_t i0 = threadIdx.x; i0 < n4; i0 += kActUnroll * kActThreads) {
     float4 g[kActUnroll], zz[kActUnroll];
@@ -220,6 +225,19 @@ __global__ void __launch_bounds__(kActThreads, 2) k_act(const __nv_bfloat16* __r
     const int64_t m = rd * per_round + static_cast<int64_t>(blockIdx.x) * rows_cta + grp;
     const bool live = m < M;
     const uint4* xr = reinterpret_cast<const uint4*>(x + (live ? m : 0) * d_i);
+    const float4* zr = kRowZ && zrows != nullptr ? reinterpret_cast<const float4*>(zrows + (live ? m : 0) * z_ld)
+                                                  : nullptr;
+    // w_norm + z of this row for piece q (8 channels)
+    auto gpiece = [&](int64_t q, float (&g8)[8]) {
+      float4 ga = g4[2 * q], gb = g4[2 * q + 1];
+      if (kRowZ && zr != nullptr) {
+        const float4 za = zr[2 * q], zb = zr[2 * q + 1];
+        ga.x += za.x; ga.y += za.y; ga.z += za.z; ga.w += za.w;
+        gb.x += zb.x; gb.y += zb.y; gb.z += zb.z; gb.w += zb.w;
+      }
+      g8[0] = ga.x; g8[1] = ga.y; g8[2] = ga.z; g8[3] = ga.w;
+      g8[4] = gb.x; g8[5] = gb.y; g8[6] = gb.z; g8[7] = gb.w;
+    };
     uint4 xv[kActPieces];
 #pragma unroll
     for (int i = 0; i < kActPieces; ++i) {
@@ -231,8 +249,8 @@ __global__ void __launch_bounds__(kActThreads, 2) k_act(const __nv_bfloat16* __r
     for (int i = 0; i < kActPieces; ++i) {
       const int64_t q = gt + static_cast<int64_t>(i) * gstride;
       if (q < nv8) {
-        const float4 ga = g4[2 * q], gb = g4[2 * q + 1];
-        const float g8[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+        float g8[8];
+        gpiece(q, g8);
         const uint32_t w4[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -274,11 +292,12 @@ __global__ void __launch_bounds__(kActThreads, 2) k_act(const __nv_bfloat16* __r
       const int64_t q = gt + static_cast<int64_t>(i) * gstride;
       if (q < nv8) {
         const uint4 v = xv[i];
-        const float4 ga = g4[2 * q], gb = g4[2 * q + 1];
-        hr[q] = make_uint4(f32x2_to_f16x2(bf16lo_to_f32(v.x) * ga.x * f, bf16hi_to_f32(v.x) * ga.y * f),
-                           f32x2_to_f16x2(bf16lo_to_f32(v.y) * ga.z * f, bf16hi_to_f32(v.y) * ga.w * f),
-                           f32x2_to_f16x2(bf16lo_to_f32(v.z) * gb.x * f, bf16hi_to_f32(v.z) * gb.y * f),
-                           f32x2_to_f16x2(bf16lo_to_f32(v.w) * gb.z * f, bf16hi_to_f32(v.w) * gb.w * f));
+        float g8[8];
+        gpiece(q, g8);
+        hr[q] = make_uint4(f32x2_to_f16x2(bf16lo_to_f32(v.x) * g8[0] * f, bf16hi_to_f32(v.x) * g8[1] * f),
+                           f32x2_to_f16x2(bf16lo_to_f32(v.y) * g8[2] * f, bf16hi_to_f32(v.y) * g8[3] * f),
+                           f32x2_to_f16x2(bf16lo_to_f32(v.z) * g8[4] * f, bf16hi_to_f32(v.z) * g8[5] * f),
+                           f32x2_to_f16x2(bf16lo_to_f32(v.w) * g8[6] * f, bf16hi_to_f32(v.w) * g8[7] * f));
       }
     }
   }
@@ -749,7 +768,9 @@ cudaError_t set_kernel_attributes() {
   std::call_once(once, [] {
     err = cudaFuncSetAttribute(k_tc_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(k_act, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+      err = cudaFuncSetAttribute(k_act<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(k_act<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
   });
   return err;
 }
@@ -931,7 +952,9 @@ cudaError_t launch_act_prologue(const LinearArgs& a, __half* hq, float* rowscale
   c.stream = stream;
   c.attrs = attr;
   c.numAttrs = 1;
-  return cudaLaunchKernelEx(&c, k_act, static_cast<const __nv_bfloat16*>(a.x), a.M, a.d_i, a.w_norm, a.z, a.eps, hq,
+  auto* kern = (a.z != nullptr && a.z_ld != 0) ? k_act<true> : k_act<false>;
+  return cudaLaunchKernelEx(&c, kern, static_cast<const __nv_bfloat16*>(a.x), a.M, a.d_i, a.w_norm, a.z, a.z_ld,
+                            a.eps, hq,
                             rowscale, static_cast<const __nv_bfloat16*>(a.A), a.r, A16, zero, n_zero, n_row_ctas,
                             wpr);
 }

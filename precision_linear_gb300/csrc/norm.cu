@@ -30,11 +30,12 @@ PL_DEVINL float block_sum(float v, float* red) {
 template <bool kF32>
 __global__ void __launch_bounds__(kThreads) k_rmsnorm_aqn(const uint4* __restrict__ x, int64_t d,
                                                           const float* __restrict__ w_norm,
-                                                          const float* __restrict__ z, float eps,
-                                                          void* __restrict__ h) {
+                                                          const float* __restrict__ z, int64_t z_ld,
+                                                          float eps, void* __restrict__ h) {
   __shared__ float red[kThreads / 32];
   const int64_t nv = d / 8;
   const uint4* xr = x + blockIdx.x * nv;
+  if (z != nullptr) z += static_cast<int64_t>(blockIdx.x) * z_ld;  // this row's noise state
   float ss = 0.f;
   for (int64_t i = threadIdx.x; i < nv; i += kThreads) {
     const uint4 v = xr[i];
@@ -82,13 +83,14 @@ __global__ void __launch_bounds__(kThreads) k_rmsnorm_aqn(const uint4* __restric
 }  // namespace
 
 cudaError_t launch_rmsnorm_aqn(const void* x, int64_t M, int64_t d, const float* w_norm,
-                               const float* z, float eps, void* h, bool h_f32, cudaStream_t stream) {
+                               const float* z, int64_t z_ld, float eps, void* h, bool h_f32,
+                               cudaStream_t stream) {
   if (h_f32)
     k_rmsnorm_aqn<true><<<static_cast<unsigned>(M), kThreads, 0, stream>>>(
-        static_cast<const uint4*>(x), d, w_norm, z, eps, h);
+        static_cast<const uint4*>(x), d, w_norm, z, z_ld, eps, h);
   else
     k_rmsnorm_aqn<false><<<static_cast<unsigned>(M), kThreads, 0, stream>>>(
-        static_cast<const uint4*>(x), d, w_norm, z, eps, h);
+        static_cast<const uint4*>(x), d, w_norm, z, z_ld, eps, h);
   return cudaGetLastError();
 }
 

@@ -55,6 +55,6 @@ extern "C" pl_status pl_nvfp4_lora_linear_static_ws(
   }
   // Nothing in the scratch has to start at zero: the kernels write every byte of it
   // that they later read, within the same call.
-  return pl_nvfp4_lora_linear(x, M, d_i, d_o, codes, scales, s_g, A, B, r, lambda, w_norm, z, eps, y, y_dtype,
+  return pl_nvfp4_lora_linear(x, M, d_i, d_o, codes, scales, s_g, A, B, r, lambda, w_norm, z, 0, eps, y, y_dtype,
                               ws, static_cast<size_t>(PL_STATIC_WORKSPACE_BYTES), stream);
 }

@@ -127,3 +127,40 @@ def proj_seed(wl: Workload, layer: int, proj_index: int) -> int:
     """Seed of one projection of one layer of a workload."""
     base = 5000 + layer if wl.layers > 1 else wl.seed
     return base * 16 + proj_index
+
+
+NORMS = ("attn", "ffn")
+
+
+def norm_seed(wl: Workload, layer: int, norm: str) -> int:
+    """Seed of the input shared by the projections that read one RMSNorm of a layer."""
+    base = 5000 + layer if wl.layers > 1 else wl.seed
+    return base * 16 + 8 + NORMS.index(norm)
+
+
+def layer_case(wl: Workload, layer: int, M: int, device="cpu") -> dict:
+    """Every input of one decoder layer's projections, wired as in the layer.
+
+    The projections behind one RMSNorm read the same tensors: q, k and v take one
+    (x, w_norm, z) -- the attention norm's input, scale and noise state -- and gate and
+    up take the FFN norm's; o and down take plain BF16 inputs of their own (the attention
+    output and the SwiGLU product, outside this path, replaced by seeded draws).  Each
+    projection has its own weight and adapter.  Returns {name: case dict}; the shared
+    entries are the same tensor objects."""
+    shared = {}
+    for nm in NORMS:
+        p0 = next(p for p in wl.projs if p.norm == nm)
+        sd = norm_seed(wl, layer, nm)
+        shared[nm] = dict(x=activations(M, p0.d_i, sd, device), w_norm=norm_scale(p0.d_i, sd, device),
+                          z=noise(p0.d_i, wl.sigma, sd, device))
+    out = {}
+    for i, p in enumerate(wl.projs):
+        sd = proj_seed(wl, layer, i)
+        A, B = lora(p.d_o, p.d_i, wl.r, sd, device)
+        c = dict(W=weight(p.d_o, p.d_i, sd, wl.outlier_frac, device), A=A, B=B)
+        if p.norm is not None:
+            c.update(shared[p.norm])
+        else:
+            c.update(x=activations(M, p.d_i, sd, device), w_norm=None, z=None)
+        out[p.name] = c
+    return out

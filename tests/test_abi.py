@@ -38,7 +38,7 @@ def test_status_strings_and_version(L):
         txt = L.pl_status_string(s).decode()
         assert txt.startswith("PL_")
     assert L.pl_status_string(99).decode() == "unknown pl_status"
-    assert L.pl_version() == 100
+    assert L.pl_version() == 200
 
 
 def test_nvfp4_bytes_is_9P_over_16(L):
@@ -71,25 +71,32 @@ def test_quantize_argument_checks(L):
 
 
 def test_rmsnorm_argument_checks(L):
-    args = [_p(FAKE), 4, 256, _p(FAKE), None, ctypes.c_float(1e-6), _p(FAKE), 0, None]
+    args = [_p(FAKE), 4, 256, _p(FAKE), None, 0, ctypes.c_float(1e-6), _p(FAKE), 0, None]
     a = list(args); a[0] = None
     assert L.pl_rmsnorm_aqn(*a) == 1
     a = list(args); a[2] = 250
     assert L.pl_rmsnorm_aqn(*a) == 2
-    a = list(args); a[6] = _p(FAKE + 2)
+    a = list(args); a[7] = _p(FAKE + 2)
     assert L.pl_rmsnorm_aqn(*a) == 3
-    a = list(args); a[7] = 2  # not a pl_dtype
+    a = list(args); a[8] = 2  # not a pl_dtype
     assert L.pl_rmsnorm_aqn(*a) == 2
+    # per-row noise: the row stride must be 0 or a multiple of 4 that is >= d
+    for z_ld in (128, 258, -256):
+        a = list(args); a[4] = _p(FAKE); a[5] = z_ld
+        assert L.pl_rmsnorm_aqn(*a) == 2, z_ld
+    a = list(args); a[4] = _p(FAKE + 4); a[5] = 256
+    assert L.pl_rmsnorm_aqn(*a) == 3  # z rows must start 16-byte aligned
 
 
 def _lin_args(**kw):
     d = dict(x=FAKE, M=4, d_i=256, d_o=256, codes=FAKE, scales=FAKE, s_g=FAKE, A=FAKE, B=FAKE, r=8,
-             lam=2.0, w_norm=FAKE, z=FAKE, eps=1e-6, y=FAKE, y_dtype=0, ws=FAKE, ws_bytes=1 << 30, stream=None)
+             lam=2.0, w_norm=FAKE, z=FAKE, z_ld=0, eps=1e-6, y=FAKE, y_dtype=0, ws=FAKE, ws_bytes=1 << 30,
+             stream=None)
     d.update(kw)
     return [_p(d["x"]) if d["x"] else None, d["M"], d["d_i"], d["d_o"], _p(d["codes"]) if d["codes"] else None,
             _p(d["scales"]), _p(d["s_g"]), _p(d["A"]) if d["A"] else None, _p(d["B"]) if d["B"] else None,
             d["r"], ctypes.c_float(d["lam"]), _p(d["w_norm"]) if d["w_norm"] else None,
-            _p(d["z"]) if d["z"] else None, ctypes.c_float(d["eps"]), _p(d["y"]), d["y_dtype"],
+            _p(d["z"]) if d["z"] else None, d["z_ld"], ctypes.c_float(d["eps"]), _p(d["y"]), d["y_dtype"],
             _p(d["ws"]) if d["ws"] else None, d["ws_bytes"], d["stream"]]
 
 
@@ -108,6 +115,9 @@ def test_linear_argument_checks(L):
     assert f(*_lin_args(ws_bytes=16)) == 7
     assert f(*_lin_args(ws=FAKE + 16)) == 7  # workspace must be 256-byte aligned
     assert f(*_lin_args(y_dtype=5)) == 2
+    assert f(*_lin_args(z_ld=100)) == 2  # per-row noise rows shorter than d_i
+    assert f(*_lin_args(z_ld=258)) == 2  # row stride not a multiple of 4
+    assert f(*_lin_args(z_ld=-256)) == 2
 
 
 def test_aqn_stage_and_sigma_follow_the_oracle(L):
@@ -169,6 +179,8 @@ def test_aqn_noise_argument_checks(L):
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
 def test_valid_arguments_without_a_device_report_device_error(L):
     assert L.pl_nvfp4_lora_linear(*_lin_args()) == 5
+    assert L.pl_nvfp4_lora_linear(*_lin_args(z_ld=256)) == 5
+    assert L.pl_rmsnorm_aqn(_p(FAKE), 4, 256, _p(FAKE), _p(FAKE), 256, ctypes.c_float(1e-6), _p(FAKE), 0, None) == 5
     assert L.pl_nvfp4_quantize(_p(FAKE), 16, 32, _p(FAKE), _p(FAKE), _p(FAKE), None) == 5
     assert L.pl_aqn_noise(1, 0, 0, 1, 256, ctypes.c_float(0.01), _p(FAKE), None) == 5
     assert L.pl_nvfp4_quantize_uaq(_p(FAKE), 16, 32, ctypes.c_float(1.5), _p(FAKE), _p(FAKE), _p(FAKE), None) == 5

@@ -84,35 +84,58 @@ def test_tc_path_shapes(cuda_ok, d_o, d_i, M, r):
     _check(d_o, d_i, M, r, seed=d_o + M + r, lora=r > 0)
 
 
+def _layer_on_device(cases):
+    """synthetic.layer_case on the device, the shared norm inputs moved once (still shared)."""
+    moved = {}
+
+    def mv(t):
+        if t is None:
+            return None
+        if id(t) not in moved:
+            moved[id(t)] = t.to(DEV)
+        return moved[id(t)]
+
+    return {n: {k: mv(v) for k, v in c.items()} for n, c in cases.items()}
+
+
+def _check_layer(wl, layer, M, rows=None, key=""):
+    """Every projection of one decoder layer, wired as in the layer (q/k/v read the attention
+    norm's x, w_norm and z; gate/up the FFN norm's), against the oracle; rows: the token rows
+    compared (all when None)."""
+    cases = _layer_on_device(synthetic.layer_case(wl, layer, M))
+    assert cases["q"]["x"] is cases["k"]["x"] is cases["v"]["x"]
+    assert cases["gate"]["z"] is cases["up"]["z"] and cases["gate"]["x"] is not cases["q"]["x"]
+    for p in wl.projs:
+        c = cases[p.name]
+        norm = p.norm is not None
+        packed, sb, s_g = oracle_quantize_cached((wl.name, layer, p.name), c["W"])
+        y = _run(c, to_dev_nvfp4(packed, sb, s_g), wl.lam, norm=norm)
+        ref = oracle_linear(c, packed, sb, s_g, wl.lam, norm=norm, rows=rows)
+        if rows is not None:
+            y = y[torch.from_numpy(rows).to(DEV)]
+        assert_linear_close(y, ref, f"{wl.name} layer {layer} {p.name} M={M} {key}")
+
+
 @pytest.mark.parametrize("M", [8, 32, 64])
 def test_7b_layer_set(cuda_ok, M):
-    wl = synthetic.WORKLOADS["layer_7b"]
-    for i, p in enumerate(wl.projs):
-        norm = p.norm is not None
-        _check(p.d_o, p.d_i, M, wl.r, wl.lam, seed=synthetic.proj_seed(wl, 0, i), norm=norm)
+    _check_layer(synthetic.WORKLOADS["layer_7b"], 0, M)
 
 
 def test_7b_layer_prefill_m4096_sampled_rows(cuda_ok):
+    """M = 4096: two full 128-token tiles (the first and one in the middle) and a spread of
+    other rows of every projection."""
     wl = synthetic.WORKLOADS["prefill_7b"]
     M = wl.Ms[0]
-    rows = np.random.default_rng(0).choice(M, 48, replace=False)
-    rows.sort()
-    for i, p in enumerate(wl.projs):
-        norm = p.norm is not None
-        case = make_case(p.d_o, p.d_i, M, wl.r, wl.sigma, synthetic.proj_seed(wl, 0, i))
-        packed, sb, s_g = oracle_quantize(case["W"])
-        y = _run(case, to_dev_nvfp4(packed, sb, s_g), wl.lam, norm=norm)
-        ref = oracle_linear(case, packed, sb, s_g, wl.lam, norm=norm, rows=rows)
-        assert_linear_close(y[torch.from_numpy(rows).to(DEV)], ref, f"prefill {p.name}")
+    rows = np.unique(np.concatenate([np.arange(0, 128), np.arange(2048, 2176),
+                                     np.random.default_rng(0).choice(M, 48, replace=False)]))
+    _check_layer(wl, 0, M, rows=rows)
 
 
-def test_32b_stack_sampled_layer(cuda_ok):
+@pytest.mark.parametrize("layer", [0, 31, 63])
+def test_32b_stack_sampled_layer(cuda_ok, layer):
     wl = synthetic.WORKLOADS["stack_32b"]
-    for i, p in enumerate(wl.projs):
-        for M in wl.Ms:
-            norm = p.norm is not None
-            _check(p.d_o, p.d_i, M, wl.r, wl.lam, seed=synthetic.proj_seed(wl, 31, i), sigma=wl.sigma,
-                   norm=norm)
+    for M in wl.Ms:
+        _check_layer(wl, layer, M)
 
 
 def test_end_to_end_gpu_quantiser_into_linear(cuda_ok):

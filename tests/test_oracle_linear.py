@@ -115,3 +115,22 @@ def test_lora_branch_and_no_norm_path():
     # no norm: the backbone acts on x itself
     yn = linear.nvfp4_lora_linear(c["x"], packed, sb, s_g, None, None, 0.0)
     assert np.allclose(yn, c["x"] @ nvfp4.dequantize(packed, sb, s_g).T, rtol=1e-12, atol=1e-14)
+
+
+def test_rmsnorm_per_row_states_brute_force():
+    """One noise state per token row (the per-response / per-token persistence scope of
+    section 6): row m of the oracle equals a pure-Python evaluation of
+    x_m / sqrt(mean(x_m^2) + eps) * (w + z_m), and a wrong row pairing is caught."""
+    rng = np.random.default_rng(11)
+    M, d, eps = 4, 7, 1e-6
+    x = rng.normal(size=(M, d))
+    w = 1.0 + 0.1 * rng.normal(size=d)
+    z = 1e-2 * rng.normal(size=(M, d))
+    got = linear.rmsnorm_aqn(x, w, z, eps)
+    for m in range(M):
+        ms = sum(float(v) * float(v) for v in x[m]) / d
+        inv = 1.0 / math.sqrt(ms + eps)
+        for j in range(d):
+            assert math.isclose(got[m, j], float(x[m, j]) * inv * (float(w[j]) + float(z[m, j])), rel_tol=1e-14)
+    swapped = linear.rmsnorm_aqn(x, w, z[::-1], eps)
+    assert np.max(np.abs(swapped - got)) > 1e-4
