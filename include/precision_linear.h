@@ -174,6 +174,73 @@ pl_status pl_nvfp4_lora_linear(const void* x_bf16, int64_t M, int64_t d_i, int64
                                void* y, int y_dtype, void* workspace, size_t workspace_bytes,
                                pl_stream_t stream);
 
+/* A group of projections that read the same input: in a decoder layer the projections
+ * behind one RMSNorm (q, k and v behind the attention norm; gate and up behind the FFN
+ * norm) share x, w_norm and the noise state z (QeRL section 5.1, "Deriving the RMSNorm
+ * identity": one noise vector is folded into each norm, so Q, K and V share one and
+ * Gate and Up the other).  One projection of a group: */
+typedef struct pl_nvfp4_proj {
+  int64_t d_o;             /* output features of this projection                        */
+  const uint8_t* codes;    /* NVFP4 weight [d_o][d_i] (layout above)                     */
+  const uint8_t* scales;
+  const float* s_g;        /* device scalar                                               */
+  const void* A_bf16;      /* BF16 [r][d_i] or NULL (with B_bf16 NULL or r == 0: no adapter) */
+  const void* B_bf16;      /* BF16 [d_o][r] or NULL                                       */
+  int r;                   /* 0 .. 64                                                     */
+  float lambda;
+  void* y;                 /* [M][d_o] of the group's y_dtype                             */
+} pl_nvfp4_proj;
+
+/* Most projections in one group call. */
+#define PL_MAX_GROUP 8
+
+/* Workspace bytes pl_nvfp4_lora_linear_group needs (0 for an invalid group). */
+size_t pl_workspace_bytes_group(int64_t M, int64_t d_i, const pl_nvfp4_proj* projs, int n_proj);
+
+/* pl_nvfp4_lora_linear of every projection of `projs` on the same x, w_norm, z, z_ld and
+ * eps: y_p = W_hat_p h + lambda_p B_p (A_p h), h = RMSNorm_AQN(x) (x when w_norm is NULL).
+ * Results equal those of separate calls within the linear's tolerance.  For decode batch
+ * sizes (M <= 64, d_i % 256 == 0, at most 4 projections, sum of ranks <= 128) the group
+ * runs as one prologue (h once, t_p = A_p h once per projection) and one main kernel over
+ * the weight tiles of all projections; otherwise the projections run one after another.
+ * Requirements: those of pl_nvfp4_lora_linear for every projection, 1 <= n_proj <=
+ * PL_MAX_GROUP; the y buffers must not overlap one another or any input.  `projs` is a
+ * HOST array, read during the call only. */
+pl_status pl_nvfp4_lora_linear_group(const void* x_bf16, int64_t M, int64_t d_i,
+                                     const float* w_norm, const float* z, int64_t z_ld, float eps,
+                                     const pl_nvfp4_proj* projs, int n_proj, int y_dtype,
+                                     void* workspace, size_t workspace_bytes, pl_stream_t stream);
+
+/* W8A8 rollout linear ("QuRL: Low-Precision Reinforcement Learning for Efficient
+ * Reasoning", reading notes, "method / overall framework": the actor is quantised before
+ * rollout with one scale per output channel for the weights and one per token for the
+ * activations, INT8 or FP8; rollout runs on 8-bit matrix products).  This library takes the
+ * FP8 E4M3 form (the 8-bit tensor-core rate of this part).  Symmetric absmax scales, no
+ * zero point:
+ *   s_w[o] = max_k |W[o, k]| / 448,  q_w = E4M3(W / s_w)       (pl_w8a8_quantize_weight)
+ *   s_x[m] = max_k |h[m, k]| / 448,  q_x = E4M3(h / s_x),  h = RMSNorm_AQN(x)
+ *   y[m, o] = s_x[m] s_w[o] sum_k q_x[m, k] q_w[o, k] + lambda sum_j B[o, j] (A h)[m, j]
+ * with the adapter on the unquantised h, as on the NVFP4 path.  FP32 IEEE arithmetic for the
+ * scales and quotients, round to nearest even onto E4M3, saturating at 448, +0 for values
+ * that round to zero, s = 1 for an all-zero row.
+ *
+ * pl_w8a8_quantize_weight: W_bf16 BF16 [d_o][d_i] in; codes uint8 [d_o][d_i] and s_w FP32
+ *   [d_o] out (device).  Bit-exact contract.  Requirements: d_o >= 1, d_i >= 16, d_i % 16 == 0,
+ *   W and codes 16-byte aligned, s_w 4-byte aligned.  One kernel launch.
+ * pl_w8a8_lora_linear: arguments as pl_nvfp4_lora_linear, with the weight given as codes and
+ *   s_w.  Requirements: 1 <= M <= 2^24, 128 <= d_i <= 32768, d_i % 128 == 0, 0 <= r <= 64,
+ *   alignment as pl_nvfp4_lora_linear, a workspace of pl_w8a8_workspace_bytes.  Two kernel
+ *   launches (activation prologue, FP8 tensor-core GEMM), asynchronous. */
+size_t pl_w8a8_workspace_bytes(int64_t M, int64_t d_i, int64_t d_o, int r);
+pl_status pl_w8a8_quantize_weight(const void* W_bf16, int64_t d_o, int64_t d_i, uint8_t* codes, float* s_w,
+                                  pl_stream_t stream);
+pl_status pl_w8a8_lora_linear(const void* x_bf16, int64_t M, int64_t d_i, int64_t d_o,
+                              const uint8_t* codes, const float* s_w,
+                              const void* A_bf16, const void* B_bf16, int r, float lambda,
+                              const float* w_norm, const float* z, int64_t z_ld, float eps,
+                              void* y, int y_dtype, void* workspace, size_t workspace_bytes,
+                              pl_stream_t stream);
+
 /* Bytes of the scratch array behind pl_nvfp4_lora_linear_static_ws. */
 #define PL_STATIC_WORKSPACE_BYTES ((size_t)8 << 20)
 

@@ -35,6 +35,13 @@ class PLError(RuntimeError):
         super().__init__(f"{where}: {status_string(status)}")
 
 
+class Proj(ctypes.Structure):
+    """pl_nvfp4_proj: one projection of a group call."""
+    _fields_ = [("d_o", ctypes.c_int64), ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("s_g", ctypes.c_void_p), ("A", ctypes.c_void_p), ("B", ctypes.c_void_p), ("r", ctypes.c_int),
+                ("lam", ctypes.c_float), ("y", ctypes.c_void_p)]
+
+
 _SIGNATURES = {
     "pl_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "pl_version": (ctypes.c_int, []),
@@ -47,6 +54,15 @@ _SIGNATURES = {
                                             _c_void_p, _c_void_p, ctypes.c_int, ctypes.c_float,
                                             _c_void_p, _c_void_p, _i64, ctypes.c_float, _c_void_p, ctypes.c_int,
                                             _c_void_p, ctypes.c_size_t, _c_void_p]),
+    "pl_workspace_bytes_group": (ctypes.c_size_t, [_i64, _i64, ctypes.POINTER(Proj), ctypes.c_int]),
+    "pl_nvfp4_lora_linear_group": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, _i64, ctypes.c_float,
+                                                  ctypes.POINTER(Proj), ctypes.c_int, ctypes.c_int, _c_void_p,
+                                                  ctypes.c_size_t, _c_void_p]),
+    "pl_w8a8_workspace_bytes": (ctypes.c_size_t, [_i64, _i64, _i64, ctypes.c_int]),
+    "pl_w8a8_quantize_weight": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, _c_void_p]),
+    "pl_w8a8_lora_linear": (ctypes.c_int, [_c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                           ctypes.c_int, ctypes.c_float, _c_void_p, _c_void_p, _i64, ctypes.c_float,
+                                           _c_void_p, ctypes.c_int, _c_void_p, ctypes.c_size_t, _c_void_p]),
     "pl_nvfp4_quantize_uaq": (ctypes.c_int, [_c_void_p, _i64, _i64, ctypes.c_float, _c_void_p, _c_void_p,
                                              _c_void_p, _c_void_p]),
     "pl_uaq_fold_norm": (ctypes.c_int, [_c_void_p, _i64, ctypes.c_float, _c_void_p, _c_void_p]),
@@ -257,6 +273,105 @@ def nvfp4_lora_linear(x, codes, scales, s_g, A=None, B=None, lam: float = 0.0, w
                                         _ptr(A), _ptr(B), r, float(lam), _ptr(w_norm), _ptr(z), z_ld, float(eps),
                                         _ptr(out), _OUT_DTYPES[out.dtype], _ptr(ws), ws.numel(), _stream(dev))
     _check(st, "pl_nvfp4_lora_linear")
+    return out
+
+
+def nvfp4_lora_linear_group(x, projs, w_norm=None, z=None, eps: float = 1e-6, outs=None,
+                            workspace: Workspace | None = None, out_dtype: torch.dtype = torch.bfloat16):
+    """The projections that read one input (e.g. q/k/v behind one RMSNorm) in one call.
+
+    projs: sequence of dicts with keys codes, scales, s_g and optionally A, B, lam; every
+    projection gets y_p = W_hat_p h + lam_p B_p (A_p h) with the shared h = RMSNorm_AQN(x)
+    (x when w_norm is None).  Returns the list of y_p."""
+    _need(x, "x", torch.bfloat16, dim=2)
+    dev = x.device
+    M, d_i = x.shape
+    if w_norm is not None:
+        _need(w_norm, "w_norm", torch.float32, dev, 1)
+    z, z_ld = _noise(z, M, d_i, dev)
+    n = len(projs)
+    arr = (Proj * max(n, 1))()
+    ys = []
+    for i, q in enumerate(projs):
+        codes, scales, s_g = q["codes"], q["scales"], q["s_g"]
+        _need(codes, "codes", torch.uint8, dev, 2)
+        _need(scales, "scales", torch.uint8, dev, 2)
+        _need(s_g, "s_g", torch.float32, dev)
+        A, B = q.get("A"), q.get("B")
+        r = 0
+        if A is not None or B is not None:
+            _need(A, "A", torch.bfloat16, dev, 2)
+            _need(B, "B", torch.bfloat16, dev, 2)
+            r = A.shape[0]
+        d_o = codes.shape[0]
+        y = outs[i] if outs is not None else torch.empty(M, d_o, dtype=out_dtype, device=dev)
+        if y.dtype != out_dtype:
+            raise TypeError("every output of a group has the group's dtype")
+        _need(y, "out", out_dtype, dev, 2)
+        ys.append(y)
+        arr[i] = Proj(d_o, codes.data_ptr(), scales.data_ptr(), s_g.data_ptr(), A.data_ptr() if A is not None else None,
+                      B.data_ptr() if B is not None else None, r, float(q.get("lam", 0.0)), y.data_ptr())
+    if out_dtype not in _OUT_DTYPES:
+        raise TypeError("out_dtype must be bfloat16 or float32")
+    need = int(lib().pl_workspace_bytes_group(M, d_i, arr, n))
+    if workspace is None:
+        workspace = _default_ws.setdefault(dev, Workspace(dev))
+    ws = workspace.get(max(need, 256))
+    with torch.cuda.device(dev):
+        st = lib().pl_nvfp4_lora_linear_group(_ptr(x), M, d_i, _ptr(w_norm), _ptr(z), z_ld, float(eps), arr, n,
+                                              _OUT_DTYPES[out_dtype], _ptr(ws), ws.numel(), _stream(dev))
+    _check(st, "pl_nvfp4_lora_linear_group")
+    return ys
+
+
+def w8a8_quantize_weight(W: torch.Tensor, codes=None, s_w=None):
+    """BF16 W [d_o, d_i] -> (E4M3 codes uint8 [d_o, d_i], s_w float32 [d_o]): one FP8 scale per
+    output channel (the W8A8 rollout linear's weight)."""
+    _need(W, "W", torch.bfloat16, dim=2)
+    d_o, d_i = W.shape
+    dev = W.device
+    if codes is None:
+        codes = torch.empty(d_o, d_i, dtype=torch.uint8, device=dev)
+    if s_w is None:
+        s_w = torch.empty(d_o, dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        st = lib().pl_w8a8_quantize_weight(_ptr(W), d_o, d_i, _ptr(codes), _ptr(s_w), _stream(dev))
+    _check(st, "pl_w8a8_quantize_weight")
+    return codes, s_w
+
+
+def w8a8_lora_linear(x, codes, s_w, A=None, B=None, lam: float = 0.0, w_norm=None, z=None, eps: float = 1e-6,
+                     out=None, workspace: Workspace | None = None, out_dtype: torch.dtype = torch.bfloat16):
+    """y = s_x s_w (q_x q_w^T) + lam * B (A h), h = RMSNorm_AQN(x) (x when w_norm is None),
+    q_x the per-token FP8 quantisation of h."""
+    _need(x, "x", torch.bfloat16, dim=2)
+    dev = x.device
+    _need(codes, "codes", torch.uint8, dev, 2)
+    _need(s_w, "s_w", torch.float32, dev, 1)
+    M, d_i = x.shape
+    d_o = codes.shape[0]
+    r = 0
+    if A is not None or B is not None:
+        _need(A, "A", torch.bfloat16, dev, 2)
+        _need(B, "B", torch.bfloat16, dev, 2)
+        r = A.shape[0]
+    if w_norm is not None:
+        _need(w_norm, "w_norm", torch.float32, dev, 1)
+    z, z_ld = _noise(z, M, d_i, dev)
+    if out is None:
+        out = torch.empty(M, d_o, dtype=out_dtype, device=dev)
+    if out.dtype not in _OUT_DTYPES:
+        raise TypeError("out must be bfloat16 or float32")
+    _need(out, "out", out.dtype, dev, 2)
+    need = int(lib().pl_w8a8_workspace_bytes(M, d_i, d_o, r))
+    if workspace is None:
+        workspace = _default_ws.setdefault(dev, Workspace(dev))
+    ws = workspace.get(max(need, 256))
+    with torch.cuda.device(dev):
+        st = lib().pl_w8a8_lora_linear(_ptr(x), M, d_i, d_o, _ptr(codes), _ptr(s_w), _ptr(A), _ptr(B), r, float(lam),
+                                       _ptr(w_norm), _ptr(z), z_ld, float(eps), _ptr(out), _OUT_DTYPES[out.dtype],
+                                       _ptr(ws), ws.numel(), _stream(dev))
+    _check(st, "pl_w8a8_lora_linear")
     return out
 
 

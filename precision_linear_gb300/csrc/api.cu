@@ -179,6 +179,105 @@ pl_status pl_nvfp4_lora_linear(const void* x, int64_t M, int64_t d_i, int64_t d_
   return check_launch(pl::launch_linear_generic(a, s));
 }
 
+size_t pl_workspace_bytes_group(int64_t M, int64_t d_i, const pl_nvfp4_proj* projs, int n_proj) {
+  if (!projs || n_proj < 1 || n_proj > PL_MAX_GROUP) return 0;
+  size_t need = 0;
+  int rtot = 0;
+  for (int i = 0; i < n_proj; ++i) {
+    const size_t w = pl_workspace_bytes(M, d_i, projs[i].d_o, projs[i].r);
+    if (w == 0) return 0;
+    need = need > w ? need : w;
+    rtot += projs[i].r;
+  }
+  if (pl::tc_supported(M, d_i, 1, 0)) {
+    const size_t g = pl::tc_group_workspace_bytes(M, d_i, rtot);
+    need = need > g ? need : g;
+  }
+  return need;
+}
+
+pl_status pl_nvfp4_lora_linear_group(const void* x, int64_t M, int64_t d_i, const float* w_norm, const float* z,
+                                     int64_t z_ld, float eps, const pl_nvfp4_proj* projs, int n_proj, int y_dtype,
+                                     void* workspace, size_t ws_bytes, pl_stream_t stream) {
+  if (!x || !projs) return PL_ERR_NULL;
+  if (n_proj < 1 || n_proj > PL_MAX_GROUP) return PL_ERR_SHAPE;
+  if (M < 1 || d_i < 16 || d_i % 16 != 0 || M > (1ll << 24) || d_i > (1ll << 31)) return PL_ERR_SHAPE;
+  if (y_dtype != PL_DTYPE_BF16 && y_dtype != PL_DTYPE_F32) return PL_ERR_SHAPE;
+  if (w_norm && z && !z_ld_ok(z_ld, M, d_i)) return PL_ERR_SHAPE;
+  if (!aligned16(x) || (w_norm && !aligned16(w_norm)) || (z && !aligned16(z))) return PL_ERR_ALIGN;
+  pl::TcProj tp[PL_MAX_GROUP];
+  for (int i = 0; i < n_proj; ++i) {
+    const pl_nvfp4_proj& q = projs[i];
+    if (!q.codes || !q.scales || !q.s_g || !q.y) return PL_ERR_NULL;
+    if (q.d_o < 1 || q.d_o > (1ll << 31)) return PL_ERR_SHAPE;
+    if (q.r < 0 || q.r > 64) return PL_ERR_RANK;
+    if (q.r > 0 && (q.A_bf16 == nullptr) != (q.B_bf16 == nullptr)) return PL_ERR_NULL;
+    const bool lora = q.r > 0 && q.A_bf16 != nullptr && q.B_bf16 != nullptr;
+    if (!aligned16(q.codes) || !aligned16(q.scales) || !aligned16(q.y) ||
+        (lora && (!aligned16(q.A_bf16) || !aligned16(q.B_bf16))))
+      return PL_ERR_ALIGN;
+    tp[i] = pl::TcProj{q.d_o, q.codes, q.scales, q.s_g, lora ? q.A_bf16 : nullptr, lora ? q.B_bf16 : nullptr,
+                       lora ? q.r : 0, q.lambda, q.y};
+  }
+  const size_t need = pl_workspace_bytes_group(M, d_i, projs, n_proj);
+  if (!workspace || need == 0 || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return PL_ERR_WORKSPACE;
+  pl_status st = device_check();
+  if (st != PL_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // one launch pair for the whole group on the two-kernel decode path; otherwise one call
+  // per projection, in order
+  if (n_proj > 1 && pl::tc_group_supported(M, d_i, tp, n_proj))
+    return check_launch(pl::launch_linear_tc_group(x, M, d_i, w_norm, w_norm ? z : nullptr,
+                                                   (w_norm && z) ? z_ld : 0, eps, tp, n_proj,
+                                                   y_dtype == PL_DTYPE_F32, workspace, s));
+  for (int i = 0; i < n_proj; ++i) {
+    st = pl_nvfp4_lora_linear(x, M, d_i, tp[i].d_o, tp[i].codes, tp[i].scales, tp[i].s_g, tp[i].A, tp[i].B, tp[i].r,
+                              tp[i].lambda, w_norm, z, z_ld, eps, tp[i].y, y_dtype, workspace, ws_bytes, stream);
+    if (st != PL_OK) return st;
+  }
+  return PL_OK;
+}
+
+size_t pl_w8a8_workspace_bytes(int64_t M, int64_t d_i, int64_t d_o, int r) {
+  if (!pl::w8a8_supported(M, d_i, d_o, r) || M > (1ll << 24)) return 0;
+  return pl::w8a8_workspace_bytes(M, d_i, d_o, r);
+}
+
+pl_status pl_w8a8_quantize_weight(const void* W, int64_t d_o, int64_t d_i, uint8_t* codes, float* s_w,
+                                  pl_stream_t stream) {
+  if (!W || !codes || !s_w) return PL_ERR_NULL;
+  if (d_o < 1 || d_o > 0x7FFFFFFF || d_i < 16 || d_i % 16 != 0) return PL_ERR_SHAPE;
+  if (!aligned16(W) || !aligned16(codes) || (reinterpret_cast<uintptr_t>(s_w) & 3u)) return PL_ERR_ALIGN;
+  pl_status st = device_check();
+  if (st != PL_OK) return st;
+  return check_launch(pl::launch_w8a8_quantize(W, d_o, d_i, codes, s_w, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pl_status pl_w8a8_lora_linear(const void* x, int64_t M, int64_t d_i, int64_t d_o, const uint8_t* codes,
+                              const float* s_w, const void* A, const void* B, int r, float lambda,
+                              const float* w_norm, const float* z, int64_t z_ld, float eps, void* y, int y_dtype,
+                              void* workspace, size_t ws_bytes, pl_stream_t stream) {
+  if (!x || !codes || !s_w || !y) return PL_ERR_NULL;
+  if (M < 1 || M > (1ll << 24) || d_o < 1 || d_o > (1ll << 31) || d_i < 128 || d_i % 128 != 0 || d_i > 32768)
+    return PL_ERR_SHAPE;
+  if (y_dtype != PL_DTYPE_BF16 && y_dtype != PL_DTYPE_F32) return PL_ERR_SHAPE;
+  if (r < 0 || r > 64) return PL_ERR_RANK;
+  if (r > 0 && (A == nullptr) != (B == nullptr)) return PL_ERR_NULL;
+  if (w_norm && z && !z_ld_ok(z_ld, M, d_i)) return PL_ERR_SHAPE;
+  const bool lora = r > 0 && A != nullptr && B != nullptr;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(y) || (reinterpret_cast<uintptr_t>(s_w) & 3u) ||
+      (lora && (!aligned16(A) || !aligned16(B))) || (w_norm && !aligned16(w_norm)) || (z && !aligned16(z)))
+    return PL_ERR_ALIGN;
+  const size_t need = pl_w8a8_workspace_bytes(M, d_i, d_o, r);
+  if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PL_ERR_WORKSPACE;
+  pl_status st = device_check();
+  if (st != PL_OK) return st;
+  pl::W8Args a{x, M, d_i, d_o, codes, s_w, lora ? A : nullptr, lora ? B : nullptr, lora ? r : 0, lambda, w_norm,
+               w_norm ? z : nullptr, (w_norm && z) ? z_ld : 0, eps, y, y_dtype == PL_DTYPE_F32, workspace};
+  return check_launch(pl::launch_w8a8_linear(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int pl_aqn_stage(int64_t done, int64_t total) {
   if (total < 1 || done < 0) return -1;
   // ten equal parts of the planned horizon, the product taken in 128 bits
@@ -212,7 +311,7 @@ pl_status pl_aqn_noise(uint64_t seed, uint32_t norm_id, uint64_t scope0, int64_t
 pl_status pl_last_device_status(pl_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return PL_ERR_CUDA;
   uint32_t bits = pl::tc_read_and_clear_status() | pl::fused_read_and_clear_status() |
-                  pl::prefill_read_and_clear_status();
+                  pl::prefill_read_and_clear_status() | pl::w8_read_and_clear_status();
   if (bits & pl::kStatusTimeout) return PL_ERR_TIMEOUT;
   return (bits & pl::kStatusRange) ? PL_ERR_RANGE : PL_OK;
 }

@@ -50,9 +50,26 @@ size_t generic_workspace_bytes(int64_t M, int64_t d_i, int64_t d_o, int r);
 cudaError_t launch_linear_generic(const LinearArgs& a, cudaStream_t stream);
 
 // ---- linear_tc.cu (tcgen05; d_i % 256 == 0)
+// One projection of a group that reads the same input x (and norm, noise).
+struct TcProj {
+  int64_t d_o;
+  const uint8_t* codes;
+  const uint8_t* scales;
+  const float* s_g;
+  const void* A;  // bf16 [r][d_i] or null
+  const void* B;  // bf16 [d_o][r] or null
+  int r;          // 0 when A or B is null
+  float lambda;
+  void* y;        // [M][d_o]
+};
 bool tc_supported(int64_t M, int64_t d_i, int64_t d_o, int r);
+bool tc_group_supported(int64_t M, int64_t d_i, const TcProj* projs, int n_proj);
 size_t tc_workspace_bytes(int64_t M, int64_t d_i, int64_t d_o, int r);
+size_t tc_group_workspace_bytes(int64_t M, int64_t d_i, int rtot);
 cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream);
+cudaError_t launch_linear_tc_group(const void* x, int64_t M, int64_t d_i, const float* w_norm, const float* z,
+                                   int64_t z_ld, float eps, const TcProj* projs, int n_proj, bool y_f32, void* ws,
+                                   cudaStream_t stream);
 uint32_t tc_read_and_clear_status();
 cudaError_t launch_wait_timeout_probe(cudaStream_t stream);
 // The row prologue on its own: hq = f16(RMSNorm_AQN(x) / rowscale) [M][d_i], rowscale
@@ -70,6 +87,35 @@ bool prefill_supported(int64_t M, int64_t d_i, int64_t d_o, int r);
 size_t prefill_workspace_bytes(int64_t M, int64_t d_i, int64_t d_o, int r);
 cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream);
 uint32_t prefill_read_and_clear_status();
+
+// ---- w8a8.cu (FP8 E4M3 W8A8 linear; d_i % 128 == 0)
+struct W8Args {
+  const void* x;         // bf16 [M][d_i]
+  int64_t M, d_i, d_o;
+  const uint8_t* codes;  // E4M3 [d_o][d_i]
+  const float* s_w;      // [d_o]
+  const void* A;         // bf16 [r][d_i] or null
+  const void* B;         // bf16 [d_o][r] or null
+  int r;
+  float lambda;
+  const float* w_norm;
+  const float* z;
+  int64_t z_ld;
+  float eps;
+  void* y;
+  bool y_f32;
+  void* ws;
+};
+bool w8a8_supported(int64_t M, int64_t d_i, int64_t d_o, int r);
+size_t w8a8_workspace_bytes(int64_t M, int64_t d_i, int64_t d_o, int r);
+cudaError_t launch_w8a8_quantize(const void* W, int64_t d_o, int64_t d_i, uint8_t* codes, float* s_w,
+                                 cudaStream_t stream);
+cudaError_t launch_w8a8_linear(const W8Args& a, cudaStream_t stream);
+uint32_t w8_read_and_clear_status();
+// linear_tc.cu: the cluster prologue in its FP8 mode (per-token E4M3 codes, s_x, t = A h)
+cudaError_t launch_pro_fp8(const void* x, int64_t M, int64_t d_i, const float* w_norm, const float* z, int64_t z_ld,
+                           float eps, const void* A, int r, uint8_t* qx, float* s_x, float* t, int t_ld,
+                           cudaStream_t stream);
 
 // ---- aqn.cu: z [n_scopes][d] = sigma * Philox4x32-10 / Box-Muller normals
 cudaError_t launch_aqn_noise(uint64_t seed, uint32_t norm_id, uint64_t scope0, int64_t n_scopes, int64_t d,

@@ -3,36 +3,39 @@
 // Computes the forward map of "QeRL: When Quantized Weights Help Reinforcement
 // Learning, and Where the Evidence Stops", section 2.1 (y = W_hat h + lambda B (A h))
 // on the section 3.1 NVFP4 backbone (w_hat = s_g s_b q) with the section 5.1
-// RMSNorm-AQN input h = u (.) (w_norm + z).
+// RMSNorm-AQN input h = u (.) (w_norm + z), for one projection or for a group of
+// projections that read the same input (the projections behind one RMSNorm of a layer:
+// q, k and v, or gate and up).
 //
 // Two kernels per call, chained by programmatic dependent launch:
 //
-// k_act (a group of warps per token row): h = x / rms (.) (w_norm + z) in FP32, a power-of-two
-//   c_m with max|h| / c_m in [2^13, 2^14), and the f16 activations h / c_m (11-bit
-//   significand, no overflow) into the workspace; a few more CTAs copy the LoRA matrix
-//   A into the workspace as f16.
+// k_pro_dec (clusters of C CTAs; a cluster owns R token rows, CTA c of it the c-th slice
+//   of the K = d_i axis): u = x (.) (w_norm + z) in FP32, per row the sum of x^2 and max |u|
+//   over the slice, and the slice's share of A_p u for every projection p of the group
+//   (CUDA cores, FP32).  One exchange over distributed shared memory gives every CTA the
+//   row statistics of the whole row: rs = 1 / sqrt(mean x^2 + eps), the power of two c_m
+//   with max |h| / c_m in [2^13, 2^14), and it writes the f16 activations h / c_m of its
+//   slice (11-bit significand, no overflow); the adapter sums of the C slices are added in
+//   slice order (deterministic) and t = rs A_p u, FP32, goes to the workspace.  The
+//   adapter's down-projection is thereby done once per call, not once per weight tile.
 //
-// k_tc_decode (a cluster of S CTAs per 128 weight rows; CTA s takes the s-th slice of
-//   the K = d_i axis in chunks of 256):
+// k_tc_decode (a cluster of S CTAs per 128 weight rows of one projection; CTA s takes the
+//   s-th slice of K in chunks of 256):
 //   * warp 0 TMA-loads, per chunk, the packed codes (128 rows x 128 B, 128-byte
-//     swizzle) and E4M3 scales (128 x 16 B) -- issued before the wait on k_act, they
-//     do not depend on it -- the f16 activations (N rows x 256, 128-byte swizzle:
-//     the canonical K-major layout) and the chunk of the f16 copy of A (r x 256);
+//     swizzle) and E4M3 scales (128 x 16 B) -- issued before the wait on the prologue,
+//     they do not depend on it -- and the f16 activations (N rows x 256, 128-byte swizzle:
+//     the canonical K-major layout);
 //   * warps 2..9 dequantise: each thread owns one weight row and half the chunk, turns
 //     8 codes per 32-bit word into 4 f16x2 words with the hardware E2M1 conversion,
 //     multiplies by the block scale (q * s_b is exact in f16) and stores them into
 //     tensor memory, where they are the MMA's A operand;
-//   * four warps issue tcgen05.mma kind::f16 (K = 16 each; one thread issues one only
-//     every few tens of ns, so the work is shared): weights (tensor memory) x
-//     activations^T into accumulator D1, and A (shared memory, 128-row operand whose
-//     rows >= r are don't-care) x activations^T into accumulator Dt, whose lanes < r are
-//     this CTA's K slice of t = A h -- each of D1 and Dt as two partial sums over the two
-//     halves of every chunk's K steps;
-//   * epilogue (warps 2..9): every CTA adds the partial sums and puts s_g c_m D1 and its
-//     Dt slice in shared memory; after a cluster barrier CTA s sums, over DSMEM and in split order
-//     (deterministic), the t slices of all S CTAs into t, and the D1 partials of its
-//     share of the 128 rows; it adds the LoRA up-projection lambda B t on CUDA cores
-//     and writes y.
+//   * two warps issue tcgen05.mma kind::f16 (K = 16 each; one thread issues one only
+//     every few tens of ns, so each takes half of every chunk's K steps): weights (tensor
+//     memory) x activations^T into two partial accumulators;
+//   * epilogue (warps 2..9): every CTA adds its two partials and puts s_g c_m D1 in
+//     shared memory; after a cluster barrier CTA s sums, over DSMEM and in split order
+//     (deterministic), the partials of its share of the 128 rows, adds lambda B t on CUDA
+//     cores (t from the prologue) and writes y.
 //
 // Every mbarrier wait is bounded (200 ms); a wait that gives up sets the device
 // status word, the CTA drains its own copies and MMAs (again bounded), frees its
@@ -69,44 +72,54 @@ constexpr int kChunkK = 256;
 constexpr int kCodesBytes = kTileO * kChunkK / 2;   // 16 KB
 constexpr int kScaleBytes = kTileO * kChunkK / 16;  // 2 KB
 constexpr int kDeqWarps = 8;
-constexpr int kIssuers = 4;        // MMA-issuing warps: D1 and Dt, each in two K halves
-constexpr int kThreads = (2 + kDeqWarps + kIssuers - 1) * 32;  // producer, issuer 0, dequant/epilogue, issuers 1..3
+constexpr int kIssuers = 2;  // MMA-issuing warps: the two K halves of every chunk
+constexpr int kThreads = (2 + kDeqWarps + kIssuers - 1) * 32;  // producer, issuer 0, dequant/epilogue, issuer 1
+constexpr int kIssuer1Warp = 2 + kDeqWarps;
 constexpr int kEpiThreads = kDeqWarps * 32;
 constexpr int kMaxStages = 8;
 constexpr int kMaxSplit = 8;
-constexpr int kMaxLa = 3;  // slots of the shared-memory ring of A chunks
 constexpr int kMaxN = 64;
-constexpr int kMaxR = 64;
+constexpr int kMaxR = 64;        // adapter rank of one projection
+constexpr int kMaxProj = 4;      // projections in one group
+constexpr int kMaxRTot = 128;    // adapter rows of a whole group
 constexpr uint32_t kTmemCols = 512;
 // tensor-memory columns: kAbuf weight (MMA A operand) buffers of 128 columns from 0, then
-// the accumulators of the four issuers, N <= 64 columns each: D1 over the first and the
-// second half of every chunk's K steps, and Dt likewise
-constexpr int kAbuf = 2;
+// the two accumulators, N <= 64 columns each: D1 over the first and the second half of
+// every chunk's K steps
+constexpr int kAbuf = 3;
 constexpr uint32_t kColA0 = 0;
-constexpr uint32_t kColAcc = 256;  // issuer q accumulates at kColAcc + 64 q
+constexpr uint32_t kColAcc = 384;  // issuer q accumulates at kColAcc + 64 q
 static_assert(kAbuf * 128 <= kColAcc && kColAcc + kIssuers * kMaxN <= kTmemCols, "TMEM columns");
-constexpr int kTStride = kMaxR + 4;  // floats per token row of the t buffers (16-byte rows, spread banks)
+constexpr int kTStride = kMaxR + 4;  // floats per token row of lambda t in shared memory
+
+// One projection of a group, as the main kernel sees it.
+struct TcProjDev {
+  int64_t d_o;
+  const float* s_g;
+  const __nv_bfloat16* B;  // [d_o][r] or null
+  void* y;                 // [M][d_o]
+  int r, toff, tile0;      // adapter rank, its first column of t, its first weight tile
+  float lambda;
+};
 
 struct TcParams {
-  int64_t M, d_i, d_o;
-  int N, r, rb, tiles, splits, kc, stages, la;
+  int64_t M, d_i;
+  int N, splits, kc, stages, n_proj, t_ld;
   uint32_t stage_bytes;
-  float lambda;
-  const float* s_g;
-  const float* rowscale;
-  const __nv_bfloat16* Blora;
-  void* y;
+  const float* rowscale;  // [M]: c_m
+  const float* t;         // [M][t_ld]: t = rs A_p u of every projection at column toff_p
   int y_f32;
+  TcProjDev proj[kMaxProj];
 };
 
 struct TcMaps {
-  CUtensorMap codes, scales, hq, alora;
+  CUtensorMap hq;
+  CUtensorMap codes[kMaxProj], scales[kMaxProj];
 };
 
 struct Smem {
   uint64_t wfull[kMaxStages], hfull[kMaxStages], empty[kMaxStages];
   uint64_t a_full[kAbuf], a_empty[kAbuf];
-  uint64_t lfull[kMaxLa], lempty[kMaxLa];  // shared-memory ring of A chunks
   uint64_t d_full;
   uint32_t tmem_base;
   int abort_flag;
@@ -114,7 +127,27 @@ struct Smem {
   float rowscale[kMaxN];
 };
 
-// Wait that also gives up when another role of the CTA has already given up.
+// Arguments of the cluster prologue.
+struct ProParams {
+  const __nv_bfloat16* x;
+  int64_t M, d_i;
+  const float* w_norm;  // [d_i] or null (no norm)
+  const float* z;       // null, [d_i] (z_ld == 0) or rows z_ld apart
+  int64_t z_ld;
+  float eps;
+  __half* hq;           // [M][d_i] (f16 mode)
+  float* rowscale;      // [M]: c_m (f16 mode), s_x (FP8 mode)
+  uint8_t* qx;          // [M][d_i] E4M3 codes (FP8 mode)
+  float* t;             // [M][t_ld]
+  int t_ld, R, C, n_proj, rtot;
+  const __nv_bfloat16* A[kMaxProj];  // [r_p][d_i]
+  int r[kMaxProj], toff[kMaxProj];
+};
+constexpr int kProThreads = 256;
+constexpr int kProWarps = kProThreads / 32;
+constexpr int kProMaxR = 4;  // token rows per cluster
+constexpr int kProMaxC = 8;  // CTAs per cluster
+
 PL_DEVINL bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   return wait_or_abort_status(bar, parity, abort_flag, &g_tc_status);
 }
@@ -304,26 +337,266 @@ __global__ void __launch_bounds__(kActThreads, 2) k_act(const __nv_bfloat16* __r
   if (threadIdx.x == 0) PL_TLP(5);
 }
 
+
+// ------------------------------------------------------------------ cluster prologue
+// A cluster of C CTAs per R token rows (rows m0 .. m0 + R - 1); CTA c of the cluster takes
+// the pieces [c n8 / C, (c + 1) n8 / C) of 8 elements along K.  See the file comment.
+// kFp8: instead of the f16 rows, the per-token FP8 quantisation of h for the W8A8 linear:
+// s_x = fp32(max |h| / 448) (1 for a zero row), codes E4M3(fp32(h / s_x)), round to
+// nearest even, saturating, +0 for values that round to zero.
+template <bool kFp8>
+__global__ void __launch_bounds__(kProThreads) k_pro_dec(const __grid_constant__ ProParams p) {
+  extern __shared__ float4 pro_smem4[];
+  float* u = reinterpret_cast<float*>(pro_smem4);  // [R][Lmax]: u = x (.) (w_norm + z), this CTA's slice
+  __shared__ float red[kProWarps][kProMaxR][2];
+  // read by the peers: per row the slice's sum of x^2 and max |u|, then the adapter sums [R][J]
+  __shared__ __align__(16) float xch[2 * kProMaxR + kProMaxR * kMaxRTot];
+  __shared__ float s_inv[kProMaxR], s_f[kProMaxR];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int C = p.C, R = p.R, J = p.rtot;
+  uint32_t rank_u;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank_u));
+  const int rank = static_cast<int>(rank_u);
+  const int64_t m0 = static_cast<int64_t>(blockIdx.x / C) * R;
+  const int64_t n8 = p.d_i / 8;
+  const int64_t q0 = rank * n8 / C, q1 = (rank + 1) * n8 / C;
+  const int L8 = static_cast<int>(q1 - q0);
+  const int Lmax = static_cast<int>((n8 + C - 1) / C) * 8;
+  const bool norm = p.w_norm != nullptr;
+  const bool zshared = norm && p.z != nullptr && p.z_ld == 0, zrows = norm && p.z != nullptr && p.z_ld != 0;
+  if (tid == 0) {
+    PL_TLP(0);
+    pdl_launch_dependents();
+  }
+  pdl_wait();  // x, w_norm and z may come from the preceding kernel, which may also still read the workspace
+  if (tid == 0) PL_TLP(1);
+
+  // 1. u of this CTA's rows and slice; per row the sum of x^2 and max |u|
+  float ss[kProMaxR], mx[kProMaxR];
+#pragma unroll
+  for (int m = 0; m < kProMaxR; ++m) {
+    ss[m] = 0.f;
+    mx[m] = 0.f;
+  }
+  for (int qi = tid; qi < L8; qi += kProThreads) {
+    const int64_t q = q0 + qi;
+    float g[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) g[i] = 1.f;
+    if (norm) {
+      const float4 a = reinterpret_cast<const float4*>(p.w_norm)[2 * q], b = reinterpret_cast<const float4*>(p.w_norm)[2 * q + 1];
+      g[0] = a.x; g[1] = a.y; g[2] = a.z; g[3] = a.w; g[4] = b.x; g[5] = b.y; g[6] = b.z; g[7] = b.w;
+      if (zshared) {
+        const float4 za = reinterpret_cast<const float4*>(p.z)[2 * q], zb = reinterpret_cast<const float4*>(p.z)[2 * q + 1];
+        g[0] += za.x; g[1] += za.y; g[2] += za.z; g[3] += za.w; g[4] += zb.x; g[5] += zb.y; g[6] += zb.z; g[7] += zb.w;
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < kProMaxR; ++m) {
+      if (m < R) {
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = 0.f;
+        const int64_t row = m0 + m;
+        if (row < p.M) {
+          const uint4 xv = reinterpret_cast<const uint4*>(p.x + row * p.d_i)[q];
+          float gz[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) gz[i] = g[i];
+          if (zrows) {
+            const float4* zr = reinterpret_cast<const float4*>(p.z + row * p.z_ld) + 2 * q;
+            const float4 za = zr[0], zb = zr[1];
+            gz[0] += za.x; gz[1] += za.y; gz[2] += za.z; gz[3] += za.w;
+            gz[4] += zb.x; gz[5] += zb.y; gz[6] += zb.z; gz[7] += zb.w;
+          }
+          const uint32_t w4[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float a0 = bf16lo_to_f32(w4[j]), a1 = bf16hi_to_f32(w4[j]);
+            ss[m] = fmaf(a0, a0, fmaf(a1, a1, ss[m]));
+            v[2 * j] = a0 * gz[2 * j];
+            v[2 * j + 1] = a1 * gz[2 * j + 1];
+            mx[m] = fmaxf(mx[m], fmaxf(fabsf(v[2 * j]), fabsf(v[2 * j + 1])));
+          }
+        }
+        float4* ud = reinterpret_cast<float4*>(u + m * Lmax + qi * 8);
+        ud[0] = make_float4(v[0], v[1], v[2], v[3]);
+        ud[1] = make_float4(v[4], v[5], v[6], v[7]);
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < kProMaxR; ++m) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      ss[m] += __shfl_xor_sync(0xFFFFFFFFu, ss[m], o);
+      mx[m] = fmaxf(mx[m], __shfl_xor_sync(0xFFFFFFFFu, mx[m], o));
+    }
+    if (lane == 0) {
+      red[warp][m][0] = ss[m];
+      red[warp][m][1] = mx[m];
+    }
+  }
+  __syncthreads();
+  if (tid < R) {
+    float s = 0.f, x = 0.f;
+#pragma unroll
+    for (int w = 0; w < kProWarps; ++w) {
+      s += red[w][tid][0];
+      x = fmaxf(x, red[w][tid][1]);
+    }
+    xch[2 * tid] = s;
+    xch[2 * tid + 1] = x;
+  }
+
+  // 2. this slice's adapter sums P[m][jj] = sum_k A[jj][k] u[m][k] over every projection of
+  //    the group (adapter rows jj = toff_p + j): warp w takes rows 4w .. 4w + 3, then
+  //    4w + 32 ..; the lanes split the pieces, a fixed shuffle tree adds them up
+  for (int jb = 4 * warp; jb < J; jb += 4 * kProWarps) {
+    const __nv_bfloat16* arow[4];
+#pragma unroll
+    for (int jr = 0; jr < 4; ++jr) {
+      arow[jr] = nullptr;
+      const int jj = jb + jr;
+      for (int pp = 0; pp < p.n_proj; ++pp)
+        if (jj >= p.toff[pp] && jj < p.toff[pp] + p.r[pp]) arow[jr] = p.A[pp] + (jj - p.toff[pp]) * p.d_i;
+    }
+    float acc[4][kProMaxR];
+#pragma unroll
+    for (int jr = 0; jr < 4; ++jr)
+#pragma unroll
+      for (int m = 0; m < kProMaxR; ++m) acc[jr][m] = 0.f;
+    for (int qi = lane; qi < L8; qi += 32) {
+      uint4 av[4];
+#pragma unroll
+      for (int jr = 0; jr < 4; ++jr)
+        av[jr] = arow[jr] != nullptr ? reinterpret_cast<const uint4*>(arow[jr])[q0 + qi] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int m = 0; m < kProMaxR; ++m) {
+        if (m < R) {
+          const float4* us = reinterpret_cast<const float4*>(u + m * Lmax + qi * 8);
+          const float4 ua = us[0], ub = us[1];
+          const float uv[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
+#pragma unroll
+          for (int jr = 0; jr < 4; ++jr) {
+            const uint32_t w4[4] = {av[jr].x, av[jr].y, av[jr].z, av[jr].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              acc[jr][m] = fmaf(bf16lo_to_f32(w4[j]), uv[2 * j], acc[jr][m]);
+              acc[jr][m] = fmaf(bf16hi_to_f32(w4[j]), uv[2 * j + 1], acc[jr][m]);
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int jr = 0; jr < 4; ++jr)
+#pragma unroll
+      for (int m = 0; m < kProMaxR; ++m) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[jr][m] += __shfl_xor_sync(0xFFFFFFFFu, acc[jr][m], o);
+        if (lane == 0 && m < R && jb + jr < J) xch[2 * kProMaxR + m * J + jb + jr] = acc[jr][m];
+      }
+  }
+  if (tid == 0) PL_TLP(2);
+
+  // 3. exchange: the row statistics of the whole row, then this CTA's f16 activations and
+  //    its share of t (entries e = rank mod C of [R][J]), the slices added in slice order
+  cluster_sync();
+  if (tid < R) {
+    float s = 0.f, x = 0.f;
+    for (int c = 0; c < C; ++c) {
+      s += ld_dsmem_f32(mapa_shared(smem_u32(&xch[2 * tid]), static_cast<uint32_t>(c)));
+      x = fmaxf(x, ld_dsmem_f32(mapa_shared(smem_u32(&xch[2 * tid + 1]), static_cast<uint32_t>(c))));
+    }
+    const float inv = norm ? 1.0f / sqrtf(s / static_cast<float>(p.d_i) + p.eps) : 1.0f;
+    const float hmax = inv * x;  // max |h|: rounding is monotone, so this is max |fl(u inv)|
+    s_inv[tid] = inv;
+    if (kFp8) {
+      const float sx = hmax > 0.f ? __fdiv_rn(hmax, 448.0f) : 1.0f;
+      s_f[tid] = sx;
+      if (rank == 0 && m0 + tid < p.M) p.rowscale[m0 + tid] = sx;
+    } else {
+      int e = hmax > 0.f ? ilogbf(hmax) - 13 : 0;  // max |h| / c_m in [2^13, 2^14)
+      e = e < -100 ? -100 : (e > 100 ? 100 : e);
+      s_f[tid] = inv * ldexpf(1.0f, -e);
+      if (rank == 0 && m0 + tid < p.M) p.rowscale[m0 + tid] = ldexpf(1.0f, e);
+    }
+  }
+  __syncthreads();
+  for (int qi = tid; qi < L8; qi += kProThreads) {
+#pragma unroll
+    for (int m = 0; m < kProMaxR; ++m) {
+      const int64_t row = m0 + m;
+      if (m < R && row < p.M) {
+        const float4* us = reinterpret_cast<const float4*>(u + m * Lmax + qi * 8);
+        const float4 a = us[0], b = us[1];
+        const float f = s_f[m];
+        if (kFp8) {
+          const float inv = s_inv[m];
+          const float hv[8] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv, b.x * inv, b.y * inv, b.z * inv, b.w * inv};
+          uint32_t w[2];
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t c4 = 0;
+#pragma unroll
+            for (int i = 0; i < 4; i += 2) {
+              // two codes per conversion; a value that rounds to zero keeps no sign
+              uint32_t c2 = cvt_e4m3x2(__fdiv_rn(hv[4 * hh + i + 1], f), __fdiv_rn(hv[4 * hh + i], f));
+              if ((c2 & 0x7Fu) == 0) c2 &= 0xFF00u;
+              if ((c2 & 0x7F00u) == 0) c2 &= 0x00FFu;
+              c4 |= c2 << (8 * i);
+            }
+            w[hh] = c4;
+          }
+          reinterpret_cast<uint2*>(p.qx + row * p.d_i)[q0 + qi] = make_uint2(w[0], w[1]);
+        } else {
+          reinterpret_cast<uint4*>(p.hq + row * p.d_i)[q0 + qi] =
+              make_uint4(f32x2_to_f16x2(a.x * f, a.y * f), f32x2_to_f16x2(a.z * f, a.w * f),
+                         f32x2_to_f16x2(b.x * f, b.y * f), f32x2_to_f16x2(b.z * f, b.w * f));
+        }
+      }
+    }
+  }
+  for (int e = rank + C * tid; e < R * J; e += C * kProThreads) {
+    const int m = e / J, jj = e % J;
+    if (m0 + m < p.M) {
+      const uint32_t a = smem_u32(&xch[2 * kProMaxR + m * J + jj]);
+      float s = 0.f;
+      for (int c = 0; c < C; ++c) s += ld_dsmem_f32(mapa_shared(a, static_cast<uint32_t>(c)));
+      p.t[(m0 + m) * p.t_ld + jj] = s_inv[m] * s;
+    }
+  }
+  if (tid == 0) PL_TLP(3);
+  cluster_sync();  // the peers read this CTA's shared memory until here
+}
+
 // ------------------------------------------------------------------ main kernel
 __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant__ TcMaps maps,
-                                                           const TcParams p) {
+                                                           const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int N = p.N, stages = p.stages, la = p.la;
+  const int N = p.N, stages = p.stages;
   const uint32_t h_bytes = static_cast<uint32_t>(N) * 512u;
-  const uint32_t l_bytes = static_cast<uint32_t>(p.rb) * 512u;  // one A chunk (rb rows x 256 bf16)
-  uint8_t* lring = smem + static_cast<size_t>(stages) * p.stage_bytes;           // la A chunks
-  __nv_bfloat16* sBt = reinterpret_cast<__nv_bfloat16*>(lring + la * l_bytes);  // [kMaxR][128]: B^T of the tile
+  __nv_bfloat16* sBt = reinterpret_cast<__nv_bfloat16*>(smem + static_cast<size_t>(stages) * p.stage_bytes);  // [kMaxR][128]: B^T of the tile
   Smem& S = *reinterpret_cast<Smem*>(reinterpret_cast<uint8_t*>(sBt) + kTileO * kMaxR * 2);
   volatile int* abort_flag = &S.abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile = blockIdx.x / p.splits, split = blockIdx.x % p.splits;
+  const int gtile = blockIdx.x / p.splits, split = blockIdx.x % p.splits;
+  // the projection of this tile: the last one whose first tile is <= gtile
+  int pj = 0;
+#pragma unroll
+  for (int q = 1; q < kMaxProj; ++q)
+    if (q < p.n_proj && gtile >= p.proj[q].tile0) pj = q;
+  const TcProjDev& P = p.proj[pj];
+  const CUtensorMap* map_codes = &maps.codes[pj];
+  const CUtensorMap* map_scales = &maps.scales[pj];
+  const int tile = gtile - P.tile0;
   const int c0 = static_cast<int>((static_cast<int64_t>(split) * p.kc) / p.splits);
   const int c1 = static_cast<int>((static_cast<int64_t>(split + 1) * p.kc) / p.splits);
   const int nch = c1 - c0;
-  const bool lora = p.r > 0;
-  const int n_iss = lora ? kIssuers : 2;  // the Dt issuers idle without an adapter
+  const bool lora = P.r > 0;
   bool go = false;  // epilogue threads: this CTA's accumulators are valid
 
   const uint64_t pol_w = policy_evict_first();  // weights are streamed once
@@ -335,17 +608,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
     for (int s = 0; s < stages; ++s) {
       mbar_init(smem_u32(&S.wfull[s]), 1);
       mbar_init(smem_u32(&S.hfull[s]), 1);
-      mbar_init(smem_u32(&S.empty[s]), kDeqWarps + n_iss);
+      mbar_init(smem_u32(&S.empty[s]), kDeqWarps + kIssuers);
     }
     for (int b = 0; b < kAbuf; ++b) {
       mbar_init(smem_u32(&S.a_full[b]), kDeqWarps);
-      mbar_init(smem_u32(&S.a_empty[b]), 2);
+      mbar_init(smem_u32(&S.a_empty[b]), kIssuers);
     }
-    for (int b = 0; b < la; ++b) {
-      mbar_init(smem_u32(&S.lfull[b]), 1);
-      mbar_init(smem_u32(&S.lempty[b]), 2);
-    }
-    mbar_init(smem_u32(&S.d_full), n_iss);
+    mbar_init(smem_u32(&S.d_full), kIssuers);
     S.abort_flag = 0;
     fence_mbar_init();
     // the first stages of weights do not depend on the prologue: issue them at once
@@ -355,11 +624,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
       mbar_arrive_expect_tx(wb, kCodesBytes + kScaleBytes);
       const int kc = c0 + c;
       PL_TLC(0, c);
-      tma_load_2d_hint(smem_u32(st), &maps.codes, kc * (kChunkK / 2), row0, wb, pol_w);
-      tma_load_2d_hint(smem_u32(st + kCodesBytes + h_bytes), &maps.scales, kc * (kChunkK / 16), row0, wb, pol_w);
+      tma_load_2d_hint(smem_u32(st), map_codes, kc * (kChunkK / 2), row0, wb, pol_w);
+      tma_load_2d_hint(smem_u32(st + kCodesBytes + h_bytes), map_scales, kc * (kChunkK / 16), row0, wb, pol_w);
     }
     tma_prefetch_desc(&maps.hq);
-    if (lora) tma_prefetch_desc(&maps.alora);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&S.tmem_base), kTmemCols);
@@ -374,9 +642,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
-      const int lpre = lora ? (nch < la ? nch : la) : 0;
       PL_TL(2);
-      pdl_wait();  // activations and the f16 copy of A come from the prologue
+      pdl_wait();  // the activations come from the prologue
       PL_TL(3);
       for (int c = 0; c < pre; ++c) {
         uint8_t* st = smem + static_cast<size_t>(c) * p.stage_bytes;
@@ -385,33 +652,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
         for (int q = 0; q < 4; ++q)
           tma_load_2d(smem_u32(st + kCodesBytes + q * N * 128), &maps.hq, (c0 + c) * kChunkK + 64 * q, 0, hb);
       }
-      for (int c = 0; c < lpre; ++c) {
-        const uint32_t lb = smem_u32(&S.lfull[c]);
-        mbar_arrive_expect_tx(lb, l_bytes);
-        for (int q = 0; q < 4; ++q)
-          tma_load_2d(smem_u32(lring + c * l_bytes + q * p.rb * 128), &maps.alora, (c0 + c) * kChunkK + 64 * q, 0,
-                      lb);
-      }
-      int c = pre, lc = lpre;
+      int c = pre;
       bool ok = true;
-      while (ok && (c < nch || lc < (lora ? nch : 0))) {
-        // Issue in the order the MMA frees the buffers: A chunk lc reuses the ring slot of
-        // chunk lc - la, weight chunk c the stage of chunk c - stages.  (Taking A first
-        // whenever it is behind would wait on the MMA of the chunk just issued and leave
-        // the weight stream one chunk deep.)
-        if (lora && lc < nch && (c >= nch || lc - la <= c - stages)) {
-          const int b = lc % la;
-          ok = wait_or_abort(smem_u32(&S.lempty[b]), ((lc / la) - 1) & 1, abort_flag);
-          if (!ok) break;
-          const uint32_t lb = smem_u32(&S.lfull[b]);
-          mbar_arrive_expect_tx(lb, l_bytes);
-          for (int q = 0; q < 4; ++q)
-            tma_load_2d(smem_u32(lring + b * l_bytes + q * p.rb * 128), &maps.alora, (c0 + lc) * kChunkK + 64 * q,
-                        0, lb);
-          ++lc;
-          continue;
-        }
-        if (c >= nch) break;
+      while (ok && c < nch) {
         const int s = c % stages;
         ok = wait_or_abort(smem_u32(&S.empty[s]), ((c / stages) - 1) & 1, abort_flag);
         if (!ok) break;
@@ -420,8 +663,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
         const int kc = c0 + c;
         PL_TLC(0, c);
         mbar_arrive_expect_tx(wb, kCodesBytes + kScaleBytes);
-        tma_load_2d_hint(smem_u32(st), &maps.codes, kc * (kChunkK / 2), row0, wb, pol_w);
-        tma_load_2d_hint(smem_u32(st + kCodesBytes + h_bytes), &maps.scales, kc * (kChunkK / 16), row0, wb, pol_w);
+        tma_load_2d_hint(smem_u32(st), map_codes, kc * (kChunkK / 2), row0, wb, pol_w);
+        tma_load_2d_hint(smem_u32(st + kCodesBytes + h_bytes), map_scales, kc * (kChunkK / 16), row0, wb, pol_w);
         mbar_arrive_expect_tx(hb, h_bytes);
         for (int q = 0; q < 4; ++q)
           tma_load_2d(smem_u32(st + kCodesBytes + q * N * 128), &maps.hq, kc * kChunkK + 64 * q, 0, hb);
@@ -432,53 +675,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
           drain(smem_u32(&S.wfull[d % stages]), (d / stages) & 1);
           drain(smem_u32(&S.hfull[d % stages]), (d / stages) & 1);
         }
-        for (int d = (lc - la > 0 ? lc - la : 0); d < lc; ++d) drain(smem_u32(&S.lfull[d % la]), (d / la) & 1);
       }
     }
-  } else if (warp == 1 || warp >= 2 + kDeqWarps) {
+  } else if (warp == 1 || warp == kIssuer1Warp) {
     // ---------------------------------------------------------------- MMA issuers
-    // One thread can issue a tcgen05.mma only every few tens of ns, so four warps share the
-    // work: issuer q takes K steps [8 (q & 1), 8 (q & 1) + 8) of every chunk, q < 2 the
-    // weights (tensor memory) x activations^T into D1 half q, q >= 2 the adapter A (shared
-    // memory, a 128-row operand whose rows >= r are don't-care) x activations^T into Dt
-    // half q - 2.  Each accumulator is a partial sum; the epilogue adds the two halves.
-    const int q = warp == 1 ? 0 : warp - (1 + kDeqWarps);
-    if (lane == 0 && q < n_iss) {
+    // One thread can issue a tcgen05.mma only every few tens of ns, so two warps share the
+    // work: issuer q takes K steps [8 q, 8 q + 8) of every chunk, weights (tensor memory) x
+    // activations^T into its own partial accumulator; the epilogue adds the two.
+    const int q = warp == 1 ? 0 : 1;
+    if (lane == 0) {
       const uint32_t idesc = idesc_f16(kTileO, N, 0);
       const uint32_t dcol = tmem + kColAcc + 64u * static_cast<uint32_t>(q);
-      const int k0 = 8 * (q & 1);
-      const bool wq = q < 2;
+      const int k0 = 8 * q;
       bool ok = true;
       for (int c = 0; c < nch && ok; ++c) {
-        const int s = c % stages, b = c % kAbuf, lb = c % la;
-        ok = (wq ? wait_or_abort(smem_u32(&S.a_full[b]), (c / kAbuf) & 1, abort_flag)
-                 : wait_or_abort(smem_u32(&S.lfull[lb]), (c / la) & 1, abort_flag)) &&
+        const int s = c % stages, b = c % kAbuf;
+        ok = wait_or_abort(smem_u32(&S.a_full[b]), (c / kAbuf) & 1, abort_flag) &&
              wait_or_abort(smem_u32(&S.hfull[s]), (c / stages) & 1, abort_flag);
         if (!ok) break;
-        PL_TLC(wq ? 1 : 2, c);
+        PL_TLC(1, c);
         tc_fence_after();
         const uint32_t hbase = smem_u32(smem + static_cast<size_t>(s) * p.stage_bytes + kCodesBytes);
-        if (wq) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int kk = k0 + i;
-            const uint64_t bdesc = smem_desc_sw128(hbase + (kk >> 2) * N * 128 + (kk & 3) * 32, 1024);
-            mma_ts(dcol, tmem + kColA0 + 128u * b + kk * 8, bdesc, idesc, (c > 0 || i > 0) ? 1u : 0u);
-          }
-          tc_commit(smem_u32(&S.a_empty[b]));
-        } else {
-          // rows >= rb of the A operand read bytes that follow the chunk (still inside this
-          // CTA's allocation) and only feed accumulator lanes >= r, which are never used
-          const uint32_t abase = smem_u32(lring + lb * l_bytes);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int kk = k0 + i;
-            const uint64_t adesc = smem_desc_sw128(abase + (kk >> 2) * p.rb * 128 + (kk & 3) * 32, 1024);
-            const uint64_t bdesc = smem_desc_sw128(hbase + (kk >> 2) * N * 128 + (kk & 3) * 32, 1024);
-            mma_ss(dcol, adesc, bdesc, idesc, (c > 0 || i > 0) ? 1u : 0u);
-          }
-          tc_commit(smem_u32(&S.lempty[lb]));
+        for (int i = 0; i < 8; ++i) {
+          const int kk = k0 + i;
+          const uint64_t bdesc = smem_desc_sw128(hbase + (kk >> 2) * N * 128 + (kk & 3) * 32, 1024);
+          mma_ts(dcol, tmem + kColA0 + 128u * b + kk * 8, bdesc, idesc, (c > 0 || i > 0) ? 1u : 0u);
         }
+        tc_commit(smem_u32(&S.a_empty[b]));
         tc_commit(smem_u32(&S.empty[s]));
       }
       tc_commit(smem_u32(&S.d_full));  // also reached on abort: tracks every MMA issued
@@ -492,31 +716,31 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
     const int row = quarter * 32 + lane;  // weight row within the tile
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     bool ok = true;
-    if (threadIdx.x == 64) S.s_g = *p.s_g;  // weight inputs: never written by the preceding kernel
+    if (threadIdx.x == 64) S.s_g = *P.s_g;  // weight inputs: never written by the preceding kernel
     if (lora) {
       // B rows of this tile, transposed into sBt[j][row] (bf16, zero past r and past d_o);
       // the tile's rows are one contiguous block of 128 r elements of B
       const int et0 = threadIdx.x - 64;
       const int64_t o0 = static_cast<int64_t>(tile) * kTileO;
-      const int rows = static_cast<int>(p.d_o - o0 < kTileO ? p.d_o - o0 : kTileO);
+      const int rows = static_cast<int>(P.d_o - o0 < kTileO ? P.d_o - o0 : kTileO);
       for (int i = et0; i < kTileO * kMaxR; i += kEpiThreads) sBt[i] = __float2bfloat16_rn(0.f);
       named_bar(1, kEpiThreads);
-      const int n8 = rows * p.r / 8;  // 16-byte pieces (r % 8 == 0) or element-wise otherwise
-      if ((p.r & 7) == 0) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.Blora + o0 * p.r);
+      const int n8 = rows * P.r / 8;  // 16-byte pieces (r % 8 == 0) or element-wise otherwise
+      if ((P.r & 7) == 0) {
+        const uint4* src = reinterpret_cast<const uint4*>(P.B + o0 * P.r);
         for (int i = et0; i < n8; i += kEpiThreads) {
           const uint4 v = src[i];
           const uint16_t* e8 = reinterpret_cast<const uint16_t*>(&v);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const int flat = 8 * i + q, rr = flat / p.r, j = flat % p.r;
-            sBt[j * kTileO + rr] = __ushort_as_bfloat16(e8[q]);
+          for (int qq = 0; qq < 8; ++qq) {
+            const int flat = 8 * i + qq, rr = flat / P.r, j = flat % P.r;
+            sBt[j * kTileO + rr] = __ushort_as_bfloat16(e8[qq]);
           }
         }
       } else {
-        for (int i = et0; i < rows * p.r; i += kEpiThreads) {
-          const int rr = i / p.r, j = i % p.r;
-          sBt[j * kTileO + rr] = p.Blora[(o0 + rr) * p.r + j];
+        for (int i = et0; i < rows * P.r; i += kEpiThreads) {
+          const int rr = i / P.r, j = i % P.r;
+          sBt[j * kTileO + rr] = P.B[(o0 + rr) * P.r + j];
         }
       }
     }
@@ -562,36 +786,42 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
     ok = wait_or_abort(smem_u32(&S.d_full), 0, abort_flag) && ok;
     tc_fence_after();
     if (threadIdx.x == 64) PL_TL(7);
-    pdl_wait();  // the row scales belong to this call's prologue
+    pdl_wait();  // the row scales and t belong to this call's prologue
     const int et = threadIdx.x - 64;  // 0 .. 255
     if (et < N) S.rowscale[et] = et < p.M ? p.rowscale[et] : 0.f;
     go = named_bar_and(1, kEpiThreads, ok && !*abort_flag);  // one decision, publishes the row scales
     if (threadIdx.x == 64) PL_TL(8);
     if (go) {
       float* red = reinterpret_cast<float*>(smem);  // [N][128]    s_g c_n D1, reuses the stages
-      float* tred = red + N * kTileO;                // [N][kTStride]  c_n Dt: this CTA's slice of t
       const float s_g = S.s_g;
       const int half = N / 2;  // 8, 16, 24 or 32 tokens per thread
       const int n0 = g * half;
-      const bool trow = lora && quarter < 2;  // lanes 0..63 hold rows of t
       const uint32_t acc = tmem + lane_addr + kColAcc + static_cast<uint32_t>(n0);
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) {
-        if (cb * 8 < half) {  // 8 tokens at a time: the two halves of D1 (and of Dt)
-          uint32_t da[8], db[8], ta[8], tb[8];
+        if (cb * 8 < half) {  // 8 tokens at a time: the two halves of D1
+          uint32_t da[8], db[8];
           tmem_ld8(acc + cb * 8, da);
           tmem_ld8(acc + 64 + cb * 8, db);
-          if (trow) {
-            tmem_ld8(acc + 128 + cb * 8, ta);
-            tmem_ld8(acc + 192 + cb * 8, tb);
-          }
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int n = n0 + cb * 8 + i;
             red[n * kTileO + row] = s_g * S.rowscale[n] * (__uint_as_float(da[i]) + __uint_as_float(db[i]));
-            if (trow) tred[n * kTStride + row] = S.rowscale[n] * (__uint_as_float(ta[i]) + __uint_as_float(tb[i]));
           }
+        }
+      }
+      // lambda t of this projection (zeros past r), from the prologue
+      if (lora) {
+        float* tful = red + N * kTileO;  // [N][kTStride]
+        const int mt = static_cast<int>(p.M < N ? p.M : N);
+        const int r4 = (P.r + 3) / 4;
+        for (int e = et; e < mt * r4; e += kEpiThreads) {
+          const int n = e / r4, jj = 4 * (e % r4);
+          const float* tr = p.t + static_cast<int64_t>(n) * p.t_ld + P.toff + jj;
+          reinterpret_cast<float4*>(tful + n * kTStride + jj)[0] =
+              make_float4(P.lambda * tr[0], jj + 1 < P.r ? P.lambda * tr[1] : 0.f,
+                          jj + 2 < P.r ? P.lambda * tr[2] : 0.f, jj + 3 < P.r ? P.lambda * tr[3] : 0.f);
         }
       }
     }
@@ -600,46 +830,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
   tc_fence_before();
   __syncthreads();
   // ------------------------------------------------------------------ epilogue, part 2
-  // After a cluster barrier every CTA sums the t slices of all S CTAs (split order) into
-  // lambda t, then the D1 partials of its row groups (4 rows each, groups
-  // [32 split / S, 32 (split+1) / S)), adds B (lambda t) and writes y.
-  cluster_sync();
+  // After a cluster barrier every CTA sums the D1 partials of its row groups (4 rows each,
+  // groups [32 split / S, 32 (split+1) / S)) over the S CTAs in split order, adds
+  // B (lambda t) and writes y.
+  if (p.splits > 1) cluster_sync();
   if (threadIdx.x == 0) PL_TL(10);
   if (threadIdx.x >= 64 && threadIdx.x < 64 + kEpiThreads && go) {
     const int et = threadIdx.x - 64;
     float* red = reinterpret_cast<float*>(smem);
-    float* tred = red + N * kTileO;
-    float* tful = tred + N * kTStride;  // [N][kTStride]: lambda t
-    const uint32_t red_addr = smem_u32(red), tred_addr = smem_u32(tred);
+    const float* tful = red + N * kTileO;
+    const uint32_t red_addr = smem_u32(red);
     const int mt = static_cast<int>(p.M < N ? p.M : N);
-    if (lora) {
-      const int rq = (p.r + 3) / 4;  // groups of 4 adapter rows
-      for (int e = et; e < mt * rq; e += kEpiThreads) {
-        const int n = e / rq, jj = 4 * (e % rq);
-        const uint32_t addr = tred_addr + static_cast<uint32_t>((n * kTStride + jj) * 4);
-        float4 part[kMaxSplit];
-#pragma unroll
-        for (int sp = 0; sp < kMaxSplit; ++sp)
-          if (sp < p.splits) part[sp] = ld_dsmem_f32x4(mapa_shared(addr, sp));
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int sp = 0; sp < kMaxSplit; ++sp)
-          if (sp < p.splits) {
-            acc.x += part[sp].x;
-            acc.y += part[sp].y;
-            acc.z += part[sp].z;
-            acc.w += part[sp].w;
-          }
-        // adapter rows past r (accumulator lanes that hold don't-care sums) become zeros
-        reinterpret_cast<float4*>(tful + n * kTStride + jj)[0] =
-            make_float4(jj < p.r ? p.lambda * acc.x : 0.f, jj + 1 < p.r ? p.lambda * acc.y : 0.f,
-                        jj + 2 < p.r ? p.lambda * acc.z : 0.f, jj + 3 < p.r ? p.lambda * acc.w : 0.f);
-      }
-      named_bar(1, kEpiThreads);
-    }
     // This CTA's share of the tile's rows: groups of 4 rows [g0, g1) of 32.  Thread et takes
-    // row r0 + et % nrows and every ngrp-th token from et / nrows; it holds the row of B in
-    // registers, sums the D1 partials of the S CTAs (split order) and adds B (lambda t).
+    // row r0 + et % nrows and every ngrp-th token from et / nrows; it sums the D1 partials
+    // of the S CTAs (split order) and adds B (lambda t).
     const int g0 = (split * (kTileO / 4)) / p.splits, g1 = ((split + 1) * (kTileO / 4)) / p.splits;
     const int r0 = 4 * g0, nrows = 4 * (g1 - g0);
     const int ngrp = kEpiThreads / nrows;  // >= 2: a share has at most 128 rows
@@ -647,7 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
     if (tg < ngrp) {
       const int rr = r0 + rl;
       const int64_t oo = static_cast<int64_t>(tile) * kTileO + rr;
-      const int r4 = lora ? (p.r + 3) / 4 : 0;
+      const int r4 = lora ? (P.r + 3) / 4 : 0;
       // y[n][rr] = (sum over splits of the D1 partials) + lora, stored as FP32 or BF16
       auto finish = [&](int n, float lora_sum) {
         float d = 0.f;
@@ -664,9 +868,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
             if (sp < p.splits) d += part[sp];
         }
         const float v = d + lora_sum;
-        if (oo < p.d_o) {
-          if (p.y_f32) static_cast<float*>(p.y)[n * p.d_o + oo] = v;
-          else static_cast<__nv_bfloat16*>(p.y)[n * p.d_o + oo] = __float2bfloat16_rn(v);
+        if (oo < P.d_o) {
+          if (p.y_f32) static_cast<float*>(P.y)[n * P.d_o + oo] = v;
+          else static_cast<__nv_bfloat16*>(P.y)[n * P.d_o + oo] = __float2bfloat16_rn(v);
         }
       };
       // four tokens per round (n + i ngrp): independent FMA chains in flight; B[rr][j] comes
@@ -698,7 +902,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
     }
   }
   if (threadIdx.x == 64) PL_TL(11);
-  cluster_sync();  // peers keep their shared memory until every reader is done
+  if (p.splits > 1) cluster_sync();  // peers keep their shared memory until every reader is done
   if (threadIdx.x == 0) PL_TL(12);
   if (warp == 1) {
     tc_fence_after();
@@ -734,32 +938,20 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void*
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-struct Plan {
-  int N, rb, tiles, kc, splits, stages, la;
-  uint32_t stage_bytes;
-  size_t smem, act_smem;
-};
-
 uint32_t stage_bytes_for(int N) { return kCodesBytes + kScaleBytes + static_cast<uint32_t>(N) * 512u; }
 
-// Shared memory: `stages` stages, the ring of `la` A chunks (rb rows x 512 B each), the
-// B rows of the tile, the control block and 1 KB of alignment slack.  The ring has a
-// third slot when that costs no weight stage.  The epilogue reuses the stage region for
-// its partials ([N][128] + 2 x [N][68] FP32 < 1.1 KB x N), which two stages always cover.
-void stage_plan(int N, int rb, int& stages, int& la, uint32_t& sb, size_t& total) {
+// Shared memory of the main kernel: as many stages as fit (at most kMaxStages), the B rows
+// of the tile, the control block and 1 KB of alignment slack.  The epilogue reuses the
+// stage region for its partials and lambda t ([N][128] + [N][68] FP32 < 0.8 KB x N), which
+// two stages always cover.
+void stage_plan(int N, int& stages, uint32_t& sb, size_t& total) {
   sb = stage_bytes_for(N);
   const size_t limit = 227 * 1024;
-  auto fit = [&](int l, size_t& fixed) {
-    fixed = 1024 + static_cast<size_t>(l) * rb * 512 + kTileO * kMaxR * 2 + sizeof(Smem);
-    int st = static_cast<int>((limit - fixed) / sb);
-    st = st > kMaxStages ? kMaxStages : st;
-    return st < 2 ? 2 : st;
-  };
-  size_t fixed2, fixed3;
-  const int st2 = fit(2, fixed2), st3 = fit(kMaxLa, fixed3);
-  la = st3 >= st2 && fixed3 + static_cast<size_t>(st3) * sb <= limit ? kMaxLa : 2;
-  stages = la == kMaxLa ? st3 : st2;
-  total = (la == kMaxLa ? fixed3 : fixed2) + static_cast<size_t>(stages) * sb;
+  const size_t fixed = 1024 + kTileO * kMaxR * 2 + sizeof(Smem);
+  int st = static_cast<int>((limit - fixed) / sb);
+  st = st > kMaxStages ? kMaxStages : st;
+  stages = st < 2 ? 2 : st;
+  total = fixed + static_cast<size_t>(stages) * sb;
 }
 
 cudaError_t set_kernel_attributes() {
@@ -771,21 +963,25 @@ cudaError_t set_kernel_attributes() {
       err = cudaFuncSetAttribute(k_act<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     if (err == cudaSuccess)
       err = cudaFuncSetAttribute(k_act<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(k_pro_dec<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(k_pro_dec<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
   });
   return err;
 }
 
-// Clusters of `cs` decode CTAs that can be resident at once (cached per N and A rows).
-int max_active_clusters(int N, int rb, int cs) {
-  static int cache[kMaxN / 16 + 1][kMaxR / 8 + 1][kMaxSplit + 1];
+// Clusters of `cs` main-kernel CTAs that can be resident at once (cached per N).
+int max_active_clusters(int N, int cs) {
+  static int cache[kMaxN / 16 + 1][kMaxSplit + 1];
   static std::mutex mu;
   std::lock_guard<std::mutex> lk(mu);
-  int& c = cache[N / 16][rb / 8][cs];
+  int& c = cache[N / 16][cs];
   if (c == 0) {
-    int st, la;
+    int st;
     uint32_t sb;
     size_t total;
-    stage_plan(N, rb, st, la, sb, total);
+    stage_plan(N, st, sb, total);
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(cs * 64));
     cfg.blockDim = dim3(kThreads);
@@ -809,11 +1005,11 @@ int max_active_clusters(int N, int rb, int cs) {
 
 // Split count: minimise (waves) x (chunks per CTA + fixed per-CTA cost), the fixed
 // cost counted as 1.5 chunks; ties go to fewer splits.
-int choose_splits(int N, int rb, int tiles, int kc) {
+int choose_splits(int N, int tiles, int kc) {
   int best = 1;
   double best_cost = 1e30;
   for (int s = 1; s <= kMaxSplit && s <= kc; ++s) {
-    const int clusters = max_active_clusters(N, rb, s);
+    const int clusters = max_active_clusters(N, s);
     const int waves = (tiles + clusters - 1) / clusters;
     const double cost = waves * (static_cast<double>((kc + s - 1) / s) + 1.5);
     if (cost < best_cost - 1e-9) {
@@ -824,26 +1020,15 @@ int choose_splits(int N, int rb, int tiles, int kc) {
   return best;
 }
 
-Plan make_plan(int64_t M, int64_t d_i, int64_t d_o, int r) {
-  Plan pl{};
-  pl.N = static_cast<int>((M + 15) / 16 * 16);
-  pl.rb = r > 0 ? (r + 7) / 8 * 8 : 8;
-  pl.tiles = static_cast<int>((d_o + kTileO - 1) / kTileO);
-  pl.kc = static_cast<int>(d_i / kChunkK);
-  pl.splits = choose_splits(pl.N, pl.rb, pl.tiles, pl.kc);
-  stage_plan(pl.N, pl.rb, pl.stages, pl.la, pl.stage_bytes, pl.smem);
-  pl.act_smem = static_cast<size_t>(d_i) * 4;
-  return pl;
-}
-
 struct TcWs {
   __half* hq;
   float* rowscale;
-  __half* A16;
+  float* t;
+  int t_ld;
   size_t bytes;
 };
 
-TcWs carve(void* ws, int64_t M, int64_t d_i, int r) {
+TcWs carve(void* ws, int64_t M, int64_t d_i, int rtot) {
   TcWs w{};
   const uintptr_t b = reinterpret_cast<uintptr_t>(ws);
   size_t off = 0;
@@ -851,79 +1036,186 @@ TcWs carve(void* ws, int64_t M, int64_t d_i, int r) {
   off += align_up(static_cast<size_t>(M) * d_i * 2, 256);
   w.rowscale = reinterpret_cast<float*>(b + off);
   off += align_up(static_cast<size_t>(M) * 4, 256);
-  w.A16 = reinterpret_cast<__half*>(b + off);
-  off += align_up(static_cast<size_t>(r) * d_i * 2, 256);
+  w.t_ld = rtot > 0 ? (rtot + 3) / 4 * 4 : 4;
+  w.t = reinterpret_cast<float*>(b + off);
+  off += align_up(static_cast<size_t>(M) * w.t_ld * 4, 256);
   w.bytes = off;
   return w;
+}
+
+// Token rows per prologue cluster: enough clusters of kProMaxC CTAs to spread the row and
+// adapter work, few enough that each cluster's slice of A is read a handful of times.
+int pro_rows(int64_t M) { return M <= 16 ? 1 : (M <= 32 ? 2 : kProMaxR); }
+
+// The cluster prologue over ceil(M / R) clusters of C CTAs.
+cudaError_t launch_pro(const ProParams& pp, bool fp8, cudaStream_t stream) {
+  const int64_t n8 = pp.d_i / 8;
+  const size_t pro_smem = static_cast<size_t>(pp.R) * static_cast<size_t>((n8 + pp.C - 1) / pp.C) * 8 * 4;
+  cudaLaunchAttribute pa[2];
+  pa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pa[0].val.programmaticStreamSerializationAllowed = 1;
+  pa[1].id = cudaLaunchAttributeClusterDimension;
+  pa[1].val.clusterDim.x = static_cast<unsigned>(pp.C);
+  pa[1].val.clusterDim.y = 1;
+  pa[1].val.clusterDim.z = 1;
+  cudaLaunchConfig_t c1{};
+  c1.gridDim = dim3(static_cast<unsigned>(((pp.M + pp.R - 1) / pp.R) * pp.C));
+  c1.blockDim = dim3(kProThreads);
+  c1.dynamicSmemBytes = pro_smem;
+  c1.stream = stream;
+  c1.attrs = pa;
+  c1.numAttrs = 2;
+  return fp8 ? cudaLaunchKernelEx(&c1, k_pro_dec<true>, pp) : cudaLaunchKernelEx(&c1, k_pro_dec<false>, pp);
 }
 
 }  // namespace
 
 bool tc_supported(int64_t M, int64_t d_i, int64_t, int r) {
-  // k_act holds a token row of at most 32768 elements in the registers of one CTA
   return M >= 1 && M <= kMaxN && d_i >= kChunkK && d_i % kChunkK == 0 && d_i <= 32768 && r >= 0 && r <= kMaxR;
+}
+
+bool tc_group_supported(int64_t M, int64_t d_i, const TcProj* projs, int n_proj) {
+  if (n_proj < 1 || n_proj > kMaxProj || !tc_supported(M, d_i, 1, 0)) return false;
+  int rtot = 0;
+  for (int i = 0; i < n_proj; ++i) {
+    if (projs[i].r < 0 || projs[i].r > kMaxR) return false;
+    rtot += projs[i].r;
+  }
+  return rtot <= kMaxRTot;
 }
 
 size_t tc_workspace_bytes(int64_t M, int64_t d_i, int64_t, int r) { return carve(nullptr, M, d_i, r).bytes; }
 
-cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
+size_t tc_group_workspace_bytes(int64_t M, int64_t d_i, int rtot) { return carve(nullptr, M, d_i, rtot).bytes; }
+
+cudaError_t launch_linear_tc_group(const void* x, int64_t M, int64_t d_i, const float* w_norm, const float* z,
+                                   int64_t z_ld, float eps, const TcProj* projs, int n_proj, bool y_f32, void* ws,
+                                   cudaStream_t stream) {
   cudaError_t e = set_kernel_attributes();
   if (e != cudaSuccess) return e;
-  const Plan pl = make_plan(a.M, a.d_i, a.d_o, a.r);
-  const TcWs w = carve(a.ws, a.M, a.d_i, a.r);
+  int rtot = 0, tiles = 0;
+  for (int i = 0; i < n_proj; ++i) {
+    rtot += projs[i].r;
+    tiles += static_cast<int>((projs[i].d_o + kTileO - 1) / kTileO);
+  }
+  const TcWs w = carve(ws, M, d_i, rtot);
+  const int N = static_cast<int>((M + 15) / 16 * 16);
+  const int kc = static_cast<int>(d_i / kChunkK);
+  const int splits = choose_splits(N, tiles, kc);
+  int stages;
+  uint32_t sb;
+  size_t smem;
+  stage_plan(N, stages, sb, smem);
+
   TcMaps maps;
-  bool ok = encode_2d(&maps.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.codes, a.d_i / 2, a.d_o, 128, kTileO,
-                      CU_TENSOR_MAP_SWIZZLE_128B) &&
-            encode_2d(&maps.scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.scales, a.d_i / 16, a.d_o, 16, kTileO,
-                      CU_TENSOR_MAP_SWIZZLE_NONE) &&
-            encode_2d(&maps.hq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.hq, a.d_i, a.M, 64, pl.N,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
-  if (ok && a.r > 0)
-    ok = encode_2d(&maps.alora, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.A16, a.d_i, a.r, 64, pl.rb,
-                   CU_TENSOR_MAP_SWIZZLE_128B);
-  else
-    maps.alora = maps.hq;  // unused
+  memset(&maps, 0, sizeof(maps));
+  bool ok = encode_2d(&maps.hq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.hq, d_i, M, 64, N, CU_TENSOR_MAP_SWIZZLE_128B);
+  for (int i = 0; i < n_proj && ok; ++i)
+    ok = encode_2d(&maps.codes[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, projs[i].codes, d_i / 2, projs[i].d_o, 128,
+                   kTileO, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         encode_2d(&maps.scales[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, projs[i].scales, d_i / 16, projs[i].d_o, 16,
+                   kTileO, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (!ok) return cudaErrorInvalidValue;
 
+  // prologue: clusters of C CTAs over R token rows each
+  ProParams pp{};
+  pp.x = static_cast<const __nv_bfloat16*>(x);
+  pp.M = M;
+  pp.d_i = d_i;
+  pp.w_norm = w_norm;
+  pp.z = w_norm != nullptr ? z : nullptr;
+  pp.z_ld = z_ld;
+  pp.eps = eps;
+  pp.hq = w.hq;
+  pp.rowscale = w.rowscale;
+  pp.t = w.t;
+  pp.t_ld = w.t_ld;
+  pp.R = pro_rows(M);
+  pp.C = kProMaxC;
+  pp.n_proj = n_proj;
+  pp.rtot = rtot;
+  for (int i = 0, off = 0; i < n_proj; ++i) {
+    pp.A[i] = static_cast<const __nv_bfloat16*>(projs[i].A);
+    pp.r[i] = projs[i].A != nullptr ? projs[i].r : 0;
+    pp.toff[i] = off;
+    off += projs[i].r;
+  }
+  e = launch_pro(pp, false, stream);
+  if (e != cudaSuccess) return e;
+
+  TcParams p{};
+  p.M = M;
+  p.d_i = d_i;
+  p.N = N;
+  p.splits = splits;
+  p.kc = kc;
+  p.stages = stages;
+  p.stage_bytes = sb;
+  p.n_proj = n_proj;
+  p.t_ld = w.t_ld;
+  p.rowscale = w.rowscale;
+  p.t = w.t;
+  p.y_f32 = y_f32 ? 1 : 0;
+  for (int i = 0, off = 0, t0 = 0; i < n_proj; ++i) {
+    const bool lora = projs[i].r > 0 && projs[i].A != nullptr && projs[i].B != nullptr;
+    p.proj[i].d_o = projs[i].d_o;
+    p.proj[i].s_g = projs[i].s_g;
+    p.proj[i].B = lora ? static_cast<const __nv_bfloat16*>(projs[i].B) : nullptr;
+    p.proj[i].y = projs[i].y;
+    p.proj[i].r = lora ? projs[i].r : 0;
+    p.proj[i].toff = off;
+    p.proj[i].tile0 = t0;
+    p.proj[i].lambda = projs[i].lambda;
+    off += projs[i].r;
+    t0 += static_cast<int>((projs[i].d_o + kTileO - 1) / kTileO);
+  }
   cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attrs[0].val.programmaticStreamSerializationAllowed = 1;
   attrs[1].id = cudaLaunchAttributeClusterDimension;
-  attrs[1].val.clusterDim.x = static_cast<unsigned>(pl.splits);
+  attrs[1].val.clusterDim.x = static_cast<unsigned>(splits);
   attrs[1].val.clusterDim.y = 1;
   attrs[1].val.clusterDim.z = 1;
-
-  e = launch_act_prologue(a, w.hq, w.rowscale, w.A16, nullptr, 0, stream);
-  if (e != cudaSuccess) return e;
-
-  TcParams p{};
-  p.M = a.M;
-  p.d_i = a.d_i;
-  p.d_o = a.d_o;
-  p.N = pl.N;
-  p.r = a.r;
-  p.rb = pl.rb;
-  p.tiles = pl.tiles;
-  p.splits = pl.splits;
-  p.kc = pl.kc;
-  p.stages = pl.stages;
-  p.la = pl.la;
-  p.stage_bytes = pl.stage_bytes;
-  p.lambda = a.lambda;
-  p.s_g = a.s_g;
-  p.rowscale = w.rowscale;
-  p.Blora = static_cast<const __nv_bfloat16*>(a.B);
-  p.y = a.y;
-  p.y_f32 = a.y_f32 ? 1 : 0;
-
   cudaLaunchConfig_t c2{};
-  c2.gridDim = dim3(static_cast<unsigned>(pl.tiles * pl.splits));
+  c2.gridDim = dim3(static_cast<unsigned>(tiles * splits));
   c2.blockDim = dim3(kThreads);
-  c2.dynamicSmemBytes = pl.smem;
+  c2.dynamicSmemBytes = smem;
   c2.stream = stream;
   c2.attrs = attrs;
   c2.numAttrs = 2;
   return cudaLaunchKernelEx(&c2, k_tc_decode, maps, p);
+}
+
+cudaError_t launch_pro_fp8(const void* x, int64_t M, int64_t d_i, const float* w_norm, const float* z, int64_t z_ld,
+                           float eps, const void* A, int r, uint8_t* qx, float* s_x, float* t, int t_ld,
+                           cudaStream_t stream) {
+  cudaError_t e = set_kernel_attributes();
+  if (e != cudaSuccess) return e;
+  ProParams pp{};
+  pp.x = static_cast<const __nv_bfloat16*>(x);
+  pp.M = M;
+  pp.d_i = d_i;
+  pp.w_norm = w_norm;
+  pp.z = w_norm != nullptr ? z : nullptr;
+  pp.z_ld = z_ld;
+  pp.eps = eps;
+  pp.qx = qx;
+  pp.rowscale = s_x;
+  pp.t = t;
+  pp.t_ld = t_ld;
+  pp.R = pro_rows(M);
+  pp.C = kProMaxC;
+  pp.n_proj = 1;
+  pp.rtot = A != nullptr ? r : 0;
+  pp.A[0] = static_cast<const __nv_bfloat16*>(A);
+  pp.r[0] = pp.rtot;
+  pp.toff[0] = 0;
+  return launch_pro(pp, true, stream);
+}
+
+cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
+  TcProj pj{a.d_o, a.codes, a.scales, a.s_g, a.A, a.B, a.r, a.lambda, a.y};
+  return launch_linear_tc_group(a.x, a.M, a.d_i, a.w_norm, a.z, a.z_ld, a.eps, &pj, 1, a.y_f32, a.ws, stream);
 }
 
 cudaError_t launch_act_prologue(const LinearArgs& a, __half* hq, float* rowscale, __half* A16, float* zero,

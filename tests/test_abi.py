@@ -196,3 +196,87 @@ def test_product_path_does_not_import_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 txt = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert not re.search(r"^\s*(from|import)\s+oracle\b", txt, re.M), f
+
+
+def _proj_array(n, **kw):
+    from precision_linear_gb300 import binding as pl
+    arr = (pl.Proj * n)()
+    for i in range(n):
+        d = dict(d_o=256, codes=FAKE, scales=FAKE, s_g=FAKE, A=FAKE, B=FAKE, r=8, lam=2.0, y=FAKE)
+        d.update(kw)
+        arr[i] = pl.Proj(d["d_o"], d["codes"], d["scales"], d["s_g"], d["A"], d["B"], d["r"], d["lam"], d["y"])
+    return arr
+
+
+def test_group_argument_checks(L):
+    from precision_linear_gb300 import binding as pl
+    f = pl.lib().pl_nvfp4_lora_linear_group
+    ok = lambda arr, n=None, **kw: [_p(kw.get("x", FAKE)) if kw.get("x", FAKE) else None, kw.get("M", 4), kw.get("d_i", 256),
+                                    _p(FAKE), _p(FAKE), kw.get("z_ld", 0), ctypes.c_float(1e-6), arr,
+                                    len(arr) if n is None else n, kw.get("y_dtype", 0),
+                                    _p(kw.get("ws", FAKE)) if kw.get("ws", FAKE) else None, 1 << 30, None]
+    assert f(*ok(_proj_array(2), x=0)) == 1
+    assert f(*ok(_proj_array(2), n=0)) == 2
+    assert f(*ok(_proj_array(9))) == 2           # more than PL_MAX_GROUP
+    assert f(*ok(_proj_array(2), d_i=250)) == 2
+    assert f(*ok(_proj_array(2), y_dtype=3)) == 2
+    assert f(*ok(_proj_array(2), z_ld=100)) == 2
+    assert f(*ok(_proj_array(2, r=65))) == 4
+    assert f(*ok(_proj_array(2, codes=None))) == 1
+    assert f(*ok(_proj_array(2, B=None))) == 1   # A without B
+    assert f(*ok(_proj_array(2, y=FAKE + 8))) == 3
+    assert f(*ok(_proj_array(2, d_o=0))) == 2
+    assert f(*ok(_proj_array(2), ws=0)) == 7
+    assert pl.lib().pl_workspace_bytes_group(4, 256, _proj_array(2), 2) > 0
+    assert pl.lib().pl_workspace_bytes_group(4, 256, _proj_array(2), 0) == 0
+    assert pl.lib().pl_workspace_bytes_group(4, 250, _proj_array(2), 2) == 0
+
+
+def test_proj_struct_layout_matches_the_header(tmp_path):
+    """The binding's ctypes mirror of pl_nvfp4_proj has the C compiler's size and offsets."""
+    import shutil
+    import subprocess
+    from precision_linear_gb300 import binding as pl
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "precision_linear.h"\n'
+                   'int main(void){printf("%zu %zu %zu %zu %zu\\n", sizeof(pl_nvfp4_proj), offsetof(pl_nvfp4_proj, r),'
+                   ' offsetof(pl_nvfp4_proj, lambda), offsetof(pl_nvfp4_proj, y), offsetof(pl_nvfp4_proj, B_bf16));'
+                   'return 0;}\n')
+    exe = tmp_path / "layout"
+    subprocess.check_call([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    got = [int(v) for v in subprocess.check_output([str(exe)]).split()]
+    P = pl.Proj
+    assert got == [ctypes.sizeof(P), P.r.offset, P.lam.offset, P.y.offset, P.B.offset]
+
+
+def test_w8a8_argument_checks(L):
+    from precision_linear_gb300 import binding as pl
+    q = pl.lib().pl_w8a8_quantize_weight
+    assert q(None, 4, 32, _p(FAKE), _p(FAKE), None) == 1
+    assert q(_p(FAKE), 4, 24, _p(FAKE), _p(FAKE), None) == 2
+    assert q(_p(FAKE + 8), 4, 32, _p(FAKE), _p(FAKE), None) == 3
+    f = pl.lib().pl_w8a8_lora_linear
+
+    def args(**kw):
+        d = dict(x=FAKE, M=4, d_i=256, d_o=64, codes=FAKE, s_w=FAKE, A=FAKE, B=FAKE, r=8, z_ld=0, y_dtype=0,
+                 ws=FAKE, ws_bytes=1 << 30)
+        d.update(kw)
+        p = lambda v: _p(v) if v else None
+        return [p(d["x"]), d["M"], d["d_i"], d["d_o"], p(d["codes"]), p(d["s_w"]), p(d["A"]), p(d["B"]), d["r"],
+                ctypes.c_float(2.0), _p(FAKE), _p(FAKE), d["z_ld"], ctypes.c_float(1e-6), _p(FAKE), d["y_dtype"],
+                p(d["ws"]), d["ws_bytes"], None]
+    assert f(*args(x=0)) == 1
+    assert f(*args(d_i=192)) == 2      # d_i % 128
+    assert f(*args(d_i=64)) == 2
+    assert f(*args(M=0)) == 2
+    assert f(*args(r=65)) == 4
+    assert f(*args(B=0)) == 1
+    assert f(*args(ws=0)) == 7
+    assert f(*args(ws_bytes=16)) == 7
+    assert f(*args(z_ld=7)) == 2
+    assert f(*args(x=FAKE + 4)) == 3
+    assert pl.lib().pl_w8a8_workspace_bytes(4, 256, 64, 8) > 0
+    assert pl.lib().pl_w8a8_workspace_bytes(4, 200, 64, 8) == 0
