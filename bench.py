@@ -289,7 +289,8 @@ def run_ours(args, world, rank, local):
         us = e0.elapsed_time(e1) * 1e3 / (reps * len(sets))
         b = algorithmic_bytes(M, d_i, d_o, r)
         per_m[str(M)] = {"us_per_call": round(us, 3), "GBps": round(b / (us * 1e-6) / 1e9, 1),
-                         "TFLOPs": round(algorithmic_flops(M, d_i, d_o, r) / (us * 1e-6) / 1e12, 2)}
+                         "TFLOPs": round(algorithmic_flops(M, d_i, d_o, r) / (us * 1e-6) / 1e12, 2),
+                         "tokens_per_s_per_projection": round(M / (us * 1e-6), 1)}
     dom = max(per_m, key=lambda k: per_m[k]["us_per_call"])
     hbm_peak, _, peak_kind = measured_peaks()
     achieved = per_m[dom]["GBps"]
@@ -311,11 +312,39 @@ def run_ours(args, world, rank, local):
                 one_call(c)
             hy.copy_(y_bufs[k], non_blocking=True)  # D2H of the step's results
 
+        copy_stream = torch.cuda.Stream(dev)
+
+        def e2e_round():
+            """Every copy set once, the next step's H2D and this step's D2H on a copy stream,
+            overlapping the calls: the H2D of step k + 1 runs under the calls of step k."""
+            n = len(sets)
+            fork = torch.cuda.Event()
+            fork.record(stream)
+            copy_stream.wait_event(fork)
+            h2d = [torch.cuda.Event() for _ in range(n)]
+            done = [torch.cuda.Event() for _ in range(n)]
+            with torch.cuda.stream(copy_stream):
+                x_bufs[0].copy_(hx, non_blocking=True)
+                h2d[0].record(copy_stream)
+            for k in range(n):
+                stream.wait_event(h2d[k])
+                for c in sets[k]:
+                    one_call(c)
+                done[k].record(stream)
+                with torch.cuda.stream(copy_stream):
+                    if k + 1 < n:
+                        x_bufs[k + 1].copy_(hx, non_blocking=True)
+                        h2d[k + 1].record(copy_stream)
+                    copy_stream.wait_event(done[k])
+                    hy.copy_(y_bufs[k], non_blocking=True)
+            join = torch.cuda.Event()
+            join.record(copy_stream)
+            stream.wait_event(join)
+
         with torch.cuda.stream(stream):
             eg = torch.cuda.CUDAGraph()
             with torch.cuda.graph(eg, stream=stream):
-                for k in range(len(sets)):
-                    e2e_step(k)
+                e2e_round()
             e1g = []
             for k in range(len(sets)):
                 g = torch.cuda.CUDAGraph()
@@ -334,7 +363,9 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         ms_e2e = max_over_ranks(world, e0.elapsed_time(e1), dev)
         e2e = {"value": round(step_bytes * args.steps * world / (ms_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
-               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": round(ms_e2e / args.steps, 4)}
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": round(ms_e2e / args.steps, 4),
+               "copies": "per step one H2D of its inputs and one D2H of its results, pinned host buffers, through "
+                         "the public binding; on a copy stream so that step k+1's H2D overlaps step k's calls"}
 
     layer_dec = None
     if not args.no_layer:
@@ -349,16 +380,26 @@ def run_ours(args, world, rank, local):
                                "frac": round(prefill["layer_TFLOPs"] / bf16_peak, 4), "peak_kind": bf16_kind,
                                "peak_note": "dense BF16 cuBLAS burst; the path computes in f16 (same tensor rate)"}
 
-    extras = None
-    if not args.no_extras:
+    def guarded(fn):
         try:
-            extras = bench_noise_and_fold(dev, stream)
+            return fn(dev, stream)
         except Exception as e:  # reported, never allowed to cost the line
-            extras = {"error": f"{type(e).__name__}: {e}"}
+            return {"error": f"{type(e).__name__}: {e}"}
+
+    extras = None if args.no_extras else guarded(bench_noise_and_fold)
+    stack = None if args.no_stack else guarded(bench_stack_32b)
+    w8 = None if args.no_extras else guarded(bench_w8a8)
+    bwd = None if args.no_extras else guarded(bench_backward)
+    quant = None if args.no_extras else guarded(bench_quantize_layer)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args, budget_s=args.cpu_seconds)
+        cpu["one_thread"] = cpu_baseline_threads(args, 1, budget_s=args.cpu_seconds)
+        try:
+            cpu["larger_workloads"] = oracle_layer_timings(budget_s=args.cpu_seconds * 4)
+        except Exception as e:
+            cpu["larger_workloads"] = {"error": f"{type(e).__name__}: {e}"}
 
     if rank == 0:
         line = {
@@ -381,7 +422,7 @@ def run_ours(args, world, rank, local):
                          "traffic": profile_traffic("k_fused_decode" if paths[int(dom)] == 2 else "k_tc_decode",
                                                     f"{args.workload}/M{dom}")},
             "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu, "layer_decode": layer_dec, "prefill": prefill,
-            "aqn_and_uaq": extras,
+            "aqn_and_uaq": extras, "stack_32b": stack, "w8a8": w8, "backward": bwd, "quantize_layer_7b": quant,
             "gpu_launches": sum(launches_per_call.values()) * args.steps,
         }
         print(json.dumps(line), flush=True)
@@ -477,39 +518,59 @@ def bench_layer_decode(dev, stream, replays: int = 20):
         c = cases[p.name]
         codes, scales, s_g = pl.nvfp4_quantize(c.pop("W"))
         projs.append(dict(p=p, copies=[(codes, scales, s_g), (codes.clone(), scales.clone(), s_g.clone())], **c))
+    ws.get(max(pl.workspace_bytes(M, p.d_i, p.d_o, r) for M in wl.Ms for p in wl.projs) + (64 << 20))
     torch.cuda.synchronize()
+    by_name = {q["p"].name: q for q in projs}
+    groups = [["q", "k", "v"], ["o"], ["gate", "up"], ["down"]]
     out = {}
     with torch.cuda.stream(stream):
         for M in wl.Ms:
-            ys = [torch.empty(M, q["p"].d_o, dtype=torch.bfloat16, device=dev) for q in projs]
+            ys = {q["p"].name: torch.empty(M, q["p"].d_o, dtype=torch.bfloat16, device=dev) for q in projs}
 
-            def layer(k):
-                for q, y in zip(projs, ys):
+            def separate(k):
+                for q in projs:
                     codes, scales, s_g = q["copies"][k]
                     pl.nvfp4_lora_linear(q["x"][:M], codes, scales, s_g, q["A"], q["B"], wl.lam, q["w_norm"], q["z"],
-                                         synthetic.EPS, out=y, workspace=ws)
+                                         synthetic.EPS, out=ys[q["p"].name], workspace=ws)
 
-            layer(0)
-            layer(1)
-            torch.cuda.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                layer(0)
-                layer(1)
-            g.replay()
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(replays):
-                g.replay()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            us = e0.elapsed_time(e1) * 1e3 / (2 * replays)
+            def grouped(k):
+                for gn in groups:
+                    q0 = by_name[gn[0]]
+                    lst = [dict(zip(("codes", "scales", "s_g"), by_name[n]["copies"][k]), A=by_name[n]["A"],
+                                B=by_name[n]["B"], lam=wl.lam) for n in gn]
+                    pl.nvfp4_lora_linear_group(q0["x"][:M], lst, q0["w_norm"], q0["z"], synthetic.EPS,
+                                               outs=[ys[n] for n in gn], workspace=ws)
+
             nbytes = sum(algorithmic_bytes(M, q["p"].d_i, q["p"].d_o, r) for q in projs)
-            out[str(M)] = {"us_per_layer": round(us, 1), "GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
+            e = {}
+            for name, fn in (("separate", separate), ("grouped", grouped)):
+                fn(0)
+                fn(1)
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    fn(0)
+                    fn(1)
+                g.replay()
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(replays):
+                    g.replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                us = e0.elapsed_time(e1) * 1e3 / (2 * replays)
+                e[name] = {"us_per_layer": round(us, 1), "GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
+                           "tokens_per_s_per_layer": round(M / (us * 1e-6), 1)}
+                del g
+            best = min(e.values(), key=lambda v: v["us_per_layer"])
+            out[str(M)] = {"us_per_layer": best["us_per_layer"], "GBps": best["GBps"],
+                           "frac_of_hbm": round(best["GBps"] / measured_peaks()[0], 4), **e,
                            "paths": {q["p"].name: pl.linear_path(M, q["p"].d_i, q["p"].d_o, r) for q in projs}}
     torch.cuda.synchronize()
-    return {"workload": "layer_7b (Qwen2.5-7B decoder-layer projection set, r=32)", "per_M": out,
+    return {"workload": "layer_7b (Qwen2.5-7B decoder-layer projection set, r=32; q/k/v and gate/up share their "
+                        "norm's input)", "per_M": out,
+            "forms": "separate: seven calls; grouped: q/k/v, o, gate/up, down as four group calls",
             "timing": f"CUDA events around {replays} replays of a CUDA graph of two layers (two weight copies)"}
 
 
@@ -572,6 +633,209 @@ def bench_prefill(dev, stream, reps: int = 5, replays: int = 3):
                                        f"projection (after 2 eager warm-up calls and one replay)"}
 
 
+# ------------------------------------------------------------------------- 32B decode stack
+def _layer_weights_on_gpu(wl, layer, dev):
+    """NVFP4 weights and adapters of one layer, drawn on the device from the layer's seeds
+    (the seeded CUDA generator of synthetic.py) and quantised by the library."""
+    from precision_linear_gb300 import binding as pl
+    from precision_linear_gb300 import synthetic
+    out = {}
+    for i, p in enumerate(wl.projs):
+        sd = synthetic.proj_seed(wl, layer, i)
+        W = synthetic.weight(p.d_o, p.d_i, sd, wl.outlier_frac, device=dev)
+        codes, scales, s_g = pl.nvfp4_quantize(W)
+        del W
+        A, B = synthetic.lora(p.d_o, p.d_i, wl.r, sd, device=dev)
+        out[p.name] = dict(codes=codes, scales=scales, s_g=s_g, A=A, B=B, lam=wl.lam)
+    return out
+
+
+def bench_stack_32b(dev, stream, replays: int = 3):
+    """One decode step through the 64 layers of the Qwen2.5-32B-shaped stack (18.7 GB of
+    distinct NVFP4 weights, no reuse), at M in {1, 16, 64}: per layer q/k/v on the attention
+    norm's input, o on a plain input, gate/up on the FFN norm's input, down on a plain input.
+    Two launch forms: every projection its own call, and the projections behind one norm as
+    one group call.  GB/s of algorithmic bytes, tokens/s = M / step time."""
+    import torch
+
+    from precision_linear_gb300 import binding as pl
+    from precision_linear_gb300 import synthetic
+
+    wl = synthetic.WORKLOADS["stack_32b"]
+    Mmax = max(wl.Ms)
+    layers = [_layer_weights_on_gpu(wl, l, dev) for l in range(wl.layers)]
+    torch.cuda.synchronize()
+    # activations: one draw per input shape, shared by the layers (they do not change the
+    # weight stream, which is what the step measures)
+    act = synthetic.layer_case(wl, 0, Mmax)
+    inp = {}
+    for p in wl.projs:
+        c = act[p.name]
+        inp[p.name] = dict(x=c["x"].to(dev), w_norm=c["w_norm"].to(dev) if c["w_norm"] is not None else None,
+                           z=c["z"].to(dev) if c["z"] is not None else None)
+    for nm in ("k", "v"):  # the shared norm input stays one tensor
+        inp[nm] = inp["q"]
+    inp["up"] = inp["gate"]
+    ws = pl.Workspace(dev)
+    ws.get(256 << 20)
+    groups = [["q", "k", "v"], ["o"], ["gate", "up"], ["down"]]
+    per_layer_bytes = {M: sum(algorithmic_bytes(M, p.d_i, p.d_o, wl.r) for p in wl.projs) for M in wl.Ms}
+    res = {}
+    with torch.cuda.stream(stream):
+        for M in wl.Ms:
+            ys = {p.name: torch.empty(M, p.d_o, dtype=torch.bfloat16, device=dev) for p in wl.projs}
+
+            def separate():
+                for L in layers:
+                    for p in wl.projs:
+                        q, a = L[p.name], inp[p.name]
+                        pl.nvfp4_lora_linear(a["x"][:M], q["codes"], q["scales"], q["s_g"], q["A"], q["B"], q["lam"],
+                                             a["w_norm"], a["z"], synthetic.EPS, out=ys[p.name], workspace=ws)
+
+            def grouped():
+                for L in layers:
+                    for gnames in groups:
+                        a = inp[gnames[0]]
+                        pl.nvfp4_lora_linear_group(a["x"][:M], [L[n] for n in gnames], a["w_norm"], a["z"],
+                                                   synthetic.EPS, outs=[ys[n] for n in gnames], workspace=ws)
+
+            out = {}
+            for name, fn in (("separate", separate), ("grouped", grouped)):
+                fn()
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    fn()
+                g.replay()
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(replays):
+                    g.replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ms = e0.elapsed_time(e1) / replays
+                nb = per_layer_bytes[M] * wl.layers
+                out[name] = {"ms_per_step": round(ms, 3), "GBps": round(nb / (ms * 1e-3) / 1e9, 1),
+                             "tokens_per_s": round(M / (ms * 1e-3), 1)}
+                del g
+            best = max(out.values(), key=lambda v: v["GBps"])
+            out["best_frac_of_hbm"] = round(best["GBps"] / measured_peaks()[0], 4)
+            res[str(M)] = out
+    del layers
+    torch.cuda.synchronize()
+    return {"workload": "stack_32b (Qwen2.5-32B-shaped decode step, 64 layers, r=32, sigma=5e-3)",
+            "weights_GB": round(sum(9 * p.d_o * p.d_i // 16 for p in wl.projs) * wl.layers / 1e9, 2),
+            "per_M": res, "timing": f"CUDA events around {replays} replays of a CUDA graph of one 64-layer step"}
+
+
+# ------------------------------------------------------------------------- W8A8 and backward
+def bench_w8a8(dev, stream):
+    """The FP8 W8A8 rollout linear on the 7B layer set: decode (M in {8, 64}, one call per
+    projection, two weight copies, HBM GB/s) and M = 4096 (TFLOP/s)."""
+    import torch
+
+    from precision_linear_gb300 import binding as pl
+    from precision_linear_gb300 import synthetic
+
+    wl = synthetic.WORKLOADS["layer_7b"]
+    cases = layer_on_device(synthetic.layer_case(wl, 0, 4096), dev)
+    projs = {}
+    for p in wl.projs:
+        c = cases[p.name]
+        codes, s_w = pl.w8a8_quantize_weight(c.pop("W"))
+        projs[p.name] = dict(p=p, copies=[(codes, s_w), (codes.clone(), s_w.clone())], **c)
+    ws = pl.Workspace(dev)
+    ws.get(max(pl.lib().pl_w8a8_workspace_bytes(4096, p.d_i, p.d_o, wl.r) for p in wl.projs))
+    out = {}
+    with torch.cuda.stream(stream):
+        for M in (8, 64, 4096):
+            ys = {n: torch.empty(M, q["p"].d_o, dtype=torch.bfloat16, device=dev) for n, q in projs.items()}
+
+            def layer(k):
+                for n, q in projs.items():
+                    codes, s_w = q["copies"][k % 2]
+                    pl.w8a8_lora_linear(q["x"][:M], codes, s_w, q["A"], q["B"], wl.lam, q["w_norm"], q["z"],
+                                        synthetic.EPS, out=ys[n], workspace=ws)
+
+            us = _graph_us(stream, layer, calls=2, replays=5 if M == 4096 else 20) / 1  # per layer
+            nbytes = sum(M * (q["p"].d_i + q["p"].d_o) * 2 + q["p"].d_o * (q["p"].d_i + 4) +
+                         2 * wl.r * (q["p"].d_i + q["p"].d_o) + 8 * q["p"].d_i for q in projs.values())
+            flops = sum(algorithmic_flops(M, q["p"].d_i, q["p"].d_o, wl.r) for q in projs.values())
+            e = {"us_per_layer": round(us, 1), "GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
+                 "TFLOPs": round(flops / (us * 1e-6) / 1e12, 1)}
+            out[str(M)] = e
+    torch.cuda.synchronize()
+    return {"workload": "layer_7b, FP8 E4M3 W8A8 (per-channel weight, per-token activation scales) + LoRA r=32",
+            "per_M": out, "bytes": "d_o (d_i + 4) weight + scale bytes, adapters, activations in and out",
+            "timing": "CUDA events around replays of a CUDA graph of two layers (two weight copies)"}
+
+
+def bench_backward(dev, stream):
+    """The frozen-backbone backward (dx through the norm, dA, dB) of the 7B layer set at
+    M = 4096 (the log-prob / backward phase), TFLOP/s of 2 M (d_o d_i + r (d_i + d_o)) for dx
+    plus the adapter gradients' 4 M r (d_i + d_o)."""
+    import torch
+
+    from precision_linear_gb300 import binding as pl
+    from precision_linear_gb300 import synthetic
+
+    wl = synthetic.WORKLOADS["prefill_7b"]
+    M = wl.Ms[0]
+    cases = layer_on_device(synthetic.layer_case(wl, 0, M), dev)
+    ws = pl.Workspace(dev)
+    out, tot_us, tot_fl = {}, 0.0, 0
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(77)
+    with torch.cuda.stream(stream):
+        for p in wl.projs:
+            c = cases[p.name]
+            codes, scales, s_g = pl.nvfp4_quantize(c["W"])
+            g = torch.randn(M, p.d_o, generator=gen, device=dev).to(torch.bfloat16)
+
+            def call(k):
+                pl.nvfp4_lora_linear_backward(g, c["x"], codes, scales, s_g, c["A"], c["B"], wl.lam, c["w_norm"],
+                                              c["z"], synthetic.EPS, workspace=ws)
+
+            call(0)
+            torch.cuda.synchronize()
+            us = _graph_us(stream, call, calls=2, replays=3)
+            fl = 2 * M * (p.d_o * p.d_i + wl.r * (p.d_i + p.d_o)) + 4 * M * wl.r * (p.d_i + p.d_o)
+            out[p.name] = {"us_per_call": round(us, 1), "TFLOPs": round(fl / (us * 1e-6) / 1e12, 1)}
+            tot_us += us
+            tot_fl += fl
+            del codes, scales, s_g, g
+    torch.cuda.synchronize()
+    return {"workload": "prefill_7b layer set, backward at M=4096 (dx, dA, dB)", "per_proj": out,
+            "layer_us": round(tot_us, 1), "layer_TFLOPs": round(tot_fl / (tot_us * 1e-6) / 1e12, 1)}
+
+
+def bench_quantize_layer(dev, stream):
+    """BF16 -> NVFP4 of all seven 7B weight matrices (466 MB of BF16): bytes are the two reads
+    of 2P and the 9P/16 written, per matrix and in total."""
+    import torch
+
+    from precision_linear_gb300 import binding as pl
+    from precision_linear_gb300 import synthetic
+
+    wl = synthetic.WORKLOADS["layer_7b"]
+    Ws = [synthetic.weight(p.d_o, p.d_i, synthetic.proj_seed(wl, 0, i), device=dev) for i, p in enumerate(wl.projs)]
+    bufs = [pl.nvfp4_quantize(W) for W in Ws]
+
+    def all7(k):
+        for W, b in zip(Ws, bufs):
+            pl.nvfp4_quantize(W, *b)
+
+    us = _graph_us(stream, all7, calls=2, replays=5)
+    P = sum(W.numel() for W in Ws)
+    nbytes = 2 * P + 2 * P + 9 * P // 16
+    res = {"bf16_MB": round(2 * P / 1e6, 1), "us_per_layer": round(us, 1), "GBps": round(nbytes / (us * 1e3), 1),
+           "frac_of_hbm": round(nbytes / (us * 1e3) / measured_peaks()[0], 4)}
+    del Ws, bufs
+    torch.cuda.synchronize()
+    return res
+
+
 # ------------------------------------------------------------------------- oracle timing
 def cpu_baseline(args, budget_s: float = 15.0, max_calls: int | None = None):
     """The CPU oracle, as it stands, on a bounded sample of the same workload:
@@ -601,11 +865,98 @@ def cpu_baseline(args, budget_s: float = 15.0, max_calls: int | None = None):
     try:
         from threadpoolctl import threadpool_info
         cores = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
-    except Exception:
-        cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    except Exception:  # not installed: the BLAS pool's size as the environment sets it, else every core
+        cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1)))
     return {"value": round(done_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"{calls} oracle calls over the M sweep {list(wl.Ms)} of {args.workload} "
                       f"(dequantise + FP64 RMSNorm-AQN + FP64 matmul + LoRA), {dt:.1f} s"}
+
+
+def cpu_baseline_threads(args, threads: int, budget_s: float = 12.0):
+    """cpu_baseline in a child process whose BLAS and OpenMP pools are pinned to `threads`."""
+    env = dict(os.environ, OMP_NUM_THREADS=str(threads), OPENBLAS_NUM_THREADS=str(threads),
+               MKL_NUM_THREADS=str(threads))
+    code = ("import json, sys; sys.path.insert(0, %r); import bench, argparse; "
+            "a = argparse.Namespace(workload=%r); print(json.dumps(bench.cpu_baseline(a, budget_s=%r)))"
+            % (ROOT, args.workload, budget_s))
+    try:
+        out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                             timeout=budget_s * 4 + 60)
+        res = json.loads(out.stdout.strip().splitlines()[-1])
+        res["cores"] = threads
+        return res
+    except Exception as e:
+        return {"error": f"{type(e).__name__}: {e}"}
+
+
+def oracle_layer_timings(budget_s: float = 60.0):
+    """The oracle on the larger workloads, within a time budget (as it stands; reported, not a
+    target): the 7B layer set at M = 64 (dequantise + FP64 RMSNorm-AQN + FP64 matmul + LoRA per
+    projection), the FP64 matmul of the 7B layer set at M = 4096, and sampled layers of the
+    32B stack at M = 16 extrapolated x64.  Timing only: the packed weights are seeded random
+    bytes of the NVFP4 layout (valid codes and finite scales), since the oracle's own quantiser
+    would take minutes on these sizes and the linear's cost does not depend on the values."""
+    import numpy as np
+
+    from oracle import linear as olin
+    from oracle import nvfp4 as onv
+    from precision_linear_gb300 import synthetic
+
+    rng = np.random.default_rng(0)
+
+    def packed_weight(d_o, d_i):
+        codes = rng.integers(0, 256, size=(d_o, d_i // 2), dtype=np.uint8)
+        scales = rng.integers(0x20, 0x50, size=(d_o, d_i // 16), dtype=np.uint8)  # finite, moderate scales
+        return codes, scales, np.float32(1e-3)
+
+    def layer(wl, M, seed):
+        t = 0.0
+        for p in wl.projs:
+            codes, scales, s_g = packed_weight(p.d_o, p.d_i)
+            x = rng.standard_normal((M, p.d_i))
+            A = rng.standard_normal((wl.r, p.d_i)) * 0.02
+            B = rng.standard_normal((p.d_o, wl.r)) * 0.02
+            w = 1 + 0.1 * rng.standard_normal(p.d_i) if p.norm else None
+            z = wl.sigma * rng.standard_normal(p.d_i) if p.norm else None
+            t0 = time.perf_counter()
+            olin.nvfp4_lora_linear(x, codes, scales, s_g, A, B, wl.lam, w, z, synthetic.EPS)
+            t += time.perf_counter() - t0
+        return t
+
+    out = {"cores": os.cpu_count(), "kind": "oracle"}
+    start = time.perf_counter()
+    wl3 = synthetic.WORKLOADS["layer_7b"]
+    # config 4 first: the FP64 matmul of the whole layer set at M = 4096 (weights dequantised
+    # in FP64, untimed), then config 3: the full oracle of the layer set at M = 64
+    fl, t4, n4 = 0, 0.0, 0
+    for p in wl3.projs:
+        codes, scales, s_g = packed_weight(p.d_o, p.d_i)
+        W = onv.dequantize(codes, scales, s_g)
+        h = rng.standard_normal((4096, p.d_i))
+        t0 = time.perf_counter()
+        h @ W.T
+        t4 += time.perf_counter() - t0
+        fl += 2 * 4096 * p.d_i * p.d_o
+        n4 += 1
+        del W, h
+    out["prefill_7b_M4096_fp64_matmul"] = {"s": round(t4, 2), "TFLOPs": round(fl / max(t4, 1e-9) / 1e12, 4),
+                                           "projections": n4}
+    t3 = layer(wl3, 64, 1)
+    b3 = sum(algorithmic_bytes(64, p.d_i, p.d_o, wl3.r) for p in wl3.projs)
+    out["layer_7b_M64"] = {"s_per_layer": round(t3, 2), "GBps": round(b3 / t3 / 1e9, 4)}
+    wl5 = synthetic.WORKLOADS["stack_32b"]
+    done, t5 = [], 0.0
+    for lay in (0, 31, 63):
+        if done and time.perf_counter() - start + t5 / len(done) > budget_s:
+            break
+        t5 += layer(wl5, 16, 5000 + lay)
+        done.append(lay)
+    b5 = sum(algorithmic_bytes(16, p.d_i, p.d_o, wl5.r) for p in wl5.projs) * wl5.layers
+    step = t5 / len(done) * wl5.layers
+    out["stack_32b_M16"] = {"layers_timed": done, "s_per_step_extrapolated_x64": round(step, 1),
+                            "GBps": round(b5 / step / 1e9, 4), "tokens_per_s": round(16 / step, 4)}
+    out["wall_s"] = round(time.perf_counter() - start, 1)
+    return out
 
 
 def synthetic_ms(args):
@@ -649,7 +1000,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the M=4096 layer-set measurement")
     ap.add_argument("--no-layer", action="store_true", help="skip the 7B decoder-layer decode measurement")
-    ap.add_argument("--no-extras", action="store_true", help="skip the AQN draw and UAQ quantiser timings")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the AQN draw, UAQ quantiser, W8A8, backward and layer quantiser timings")
+    ap.add_argument("--no-stack", action="store_true", help="skip the 64-layer 32B-shaped decode step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

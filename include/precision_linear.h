@@ -120,7 +120,9 @@ pl_status pl_nvfp4_quantize(const void* W_bf16, int64_t d_o, int64_t d_i,
  * pl_nvfp4_quantize_uaq: pl_nvfp4_quantize of W' = fp32(W / s) (IEEE division of every
  *   weight): s_g = fp32(max|W'| / 2688), block scales and codes of W' under the same
  *   contract.  s == 1 is exactly pl_nvfp4_quantize.  Requirements as pl_nvfp4_quantize,
- *   plus s finite and > 0 (PL_ERR_SHAPE).
+ *   plus s finite and > 0 (PL_ERR_SHAPE).  For s >= 1 (the method's own setting) every
+ *   W / s is finite; for s < 1 the caller must keep max|W| / s below the FP32 maximum
+ *   (3.4e38), else s_g, scales and codes are not meaningful (not checked).
  * pl_uaq_fold_norm: out[i] = fp32(w_norm[i] * s), i < d (FP32 [d] in and out, device,
  *   4-byte aligned; out may equal w_norm).  Requirements: 1 <= d <= 2^40, s finite and > 0
  *   (PL_ERR_SHAPE), pointers non-NULL (PL_ERR_NULL) and 4-byte aligned (PL_ERR_ALIGN); one
@@ -241,6 +243,31 @@ pl_status pl_w8a8_lora_linear(const void* x_bf16, int64_t M, int64_t d_i, int64_
                               void* y, int y_dtype, void* workspace, size_t workspace_bytes,
                               pl_stream_t stream);
 
+/* Backward of the frozen-backbone linear (QeRL section 2.1, "Weight storage and trainable
+ * state are different budgets": the quantised backbone is frozen, the gradients train A and
+ * B and still pass through the frozen projection to the layers before it), with the
+ * RMSNorm-AQN prologue's backward when w_norm is given (w_norm and z are not trained):
+ *   u  = lambda g B;   dh = g W_hat + u A;   dA = u^T h;   dB = lambda g^T (h A^T)
+ *   dx = rho s (.) dh - rho^3 x (sum_j x_j s_j dh_j) / d_i,  s = w_norm + z_m,
+ *   rho = (mean_j x_j^2 + eps)^(-1/2),  h = RMSNorm_AQN(x)   (h = x and dx = dh without norm)
+ *  g_bf16 in : BF16 [M][d_o], the upstream gradient dL/dy
+ *  codes, scales, s_g, A_bf16, B_bf16, r, lambda: the forward call's weight and adapter
+ *  x_bf16 in : BF16 [M][d_i], the forward input; w_norm, z, z_ld, eps as in the forward
+ *  dx     out: FP32 [M][d_i];  dA out: FP32 [r][d_i] or NULL;  dB out: FP32 [d_o][r] or NULL
+ *  workspace : pl_backward_workspace_bytes(M, d_i, d_o, r, w_norm != NULL), 256-byte aligned.
+ * All contractions on tensor cores with BF16 operands (W_hat and g exact; h, u and h A^T
+ * rounded to BF16) and FP32 accumulation; every sum in a fixed order (repeatable bit for
+ * bit).  Requirements: M >= 1, d_i >= 256, d_i % 256 == 0, d_o % 8 == 0, 0 <= r <= 64; g,
+ * codes, scales, x, dx, A, B, w_norm, z, dA 16-byte aligned, dB 4-byte aligned.  Up to
+ * eight kernel launches, asynchronous. */
+size_t pl_backward_workspace_bytes(int64_t M, int64_t d_i, int64_t d_o, int r, int with_norm);
+pl_status pl_nvfp4_lora_linear_backward(const void* g_bf16, int64_t M, int64_t d_i, int64_t d_o,
+                                        const uint8_t* codes, const uint8_t* scales, const float* s_g,
+                                        const void* A_bf16, const void* B_bf16, int r, float lambda,
+                                        const void* x_bf16, const float* w_norm, const float* z,
+                                        int64_t z_ld, float eps, float* dx, float* dA, float* dB,
+                                        void* workspace, size_t workspace_bytes, pl_stream_t stream);
+
 /* Bytes of the scratch array behind pl_nvfp4_lora_linear_static_ws. */
 #define PL_STATIC_WORKSPACE_BYTES ((size_t)8 << 20)
 
@@ -260,9 +287,10 @@ pl_status pl_w8a8_lora_linear(const void* x_bf16, int64_t M, int64_t d_i, int64_
  * PL_ERR_WORKSPACE is returned, with nothing
  * launched, when pl_workspace_bytes(M, d_i, d_o, r) exceeds
  * PL_STATIC_WORKSPACE_BYTES (e.g. M = 64 decode fits for d_i up to 28672).
- * The call allocates nothing.  Its first call on a device looks up the array's
- * device address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture.  All calls share the one array and it keeps the
+ * The call allocates nothing.  Every call looks up the array's device address on the
+ * current device (cudaGetSymbolAddress; the first lookup on a device loads the module, so
+ * make the first call on a device before any stream capture).  All calls share the one
+ * array and it keeps the
  * last call's contents (nothing in it needs to start at zero): calls that may
  * overlap on the GPU -- on different streams, or concurrently from several host
  * threads -- race on it and must be serialised by the caller. */

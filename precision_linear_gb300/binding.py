@@ -63,6 +63,11 @@ _SIGNATURES = {
     "pl_w8a8_lora_linear": (ctypes.c_int, [_c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                                            ctypes.c_int, ctypes.c_float, _c_void_p, _c_void_p, _i64, ctypes.c_float,
                                            _c_void_p, ctypes.c_int, _c_void_p, ctypes.c_size_t, _c_void_p]),
+    "pl_backward_workspace_bytes": (ctypes.c_size_t, [_i64, _i64, _i64, ctypes.c_int, ctypes.c_int]),
+    "pl_nvfp4_lora_linear_backward": (ctypes.c_int, [_c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p, _c_void_p,
+                                                     _c_void_p, _c_void_p, ctypes.c_int, ctypes.c_float, _c_void_p,
+                                                     _c_void_p, _c_void_p, _i64, ctypes.c_float, _c_void_p,
+                                                     _c_void_p, _c_void_p, _c_void_p, ctypes.c_size_t, _c_void_p]),
     "pl_nvfp4_quantize_uaq": (ctypes.c_int, [_c_void_p, _i64, _i64, ctypes.c_float, _c_void_p, _c_void_p,
                                              _c_void_p, _c_void_p]),
     "pl_uaq_fold_norm": (ctypes.c_int, [_c_void_p, _i64, ctypes.c_float, _c_void_p, _c_void_p]),
@@ -373,6 +378,42 @@ def w8a8_lora_linear(x, codes, s_w, A=None, B=None, lam: float = 0.0, w_norm=Non
                                        _ptr(ws), ws.numel(), _stream(dev))
     _check(st, "pl_w8a8_lora_linear")
     return out
+
+
+def nvfp4_lora_linear_backward(g, x, codes, scales, s_g, A=None, B=None, lam: float = 0.0, w_norm=None, z=None,
+                               eps: float = 1e-6, want_adapter_grads: bool = True, workspace: Workspace | None = None):
+    """Gradients of the frozen-backbone linear for dL/dy = g (BF16 [M, d_o]): returns
+    (dx FP32 [M, d_i], dA FP32 [r, d_i] or None, dB FP32 [d_o, r] or None)."""
+    _need(g, "g", torch.bfloat16, dim=2)
+    dev = g.device
+    _need(x, "x", torch.bfloat16, dev, 2)
+    _need(codes, "codes", torch.uint8, dev, 2)
+    _need(scales, "scales", torch.uint8, dev, 2)
+    _need(s_g, "s_g", torch.float32, dev)
+    M, d_o = g.shape
+    d_i = x.shape[1]
+    r = 0
+    if A is not None or B is not None:
+        _need(A, "A", torch.bfloat16, dev, 2)
+        _need(B, "B", torch.bfloat16, dev, 2)
+        r = A.shape[0]
+    if w_norm is not None:
+        _need(w_norm, "w_norm", torch.float32, dev, 1)
+    z, z_ld = _noise(z, M, d_i, dev)
+    dx = torch.empty(M, d_i, dtype=torch.float32, device=dev)
+    dA = torch.empty(r, d_i, dtype=torch.float32, device=dev) if (r > 0 and want_adapter_grads) else None
+    dB = torch.empty(d_o, r, dtype=torch.float32, device=dev) if (r > 0 and want_adapter_grads) else None
+    need = int(lib().pl_backward_workspace_bytes(M, d_i, d_o, r, 1 if w_norm is not None else 0))
+    if workspace is None:
+        workspace = _default_ws.setdefault(dev, Workspace(dev))
+    ws = workspace.get(max(need, 256))
+    with torch.cuda.device(dev):
+        st = lib().pl_nvfp4_lora_linear_backward(_ptr(g), M, d_i, d_o, _ptr(codes), _ptr(scales), _ptr(s_g), _ptr(A),
+                                                 _ptr(B), r, float(lam), _ptr(x), _ptr(w_norm), _ptr(z), z_ld,
+                                                 float(eps), _ptr(dx), _ptr(dA), _ptr(dB), _ptr(ws), ws.numel(),
+                                                 _stream(dev))
+    _check(st, "pl_nvfp4_lora_linear_backward")
+    return dx, dA, dB
 
 
 def aqn_stage(done: int, total: int) -> int:

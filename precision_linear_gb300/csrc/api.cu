@@ -58,6 +58,8 @@ pl_status device_check() {
 }  // namespace
 
 namespace pl {
+bool device_supported() { return device_check() == PL_OK; }
+
 int sm_count() {
   int dev = 0;
   cudaGetDevice(&dev);
@@ -278,6 +280,38 @@ pl_status pl_w8a8_lora_linear(const void* x, int64_t M, int64_t d_i, int64_t d_o
   return check_launch(pl::launch_w8a8_linear(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t pl_backward_workspace_bytes(int64_t M, int64_t d_i, int64_t d_o, int r, int with_norm) {
+  if (!pl::backward_supported(M, d_i, d_o, r) || M > (1ll << 24)) return 0;
+  return pl::backward_workspace_bytes(M, d_i, d_o, r, with_norm != 0);
+}
+
+pl_status pl_nvfp4_lora_linear_backward(const void* g, int64_t M, int64_t d_i, int64_t d_o, const uint8_t* codes,
+                                        const uint8_t* scales, const float* s_g, const void* A, const void* B, int r,
+                                        float lambda, const void* x, const float* w_norm, const float* z,
+                                        int64_t z_ld, float eps, float* dx, float* dA, float* dB, void* workspace,
+                                        size_t ws_bytes, pl_stream_t stream) {
+  if (!g || !codes || !scales || !s_g || !dx || !x) return PL_ERR_NULL;
+  if (M < 1 || M > (1ll << 24) || d_o < 8 || d_o % 8 != 0 || d_o > (1ll << 31) || d_i < 256 || d_i % 256 != 0 ||
+      d_i > (1ll << 31))
+    return PL_ERR_SHAPE;
+  if (r < 0 || r > 64) return PL_ERR_RANK;
+  if (r > 0 && (A == nullptr) != (B == nullptr)) return PL_ERR_NULL;
+  if (w_norm && z && !z_ld_ok(z_ld, M, d_i)) return PL_ERR_SHAPE;
+  const bool lora = r > 0 && A != nullptr && B != nullptr;
+  if (!aligned16(g) || !aligned16(codes) || !aligned16(scales) || !aligned16(x) || !aligned16(dx) ||
+      (lora && (!aligned16(A) || !aligned16(B))) || (w_norm && !aligned16(w_norm)) || (z && !aligned16(z)) ||
+      (dA && !aligned16(dA)) || (dB && (reinterpret_cast<uintptr_t>(dB) & 3u)))
+    return PL_ERR_ALIGN;
+  const size_t need = pl_backward_workspace_bytes(M, d_i, d_o, lora ? r : 0, w_norm != nullptr);
+  if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PL_ERR_WORKSPACE;
+  pl_status st = device_check();
+  if (st != PL_OK) return st;
+  pl::BwArgs a{g, M, d_i, d_o, codes, scales, s_g, lora ? A : nullptr, lora ? B : nullptr, lora ? r : 0, lambda, x,
+               w_norm, w_norm ? z : nullptr, (w_norm && z) ? z_ld : 0, eps, dx, lora ? dA : nullptr,
+               lora ? dB : nullptr, workspace};
+  return check_launch(pl::launch_backward(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int pl_aqn_stage(int64_t done, int64_t total) {
   if (total < 1 || done < 0) return -1;
   // ten equal parts of the planned horizon, the product taken in 128 bits
@@ -311,7 +345,8 @@ pl_status pl_aqn_noise(uint64_t seed, uint32_t norm_id, uint64_t scope0, int64_t
 pl_status pl_last_device_status(pl_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return PL_ERR_CUDA;
   uint32_t bits = pl::tc_read_and_clear_status() | pl::fused_read_and_clear_status() |
-                  pl::prefill_read_and_clear_status() | pl::w8_read_and_clear_status();
+                  pl::prefill_read_and_clear_status() | pl::w8_read_and_clear_status() |
+                  pl::bw_read_and_clear_status();
   if (bits & pl::kStatusTimeout) return PL_ERR_TIMEOUT;
   return (bits & pl::kStatusRange) ? PL_ERR_RANGE : PL_OK;
 }

@@ -300,4 +300,23 @@ PL_DEVINL uint64_t smem_desc_sw128(uint32_t saddr, uint32_t sbo) {
   return d;
 }
 
+// Instruction descriptor for tcgen05.mma kind::f16 with the operands' major-ness given:
+// a_mn / b_mn = 1 reads that operand MN-major (its MN elements contiguous in shared memory).
+__host__ __device__ constexpr uint32_t idesc_f16_major(int M, int N, int ab_bf16, int a_mn, int b_mn) {
+  return idesc_f16(M, N, ab_bf16) | (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16);
+}
+
+// Shared-memory matrix descriptor, MN-major, 128-byte swizzle: swizzle atoms of 8 K-rows x
+// 64 MN elements (16-bit; one 128-byte line per K index), atoms `lbo` bytes apart along MN
+// and `sbo` bytes apart along K.
+PL_DEVINL uint64_t smem_desc_mn_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo & 0x3FFFFu) >> 4) << 16;
+  d |= static_cast<uint64_t>((sbo & 0x3FFFFu) >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;  // descriptor version (tcgen05)
+  d |= static_cast<uint64_t>(2) << 61;  // 128-byte swizzle
+  return d;
+}
+
 }  // namespace pl

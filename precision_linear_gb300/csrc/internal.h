@@ -117,12 +117,39 @@ cudaError_t launch_pro_fp8(const void* x, int64_t M, int64_t d_i, const float* w
                            float eps, const void* A, int r, uint8_t* qx, float* s_x, float* t, int t_ld,
                            cudaStream_t stream);
 
+// ---- backward.cu (frozen-backbone backward; d_i % 256 == 0, d_o % 8 == 0)
+struct BwArgs {
+  const void* g;          // bf16 [M][d_o]
+  int64_t M, d_i, d_o;
+  const uint8_t* codes;
+  const uint8_t* scales;
+  const float* s_g;
+  const void* A;          // bf16 [r][d_i] or null
+  const void* B;          // bf16 [d_o][r] or null
+  int r;                  // 0 when A or B is null
+  float lambda;
+  const void* x;          // bf16 [M][d_i]
+  const float* w_norm;    // or null
+  const float* z;
+  int64_t z_ld;
+  float eps;
+  float* dx;              // [M][d_i]
+  float* dA;              // [r][d_i] or null
+  float* dB;              // [d_o][r] or null
+  void* ws;
+};
+bool backward_supported(int64_t M, int64_t d_i, int64_t d_o, int r);
+size_t backward_workspace_bytes(int64_t M, int64_t d_i, int64_t d_o, int r, bool norm);
+cudaError_t launch_backward(const BwArgs& a, cudaStream_t stream);
+uint32_t bw_read_and_clear_status();
+
 // ---- aqn.cu: z [n_scopes][d] = sigma * Philox4x32-10 / Box-Muller normals
 cudaError_t launch_aqn_noise(uint64_t seed, uint32_t norm_id, uint64_t scope0, int64_t n_scopes, int64_t d,
                              float sigma, float* z, cudaStream_t stream);
 
 // ---- api.cu
-int sm_count();  // SMs of the current device (cached)
+int sm_count();            // SMs of the current device (cached)
+bool device_supported();   // the current device is one this library runs on (compute capability 10.3)
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 

@@ -5,9 +5,8 @@
 // device that loads the library holds it until the process exits.  Host code never
 // passes the array's name to a kernel -- on the host that name is only a stand-in
 // symbol -- but the device address that cudaGetSymbolAddress returns for the current
-// device, looked up once per device on the first call.
-#include <mutex>
-
+// device.  That lookup is made on every call (it is cheap once the module is loaded), so
+// an address never outlives a device reset or a context torn down and created again.
 #include "../../include/precision_linear.h"
 #include "internal.h"
 
@@ -15,28 +14,15 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_static_ws[PL_STATIC_WORKSPACE_BYTES];
 
-constexpr int kMaxDevices = 64;
-void* g_static_ws_addr[kMaxDevices];
-std::mutex g_static_ws_mu;
-
-// Device address of the scratch array on the current device (looked up on first use).
+// Device address of the scratch array on the current device.
 pl_status static_ws_address(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_static_ws);
+  if (e != cudaSuccess || p == nullptr) {
     cudaGetLastError();
-    return PL_ERR_DEVICE;
+    return PL_ERR_CUDA;
   }
-  std::lock_guard<std::mutex> lk(g_static_ws_mu);
-  if (g_static_ws_addr[dev] == nullptr) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_ws);
-    if (e != cudaSuccess || p == nullptr) {
-      cudaGetLastError();
-      return PL_ERR_CUDA;
-    }
-    g_static_ws_addr[dev] = p;
-  }
-  *out = g_static_ws_addr[dev];
+  *out = p;
   return PL_OK;
 }
 
@@ -50,6 +36,9 @@ extern "C" pl_status pl_nvfp4_lora_linear_static_ws(
   if (need > static_cast<size_t>(PL_STATIC_WORKSPACE_BYTES)) return PL_ERR_WORKSPACE;
   void* ws = nullptr;
   if (need != 0) {  // need == 0: invalid shape, reported by the call below
+    // on a device this library does not support the symbol has no image: report that
+    // device as unsupported, as the workspace entry point does
+    if (!pl::device_supported()) return PL_ERR_DEVICE;
     const pl_status st = static_ws_address(&ws);
     if (st != PL_OK) return st;
   }

@@ -2,6 +2,9 @@
 
     python -m precision_linear_gb300.profile_case --op linear --workload decode_proj_7b --M 64 --calls 6
     python -m precision_linear_gb300.profile_case --op quantize --workload decode_proj_7b --calls 3
+    python -m precision_linear_gb300.profile_case --op w8a8 --workload prefill_7b --M 4096 --calls 2
+    python -m precision_linear_gb300.profile_case --op backward --workload prefill_7b --M 4096 --calls 2
+    python -m precision_linear_gb300.profile_case --op group --workload layer_7b --proj 4 --M 8 --calls 3
 
 It draws the seeded workload, quantises its weight once, makes enough distinct
 weight copies that the set is larger than L2 (so each profiled launch reads its
@@ -21,7 +24,7 @@ from . import synthetic
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--op", choices=["linear", "quantize", "rmsnorm"], default="linear")
+    ap.add_argument("--op", choices=["linear", "quantize", "rmsnorm", "w8a8", "backward", "group"], default="linear")
     ap.add_argument("--workload", default="decode_proj_7b")
     ap.add_argument("--proj", type=int, default=0, help="index of the projection in the workload")
     ap.add_argument("--M", type=int, default=64)
@@ -41,6 +44,34 @@ def main(argv=None):
     if a.op == "rmsnorm":
         for _ in range(a.calls):
             pl.rmsnorm_aqn(g["x"], g["w_norm"], g["z"], synthetic.EPS)
+        torch.cuda.synchronize()
+        return
+    if a.op == "w8a8":
+        codes, s_w = pl.w8a8_quantize_weight(g["W"])
+        for _ in range(a.calls):
+            pl.w8a8_lora_linear(g["x"], codes, s_w, g["A"], g["B"], wl.lam, g["w_norm"], g["z"], synthetic.EPS)
+        torch.cuda.synchronize()
+        return
+    if a.op == "backward":
+        codes, scales, s_g = pl.nvfp4_quantize(g["W"])
+        gr = torch.randn(a.M, p.d_o, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16).to(dev)
+        for _ in range(a.calls):
+            pl.nvfp4_lora_linear_backward(gr, g["x"], codes, scales, s_g, g["A"], g["B"], wl.lam, g["w_norm"], g["z"],
+                                          synthetic.EPS)
+        torch.cuda.synchronize()
+        return
+    if a.op == "group":  # the projections of the workload behind the same norm as --proj, one group call
+        cases = synthetic.layer_case(wl, 0, a.M)
+        names = [q.name for q in wl.projs if q.norm == p.norm and q.norm is not None] or [p.name]
+        c0 = cases[names[0]]
+        projs = []
+        for n in names:
+            cc, ss, sg = pl.nvfp4_quantize(cases[n]["W"].to(dev))
+            projs.append(dict(codes=cc, scales=ss, s_g=sg, A=cases[n]["A"].to(dev), B=cases[n]["B"].to(dev),
+                              lam=wl.lam))
+        x, w, z = c0["x"].to(dev), c0["w_norm"].to(dev), c0["z"].to(dev)
+        for _ in range(a.calls):
+            pl.nvfp4_lora_linear_group(x, projs, w, z, synthetic.EPS)
         torch.cuda.synchronize()
         return
     codes, scales, s_g = pl.nvfp4_quantize(g["W"])

@@ -280,3 +280,44 @@ def test_w8a8_argument_checks(L):
     assert f(*args(x=FAKE + 4)) == 3
     assert pl.lib().pl_w8a8_workspace_bytes(4, 256, 64, 8) > 0
     assert pl.lib().pl_w8a8_workspace_bytes(4, 200, 64, 8) == 0
+
+
+def test_backward_argument_checks(L):
+    from precision_linear_gb300 import binding as pl
+    f = pl.lib().pl_nvfp4_lora_linear_backward
+
+    def args(**kw):
+        d = dict(g=FAKE, M=4, d_i=256, d_o=64, A=FAKE, B=FAKE, r=8, x=FAKE, dx=FAKE, ws=FAKE, z_ld=0)
+        d.update(kw)
+        p = lambda v: _p(v) if v else None
+        return [p(d["g"]), d["M"], d["d_i"], d["d_o"], _p(FAKE), _p(FAKE), _p(FAKE), p(d["A"]), p(d["B"]), d["r"],
+                ctypes.c_float(2.0), p(d["x"]), _p(FAKE), _p(FAKE), d["z_ld"], ctypes.c_float(1e-6), p(d["dx"]),
+                _p(FAKE), _p(FAKE), p(d["ws"]), 1 << 30, None]
+    assert f(*args(g=0)) == 1
+    assert f(*args(x=0)) == 1
+    assert f(*args(dx=0)) == 1
+    assert f(*args(d_i=128)) == 2    # d_i >= 256
+    assert f(*args(d_i=384)) == 2    # d_i % 256 (the rows of block scales feed TMA)
+    assert f(*args(d_o=60)) == 2     # d_o % 8
+    assert f(*args(r=65)) == 4
+    assert f(*args(B=0)) == 1
+    assert f(*args(ws=0)) == 7
+    assert f(*args(z_ld=3)) == 2
+    assert f(*args(g=FAKE + 8)) == 3
+    assert pl.lib().pl_backward_workspace_bytes(4, 256, 64, 8, 1) > pl.lib().pl_backward_workspace_bytes(4, 256, 64, 8, 0)
+    assert pl.lib().pl_backward_workspace_bytes(4, 250, 64, 8, 1) == 0
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_static_workspace_entry_reports_an_unsupported_device(L):
+    from precision_linear_gb300 import binding as pl
+    f = pl.lib().pl_nvfp4_lora_linear_static_ws
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+    # a valid problem on a host without a device of compute capability 10.3: the device error,
+    # not a failed symbol lookup
+    st = f(_p(FAKE), 4, 256, 256, _p(FAKE), _p(FAKE), _p(FAKE), _p(FAKE), _p(FAKE), 8, ctypes.c_float(2.0), _p(FAKE),
+           _p(FAKE), ctypes.c_float(1e-6), _p(FAKE), 0, None)
+    assert st == 5

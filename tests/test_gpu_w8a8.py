@@ -3,18 +3,23 @@ against the oracle (oracle/w8a8.py, "QuRL: Low-Precision Reinforcement Learning 
 Efficient Reasoning", reading notes, method / overall framework).
 
 The weight quantiser must be bit-exact (codes and FP32 scales).  The linear is compared
-on FP32 output with max |y - y_ref| <= 1e-2 rms(y_ref); y_ref quantises the activations
-from the FP64 RMSNorm-AQN rounded to FP32, so a few activation codes may sit one E4M3 step
-apart where h lies within FP32 rounding of a rounding boundary."""
+on FP32 output with |y - y_ref| <= 1e-2 rms(y_ref) + allowance.  The activation codes are
+an integer decision taken on FP32 values of h: where the exact quotient h / s_x lies
+within a few FP32 ulps of a midpoint between two E4M3 values, either code is a correct
+result (the kernel's FP32 h and the oracle's FP32 rounding of its FP64 h may differ by an
+ulp).  For those elements only, the allowance admits the other code: one E4M3 step times
+s_x s_w |q_w| per output.  The test also requires such elements to be rare (<= 1e-3)."""
 
 import numpy as np
 import pytest
 import torch
 
+from oracle import linear as olin
 from oracle import w8a8
+from oracle.nvfp4 import E4M3_TABLE
 from precision_linear_gb300 import binding as pl
 from precision_linear_gb300 import synthetic
-from tests.gpu_cases import DEV, assert_bf16_is_rounded_f32, assert_linear_close, np32
+from tests.gpu_cases import DEV, LINEAR_TOL, assert_bf16_is_rounded_f32, np32
 
 pytestmark = pytest.mark.gpu
 
@@ -55,6 +60,26 @@ def _case(d_o, d_i, M, r, seed, outliers=0.0):
     return {k: v.to(DEV) for k, v in c.items()}, c
 
 
+_E4M3_POS = np.unique(np.abs(E4M3_TABLE[np.isfinite(E4M3_TABLE)]))  # 0 .. 448, ascending
+_MIDS = (_E4M3_POS[:-1] + _E4M3_POS[1:]) / 2
+_AMBIG_REL = 2.0 ** -19  # 16 FP32 ulps of the quotient
+
+
+def _allowance(h, q_ref, s_ref):
+    """Per output [M, d_o]: one E4M3 step s_x s_w |q_w| summed over the activations whose exact
+    quotient 448 h / max|h| sits within _AMBIG_REL of a rounding midpoint; and their fraction."""
+    amax = np.max(np.abs(h), axis=1, keepdims=True)
+    amax = np.where(amax > 0, amax, 1.0)
+    v = np.abs(448.0 * h / amax)
+    i = np.clip(np.searchsorted(_MIDS, v), 1, len(_MIDS) - 1)
+    near = np.where(np.abs(v - _MIDS[i - 1]) < np.abs(v - _MIDS[i]), i - 1, i)
+    amb = np.abs(v - _MIDS[near]) <= _AMBIG_REL * np.maximum(v, 1e-30)
+    step = np.where(amb, _E4M3_POS[near + 1] - _E4M3_POS[near], 0.0)
+    s_x = amax[:, 0] / 448.0
+    wq = np.abs(E4M3_TABLE[q_ref]) * s_ref[:, None].astype(np.float64)
+    return (step * s_x[:, None]) @ wq.T, float(amb.mean())
+
+
 def _oracle(c_cpu, q_ref, s_ref, lam, norm=True, noise=True, lora=True, rows=None, z=None):
     x = np32(c_cpu["x"]).astype(np.float64)
     if rows is not None:
@@ -62,9 +87,27 @@ def _oracle(c_cpu, q_ref, s_ref, lam, norm=True, noise=True, lora=True, rows=Non
         if z is not None and z.ndim == 2:
             z = z[rows]
     zz = z if z is not None else (np32(c_cpu["z"]) if noise else None)
-    return w8a8.w8a8_linear(x, q_ref, s_ref, "fp8", np32(c_cpu["A"]) if lora else None,
-                            np32(c_cpu["B"]) if lora else None, lam, np32(c_cpu["w_norm"]) if norm else None,
-                            zz if norm else None, synthetic.EPS)
+    w = np32(c_cpu["w_norm"]) if norm else None
+    y = w8a8.w8a8_linear(x, q_ref, s_ref, "fp8", np32(c_cpu["A"]) if lora else None,
+                         np32(c_cpu["B"]) if lora else None, lam, w, zz if norm else None, synthetic.EPS)
+    if not norm:
+        # without the norm both sides quantise the same FP32 values (h = x, BF16) with the same
+        # FP32 operations: the codes are unique and no allowance applies
+        return y, np.zeros_like(y)
+    h = olin.rmsnorm_aqn(x, w, zz, synthetic.EPS)
+    allow, frac = _allowance(h, q_ref, s_ref)
+    assert frac <= 1e-3, f"{frac:.2e} of the activations sit at an FP32-ambiguous rounding midpoint"
+    return y, allow
+
+
+def _assert_close(y_gpu, ref, what):
+    y_ref, allow = ref
+    y = np32(y_gpu).astype(np.float64)
+    assert y.shape == y_ref.shape and np.all(np.isfinite(y)), what
+    rms = float(np.sqrt(np.mean(y_ref * y_ref)))
+    excess = np.abs(y - y_ref) - (LINEAR_TOL * rms + allow)
+    assert float(excess.max()) <= 0.0, (f"{what}: max |y - y_ref| {np.abs(y - y_ref).max():.3e}, "
+                                         f"bound {LINEAR_TOL} * rms {rms:.3e} + allowance")
 
 
 @pytest.mark.parametrize("d_o,d_i,M", [(3584, 3584, 1), (3584, 3584, 8), (3584, 3584, 64), (512, 3584, 16),
@@ -76,7 +119,7 @@ def test_w8a8_linear_matches_oracle(cuda_ok, d_o, d_i, M):
     y = pl.w8a8_lora_linear(*args, out_dtype=torch.float32)
     yb = pl.w8a8_lora_linear(*args)
     assert_bf16_is_rounded_f32(yb, y, f"w8a8 {d_o}x{d_i} M={M}")
-    assert_linear_close(y, _oracle(c, q_ref, s_ref, 2.0), f"w8a8 {d_o}x{d_i} M={M}")
+    _assert_close(y, _oracle(c, q_ref, s_ref, 2.0), f"w8a8 {d_o}x{d_i} M={M}")
 
 
 @pytest.mark.parametrize("kw", [dict(lora=False), dict(norm=False), dict(noise=False)])
@@ -88,7 +131,7 @@ def test_w8a8_variants(cuda_ok, kw):
     y = pl.w8a8_lora_linear(g["x"], codes, s_w, g["A"] if lora else None, g["B"] if lora else None, 2.0,
                             g["w_norm"] if norm else None, g["z"] if (norm and noise) else None, synthetic.EPS,
                             out_dtype=torch.float32)
-    assert_linear_close(y, _oracle(c, q_ref, s_ref, 2.0, norm, noise, lora), f"w8a8 {kw}")
+    _assert_close(y, _oracle(c, q_ref, s_ref, 2.0, norm, noise, lora), f"w8a8 {kw}")
 
 
 def test_w8a8_per_token_states_and_odd_rank(cuda_ok):
@@ -98,7 +141,7 @@ def test_w8a8_per_token_states_and_odd_rank(cuda_ok):
     z = (torch.randn(M, d_i, generator=torch.Generator().manual_seed(1)) * 1e-2)
     y = pl.w8a8_lora_linear(g["x"], codes, s_w, g["A"], g["B"], 2.0, g["w_norm"], z.to(DEV), synthetic.EPS,
                             out_dtype=torch.float32)
-    assert_linear_close(y, _oracle(c, q_ref, s_ref, 2.0, z=np32(z)), "w8a8 per-token states")
+    _assert_close(y, _oracle(c, q_ref, s_ref, 2.0, z=np32(z)), "w8a8 per-token states")
 
 
 def test_w8a8_m4096_sampled_rows(cuda_ok):
@@ -109,7 +152,7 @@ def test_w8a8_m4096_sampled_rows(cuda_ok):
     y = pl.w8a8_lora_linear(g["x"], codes, s_w, g["A"], g["B"], 2.0, g["w_norm"], g["z"], synthetic.EPS,
                             out_dtype=torch.float32)
     rows = np.unique(np.concatenate([np.arange(256, 384), np.random.default_rng(3).choice(M, 32, replace=False)]))
-    assert_linear_close(y[torch.from_numpy(rows).to(DEV)], _oracle(c, q_ref, s_ref, 2.0, rows=rows), "w8a8 M=4096")
+    _assert_close(y[torch.from_numpy(rows).to(DEV)], _oracle(c, q_ref, s_ref, 2.0, rows=rows), "w8a8 M=4096")
     assert pl.last_device_status() == 0
 
 

@@ -6,7 +6,8 @@ serving path), so it keeps its scratch in a library-owned device array instead o
 a caller workspace.  Here it is called through the C ABI and must match the
 workspace entry point, within the linear tolerance of the other tests, on two
 calls in a row (the second call starts from whatever the first left in the shared
-array); a problem too large for the array is refused before anything launches.
+array); a problem too large for the array is refused before anything launches.  Both entry points
+are also compared with the FP64 oracle on the oracle's own encoding of the weight.
 """
 
 import ctypes
@@ -17,6 +18,7 @@ import torch
 
 from precision_linear_gb300 import binding as pl
 from precision_linear_gb300 import build
+from oracle import linear as olin
 from tests.gpu_cases import LINEAR_TOL, make_case, np32, oracle_quantize, to_dev_nvfp4
 
 pytestmark = pytest.mark.gpu
@@ -53,6 +55,12 @@ def test_static_workspace_matches_workspace_entry(cuda_ok, static_entry, d_o, d_
                                out_dtype=torch.float32)
     torch.cuda.synchronize()
     rms = float(torch.sqrt(torch.mean(ref.double() ** 2)))
+    # the FP64 oracle on the same weights, for both entry points
+    packed, sb, sg = oracle_quantize(case["W"])
+    y_oracle = olin.nvfp4_lora_linear(np32(case["x"]).astype(np.float64), packed, sb, sg, np32(case["A"]),
+                                      np32(case["B"]), 2.0, np32(w_norm) if norm else None,
+                                      np32(z) if norm else None, 1e-6)
+    rms_o = float(np.sqrt(np.mean(y_oracle ** 2)))
     stream = _P(torch.cuda.current_stream().cuda_stream)
     for call in range(2):
         y = torch.full((M, d_o), float("nan"), dtype=torch.float32, device="cuda")
@@ -62,6 +70,8 @@ def test_static_workspace_matches_workspace_entry(cuda_ok, static_entry, d_o, d_
         torch.cuda.synchronize()
         err = float(torch.max(torch.abs(y.double() - ref.double())))
         assert np.isfinite(err) and err <= LINEAR_TOL * rms, (call, err, rms)
+        err_o = float(np.max(np.abs(np32(y).astype(np.float64) - y_oracle)))
+        assert err_o <= LINEAR_TOL * rms_o, (call, "vs oracle", err_o, rms_o)
     assert pl.last_device_status() == 0
 
 
