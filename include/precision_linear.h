@@ -338,7 +338,8 @@ pl_status pl_aqn_noise(uint64_t seed, uint32_t norm_id, uint64_t scope0, int64_t
 pl_status pl_last_device_status(pl_stream_t stream);
 
 /* Test hook: which kernel path pl_nvfp4_lora_linear takes for this shape on the
- * current device: 2 = one fused tcgen05 kernel (every CTA's K slice on chip),
+ * current device with one noise vector per call (z_ld = 0; with one per row, path 2 becomes
+ * path 1): 2 = one fused tcgen05 kernel (every CTA's K slice on chip),
  * 1 = tcgen05 prologue + main kernel (M <= 64), 3 = large-M tcgen05 path (row
  * prologue, LoRA down-projection, persistent NVFP4 GEMM), 0 = generic CUDA-core
  * kernels, -1 = invalid shape or unsupported device.  Launches nothing. */

@@ -175,7 +175,9 @@ pl_status pl_nvfp4_lora_linear(const void* x, int64_t M, int64_t d_i, int64_t d_
                    y_dtype == PL_DTYPE_F32,
                    workspace, ws_bytes};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (pl::fused_supported(M, d_i, d_o, a.r)) return check_launch(pl::launch_linear_fused(a, s));
+  // the one-kernel path takes one noise vector per call; per-row states go to the two-kernel
+  // path, whose prologue reads them row by row
+  if (a.z_ld == 0 && pl::fused_supported(M, d_i, d_o, a.r)) return check_launch(pl::launch_linear_fused(a, s));
   if (pl::tc_supported(M, d_i, d_o, a.r)) return check_launch(pl::launch_linear_tc(a, s));
   if (pl::prefill_supported(M, d_i, d_o, a.r)) return check_launch(pl::launch_linear_prefill(a, s));
   return check_launch(pl::launch_linear_generic(a, s));

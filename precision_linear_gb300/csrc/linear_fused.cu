@@ -94,7 +94,6 @@ struct FParams {
   const float* s_g;
   const float* w_norm;
   const float* z;
-  int64_t z_ld;  // 0: z is one vector for every row; else row m's vector is z + m z_ld
   const __nv_bfloat16* B;
   void* y;
   int y_f32;
@@ -170,40 +169,25 @@ PL_DEVINL int owner_row0(int s, int S) { return (s * kTileO) / S; }
 // slab q / 8, column q % 8; one piece per lane per chunk), so its eight values of
 // w_norm + z per piece stay in registers for every row, and the row's pieces stay in
 // registers between the two passes.  Out of line: it is called from two roles.
-// kRowZ: one noise vector per token row (zrows = z + k0 of this CTA's slice, rows z_ld
-// floats apart); the row's w_norm + z is then formed as the row is taken, w_norm from
-// shared memory and z from global memory.
-template <bool kRowZ>
 __device__ __noinline__ void convert_rows_warp(uint8_t* smem, uint32_t off_x, const float* gsh, float* qrecv, Ctrl* C,
                                                int N, int nslab, int M, int S, int me, bool norm,
-                                               const float* zrows, int64_t z_ld, volatile int* abort_flag) {
+                                               volatile int* abort_flag) {
   constexpr int kRows = 1;
   const int lane = threadIdx.x & 31;
   const int nk = nslab / 4;  // pieces per lane: one per chunk
   const int ch = lane & 7;
   float g[kMaxChunks][8];
-  // w_norm (+ the shared z, already added in shared memory) of this lane's pieces, plus
-  // row n's own z when there is one per row
-  auto load_g = [&](int n) {
 #pragma unroll
-    for (int k = 0; k < kMaxChunks; ++k) {
-      float4 ga = make_float4(1.f, 1.f, 1.f, 1.f), gb = ga;
-      if (norm && k < nk) {
-        const float4* g4 = reinterpret_cast<const float4*>(gsh) + (lane + 32 * k) * 2;
-        ga = g4[0];
-        gb = g4[1];
-        if (kRowZ) {
-          const float4* z4 = reinterpret_cast<const float4*>(zrows + static_cast<int64_t>(n) * z_ld) + (lane + 32 * k) * 2;
-          const float4 za = z4[0], zb = z4[1];
-          ga.x += za.x; ga.y += za.y; ga.z += za.z; ga.w += za.w;
-          gb.x += zb.x; gb.y += zb.y; gb.z += zb.z; gb.w += zb.w;
-        }
-      }
-      g[k][0] = ga.x; g[k][1] = ga.y; g[k][2] = ga.z; g[k][3] = ga.w;
-      g[k][4] = gb.x; g[k][5] = gb.y; g[k][6] = gb.z; g[k][7] = gb.w;
+  for (int k = 0; k < kMaxChunks; ++k) {
+    float4 ga = make_float4(1.f, 1.f, 1.f, 1.f), gb = ga;
+    if (norm && k < nk) {
+      const float4* g4 = reinterpret_cast<const float4*>(gsh) + (lane + 32 * k) * 2;
+      ga = g4[0];
+      gb = g4[1];
     }
-  };
-  if (!kRowZ) load_g(0);
+    g[k][0] = ga.x; g[k][1] = ga.y; g[k][2] = ga.z; g[k][3] = ga.w;
+    g[k][4] = gb.x; g[k][5] = gb.y; g[k][6] = gb.z; g[k][7] = gb.w;
+  }
   // byte offset of this lane's piece k within a row n: slab (lane + 32 k) / 8, column ch
   auto piece = [&](int n, int k) {
     return off_x + static_cast<uint32_t>(n * 128 + ((lane >> 3) + 4 * k) * N * 128 + ((ch ^ (n & 7)) << 4));
@@ -214,7 +198,6 @@ __device__ __noinline__ void convert_rows_warp(uint8_t* smem, uint32_t off_x, co
     if (lane == 0) base = atomicAdd(&C->next_row, kRows);
     base = __shfl_sync(0xFFFFFFFFu, base, 0);
     if (base >= M || *abort_flag) break;
-    if (kRowZ) load_g(base);
     uint4 v[kRows][kMaxChunks];
     float ss[kRows], mx[kRows];
 #pragma unroll
@@ -364,9 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
   const int c0 = (me * p.kc) / S, c1 = ((me + 1) * p.kc) / S;
   const int nch = c1 - c0;
   const int nslab = nch * 4;  // 64-element k slabs of this CTA
-  const bool lora = p.r > 0, norm = p.w_norm != nullptr;
-  // one noise vector for every row (added to w_norm once, in shared memory), or one per row
-  const bool noise = norm && p.z != nullptr && p.z_ld == 0, row_noise = norm && p.z != nullptr && p.z_ld != 0;
+  const bool lora = p.r > 0, norm = p.w_norm != nullptr, noise = norm && p.z != nullptr;
   const int R0 = owner_row0(me, S), rows_own = owner_row0(me + 1, S) - R0;
   const int32_t row0 = tile * kTileO;
   const uint32_t sbase = smem_u32(smem);
@@ -440,13 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused_decode(const __grid_const
   const float* gsh = reinterpret_cast<const float*>(smem + p.off_gw);
 
   auto convert_rows = [&]() {
-    if (row_noise) {
-      pdl_wait();  // z may come from the preceding kernel
-      convert_rows_warp<true>(smem, p.off_x, gsh, qrecv, &C, N, nslab, M, S, me, norm,
-                              p.z + static_cast<int64_t>(c0) * kChunkK, p.z_ld, abort_flag);
-    } else {
-      convert_rows_warp<false>(smem, p.off_x, gsh, qrecv, &C, N, nslab, M, S, me, norm, nullptr, 0, abort_flag);
-    }
+    convert_rows_warp(smem, p.off_x, gsh, qrecv, &C, N, nslab, M, S, me, norm, abort_flag);
   };
 
   auto issue_d1 = [&](int q) {
@@ -1014,7 +989,6 @@ cudaError_t launch_linear_fused(const LinearArgs& a, cudaStream_t stream) {
   p.s_g = a.s_g;
   p.w_norm = a.w_norm;
   p.z = a.z;
-  p.z_ld = a.z_ld;
   p.B = static_cast<const __nv_bfloat16*>(a.B);
   p.y = a.y;
   p.y_f32 = a.y_f32 ? 1 : 0;

@@ -59,8 +59,10 @@ def test_rmsnorm_rows_with_a_padded_stride(cuda_ok):
     assert float(rel.max()) <= NORM_REL_TOL
 
 
-# Every kernel path of the linear: fused decode (3584^2), two-kernel decode (the 7B gate
-# and down shapes), large M (CTA pairs), generic CUDA cores (d_i % 256 != 0).
+# Every kernel path of the linear: the shapes of the one-kernel decode path (3584^2; with
+# one state per row they take the two-kernel path, whose prologue reads the rows), two-kernel
+# decode (the 7B gate and down shapes), large M (CTA pairs), generic CUDA cores
+# (d_i % 256 != 0).
 @pytest.mark.parametrize("d_o,d_i,M,path", [
     (3584, 3584, 8, 2), (3584, 3584, 64, 2),
     (18944, 3584, 8, 1), (3584, 18944, 64, 1),
@@ -69,7 +71,7 @@ def test_rmsnorm_rows_with_a_padded_stride(cuda_ok):
 ])
 def test_linear_with_per_token_states(cuda_ok, d_o, d_i, M, path):
     r, seed = 32, d_o + M
-    assert pl.linear_path(M, d_i, d_o, r) == path
+    assert pl.linear_path(M, d_i, d_o, r) == path  # the path with one state per call
     sig = pl.aqn_sigma(2, 0.01, 0.0005)
     z_dev, z_ref = _states(99, 1, 7 * M, M, d_i, sig)
     case = make_case(d_o, d_i, M, r, 1e-2, seed, 0.0)
