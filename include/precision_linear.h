@@ -71,8 +71,9 @@ typedef enum pl_status {
   PL_ERR_CUDA = 6,      /* a CUDA runtime call or kernel launch failed        */
   PL_ERR_WORKSPACE = 7, /* workspace NULL, misaligned or smaller than needed  */
   PL_ERR_TIMEOUT = 8,   /* a bounded device-side wait gave up                 */
-  PL_ERR_RANGE = 9      /* reserved: an intermediate left its number format's
+  PL_ERR_RANGE = 9,     /* reserved: an intermediate left its number format's
                            range (no current path raises it)                  */
+  PL_ERR_OVERLAP = 10   /* a batch's output overlaps another output or an input */
 } pl_status;
 
 /* Static, human-readable name of a status code.  Never NULL. */
@@ -267,6 +268,46 @@ pl_status pl_nvfp4_lora_linear_backward(const void* g_bf16, int64_t M, int64_t d
                                         const void* x_bf16, const float* w_norm, const float* z,
                                         int64_t z_ld, float eps, float* dx, float* dA, float* dB,
                                         void* workspace, size_t workspace_bytes, pl_stream_t stream);
+
+/* A batch of independent calls of the linear, each with its own input: e.g. the
+ * projections of several decode streams, or of one layer whose projections read different
+ * inputs.  One call of a batch (every field as the argument of the same name of
+ * pl_nvfp4_lora_linear): */
+typedef struct pl_nvfp4_call {
+  const void* x_bf16;      /* BF16 [M][d_i]                                               */
+  int64_t M;
+  int64_t d_o;
+  const uint8_t* codes;
+  const uint8_t* scales;
+  const float* s_g;
+  const void* A_bf16;
+  const void* B_bf16;
+  int r;
+  float lambda;
+  const float* w_norm;
+  const float* z;
+  int64_t z_ld;
+  void* y;                 /* [M][d_o] of the batch's y_dtype                             */
+} pl_nvfp4_call;
+
+/* Most calls in one batch. */
+#define PL_MAX_BATCH 8
+
+/* Workspace bytes pl_nvfp4_lora_linear_batch needs (0 for an invalid batch). */
+size_t pl_workspace_bytes_batch(int64_t d_i, const pl_nvfp4_call* calls, int n_calls);
+
+/* Every call of `calls` (a HOST array, read during the call only), with the same d_i and
+ * eps: results equal those of separate pl_nvfp4_lora_linear calls within the linear's
+ * tolerance.  The calls must be independent: no call's y may overlap another call's y or
+ * any call's x (else PL_ERR_OVERLAP, nothing launched).  Calls with the same x, M, w_norm,
+ * z and z_ld share one prologue row pass (a group).  For decode batch sizes (every M <= 64,
+ * d_i % 256 == 0, at most 8 calls, at most 4 calls per distinct input) the batch runs as one
+ * prologue and one main kernel over the weight tiles of every call, so that the weight
+ * streams of the calls overlap; otherwise the calls run one after another.  Requirements:
+ * those of pl_nvfp4_lora_linear for every call, 1 <= n_calls <= PL_MAX_BATCH. */
+pl_status pl_nvfp4_lora_linear_batch(int64_t d_i, float eps, const pl_nvfp4_call* calls, int n_calls,
+                                     int y_dtype, void* workspace, size_t workspace_bytes,
+                                     pl_stream_t stream);
 
 /* Bytes of the scratch array behind pl_nvfp4_lora_linear_static_ws. */
 #define PL_STATIC_WORKSPACE_BYTES ((size_t)8 << 20)

@@ -42,6 +42,14 @@ class Proj(ctypes.Structure):
                 ("lam", ctypes.c_float), ("y", ctypes.c_void_p)]
 
 
+class Call(ctypes.Structure):
+    """pl_nvfp4_call: one call of a batch."""
+    _fields_ = [("x", ctypes.c_void_p), ("M", ctypes.c_int64), ("d_o", ctypes.c_int64), ("codes", ctypes.c_void_p),
+                ("scales", ctypes.c_void_p), ("s_g", ctypes.c_void_p), ("A", ctypes.c_void_p), ("B", ctypes.c_void_p),
+                ("r", ctypes.c_int), ("lam", ctypes.c_float), ("w_norm", ctypes.c_void_p), ("z", ctypes.c_void_p),
+                ("z_ld", ctypes.c_int64), ("y", ctypes.c_void_p)]
+
+
 _SIGNATURES = {
     "pl_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "pl_version": (ctypes.c_int, []),
@@ -58,6 +66,9 @@ _SIGNATURES = {
     "pl_nvfp4_lora_linear_group": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, _i64, ctypes.c_float,
                                                   ctypes.POINTER(Proj), ctypes.c_int, ctypes.c_int, _c_void_p,
                                                   ctypes.c_size_t, _c_void_p]),
+    "pl_workspace_bytes_batch": (ctypes.c_size_t, [_i64, ctypes.POINTER(Call), ctypes.c_int]),
+    "pl_nvfp4_lora_linear_batch": (ctypes.c_int, [_i64, ctypes.c_float, ctypes.POINTER(Call), ctypes.c_int,
+                                                  ctypes.c_int, _c_void_p, ctypes.c_size_t, _c_void_p]),
     "pl_w8a8_workspace_bytes": (ctypes.c_size_t, [_i64, _i64, _i64, ctypes.c_int]),
     "pl_w8a8_quantize_weight": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, _c_void_p]),
     "pl_w8a8_lora_linear": (ctypes.c_int, [_c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
@@ -326,6 +337,61 @@ def nvfp4_lora_linear_group(x, projs, w_norm=None, z=None, eps: float = 1e-6, ou
         st = lib().pl_nvfp4_lora_linear_group(_ptr(x), M, d_i, _ptr(w_norm), _ptr(z), z_ld, float(eps), arr, n,
                                               _OUT_DTYPES[out_dtype], _ptr(ws), ws.numel(), _stream(dev))
     _check(st, "pl_nvfp4_lora_linear_group")
+    return ys
+
+
+def nvfp4_lora_linear_batch(calls, eps: float = 1e-6, outs=None, workspace: Workspace | None = None,
+                            out_dtype: torch.dtype = torch.bfloat16):
+    """Independent calls of the linear in one batch: calls is a sequence of dicts with keys x,
+    codes, scales, s_g and optionally A, B, lam, w_norm, z (as nvfp4_lora_linear's arguments);
+    every call has the same d_i.  Returns the list of y."""
+    n = len(calls)
+    arr = (Call * max(n, 1))()
+    ys, keep = [], []
+    d_i = None
+    for i, c in enumerate(calls):
+        x = c["x"]
+        _need(x, "x", torch.bfloat16, dim=2)
+        dev = x.device
+        M, di = x.shape
+        if d_i is None:
+            d_i = di
+        elif di != d_i:
+            raise ValueError("every call of a batch has the same d_i")
+        codes, scales, s_g = c["codes"], c["scales"], c["s_g"]
+        _need(codes, "codes", torch.uint8, dev, 2)
+        _need(scales, "scales", torch.uint8, dev, 2)
+        _need(s_g, "s_g", torch.float32, dev)
+        A, B = c.get("A"), c.get("B")
+        r = 0
+        if A is not None or B is not None:
+            _need(A, "A", torch.bfloat16, dev, 2)
+            _need(B, "B", torch.bfloat16, dev, 2)
+            r = A.shape[0]
+        w = c.get("w_norm")
+        if w is not None:
+            _need(w, "w_norm", torch.float32, dev, 1)
+        z, z_ld = _noise(c.get("z"), M, d_i, dev)
+        d_o = codes.shape[0]
+        y = outs[i] if outs is not None else torch.empty(M, d_o, dtype=out_dtype, device=dev)
+        _need(y, "out", out_dtype, dev, 2)
+        ys.append(y)
+        keep.append(z)
+        arr[i] = Call(x.data_ptr(), M, d_o, codes.data_ptr(), scales.data_ptr(), s_g.data_ptr(),
+                      A.data_ptr() if A is not None else None, B.data_ptr() if B is not None else None, r,
+                      float(c.get("lam", 0.0)), w.data_ptr() if w is not None else None,
+                      z.data_ptr() if z is not None else None, z_ld, y.data_ptr())
+    if out_dtype not in _OUT_DTYPES:
+        raise TypeError("out_dtype must be bfloat16 or float32")
+    dev = calls[0]["x"].device
+    need = int(lib().pl_workspace_bytes_batch(d_i, arr, n))
+    if workspace is None:
+        workspace = _default_ws.setdefault(dev, Workspace(dev))
+    ws = workspace.get(max(need, 256))
+    with torch.cuda.device(dev):
+        st = lib().pl_nvfp4_lora_linear_batch(d_i, float(eps), arr, n, _OUT_DTYPES[out_dtype], _ptr(ws), ws.numel(),
+                                              _stream(dev))
+    _check(st, "pl_nvfp4_lora_linear_batch")
     return ys
 
 

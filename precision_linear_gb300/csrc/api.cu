@@ -83,6 +83,7 @@ const char* pl_status_string(pl_status s) {
     case PL_ERR_WORKSPACE: return "PL_ERR_WORKSPACE: workspace missing, misaligned or too small";
     case PL_ERR_TIMEOUT: return "PL_ERR_TIMEOUT: a bounded device-side wait gave up";
     case PL_ERR_RANGE: return "PL_ERR_RANGE: an intermediate left its number format's range";
+    case PL_ERR_OVERLAP: return "PL_ERR_OVERLAP: a batch's output overlaps another output or an input";
   }
   return "unknown pl_status";
 }
@@ -183,18 +184,40 @@ pl_status pl_nvfp4_lora_linear(const void* x, int64_t M, int64_t d_i, int64_t d_
   return check_launch(pl::launch_linear_generic(a, s));
 }
 
+// Host checks shared by the group and batch entries for one projection.
+pl_status check_proj(int64_t d_o, const uint8_t* codes, const uint8_t* scales, const float* s_g, const void* A,
+                     const void* B, int r, const void* y) {
+  if (!codes || !scales || !s_g || !y) return PL_ERR_NULL;
+  if (d_o < 1 || d_o > (1ll << 31)) return PL_ERR_SHAPE;
+  if (r < 0 || r > 64) return PL_ERR_RANK;
+  if (r > 0 && (A == nullptr) != (B == nullptr)) return PL_ERR_NULL;
+  const bool lora = r > 0 && A != nullptr && B != nullptr;
+  if (!aligned16(codes) || !aligned16(scales) || !aligned16(y) || (lora && (!aligned16(A) || !aligned16(B))))
+    return PL_ERR_ALIGN;
+  return PL_OK;
+}
+
+pl::TcProj tc_proj(int64_t d_o, const uint8_t* codes, const uint8_t* scales, const float* s_g, const void* A,
+                   const void* B, int r, float lambda, void* y, int set) {
+  const bool lora = r > 0 && A != nullptr && B != nullptr;
+  return pl::TcProj{d_o, codes, scales, s_g, lora ? A : nullptr, lora ? B : nullptr, lora ? r : 0, lambda, y, set};
+}
+
 size_t pl_workspace_bytes_group(int64_t M, int64_t d_i, const pl_nvfp4_proj* projs, int n_proj) {
   if (!projs || n_proj < 1 || n_proj > PL_MAX_GROUP) return 0;
   size_t need = 0;
-  int rtot = 0;
+  pl::TcProj tp[PL_MAX_GROUP];
   for (int i = 0; i < n_proj; ++i) {
     const size_t w = pl_workspace_bytes(M, d_i, projs[i].d_o, projs[i].r);
     if (w == 0) return 0;
     need = need > w ? need : w;
-    rtot += projs[i].r;
+    tp[i] = tc_proj(projs[i].d_o, projs[i].codes, projs[i].scales, projs[i].s_g, projs[i].A_bf16, projs[i].B_bf16,
+                    projs[i].r, projs[i].lambda, projs[i].y, 0);
+    tp[i].r = projs[i].r;  // the workspace is sized for the declared ranks
   }
   if (pl::tc_supported(M, d_i, 1, 0)) {
-    const size_t g = pl::tc_group_workspace_bytes(M, d_i, rtot);
+    const pl::TcSet set{nullptr, M, nullptr, nullptr, 0};
+    const size_t g = pl::tc_batch_workspace_bytes(d_i, &set, 1, tp, n_proj);
     need = need > g ? need : g;
   }
   return need;
@@ -212,16 +235,9 @@ pl_status pl_nvfp4_lora_linear_group(const void* x, int64_t M, int64_t d_i, cons
   pl::TcProj tp[PL_MAX_GROUP];
   for (int i = 0; i < n_proj; ++i) {
     const pl_nvfp4_proj& q = projs[i];
-    if (!q.codes || !q.scales || !q.s_g || !q.y) return PL_ERR_NULL;
-    if (q.d_o < 1 || q.d_o > (1ll << 31)) return PL_ERR_SHAPE;
-    if (q.r < 0 || q.r > 64) return PL_ERR_RANK;
-    if (q.r > 0 && (q.A_bf16 == nullptr) != (q.B_bf16 == nullptr)) return PL_ERR_NULL;
-    const bool lora = q.r > 0 && q.A_bf16 != nullptr && q.B_bf16 != nullptr;
-    if (!aligned16(q.codes) || !aligned16(q.scales) || !aligned16(q.y) ||
-        (lora && (!aligned16(q.A_bf16) || !aligned16(q.B_bf16))))
-      return PL_ERR_ALIGN;
-    tp[i] = pl::TcProj{q.d_o, q.codes, q.scales, q.s_g, lora ? q.A_bf16 : nullptr, lora ? q.B_bf16 : nullptr,
-                       lora ? q.r : 0, q.lambda, q.y};
+    const pl_status st = check_proj(q.d_o, q.codes, q.scales, q.s_g, q.A_bf16, q.B_bf16, q.r, q.y);
+    if (st != PL_OK) return st;
+    tp[i] = tc_proj(q.d_o, q.codes, q.scales, q.s_g, q.A_bf16, q.B_bf16, q.r, q.lambda, q.y, 0);
   }
   const size_t need = pl_workspace_bytes_group(M, d_i, projs, n_proj);
   if (!workspace || need == 0 || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
@@ -231,13 +247,108 @@ pl_status pl_nvfp4_lora_linear_group(const void* x, int64_t M, int64_t d_i, cons
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // one launch pair for the whole group on the two-kernel decode path; otherwise one call
   // per projection, in order
-  if (n_proj > 1 && pl::tc_group_supported(M, d_i, tp, n_proj))
-    return check_launch(pl::launch_linear_tc_group(x, M, d_i, w_norm, w_norm ? z : nullptr,
-                                                   (w_norm && z) ? z_ld : 0, eps, tp, n_proj,
-                                                   y_dtype == PL_DTYPE_F32, workspace, s));
+  const pl::TcSet set{x, M, w_norm, w_norm ? z : nullptr, (w_norm && z) ? z_ld : 0};
+  if (n_proj > 1 && pl::tc_batch_supported(d_i, &set, 1, tp, n_proj))
+    return check_launch(pl::launch_linear_tc_batch(d_i, eps, &set, 1, tp, n_proj, y_dtype == PL_DTYPE_F32,
+                                                   workspace, s));
   for (int i = 0; i < n_proj; ++i) {
     st = pl_nvfp4_lora_linear(x, M, d_i, tp[i].d_o, tp[i].codes, tp[i].scales, tp[i].s_g, tp[i].A, tp[i].B, tp[i].r,
                               tp[i].lambda, w_norm, z, z_ld, eps, tp[i].y, y_dtype, workspace, ws_bytes, stream);
+    if (st != PL_OK) return st;
+  }
+  return PL_OK;
+}
+
+namespace {
+// The distinct inputs of a batch (calls with the same x, M, w_norm, z and z_ld share one) and
+// each call's index among them.
+int batch_sets(const pl_nvfp4_call* calls, int n, pl::TcSet* sets, int* which) {
+  int n_sets = 0;
+  for (int i = 0; i < n; ++i) {
+    const pl_nvfp4_call& c = calls[i];
+    const float* z = c.w_norm ? c.z : nullptr;
+    const int64_t z_ld = (c.w_norm && c.z) ? c.z_ld : 0;
+    int s = 0;
+    while (s < n_sets && !(sets[s].x == c.x_bf16 && sets[s].M == c.M && sets[s].w_norm == c.w_norm &&
+                           sets[s].z == z && sets[s].z_ld == z_ld))
+      ++s;
+    if (s == n_sets) sets[n_sets++] = pl::TcSet{c.x_bf16, c.M, c.w_norm, z, z_ld};
+    which[i] = s;
+  }
+  return n_sets;
+}
+
+bool ranges_overlap(uintptr_t a0, size_t an, uintptr_t b0, size_t bn) { return a0 < b0 + bn && b0 < a0 + an; }
+}  // namespace
+
+size_t pl_workspace_bytes_batch(int64_t d_i, const pl_nvfp4_call* calls, int n_calls) {
+  if (!calls || n_calls < 1 || n_calls > PL_MAX_BATCH) return 0;
+  size_t need = 0;
+  for (int i = 0; i < n_calls; ++i) {
+    const size_t w = pl_workspace_bytes(calls[i].M, d_i, calls[i].d_o, calls[i].r);
+    if (w == 0) return 0;
+    need = need > w ? need : w;
+  }
+  pl::TcSet sets[PL_MAX_BATCH];
+  int which[PL_MAX_BATCH];
+  const int n_sets = batch_sets(calls, n_calls, sets, which);
+  pl::TcProj tp[PL_MAX_BATCH];
+  for (int i = 0; i < n_calls; ++i)
+    tp[i] = pl::TcProj{calls[i].d_o, calls[i].codes, calls[i].scales, calls[i].s_g, calls[i].A_bf16, calls[i].B_bf16,
+                       calls[i].r, calls[i].lambda, calls[i].y, which[i]};
+  if (pl::tc_batch_supported(d_i, sets, n_sets, tp, n_calls)) {
+    const size_t g = pl::tc_batch_workspace_bytes(d_i, sets, n_sets, tp, n_calls);
+    need = need > g ? need : g;
+  }
+  return need;
+}
+
+pl_status pl_nvfp4_lora_linear_batch(int64_t d_i, float eps, const pl_nvfp4_call* calls, int n_calls, int y_dtype,
+                                     void* workspace, size_t ws_bytes, pl_stream_t stream) {
+  if (!calls) return PL_ERR_NULL;
+  if (n_calls < 1 || n_calls > PL_MAX_BATCH || d_i < 16 || d_i % 16 != 0 || d_i > (1ll << 31)) return PL_ERR_SHAPE;
+  if (y_dtype != PL_DTYPE_BF16 && y_dtype != PL_DTYPE_F32) return PL_ERR_SHAPE;
+  const size_t ysz = y_dtype == PL_DTYPE_F32 ? 4 : 2;
+  for (int i = 0; i < n_calls; ++i) {
+    const pl_nvfp4_call& c = calls[i];
+    if (!c.x_bf16) return PL_ERR_NULL;
+    if (c.M < 1 || c.M > (1ll << 24)) return PL_ERR_SHAPE;
+    if (c.w_norm && c.z && !z_ld_ok(c.z_ld, c.M, d_i)) return PL_ERR_SHAPE;
+    if (!aligned16(c.x_bf16) || (c.w_norm && !aligned16(c.w_norm)) || (c.z && !aligned16(c.z))) return PL_ERR_ALIGN;
+    const pl_status st = check_proj(c.d_o, c.codes, c.scales, c.s_g, c.A_bf16, c.B_bf16, c.r, c.y);
+    if (st != PL_OK) return st;
+  }
+  // independent calls: no output may overlap another call's output or any call's activations
+  for (int i = 0; i < n_calls; ++i) {
+    const uintptr_t yi = reinterpret_cast<uintptr_t>(calls[i].y);
+    const size_t ni = static_cast<size_t>(calls[i].M) * calls[i].d_o * ysz;
+    for (int j = 0; j < n_calls; ++j) {
+      const uintptr_t xj = reinterpret_cast<uintptr_t>(calls[j].x_bf16);
+      if (ranges_overlap(yi, ni, xj, static_cast<size_t>(calls[j].M) * d_i * 2)) return PL_ERR_OVERLAP;
+      if (j != i && ranges_overlap(yi, ni, reinterpret_cast<uintptr_t>(calls[j].y),
+                                   static_cast<size_t>(calls[j].M) * calls[j].d_o * ysz))
+        return PL_ERR_OVERLAP;
+    }
+  }
+  const size_t need = pl_workspace_bytes_batch(d_i, calls, n_calls);
+  if (!workspace || need == 0 || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return PL_ERR_WORKSPACE;
+  pl_status st = device_check();
+  if (st != PL_OK) return st;
+  pl::TcSet sets[PL_MAX_BATCH];
+  int which[PL_MAX_BATCH];
+  const int n_sets = batch_sets(calls, n_calls, sets, which);
+  pl::TcProj tp[PL_MAX_BATCH];
+  for (int i = 0; i < n_calls; ++i)
+    tp[i] = tc_proj(calls[i].d_o, calls[i].codes, calls[i].scales, calls[i].s_g, calls[i].A_bf16, calls[i].B_bf16,
+                    calls[i].r, calls[i].lambda, calls[i].y, which[i]);
+  if (n_calls > 1 && pl::tc_batch_supported(d_i, sets, n_sets, tp, n_calls))
+    return check_launch(pl::launch_linear_tc_batch(d_i, eps, sets, n_sets, tp, n_calls, y_dtype == PL_DTYPE_F32,
+                                                   workspace, reinterpret_cast<cudaStream_t>(stream)));
+  for (int i = 0; i < n_calls; ++i) {
+    const pl_nvfp4_call& c = calls[i];
+    st = pl_nvfp4_lora_linear(c.x_bf16, c.M, d_i, c.d_o, c.codes, c.scales, c.s_g, c.A_bf16, c.B_bf16, c.r, c.lambda,
+                              c.w_norm, c.z, c.z_ld, eps, c.y, y_dtype, workspace, ws_bytes, stream);
     if (st != PL_OK) return st;
   }
   return PL_OK;

@@ -50,7 +50,15 @@ size_t generic_workspace_bytes(int64_t M, int64_t d_i, int64_t d_o, int r);
 cudaError_t launch_linear_generic(const LinearArgs& a, cudaStream_t stream);
 
 // ---- linear_tc.cu (tcgen05; d_i % 256 == 0)
-// One projection of a group that reads the same input x (and norm, noise).
+// One input of a launch of the two-kernel decode path: x and its norm and noise.
+struct TcSet {
+  const void* x;  // bf16 [M][d_i]
+  int64_t M;
+  const float* w_norm;  // or null
+  const float* z;
+  int64_t z_ld;
+};
+// One projection (member) of such a launch; `set` is the index of the input it reads.
 struct TcProj {
   int64_t d_o;
   const uint8_t* codes;
@@ -61,15 +69,17 @@ struct TcProj {
   int r;          // 0 when A or B is null
   float lambda;
   void* y;        // [M][d_o]
+  int set;
 };
 bool tc_supported(int64_t M, int64_t d_i, int64_t d_o, int r);
-bool tc_group_supported(int64_t M, int64_t d_i, const TcProj* projs, int n_proj);
+// at most 8 inputs and 8 members, at most 4 members and 128 adapter rows per input, M <= 64
+bool tc_batch_supported(int64_t d_i, const TcSet* sets, int n_sets, const TcProj* projs, int n_proj);
 size_t tc_workspace_bytes(int64_t M, int64_t d_i, int64_t d_o, int r);
-size_t tc_group_workspace_bytes(int64_t M, int64_t d_i, int rtot);
+size_t tc_batch_workspace_bytes(int64_t d_i, const TcSet* sets, int n_sets, const TcProj* projs, int n_proj);
 cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream);
-cudaError_t launch_linear_tc_group(const void* x, int64_t M, int64_t d_i, const float* w_norm, const float* z,
-                                   int64_t z_ld, float eps, const TcProj* projs, int n_proj, bool y_f32, void* ws,
-                                   cudaStream_t stream);
+// one prologue over every input, one main kernel over every member's weight tiles
+cudaError_t launch_linear_tc_batch(int64_t d_i, float eps, const TcSet* sets, int n_sets, const TcProj* projs,
+                                   int n_proj, bool y_f32, void* ws, cudaStream_t stream);
 uint32_t tc_read_and_clear_status();
 cudaError_t launch_wait_timeout_probe(cudaStream_t stream);
 // The row prologue on its own: hq = f16(RMSNorm_AQN(x) / rowscale) [M][d_i], rowscale

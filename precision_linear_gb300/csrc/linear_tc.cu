@@ -80,8 +80,10 @@ constexpr int kMaxStages = 8;
 constexpr int kMaxSplit = 8;
 constexpr int kMaxN = 64;
 constexpr int kMaxR = 64;        // adapter rank of one projection
-constexpr int kMaxProj = 4;      // projections in one group
-constexpr int kMaxRTot = 128;    // adapter rows of a whole group
+constexpr int kMaxProj = 8;      // members (projections) of one launch
+constexpr int kMaxSets = 8;      // distinct inputs (x, M, norm, noise) of one launch
+constexpr int kMaxAdapt = 4;     // members reading one input
+constexpr int kMaxRTot = 128;    // adapter rows over the members reading one input
 constexpr uint32_t kTmemCols = 512;
 // tensor-memory columns: kAbuf weight (MMA A operand) buffers of 128 columns from 0, then
 // the two accumulators, N <= 64 columns each: D1 over the first and the second half of
@@ -100,20 +102,30 @@ struct TcProjDev {
   void* y;                 // [M][d_o]
   int r, toff, tile0;      // adapter rank, its first column of t, its first weight tile
   float lambda;
+  int set;                 // the input it reads
+};
+
+// One input of a launch, as the main kernel sees it.
+struct TcSetDev {
+  int64_t M;
+  int N;                   // M rounded up to 16: the MMA's N
+  const float* rowscale;   // [M]: c_m
+  const float* t;          // [M][t_ld]: t = rs A_p u of every member reading this input, at column toff_p
+  int t_ld;
 };
 
 struct TcParams {
-  int64_t M, d_i;
-  int N, splits, kc, stages, n_proj, t_ld;
-  uint32_t stage_bytes;
-  const float* rowscale;  // [M]: c_m
-  const float* t;         // [M][t_ld]: t = rs A_p u of every projection at column toff_p
+  int64_t d_i;
+  int splits, kc, n_proj;
+  uint32_t stage_region;   // shared-memory bytes for the weight ring; each CTA fits as many
+                           // stages of its own N as the region holds (at most kMaxStages)
   int y_f32;
   TcProjDev proj[kMaxProj];
+  TcSetDev set[kMaxSets];
 };
 
 struct TcMaps {
-  CUtensorMap hq;
+  CUtensorMap hq[kMaxSets];
   CUtensorMap codes[kMaxProj], scales[kMaxProj];
 };
 
@@ -127,8 +139,8 @@ struct Smem {
   float rowscale[kMaxN];
 };
 
-// Arguments of the cluster prologue.
-struct ProParams {
+// One input of the cluster prologue (its clusters start at cluster cl0).
+struct ProSet {
   const __nv_bfloat16* x;
   int64_t M, d_i;
   const float* w_norm;  // [d_i] or null (no norm)
@@ -139,9 +151,14 @@ struct ProParams {
   float* rowscale;      // [M]: c_m (f16 mode), s_x (FP8 mode)
   uint8_t* qx;          // [M][d_i] E4M3 codes (FP8 mode)
   float* t;             // [M][t_ld]
-  int t_ld, R, C, n_proj, rtot;
-  const __nv_bfloat16* A[kMaxProj];  // [r_p][d_i]
-  int r[kMaxProj], toff[kMaxProj];
+  int t_ld, R, C, n_proj, rtot, cl0;
+  const __nv_bfloat16* A[kMaxAdapt];  // [r_p][d_i]
+  int r[kMaxAdapt], toff[kMaxAdapt];
+};
+// Arguments of the cluster prologue: its inputs, one cluster range each.
+struct ProParams {
+  int n_sets;
+  ProSet set[kMaxSets];
 };
 constexpr int kProThreads = 256;
 constexpr int kProWarps = kProThreads / 32;
@@ -345,7 +362,13 @@ __global__ void __launch_bounds__(kActThreads, 2) k_act(const __nv_bfloat16* __r
 // s_x = fp32(max |h| / 448) (1 for a zero row), codes E4M3(fp32(h / s_x)), round to
 // nearest even, saturating, +0 for values that round to zero.
 template <bool kFp8>
-__global__ void __launch_bounds__(kProThreads) k_pro_dec(const __grid_constant__ ProParams p) {
+__global__ void __launch_bounds__(kProThreads) k_pro_dec(const __grid_constant__ ProParams pr) {
+  // the input this cluster works on: the last one whose first cluster is <= this one
+  int si = 0;
+#pragma unroll
+  for (int q = 1; q < kMaxSets; ++q)
+    if (q < pr.n_sets && static_cast<int>(blockIdx.x) / pr.set[0].C >= pr.set[q].cl0) si = q;
+  const ProSet& p = pr.set[si];
   extern __shared__ float4 pro_smem4[];
   float* u = reinterpret_cast<float*>(pro_smem4);  // [R][Lmax]: u = x (.) (w_norm + z), this CTA's slice
   __shared__ float red[kProWarps][kProMaxR][2];
@@ -357,7 +380,7 @@ __global__ void __launch_bounds__(kProThreads) k_pro_dec(const __grid_constant__
   uint32_t rank_u;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank_u));
   const int rank = static_cast<int>(rank_u);
-  const int64_t m0 = static_cast<int64_t>(blockIdx.x / C) * R;
+  const int64_t m0 = static_cast<int64_t>(blockIdx.x / C - p.cl0) * R;
   const int64_t n8 = p.d_i / 8;
   const int64_t q0 = rank * n8 / C, q1 = (rank + 1) * n8 / C;
   const int L8 = static_cast<int>(q1 - q0);
@@ -576,9 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
                                                            const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int N = p.N, stages = p.stages;
-  const uint32_t h_bytes = static_cast<uint32_t>(N) * 512u;
-  __nv_bfloat16* sBt = reinterpret_cast<__nv_bfloat16*>(smem + static_cast<size_t>(stages) * p.stage_bytes);  // [kMaxR][128]: B^T of the tile
+  __nv_bfloat16* sBt = reinterpret_cast<__nv_bfloat16*>(smem + p.stage_region);  // [kMaxR][128]: B^T of the tile
   Smem& S = *reinterpret_cast<Smem*>(reinterpret_cast<uint8_t*>(sBt) + kTileO * kMaxR * 2);
   volatile int* abort_flag = &S.abort_flag;
 
@@ -590,8 +611,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
   for (int q = 1; q < kMaxProj; ++q)
     if (q < p.n_proj && gtile >= p.proj[q].tile0) pj = q;
   const TcProjDev& P = p.proj[pj];
+  const TcSetDev& Q = p.set[P.set];  // its input
+  const int N = Q.N;
+  const uint32_t h_bytes = static_cast<uint32_t>(N) * 512u;
+  const uint32_t stage_bytes = static_cast<uint32_t>(kCodesBytes + kScaleBytes) + h_bytes;
+  const int stages = static_cast<int>(p.stage_region / stage_bytes) < kMaxStages
+                         ? static_cast<int>(p.stage_region / stage_bytes) : kMaxStages;
   const CUtensorMap* map_codes = &maps.codes[pj];
   const CUtensorMap* map_scales = &maps.scales[pj];
+  const CUtensorMap* map_hq = &maps.hq[P.set];
   const int tile = gtile - P.tile0;
   const int c0 = static_cast<int>((static_cast<int64_t>(split) * p.kc) / p.splits);
   const int c1 = static_cast<int>((static_cast<int64_t>(split + 1) * p.kc) / p.splits);
@@ -619,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
     fence_mbar_init();
     // the first stages of weights do not depend on the prologue: issue them at once
     for (int c = 0; c < pre; ++c) {
-      uint8_t* st = smem + static_cast<size_t>(c) * p.stage_bytes;
+      uint8_t* st = smem + static_cast<size_t>(c) * stage_bytes;
       const uint32_t wb = smem_u32(&S.wfull[c]);
       mbar_arrive_expect_tx(wb, kCodesBytes + kScaleBytes);
       const int kc = c0 + c;
@@ -627,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
       tma_load_2d_hint(smem_u32(st), map_codes, kc * (kChunkK / 2), row0, wb, pol_w);
       tma_load_2d_hint(smem_u32(st + kCodesBytes + h_bytes), map_scales, kc * (kChunkK / 16), row0, wb, pol_w);
     }
-    tma_prefetch_desc(&maps.hq);
+    tma_prefetch_desc(map_hq);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&S.tmem_base), kTmemCols);
@@ -646,11 +674,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
       pdl_wait();  // the activations come from the prologue
       PL_TL(3);
       for (int c = 0; c < pre; ++c) {
-        uint8_t* st = smem + static_cast<size_t>(c) * p.stage_bytes;
+        uint8_t* st = smem + static_cast<size_t>(c) * stage_bytes;
         const uint32_t hb = smem_u32(&S.hfull[c]);
         mbar_arrive_expect_tx(hb, h_bytes);
         for (int q = 0; q < 4; ++q)
-          tma_load_2d(smem_u32(st + kCodesBytes + q * N * 128), &maps.hq, (c0 + c) * kChunkK + 64 * q, 0, hb);
+          tma_load_2d(smem_u32(st + kCodesBytes + q * N * 128), map_hq, (c0 + c) * kChunkK + 64 * q, 0, hb);
       }
       int c = pre;
       bool ok = true;
@@ -658,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
         const int s = c % stages;
         ok = wait_or_abort(smem_u32(&S.empty[s]), ((c / stages) - 1) & 1, abort_flag);
         if (!ok) break;
-        uint8_t* st = smem + static_cast<size_t>(s) * p.stage_bytes;
+        uint8_t* st = smem + static_cast<size_t>(s) * stage_bytes;
         const uint32_t wb = smem_u32(&S.wfull[s]), hb = smem_u32(&S.hfull[s]);
         const int kc = c0 + c;
         PL_TLC(0, c);
@@ -667,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
         tma_load_2d_hint(smem_u32(st + kCodesBytes + h_bytes), map_scales, kc * (kChunkK / 16), row0, wb, pol_w);
         mbar_arrive_expect_tx(hb, h_bytes);
         for (int q = 0; q < 4; ++q)
-          tma_load_2d(smem_u32(st + kCodesBytes + q * N * 128), &maps.hq, kc * kChunkK + 64 * q, 0, hb);
+          tma_load_2d(smem_u32(st + kCodesBytes + q * N * 128), map_hq, kc * kChunkK + 64 * q, 0, hb);
         ++c;
       }
       if (*abort_flag) {  // every issued copy must land before this CTA exits
@@ -695,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
         if (!ok) break;
         PL_TLC(1, c);
         tc_fence_after();
-        const uint32_t hbase = smem_u32(smem + static_cast<size_t>(s) * p.stage_bytes + kCodesBytes);
+        const uint32_t hbase = smem_u32(smem + static_cast<size_t>(s) * stage_bytes + kCodesBytes);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int kk = k0 + i;
@@ -751,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
       if (!ok) break;
       if (c == 0 && threadIdx.x == 64) PL_TL(4);
       if (threadIdx.x == 64) PL_TLC(3, c);
-      const uint8_t* st = smem + static_cast<size_t>(s) * p.stage_bytes;
+      const uint8_t* st = smem + static_cast<size_t>(s) * stage_bytes;
       const uint8_t* crow = st + row * 128;
       const uint2 sc8 = *reinterpret_cast<const uint2*>(st + kCodesBytes + h_bytes + row * 16 + g * 8);
       const uint32_t sc_words[2] = {sc8.x, sc8.y};
@@ -788,7 +816,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
     if (threadIdx.x == 64) PL_TL(7);
     pdl_wait();  // the row scales and t belong to this call's prologue
     const int et = threadIdx.x - 64;  // 0 .. 255
-    if (et < N) S.rowscale[et] = et < p.M ? p.rowscale[et] : 0.f;
+    if (et < N) S.rowscale[et] = et < Q.M ? Q.rowscale[et] : 0.f;
     go = named_bar_and(1, kEpiThreads, ok && !*abort_flag);  // one decision, publishes the row scales
     if (threadIdx.x == 64) PL_TL(8);
     if (go) {
@@ -814,11 +842,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
       // lambda t of this projection (zeros past r), from the prologue
       if (lora) {
         float* tful = red + N * kTileO;  // [N][kTStride]
-        const int mt = static_cast<int>(p.M < N ? p.M : N);
+        const int mt = static_cast<int>(Q.M < N ? Q.M : N);
         const int r4 = (P.r + 3) / 4;
         for (int e = et; e < mt * r4; e += kEpiThreads) {
           const int n = e / r4, jj = 4 * (e % r4);
-          const float* tr = p.t + static_cast<int64_t>(n) * p.t_ld + P.toff + jj;
+          const float* tr = Q.t + static_cast<int64_t>(n) * Q.t_ld + P.toff + jj;
           reinterpret_cast<float4*>(tful + n * kTStride + jj)[0] =
               make_float4(P.lambda * tr[0], jj + 1 < P.r ? P.lambda * tr[1] : 0.f,
                           jj + 2 < P.r ? P.lambda * tr[2] : 0.f, jj + 3 < P.r ? P.lambda * tr[3] : 0.f);
@@ -840,7 +868,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
     float* red = reinterpret_cast<float*>(smem);
     const float* tful = red + N * kTileO;
     const uint32_t red_addr = smem_u32(red);
-    const int mt = static_cast<int>(p.M < N ? p.M : N);
+    const int mt = static_cast<int>(Q.M < N ? Q.M : N);
     // This CTA's share of the tile's rows: groups of 4 rows [g0, g1) of 32.  Thread et takes
     // row r0 + et % nrows and every ngrp-th token from et / nrows; it sums the D1 partials
     // of the S CTAs (split order) and adds B (lambda t).
@@ -1020,52 +1048,62 @@ int choose_splits(int N, int tiles, int kc) {
   return best;
 }
 
-struct TcWs {
+// Workspace of one launch: per input, the f16 rows [M][d_i], the row scales [M] and t [M][t_ld].
+struct TcSetWs {
   __half* hq;
   float* rowscale;
   float* t;
   int t_ld;
-  size_t bytes;
 };
 
-TcWs carve(void* ws, int64_t M, int64_t d_i, int rtot) {
-  TcWs w{};
+size_t carve_sets(void* ws, int64_t d_i, const int64_t* Ms, const int* rtot, int n_sets, TcSetWs* out) {
   const uintptr_t b = reinterpret_cast<uintptr_t>(ws);
   size_t off = 0;
-  w.hq = reinterpret_cast<__half*>(b + off);
-  off += align_up(static_cast<size_t>(M) * d_i * 2, 256);
-  w.rowscale = reinterpret_cast<float*>(b + off);
-  off += align_up(static_cast<size_t>(M) * 4, 256);
-  w.t_ld = rtot > 0 ? (rtot + 3) / 4 * 4 : 4;
-  w.t = reinterpret_cast<float*>(b + off);
-  off += align_up(static_cast<size_t>(M) * w.t_ld * 4, 256);
-  w.bytes = off;
-  return w;
+  for (int s = 0; s < n_sets; ++s) {
+    TcSetWs w{};
+    w.hq = reinterpret_cast<__half*>(b + off);
+    off += align_up(static_cast<size_t>(Ms[s]) * d_i * 2, 256);
+    w.rowscale = reinterpret_cast<float*>(b + off);
+    off += align_up(static_cast<size_t>(Ms[s]) * 4, 256);
+    w.t_ld = rtot[s] > 0 ? (rtot[s] + 3) / 4 * 4 : 4;
+    w.t = reinterpret_cast<float*>(b + off);
+    off += align_up(static_cast<size_t>(Ms[s]) * w.t_ld * 4, 256);
+    if (out != nullptr) out[s] = w;
+  }
+  return off;
 }
 
 // Token rows per prologue cluster: enough clusters of kProMaxC CTAs to spread the row and
 // adapter work, few enough that each cluster's slice of A is read a handful of times.
 int pro_rows(int64_t M) { return M <= 16 ? 1 : (M <= 32 ? 2 : kProMaxR); }
 
-// The cluster prologue over ceil(M / R) clusters of C CTAs.
-cudaError_t launch_pro(const ProParams& pp, bool fp8, cudaStream_t stream) {
-  const int64_t n8 = pp.d_i / 8;
-  const size_t pro_smem = static_cast<size_t>(pp.R) * static_cast<size_t>((n8 + pp.C - 1) / pp.C) * 8 * 4;
+// The cluster prologue: input s takes clusters [cl0_s, cl0_s + ceil(M_s / R_s)) of C CTAs.
+cudaError_t launch_pro(ProParams pr, bool fp8, cudaStream_t stream) {
+  int clusters = 0;
+  size_t pro_smem = 0;
+  for (int s = 0; s < pr.n_sets; ++s) {
+    ProSet& q = pr.set[s];
+    q.cl0 = clusters;
+    clusters += static_cast<int>((q.M + q.R - 1) / q.R);
+    const int64_t n8 = q.d_i / 8;
+    const size_t need = static_cast<size_t>(q.R) * static_cast<size_t>((n8 + q.C - 1) / q.C) * 8 * 4;
+    pro_smem = need > pro_smem ? need : pro_smem;
+  }
   cudaLaunchAttribute pa[2];
   pa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pa[0].val.programmaticStreamSerializationAllowed = 1;
   pa[1].id = cudaLaunchAttributeClusterDimension;
-  pa[1].val.clusterDim.x = static_cast<unsigned>(pp.C);
+  pa[1].val.clusterDim.x = static_cast<unsigned>(pr.set[0].C);
   pa[1].val.clusterDim.y = 1;
   pa[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t c1{};
-  c1.gridDim = dim3(static_cast<unsigned>(((pp.M + pp.R - 1) / pp.R) * pp.C));
+  c1.gridDim = dim3(static_cast<unsigned>(clusters * pr.set[0].C));
   c1.blockDim = dim3(kProThreads);
   c1.dynamicSmemBytes = pro_smem;
   c1.stream = stream;
   c1.attrs = pa;
   c1.numAttrs = 2;
-  return fp8 ? cudaLaunchKernelEx(&c1, k_pro_dec<true>, pp) : cudaLaunchKernelEx(&c1, k_pro_dec<false>, pp);
+  return fp8 ? cudaLaunchKernelEx(&c1, k_pro_dec<true>, pr) : cudaLaunchKernelEx(&c1, k_pro_dec<false>, pr);
 }
 
 }  // namespace
@@ -1074,42 +1112,64 @@ bool tc_supported(int64_t M, int64_t d_i, int64_t, int r) {
   return M >= 1 && M <= kMaxN && d_i >= kChunkK && d_i % kChunkK == 0 && d_i <= 32768 && r >= 0 && r <= kMaxR;
 }
 
-bool tc_group_supported(int64_t M, int64_t d_i, const TcProj* projs, int n_proj) {
-  if (n_proj < 1 || n_proj > kMaxProj || !tc_supported(M, d_i, 1, 0)) return false;
-  int rtot = 0;
+bool tc_batch_supported(int64_t d_i, const TcSet* sets, int n_sets, const TcProj* projs, int n_proj) {
+  if (n_sets < 1 || n_sets > kMaxSets || n_proj < 1 || n_proj > kMaxProj) return false;
+  int rtot[kMaxSets] = {0}, count[kMaxSets] = {0};
+  for (int s = 0; s < n_sets; ++s)
+    if (!tc_supported(sets[s].M, d_i, 1, 0)) return false;
   for (int i = 0; i < n_proj; ++i) {
-    if (projs[i].r < 0 || projs[i].r > kMaxR) return false;
-    rtot += projs[i].r;
+    const int s = projs[i].set;
+    if (s < 0 || s >= n_sets || projs[i].r < 0 || projs[i].r > kMaxR) return false;
+    rtot[s] += projs[i].r;
+    if (++count[s] > kMaxAdapt || rtot[s] > kMaxRTot) return false;
   }
-  return rtot <= kMaxRTot;
+  return true;
 }
 
-size_t tc_workspace_bytes(int64_t M, int64_t d_i, int64_t, int r) { return carve(nullptr, M, d_i, r).bytes; }
+size_t tc_workspace_bytes(int64_t M, int64_t d_i, int64_t, int r) { return carve_sets(nullptr, d_i, &M, &r, 1, nullptr); }
 
-size_t tc_group_workspace_bytes(int64_t M, int64_t d_i, int rtot) { return carve(nullptr, M, d_i, rtot).bytes; }
+size_t tc_batch_workspace_bytes(int64_t d_i, const TcSet* sets, int n_sets, const TcProj* projs, int n_proj) {
+  int64_t Ms[kMaxSets];
+  int rtot[kMaxSets] = {0};
+  if (n_sets < 1 || n_sets > kMaxSets) return 0;
+  for (int s = 0; s < n_sets; ++s) Ms[s] = sets[s].M;
+  for (int i = 0; i < n_proj; ++i)
+    if (projs[i].set >= 0 && projs[i].set < n_sets) rtot[projs[i].set] += projs[i].r;
+  return carve_sets(nullptr, d_i, Ms, rtot, n_sets, nullptr);
+}
 
-cudaError_t launch_linear_tc_group(const void* x, int64_t M, int64_t d_i, const float* w_norm, const float* z,
-                                   int64_t z_ld, float eps, const TcProj* projs, int n_proj, bool y_f32, void* ws,
-                                   cudaStream_t stream) {
+cudaError_t launch_linear_tc_batch(int64_t d_i, float eps, const TcSet* sets, int n_sets, const TcProj* projs,
+                                   int n_proj, bool y_f32, void* ws, cudaStream_t stream) {
   cudaError_t e = set_kernel_attributes();
   if (e != cudaSuccess) return e;
-  int rtot = 0, tiles = 0;
+  int64_t Ms[kMaxSets];
+  int rtot[kMaxSets] = {0}, toff[kMaxProj], tiles = 0, Nmax = 16;
+  for (int s = 0; s < n_sets; ++s) {
+    Ms[s] = sets[s].M;
+    const int N = static_cast<int>((sets[s].M + 15) / 16 * 16);
+    Nmax = N > Nmax ? N : Nmax;
+  }
   for (int i = 0; i < n_proj; ++i) {
-    rtot += projs[i].r;
+    toff[i] = rtot[projs[i].set];
+    rtot[projs[i].set] += projs[i].r;
     tiles += static_cast<int>((projs[i].d_o + kTileO - 1) / kTileO);
   }
-  const TcWs w = carve(ws, M, d_i, rtot);
-  const int N = static_cast<int>((M + 15) / 16 * 16);
+  TcSetWs w[kMaxSets];
+  carve_sets(ws, d_i, Ms, rtot, n_sets, w);
   const int kc = static_cast<int>(d_i / kChunkK);
-  const int splits = choose_splits(N, tiles, kc);
+  const int splits = choose_splits(Nmax, tiles, kc);
   int stages;
   uint32_t sb;
   size_t smem;
-  stage_plan(N, stages, sb, smem);
+  stage_plan(Nmax, stages, sb, smem);  // the largest N sets the allocation: at least two of its stages
+  const uint32_t stage_region = static_cast<uint32_t>(smem - (1024 + kTileO * kMaxR * 2 + sizeof(Smem)));
 
   TcMaps maps;
   memset(&maps, 0, sizeof(maps));
-  bool ok = encode_2d(&maps.hq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.hq, d_i, M, 64, N, CU_TENSOR_MAP_SWIZZLE_128B);
+  bool ok = true;
+  for (int s = 0; s < n_sets && ok; ++s)
+    ok = encode_2d(&maps.hq[s], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w[s].hq, d_i, sets[s].M, 64,
+                   static_cast<uint32_t>((sets[s].M + 15) / 16 * 16), CU_TENSOR_MAP_SWIZZLE_128B);
   for (int i = 0; i < n_proj && ok; ++i)
     ok = encode_2d(&maps.codes[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, projs[i].codes, d_i / 2, projs[i].d_o, 128,
                    kTileO, CU_TENSOR_MAP_SWIZZLE_128B) &&
@@ -1117,56 +1177,57 @@ cudaError_t launch_linear_tc_group(const void* x, int64_t M, int64_t d_i, const 
                    kTileO, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (!ok) return cudaErrorInvalidValue;
 
-  // prologue: clusters of C CTAs over R token rows each
-  ProParams pp{};
-  pp.x = static_cast<const __nv_bfloat16*>(x);
-  pp.M = M;
-  pp.d_i = d_i;
-  pp.w_norm = w_norm;
-  pp.z = w_norm != nullptr ? z : nullptr;
-  pp.z_ld = z_ld;
-  pp.eps = eps;
-  pp.hq = w.hq;
-  pp.rowscale = w.rowscale;
-  pp.t = w.t;
-  pp.t_ld = w.t_ld;
-  pp.R = pro_rows(M);
-  pp.C = kProMaxC;
-  pp.n_proj = n_proj;
-  pp.rtot = rtot;
-  for (int i = 0, off = 0; i < n_proj; ++i) {
-    pp.A[i] = static_cast<const __nv_bfloat16*>(projs[i].A);
-    pp.r[i] = projs[i].A != nullptr ? projs[i].r : 0;
-    pp.toff[i] = off;
-    off += projs[i].r;
+  // prologue: per input, clusters of C CTAs over R token rows each, with the adapters of the
+  // members that read it
+  ProParams pr{};
+  pr.n_sets = n_sets;
+  for (int s = 0; s < n_sets; ++s) {
+    ProSet& q = pr.set[s];
+    q.x = static_cast<const __nv_bfloat16*>(sets[s].x);
+    q.M = sets[s].M;
+    q.d_i = d_i;
+    q.w_norm = sets[s].w_norm;
+    q.z = sets[s].w_norm != nullptr ? sets[s].z : nullptr;
+    q.z_ld = sets[s].z_ld;
+    q.eps = eps;
+    q.hq = w[s].hq;
+    q.rowscale = w[s].rowscale;
+    q.t = w[s].t;
+    q.t_ld = w[s].t_ld;
+    q.R = pro_rows(sets[s].M);
+    q.C = kProMaxC;
+    q.rtot = rtot[s];
+    for (int i = 0; i < n_proj; ++i)
+      if (projs[i].set == s) {
+        q.A[q.n_proj] = static_cast<const __nv_bfloat16*>(projs[i].A);
+        q.r[q.n_proj] = projs[i].A != nullptr ? projs[i].r : 0;
+        q.toff[q.n_proj] = toff[i];
+        ++q.n_proj;
+      }
   }
-  e = launch_pro(pp, false, stream);
+  e = launch_pro(pr, false, stream);
   if (e != cudaSuccess) return e;
 
   TcParams p{};
-  p.M = M;
   p.d_i = d_i;
-  p.N = N;
   p.splits = splits;
   p.kc = kc;
-  p.stages = stages;
-  p.stage_bytes = sb;
+  p.stage_region = stage_region;
   p.n_proj = n_proj;
-  p.t_ld = w.t_ld;
-  p.rowscale = w.rowscale;
-  p.t = w.t;
   p.y_f32 = y_f32 ? 1 : 0;
-  for (int i = 0, off = 0, t0 = 0; i < n_proj; ++i) {
+  for (int s = 0; s < n_sets; ++s)
+    p.set[s] = TcSetDev{sets[s].M, static_cast<int>((sets[s].M + 15) / 16 * 16), w[s].rowscale, w[s].t, w[s].t_ld};
+  for (int i = 0, t0 = 0; i < n_proj; ++i) {
     const bool lora = projs[i].r > 0 && projs[i].A != nullptr && projs[i].B != nullptr;
     p.proj[i].d_o = projs[i].d_o;
     p.proj[i].s_g = projs[i].s_g;
     p.proj[i].B = lora ? static_cast<const __nv_bfloat16*>(projs[i].B) : nullptr;
     p.proj[i].y = projs[i].y;
     p.proj[i].r = lora ? projs[i].r : 0;
-    p.proj[i].toff = off;
+    p.proj[i].toff = toff[i];
     p.proj[i].tile0 = t0;
     p.proj[i].lambda = projs[i].lambda;
-    off += projs[i].r;
+    p.proj[i].set = projs[i].set;
     t0 += static_cast<int>((projs[i].d_o + kTileO - 1) / kTileO);
   }
   cudaLaunchAttribute attrs[2];
@@ -1191,31 +1252,34 @@ cudaError_t launch_pro_fp8(const void* x, int64_t M, int64_t d_i, const float* w
                            cudaStream_t stream) {
   cudaError_t e = set_kernel_attributes();
   if (e != cudaSuccess) return e;
-  ProParams pp{};
-  pp.x = static_cast<const __nv_bfloat16*>(x);
-  pp.M = M;
-  pp.d_i = d_i;
-  pp.w_norm = w_norm;
-  pp.z = w_norm != nullptr ? z : nullptr;
-  pp.z_ld = z_ld;
-  pp.eps = eps;
-  pp.qx = qx;
-  pp.rowscale = s_x;
-  pp.t = t;
-  pp.t_ld = t_ld;
-  pp.R = pro_rows(M);
-  pp.C = kProMaxC;
-  pp.n_proj = 1;
-  pp.rtot = A != nullptr ? r : 0;
-  pp.A[0] = static_cast<const __nv_bfloat16*>(A);
-  pp.r[0] = pp.rtot;
-  pp.toff[0] = 0;
-  return launch_pro(pp, true, stream);
+  ProParams pr{};
+  pr.n_sets = 1;
+  ProSet& q = pr.set[0];
+  q.x = static_cast<const __nv_bfloat16*>(x);
+  q.M = M;
+  q.d_i = d_i;
+  q.w_norm = w_norm;
+  q.z = w_norm != nullptr ? z : nullptr;
+  q.z_ld = z_ld;
+  q.eps = eps;
+  q.qx = qx;
+  q.rowscale = s_x;
+  q.t = t;
+  q.t_ld = t_ld;
+  q.R = pro_rows(M);
+  q.C = kProMaxC;
+  q.n_proj = 1;
+  q.rtot = A != nullptr ? r : 0;
+  q.A[0] = static_cast<const __nv_bfloat16*>(A);
+  q.r[0] = q.rtot;
+  q.toff[0] = 0;
+  return launch_pro(pr, true, stream);
 }
 
 cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
-  TcProj pj{a.d_o, a.codes, a.scales, a.s_g, a.A, a.B, a.r, a.lambda, a.y};
-  return launch_linear_tc_group(a.x, a.M, a.d_i, a.w_norm, a.z, a.z_ld, a.eps, &pj, 1, a.y_f32, a.ws, stream);
+  const TcSet set{a.x, a.M, a.w_norm, a.z, a.z_ld};
+  TcProj pj{a.d_o, a.codes, a.scales, a.s_g, a.A, a.B, a.r, a.lambda, a.y, 0};
+  return launch_linear_tc_batch(a.d_i, a.eps, &set, 1, &pj, 1, a.y_f32, a.ws, stream);
 }
 
 cudaError_t launch_act_prologue(const LinearArgs& a, __half* hq, float* rowscale, __half* A16, float* zero,

@@ -24,7 +24,7 @@ from . import synthetic
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--op", choices=["linear", "quantize", "rmsnorm", "w8a8", "backward", "group"], default="linear")
+    ap.add_argument("--op", choices=["linear", "quantize", "rmsnorm", "w8a8", "backward", "group", "batch"], default="linear")
     ap.add_argument("--workload", default="decode_proj_7b")
     ap.add_argument("--proj", type=int, default=0, help="index of the projection in the workload")
     ap.add_argument("--M", type=int, default=64)
@@ -58,6 +58,21 @@ def main(argv=None):
         for _ in range(a.calls):
             pl.nvfp4_lora_linear_backward(gr, g["x"], codes, scales, s_g, g["A"], g["B"], wl.lam, g["w_norm"], g["z"],
                                           synthetic.EPS)
+        torch.cuda.synchronize()
+        return
+    if a.op == "batch":  # the workload's projection at every M of its sweep, one batch call per weight set
+        batches = []
+        per = 9 * p.d_o * p.d_i // 16 * len(wl.Ms)
+        for k in range(a.copies or max(2, (2 * 129 * 2 ** 20) // per + 1)):  # weight sets larger than 2x L2
+            calls = []
+            for M in wl.Ms:
+                cc = synthetic.projection_case(p.d_o, p.d_i, M, wl.r, wl.sigma, wl.seed + M, wl.outlier_frac)
+                co, sc, sg = pl.nvfp4_quantize(cc["W"].to(dev))
+                calls.append(dict(x=cc["x"].to(dev), codes=co, scales=sc, s_g=sg, A=cc["A"].to(dev),
+                                  B=cc["B"].to(dev), lam=wl.lam, w_norm=cc["w_norm"].to(dev), z=cc["z"].to(dev)))
+            batches.append(calls)
+        for i in range(a.calls):
+            pl.nvfp4_lora_linear_batch(batches[i % len(batches)], synthetic.EPS)
         torch.cuda.synchronize()
         return
     if a.op == "group":  # the projections of the workload behind the same norm as --proj, one group call

@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_status_strings_and_version(L):
-    for s in range(10):
+    for s in range(11):
         txt = L.pl_status_string(s).decode()
         assert txt.startswith("PL_")
     assert L.pl_status_string(99).decode() == "unknown pl_status"
@@ -321,3 +321,62 @@ def test_static_workspace_entry_reports_an_unsupported_device(L):
     st = f(_p(FAKE), 4, 256, 256, _p(FAKE), _p(FAKE), _p(FAKE), _p(FAKE), _p(FAKE), 8, ctypes.c_float(2.0), _p(FAKE),
            _p(FAKE), ctypes.c_float(1e-6), _p(FAKE), 0, None)
     assert st == 5
+
+
+def _calls(n, over=None):
+    from precision_linear_gb300 import binding as pl
+    arr = (pl.Call * n)()
+    for i in range(n):
+        d = dict(x=FAKE + i * (1 << 16), M=4, d_o=256, codes=FAKE, scales=FAKE, s_g=FAKE, A=FAKE, B=FAKE, r=8,
+                 lam=2.0, w_norm=FAKE, z=None, z_ld=0, y=FAKE + (1 << 24) + i * (1 << 16))
+        d.update((over or {}).get(i, {}))
+        arr[i] = pl.Call(d["x"], d["M"], d["d_o"], d["codes"], d["scales"], d["s_g"], d["A"], d["B"], d["r"],
+                         d["lam"], d["w_norm"], d["z"], d["z_ld"], d["y"])
+    return arr
+
+
+def test_batch_argument_checks(L):
+    from precision_linear_gb300 import binding as pl
+    f = pl.lib().pl_nvfp4_lora_linear_batch
+    ws = _p(FAKE)
+    assert f(256, ctypes.c_float(1e-6), None, 2, 0, ws, 1 << 30, None) == 1
+    assert f(256, ctypes.c_float(1e-6), _calls(2), 0, 0, ws, 1 << 30, None) == 2
+    assert f(256, ctypes.c_float(1e-6), _calls(9), 9, 0, ws, 1 << 30, None) == 2  # more than PL_MAX_BATCH
+    assert f(250, ctypes.c_float(1e-6), _calls(2), 2, 0, ws, 1 << 30, None) == 2
+    assert f(256, ctypes.c_float(1e-6), _calls(2, {1: dict(x=None)}), 2, 0, ws, 1 << 30, None) == 1
+    assert f(256, ctypes.c_float(1e-6), _calls(2, {1: dict(r=65)}), 2, 0, ws, 1 << 30, None) == 4
+    assert f(256, ctypes.c_float(1e-6), _calls(2, {1: dict(y=FAKE + 8)}), 2, 0, ws, 1 << 30, None) == 3
+    # an output overlapping another call's output, or any call's input: refused
+    same_y = {1: dict(y=FAKE + (1 << 24))}
+    assert f(256, ctypes.c_float(1e-6), _calls(2, same_y), 2, 0, ws, 1 << 30, None) == 10
+    y_on_x = {0: dict(y=FAKE + (1 << 16) + 256)}
+    assert f(256, ctypes.c_float(1e-6), _calls(2, y_on_x), 2, 0, ws, 1 << 30, None) == 10
+    assert f(256, ctypes.c_float(1e-6), _calls(2), 2, 0, None, 1 << 30, None) == 7
+    assert pl.lib().pl_workspace_bytes_batch(256, _calls(3), 3) > 0
+    assert pl.lib().pl_workspace_bytes_batch(250, _calls(3), 3) == 0
+
+
+def test_call_struct_layout_matches_the_header(tmp_path):
+    import shutil
+    import subprocess
+    from precision_linear_gb300 import binding as pl
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "precision_linear.h"\n'
+                   'int main(void){printf("%zu %zu %zu %zu %zu\\n", sizeof(pl_nvfp4_call), offsetof(pl_nvfp4_call, r),'
+                   ' offsetof(pl_nvfp4_call, lambda), offsetof(pl_nvfp4_call, z_ld), offsetof(pl_nvfp4_call, y));'
+                   'return 0;}\n')
+    exe = tmp_path / "layout"
+    subprocess.check_call([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    got = [int(v) for v in subprocess.check_output([str(exe)]).split()]
+    C = pl.Call
+    assert got == [ctypes.sizeof(C), C.r.offset, C.lam.offset, C.z_ld.offset, C.y.offset]
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_batch_without_a_device_reports_device_error(L):
+    from precision_linear_gb300 import binding as pl
+    assert pl.lib().pl_nvfp4_lora_linear_batch(256, ctypes.c_float(1e-6), _calls(3), 3, 0, _p(FAKE), 1 << 30,
+                                               None) == 5

@@ -84,15 +84,20 @@ def test_linear_with_per_token_states(cuda_ok, d_o, d_i, M, path):
     ref_case = dict(case)
     ref_case["z"] = torch.from_numpy(z_ref)
     assert_linear_close(y, oracle_linear(ref_case, packed, sb, s_g, 2.0), f"per-token states path {path}")
-    # the states differ per row: the shared-state result (row 0's state for all) differs
-    y_shared = pl.nvfp4_lora_linear(*args[:8], z_dev[0].contiguous(), synthetic.EPS, out_dtype=torch.float32)
+    # the states differ per row: every row given row 0's state (the same kernel path) agrees
+    # with y in row 0 only
+    z_row0 = z_dev[0:1].expand(M, d_i).contiguous()
+    y_shared = pl.nvfp4_lora_linear(*args[:8], z_row0, synthetic.EPS, out_dtype=torch.float32)
     assert torch.equal(y[0], y_shared[0]) and not torch.equal(y[1:], y_shared[1:])
 
 
-@pytest.mark.parametrize("d_o,d_i,M", [(3584, 3584, 16), (18944, 3584, 8), (1000, 1024, 300), (300, 272, 9)])
+@pytest.mark.parametrize("d_o,d_i,M", [(3584, 18944, 16), (18944, 3584, 8), (1000, 1024, 300), (300, 272, 9)])
 def test_equal_rows_reproduce_the_shared_state_bitwise(cuda_ok, d_o, d_i, M):
     """Every row given the same state: the per-row form is bit for bit the shared form
-    (both add w_norm + z in FP32 before any other use)."""
+    (both add w_norm + z in FP32 before any other use).  Shapes whose kernel path does not
+    change with the noise layout; the one-kernel decode shapes run per-row states on the
+    two-kernel path, checked against the oracle above."""
+    assert pl.linear_path(M, d_i, d_o, 16) != 2
     case = make_case(d_o, d_i, M, 16, 1e-2, 5, 0.0)
     dev_w = pl.nvfp4_quantize(case["W"])
     z_rows = case["z"].unsqueeze(0).expand(M, d_i).contiguous()
