@@ -54,7 +54,7 @@ __device__ uint32_t g_tc_status = 0;
 #ifdef PL_TIMELINE
 __device__ unsigned long long g_tl_main[1024][16];
 __device__ unsigned long long g_tl_pro[256][8];
-__device__ unsigned long long g_tl_chunk[1024][4][32];  // per chunk: W issued, MMA ready, A ready, dequant start
+__device__ unsigned long long g_tl_chunk[1024][6][32];  // per chunk: W issued, MMA ready, dequant end, dequant start, weights landed, issuer saw A
 #define PL_TLC(kind, c) do { if (blockIdx.x < 1024 && (c) < 32) g_tl_chunk[blockIdx.x][kind][c] = globaltimer_ns(); } while (0)
 #define PL_TL(slot) do { if (blockIdx.x < 1024) g_tl_main[blockIdx.x][slot] = globaltimer_ns(); } while (0)
 #define PL_TLP(slot) do { const unsigned b_ = blockIdx.x + gridDim.x * blockIdx.y; \
@@ -73,10 +73,14 @@ constexpr int kCodesBytes = kTileO * kChunkK / 2;   // 16 KB
 constexpr int kScaleBytes = kTileO * kChunkK / 16;  // 2 KB
 constexpr int kDeqWarps = 8;
 constexpr int kIssuers = 2;  // MMA-issuing warps: the two K halves of every chunk
-constexpr int kThreads = (2 + kDeqWarps + kIssuers - 1) * 32;  // producer, issuer 0, dequant/epilogue, issuer 1
+// warps: weight producer, issuer 0, dequant/epilogue, issuer 1, activation producer
+constexpr int kThreads = (2 + kDeqWarps + kIssuers) * 32;
 constexpr int kIssuer1Warp = 2 + kDeqWarps;
+constexpr int kHWarp = 3 + kDeqWarps;
 constexpr int kEpiThreads = kDeqWarps * 32;
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 10;   // weight stages (codes + scales of one chunk)
+constexpr int kMaxHStages = 4;   // activation stages (the N token rows of one chunk)
+constexpr uint32_t kWStage = kCodesBytes + kScaleBytes;  // 18 KB
 constexpr int kMaxSplit = 8;
 constexpr int kMaxN = 64;
 constexpr int kMaxR = 64;        // adapter rank of one projection
@@ -92,7 +96,26 @@ constexpr int kAbuf = 3;
 constexpr uint32_t kColA0 = 0;
 constexpr uint32_t kColAcc = 384;  // issuer q accumulates at kColAcc + 64 q
 static_assert(kAbuf * 128 <= kColAcc && kColAcc + kIssuers * kMaxN <= kTmemCols, "TMEM columns");
-constexpr int kTStride = kMaxR + 4;  // floats per token row of lambda t in shared memory
+// Activation stages for N token rows: as many as 64 KB hold, 2 to kMaxHStages (the rows come
+// from L2, written by the prologue).
+__host__ __device__ constexpr int h_stages_for(int N) {
+  return 65536 / (N * 512) < 2 ? 2 : (65536 / (N * 512) > kMaxHStages ? kMaxHStages : 65536 / (N * 512));
+}
+
+// Bulk prefetch of [p, p + bytes) into L2 (16-byte aligned, bytes a multiple of 16).  Only a
+// hint: L2 is the point of coherence, so a line fetched before its producer finished is
+// refreshed by that producer's writes and later loads see them.
+__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(ptr), "r"(bytes) : "memory");
+}
+
+// Orders this thread's generic shared-memory writes before later tensor-core (async-proxy) reads.
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Shared-memory operands of the adapter's up-projection (128-byte swizzled, K-major, bf16,
+// zero past r): the B rows of the tile [128][64] and lambda t of the tokens [N][64], N the
+// largest of the launch.
+constexpr uint32_t kBaBytes = kTileO * 128;
 
 // One projection of a group, as the main kernel sees it.
 struct TcProjDev {
@@ -119,6 +142,7 @@ struct TcParams {
   int splits, kc, n_proj;
   uint32_t stage_region;   // shared-memory bytes for the weight ring; each CTA fits as many
                            // stages of its own N as the region holds (at most kMaxStages)
+  uint32_t tq_region;      // bytes of the lambda t operand: the launch's largest N x 128
   int y_f32;
   TcProjDev proj[kMaxProj];
   TcSetDev set[kMaxSets];
@@ -130,9 +154,9 @@ struct TcMaps {
 };
 
 struct Smem {
-  uint64_t wfull[kMaxStages], hfull[kMaxStages], empty[kMaxStages];
+  uint64_t wfull[kMaxStages], empty[kMaxStages], hfull[kMaxHStages], hempty[kMaxHStages];
   uint64_t a_full[kAbuf], a_empty[kAbuf];
-  uint64_t d_full;
+  uint64_t d_full, tq_full;
   uint32_t tmem_base;
   int abort_flag;
   float s_g;
@@ -391,6 +415,24 @@ __global__ void __launch_bounds__(kProThreads) k_pro_dec(const __grid_constant__
     PL_TLP(0);
     pdl_launch_dependents();
   }
+  // While the preceding kernel finishes: bring this CTA's slices of the rows, the norm
+  // scale, the noise and the adapters into L2 (one bulk prefetch per row slice).
+  {
+    const uint32_t xb = static_cast<uint32_t>(L8) * 16u, fb = static_cast<uint32_t>(L8) * 32u;
+    if (tid < R && m0 + tid < p.M) {
+      prefetch_l2(p.x + (m0 + tid) * p.d_i + q0 * 8, xb);
+      if (zrows) prefetch_l2(p.z + (m0 + tid) * p.z_ld + q0 * 8, fb);
+    } else if (tid == kProMaxR && norm) {
+      prefetch_l2(p.w_norm + q0 * 8, fb);
+    } else if (tid == kProMaxR + 1 && zshared) {
+      prefetch_l2(p.z + q0 * 8, fb);
+    } else if (tid >= 32 && tid - 32 < J) {
+      const int jj = tid - 32;
+      for (int pp = 0; pp < p.n_proj; ++pp)
+        if (jj >= p.toff[pp] && jj < p.toff[pp] + p.r[pp])
+          prefetch_l2(p.A[pp] + static_cast<int64_t>(jj - p.toff[pp]) * p.d_i + q0 * 8, xb);
+    }
+  }
   pdl_wait();  // x, w_norm and z may come from the preceding kernel, which may also still read the workspace
   if (tid == 0) PL_TLP(1);
 
@@ -599,8 +641,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
                                                            const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __nv_bfloat16* sBt = reinterpret_cast<__nv_bfloat16*>(smem + p.stage_region);  // [kMaxR][128]: B^T of the tile
-  Smem& S = *reinterpret_cast<Smem*>(reinterpret_cast<uint8_t*>(sBt) + kTileO * kMaxR * 2);
+  uint8_t* sBa = smem + p.stage_region;  // [128][64] bf16: the B rows of the tile
+  uint8_t* sTq = sBa + kBaBytes;          // [N][64] bf16: lambda t of the tokens
+  Smem& S = *reinterpret_cast<Smem*>(sTq + p.tq_region);
   volatile int* abort_flag = &S.abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -613,10 +656,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
   const TcProjDev& P = p.proj[pj];
   const TcSetDev& Q = p.set[P.set];  // its input
   const int N = Q.N;
+  // the stage region: weight stages of 18 KB from its start, then hst activation stages
   const uint32_t h_bytes = static_cast<uint32_t>(N) * 512u;
-  const uint32_t stage_bytes = static_cast<uint32_t>(kCodesBytes + kScaleBytes) + h_bytes;
-  const int stages = static_cast<int>(p.stage_region / stage_bytes) < kMaxStages
-                         ? static_cast<int>(p.stage_region / stage_bytes) : kMaxStages;
+  const int hst = h_stages_for(N);
+  const int wfit = static_cast<int>((p.stage_region - static_cast<uint32_t>(hst) * h_bytes) / kWStage);
+  const int stages = wfit < kMaxStages ? wfit : kMaxStages;
+  uint8_t* hreg = smem + static_cast<size_t>(stages) * kWStage;
   const CUtensorMap* map_codes = &maps.codes[pj];
   const CUtensorMap* map_scales = &maps.scales[pj];
   const CUtensorMap* map_hq = &maps.hq[P.set];
@@ -625,6 +670,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
   const int c1 = static_cast<int>((static_cast<int64_t>(split + 1) * p.kc) / p.splits);
   const int nch = c1 - c0;
   const bool lora = P.r > 0;
+  const bool lora_here = lora && split == 0;  // the split that adds the adapter's term
+  // the up-projection accumulates into the weight buffer the next chunk would use, free
+  // once the last chunk that used it has completed
+  const int b_lora = nch % kAbuf;
   bool go = false;  // epilogue threads: this CTA's accumulators are valid
 
   const uint64_t pol_w = policy_evict_first();  // weights are streamed once
@@ -635,25 +684,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
     pdl_launch_dependents();
     for (int s = 0; s < stages; ++s) {
       mbar_init(smem_u32(&S.wfull[s]), 1);
+      mbar_init(smem_u32(&S.empty[s]), kDeqWarps);  // released once dequantised
+    }
+    for (int s = 0; s < hst; ++s) {
       mbar_init(smem_u32(&S.hfull[s]), 1);
-      mbar_init(smem_u32(&S.empty[s]), kDeqWarps + kIssuers);
+      mbar_init(smem_u32(&S.hempty[s]), kIssuers);  // released once its MMAs completed
     }
     for (int b = 0; b < kAbuf; ++b) {
       mbar_init(smem_u32(&S.a_full[b]), kDeqWarps);
       mbar_init(smem_u32(&S.a_empty[b]), kIssuers);
     }
     mbar_init(smem_u32(&S.d_full), kIssuers);
+    mbar_init(smem_u32(&S.tq_full), kDeqWarps);
     S.abort_flag = 0;
     fence_mbar_init();
     // the first stages of weights do not depend on the prologue: issue them at once
     for (int c = 0; c < pre; ++c) {
-      uint8_t* st = smem + static_cast<size_t>(c) * stage_bytes;
+      uint8_t* st = smem + static_cast<size_t>(c) * kWStage;
       const uint32_t wb = smem_u32(&S.wfull[c]);
-      mbar_arrive_expect_tx(wb, kCodesBytes + kScaleBytes);
+      mbar_arrive_expect_tx(wb, kWStage);
       const int kc = c0 + c;
       PL_TLC(0, c);
       tma_load_2d_hint(smem_u32(st), map_codes, kc * (kChunkK / 2), row0, wb, pol_w);
-      tma_load_2d_hint(smem_u32(st + kCodesBytes + h_bytes), map_scales, kc * (kChunkK / 16), row0, wb, pol_w);
+      tma_load_2d_hint(smem_u32(st + kCodesBytes), map_scales, kc * (kChunkK / 16), row0, wb, pol_w);
     }
     tma_prefetch_desc(map_hq);
   }
@@ -668,42 +721,49 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
   if (threadIdx.x == 0) PL_TL(1);
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- TMA producer
+    // ---------------------------------------------------------------- weight producer
+    // The weights never depend on the prologue: this thread streams them without waiting
+    // for it, each stage as soon as the dequant warps have released it.
     if (lane == 0) {
-      PL_TL(2);
-      pdl_wait();  // the activations come from the prologue
-      PL_TL(3);
-      for (int c = 0; c < pre; ++c) {
-        uint8_t* st = smem + static_cast<size_t>(c) * stage_bytes;
-        const uint32_t hb = smem_u32(&S.hfull[c]);
-        mbar_arrive_expect_tx(hb, h_bytes);
-        for (int q = 0; q < 4; ++q)
-          tma_load_2d(smem_u32(st + kCodesBytes + q * N * 128), map_hq, (c0 + c) * kChunkK + 64 * q, 0, hb);
-      }
       int c = pre;
       bool ok = true;
       while (ok && c < nch) {
         const int s = c % stages;
         ok = wait_or_abort(smem_u32(&S.empty[s]), ((c / stages) - 1) & 1, abort_flag);
         if (!ok) break;
-        uint8_t* st = smem + static_cast<size_t>(s) * stage_bytes;
-        const uint32_t wb = smem_u32(&S.wfull[s]), hb = smem_u32(&S.hfull[s]);
+        uint8_t* st = smem + static_cast<size_t>(s) * kWStage;
+        const uint32_t wb = smem_u32(&S.wfull[s]);
         const int kc = c0 + c;
         PL_TLC(0, c);
-        mbar_arrive_expect_tx(wb, kCodesBytes + kScaleBytes);
+        mbar_arrive_expect_tx(wb, kWStage);
         tma_load_2d_hint(smem_u32(st), map_codes, kc * (kChunkK / 2), row0, wb, pol_w);
-        tma_load_2d_hint(smem_u32(st + kCodesBytes + h_bytes), map_scales, kc * (kChunkK / 16), row0, wb, pol_w);
-        mbar_arrive_expect_tx(hb, h_bytes);
-        for (int q = 0; q < 4; ++q)
-          tma_load_2d(smem_u32(st + kCodesBytes + q * N * 128), map_hq, kc * kChunkK + 64 * q, 0, hb);
+        tma_load_2d_hint(smem_u32(st + kCodesBytes), map_scales, kc * (kChunkK / 16), row0, wb, pol_w);
         ++c;
       }
-      if (*abort_flag) {  // every issued copy must land before this CTA exits
-        for (int d = (c - stages > 0 ? c - stages : 0); d < c; ++d) {
-          drain(smem_u32(&S.wfull[d % stages]), (d / stages) & 1);
-          drain(smem_u32(&S.hfull[d % stages]), (d / stages) & 1);
-        }
+      if (*abort_flag)  // every issued copy must land before this CTA exits
+        for (int d = (c - stages > 0 ? c - stages : 0); d < c; ++d) drain(smem_u32(&S.wfull[d % stages]), (d / stages) & 1);
+    }
+  } else if (warp == kHWarp) {
+    // ---------------------------------------------------------------- activation producer
+    if (lane == 0) {
+      PL_TL(2);
+      pdl_wait();  // the activations come from the prologue
+      PL_TL(3);
+      int c = 0;
+      bool ok = true;
+      while (ok && c < nch) {
+        const int s = c % hst;
+        if (c >= hst) ok = wait_or_abort(smem_u32(&S.hempty[s]), ((c / hst) - 1) & 1, abort_flag);
+        if (!ok) break;
+        uint8_t* st = hreg + static_cast<size_t>(s) * h_bytes;
+        const uint32_t hb = smem_u32(&S.hfull[s]);
+        mbar_arrive_expect_tx(hb, h_bytes);
+        for (int q = 0; q < 4; ++q)
+          tma_load_2d(smem_u32(st + q * N * 128), map_hq, (c0 + c) * kChunkK + 64 * q, 0, hb);
+        ++c;
       }
+      if (*abort_flag)
+        for (int d = (c - hst > 0 ? c - hst : 0); d < c; ++d) drain(smem_u32(&S.hfull[d % hst]), (d / hst) & 1);
     }
   } else if (warp == 1 || warp == kIssuer1Warp) {
     // ---------------------------------------------------------------- MMA issuers
@@ -717,13 +777,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
       const int k0 = 8 * q;
       bool ok = true;
       for (int c = 0; c < nch && ok; ++c) {
-        const int s = c % stages, b = c % kAbuf;
-        ok = wait_or_abort(smem_u32(&S.a_full[b]), (c / kAbuf) & 1, abort_flag) &&
-             wait_or_abort(smem_u32(&S.hfull[s]), (c / stages) & 1, abort_flag);
+        const int hs = c % hst, b = c % kAbuf;
+        ok = wait_or_abort(smem_u32(&S.a_full[b]), (c / kAbuf) & 1, abort_flag);
+        if (q == 0) PL_TLC(5, c);
+        ok = ok && wait_or_abort(smem_u32(&S.hfull[hs]), (c / hst) & 1, abort_flag);
         if (!ok) break;
-        PL_TLC(1, c);
+        if (q == 0) PL_TLC(1, c);
         tc_fence_after();
-        const uint32_t hbase = smem_u32(smem + static_cast<size_t>(s) * stage_bytes + kCodesBytes);
+        const uint32_t hbase = smem_u32(hreg + static_cast<size_t>(hs) * h_bytes);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int kk = k0 + i;
@@ -731,7 +792,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
           mma_ts(dcol, tmem + kColA0 + 128u * b + kk * 8, bdesc, idesc, (c > 0 || i > 0) ? 1u : 0u);
         }
         tc_commit(smem_u32(&S.a_empty[b]));
-        tc_commit(smem_u32(&S.empty[s]));
+        tc_commit(smem_u32(&S.hempty[hs]));
+      }
+      if (ok && q == 0 && lora_here) {
+        // lambda B t: K steps over the rank, B rows (as stored) x bf16(lambda t)^T, into a
+        // weight buffer whose last chunk has completed (by both issuers)
+        ok = wait_or_abort(smem_u32(&S.tq_full), 0, abort_flag) &&
+             (nch < kAbuf || wait_or_abort(smem_u32(&S.a_empty[b_lora]), ((nch - kAbuf) / kAbuf) & 1, abort_flag));
+        if (ok) {
+          tc_fence_after();
+          const uint32_t idesc_l = idesc_f16(kTileO, N, 1);
+          const int ksteps = (P.r + 15) / 16;
+          for (int kk = 0; kk < ksteps; ++kk)
+            mma_ss(tmem + kColA0 + 128u * b_lora, smem_desc_sw128(smem_u32(sBa) + kk * 32, 1024),
+                   smem_desc_sw128(smem_u32(sTq) + kk * 32, 1024), idesc_l, kk > 0 ? 1u : 0u);
+        }
       }
       tc_commit(smem_u32(&S.d_full));  // also reached on abort: tracks every MMA issued
       if (q == 0) PL_TL(6);
@@ -745,43 +820,41 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     bool ok = true;
     if (threadIdx.x == 64) S.s_g = *P.s_g;  // weight inputs: never written by the preceding kernel
-    if (lora) {
-      // B rows of this tile, transposed into sBt[j][row] (bf16, zero past r and past d_o);
-      // the tile's rows are one contiguous block of 128 r elements of B
+    if (lora_here) {
+      // B rows of this tile into sBa (bf16, 128-byte swizzle, zero past r and past d_o):
+      // thread et fills 16-byte pieces (row o, columns 8 j8 .. 8 j8 + 7)
       const int et0 = threadIdx.x - 64;
       const int64_t o0 = static_cast<int64_t>(tile) * kTileO;
       const int rows = static_cast<int>(P.d_o - o0 < kTileO ? P.d_o - o0 : kTileO);
-      for (int i = et0; i < kTileO * kMaxR; i += kEpiThreads) sBt[i] = __float2bfloat16_rn(0.f);
-      named_bar(1, kEpiThreads);
-      const int n8 = rows * P.r / 8;  // 16-byte pieces (r % 8 == 0) or element-wise otherwise
-      if ((P.r & 7) == 0) {
-        const uint4* src = reinterpret_cast<const uint4*>(P.B + o0 * P.r);
-        for (int i = et0; i < n8; i += kEpiThreads) {
-          const uint4 v = src[i];
-          const uint16_t* e8 = reinterpret_cast<const uint16_t*>(&v);
+      for (int i = et0; i < kTileO * 8; i += kEpiThreads) {
+        const int o = i >> 3, j8 = i & 7;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (o < rows && 8 * j8 < P.r) {
+          const __nv_bfloat16* src = P.B + (o0 + o) * P.r + 8 * j8;
+          if ((P.r & 7) == 0) {
+            v = *reinterpret_cast<const uint4*>(src);
+          } else {
+            uint16_t e[8];
 #pragma unroll
-          for (int qq = 0; qq < 8; ++qq) {
-            const int flat = 8 * i + qq, rr = flat / P.r, j = flat % P.r;
-            sBt[j * kTileO + rr] = __ushort_as_bfloat16(e8[qq]);
+            for (int q = 0; q < 8; ++q) e[q] = 8 * j8 + q < P.r ? __bfloat16_as_ushort(src[q]) : 0;
+            v = make_uint4(e[0] | (uint32_t(e[1]) << 16), e[2] | (uint32_t(e[3]) << 16),
+                           e[4] | (uint32_t(e[5]) << 16), e[6] | (uint32_t(e[7]) << 16));
           }
         }
-      } else {
-        for (int i = et0; i < rows * P.r; i += kEpiThreads) {
-          const int rr = i / P.r, j = i % P.r;
-          sBt[j * kTileO + rr] = P.B[(o0 + rr) * P.r + j];
-        }
+        *reinterpret_cast<uint4*>(sBa + o * 128 + ((j8 ^ (o & 7)) << 4)) = v;
       }
     }
     for (int c = 0; c < nch; ++c) {
       const int s = c % stages, b = c % kAbuf;
-      ok = wait_or_abort(smem_u32(&S.wfull[s]), (c / stages) & 1, abort_flag) &&
-           (c < kAbuf || wait_or_abort(smem_u32(&S.a_empty[b]), ((c / kAbuf) - 1) & 1, abort_flag));
+      ok = wait_or_abort(smem_u32(&S.wfull[s]), (c / stages) & 1, abort_flag);
+      if (threadIdx.x == 64) PL_TLC(4, c);
+      ok = ok && (c < kAbuf || wait_or_abort(smem_u32(&S.a_empty[b]), ((c / kAbuf) - 1) & 1, abort_flag));
       if (!ok) break;
       if (c == 0 && threadIdx.x == 64) PL_TL(4);
       if (threadIdx.x == 64) PL_TLC(3, c);
-      const uint8_t* st = smem + static_cast<size_t>(s) * stage_bytes;
+      const uint8_t* st = smem + static_cast<size_t>(s) * kWStage;
       const uint8_t* crow = st + row * 128;
-      const uint2 sc8 = *reinterpret_cast<const uint2*>(st + kCodesBytes + h_bytes + row * 16 + g * 8);
+      const uint2 sc8 = *reinterpret_cast<const uint2*>(st + kCodesBytes + row * 16 + g * 8);
       const uint32_t sc_words[2] = {sc8.x, sc8.y};
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
@@ -804,52 +877,75 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
+      if (threadIdx.x == 64) PL_TLC(2, c);
       if (lane == 0) {
         mbar_arrive(smem_u32(&S.a_full[b]));
         mbar_arrive(smem_u32(&S.empty[s]));
       }
     }
     if (threadIdx.x == 64) PL_TL(5);
+    // ---------------------------------------------------------------- lambda t operand
+    pdl_wait();  // the row scales and t belong to this call's prologue
+    const int et = threadIdx.x - 64;  // 0 .. 255
+    if (lora_here) {
+      // sTq[n][j] = bf16(lambda t[n][toff + j]), zero past r and past M, 16 bytes a thread
+      const int mt = static_cast<int>(Q.M < N ? Q.M : N);
+      for (int i = et; i < N * 8; i += kEpiThreads) {
+        const int n = i >> 3, j8 = i & 7;
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        if (n < mt && 8 * j8 < P.r) {
+          const float* tr = Q.t + static_cast<int64_t>(n) * Q.t_ld + P.toff + 8 * j8;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float lo = 8 * j8 + 2 * q < P.r ? P.lambda * tr[2 * q] : 0.f;
+            const float hi = 8 * j8 + 2 * q + 1 < P.r ? P.lambda * tr[2 * q + 1] : 0.f;
+            w[q] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+                   (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+          }
+        }
+        *reinterpret_cast<uint4*>(sTq + n * 128 + ((j8 ^ (n & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      fence_proxy_async_smem();  // sBa and sTq are read by the tensor cores
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&S.tq_full));
+    }
     // ---------------------------------------------------------------- epilogue, part 1
     ok = wait_or_abort(smem_u32(&S.d_full), 0, abort_flag) && ok;
     tc_fence_after();
     if (threadIdx.x == 64) PL_TL(7);
-    pdl_wait();  // the row scales and t belong to this call's prologue
-    const int et = threadIdx.x - 64;  // 0 .. 255
     if (et < N) S.rowscale[et] = et < Q.M ? Q.rowscale[et] : 0.f;
     go = named_bar_and(1, kEpiThreads, ok && !*abort_flag);  // one decision, publishes the row scales
     if (threadIdx.x == 64) PL_TL(8);
     if (go) {
-      float* red = reinterpret_cast<float*>(smem);  // [N][128]    s_g c_n D1, reuses the stages
+      // y[n][o] = s_g c_n (D1 even + D1 odd)[o][n] + (lambda B t)[o][n]: stored at once
+      // without a K split, else as this split's partial into red [N][128] (the stages)
+      float* red = reinterpret_cast<float*>(smem);
       const float s_g = S.s_g;
       const int half = N / 2;  // 8, 16, 24 or 32 tokens per thread
       const int n0 = g * half;
       const uint32_t acc = tmem + lane_addr + kColAcc + static_cast<uint32_t>(n0);
+      const uint32_t accl = tmem + lane_addr + kColA0 + 128u * b_lora + static_cast<uint32_t>(n0);
+      const int64_t oo = static_cast<int64_t>(tile) * kTileO + row;
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) {
-        if (cb * 8 < half) {  // 8 tokens at a time: the two halves of D1
-          uint32_t da[8], db[8];
+        if (cb * 8 < half) {  // 8 tokens at a time
+          uint32_t da[8], db[8], dl[8];
           tmem_ld8(acc + cb * 8, da);
           tmem_ld8(acc + 64 + cb * 8, db);
+          if (lora_here) tmem_ld8(accl + cb * 8, dl);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int n = n0 + cb * 8 + i;
-            red[n * kTileO + row] = s_g * S.rowscale[n] * (__uint_as_float(da[i]) + __uint_as_float(db[i]));
+            float v = s_g * S.rowscale[n] * (__uint_as_float(da[i]) + __uint_as_float(db[i]));
+            if (lora_here) v += __uint_as_float(dl[i]);
+            if (p.splits > 1) {
+              red[n * kTileO + row] = v;
+            } else if (n < Q.M && oo < P.d_o) {
+              if (p.y_f32) static_cast<float*>(P.y)[n * P.d_o + oo] = v;
+              else static_cast<__nv_bfloat16*>(P.y)[n * P.d_o + oo] = __float2bfloat16_rn(v);
+            }
           }
-        }
-      }
-      // lambda t of this projection (zeros past r), from the prologue
-      if (lora) {
-        float* tful = red + N * kTileO;  // [N][kTStride]
-        const int mt = static_cast<int>(Q.M < N ? Q.M : N);
-        const int r4 = (P.r + 3) / 4;
-        for (int e = et; e < mt * r4; e += kEpiThreads) {
-          const int n = e / r4, jj = 4 * (e % r4);
-          const float* tr = Q.t + static_cast<int64_t>(n) * Q.t_ld + P.toff + jj;
-          reinterpret_cast<float4*>(tful + n * kTStride + jj)[0] =
-              make_float4(P.lambda * tr[0], jj + 1 < P.r ? P.lambda * tr[1] : 0.f,
-                          jj + 2 < P.r ? P.lambda * tr[2] : 0.f, jj + 3 < P.r ? P.lambda * tr[3] : 0.f);
         }
       }
     }
@@ -858,20 +954,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
   tc_fence_before();
   __syncthreads();
   // ------------------------------------------------------------------ epilogue, part 2
-  // After a cluster barrier every CTA sums the D1 partials of its row groups (4 rows each,
-  // groups [32 split / S, 32 (split+1) / S)) over the S CTAs in split order, adds
-  // B (lambda t) and writes y.
+  // With a K split: after a cluster barrier every CTA sums the partials of its row groups
+  // (4 rows each, groups [32 split / S, 32 (split+1) / S)) over the S CTAs in split order
+  // and writes y.
   if (p.splits > 1) cluster_sync();
   if (threadIdx.x == 0) PL_TL(10);
-  if (threadIdx.x >= 64 && threadIdx.x < 64 + kEpiThreads && go) {
+  if (p.splits > 1 && threadIdx.x >= 64 && threadIdx.x < 64 + kEpiThreads && go) {
     const int et = threadIdx.x - 64;
-    float* red = reinterpret_cast<float*>(smem);
-    const float* tful = red + N * kTileO;
-    const uint32_t red_addr = smem_u32(red);
+    const uint32_t red_addr = smem_u32(smem);
     const int mt = static_cast<int>(Q.M < N ? Q.M : N);
-    // This CTA's share of the tile's rows: groups of 4 rows [g0, g1) of 32.  Thread et takes
-    // row r0 + et % nrows and every ngrp-th token from et / nrows; it sums the D1 partials
-    // of the S CTAs (split order) and adds B (lambda t).
     const int g0 = (split * (kTileO / 4)) / p.splits, g1 = ((split + 1) * (kTileO / 4)) / p.splits;
     const int r0 = 4 * g0, nrows = 4 * (g1 - g0);
     const int ngrp = kEpiThreads / nrows;  // >= 2: a share has at most 128 rows
@@ -879,53 +970,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant
     if (tg < ngrp) {
       const int rr = r0 + rl;
       const int64_t oo = static_cast<int64_t>(tile) * kTileO + rr;
-      const int r4 = lora ? (P.r + 3) / 4 : 0;
-      // y[n][rr] = (sum over splits of the D1 partials) + lora, stored as FP32 or BF16
-      auto finish = [&](int n, float lora_sum) {
-        float d = 0.f;
-        if (p.splits == 1) {
-          d = red[n * kTileO + rr];
-        } else {
-          const uint32_t addr = red_addr + static_cast<uint32_t>((n * kTileO + rr) * 4);
-          float part[kMaxSplit];
+      for (int n = tg; n < mt; n += ngrp) {
+        const uint32_t addr = red_addr + static_cast<uint32_t>((n * kTileO + rr) * 4);
+        float part[kMaxSplit];
 #pragma unroll
-          for (int sp = 0; sp < kMaxSplit; ++sp)
-            if (sp < p.splits) part[sp] = ld_dsmem_f32(mapa_shared(addr, sp));
+        for (int sp = 0; sp < kMaxSplit; ++sp)
+          if (sp < p.splits) part[sp] = ld_dsmem_f32(mapa_shared(addr, sp));
+        float v = 0.f;
 #pragma unroll
-          for (int sp = 0; sp < kMaxSplit; ++sp)
-            if (sp < p.splits) d += part[sp];
-        }
-        const float v = d + lora_sum;
+        for (int sp = 0; sp < kMaxSplit; ++sp)
+          if (sp < p.splits) v += part[sp];
         if (oo < P.d_o) {
           if (p.y_f32) static_cast<float*>(P.y)[n * P.d_o + oo] = v;
           else static_cast<__nv_bfloat16*>(P.y)[n * P.d_o + oo] = __float2bfloat16_rn(v);
         }
-      };
-      // four tokens per round (n + i ngrp): independent FMA chains in flight; B[rr][j] comes
-      // from sBt[j][rr] (zeros past r), 32 neighbouring rows of one row of sBt per warp
-      constexpr int kTok = 4;
-      for (int n = tg; n < mt; n += kTok * ngrp) {
-        float acc[kTok] = {0.f, 0.f, 0.f, 0.f};
-        const float4* tn[kTok];
-#pragma unroll
-        for (int i = 0; i < kTok; ++i) {
-          const int ni = n + i * ngrp;
-          tn[i] = reinterpret_cast<const float4*>(tful + (ni < mt ? ni : n) * kTStride);
-        }
-        for (int j4 = 0; j4 < r4; ++j4) {
-          const float w0 = __bfloat162float(sBt[(4 * j4) * kTileO + rr]);
-          const float w1 = __bfloat162float(sBt[(4 * j4 + 1) * kTileO + rr]);
-          const float w2 = __bfloat162float(sBt[(4 * j4 + 2) * kTileO + rr]);
-          const float w3 = __bfloat162float(sBt[(4 * j4 + 3) * kTileO + rr]);
-#pragma unroll
-          for (int i = 0; i < kTok; ++i) {
-            const float4 t4 = tn[i][j4];  // the same address across the warp: a broadcast
-            acc[i] = fmaf(w0, t4.x, fmaf(w1, t4.y, fmaf(w2, t4.z, fmaf(w3, t4.w, acc[i]))));
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < kTok; ++i)
-          if (n + i * ngrp < mt) finish(n + i * ngrp, acc[i]);
       }
     }
   }
@@ -966,20 +1024,20 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void*
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-uint32_t stage_bytes_for(int N) { return kCodesBytes + kScaleBytes + static_cast<uint32_t>(N) * 512u; }
-
-// Shared memory of the main kernel: as many stages as fit (at most kMaxStages), the B rows
-// of the tile, the control block and 1 KB of alignment slack.  The epilogue reuses the
-// stage region for its partials and lambda t ([N][128] + [N][68] FP32 < 0.8 KB x N), which
-// two stages always cover.
-void stage_plan(int N, int& stages, uint32_t& sb, size_t& total) {
-  sb = stage_bytes_for(N);
+// Shared memory of the main kernel: the stage region (as many weight stages as fit, at
+// most kMaxStages, then h_stages_for(N) activation stages), the B rows of the tile and
+// lambda t (the up-projection's operands), the control block and 1 KB of alignment slack.
+// With a K split the epilogue reuses the stage region for its partials ([N][128] FP32,
+// 0.5 KB x N), which two weight stages always cover.  A member of a launch with fewer
+// tokens than the largest lays its own stages out in the same region.
+void stage_plan(int N, uint32_t& region, size_t& total) {
   const size_t limit = 227 * 1024;
-  const size_t fixed = 1024 + kTileO * kMaxR * 2 + sizeof(Smem);
-  int st = static_cast<int>((limit - fixed) / sb);
-  st = st > kMaxStages ? kMaxStages : st;
-  stages = st < 2 ? 2 : st;
-  total = fixed + static_cast<size_t>(stages) * sb;
+  const size_t fixed = 1024 + kBaBytes + static_cast<size_t>(N) * 128 + sizeof(Smem);
+  const size_t hpart = static_cast<size_t>(h_stages_for(N)) * static_cast<size_t>(N) * 512;
+  int ws = static_cast<int>((limit - fixed - hpart) / kWStage);
+  ws = ws > kMaxStages ? kMaxStages : (ws < 2 ? 2 : ws);
+  region = static_cast<uint32_t>(static_cast<size_t>(ws) * kWStage + hpart);
+  total = fixed + region;
 }
 
 cudaError_t set_kernel_attributes() {
@@ -1006,10 +1064,9 @@ int max_active_clusters(int N, int cs) {
   std::lock_guard<std::mutex> lk(mu);
   int& c = cache[N / 16][cs];
   if (c == 0) {
-    int st;
-    uint32_t sb;
+    uint32_t region;
     size_t total;
-    stage_plan(N, st, sb, total);
+    stage_plan(N, region, total);
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(cs * 64));
     cfg.blockDim = dim3(kThreads);
@@ -1158,11 +1215,15 @@ cudaError_t launch_linear_tc_batch(int64_t d_i, float eps, const TcSet* sets, in
   carve_sets(ws, d_i, Ms, rtot, n_sets, w);
   const int kc = static_cast<int>(d_i / kChunkK);
   const int splits = choose_splits(Nmax, tiles, kc);
-  int stages;
-  uint32_t sb;
+  uint32_t stage_region;
   size_t smem;
-  stage_plan(Nmax, stages, sb, smem);  // the largest N sets the allocation: at least two of its stages
-  const uint32_t stage_region = static_cast<uint32_t>(smem - (1024 + kTileO * kMaxR * 2 + sizeof(Smem)));
+  stage_plan(Nmax, stage_region, smem);  // the largest N sets the allocation
+  const uint32_t tq_region = static_cast<uint32_t>(Nmax) * 128u;
+  for (int s = 0; s < n_sets; ++s) {  // every member's own layout holds two weight stages
+    const uint32_t N = static_cast<uint32_t>((sets[s].M + 15) / 16 * 16);
+    const uint32_t hpart = static_cast<uint32_t>(h_stages_for(static_cast<int>(N))) * N * 512u;
+    if (hpart + 2 * kWStage > stage_region) return cudaErrorInvalidValue;
+  }
 
   TcMaps maps;
   memset(&maps, 0, sizeof(maps));
@@ -1213,6 +1274,7 @@ cudaError_t launch_linear_tc_batch(int64_t d_i, float eps, const TcSet* sets, in
   p.splits = splits;
   p.kc = kc;
   p.stage_region = stage_region;
+  p.tq_region = tq_region;
   p.n_proj = n_proj;
   p.y_f32 = y_f32 ? 1 : 0;
   for (int s = 0; s < n_sets; ++s)
