@@ -205,7 +205,10 @@ size_t pl_workspace_bytes_group(int64_t M, int64_t d_i, const pl_nvfp4_proj* pro
  * Results equal those of separate calls within the linear's tolerance.  For decode batch
  * sizes (M <= 64, d_i % 256 == 0, at most 4 projections, sum of ranks <= 128) the group
  * runs as one prologue (h once, t_p = A_p h once per projection) and one main kernel over
- * the weight tiles of all projections; otherwise the projections run one after another.
+ * the weight tiles of all projections.  For large M (M > 64, d_i % 256 == 0, at most 4
+ * projections, ranks <= 32) it runs as one row pass (h / c_m once), one adapter
+ * down-projection per projection and one contraction over the weight tiles of all
+ * projections.  Otherwise the projections run one after another.
  * Requirements: those of pl_nvfp4_lora_linear for every projection, 1 <= n_proj <=
  * PL_MAX_GROUP; the y buffers must not overlap one another or any input.  `projs` is a
  * HOST array, read during the call only. */

@@ -220,6 +220,10 @@ size_t pl_workspace_bytes_group(int64_t M, int64_t d_i, const pl_nvfp4_proj* pro
     const size_t g = pl::tc_batch_workspace_bytes(d_i, &set, 1, tp, n_proj);
     need = need > g ? need : g;
   }
+  if (pl::prefill_group_supported(M, d_i, tp, n_proj)) {
+    const size_t g = pl::prefill_group_workspace_bytes(M, d_i, tp, n_proj);
+    need = need > g ? need : g;
+  }
   return need;
 }
 
@@ -245,12 +249,26 @@ pl_status pl_nvfp4_lora_linear_group(const void* x, int64_t M, int64_t d_i, cons
   pl_status st = device_check();
   if (st != PL_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // one launch pair for the whole group on the two-kernel decode path; otherwise one call
-  // per projection, in order
+  // one launch pair for the whole group on the two-kernel decode path, one row pass and one
+  // contraction at large M; otherwise one call per projection, in order
   const pl::TcSet set{x, M, w_norm, w_norm ? z : nullptr, (w_norm && z) ? z_ld : 0};
   if (n_proj > 1 && pl::tc_batch_supported(d_i, &set, 1, tp, n_proj))
     return check_launch(pl::launch_linear_tc_batch(d_i, eps, &set, 1, tp, n_proj, y_dtype == PL_DTYPE_F32,
                                                    workspace, s));
+  if (n_proj > 1 && pl::prefill_group_supported(M, d_i, tp, n_proj)) {
+    pl::LinearArgs in{};
+    in.x = x;
+    in.M = M;
+    in.d_i = d_i;
+    in.w_norm = w_norm;
+    in.z = w_norm ? z : nullptr;
+    in.z_ld = (w_norm && z) ? z_ld : 0;
+    in.eps = eps;
+    in.y_f32 = y_dtype == PL_DTYPE_F32;
+    in.ws = workspace;
+    in.ws_bytes = ws_bytes;
+    return check_launch(pl::launch_linear_prefill_group(in, tp, n_proj, s));
+  }
   for (int i = 0; i < n_proj; ++i) {
     st = pl_nvfp4_lora_linear(x, M, d_i, tp[i].d_o, tp[i].codes, tp[i].scales, tp[i].s_g, tp[i].A, tp[i].B, tp[i].r,
                               tp[i].lambda, w_norm, z, z_ld, eps, tp[i].y, y_dtype, workspace, ws_bytes, stream);

@@ -84,8 +84,19 @@ uint32_t tc_read_and_clear_status();
 cudaError_t launch_wait_timeout_probe(cudaStream_t stream);
 // The row prologue on its own: hq = f16(RMSNorm_AQN(x) / rowscale) [M][d_i], rowscale
 // [M] (powers of two), A16 = f16(A) [r][d_i], and n_zero zeros (a multiple of 4) at zero.
-cudaError_t launch_act_prologue(const LinearArgs& a, __half* hq, float* rowscale, __half* A16, float* zero,
-                                int64_t n_zero, cudaStream_t stream);
+// The adapters a row prologue converts to f16 (and the counters it zeroes), one segment per
+// projection of a large-M group.
+constexpr int kMaxActConv = 4;
+struct ActConv {
+  const void* A[kMaxActConv];   // bf16 [r][d_i]
+  __half* A16[kMaxActConv];     // f16 [r][d_i]
+  int r[kMaxActConv];
+  float* zero[kMaxActConv];     // floats to zero (or null)
+  int64_t n_zero[kMaxActConv];  // a multiple of 4
+  int n;
+};
+cudaError_t launch_act_prologue(const LinearArgs& a, __half* hq, float* rowscale, const ActConv& conv,
+                                cudaStream_t stream);
 
 // ---- linear_fused.cu (tcgen05, one kernel; M <= 64 and at most 3 K chunks of 256 per CTA)
 bool fused_supported(int64_t M, int64_t d_i, int64_t d_o, int r);
@@ -96,6 +107,14 @@ uint32_t fused_read_and_clear_status();
 bool prefill_supported(int64_t M, int64_t d_i, int64_t d_o, int r);
 size_t prefill_workspace_bytes(int64_t M, int64_t d_i, int64_t d_o, int r);
 cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream);
+// A group of projections on one input at large M (q/k/v, gate/up): one row prologue, one
+// LoRA down-projection per adapter, one contraction over every member's weight tiles.
+// `in` carries the input, norm, noise, eps, y_f32 and the workspace; the members' fields
+// are those of the group entry (TcProj::set unused).
+constexpr int kMaxPrefillGroup = 4;
+bool prefill_group_supported(int64_t M, int64_t d_i, const TcProj* projs, int n);
+size_t prefill_group_workspace_bytes(int64_t M, int64_t d_i, const TcProj* projs, int n);
+cudaError_t launch_linear_prefill_group(const LinearArgs& in, const TcProj* projs, int n, cudaStream_t stream);
 uint32_t prefill_read_and_clear_status();
 
 // ---- w8a8.cu (FP8 E4M3 W8A8 linear; d_i % 128 == 0)

@@ -89,20 +89,38 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxR = 32;
 constexpr int kLoraK = 64;  // K columns the LoRA step adds (r <= 32 of them nonzero)
 
-struct GParams {
-  int64_t M, d_i, d_o;
-  int r, n_ot, n_tiles, n_ks, stages;
+// One projection of a launch (a group shares the input): its pairs of weight tiles are
+// [ot0, ot0 + ceil(d_o / 256)) of the launch's n_ot.
+struct GMember {
+  int64_t d_o;
+  int r, ot0;
   const float* s_g;
-  const __nv_bfloat16* B; // [d_o][r], as stored: the A operand of the LoRA step
+  const __nv_bfloat16* B;  // [d_o][r], as stored: the A operand of the LoRA step
+  void* y;                 // [M][d_o]
+};
+
+struct GParams {
+  int64_t M, d_i;
+  int n_ot, n_tiles, n_ks, stages, n_g;
   const float* rowscale;  // [M_pad]
-  void* y;
   int y_f32;
   uint32_t off_scales, off_t, t_slot_bytes, off_ctrl;
+  GMember g[kMaxPrefillGroup];
 };
 
 struct GMaps {
-  CUtensorMap codes, scales, hq, tq;
+  CUtensorMap hq;
+  CUtensorMap codes[kMaxPrefillGroup], scales[kMaxPrefillGroup], tq[kMaxPrefillGroup];
 };
+
+// The member a pair of weight tiles belongs to: the last one whose first pair is <= ot.
+__device__ __forceinline__ int member_of(const GParams& p, int ot) {
+  int gi = 0;
+#pragma unroll
+  for (int q = 1; q < kMaxPrefillGroup; ++q)
+    if (q < p.n_g && ot >= p.g[q].ot0) gi = q;
+  return gi;
+}
 
 struct GCtrl {
   uint64_t full[kMaxStages], empty[kMaxStages];
@@ -112,7 +130,7 @@ struct GCtrl {
   uint64_t mma_done;  // every MMA this CTA issued has completed
   uint32_t tmem_base;
   int abort_flag;
-  float s_g;
+  float s_g[kMaxPrefillGroup];
 };
 
 __device__ __noinline__ bool wait_p_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
@@ -188,8 +206,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = smem_u32(smem);
   const int nst = p.stages, n_ks = p.n_ks;
-  const bool lora = p.r > 0;
-  const int n_steps = n_ks + (lora ? 1 : 0);  // K steps per tile, the LoRA step last
   const int rank = static_cast<int>(cta_rank());  // 0: issues the MMAs of the pair
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
@@ -214,10 +230,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
     }
     mbar_init(smem_u32(&C.mma_done), 1);
     C.abort_flag = 0;
-    C.s_g = *p.s_g;  // a weight input: not written by the preceding kernel
+    for (int q = 0; q < p.n_g; ++q) {
+      C.s_g[q] = *p.g[q].s_g;  // weight inputs: not written by the preceding kernel
+      tma_prefetch_desc(&maps.codes[q]);
+      tma_prefetch_desc(&maps.scales[q]);
+    }
     fence_mbar_init();
-    tma_prefetch_desc(&maps.codes);
-    tma_prefetch_desc(&maps.scales);
     tma_prefetch_desc(&maps.hq);
   }
   if (warp == 1) {
@@ -242,7 +260,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
       int it = 0, t_issued = 0;
       for (int tile = pair; tile < p.n_tiles && ok; tile += npairs, ++it) {
         const int mt = tile / p.n_ot, ot = tile % p.n_ot;
-        const int32_t m0 = mt * TN, o0 = ot * 2 * kTO + rank * kTO, mh = m0 + rank * kTH;
+        const int gi = member_of(p, ot);
+        const int n_steps = n_ks + (p.g[gi].r > 0 ? 1 : 0);  // K steps of this tile, the LoRA step last
+        const int32_t m0 = mt * TN, o0 = (ot - p.g[gi].ot0) * 2 * kTO + rank * kTO, mh = m0 + rank * kTH;
         {  // the row scales of this tile's tokens (all TN: this CTA's accumulator spans them)
           const int tb = it & 1;
           {
@@ -268,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
           const uint32_t fb = smem_u32(&C.full[st]);
           if (s == n_ks) {  // the LoRA step: Tq rows of this CTA's half of the tokens
             mbar_arrive_expect_tx(fb, kHBytesT);
-            tma_load_2d(sbase + st * kStageBytes, &maps.tq, 0, mh, fb);
+            tma_load_2d(sbase + st * kStageBytes, &maps.tq[gi], 0, mh, fb);
             continue;
           }
           const bool scl = (s & 3) == 0;
@@ -276,10 +296,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
           const uint32_t stage = sbase + st * kStageBytes;
           tma_load_2d(stage, &maps.hq, s * kKS, mh, fb);
           // weights and hq both stay in L2: every weight tile is read once per token tile
-          tma_load_2d(stage + kHBytesT, &maps.codes, s * (kKS / 2), o0, fb);
+          tma_load_2d(stage + kHBytesT, &maps.codes[gi], s * (kKS / 2), o0, fb);
           if (scl) {
             ++grp;
-            tma_load_2d(sbase + p.off_scales + (grp % kScaleSlots) * kScaleBytes, &maps.scales,
+            tma_load_2d(sbase + p.off_scales + (grp % kScaleSlots) * kScaleBytes, &maps.scales[gi],
                         s * (kKS / 16), o0, fb);
           }
         }
@@ -296,13 +316,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
     if (lane == 0 && rank == 0) {
       const uint32_t idesc = idesc_f16(2 * kTO, TN, 0);
       const uint32_t idesc_l = idesc_f16(2 * kTO, TN, 1);  // the LoRA step: bf16 B and T
-      const int l_sub = (p.r + 15) / 16;                      // its K sub-steps of 16
       bool ok = true;
       Ring rs, ra;  // stage and slot rings
       const uint64_t hdesc0 = smem_desc_sw128(sbase, 1024);
       int it = 0;
       for (int tile = pair; tile < p.n_tiles && ok; tile += npairs, ++it) {
         const int b = it & 1;
+        const int r_t = p.g[member_of(p, tile % p.n_ot)].r;  // this tile's adapter rank
+        const bool lora = r_t > 0;
+        const int l_sub = (r_t + 15) / 16;  // the LoRA step's K sub-steps of 16
         {
           PF_T0();
           if (it >= 2) ok = wait_p(smem_u32(&C.dempty[b]), ((it >> 1) - 1) & 1, abort_flag);
@@ -366,22 +388,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
     int it = 0;
     for (int tile = pair; tile < p.n_tiles && ok; tile += npairs, ++it) {
       const int ot = tile % p.n_ot;
-      const int64_t o = static_cast<int64_t>(ot) * 2 * kTO + rank * kTO + row;
+      const GMember& G = p.g[member_of(p, ot)];
+      const int r = G.r;
+      const bool lora = r > 0;
+      const int n_steps = n_ks + (lora ? 1 : 0);
+      const int64_t o = static_cast<int64_t>(ot - G.ot0) * 2 * kTO + rank * kTO + row;
       // this thread's half of the LoRA step's 64 K columns of its row: B[o][32 g .. 32 g + 32),
       // bf16 as stored, zero beyond r (r <= 32: the g = 1 half is all zero)
       uint4 bq[4] = {};
-      if (lora && g == 0 && o < p.d_o) {
-        if ((p.r & 7) == 0) {
-          const uint4* src = reinterpret_cast<const uint4*>(p.B + o * p.r);
+      if (lora && g == 0 && o < G.d_o) {
+        if ((r & 7) == 0) {
+          const uint4* src = reinterpret_cast<const uint4*>(G.B + o * r);
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            if (8 * q < p.r) bq[q] = src[q];
+            if (8 * q < r) bq[q] = src[q];
         } else {
-          const uint16_t* src = reinterpret_cast<const uint16_t*>(p.B + o * p.r);
+          const uint16_t* src = reinterpret_cast<const uint16_t*>(G.B + o * r);
           uint32_t w[16];
 #pragma unroll
           for (int j2 = 0; j2 < 16; ++j2) {
-            const uint32_t lo = 2 * j2 < p.r ? src[2 * j2] : 0u, hi = 2 * j2 + 1 < p.r ? src[2 * j2 + 1] : 0u;
+            const uint32_t lo = 2 * j2 < r ? src[2 * j2] : 0u, hi = 2 * j2 + 1 < r ? src[2 * j2 + 1] : 0u;
             w[j2] = lo | (hi << 16);
           }
 #pragma unroll
@@ -440,13 +466,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    const float s_g = C.s_g;
     bool ok = true;
     int it = 0;
     for (int tile = pair; tile < p.n_tiles && ok; tile += npairs, ++it) {
       const int mt = tile / p.n_ot, ot = tile % p.n_ot;
       const int b = it & 1;
-      const int64_t o = static_cast<int64_t>(ot) * 2 * kTO + rank * kTO + row;
+      const int gi = member_of(p, ot);
+      const GMember& G = p.g[gi];
+      const float s_g = C.s_g[gi];
+      const int64_t o = static_cast<int64_t>(ot - G.ot0) * 2 * kTO + rank * kTO + row;
       {
         PF_T0();
         ok = wait_p(smem_u32(&C.dfull[b]), (it >> 1) & 1, abort_flag) &&
@@ -461,14 +489,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
         uint32_t dv[16];
         tmem_ld16(tmem + lane_addr + (kColD0 + static_cast<uint32_t>(TN) * b) + col, dv);
         tmem_ld_wait();
-        if (o < p.d_o) {
+        if (o < G.d_o) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int64_t m = static_cast<int64_t>(mt) * TN + col + i;
             const float v = s_g * rsc[col + i] * __uint_as_float(dv[i]);
             if (m < p.M) {
-              if (p.y_f32) static_cast<float*>(p.y)[m * p.d_o + o] = v;
-              else static_cast<__nv_bfloat16*>(p.y)[m * p.d_o + o] = __float2bfloat16_rn(v);
+              if (p.y_f32) static_cast<float*>(G.y)[m * G.d_o + o] = v;
+              else static_cast<__nv_bfloat16*>(G.y)[m * G.d_o + o] = __float2bfloat16_rn(v);
             }
           }
         }
@@ -684,17 +712,22 @@ int r4(int r) { return r > 0 ? (r + 3) / 4 * 4 : 0; }
 
 constexpr int kMaxLdSplits = 8;
 
-struct PfWs {
-  __half* hq;
-  float* rowscale;
+// Workspace of one launch: the shared f16 rows and row scales, then per member the f16
+// adapter, the LoRA down-projection's split partials and counters, and Tq.
+struct PfMemberWs {
   __half* A16;
   float* t_part;
   int* counters;          // [token tiles of the down-projection]
   __nv_bfloat16* Tq;      // [Mp][64]: bf16(T), zero beyond r
+};
+struct PfWs {
+  __half* hq;
+  float* rowscale;
+  PfMemberWs m[kMaxPrefillGroup];
   size_t bytes;
 };
 
-PfWs carve(void* ws, int64_t M, int64_t d_i, int64_t d_o, int r) {
+PfWs carve(void* ws, int64_t M, int64_t d_i, const int* r, int n) {
   PfWs w{};
   const uintptr_t b = reinterpret_cast<uintptr_t>(ws);
   size_t off = 0;
@@ -703,14 +736,18 @@ PfWs carve(void* ws, int64_t M, int64_t d_i, int64_t d_o, int r) {
   off += align_up(static_cast<size_t>(M) * d_i * 2, 256);
   w.rowscale = reinterpret_cast<float*>(b + off);
   off += align_up(static_cast<size_t>(Mp) * 4, 256);
-  w.A16 = reinterpret_cast<__half*>(b + off);
-  off += align_up(static_cast<size_t>(r) * d_i * 2, 256);
-  w.t_part = reinterpret_cast<float*>(b + off);
-  off += align_up(static_cast<size_t>(kMaxLdSplits) * Mp * r4(r) * 4, 256);
-  w.counters = reinterpret_cast<int*>(b + off);
-  off += align_up(static_cast<size_t>((M + 127) / 128 + 6) * 4, 256);
-  w.Tq = reinterpret_cast<__nv_bfloat16*>(b + off);
-  off += align_up(static_cast<size_t>(Mp) * kLoraK * 2, 256);
+  for (int i = 0; i < n; ++i) {
+    PfMemberWs& q = w.m[i];
+    if (r[i] == 0) continue;
+    q.A16 = reinterpret_cast<__half*>(b + off);
+    off += align_up(static_cast<size_t>(r[i]) * d_i * 2, 256);
+    q.t_part = reinterpret_cast<float*>(b + off);
+    off += align_up(static_cast<size_t>(kMaxLdSplits) * Mp * r4(r[i]) * 4, 256);
+    q.counters = reinterpret_cast<int*>(b + off);
+    off += align_up(static_cast<size_t>((M + 127) / 128 + 6) * 4, 256);
+    q.Tq = reinterpret_cast<__nv_bfloat16*>(b + off);
+    off += align_up(static_cast<size_t>(Mp) * kLoraK * 2, 256);
+  }
   w.bytes = off;
   return w;
 }
@@ -757,53 +794,81 @@ bool prefill_supported(int64_t M, int64_t d_i, int64_t d_o, int r) {
          gplan(r, kTN).stages >= 3;
 }
 
-size_t prefill_workspace_bytes(int64_t M, int64_t d_i, int64_t d_o, int r) {
-  return carve(nullptr, M, d_i, d_o, r).bytes;
+bool prefill_group_supported(int64_t M, int64_t d_i, const TcProj* projs, int n) {
+  if (n < 1 || n > kMaxPrefillGroup) return false;
+  for (int i = 0; i < n; ++i)
+    if (!prefill_supported(M, d_i, projs[i].d_o, projs[i].r)) return false;
+  return true;
 }
 
-cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream) {
+size_t prefill_group_workspace_bytes(int64_t M, int64_t d_i, const TcProj* projs, int n) {
+  int r[kMaxPrefillGroup] = {0};
+  for (int i = 0; i < n && i < kMaxPrefillGroup; ++i) r[i] = projs[i].r;
+  return carve(nullptr, M, d_i, r, n < kMaxPrefillGroup ? n : kMaxPrefillGroup).bytes;
+}
+
+size_t prefill_workspace_bytes(int64_t M, int64_t d_i, int64_t d_o, int r) {
+  const TcProj one{d_o, nullptr, nullptr, nullptr, nullptr, nullptr, r, 0.f, nullptr, 0};
+  return prefill_group_workspace_bytes(M, d_i, &one, 1);
+}
+
+cudaError_t launch_linear_prefill_group(const LinearArgs& in, const TcProj* projs, int n, cudaStream_t stream) {
   cudaError_t e = set_attributes();
   if (e != cudaSuccess) return e;
-  const PfWs w = carve(a.ws, a.M, a.d_i, a.d_o, a.r);
-  const int64_t Mp = m_pad(a.M);
-  const int R4 = r4(a.r);
-  const bool lora = a.r > 0;
-  const int mtiles = static_cast<int>((a.M + 127) / 128);  // token tiles of the LoRA down-projection
-  e = launch_act_prologue(a, w.hq, w.rowscale, w.A16, lora ? reinterpret_cast<float*>(w.counters) : nullptr,
-                          lora ? (mtiles + 3) / 4 * 4 : 0, stream);
+  if (n < 1 || n > kMaxPrefillGroup) return cudaErrorInvalidValue;
+  int r[kMaxPrefillGroup] = {0};
+  for (int i = 0; i < n; ++i) r[i] = projs[i].A != nullptr && projs[i].B != nullptr ? projs[i].r : 0;
+  const PfWs w = carve(in.ws, in.M, in.d_i, r, n);
+  const int64_t Mp = m_pad(in.M);
+  const int mtiles = static_cast<int>((in.M + 127) / 128);  // token tiles of the LoRA down-projection
+
+  // 1. one row pass for the group; every adapter to f16, every down-projection's counters zeroed
+  ActConv conv{};
+  for (int i = 0; i < n; ++i) {
+    if (r[i] == 0) continue;
+    conv.A[conv.n] = projs[i].A;
+    conv.A16[conv.n] = w.m[i].A16;
+    conv.r[conv.n] = r[i];
+    conv.zero[conv.n] = reinterpret_cast<float*>(w.m[i].counters);
+    conv.n_zero[conv.n] = (mtiles + 3) / 4 * 4;
+    ++conv.n;
+  }
+  e = launch_act_prologue(in, w.hq, w.rowscale, conv, stream);
   if (e != cudaSuccess) return e;
 
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
-  const int n_ks = static_cast<int>(a.d_i / kKS);
+  const int n_ks = static_cast<int>(in.d_i / kKS);
   const int sms = sm_count();
 
-  if (lora) {
+  // 2. the LoRA down-projection of every member with an adapter: Tq = bf16((lambda / s_g) A hq)
+  for (int i = 0; i < n; ++i) {
+    if (r[i] == 0) continue;
     LMaps lm;
-    const int rb = (a.r + 15) / 16 * 16;
-    bool ok = encode_2d(&lm.hq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.hq, a.d_i, a.M, 64, 128,
+    const int rb = (r[i] + 15) / 16 * 16;
+    bool ok = encode_2d(&lm.hq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.hq, in.d_i, in.M, 64, 128,
                         CU_TENSOR_MAP_SWIZZLE_128B) &&
-              encode_2d(&lm.a16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.A16, a.d_i, a.r, 64, rb,
+              encode_2d(&lm.a16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.m[i].A16, in.d_i, r[i], 64, rb,
                         CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return cudaErrorInvalidValue;
     LParams lp{};
-    lp.M = a.M;
-    lp.d_i = a.d_i;
+    lp.M = in.M;
+    lp.d_i = in.d_i;
     lp.Mp = Mp;
-    lp.r = a.r;
-    lp.R4 = R4;
+    lp.r = r[i];
+    lp.R4 = r4(r[i]);
     lp.rb = rb;
     lp.n_ks = n_ks;
     int splits = sms / mtiles;  // one wave: every split of every token tile resident at once
     splits = splits > kMaxLdSplits ? kMaxLdSplits : splits;
     splits = splits > n_ks ? n_ks : (splits < 1 ? 1 : splits);  // every split has at least one K step
     lp.splits = splits;
-    lp.lambda = a.lambda;
-    lp.s_g = a.s_g;
-    lp.t_part = w.t_part;
-    lp.Tq = w.Tq;
-    lp.counters = w.counters;
+    lp.lambda = projs[i].lambda;
+    lp.s_g = projs[i].s_g;
+    lp.t_part = w.m[i].t_part;
+    lp.Tq = w.m[i].Tq;
+    lp.counters = w.m[i].counters;
     lp.mtiles = mtiles;
     cudaLaunchConfig_t c{};
     c.gridDim = dim3(static_cast<unsigned>(mtiles * splits));
@@ -814,50 +879,61 @@ cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream) {
     c.numAttrs = 1;
     e = cudaLaunchKernelEx(&c, k_lora_down, lm, lp);
     if (e != cudaSuccess) return e;
-    if (e != cudaSuccess) return e;
   }
 
-  // pair tiles of 256 weight rows x tn tokens: 128 when 192 leaves pairs idle; else 192 (the
-  // widest MMA the two accumulator buffers allow) or 160, whichever needs fewer rounds of
-  // the pairs, a round of 160-token tiles costing 0.966 of one of 192 (measured)
+  // 3. one contraction over every member's pairs of weight tiles (o fastest).  Token tiles
+  // of 128 when 192 leaves pairs idle; else 192 (the widest MMA the two accumulator buffers
+  // allow) or 160, whichever needs fewer rounds of the pairs, a round of 160-token tiles
+  // costing 0.966 of one of 192 (measured)
   const int pairs = sms / 2;
-  const int64_t n_ot64 = (a.d_o + 2 * kTO - 1) / (2 * kTO);
-  auto rounds = [&](int t) { return (n_ot64 * ((a.M + t - 1) / t) + pairs - 1) / pairs; };
+  int64_t n_ot64 = 0;
+  for (int i = 0; i < n; ++i) n_ot64 += (projs[i].d_o + 2 * kTO - 1) / (2 * kTO);
+  auto rounds = [&](int t) { return (n_ot64 * ((in.M + t - 1) / t) + pairs - 1) / pairs; };
   int tn = kTN;
-  if (n_ot64 * ((a.M + tn - 1) / tn) < pairs) tn = 128;
+  if (n_ot64 * ((in.M + tn - 1) / tn) < pairs) tn = 128;
   else if (0.966 * static_cast<double>(rounds(160)) < static_cast<double>(rounds(192))) tn = 160;
   GMaps gm;
-  bool ok = encode_2d(&gm.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.codes, a.d_i / 2, a.d_o, kKS / 2, kTO,
-                      CU_TENSOR_MAP_SWIZZLE_NONE) &&
-            encode_2d(&gm.scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.scales, a.d_i / 16, a.d_o, 16, kTO,
-                      CU_TENSOR_MAP_SWIZZLE_NONE) &&
-            encode_2d(&gm.hq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.hq, a.d_i, a.M, 64, tn / 2,
+  memset(&gm, 0, sizeof(gm));
+  bool ok = encode_2d(&gm.hq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.hq, in.d_i, in.M, 64, tn / 2,
                       CU_TENSOR_MAP_SWIZZLE_128B);
-  if (ok && lora)
-    ok = encode_2d(&gm.tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w.Tq, kLoraK, Mp, 64, tn / 2,
-                   CU_TENSOR_MAP_SWIZZLE_128B);
-  else
-    gm.tq = gm.hq;  // unused
+  for (int i = 0; i < n && ok; ++i) {
+    ok = encode_2d(&gm.codes[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, projs[i].codes, in.d_i / 2, projs[i].d_o, kKS / 2,
+                   kTO, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+         encode_2d(&gm.scales[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, projs[i].scales, in.d_i / 16, projs[i].d_o, 16,
+                   kTO, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (ok && r[i] > 0)
+      ok = encode_2d(&gm.tq[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w.m[i].Tq, kLoraK, Mp, 64, tn / 2,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+    else
+      gm.tq[i] = gm.hq;  // unused
+  }
   if (!ok) return cudaErrorInvalidValue;
-  const GPlan g = gplan(a.r, tn);
+  int rmax = 0;
+  for (int i = 0; i < n; ++i) rmax = r[i] > rmax ? r[i] : rmax;
+  const GPlan g = gplan(rmax, tn);
   GParams p{};
-  p.M = a.M;
-  p.d_i = a.d_i;
-  p.d_o = a.d_o;
-  p.r = a.r;
+  p.M = in.M;
+  p.d_i = in.d_i;
   p.n_ot = static_cast<int>(n_ot64);
-  p.n_tiles = static_cast<int>(p.n_ot * ((a.M + tn - 1) / tn));
+  p.n_tiles = static_cast<int>(p.n_ot * ((in.M + tn - 1) / tn));
   p.n_ks = n_ks;
   p.stages = g.stages;
-  p.s_g = a.s_g;
-  p.B = static_cast<const __nv_bfloat16*>(a.B);
+  p.n_g = n;
   p.rowscale = w.rowscale;
-  p.y = a.y;
-  p.y_f32 = a.y_f32 ? 1 : 0;
+  p.y_f32 = in.y_f32 ? 1 : 0;
   p.off_scales = g.off_scales;
   p.off_t = g.off_t;
   p.t_slot_bytes = g.t_slot_bytes;
   p.off_ctrl = g.off_ctrl;
+  for (int i = 0, ot0 = 0; i < n; ++i) {
+    p.g[i].d_o = projs[i].d_o;
+    p.g[i].r = r[i];
+    p.g[i].ot0 = ot0;
+    p.g[i].s_g = projs[i].s_g;
+    p.g[i].B = r[i] > 0 ? static_cast<const __nv_bfloat16*>(projs[i].B) : nullptr;
+    p.g[i].y = projs[i].y;
+    ot0 += static_cast<int>((projs[i].d_o + 2 * kTO - 1) / (2 * kTO));
+  }
   cudaLaunchAttribute gattrs[2];
   gattrs[0] = pdl[0];
   gattrs[1].id = cudaLaunchAttributeClusterDimension;
@@ -874,6 +950,12 @@ cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream) {
   if (tn == 128) return cudaLaunchKernelEx(&c, k_gemm_nvfp4<128>, gm, p);
   if (tn == 160) return cudaLaunchKernelEx(&c, k_gemm_nvfp4<160>, gm, p);
   return cudaLaunchKernelEx(&c, k_gemm_nvfp4<192>, gm, p);
+}
+
+cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream) {
+  const TcProj one{a.d_o, a.codes, a.scales, a.s_g, a.r > 0 ? a.A : nullptr, a.r > 0 ? a.B : nullptr, a.r, a.lambda,
+                   a.y, 0};
+  return launch_linear_prefill_group(a, &one, 1, stream);
 }
 
 #ifdef PL_TIMELINE

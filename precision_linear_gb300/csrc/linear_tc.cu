@@ -227,9 +227,7 @@ __global__ void __launch_bounds__(kActThreads, 2) k_act(const __nv_bfloat16* __r
                                                      const float* __restrict__ w_norm,
                                                      const float* __restrict__ z, int64_t z_ld, float eps,
                                                      __half* __restrict__ hq, float* __restrict__ rowscale,
-                                                     const __nv_bfloat16* __restrict__ A, int r,
-                                                     __half* __restrict__ A16, float* __restrict__ zero,
-                                                     int64_t n_zero, int n_row_ctas, int wpr) {
+                                                     const __grid_constant__ ActConv conv, int n_row_ctas, int wpr) {
   extern __shared__ float4 g4[];  // [d_i / 4]: w_norm + z of the whole row (1 without the norm)
   __shared__ float red_s[kActWarps], red_m[kActWarps];
   if (threadIdx.x == 0) {
@@ -239,29 +237,34 @@ __global__ void __launch_bounds__(kActThreads, 2) k_act(const __nv_bfloat16* __r
   pdl_wait();  // x may come from the preceding kernel, which may also still read the workspace
   if (threadIdx.x == 0) PL_TLP(1);
   if (static_cast<int>(blockIdx.x) >= n_row_ctas) {
-    const int64_t nslot = static_cast<int64_t>(r) * d_i / 8;
+    // the adapters to f16 (one segment per projection) and the counters to zero
     const int64_t stride = static_cast<int64_t>(gridDim.x - n_row_ctas) * kActThreads;
-    // kActUnroll slots per thread and round, every load of the round in flight before the stores
-    for (int64_t s0 = (blockIdx.x - n_row_ctas) * kActThreads + threadIdx.x; s0 < nslot; s0 += kActUnroll * stride) {
-      uint4 v[kActUnroll];
+    for (int sg = 0; sg < conv.n; ++sg) {
+      const __nv_bfloat16* A = static_cast<const __nv_bfloat16*>(conv.A[sg]);
+      __half* A16 = conv.A16[sg];
+      const int64_t nslot = static_cast<int64_t>(conv.r[sg]) * d_i / 8;
+      // kActUnroll slots per thread and round, every load of the round in flight before the stores
+      for (int64_t s0 = (blockIdx.x - n_row_ctas) * kActThreads + threadIdx.x; s0 < nslot; s0 += kActUnroll * stride) {
+        uint4 v[kActUnroll];
 #pragma unroll
-      for (int u = 0; u < kActUnroll; ++u) {
-        const int64_t sl = s0 + u * stride;
-        if (sl < nslot) v[u] = reinterpret_cast<const uint4*>(A)[sl];
-      }
+        for (int u = 0; u < kActUnroll; ++u) {
+          const int64_t sl = s0 + u * stride;
+          if (sl < nslot) v[u] = reinterpret_cast<const uint4*>(A)[sl];
+        }
 #pragma unroll
-      for (int u = 0; u < kActUnroll; ++u) {
-        const int64_t sl = s0 + u * stride;
-        if (sl < nslot)
-          reinterpret_cast<uint4*>(A16)[sl] =
-              make_uint4(f32x2_to_f16x2(bf16lo_to_f32(v[u].x), bf16hi_to_f32(v[u].x)),
-                         f32x2_to_f16x2(bf16lo_to_f32(v[u].y), bf16hi_to_f32(v[u].y)),
-                         f32x2_to_f16x2(bf16lo_to_f32(v[u].z), bf16hi_to_f32(v[u].z)),
-                         f32x2_to_f16x2(bf16lo_to_f32(v[u].w), bf16hi_to_f32(v[u].w)));
+        for (int u = 0; u < kActUnroll; ++u) {
+          const int64_t sl = s0 + u * stride;
+          if (sl < nslot)
+            reinterpret_cast<uint4*>(A16)[sl] =
+                make_uint4(f32x2_to_f16x2(bf16lo_to_f32(v[u].x), bf16hi_to_f32(v[u].x)),
+                           f32x2_to_f16x2(bf16lo_to_f32(v[u].y), bf16hi_to_f32(v[u].y)),
+                           f32x2_to_f16x2(bf16lo_to_f32(v[u].z), bf16hi_to_f32(v[u].z)),
+                           f32x2_to_f16x2(bf16lo_to_f32(v[u].w), bf16hi_to_f32(v[u].w)));
+        }
       }
+      for (int64_t sl = (blockIdx.x - n_row_ctas) * kActThreads + threadIdx.x; sl < conv.n_zero[sg] / 4; sl += stride)
+        reinterpret_cast<float4*>(conv.zero[sg])[sl] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    for (int64_t sl = (blockIdx.x - n_row_ctas) * kActThreads + threadIdx.x; sl < n_zero / 4; sl += stride)
-      reinterpret_cast<float4*>(zero)[sl] = make_float4(0.f, 0.f, 0.f, 0.f);
     return;
   }
   const bool norm = w_norm != nullptr, noise = !kRowZ && norm && z != nullptr;
@@ -1344,14 +1347,15 @@ cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   return launch_linear_tc_batch(a.d_i, a.eps, &set, 1, &pj, 1, a.y_f32, a.ws, stream);
 }
 
-cudaError_t launch_act_prologue(const LinearArgs& a, __half* hq, float* rowscale, __half* A16, float* zero,
-                                int64_t n_zero, cudaStream_t stream) {
+cudaError_t launch_act_prologue(const LinearArgs& a, __half* hq, float* rowscale, const ActConv& conv,
+                                cudaStream_t stream) {
   cudaError_t e = set_kernel_attributes();
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  const int64_t a_slots = static_cast<int64_t>(a.r) * a.d_i / 8 + n_zero / 4;
+  int64_t a_slots = 0;
+  for (int sg = 0; sg < conv.n; ++sg) a_slots += static_cast<int64_t>(conv.r[sg]) * a.d_i / 8 + conv.n_zero[sg] / 4;
   int nconv = static_cast<int>((a_slots + kActThreads * 4 - 1) / (kActThreads * 4));
   nconv = a_slots > 0 ? (nconv < 1 ? 1 : (nconv > 64 ? 64 : nconv)) : 0;
   // row CTAs, at most two per SM (each holds w_norm + z): a group of wpr warps per row,
@@ -1372,9 +1376,7 @@ cudaError_t launch_act_prologue(const LinearArgs& a, __half* hq, float* rowscale
   c.numAttrs = 1;
   auto* kern = (a.z != nullptr && a.z_ld != 0) ? k_act<true> : k_act<false>;
   return cudaLaunchKernelEx(&c, kern, static_cast<const __nv_bfloat16*>(a.x), a.M, a.d_i, a.w_norm, a.z, a.z_ld,
-                            a.eps, hq,
-                            rowscale, static_cast<const __nv_bfloat16*>(a.A), a.r, A16, zero, n_zero, n_row_ctas,
-                            wpr);
+                            a.eps, hq, rowscale, conv, n_row_ctas, wpr);
 }
 
 cudaError_t launch_wait_timeout_probe(cudaStream_t stream) {

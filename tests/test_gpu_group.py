@@ -102,10 +102,54 @@ def test_group_per_token_states(cuda_ok):
 
 
 def test_large_group_runs_projection_by_projection(cuda_ok):
-    """Five projections (more than one launch takes) and M > 64: one call per projection."""
+    """Five projections (more than one launch takes, at decode and at large M): one call per
+    projection."""
     wl = synthetic.WORKLOADS["layer_7b"]
     _group_check(wl, ["q", "k", "v", "k", "v"], 4)
-    _group_check(wl, ["k", "v"], 100)
+    _group_check(wl, ["k", "v", "k", "v", "k"], 100)
+
+
+@pytest.mark.parametrize("names,M", [(["q", "k", "v"], 300), (["gate", "up"], 130), (["k", "v"], 100)])
+def test_large_m_group(cuda_ok, names, M):
+    """M > 64: one row pass, one adapter down-projection per member and one contraction over
+    every member's weight tiles (ragged token tiles at M = 300 and 130)."""
+    assert pl.linear_path(M, 3584, 512, 32) == 3
+    _group_check(synthetic.WORKLOADS["layer_7b"], names, M)
+
+
+def test_large_m_group_mixed_ranks_no_norm_and_row_states(cuda_ok):
+    wl = synthetic.WORKLOADS["layer_7b"]
+    _group_check(wl, ["q", "k", "v"], 100, ranks=[0, 8, 32])
+    _group_check(wl, ["k", "v"], 77, norm=False)
+    M = 96
+    z_rows = (torch.randn(M, 3584, generator=torch.Generator().manual_seed(77)) * wl.sigma).to(DEV)
+    _group_check(wl, ["k", "v"], M, z_rows=z_rows)
+
+
+def test_prefill_qkv_group_m4096_sampled_rows(cuda_ok):
+    """The 7B q/k/v group at M = 4096: one full 128-token tile and a spread of other rows of
+    every member against the oracle."""
+    from oracle import linear as olin
+    from tests.gpu_cases import np32
+    wl = synthetic.WORKLOADS["prefill_7b"]
+    M = wl.Ms[0]
+    cases = _layer(wl, M)
+    names = ["q", "k", "v"]
+    c0 = cases["q"]
+    rows = np.unique(np.concatenate([np.arange(256, 384), np.random.default_rng(3).choice(M, 24, replace=False)]))
+    projs, encs = [], []
+    for n in names:
+        packed, sb, s_g = oracle_quantize_cached((wl.name, n, "m4096"), cases[n]["W"])
+        codes, scales, sg = to_dev_nvfp4(packed, sb, s_g)
+        projs.append(dict(codes=codes, scales=scales, s_g=sg, A=cases[n]["A"], B=cases[n]["B"], lam=wl.lam))
+        encs.append((packed, sb, s_g))
+    ys = pl.nvfp4_lora_linear_group(c0["x"], projs, c0["w_norm"], c0["z"], synthetic.EPS, out_dtype=torch.float32)
+    x = np32(c0["x"]).astype(np.float64)[rows]
+    sel = torch.from_numpy(rows).to(DEV)
+    for n, y, (packed, sb, s_g) in zip(names, ys, encs):
+        ref = olin.nvfp4_lora_linear(x, packed, sb, s_g, np32(cases[n]["A"]), np32(cases[n]["B"]), wl.lam,
+                                     np32(c0["w_norm"]), np32(c0["z"]), synthetic.EPS)
+        assert_linear_close(y[sel], ref, f"prefill group {n}")
 
 
 def test_group_repeatable_bitwise(cuda_ok):
