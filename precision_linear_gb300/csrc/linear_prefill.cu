@@ -90,10 +90,12 @@ constexpr int kMaxR = 32;
 constexpr int kLoraK = 64;  // K columns the LoRA step adds (r <= 32 of them nonzero)
 
 // One projection of a launch (a group shares the input): its pairs of weight tiles are
-// [ot0, ot0 + ceil(d_o / 256)) of the launch's n_ot.
+// [ot0, ot0 + n_ot) of the launch's; its tiles (n_ot pairs x the token tiles) are
+// [t0, t0 + n_ot x token tiles) of the launch's, member after member, so that one member's
+// weights stay in L2 across its token tiles.
 struct GMember {
   int64_t d_o;
-  int r, ot0;
+  int r, ot0, n_ot, t0;
   const float* s_g;
   const __nv_bfloat16* B;  // [d_o][r], as stored: the A operand of the LoRA step
   void* y;                 // [M][d_o]
@@ -113,13 +115,18 @@ struct GMaps {
   CUtensorMap codes[kMaxPrefillGroup], scales[kMaxPrefillGroup], tq[kMaxPrefillGroup];
 };
 
-// The member a pair of weight tiles belongs to: the last one whose first pair is <= ot.
-__device__ __forceinline__ int member_of(const GParams& p, int ot) {
+// Tile -> (member, token tile, the member's pair of weight tiles): members one after
+// another, within a member the weight pairs fastest (concurrent pairs share their token tile).
+struct TileAt {
+  int gi, mt, otl;
+};
+__device__ __forceinline__ TileAt tile_at(const GParams& p, int tile) {
   int gi = 0;
 #pragma unroll
   for (int q = 1; q < kMaxPrefillGroup; ++q)
-    if (q < p.n_g && ot >= p.g[q].ot0) gi = q;
-  return gi;
+    if (q < p.n_g && tile >= p.g[q].t0) gi = q;
+  const int local = tile - p.g[gi].t0;
+  return TileAt{gi, local / p.g[gi].n_ot, local % p.g[gi].n_ot};
 }
 
 struct GCtrl {
@@ -259,10 +266,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
       uint32_t grp = ~0u;  // scale groups loaded so far - 1
       int it = 0, t_issued = 0;
       for (int tile = pair; tile < p.n_tiles && ok; tile += npairs, ++it) {
-        const int mt = tile / p.n_ot, ot = tile % p.n_ot;
-        const int gi = member_of(p, ot);
+        const TileAt at = tile_at(p, tile);
+        const int gi = at.gi, mt = at.mt;
         const int n_steps = n_ks + (p.g[gi].r > 0 ? 1 : 0);  // K steps of this tile, the LoRA step last
-        const int32_t m0 = mt * TN, o0 = (ot - p.g[gi].ot0) * 2 * kTO + rank * kTO, mh = m0 + rank * kTH;
+        const int32_t m0 = mt * TN, o0 = at.otl * 2 * kTO + rank * kTO, mh = m0 + rank * kTH;
         {  // the row scales of this tile's tokens (all TN: this CTA's accumulator spans them)
           const int tb = it & 1;
           {
@@ -322,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
       int it = 0;
       for (int tile = pair; tile < p.n_tiles && ok; tile += npairs, ++it) {
         const int b = it & 1;
-        const int r_t = p.g[member_of(p, tile % p.n_ot)].r;  // this tile's adapter rank
+        const int r_t = p.g[tile_at(p, tile).gi].r;  // this tile's adapter rank
         const bool lora = r_t > 0;
         const int l_sub = (r_t + 15) / 16;  // the LoRA step's K sub-steps of 16
         {
@@ -387,12 +394,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
     uint32_t grp = ~0u;  // scale groups used so far - 1
     int it = 0;
     for (int tile = pair; tile < p.n_tiles && ok; tile += npairs, ++it) {
-      const int ot = tile % p.n_ot;
-      const GMember& G = p.g[member_of(p, ot)];
+      const TileAt at = tile_at(p, tile);
+      const GMember& G = p.g[at.gi];
       const int r = G.r;
       const bool lora = r > 0;
       const int n_steps = n_ks + (lora ? 1 : 0);
-      const int64_t o = static_cast<int64_t>(ot - G.ot0) * 2 * kTO + rank * kTO + row;
+      const int64_t o = static_cast<int64_t>(at.otl) * 2 * kTO + rank * kTO + row;
       // this thread's half of the LoRA step's 64 K columns of its row: B[o][32 g .. 32 g + 32),
       // bf16 as stored, zero beyond r (r <= 32: the g = 1 half is all zero)
       uint4 bq[4] = {};
@@ -469,12 +476,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
     bool ok = true;
     int it = 0;
     for (int tile = pair; tile < p.n_tiles && ok; tile += npairs, ++it) {
-      const int mt = tile / p.n_ot, ot = tile % p.n_ot;
+      const TileAt at = tile_at(p, tile);
+      const int mt = at.mt, gi = at.gi;
       const int b = it & 1;
-      const int gi = member_of(p, ot);
       const GMember& G = p.g[gi];
       const float s_g = C.s_g[gi];
-      const int64_t o = static_cast<int64_t>(ot - G.ot0) * 2 * kTO + rank * kTO + row;
+      const int64_t o = static_cast<int64_t>(at.otl) * 2 * kTO + rank * kTO + row;
       {
         PF_T0();
         ok = wait_p(smem_u32(&C.dfull[b]), (it >> 1) & 1, abort_flag) &&
@@ -925,10 +932,15 @@ cudaError_t launch_linear_prefill_group(const LinearArgs& in, const TcProj* proj
   p.off_t = g.off_t;
   p.t_slot_bytes = g.t_slot_bytes;
   p.off_ctrl = g.off_ctrl;
-  for (int i = 0, ot0 = 0; i < n; ++i) {
+  const int mtiles_g = static_cast<int>((in.M + tn - 1) / tn);
+  for (int i = 0, ot0 = 0, t0 = 0; i < n; ++i) {
+    const int n_ot_i = static_cast<int>((projs[i].d_o + 2 * kTO - 1) / (2 * kTO));
     p.g[i].d_o = projs[i].d_o;
     p.g[i].r = r[i];
     p.g[i].ot0 = ot0;
+    p.g[i].n_ot = n_ot_i;
+    p.g[i].t0 = t0;
+    t0 += n_ot_i * mtiles_g;
     p.g[i].s_g = projs[i].s_g;
     p.g[i].B = r[i] > 0 ? static_cast<const __nv_bfloat16*>(projs[i].B) : nullptr;
     p.g[i].y = projs[i].y;
