@@ -84,16 +84,17 @@ uint32_t tc_read_and_clear_status();
 cudaError_t launch_wait_timeout_probe(cudaStream_t stream);
 // The row prologue on its own: hq = f16(RMSNorm_AQN(x) / rowscale) [M][d_i], rowscale
 // [M] (powers of two), A16 = f16(A) [r][d_i], and n_zero zeros (a multiple of 4) at zero.
-// The adapters a row prologue converts to f16 (and the counters it zeroes), one segment per
-// projection of a large-M group.
+// The adapters a row prologue converts to f16, one segment per projection of a large-M
+// group, and the float ranges it zeroes (counters, padding rows of the f16 adapters).
 constexpr int kMaxActConv = 4;
 struct ActConv {
   const void* A[kMaxActConv];   // bf16 [r][d_i]
   __half* A16[kMaxActConv];     // f16 [r][d_i]
   int r[kMaxActConv];
-  float* zero[kMaxActConv];     // floats to zero (or null)
-  int64_t n_zero[kMaxActConv];  // a multiple of 4
   int n;
+  float* zero[kMaxActConv + 1];     // floats to zero
+  int64_t n_zero[kMaxActConv + 1];  // a multiple of 4
+  int n_zero_ranges;
 };
 cudaError_t launch_act_prologue(const LinearArgs& a, __half* hq, float* rowscale, const ActConv& conv,
                                 cudaStream_t stream);

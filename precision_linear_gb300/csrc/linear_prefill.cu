@@ -536,15 +536,21 @@ constexpr int kLdStages = 8;
 constexpr int kLdThreads = 6 * 32;  // TMA, MMA, 4 epilogue warps
 constexpr uint32_t kLdH = 128 * kKS * 2;  // 16 KB
 
-struct LParams {
-  int64_t M, d_i, Mp;
-  int r, R4, rb, n_ks, splits;
+// One adapter of a down-projection launch: its r rows of A16 (and columns of the MMA's N)
+// start at col0; the launch writes its Tq.
+struct LMember {
+  int r, col0;
   float lambda;
   const float* s_g;
-  float* t_part;           // [splits][Mp][R4]
   __nv_bfloat16* Tq;       // [Mp][64]: bf16(T), T = (lambda / s_g) A hq, zero beyond r
+};
+struct LParams {
+  int64_t M, d_i, Mp;
+  int rb, n_ks, splits, stages;  // rb: every member's rows, each rounded up to 16 (the MMA's N)
+  float* t_part;           // [splits][Mp][rb]
   int* counters;           // [token tiles]; zero on entry
-  int mtiles;
+  int mtiles, n_m;
+  LMember m[kMaxPrefillGroup];
 };
 struct LMaps {
   CUtensorMap hq, a16;
@@ -561,7 +567,8 @@ __global__ void __launch_bounds__(kLdThreads, 1) k_lora_down(const __grid_consta
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t abytes = static_cast<uint32_t>(p.rb) * kKS * 2;
   const uint32_t stage_bytes = kLdH + abytes;
-  LCtrl& C = *reinterpret_cast<LCtrl*>(smem + kLdStages * stage_bytes);
+  const int nst = p.stages;
+  LCtrl& C = *reinterpret_cast<LCtrl*>(smem + nst * stage_bytes);
   volatile int* abort_flag = &C.abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = smem_u32(smem);
@@ -570,7 +577,7 @@ __global__ void __launch_bounds__(kLdThreads, 1) k_lora_down(const __grid_consta
   const int32_t m0 = mtile * 128;
   if (threadIdx.x == 0) {
     pdl_launch_dependents();
-    for (int s = 0; s < kLdStages; ++s) {
+    for (int s = 0; s < nst; ++s) {
       mbar_init(smem_u32(&C.full[s]), 1);
       mbar_init(smem_u32(&C.empty[s]), 1);
     }
@@ -578,8 +585,9 @@ __global__ void __launch_bounds__(kLdThreads, 1) k_lora_down(const __grid_consta
     C.abort_flag = 0;
     fence_mbar_init();
   }
+  const uint32_t tcols = p.rb <= 32 ? 32u : (p.rb <= 64 ? 64u : 128u);
   if (warp == 1) {
-    tmem_alloc(smem_u32(&C.tmem_base), 32);
+    tmem_alloc(smem_u32(&C.tmem_base), tcols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -592,8 +600,8 @@ __global__ void __launch_bounds__(kLdThreads, 1) k_lora_down(const __grid_consta
       bool ok = true;
       int i = 0;
       for (int s = s0; s < s1 && ok; ++s, ++i) {
-        const int st = i % kLdStages;
-        if (i >= kLdStages) ok = wait_p(smem_u32(&C.empty[st]), ((i / kLdStages) - 1) & 1, abort_flag);
+        const int st = i % nst;
+        if (i >= nst) ok = wait_p(smem_u32(&C.empty[st]), ((i / nst) - 1) & 1, abort_flag);
         if (!ok) break;
         const uint32_t fb = smem_u32(&C.full[st]);
         mbar_arrive_expect_tx(fb, stage_bytes);
@@ -601,8 +609,7 @@ __global__ void __launch_bounds__(kLdThreads, 1) k_lora_down(const __grid_consta
         tma_load_2d(sbase + st * stage_bytes + kLdH, &maps.a16, s * kKS, 0, fb);
       }
       if (*abort_flag)
-        for (int d = i - kLdStages > 0 ? i - kLdStages : 0; d < i; ++d)
-          drain(smem_u32(&C.full[d % kLdStages]), (d / kLdStages) & 1);
+        for (int d = i - nst > 0 ? i - nst : 0; d < i; ++d) drain(smem_u32(&C.full[d % nst]), (d / nst) & 1);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -610,8 +617,8 @@ __global__ void __launch_bounds__(kLdThreads, 1) k_lora_down(const __grid_consta
       bool ok = true;
       int i = 0;
       for (int s = s0; s < s1 && ok; ++s, ++i) {
-        const int st = i % kLdStages;
-        ok = wait_p(smem_u32(&C.full[st]), (i / kLdStages) & 1, abort_flag);
+        const int st = i % nst;
+        ok = wait_p(smem_u32(&C.full[st]), (i / nst) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
         const uint64_t hd = smem_desc_sw128(sbase + st * stage_bytes, 1024);
@@ -627,30 +634,33 @@ __global__ void __launch_bounds__(kLdThreads, 1) k_lora_down(const __grid_consta
     const int64_t m = static_cast<int64_t>(m0) + quarter * 32 + lane;  // < Mp
     const bool ok = wait_p(smem_u32(&C.dfull), 0, abort_flag) && !*abort_flag && s1 > s0;
     tc_fence_after();
-    float* part = p.t_part + (static_cast<int64_t>(sp) * p.Mp + m) * p.R4;
+    float* part = p.t_part + (static_cast<int64_t>(sp) * p.Mp + m) * p.rb;
     uint32_t v[16];
     for (int jb = 0; jb < p.rb; jb += 16) {
       tmem_ld16(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + jb, v);
       tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (jb + j < p.R4) part[jb + j] = (ok && m < p.M) ? __uint_as_float(v[j]) : 0.f;
+      for (int j = 0; j < 16; ++j) part[jb + j] = (ok && m < p.M) ? __uint_as_float(v[j]) : 0.f;
     }
     __threadfence();
     named_bar(1, 128);
     if (threadIdx.x == 64) C.last = atomicAdd(&p.counters[mtile], 1) == p.splits - 1;
     named_bar(1, 128);
-    if (C.last) {  // every split of this token tile is in memory: add them up in split order
+    for (int mi = 0; C.last && mi < p.n_m; ++mi) {
+      // every split of this token tile is in memory: add member mi's columns up in split order
       __threadfence();
-      const float f = p.lambda / *p.s_g;
+      const LMember& L = p.m[mi];
+      const float f = L.lambda / *L.s_g;
+      const int R4 = (L.r + 3) / 4 * 4;
       float acc[kMaxR];
 #pragma unroll
       for (int j = 0; j < kMaxR; ++j) acc[j] = 0.f;
       for (int q = 0; q < p.splits; ++q) {  // all loads of one split issued together
-        const float4* src = reinterpret_cast<const float4*>(p.t_part + (static_cast<int64_t>(q) * p.Mp + m) * p.R4);
+        const float4* src =
+            reinterpret_cast<const float4*>(p.t_part + (static_cast<int64_t>(q) * p.Mp + m) * p.rb + L.col0);
         float4 v[kMaxR / 4];
 #pragma unroll
-        for (int j4 = 0; j4 < kMaxR / 4; ++j4) v[j4] = 4 * j4 < p.R4 ? __ldcg(src + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j4 = 0; j4 < kMaxR / 4; ++j4) v[j4] = 4 * j4 < R4 ? __ldcg(src + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int j4 = 0; j4 < kMaxR / 4; ++j4) {
           acc[4 * j4] += v[j4].x;
@@ -660,15 +670,15 @@ __global__ void __launch_bounds__(kLdThreads, 1) k_lora_down(const __grid_consta
         }
       }
       // the LoRA step's B operand row: 64 bf16, T in the first r, zero beyond
-      uint4* dst = reinterpret_cast<uint4*>(p.Tq + m * kLoraK);
+      uint4* dst = reinterpret_cast<uint4*>(L.Tq + m * kLoraK);
 #pragma unroll
       for (int q = 0; q < kLoraK / 8; ++q) {
         uint32_t w[4];
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
           const int j = 8 * q + 2 * h;
-          const float lo = j < p.r && j < kMaxR ? f * acc[j < kMaxR ? j : 0] : 0.f;
-          const float hi = j + 1 < p.r && j + 1 < kMaxR ? f * acc[j + 1 < kMaxR ? j + 1 : 0] : 0.f;
+          const float lo = j < L.r && j < kMaxR ? f * acc[j < kMaxR ? j : 0] : 0.f;
+          const float hi = j + 1 < L.r && j + 1 < kMaxR ? f * acc[j + 1 < kMaxR ? j + 1 : 0] : 0.f;
           w[h] = f32x2_to_bf16x2(lo, hi);
         }
         dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -679,7 +689,7 @@ __global__ void __launch_bounds__(kLdThreads, 1) k_lora_down(const __grid_consta
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 32);
+    tmem_dealloc(tmem, tcols);
   }
 }
 
@@ -715,22 +725,21 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void*
 // or 192 for the GEMM, 128 for the down-projection), so that whole tiles can be read and
 // written.
 int64_t m_pad(int64_t M) { return (M + 1919) / 1920 * 1920; }
-int r4(int r) { return r > 0 ? (r + 3) / 4 * 4 : 0; }
 
 constexpr int kMaxLdSplits = 8;
 
-// Workspace of one launch: the shared f16 rows and row scales, then per member the f16
-// adapter, the LoRA down-projection's split partials and counters, and Tq.
-struct PfMemberWs {
-  __half* A16;
-  float* t_part;
-  int* counters;          // [token tiles of the down-projection]
-  __nv_bfloat16* Tq;      // [Mp][64]: bf16(T), zero beyond r
-};
+// Workspace of one launch: the shared f16 rows and row scales; the f16 adapters of every
+// member with one, side by side (each member's rows rounded up to 16, the padding zero); the
+// down-projection's split partials and counters; per member its Tq.
+int r16(int r) { return (r + 15) / 16 * 16; }
+
 struct PfWs {
   __half* hq;
   float* rowscale;
-  PfMemberWs m[kMaxPrefillGroup];
+  __half* A16;            // [rb][d_i], rb = sum of the members' r16(r)
+  float* t_part;          // [kMaxLdSplits][Mp][rb]
+  int* counters;          // [token tiles of the down-projection]
+  __nv_bfloat16* Tq[kMaxPrefillGroup];  // [Mp][64]: bf16(T), zero beyond r
   size_t bytes;
 };
 
@@ -739,20 +748,23 @@ PfWs carve(void* ws, int64_t M, int64_t d_i, const int* r, int n) {
   const uintptr_t b = reinterpret_cast<uintptr_t>(ws);
   size_t off = 0;
   const int64_t Mp = m_pad(M);
+  int rb = 0;
+  for (int i = 0; i < n; ++i) rb += r16(r[i]);
   w.hq = reinterpret_cast<__half*>(b + off);
   off += align_up(static_cast<size_t>(M) * d_i * 2, 256);
   w.rowscale = reinterpret_cast<float*>(b + off);
   off += align_up(static_cast<size_t>(Mp) * 4, 256);
-  for (int i = 0; i < n; ++i) {
-    PfMemberWs& q = w.m[i];
-    if (r[i] == 0) continue;
-    q.A16 = reinterpret_cast<__half*>(b + off);
-    off += align_up(static_cast<size_t>(r[i]) * d_i * 2, 256);
-    q.t_part = reinterpret_cast<float*>(b + off);
-    off += align_up(static_cast<size_t>(kMaxLdSplits) * Mp * r4(r[i]) * 4, 256);
-    q.counters = reinterpret_cast<int*>(b + off);
+  if (rb > 0) {
+    w.A16 = reinterpret_cast<__half*>(b + off);
+    off += align_up(static_cast<size_t>(rb) * d_i * 2, 256);
+    w.t_part = reinterpret_cast<float*>(b + off);
+    off += align_up(static_cast<size_t>(kMaxLdSplits) * Mp * rb * 4, 256);
+    w.counters = reinterpret_cast<int*>(b + off);
     off += align_up(static_cast<size_t>((M + 127) / 128 + 6) * 4, 256);
-    q.Tq = reinterpret_cast<__nv_bfloat16*>(b + off);
+  }
+  for (int i = 0; i < n; ++i) {
+    if (r[i] == 0) continue;
+    w.Tq[i] = reinterpret_cast<__nv_bfloat16*>(b + off);
     off += align_up(static_cast<size_t>(Mp) * kLoraK * 2, 256);
   }
   w.bytes = off;
@@ -829,16 +841,28 @@ cudaError_t launch_linear_prefill_group(const LinearArgs& in, const TcProj* proj
   const int64_t Mp = m_pad(in.M);
   const int mtiles = static_cast<int>((in.M + 127) / 128);  // token tiles of the LoRA down-projection
 
-  // 1. one row pass for the group; every adapter to f16, every down-projection's counters zeroed
+  // 1. one row pass for the group; every adapter to f16 (side by side, padding rows zeroed),
+  //    the down-projection's counters zeroed
   ActConv conv{};
+  int rb = 0, col0[kMaxPrefillGroup] = {0};
+  for (int i = 0; i < n; ++i) {
+    col0[i] = rb;
+    rb += r16(r[i]);
+  }
+  if (rb > 0) {
+    conv.zero[conv.n_zero_ranges] = reinterpret_cast<float*>(w.counters);
+    conv.n_zero[conv.n_zero_ranges++] = (mtiles + 3) / 4 * 4;
+  }
   for (int i = 0; i < n; ++i) {
     if (r[i] == 0) continue;
     conv.A[conv.n] = projs[i].A;
-    conv.A16[conv.n] = w.m[i].A16;
+    conv.A16[conv.n] = w.A16 + static_cast<int64_t>(col0[i]) * in.d_i;
     conv.r[conv.n] = r[i];
-    conv.zero[conv.n] = reinterpret_cast<float*>(w.m[i].counters);
-    conv.n_zero[conv.n] = (mtiles + 3) / 4 * 4;
     ++conv.n;
+    if (r16(r[i]) > r[i]) {  // padding rows: (r16 - r) d_i halves = (r16 - r) d_i / 2 floats
+      conv.zero[conv.n_zero_ranges] = reinterpret_cast<float*>(w.A16 + static_cast<int64_t>(col0[i] + r[i]) * in.d_i);
+      conv.n_zero[conv.n_zero_ranges++] = static_cast<int64_t>(r16(r[i]) - r[i]) * in.d_i / 2;
+    }
   }
   e = launch_act_prologue(in, w.hq, w.rowscale, conv, stream);
   if (e != cudaSuccess) return e;
@@ -849,38 +873,39 @@ cudaError_t launch_linear_prefill_group(const LinearArgs& in, const TcProj* proj
   const int n_ks = static_cast<int>(in.d_i / kKS);
   const int sms = sm_count();
 
-  // 2. the LoRA down-projection of every member with an adapter: Tq = bf16((lambda / s_g) A hq)
-  for (int i = 0; i < n; ++i) {
-    if (r[i] == 0) continue;
+  // 2. the adapters' down-projection, every member at once (the MMA's N = rb):
+  //    Tq_i = bf16((lambda_i / s_g_i) A_i hq)
+  if (rb > 0) {
     LMaps lm;
-    const int rb = (r[i] + 15) / 16 * 16;
     bool ok = encode_2d(&lm.hq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.hq, in.d_i, in.M, 64, 128,
                         CU_TENSOR_MAP_SWIZZLE_128B) &&
-              encode_2d(&lm.a16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.m[i].A16, in.d_i, r[i], 64, rb,
+              encode_2d(&lm.a16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.A16, in.d_i, rb, 64, rb,
                         CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return cudaErrorInvalidValue;
     LParams lp{};
     lp.M = in.M;
     lp.d_i = in.d_i;
     lp.Mp = Mp;
-    lp.r = r[i];
-    lp.R4 = r4(r[i]);
     lp.rb = rb;
     lp.n_ks = n_ks;
     int splits = sms / mtiles;  // one wave: every split of every token tile resident at once
     splits = splits > kMaxLdSplits ? kMaxLdSplits : splits;
     splits = splits > n_ks ? n_ks : (splits < 1 ? 1 : splits);  // every split has at least one K step
     lp.splits = splits;
-    lp.lambda = projs[i].lambda;
-    lp.s_g = projs[i].s_g;
-    lp.t_part = w.m[i].t_part;
-    lp.Tq = w.m[i].Tq;
-    lp.counters = w.m[i].counters;
+    const size_t stage_bytes = kLdH + static_cast<size_t>(rb) * kKS * 2;
+    int st = static_cast<int>((227 * 1024 - sizeof(LCtrl) - 1024) / stage_bytes);
+    lp.stages = st > kLdStages ? kLdStages : st;
+    lp.t_part = w.t_part;
+    lp.counters = w.counters;
     lp.mtiles = mtiles;
+    for (int i = 0; i < n; ++i) {
+      if (r[i] == 0) continue;
+      lp.m[lp.n_m++] = LMember{r[i], col0[i], projs[i].lambda, projs[i].s_g, w.Tq[i]};
+    }
     cudaLaunchConfig_t c{};
     c.gridDim = dim3(static_cast<unsigned>(mtiles * splits));
     c.blockDim = dim3(kLdThreads);
-    c.dynamicSmemBytes = kLdStages * (kLdH + static_cast<size_t>(rb) * kKS * 2) + sizeof(LCtrl) + 1024;
+    c.dynamicSmemBytes = lp.stages * stage_bytes + sizeof(LCtrl) + 1024;
     c.stream = stream;
     c.attrs = pdl;
     c.numAttrs = 1;
@@ -909,7 +934,7 @@ cudaError_t launch_linear_prefill_group(const LinearArgs& in, const TcProj* proj
          encode_2d(&gm.scales[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, projs[i].scales, in.d_i / 16, projs[i].d_o, 16,
                    kTO, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (ok && r[i] > 0)
-      ok = encode_2d(&gm.tq[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w.m[i].Tq, kLoraK, Mp, 64, tn / 2,
+      ok = encode_2d(&gm.tq[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w.Tq[i], kLoraK, Mp, 64, tn / 2,
                      CU_TENSOR_MAP_SWIZZLE_128B);
     else
       gm.tq[i] = gm.hq;  // unused

@@ -239,6 +239,9 @@ __global__ void __launch_bounds__(kActThreads, 2) k_act(const __nv_bfloat16* __r
   if (static_cast<int>(blockIdx.x) >= n_row_ctas) {
     // the adapters to f16 (one segment per projection) and the counters to zero
     const int64_t stride = static_cast<int64_t>(gridDim.x - n_row_ctas) * kActThreads;
+    for (int zr = 0; zr < conv.n_zero_ranges; ++zr)
+      for (int64_t sl = (blockIdx.x - n_row_ctas) * kActThreads + threadIdx.x; sl < conv.n_zero[zr] / 4; sl += stride)
+        reinterpret_cast<float4*>(conv.zero[zr])[sl] = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int sg = 0; sg < conv.n; ++sg) {
       const __nv_bfloat16* A = static_cast<const __nv_bfloat16*>(conv.A[sg]);
       __half* A16 = conv.A16[sg];
@@ -262,8 +265,6 @@ __global__ void __launch_bounds__(kActThreads, 2) k_act(const __nv_bfloat16* __r
                            f32x2_to_f16x2(bf16lo_to_f32(v[u].w), bf16hi_to_f32(v[u].w)));
         }
       }
-      for (int64_t sl = (blockIdx.x - n_row_ctas) * kActThreads + threadIdx.x; sl < conv.n_zero[sg] / 4; sl += stride)
-        reinterpret_cast<float4*>(conv.zero[sg])[sl] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     return;
   }
@@ -1355,7 +1356,8 @@ cudaError_t launch_act_prologue(const LinearArgs& a, __half* hq, float* rowscale
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   int64_t a_slots = 0;
-  for (int sg = 0; sg < conv.n; ++sg) a_slots += static_cast<int64_t>(conv.r[sg]) * a.d_i / 8 + conv.n_zero[sg] / 4;
+  for (int sg = 0; sg < conv.n; ++sg) a_slots += static_cast<int64_t>(conv.r[sg]) * a.d_i / 8;
+  for (int zr = 0; zr < conv.n_zero_ranges; ++zr) a_slots += conv.n_zero[zr] / 4;
   int nconv = static_cast<int>((a_slots + kActThreads * 4 - 1) / (kActThreads * 4));
   nconv = a_slots > 0 ? (nconv < 1 ? 1 : (nconv > 64 ? 64 : nconv)) : 0;
   // row CTAs, at most two per SM (each holds w_norm + z): a group of wpr warps per row,
