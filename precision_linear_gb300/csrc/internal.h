@@ -96,8 +96,10 @@ struct ActConv {
   int64_t n_zero[kMaxActConv + 1];  // a multiple of 4
   int n_zero_ranges;
 };
+// The row prologue of the large-M paths: hq = f16(h / c_m) and c_m per row, the adapters of
+// `conv`; with qx / s_x also the W8A8 form's E4M3 codes and per-row scale of h.
 cudaError_t launch_act_prologue(const LinearArgs& a, __half* hq, float* rowscale, const ActConv& conv,
-                                cudaStream_t stream);
+                                cudaStream_t stream, uint8_t* qx = nullptr, float* s_x = nullptr);
 
 // ---- linear_fused.cu (tcgen05, one kernel; M <= 64 and at most 3 K chunks of 256 per CTA)
 bool fused_supported(int64_t M, int64_t d_i, int64_t d_o, int r);
@@ -114,6 +116,13 @@ cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream);
 // are those of the group entry (TcProj::set unused).
 constexpr int kMaxPrefillGroup = 4;
 bool prefill_group_supported(int64_t M, int64_t d_i, const TcProj* projs, int n);
+// The adapter's down-projection of the W8A8 form at large M: t[m][j] = c_m (A16 hq)[m][j] in
+// FP32 from the row prologue's f16 rows, with A16 [r16(r)][d_i] (padding rows zero) and the
+// counters [ceil(M / 128)] zeroed beforehand; t_part takes lora_down_t_scratch_bytes.
+size_t lora_down_t_scratch_bytes(int64_t M, int r);
+cudaError_t launch_lora_down_t(const __half* hq, int64_t M, int64_t d_i, const __half* A16, int r,
+                               const float* rowscale, float* t, int t_ld, float* t_part, int* counters,
+                               cudaStream_t stream);
 size_t prefill_group_workspace_bytes(int64_t M, int64_t d_i, const TcProj* projs, int n);
 cudaError_t launch_linear_prefill_group(const LinearArgs& in, const TcProj* projs, int n, cudaStream_t stream);
 uint32_t prefill_read_and_clear_status();

@@ -543,9 +543,12 @@ struct LMember {
   float lambda;
   const float* s_g;
   __nv_bfloat16* Tq;       // [Mp][64]: bf16(T), T = (lambda / s_g) A hq, zero beyond r
+  float* t;                // or, when not null, t[m][j] = c_m (A hq)[m][j] = (A h)[m][j] in FP32
+  int t_ld;
 };
 struct LParams {
   int64_t M, d_i, Mp;
+  const float* rowscale;   // [M]: c_m (read in the t form only)
   int rb, n_ks, splits, stages;  // rb: every member's rows, each rounded up to 16 (the MMA's N)
   float* t_part;           // [splits][Mp][rb]
   int* counters;           // [token tiles]; zero on entry
@@ -650,7 +653,7 @@ __global__ void __launch_bounds__(kLdThreads, 1) k_lora_down(const __grid_consta
       // every split of this token tile is in memory: add member mi's columns up in split order
       __threadfence();
       const LMember& L = p.m[mi];
-      const float f = L.lambda / *L.s_g;
+      const float f = L.t != nullptr ? 1.f : L.lambda / *L.s_g;  // the t form has no s_g
       const int R4 = (L.r + 3) / 4 * 4;
       float acc[kMaxR];
 #pragma unroll
@@ -668,6 +671,15 @@ __global__ void __launch_bounds__(kLdThreads, 1) k_lora_down(const __grid_consta
           acc[4 * j4 + 2] += v[j4].z;
           acc[4 * j4 + 3] += v[j4].w;
         }
+      }
+      if (L.t != nullptr) {  // FP32 t = c_m A hq (the W8A8 form's adapter input)
+        if (m < p.M) {
+          const float c = p.rowscale[m];
+#pragma unroll
+          for (int j = 0; j < kMaxR; ++j)
+            if (j < L.r) L.t[m * L.t_ld + j] = c * acc[j];
+        }
+        continue;
       }
       // the LoRA step's B operand row: 64 bf16, T in the first r, zero beyond
       uint4* dst = reinterpret_cast<uint4*>(L.Tq + m * kLoraK);
@@ -900,7 +912,7 @@ cudaError_t launch_linear_prefill_group(const LinearArgs& in, const TcProj* proj
     lp.mtiles = mtiles;
     for (int i = 0; i < n; ++i) {
       if (r[i] == 0) continue;
-      lp.m[lp.n_m++] = LMember{r[i], col0[i], projs[i].lambda, projs[i].s_g, w.Tq[i]};
+      lp.m[lp.n_m++] = LMember{r[i], col0[i], projs[i].lambda, projs[i].s_g, w.Tq[i], nullptr, 0};
     }
     cudaLaunchConfig_t c{};
     c.gridDim = dim3(static_cast<unsigned>(mtiles * splits));
@@ -987,6 +999,54 @@ cudaError_t launch_linear_prefill_group(const LinearArgs& in, const TcProj* proj
   if (tn == 128) return cudaLaunchKernelEx(&c, k_gemm_nvfp4<128>, gm, p);
   if (tn == 160) return cudaLaunchKernelEx(&c, k_gemm_nvfp4<160>, gm, p);
   return cudaLaunchKernelEx(&c, k_gemm_nvfp4<192>, gm, p);
+}
+
+size_t lora_down_t_scratch_bytes(int64_t M, int r) {
+  const int64_t Mp = (M + 127) / 128 * 128;
+  return align_up(static_cast<size_t>(kMaxLdSplits) * Mp * r16(r) * 4, 256);
+}
+
+cudaError_t launch_lora_down_t(const __half* hq, int64_t M, int64_t d_i, const __half* A16, int r,
+                               const float* rowscale, float* t, int t_ld, float* t_part, int* counters,
+                               cudaStream_t stream) {
+  cudaError_t e = set_attributes();
+  if (e != cudaSuccess) return e;
+  const int rb = r16(r);
+  const int mtiles = static_cast<int>((M + 127) / 128);
+  const int n_ks = static_cast<int>(d_i / kKS);
+  LMaps lm;
+  if (!encode_2d(&lm.hq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, hq, d_i, M, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&lm.a16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A16, d_i, rb, 64, rb, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  LParams lp{};
+  lp.M = M;
+  lp.d_i = d_i;
+  lp.Mp = (M + 127) / 128 * 128;
+  lp.rowscale = rowscale;
+  lp.rb = rb;
+  lp.n_ks = n_ks;
+  int splits = sm_count() / mtiles;
+  splits = splits > kMaxLdSplits ? kMaxLdSplits : splits;
+  lp.splits = splits > n_ks ? n_ks : (splits < 1 ? 1 : splits);
+  const size_t stage_bytes = kLdH + static_cast<size_t>(rb) * kKS * 2;
+  const int st = static_cast<int>((227 * 1024 - sizeof(LCtrl) - 1024) / stage_bytes);
+  lp.stages = st > kLdStages ? kLdStages : st;
+  lp.t_part = t_part;
+  lp.counters = counters;
+  lp.mtiles = mtiles;
+  lp.n_m = 1;
+  lp.m[0] = LMember{r, 0, 0.f, nullptr, nullptr, t, t_ld};
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t c{};
+  c.gridDim = dim3(static_cast<unsigned>(mtiles * lp.splits));
+  c.blockDim = dim3(kLdThreads);
+  c.dynamicSmemBytes = lp.stages * stage_bytes + sizeof(LCtrl) + 1024;
+  c.stream = stream;
+  c.attrs = pdl;
+  c.numAttrs = 1;
+  return cudaLaunchKernelEx(&c, k_lora_down, lm, lp);
 }
 
 cudaError_t launch_linear_prefill(const LinearArgs& a, cudaStream_t stream) {

@@ -227,6 +227,7 @@ __global__ void __launch_bounds__(kActThreads, 2) k_act(const __nv_bfloat16* __r
                                                      const float* __restrict__ w_norm,
                                                      const float* __restrict__ z, int64_t z_ld, float eps,
                                                      __half* __restrict__ hq, float* __restrict__ rowscale,
+                                                     uint8_t* __restrict__ qx, float* __restrict__ s_x,
                                                      const __grid_constant__ ActConv conv, int n_row_ctas, int wpr) {
   extern __shared__ float4 g4[];  // [d_i / 4]: w_norm + z of the whole row (1 without the norm)
   __shared__ float red_s[kActWarps], red_m[kActWarps];
@@ -364,6 +365,40 @@ __global__ void __launch_bounds__(kActThreads, 2) k_act(const __nv_bfloat16* __r
     e = e < -100 ? -100 : (e > 100 ? 100 : e);
     const float f = inv * ldexpf(1.0f, -e);
     if (gt == 0) rowscale[m] = ldexpf(1.0f, e);
+    if (qx != nullptr) {
+      // the W8A8 form's activations, as the cluster prologue computes them: s_x = max |h| / 448,
+      // q_x = E4M3(h / s_x) (round to nearest even, saturating, +0 for values rounding to zero)
+      const float sx = hmax > 0.f ? __fdiv_rn(hmax, 448.0f) : 1.0f;
+      if (gt == 0) s_x[m] = sx;
+      uint2* qr = reinterpret_cast<uint2*>(qx + m * d_i);
+#pragma unroll
+      for (int i = 0; i < kActPieces; ++i) {
+        const int64_t q = gt + static_cast<int64_t>(i) * gstride;
+        if (q < nv8) {
+          const uint4 v = xv[i];
+          float g8[8];
+          gpiece(q, g8);
+          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+          uint32_t c[2];
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t c4 = 0;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const uint32_t w = w4[2 * hh + j];
+              const float h0 = bf16lo_to_f32(w) * g8[4 * hh + 2 * j] * inv;
+              const float h1 = bf16hi_to_f32(w) * g8[4 * hh + 2 * j + 1] * inv;
+              uint32_t c2 = cvt_e4m3x2(__fdiv_rn(h1, sx), __fdiv_rn(h0, sx));
+              if ((c2 & 0x7Fu) == 0) c2 &= 0xFF00u;
+              if ((c2 & 0x7F00u) == 0) c2 &= 0x00FFu;
+              c4 |= c2 << (16 * j);
+            }
+            c[hh] = c4;
+          }
+          qr[q] = make_uint2(c[0], c[1]);
+        }
+      }
+    }
     uint4* hr = reinterpret_cast<uint4*>(hq + m * d_i);
 #pragma unroll
     for (int i = 0; i < kActPieces; ++i) {
@@ -1349,7 +1384,7 @@ cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_act_prologue(const LinearArgs& a, __half* hq, float* rowscale, const ActConv& conv,
-                                cudaStream_t stream) {
+                                cudaStream_t stream, uint8_t* qx, float* s_x) {
   cudaError_t e = set_kernel_attributes();
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
@@ -1378,7 +1413,7 @@ cudaError_t launch_act_prologue(const LinearArgs& a, __half* hq, float* rowscale
   c.numAttrs = 1;
   auto* kern = (a.z != nullptr && a.z_ld != 0) ? k_act<true> : k_act<false>;
   return cudaLaunchKernelEx(&c, kern, static_cast<const __nv_bfloat16*>(a.x), a.M, a.d_i, a.w_norm, a.z, a.z_ld,
-                            a.eps, hq, rowscale, conv, n_row_ctas, wpr);
+                            a.eps, hq, rowscale, qx, s_x, conv, n_row_ctas, wpr);
 }
 
 cudaError_t launch_wait_timeout_probe(cudaStream_t stream) {

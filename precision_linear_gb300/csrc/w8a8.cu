@@ -13,7 +13,7 @@
 //   E4M3(fp32(w / s_w)), round to nearest even, saturating, +0 for values rounding to zero.
 // The activations come from the cluster prologue of the tensor-core decode path in its FP8
 // mode (linear_tc.cu): q_x, s_x and t = A h, FP32.
-// k_w8_gemm (a cluster of S CTAs per 128 weight rows x N tokens; CTA s takes the s-th slice
+// k_w8_gemm (decode, M <= 64; a cluster of S CTAs per 128 weight rows x N tokens; CTA s takes the s-th slice
 //   of K in chunks of 128):
 //   * warp 0 TMA-loads per chunk the weight codes (128 rows x 128 B) and the activation codes
 //     (N rows x 128 B), both with the 128-byte swizzle: they are the MMA operands as stored;
@@ -24,6 +24,8 @@
 //   * warps 2..5 build A' and B' in shared memory while the main loop runs, then read the
 //     accumulator, scale it by s_x s_w and write y (after summing the S partials of their
 //     share of the rows over DSMEM, in split order, when K is split).
+// k_w8_gemm_p (M > 64): the same arithmetic, persistent over tiles of 128 weight rows x 256
+//   tokens with two accumulators (see its comment below).
 // Every wait is bounded (200 ms); a wait that gives up sets the status word, the CTA drains
 // its copies and MMAs, frees its tensor memory and returns.
 #include <cudaTypedefs.h>
@@ -47,11 +49,10 @@ constexpr int kEpiThreads = 128;
 constexpr int kMaxSplit = 8;
 constexpr int kMaxR = 64;
 constexpr int kLoraK = 64;                  // adapter K columns (zeros past r)
-constexpr int kMaxNTile = 128;              // tokens per tile
 
 struct W8Params {
   int64_t M, d_i, d_o;
-  int N, otiles, splits, kc, stages;
+  int N, otiles, splits, kc, stages, n_tiles, mtiles;
   uint32_t stage_bytes, off_la, off_lb, off_ctrl;
   const float* s_w;   // [d_o]
   const float* s_x;   // [M]
@@ -353,6 +354,215 @@ __global__ void __launch_bounds__(kThreads, 1) k_w8_gemm(const __grid_constant__
   }
 }
 
+// ------------------------------------------------------------------ GEMM, large M
+// k_w8_gemm_p: persistent, one CTA per SM over tiles of 128 weight rows x kPN tokens (the
+// token tiles fastest, so that concurrent CTAs share their weight tile in L2 and the weights
+// are read from DRAM about once; the activations, 1 byte per element, stay in L2); two
+// accumulators of kPN columns, so that a tile's epilogue runs under the next tile's MMAs.
+//   * warp 0 TMA-loads per chunk of 128 K the weight codes (16 KB) and the activation codes
+//     (kPN rows, 32 KB) into a ring of kPStages stages;
+//   * warp 1: one thread issues 4 MMAs per chunk (E4M3 x E4M3, K = 32, M = 128, N = kPN),
+//     then the adapter's K steps (bf16 A' = B / s_w and B' = lambda t / s_x, as in
+//     k_w8_gemm), and commits the accumulator;
+//   * warps 2..5 write y = s_x s_w D of a finished tile, free its accumulator, then build the
+//     next tile's adapter operands (the previous tile's adapter step has completed by then).
+constexpr int kPN = 256;
+constexpr int kPStages = 3;
+constexpr uint32_t kPStageBytes = kWBytes + kPN * kChunk;  // 48 KB
+
+struct W8PCtrl {
+  uint64_t full[kPStages], empty[kPStages];
+  uint64_t lora_ready, d_full[2], d_empty[2], mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__global__ void __launch_bounds__(kThreads, 1) k_w8_gemm_p(const __grid_constant__ W8Maps maps,
+                                                           const __grid_constant__ W8Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  W8PCtrl& C = *reinterpret_cast<W8PCtrl*>(smem + p.off_ctrl);
+  volatile int* abort_flag = &C.abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool lora = p.r > 0;
+  const int kc = p.kc;
+
+  if (threadIdx.x == 0) {
+    pdl_launch_dependents();
+    for (int s = 0; s < kPStages; ++s) {
+      mbar_init(smem_u32(&C.full[s]), 1);
+      mbar_init(smem_u32(&C.empty[s]), 1);
+    }
+    mbar_init(smem_u32(&C.lora_ready), kEpiThreads / 32);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&C.d_full[b]), 1);
+      mbar_init(smem_u32(&C.d_empty[b]), kEpiThreads / 32);
+    }
+    mbar_init(smem_u32(&C.mma_done), 1);
+    C.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&C.tmem_base), 2 * kPN);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = C.tmem_base;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      pdl_wait();  // the activation codes come from the prologue
+      bool ok = true;
+      int64_t gs = 0;
+      for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x) {
+        const int32_t row0 = (tile / p.mtiles) * kTileO, tok0 = (tile % p.mtiles) * kPN;
+        for (int c = 0; c < kc && ok; ++c, ++gs) {
+          const int s = static_cast<int>(gs % kPStages);
+          if (gs >= kPStages) ok = wait8(smem_u32(&C.empty[s]), static_cast<uint32_t>((gs / kPStages) - 1) & 1, abort_flag);
+          if (!ok) break;
+          const uint32_t fb = smem_u32(&C.full[s]);
+          mbar_arrive_expect_tx(fb, kPStageBytes);
+          tma_load_2d_hint(smem_u32(smem + s * kPStageBytes), &maps.w, c * kChunk, row0, fb, pol_w);
+          tma_load_2d(smem_u32(smem + s * kPStageBytes + kWBytes), &maps.x, c * kChunk, tok0, fb);
+        }
+      }
+      if (*abort_flag)
+        for (int64_t d = gs - kPStages > 0 ? gs - kPStages : 0; d < gs; ++d)
+          drain(smem_u32(&C.full[d % kPStages]), static_cast<uint32_t>(d / kPStages) & 1);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(kTileO, kPN, 0);    // E4M3 x E4M3 shares the f16 field codes (0)
+      const uint32_t idesc_b = idesc_f16(kTileO, kPN, 1);  // the adapter step: bf16
+      const int ksteps = (p.r + 15) / 16;
+      const uint32_t la = smem_u32(smem + p.off_la), lb = smem_u32(smem + p.off_lb);
+      bool ok = true;
+      int64_t gs = 0;
+      int it = 0;
+      for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x, ++it) {
+        const int b = it & 1;
+        if (it >= 2) ok = wait8(smem_u32(&C.d_empty[b]), ((it >> 1) - 1) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(kPN * b);
+        for (int c = 0; c < kc && ok; ++c, ++gs) {
+          const int s = static_cast<int>(gs % kPStages);
+          ok = wait8(smem_u32(&C.full[s]), static_cast<uint32_t>(gs / kPStages) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t wa = smem_u32(smem + s * kPStageBytes), xa = wa + kWBytes;
+#pragma unroll
+          for (int k = 0; k < kChunk / 32; ++k)
+            mma_f8(d, smem_desc_sw128(wa + 32 * k, 1024), smem_desc_sw128(xa + 32 * k, 1024), idesc,
+                   (c > 0 || k > 0) ? 1u : 0u);
+          tc_commit(smem_u32(&C.empty[s]));
+        }
+        if (ok && lora) {
+          ok = wait8(smem_u32(&C.lora_ready), it & 1, abort_flag);
+          if (ok) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int k = 0; k < ksteps; ++k)
+              mma_ss(d, smem_desc_sw128(la + 32 * k, 1024), smem_desc_sw128(lb + 32 * k, 1024), idesc_b, 1u);
+          }
+        }
+        tc_commit(smem_u32(&C.d_full[b]));  // also reached on abort: tracks every MMA issued
+      }
+      tc_commit(smem_u32(&C.mma_done));
+      drain(smem_u32(&C.mma_done), 0);  // tensor memory is freed only after the last MMA
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue, adapter operands
+    const int et = threadIdx.x - 64;       // 0 .. 127
+    const int quarter = warp & 3;          // tensor-memory lane quarter of this warp
+    const int row = quarter * 32 + lane;   // weight row within the tile
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    pdl_wait();  // t and s_x come from the prologue
+    // A' [128][64] = B[o, :] / s_w[o] and B' [kPN][64] = lambda t[m, :] / s_x[m] of a tile
+    // (bf16, zeros past r, d_o and M; K-major 128-byte swizzled rows), then the arrival
+    auto build_lora = [&](int tile) {
+      const int64_t o = static_cast<int64_t>(tile / p.mtiles) * kTileO + row;
+      const int64_t tok0 = static_cast<int64_t>(tile % p.mtiles) * kPN;
+      const float sw = o < p.d_o ? p.s_w[o] : 1.f;
+      uint8_t* la = smem + p.off_la + row * 128;
+#pragma unroll
+      for (int j8 = 0; j8 < kLoraK / 8; ++j8) {
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int j = 8 * j8 + i;
+          v[i] = (o < p.d_o && j < p.r) ? __bfloat162float(p.B[o * p.r + j]) / sw : 0.f;
+        }
+        *reinterpret_cast<uint4*>(la + ((j8 ^ (row & 7)) << 4)) =
+            make_uint4(f32x2_to_bf16x2(v[0], v[1]), f32x2_to_bf16x2(v[2], v[3]), f32x2_to_bf16x2(v[4], v[5]),
+                       f32x2_to_bf16x2(v[6], v[7]));
+      }
+      for (int n = et; n < kPN; n += kEpiThreads) {
+        const int64_t m = tok0 + n;
+        const float f = m < p.M ? __fdiv_rn(p.lambda, p.s_x[m]) : 0.f;
+        uint8_t* lb = smem + p.off_lb + n * 128;
+#pragma unroll
+        for (int j8 = 0; j8 < kLoraK / 8; ++j8) {
+          float v[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int j = 8 * j8 + i;
+            v[i] = (m < p.M && j < p.r) ? p.t[m * p.t_ld + j] * f : 0.f;
+          }
+          *reinterpret_cast<uint4*>(lb + ((j8 ^ (n & 7)) << 4)) =
+              make_uint4(f32x2_to_bf16x2(v[0], v[1]), f32x2_to_bf16x2(v[2], v[3]), f32x2_to_bf16x2(v[4], v[5]),
+                         f32x2_to_bf16x2(v[6], v[7]));
+        }
+      }
+      fence_proxy_async_smem();  // read by the tensor cores
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&C.lora_ready));
+    };
+    bool ok = true;
+    int it = 0;
+    if (lora && static_cast<int>(blockIdx.x) < p.n_tiles) build_lora(blockIdx.x);
+    for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x, ++it) {
+      const int b = it & 1;
+      ok = wait8(smem_u32(&C.d_full[b]), (it >> 1) & 1, abort_flag);
+      ok = __all_sync(0xFFFFFFFFu, ok && !*abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      const int64_t o = static_cast<int64_t>(tile / p.mtiles) * kTileO + row;
+      const int64_t tok0 = static_cast<int64_t>(tile % p.mtiles) * kPN;
+      const float sw = o < p.d_o ? p.s_w[o] : 0.f;
+      for (int n0 = 0; n0 < kPN; n0 += 16) {
+        uint32_t dv[16];
+        tmem_ld16(tmem + lane_addr + static_cast<uint32_t>(kPN * b + n0), dv);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int64_t m = tok0 + n0 + i;
+          if (m < p.M && o < p.d_o) {
+            const float v = p.s_x[m] * sw * __uint_as_float(dv[i]);
+            if (p.y_f32) static_cast<float*>(p.y)[m * p.d_o + o] = v;
+            else static_cast<__nv_bfloat16*>(p.y)[m * p.d_o + o] = __float2bfloat16_rn(v);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&C.d_empty[b]));
+      if (lora && tile + static_cast<int>(gridDim.x) < p.n_tiles) build_lora(tile + gridDim.x);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 2 * kPN);
+  }
+}
+
 // ------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -382,11 +592,19 @@ bool encode_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Workspace: the E4M3 activations, s_x and t = A h; at large M also the row prologue's f16
+// rows and row scales, the f16 adapter (rows rounded up to 16, padding zero), the adapter
+// down-projection's split partials and counters.
 struct W8Ws {
   uint8_t* qx;
   float* s_x;
   float* t;
   int t_ld;
+  __half* hq;
+  float* rowscale;
+  __half* A16;
+  float* t_part;
+  int* counters;
   size_t bytes;
 };
 
@@ -401,6 +619,21 @@ W8Ws carve_w8(void* ws, int64_t M, int64_t d_i, int r) {
   w.t_ld = r > 0 ? (r + 3) / 4 * 4 : 4;
   w.t = reinterpret_cast<float*>(b + off);
   off += align_up(static_cast<size_t>(M) * w.t_ld * 4, 256);
+  if (M > 64 && r <= 32) {
+    w.hq = reinterpret_cast<__half*>(b + off);
+    off += align_up(static_cast<size_t>(M) * d_i * 2, 256);
+    w.rowscale = reinterpret_cast<float*>(b + off);
+    off += align_up(static_cast<size_t>(M) * 4, 256);
+    if (r > 0) {
+      const int r16 = (r + 15) / 16 * 16;
+      w.A16 = reinterpret_cast<__half*>(b + off);
+      off += align_up(static_cast<size_t>(r16) * d_i * 2, 256);
+      w.t_part = reinterpret_cast<float*>(b + off);
+      off += lora_down_t_scratch_bytes(M, r);
+      w.counters = reinterpret_cast<int*>(b + off);
+      off += align_up(static_cast<size_t>((M + 127) / 128 + 8) * 4, 256);
+    }
+  }
   w.bytes = off;
   return w;
 }
@@ -425,21 +658,87 @@ cudaError_t launch_w8a8_linear(const W8Args& a, cudaStream_t stream) {
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
     attr_err = cudaFuncSetAttribute(k_w8_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(k_w8_gemm_p, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   });
   if (attr_err != cudaSuccess) return attr_err;
   const W8Ws w = carve_w8(a.ws, a.M, a.d_i, a.r);
-  cudaError_t e = launch_pro_fp8(a.x, a.M, a.d_i, a.w_norm, a.z, a.z_ld, a.eps, a.A, a.r, w.qx, w.s_x, w.t, w.t_ld,
-                                 stream);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  if (a.M > 64 && a.r <= 32) {
+    // large M: the row prologue (E4M3 codes, s_x, f16 rows) and the adapter's down-projection
+    // on the tensor cores (ranks up to 32), in place of the cluster prologue
+    LinearArgs in{};
+    in.x = a.x;
+    in.M = a.M;
+    in.d_i = a.d_i;
+    in.w_norm = a.w_norm;
+    in.z = a.w_norm ? a.z : nullptr;
+    in.z_ld = (a.w_norm && a.z) ? a.z_ld : 0;
+    in.eps = a.eps;
+    ActConv conv{};
+    if (a.r > 0) {
+      const int r16 = (a.r + 15) / 16 * 16;
+      conv.A[0] = a.A;
+      conv.A16[0] = w.A16;
+      conv.r[0] = a.r;
+      conv.n = 1;
+      conv.zero[conv.n_zero_ranges] = reinterpret_cast<float*>(w.counters);
+      conv.n_zero[conv.n_zero_ranges++] = ((a.M + 127) / 128 + 3) / 4 * 4;
+      if (r16 > a.r) {
+        conv.zero[conv.n_zero_ranges] = reinterpret_cast<float*>(w.A16 + static_cast<int64_t>(a.r) * a.d_i);
+        conv.n_zero[conv.n_zero_ranges++] = static_cast<int64_t>(r16 - a.r) * a.d_i / 2;
+      }
+    }
+    e = launch_act_prologue(in, w.hq, w.rowscale, conv, stream, w.qx, w.s_x);
+    if (e != cudaSuccess) return e;
+    if (a.r > 0) {
+      e = launch_lora_down_t(w.hq, a.M, a.d_i, w.A16, a.r, w.rowscale, w.t, w.t_ld, w.t_part, w.counters, stream);
+      if (e != cudaSuccess) return e;
+    }
+  } else {
+    e = launch_pro_fp8(a.x, a.M, a.d_i, a.w_norm, a.z, a.z_ld, a.eps, a.A, a.r, w.qx, w.s_x, w.t, w.t_ld, stream);
+    if (e != cudaSuccess) return e;
+  }
 
   W8Params p{};
   p.M = a.M;
   p.d_i = a.d_i;
   p.d_o = a.d_o;
-  p.N = a.M <= 64 ? static_cast<int>((a.M + 15) / 16 * 16) : kMaxNTile;
-  p.otiles = static_cast<int>((a.d_o + kTileO - 1) / kTileO);
-  const int mtiles = static_cast<int>((a.M + p.N - 1) / p.N);
+  p.s_w = a.s_w;
+  p.s_x = w.s_x;
+  p.t = w.t;
+  p.t_ld = w.t_ld;
+  p.B = a.r > 0 ? static_cast<const __nv_bfloat16*>(a.B) : nullptr;
+  p.r = a.r;
+  p.lambda = a.lambda;
+  p.y = a.y;
+  p.y_f32 = a.y_f32 ? 1 : 0;
   p.kc = static_cast<int>(a.d_i / kChunk);
+  p.otiles = static_cast<int>((a.d_o + kTileO - 1) / kTileO);
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  if (a.M > 64) {  // large M: the persistent kernel
+    p.N = kPN;
+    p.mtiles = static_cast<int>((a.M + kPN - 1) / kPN);
+    p.n_tiles = p.otiles * p.mtiles;
+    p.off_la = kPStages * kPStageBytes;
+    p.off_lb = p.off_la + kTileO * 128;
+    p.off_ctrl = static_cast<uint32_t>(align_up(p.off_lb + static_cast<size_t>(kPN) * 128, 128));
+    W8Maps maps;
+    if (!encode_u8(&maps.w, a.codes, a.d_i, a.d_o, kChunk, kTileO) || !encode_u8(&maps.x, w.qx, a.d_i, a.M, kChunk, kPN))
+      return cudaErrorInvalidValue;
+    cudaLaunchConfig_t c{};
+    c.gridDim = dim3(static_cast<unsigned>(p.n_tiles < sm_count() ? p.n_tiles : sm_count()));
+    c.blockDim = dim3(kThreads);
+    c.dynamicSmemBytes = 1024 + p.off_ctrl + sizeof(W8PCtrl);
+    c.stream = stream;
+    c.attrs = pdl;
+    c.numAttrs = 1;
+    return cudaLaunchKernelEx(&c, k_w8_gemm_p, maps, p);
+  }
+  p.N = static_cast<int>((a.M + 15) / 16 * 16);
+  const int mtiles = static_cast<int>((a.M + p.N - 1) / p.N);
   // split K when the tiles alone leave most SMs idle (decode)
   const int tiles = p.otiles * mtiles;
   int S = 1;
@@ -456,23 +755,13 @@ cudaError_t launch_w8a8_linear(const W8Args& a, cudaStream_t stream) {
   const size_t smem = 1024 + p.off_ctrl + sizeof(W8Ctrl);
   if (st < 2 || (S > 1 && static_cast<size_t>(p.N) * kTileO * 4 > static_cast<size_t>(st) * p.stage_bytes))
     return cudaErrorInvalidValue;
-  p.s_w = a.s_w;
-  p.s_x = w.s_x;
-  p.t = w.t;
-  p.t_ld = w.t_ld;
-  p.B = a.r > 0 ? static_cast<const __nv_bfloat16*>(a.B) : nullptr;
-  p.r = a.r;
-  p.lambda = a.lambda;
-  p.y = a.y;
-  p.y_f32 = a.y_f32 ? 1 : 0;
 
   W8Maps maps;
   if (!encode_u8(&maps.w, a.codes, a.d_i, a.d_o, kChunk, kTileO) ||
       !encode_u8(&maps.x, w.qx, a.d_i, a.M, kChunk, p.N))
     return cudaErrorInvalidValue;
   cudaLaunchAttribute attrs[2];
-  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  attrs[0] = pdl[0];
   attrs[1].id = cudaLaunchAttributeClusterDimension;
   attrs[1].val.clusterDim.x = static_cast<unsigned>(S);
   attrs[1].val.clusterDim.y = 1;

@@ -156,8 +156,32 @@ def test_w8a8_m4096_sampled_rows(cuda_ok):
     assert pl.last_device_status() == 0
 
 
+@pytest.mark.parametrize("kw", [dict(lora=False), dict(norm=False), dict(rows=True)])
+def test_w8a8_large_m_variants(cuda_ok, kw):
+    """M > 64 (the persistent kernel, ragged last token and weight tiles): no adapter, no norm,
+    and per-token states with an odd rank."""
+    d_o, d_i, M = 640, 1024, 300
+    r = 5 if kw.get("rows") else 16
+    g, c = _case(d_o, d_i, M, r, seed=31)
+    codes, s_w, q_ref, s_ref = _quant_check(c["W"])
+    lora, norm = kw.get("lora", True), kw.get("norm", True)
+    z, z_ref = g["z"], None
+    if kw.get("rows"):
+        zt = torch.randn(M, d_i, generator=torch.Generator().manual_seed(3)) * 1e-2
+        z, z_ref = zt.to(DEV), np32(zt)
+    y = pl.w8a8_lora_linear(g["x"], codes, s_w, g["A"] if lora else None, g["B"] if lora else None, 2.0,
+                            g["w_norm"] if norm else None, z if norm else None, synthetic.EPS, out_dtype=torch.float32)
+    ref = _oracle(c, q_ref, s_ref, 2.0, norm, norm, lora) if z_ref is None else _oracle(c, q_ref, s_ref, 2.0, z=z_ref)
+    _assert_close(y, ref, f"w8a8 large M {kw}")
+    assert pl.last_device_status() == 0
+
+
 def test_w8a8_repeatable_bitwise(cuda_ok):
     g, c = _case(3584, 3584, 64, 32, seed=2)
+    codes, s_w = pl.w8a8_quantize_weight(g["W"])
+    ys = [pl.w8a8_lora_linear(g["x"], codes, s_w, g["A"], g["B"], 2.0, g["w_norm"], g["z"]) for _ in range(3)]
+    assert torch.equal(ys[0], ys[1]) and torch.equal(ys[0], ys[2])
+    g, c = _case(1000, 1024, 300, 32, seed=3)  # the persistent large-M kernel
     codes, s_w = pl.w8a8_quantize_weight(g["W"])
     ys = [pl.w8a8_lora_linear(g["x"], codes, s_w, g["A"], g["B"], 2.0, g["w_norm"], g["z"]) for _ in range(3)]
     assert torch.equal(ys[0], ys[1]) and torch.equal(ys[0], ys[2])
