@@ -425,7 +425,8 @@ __global__ void __launch_bounds__(kActThreads, 2) k_act(const __nv_bfloat16* __r
 // s_x = fp32(max |h| / 448) (1 for a zero row), codes E4M3(fp32(h / s_x)), round to
 // nearest even, saturating, +0 for values that round to zero.
 template <bool kFp8>
-__global__ void __launch_bounds__(kProThreads) k_pro_dec(const __grid_constant__ ProParams pr) {
+// At most 64 registers a thread: four CTAs per SM, so that a batch's clusters fit in one wave.
+__global__ void __launch_bounds__(kProThreads, 4) k_pro_dec(const __grid_constant__ ProParams pr) {
   // the input this cluster works on: the last one whose first cluster is <= this one
   int si = 0;
 #pragma unroll
@@ -608,11 +609,19 @@ __global__ void __launch_bounds__(kProThreads) k_pro_dec(const __grid_constant__
   //    its share of t (entries e = rank mod C of [R][J]), the slices added in slice order
   cluster_sync();
   if (tid < R) {
-    float s = 0.f, x = 0.f;
-    for (int c = 0; c < C; ++c) {
-      s += ld_dsmem_f32(mapa_shared(smem_u32(&xch[2 * tid]), static_cast<uint32_t>(c)));
-      x = fmaxf(x, ld_dsmem_f32(mapa_shared(smem_u32(&xch[2 * tid + 1]), static_cast<uint32_t>(c))));
-    }
+    float s = 0.f, x = 0.f, sv[kProMaxC], xv[kProMaxC];
+#pragma unroll
+    for (int c = 0; c < kProMaxC; ++c)  // all loads first: they are in flight together
+      if (c < C) {
+        sv[c] = ld_dsmem_f32(mapa_shared(smem_u32(&xch[2 * tid]), static_cast<uint32_t>(c)));
+        xv[c] = ld_dsmem_f32(mapa_shared(smem_u32(&xch[2 * tid + 1]), static_cast<uint32_t>(c)));
+      }
+#pragma unroll
+    for (int c = 0; c < kProMaxC; ++c)
+      if (c < C) {
+        s += sv[c];
+        x = fmaxf(x, xv[c]);
+      }
     const float inv = norm ? 1.0f / sqrtf(s / static_cast<float>(p.d_i) + p.eps) : 1.0f;
     const float hmax = inv * x;  // max |h|: rounding is monotone, so this is max |fl(u inv)|
     s_inv[tid] = inv;
@@ -666,8 +675,13 @@ __global__ void __launch_bounds__(kProThreads) k_pro_dec(const __grid_constant__
     const int m = e / J, jj = e % J;
     if (m0 + m < p.M) {
       const uint32_t a = smem_u32(&xch[2 * kProMaxR + m * J + jj]);
-      float s = 0.f;
-      for (int c = 0; c < C; ++c) s += ld_dsmem_f32(mapa_shared(a, static_cast<uint32_t>(c)));
+      float s = 0.f, sv[kProMaxC];
+#pragma unroll
+      for (int c = 0; c < kProMaxC; ++c)  // all loads first: they are in flight together
+        if (c < C) sv[c] = ld_dsmem_f32(mapa_shared(a, static_cast<uint32_t>(c)));
+#pragma unroll
+      for (int c = 0; c < kProMaxC; ++c)
+        if (c < C) s += sv[c];
       p.t[(m0 + m) * p.t_ld + jj] = s_inv[m] * s;
     }
   }
