@@ -129,9 +129,14 @@ __device__ __forceinline__ TileAt tile_at(const GParams& p, int tile) {
   return TileAt{gi, local / p.g[gi].n_ot, local % p.g[gi].n_ot};
 }
 
+// One commit per K step (main or LoRA) to sdone[step mod kSDone]: it releases that step's stage
+// (both CTAs' dequant warps read its codes before the MMAs could start, the MMAs read its
+// token rows) and its tensor-memory slot, so one tensor-core instruction serves both.
+constexpr int kSDone = 16;
+static_assert(kMaxStages <= kSDone && kMaxASlots <= kSDone, "a waiter is never two phases behind");
 struct GCtrl {
-  uint64_t full[kMaxStages], empty[kMaxStages];
-  uint64_t afull[kMaxASlots], aempty[kMaxASlots];
+  uint64_t full[kMaxStages], sdone[kSDone];
+  uint64_t afull[kMaxASlots];
   uint64_t dfull[2], dempty[2];
   uint64_t tfull[2], tempty[2];
   uint64_t mma_done;  // every MMA this CTA issued has completed
@@ -221,14 +226,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
     if (blockIdx.x < 1024) g_pf_wait[blockIdx.x][10] = globaltimer_ns();
 #endif
     pdl_launch_dependents();
-    for (int s = 0; s < nst; ++s) {
-      mbar_init(smem_u32(&C.full[s]), 1);
-      mbar_init(smem_u32(&C.empty[s]), kDeqWarps + 1);  // + the pair's MMA commit
-    }
-    for (int a = 0; a < kASlots; ++a) {
+    for (int s = 0; s < nst; ++s) mbar_init(smem_u32(&C.full[s]), 1);
+    for (int s = 0; s < kSDone; ++s) mbar_init(smem_u32(&C.sdone[s]), 1);  // the pair's MMA commit
+    for (int a = 0; a < kASlots; ++a)
       mbar_init(smem_u32(&C.afull[a]), 2 * kDeqWarps);  // both CTAs' dequant warps (waited on in the even one)
-      mbar_init(smem_u32(&C.aempty[a]), 1);
-    }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&C.dfull[b]), 1);
       mbar_init(smem_u32(&C.dempty[b]), 2 * kEpiWarps);  // both CTAs' epilogue warps (waited on in the even one)
@@ -288,7 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
           const int st = rs.i;
           {
             PF_T0();
-            if (gs >= nst) ok = wait_p(smem_u32(&C.empty[st]), rs.ph ^ 1u, abort_flag);
+            const int64_t gd = gs - nst;  // the step that last used stage st
+            if (gs >= nst) ok = wait_p(smem_u32(&C.sdone[gd % kSDone]), static_cast<uint32_t>(gd / kSDone) & 1u, abort_flag);
             PF_ACC(0);
           }
           if (!ok) break;
@@ -327,6 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
       Ring rs, ra;  // stage and slot rings
       const uint64_t hdesc0 = smem_desc_sw128(sbase, 1024);
       int it = 0;
+      int64_t gstep = 0;  // K steps issued, main and LoRA
       for (int tile = pair; tile < p.n_tiles && ok; tile += npairs, ++it) {
         const int b = it & 1;
         const int r_t = p.g[tile_at(p, tile).gi].r;  // this tile's adapter rank
@@ -359,8 +362,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
           mma2_ts(d, acol + 8u, hdesc + 2u, idesc, 1u);
           mma2_ts(d, acol + 16u, hdesc + 4u, idesc, 1u);
           mma2_ts(d, acol + 24u, hdesc + 6u, idesc, 1u);
-          tc_commit2(smem_u32(&C.empty[st]));
-          tc_commit2(smem_u32(&C.aempty[a]));
+          tc_commit2(smem_u32(&C.sdone[gstep % kSDone]));
+          ++gstep;
           rs.next(nst);
           ra.next(kASlots);
         }
@@ -372,8 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
             const uint64_t hdesc = hdesc0 + static_cast<uint64_t>(static_cast<uint32_t>(st) * (kStageBytes >> 4));
             const uint32_t acol = tmem + 32u * a;
             for (int kk = 0; kk < l_sub; ++kk) mma2_ts(d, acol + 8u * kk, hdesc + 2u * kk, idesc_l, 1u);
-            tc_commit2(smem_u32(&C.empty[st]));
-            tc_commit2(smem_u32(&C.aempty[a]));
+            tc_commit2(smem_u32(&C.sdone[gstep % kSDone]));
+            ++gstep;
             rs.next(nst);
             ra.next(kASlots);
           }
@@ -430,7 +433,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
         }
         {
           PF_T0();
-          ok = ok && (gs < kASlots || wait_p(smem_u32(&C.aempty[a]), ra.ph ^ 1u, abort_flag));
+          const int64_t gd = gs - kASlots;  // the step that last used slot a
+          ok = ok && (gs < kASlots || wait_p(smem_u32(&C.sdone[gd % kSDone]), static_cast<uint32_t>(gd / kSDone) & 1u, abort_flag));
           if (lane == 0 && warp == 2) PF_ACC(6);
         }
         if (!ok) break;
@@ -464,7 +468,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_nvfp4(const __grid_constan
         if (lane == 0) {
           if (rank == 0) mbar_arrive(smem_u32(&C.afull[a]));
           else mbar_arrive_leader(smem_u32(&C.afull[a]));
-          mbar_arrive(smem_u32(&C.empty[st]));
         }
       }
     }
