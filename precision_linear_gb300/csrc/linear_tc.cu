@@ -496,6 +496,10 @@ __global__ void __launch_bounds__(kProThreads, 4) k_pro_dec(const __grid_constan
         g[0] += za.x; g[1] += za.y; g[2] += za.z; g[3] += za.w; g[4] += zb.x; g[5] += zb.y; g[6] += zb.z; g[7] += zb.w;
       }
     }
+    uint4 xr[kProMaxR];  // the rows' pieces, all loads issued before any use
+#pragma unroll
+    for (int m = 0; m < kProMaxR; ++m)
+      xr[m] = m < R && m0 + m < p.M ? reinterpret_cast<const uint4*>(p.x + (m0 + m) * p.d_i)[q] : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int m = 0; m < kProMaxR; ++m) {
       if (m < R) {
@@ -504,7 +508,7 @@ __global__ void __launch_bounds__(kProThreads, 4) k_pro_dec(const __grid_constan
         for (int i = 0; i < 8; ++i) v[i] = 0.f;
         const int64_t row = m0 + m;
         if (row < p.M) {
-          const uint4 xv = reinterpret_cast<const uint4*>(p.x + row * p.d_i)[q];
+          const uint4 xv = xr[m];
           float gz[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) gz[i] = g[i];
