@@ -9,15 +9,15 @@
 //
 // Two kernels per call, chained by programmatic dependent launch:
 //
-// k_pro_dec (clusters of C CTAs; a cluster owns R token rows, CTA c of it the c-th slice
-//   of the K = d_i axis): u = x (.) (w_norm + z) in FP32, per row the sum of x^2 and max |u|
-//   over the slice, and the slice's share of A_p u for every projection p of the group
-//   (CUDA cores, FP32).  One exchange over distributed shared memory gives every CTA the
-//   row statistics of the whole row: rs = 1 / sqrt(mean x^2 + eps), the power of two c_m
-//   with max |h| / c_m in [2^13, 2^14), and it writes the f16 activations h / c_m of its
-//   slice (11-bit significand, no overflow); the adapter sums of the C slices are added in
-//   slice order (deterministic) and t = rs A_p u, FP32, goes to the workspace.  The
-//   adapter's down-projection is thereby done once per call, not once per weight tile.
+// k_pro_rows (rows up to 8192 long; one CTA per input, group of R <= 4 token rows and group
+//   of 8 adapter rows): u = x (.) (w_norm + z) in FP32 for the whole rows, per row the sum of x^2 and max
+//   |u|, rs = 1 / sqrt(mean x^2 + eps) and the power of two c_m with max |h| / c_m in
+//   [2^13, 2^14); the CTA of adapter group 0 writes the f16 activations h / c_m (11-bit
+//   significand, no overflow) and c_m, every CTA t = rs A_p u (FP32, CUDA cores) for its
+//   adapter rows.  The adapter's down-projection is thereby done once per call, not once per
+//   weight tile, and no CTA waits on another.  Longer rows take k_pro_dec: clusters of 8 CTAs
+//   over 1, 2 or 4 token rows, CTA c the c-th slice of K, one exchange of the row statistics
+//   and of the adapter sums over distributed shared memory.
 //
 // k_tc_decode (a cluster of S CTAs per 128 weight rows of one projection; CTA s takes the
 //   s-th slice of K in chunks of 256):
@@ -163,7 +163,8 @@ struct Smem {
   float rowscale[kMaxN];
 };
 
-// One input of the cluster prologue (its clusters start at cluster cl0).
+// One input of the prologue (cluster prologue: its clusters start at cl0; row prologue: its
+// CTAs start at cta0).
 struct ProSet {
   const __nv_bfloat16* x;
   int64_t M, d_i;
@@ -175,19 +176,24 @@ struct ProSet {
   float* rowscale;      // [M]: c_m (f16 mode), s_x (FP8 mode)
   uint8_t* qx;          // [M][d_i] E4M3 codes (FP8 mode)
   float* t;             // [M][t_ld]
-  int t_ld, R, C, n_proj, rtot, cl0;
+  int t_ld;
+  int R;                // token rows per cluster (cluster prologue) or per CTA (row prologue)
+  int C, cl0;           // cluster prologue: CTAs per cluster, first cluster
+  int H, JG, cta0;      // row prologue: adapter groups, adapter rows per group (4 or 8), first CTA
+  int n_proj, rtot;
   const __nv_bfloat16* A[kMaxAdapt];  // [r_p][d_i]
   int r[kMaxAdapt], toff[kMaxAdapt];
 };
-// Arguments of the cluster prologue: its inputs, one cluster range each.
+// Arguments of the prologue: its inputs, one cluster or CTA range each.
 struct ProParams {
   int n_sets;
   ProSet set[kMaxSets];
 };
 constexpr int kProThreads = 256;
 constexpr int kProWarps = kProThreads / 32;
-constexpr int kProMaxR = 4;  // token rows per cluster
-constexpr int kProMaxC = 8;  // CTAs per cluster
+constexpr int kProMaxR = 4;  // token rows per cluster or per CTA
+constexpr int kProMaxC = 8;  // CTAs per cluster (cluster prologue)
+constexpr int64_t kRowsMaxDi = 8192;  // the row prologue takes rows up to this long
 
 PL_DEVINL bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   return wait_or_abort_status(bar, parity, abort_flag, &g_tc_status);
@@ -693,6 +699,257 @@ __global__ void __launch_bounds__(kProThreads, 4) k_pro_dec(const __grid_constan
   cluster_sync();  // the peers read this CTA's shared memory until here
 }
 
+// ------------------------------------------------------------------ row prologue
+// One CTA per (input, group of R token rows, group of JG adapter rows).  Every CTA of a row
+// group reads its R rows whole: u = x (.) (w_norm + z) in FP32 into shared memory and, per
+// row, the sum of x^2 and max |u| (a fixed shuffle tree, then the warps in order), so
+// rs = 1 / sqrt(mean x^2 + eps) and the power of two c_m need no exchange between CTAs.  The
+// CTA of adapter group 0 writes the f16 rows h / c_m (max |h| / c_m in [2^13, 2^14)) and c_m;
+// every CTA writes t = rs A_p u for its adapter rows: warp w takes four adapter rows and one
+// slice of K (JG / 4 row groups x 8 / (JG / 4) slices), the lanes split the slice in pieces
+// of 8, a fixed shuffle tree and then the slices in order add them up (deterministic).
+// kFp8: instead of the f16 rows, the per-token FP8 quantisation of h for the W8A8 linear:
+// s_x = fp32(max |h| / 448) (1 for a zero row), codes E4M3(fp32(h / s_x)), round to
+// nearest even, saturating, +0 for values that round to zero.
+template <bool kFp8>
+__global__ void __launch_bounds__(kProThreads, 1) k_pro_rows(const __grid_constant__ ProParams pr) {
+  // the input of this CTA: the last one whose first CTA is <= this one
+  int si = 0;
+#pragma unroll
+  for (int q = 1; q < kMaxSets; ++q)
+    if (q < pr.n_sets && static_cast<int>(blockIdx.x) >= pr.set[q].cta0) si = q;
+  const ProSet& p = pr.set[si];
+  extern __shared__ float4 pro_smem4[];
+  float* u = reinterpret_cast<float*>(pro_smem4);  // [R][d_i]
+  __shared__ float red[kProWarps][kProMaxR][2];
+  __shared__ float part[kProWarps][4][kProMaxR];   // adapter sums per K slice
+  __shared__ float s_inv[kProMaxR], s_f[kProMaxR];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int local = static_cast<int>(blockIdx.x) - p.cta0;
+  const int grp = local / p.H, hg = local - grp * p.H;  // row group, adapter group
+  const int64_t m0 = static_cast<int64_t>(grp) * p.R;
+  const int rows = static_cast<int>(p.M - m0 < p.R ? p.M - m0 : p.R);
+  const int J = p.rtot, JG = p.JG;
+  const int j0 = hg * JG, j1 = j0 + JG < J ? j0 + JG : J;
+  const int64_t n8 = p.d_i / 8;
+  const bool norm = p.w_norm != nullptr;
+  const bool zshared = norm && p.z != nullptr && p.z_ld == 0, zrows = norm && p.z != nullptr && p.z_ld != 0;
+  // the member and row of adapter row jj of this input (null past J)
+  auto arow_of = [&](int jj) -> const __nv_bfloat16* {
+    const __nv_bfloat16* a = nullptr;
+    for (int pp = 0; pp < p.n_proj; ++pp)
+      if (jj < j1 && jj >= p.toff[pp] && jj < p.toff[pp] + p.r[pp]) a = p.A[pp] + static_cast<int64_t>(jj - p.toff[pp]) * p.d_i;
+    return a;
+  };
+  if (tid == 0) {
+    PL_TLP(0);
+    pdl_launch_dependents();
+  }
+  // While the preceding kernel finishes: bring this CTA's rows, its adapter rows, the norm
+  // scale and the noise into L2.
+  {
+    const uint32_t rb = static_cast<uint32_t>(p.d_i) * 2u, fb = static_cast<uint32_t>(p.d_i) * 4u;
+    if (tid < rows) {
+      prefetch_l2(p.x + (m0 + tid) * p.d_i, rb);
+      if (zrows) prefetch_l2(p.z + (m0 + tid) * p.z_ld, fb);
+    } else if (tid == kProMaxR && norm) {
+      prefetch_l2(p.w_norm, fb);
+    } else if (tid == kProMaxR + 1 && zshared) {
+      prefetch_l2(p.z, fb);
+    } else if (tid >= 32 && tid - 32 < j1 - j0) {
+      const __nv_bfloat16* a = arow_of(j0 + tid - 32);
+      if (a != nullptr) prefetch_l2(a, rb);
+    }
+  }
+  pdl_wait();  // x, w_norm and z may come from the preceding kernel, which may also still read the workspace
+  if (tid == 0) PL_TLP(1);
+
+  // 1. u of the rows; per row the sum of x^2 and max |u|
+  float ss[kProMaxR], mx[kProMaxR];
+#pragma unroll
+  for (int m = 0; m < kProMaxR; ++m) {
+    ss[m] = 0.f;
+    mx[m] = 0.f;
+  }
+  for (int64_t q = tid; q < n8; q += kProThreads) {
+    uint4 xr[kProMaxR];  // the rows' pieces, all loads issued before any use
+#pragma unroll
+    for (int m = 0; m < kProMaxR; ++m)
+      xr[m] = m < rows ? reinterpret_cast<const uint4*>(p.x + (m0 + m) * p.d_i)[q] : make_uint4(0u, 0u, 0u, 0u);
+    float g[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) g[i] = 1.f;
+    if (norm) {
+      const float4 a = reinterpret_cast<const float4*>(p.w_norm)[2 * q], b = reinterpret_cast<const float4*>(p.w_norm)[2 * q + 1];
+      g[0] = a.x; g[1] = a.y; g[2] = a.z; g[3] = a.w; g[4] = b.x; g[5] = b.y; g[6] = b.z; g[7] = b.w;
+      if (zshared) {
+        const float4 za = reinterpret_cast<const float4*>(p.z)[2 * q], zb = reinterpret_cast<const float4*>(p.z)[2 * q + 1];
+        g[0] += za.x; g[1] += za.y; g[2] += za.z; g[3] += za.w; g[4] += zb.x; g[5] += zb.y; g[6] += zb.z; g[7] += zb.w;
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < kProMaxR; ++m) {
+      if (m < rows) {
+        float gz[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) gz[i] = g[i];
+        if (zrows) {
+          const float4* zr = reinterpret_cast<const float4*>(p.z + (m0 + m) * p.z_ld) + 2 * q;
+          const float4 za = zr[0], zb = zr[1];
+          gz[0] += za.x; gz[1] += za.y; gz[2] += za.z; gz[3] += za.w;
+          gz[4] += zb.x; gz[5] += zb.y; gz[6] += zb.z; gz[7] += zb.w;
+        }
+        const uint32_t w4[4] = {xr[m].x, xr[m].y, xr[m].z, xr[m].w};
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float a0 = bf16lo_to_f32(w4[j]), a1 = bf16hi_to_f32(w4[j]);
+          ss[m] = fmaf(a0, a0, fmaf(a1, a1, ss[m]));
+          v[2 * j] = a0 * gz[2 * j];
+          v[2 * j + 1] = a1 * gz[2 * j + 1];
+          mx[m] = fmaxf(mx[m], fmaxf(fabsf(v[2 * j]), fabsf(v[2 * j + 1])));
+        }
+        float4* ud = reinterpret_cast<float4*>(u + m * p.d_i + q * 8);
+        ud[0] = make_float4(v[0], v[1], v[2], v[3]);
+        ud[1] = make_float4(v[4], v[5], v[6], v[7]);
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < kProMaxR; ++m) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      ss[m] += __shfl_xor_sync(0xFFFFFFFFu, ss[m], o);
+      mx[m] = fmaxf(mx[m], __shfl_xor_sync(0xFFFFFFFFu, mx[m], o));
+    }
+    if (lane == 0) {
+      red[warp][m][0] = ss[m];
+      red[warp][m][1] = mx[m];
+    }
+  }
+  __syncthreads();
+  if (tid < rows) {
+    float s = 0.f, x = 0.f;
+#pragma unroll
+    for (int w = 0; w < kProWarps; ++w) {
+      s += red[w][tid][0];
+      x = fmaxf(x, red[w][tid][1]);
+    }
+    const float inv = norm ? 1.0f / sqrtf(s / static_cast<float>(p.d_i) + p.eps) : 1.0f;
+    const float hmax = inv * x;  // max |h|: rounding is monotone, so this is max |fl(u inv)|
+    s_inv[tid] = inv;
+    if (kFp8) {
+      const float sx = hmax > 0.f ? __fdiv_rn(hmax, 448.0f) : 1.0f;
+      s_f[tid] = sx;
+      if (hg == 0) p.rowscale[m0 + tid] = sx;
+    } else {
+      int e = hmax > 0.f ? ilogbf(hmax) - 13 : 0;  // max |h| / c_m in [2^13, 2^14)
+      e = e < -100 ? -100 : (e > 100 ? 100 : e);
+      s_f[tid] = inv * ldexpf(1.0f, -e);
+      if (hg == 0) p.rowscale[m0 + tid] = ldexpf(1.0f, e);
+    }
+  }
+  __syncthreads();
+  if (tid == 0) PL_TLP(4);
+
+  // 2. the activations (adapter group 0)
+  if (hg == 0) {
+    for (int64_t q = tid; q < n8; q += kProThreads) {
+#pragma unroll
+      for (int m = 0; m < kProMaxR; ++m) {
+        if (m < rows) {
+          const int64_t row = m0 + m;
+          const float4* us = reinterpret_cast<const float4*>(u + m * p.d_i + q * 8);
+          const float4 a = us[0], b = us[1];
+          const float f = s_f[m];
+          if (kFp8) {
+            const float inv = s_inv[m];
+            const float hv[8] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv, b.x * inv, b.y * inv, b.z * inv, b.w * inv};
+            uint32_t w[2];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              uint32_t c4 = 0;
+#pragma unroll
+              for (int i = 0; i < 4; i += 2) {
+                // two codes per conversion; a value that rounds to zero keeps no sign
+                uint32_t c2 = cvt_e4m3x2(__fdiv_rn(hv[4 * hh + i + 1], f), __fdiv_rn(hv[4 * hh + i], f));
+                if ((c2 & 0x7Fu) == 0) c2 &= 0xFF00u;
+                if ((c2 & 0x7F00u) == 0) c2 &= 0x00FFu;
+                c4 |= c2 << (8 * i);
+              }
+              w[hh] = c4;
+            }
+            reinterpret_cast<uint2*>(p.qx + row * p.d_i)[q] = make_uint2(w[0], w[1]);
+          } else {
+            reinterpret_cast<uint4*>(p.hq + row * p.d_i)[q] =
+                make_uint4(f32x2_to_f16x2(a.x * f, a.y * f), f32x2_to_f16x2(a.z * f, a.w * f),
+                           f32x2_to_f16x2(b.x * f, b.y * f), f32x2_to_f16x2(b.z * f, b.w * f));
+          }
+        }
+      }
+    }
+  }
+
+  // 3. t = rs A_p u for adapter rows [j0, j1): warp w takes rows j0 + 4 (w mod nj) .. + 3 and
+  //    K slice w / nj of ns
+  const int nj = JG / 4, ns = kProWarps / nj;
+  const int jb = j0 + 4 * (warp % nj), ks = warp / nj;
+  const int64_t k0 = ks * n8 / ns, k1 = (ks + 1) * n8 / ns;
+  const __nv_bfloat16* arow[4];
+#pragma unroll
+  for (int jr = 0; jr < 4; ++jr) arow[jr] = arow_of(jb + jr);
+  float acc[4][kProMaxR];
+#pragma unroll
+  for (int jr = 0; jr < 4; ++jr)
+#pragma unroll
+    for (int m = 0; m < kProMaxR; ++m) acc[jr][m] = 0.f;
+#pragma unroll 2
+  for (int64_t q = k0 + lane; q < k1; q += 32) {  // two iterations unrolled: their loads are in flight together
+    uint4 av[4];
+#pragma unroll
+    for (int jr = 0; jr < 4; ++jr)
+      av[jr] = arow[jr] != nullptr ? reinterpret_cast<const uint4*>(arow[jr])[q] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int m = 0; m < kProMaxR; ++m) {
+      if (m < rows) {
+        const float4* us = reinterpret_cast<const float4*>(u + m * p.d_i + q * 8);
+        const float4 ua = us[0], ub = us[1];
+        const float uv[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
+#pragma unroll
+        for (int jr = 0; jr < 4; ++jr) {
+          const uint32_t w4[4] = {av[jr].x, av[jr].y, av[jr].z, av[jr].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            acc[jr][m] = fmaf(bf16lo_to_f32(w4[j]), uv[2 * j], acc[jr][m]);
+            acc[jr][m] = fmaf(bf16hi_to_f32(w4[j]), uv[2 * j + 1], acc[jr][m]);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int jr = 0; jr < 4; ++jr)
+#pragma unroll
+    for (int m = 0; m < kProMaxR; ++m) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc[jr][m] += __shfl_xor_sync(0xFFFFFFFFu, acc[jr][m], o);
+      if (lane == 0) part[warp][jr][m] = acc[jr][m];
+    }
+  __syncthreads();
+  // thread (jr, m, group) of each row group: the slices in order
+  if (tid < JG * kProMaxR) {
+    const int jl = tid / kProMaxR, m = tid % kProMaxR;  // adapter row j0 + jl, token row m
+    const int jj = j0 + jl;
+    if (jj < j1 && m < rows) {
+      const int wg = jl / 4, jr = jl % 4;  // its warps: wg + nj s, s = 0 .. ns - 1
+      float s = 0.f;
+      for (int sl = 0; sl < ns; ++sl) s += part[wg + nj * sl][jr][m];
+      p.t[(m0 + m) * p.t_ld + jj] = s_inv[m] * s;
+    }
+  }
+  if (tid == 0) PL_TLP(3);
+}
+
 // ------------------------------------------------------------------ main kernel
 __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(const __grid_constant__ TcMaps maps,
                                                            const __grid_constant__ TcParams p) {
@@ -1107,9 +1364,13 @@ cudaError_t set_kernel_attributes() {
     if (err == cudaSuccess)
       err = cudaFuncSetAttribute(k_act<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(k_pro_rows<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+    if (err == cudaSuccess)
       err = cudaFuncSetAttribute(k_pro_dec<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
     if (err == cudaSuccess)
       err = cudaFuncSetAttribute(k_pro_dec<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(k_pro_rows<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
   });
   return err;
 }
@@ -1187,16 +1448,28 @@ size_t carve_sets(void* ws, int64_t d_i, const int64_t* Ms, const int* rtot, int
   return off;
 }
 
-// Token rows per prologue cluster: enough clusters of kProMaxC CTAs to spread the row and
-// adapter work, few enough that each cluster's slice of A is read a handful of times.
-int pro_rows(int64_t M) { return M <= 16 ? 1 : (M <= 32 ? 2 : kProMaxR); }
+// The row prologue's decomposition of one input: R token rows per CTA (their FP32 u, R d_i x 4
+// bytes of shared memory, at most 160 KB), adapter groups of JG rows (fewer rows for long
+// rows: with 8 (4 past d_i = 4096) each warp sums a quarter (an eighth) of K, a few pieces of
+// 8 per lane).
+void pro_plan(ProSet& q) {
+  const int64_t fit = (160 * 1024) / (q.d_i * 4);
+  int64_t r = q.M < kProMaxR ? q.M : kProMaxR;
+  r = r < fit ? r : fit;
+  q.R = r < 1 ? 1 : static_cast<int>(r);
+  q.JG = q.d_i <= 4096 ? 8 : 4;
+  q.H = q.rtot > 0 ? (q.rtot + q.JG - 1) / q.JG : 1;
+}
 
-// The cluster prologue: input s takes clusters [cl0_s, cl0_s + ceil(M_s / R_s)) of C CTAs.
-cudaError_t launch_pro(ProParams pr, bool fp8, cudaStream_t stream) {
+// The cluster prologue (rows longer than kRowsMaxDi): input s takes clusters [cl0_s,
+// cl0_s + ceil(M_s / R_s)) of kProMaxC CTAs, R_s = 1, 2 or 4 token rows each.
+cudaError_t launch_pro_clusters(ProParams pr, bool fp8, cudaStream_t stream) {
   int clusters = 0;
   size_t pro_smem = 0;
   for (int s = 0; s < pr.n_sets; ++s) {
     ProSet& q = pr.set[s];
+    q.R = q.M <= 16 ? 1 : (q.M <= 32 ? 2 : kProMaxR);
+    q.C = kProMaxC;
     q.cl0 = clusters;
     clusters += static_cast<int>((q.M + q.R - 1) / q.R);
     const int64_t n8 = q.d_i / 8;
@@ -1207,17 +1480,46 @@ cudaError_t launch_pro(ProParams pr, bool fp8, cudaStream_t stream) {
   pa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pa[0].val.programmaticStreamSerializationAllowed = 1;
   pa[1].id = cudaLaunchAttributeClusterDimension;
-  pa[1].val.clusterDim.x = static_cast<unsigned>(pr.set[0].C);
+  pa[1].val.clusterDim.x = static_cast<unsigned>(kProMaxC);
   pa[1].val.clusterDim.y = 1;
   pa[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t c1{};
-  c1.gridDim = dim3(static_cast<unsigned>(clusters * pr.set[0].C));
+  c1.gridDim = dim3(static_cast<unsigned>(clusters * kProMaxC));
   c1.blockDim = dim3(kProThreads);
   c1.dynamicSmemBytes = pro_smem;
   c1.stream = stream;
   c1.attrs = pa;
   c1.numAttrs = 2;
   return fp8 ? cudaLaunchKernelEx(&c1, k_pro_dec<true>, pr) : cudaLaunchKernelEx(&c1, k_pro_dec<false>, pr);
+}
+
+// The row prologue: input s takes CTAs [cta0_s, cta0_s + ceil(M_s / R_s) H_s).  Rows longer than
+// kRowsMaxDi take the cluster prologue (a CTA would hold too few rows of u), and so does the
+// FP8 mode (measured: the W8A8 decode layer ran 17 % longer on the row prologue, whose CTAs each
+// divide four whole rows).
+cudaError_t launch_pro(ProParams pr, bool fp8, cudaStream_t stream) {
+  if (fp8 || pr.set[0].d_i > kRowsMaxDi) return launch_pro_clusters(pr, fp8, stream);
+  int ctas = 0;
+  size_t pro_smem = 0;
+  for (int s = 0; s < pr.n_sets; ++s) {
+    ProSet& q = pr.set[s];
+    pro_plan(q);
+    q.cta0 = ctas;
+    ctas += static_cast<int>((q.M + q.R - 1) / q.R) * q.H;
+    const size_t need = static_cast<size_t>(q.R) * static_cast<size_t>(q.d_i) * 4;
+    pro_smem = need > pro_smem ? need : pro_smem;
+  }
+  cudaLaunchAttribute pa[1];
+  pa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pa[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t c1{};
+  c1.gridDim = dim3(static_cast<unsigned>(ctas));
+  c1.blockDim = dim3(kProThreads);
+  c1.dynamicSmemBytes = pro_smem;
+  c1.stream = stream;
+  c1.attrs = pa;
+  c1.numAttrs = 1;
+  return fp8 ? cudaLaunchKernelEx(&c1, k_pro_rows<true>, pr) : cudaLaunchKernelEx(&c1, k_pro_rows<false>, pr);
 }
 
 }  // namespace
@@ -1312,8 +1614,6 @@ cudaError_t launch_linear_tc_batch(int64_t d_i, float eps, const TcSet* sets, in
     q.rowscale = w[s].rowscale;
     q.t = w[s].t;
     q.t_ld = w[s].t_ld;
-    q.R = pro_rows(sets[s].M);
-    q.C = kProMaxC;
     q.rtot = rtot[s];
     for (int i = 0; i < n_proj; ++i)
       if (projs[i].set == s) {
@@ -1385,8 +1685,6 @@ cudaError_t launch_pro_fp8(const void* x, int64_t M, int64_t d_i, const float* w
   q.rowscale = s_x;
   q.t = t;
   q.t_ld = t_ld;
-  q.R = pro_rows(M);
-  q.C = kProMaxC;
   q.n_proj = 1;
   q.rtot = A != nullptr ? r : 0;
   q.A[0] = static_cast<const __nv_bfloat16*>(A);
