@@ -330,7 +330,7 @@ def run_ours(args, world, rank, local):
     # the step's time (the prologue's time included); both from CUDA events on the launching
     # stream around the K steps, i.e. the step's GB/s
     if form == "batch":
-        kern, per_launch, n_launch = "k_tc_decode (+ k_pro_dec)", step_bytes, 1
+        kern, per_launch, n_launch = "k_tc_decode (+ k_pro_rows)", step_bytes, 1
         traffic = profile_traffic("k_tc_decode", f"{args.workload}/batch")
     else:
         kern = "k_fused_decode" if all(v == 2 for v in paths.values()) else "decode kernels"
