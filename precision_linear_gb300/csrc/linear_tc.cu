@@ -1590,11 +1590,24 @@ cudaError_t launch_linear_tc_batch(int64_t d_i, float eps, const TcSet* sets, in
   for (int s = 0; s < n_sets && ok; ++s)
     ok = encode_2d(&maps.hq[s], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w[s].hq, d_i, sets[s].M, 64,
                    static_cast<uint32_t>((sets[s].M + 15) / 16 * 16), CU_TENSOR_MAP_SWIZZLE_128B);
-  for (int i = 0; i < n_proj && ok; ++i)
-    ok = encode_2d(&maps.codes[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, projs[i].codes, d_i / 2, projs[i].d_o, 128,
+  // the main kernel's members in order of decreasing token count: the block scheduler starts
+  // low tile indices first, so the members with the longest main loops get their SMs first
+  int order[kMaxProj];
+  for (int i = 0; i < n_proj; ++i) {
+    int k = i;
+    while (k > 0 && sets[projs[order[k - 1]].set].M < sets[projs[i].set].M) {
+      order[k] = order[k - 1];
+      --k;
+    }
+    order[k] = i;
+  }
+  for (int k = 0; k < n_proj && ok; ++k) {
+    const int i = order[k];
+    ok = encode_2d(&maps.codes[k], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, projs[i].codes, d_i / 2, projs[i].d_o, 128,
                    kTileO, CU_TENSOR_MAP_SWIZZLE_128B) &&
-         encode_2d(&maps.scales[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, projs[i].scales, d_i / 16, projs[i].d_o, 16,
+         encode_2d(&maps.scales[k], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, projs[i].scales, d_i / 16, projs[i].d_o, 16,
                    kTileO, CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
   if (!ok) return cudaErrorInvalidValue;
 
   // prologue: per input, clusters of C CTAs over R token rows each, with the adapters of the
@@ -1636,17 +1649,18 @@ cudaError_t launch_linear_tc_batch(int64_t d_i, float eps, const TcSet* sets, in
   p.y_f32 = y_f32 ? 1 : 0;
   for (int s = 0; s < n_sets; ++s)
     p.set[s] = TcSetDev{sets[s].M, static_cast<int>((sets[s].M + 15) / 16 * 16), w[s].rowscale, w[s].t, w[s].t_ld};
-  for (int i = 0, t0 = 0; i < n_proj; ++i) {
+  for (int k = 0, t0 = 0; k < n_proj; ++k) {
+    const int i = order[k];
     const bool lora = projs[i].r > 0 && projs[i].A != nullptr && projs[i].B != nullptr;
-    p.proj[i].d_o = projs[i].d_o;
-    p.proj[i].s_g = projs[i].s_g;
-    p.proj[i].B = lora ? static_cast<const __nv_bfloat16*>(projs[i].B) : nullptr;
-    p.proj[i].y = projs[i].y;
-    p.proj[i].r = lora ? projs[i].r : 0;
-    p.proj[i].toff = toff[i];
-    p.proj[i].tile0 = t0;
-    p.proj[i].lambda = projs[i].lambda;
-    p.proj[i].set = projs[i].set;
+    p.proj[k].d_o = projs[i].d_o;
+    p.proj[k].s_g = projs[i].s_g;
+    p.proj[k].B = lora ? static_cast<const __nv_bfloat16*>(projs[i].B) : nullptr;
+    p.proj[k].y = projs[i].y;
+    p.proj[k].r = lora ? projs[i].r : 0;
+    p.proj[k].toff = toff[i];
+    p.proj[k].tile0 = t0;
+    p.proj[k].lambda = projs[i].lambda;
+    p.proj[k].set = projs[i].set;
     t0 += static_cast<int>((projs[i].d_o + kTileO - 1) / kTileO);
   }
   cudaLaunchAttribute attrs[2];
