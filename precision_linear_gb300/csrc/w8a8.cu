@@ -11,10 +11,8 @@
 //
 // k_w8_quant: one CTA per weight row: s_w = fp32(amax / 448) (1 for a zero row), codes
 //   E4M3(fp32(w / s_w)), round to nearest even, saturating, +0 for values rounding to zero.
-// The activations come, at M <= 64, from the cluster prologue of the tensor-core decode path
-// in its FP8 mode (linear_tc.cu): q_x, s_x and t = A h, FP32; above, from the large-M row
-// prologue in its FP8 mode (q_x, s_x and the f16 rows) and the adapter's down-projection on
-// the tensor cores in t mode (FP32 t), ranks up to 32.
+// The activations come from the cluster prologue of the tensor-core decode path in its FP8
+// mode (linear_tc.cu): q_x, s_x and t = A h, FP32.
 // k_w8_gemm (decode, M <= 64; a cluster of S CTAs per 128 weight rows x N tokens; CTA s takes the s-th slice
 //   of K in chunks of 128):
 //   * warp 0 TMA-loads per chunk the weight codes (128 rows x 128 B) and the activation codes
