@@ -775,7 +775,7 @@ __global__ void __launch_bounds__(kProThreads, 1) k_pro_rows(const __grid_consta
     uint4 xr[kProMaxR];  // the rows' pieces, all loads issued before any use
 #pragma unroll
     for (int m = 0; m < kProMaxR; ++m)
-      xr[m] = m < rows ? reinterpret_cast<const uint4*>(p.x + (m0 + m) * p.d_i)[q] : make_uint4(0u, 0u, 0u, 0u);
+      xr[m] = m < rows ? __ldg(reinterpret_cast<const uint4*>(p.x + (m0 + m) * p.d_i) + q) : make_uint4(0u, 0u, 0u, 0u);
     float g[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) g[i] = 1.f;
@@ -903,27 +903,30 @@ __global__ void __launch_bounds__(kProThreads, 1) k_pro_rows(const __grid_consta
   for (int jr = 0; jr < 4; ++jr)
 #pragma unroll
     for (int m = 0; m < kProMaxR; ++m) acc[jr][m] = 0.f;
+  const int qk0 = static_cast<int>(k0), qk1 = static_cast<int>(k1), di = static_cast<int>(p.d_i);  // d_i <= 8192 here
 #pragma unroll 2
-  for (int64_t q = k0 + lane; q < k1; q += 32) {  // two iterations unrolled: their loads are in flight together
-    uint4 av[4];
+  for (int q = qk0 + lane; q < qk1; q += 32) {  // two iterations unrolled: their loads are in flight together
+    float af[4][8];  // the adapter values of this piece, converted once for all token rows
 #pragma unroll
-    for (int jr = 0; jr < 4; ++jr)
-      av[jr] = arow[jr] != nullptr ? reinterpret_cast<const uint4*>(arow[jr])[q] : make_uint4(0u, 0u, 0u, 0u);
+    for (int jr = 0; jr < 4; ++jr) {
+      const uint4 a = arow[jr] != nullptr ? __ldg(reinterpret_cast<const uint4*>(arow[jr]) + q) : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t w4[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        af[jr][2 * j] = bf16lo_to_f32(w4[j]);
+        af[jr][2 * j + 1] = bf16hi_to_f32(w4[j]);
+      }
+    }
 #pragma unroll
     for (int m = 0; m < kProMaxR; ++m) {
       if (m < rows) {
-        const float4* us = reinterpret_cast<const float4*>(u + m * p.d_i + q * 8);
+        const float4* us = reinterpret_cast<const float4*>(u + m * di + q * 8);
         const float4 ua = us[0], ub = us[1];
         const float uv[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
 #pragma unroll
-        for (int jr = 0; jr < 4; ++jr) {
-          const uint32_t w4[4] = {av[jr].x, av[jr].y, av[jr].z, av[jr].w};
+        for (int jr = 0; jr < 4; ++jr)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            acc[jr][m] = fmaf(bf16lo_to_f32(w4[j]), uv[2 * j], acc[jr][m]);
-            acc[jr][m] = fmaf(bf16hi_to_f32(w4[j]), uv[2 * j + 1], acc[jr][m]);
-          }
-        }
+          for (int e = 0; e < 8; ++e) acc[jr][m] = fmaf(af[jr][e], uv[e], acc[jr][m]);
       }
     }
   }
