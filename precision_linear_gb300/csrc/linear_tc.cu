@@ -505,7 +505,7 @@ __global__ void __launch_bounds__(kProThreads, 4) k_pro_dec(const __grid_constan
     uint4 xr[kProMaxR];  // the rows' pieces, all loads issued before any use
 #pragma unroll
     for (int m = 0; m < kProMaxR; ++m)
-      xr[m] = m < R && m0 + m < p.M ? reinterpret_cast<const uint4*>(p.x + (m0 + m) * p.d_i)[q] : make_uint4(0u, 0u, 0u, 0u);
+      xr[m] = m < R && m0 + m < p.M ? __ldg(reinterpret_cast<const uint4*>(p.x + (m0 + m) * p.d_i) + q) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int m = 0; m < kProMaxR; ++m) {
       if (m < R) {
@@ -585,7 +585,7 @@ __global__ void __launch_bounds__(kProThreads, 4) k_pro_dec(const __grid_constan
       uint4 av[4];
 #pragma unroll
       for (int jr = 0; jr < 4; ++jr)
-        av[jr] = arow[jr] != nullptr ? reinterpret_cast<const uint4*>(arow[jr])[q0 + qi] : make_uint4(0u, 0u, 0u, 0u);
+        av[jr] = arow[jr] != nullptr ? __ldg(reinterpret_cast<const uint4*>(arow[jr]) + q0 + qi) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
       for (int m = 0; m < kProMaxR; ++m) {
         if (m < R) {
